@@ -1,0 +1,200 @@
+"""The test oracle: plain CPU restatement of the sparse x dense products.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with ``csr_bsr_spmv_gb300`` and never imports it; the arithmetic lives in
+``oracle.c`` (plain C, fp64 accumulation, single-threaded), built with the
+host C compiler.  Each function's docstring in ``oracle.c`` cites the page
+section it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_ARG, ERR_INDEX, ERR_DUP = 0, -1, -2, -4
+
+# plan option order mirrors or_plan_opts_t
+PLAN_FIELDS = ("block_nnz", "block_rows", "pack_max", "cta_max", "seg_nnz", "lanes_div")
+TASK_GROUP, TASK_CTA, TASK_SEG = 0, 1, 2
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int32) for f in PLAN_FIELDS]
+
+
+class RowStats(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("nnz", ctypes.c_int64), ("sumsq", ctypes.c_int64),
+                ("min", ctypes.c_int32), ("max", ctypes.c_int32), ("p50", ctypes.c_int32),
+                ("p95", ctypes.c_int32), ("p99", ctypes.c_int32), ("empty", ctypes.c_int32),
+                ("mean", ctypes.c_double), ("var", ctypes.c_double), ("cv", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so: -O2, no fast-math, no FMA contraction."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _lib_():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            sig = {
+                "or_build_csr": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
+                "or_transpose": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
+                "or_build_bsr": [i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp],
+                "or_row_stats": [i32, vp, vp],
+                "or_plan_spmv": [i32, vp, vp, vp, vp, vp],
+                "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
+                "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
+                "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, vp, i64, vp, vp],
+            }
+            for name, args in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code):
+        super().__init__(f"oracle status {code}")
+        self.code = code
+
+
+def _check(rc):
+    if rc != OK:
+        raise OracleError(rc)
+
+
+def build_csr(M, K, row, col, val):
+    row, col = _c(row, np.int32), _c(col, np.int32)
+    val = np.ascontiguousarray(val)
+    nnz = row.size
+    rp = np.empty(M + 1, np.int32)
+    co = np.empty(nnz, np.int32)
+    vo = np.empty(nnz, val.dtype)
+    _check(_lib_().or_build_csr(M, K, nnz, _p(row), _p(col), _p(val), val.itemsize, _p(rp), _p(co), _p(vo)))
+    return rp, co, vo
+
+
+def transpose(M, K, rp, col, val):
+    rp, col = _c(rp, np.int32), _c(col, np.int32)
+    val = np.ascontiguousarray(val)
+    nnz = int(rp[M])
+    trp = np.empty(K + 1, np.int32)
+    tc = np.empty(nnz, np.int32)
+    tv = np.empty(nnz, val.dtype)
+    _check(_lib_().or_transpose(M, K, nnz, _p(rp), _p(col), _p(val), val.itemsize, _p(trp), _p(tc), _p(tv)))
+    return trp, tc, tv
+
+
+def build_bsr(M, K, rp, col, val, br, bc):
+    """Returns (bsr_row_ptr, bsr_col, bsr_val[nnzb, br, bc], fill)."""
+    rp, col = _c(rp, np.int32), _c(col, np.int32)
+    val = np.ascontiguousarray(val)
+    MB = (M + br - 1) // br
+    nnzb = ctypes.c_int64(0)
+    fill = ctypes.c_double(0.0)
+    brp = np.empty(MB + 1, np.int32)
+    lib = _lib_()
+    _check(lib.or_build_bsr(M, K, _p(rp), _p(col), _p(val), val.itemsize, br, bc, _p(brp), None, None,
+                            ctypes.byref(nnzb), ctypes.byref(fill)))
+    nb = nnzb.value
+    bcol = np.empty(nb, np.int32)
+    bval = np.empty(nb * br * bc, val.dtype)
+    _check(lib.or_build_bsr(M, K, _p(rp), _p(col), _p(val), val.itemsize, br, bc, _p(brp), _p(bcol), _p(bval),
+                            ctypes.byref(nnzb), ctypes.byref(fill)))
+    return brp, bcol, bval.reshape(nb, br, bc), fill.value
+
+
+def row_stats(M, rp):
+    rp = _c(rp, np.int32)
+    st = RowStats()
+    _check(_lib_().or_row_stats(M, _p(rp), ctypes.byref(st)))
+    return st.as_dict()
+
+
+def plan_spmv(M, rp, **opts):
+    """Returns dict(tasks[ntasks,4], longrows[nlong,4], counts)."""
+    rp = _c(rp, np.int32)
+    o = PlanOpts(**{f: int(opts[f]) for f in PLAN_FIELDS})
+    counts = np.zeros(8, np.int64)
+    lib = _lib_()
+    _check(lib.or_plan_spmv(M, _p(rp), ctypes.byref(o), None, None, _p(counts)))
+    tasks = np.empty((int(counts[0]), 4), np.int32)
+    longrows = np.empty((int(counts[1]), 4), np.int32)
+    _check(lib.or_plan_spmv(M, _p(rp), ctypes.byref(o), _p(tasks), _p(longrows), _p(counts)))
+    names = ("tasks", "long_rows", "slots", "packed_rows", "cta_rows", "split_rows", "thread_groups",
+             "lane_groups")
+    return dict(tasks=tasks, longrows=longrows, counts=dict(zip(names, (int(c) for c in counts))))
+
+
+def spmv(M, rp, col, val, x, alpha=1.0, beta=0.0, y=None, rows=None):
+    """(ref, bound) in fp64, for all rows or the given sample of rows."""
+    rp, col, val, x = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32), _c(x, np.float32)
+    yv = _c(y, np.float32) if (y is not None and beta != 0.0) else None
+    rr = None if rows is None else _c(rows, np.int32)
+    n = M if rr is None else rr.size
+    ref = np.empty(n, np.float64)
+    bnd = np.empty(n, np.float64)
+    _check(_lib_().or_spmv(M, _p(rp), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv), _p(rr),
+                           0 if rr is None else rr.size, _p(ref), _p(bnd)))
+    return ref, bnd
+
+
+def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None):
+    rp, col, val = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32)
+    B = _c(B, np.float32)
+    N = B.shape[1]
+    Cv = _c(C, np.float32) if (C is not None and beta != 0.0) else None
+    rr = None if rows is None else _c(rows, np.int32)
+    n = M if rr is None else rr.size
+    ref = np.empty((n, N), np.float64)
+    bnd = np.empty((n, N), np.float64)
+    _check(_lib_().or_spmm(M, N, _p(rp), _p(col), _p(val), _p(B), N, float(alpha), float(beta), _p(Cv),
+                           N if Cv is not None else 0, _p(rr), 0 if rr is None else rr.size, _p(ref), _p(bnd)))
+    return ref, bnd
+
+
+def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None):
+    brp, bcol = _c(brp, np.int32), _c(bcol, np.int32)
+    bval = _c(bval_bf16, np.uint16)
+    B = _c(B_bf16, np.uint16)
+    N = B.shape[1]
+    rr = None if rows is None else _c(rows, np.int32)
+    n = M if rr is None else rr.size
+    ref = np.empty((n, N), np.float64)
+    bnd = np.empty((n, N), np.float64)
+    _check(_lib_().or_bsr_spmm(M, K, br, bc, _p(brp), _p(bcol), _p(bval), N, _p(B), N, _p(rr),
+                               0 if rr is None else rr.size, _p(ref), _p(bnd)))
+    return ref, bnd

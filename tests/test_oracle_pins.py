@@ -1,0 +1,346 @@
+"""Pins of the oracle against things other than itself.
+
+The printed worked example (tests/golden/worked_example_5x5.json), values
+derived from it by hand, dense brute force with small-integer values (where
+fp64 sums are exact, so any dropped term, wrong index or transposed operand
+shows), scipy's own sparse conversions, round trips and closed forms.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "worked_example_5x5.json")
+
+
+@pytest.fixture(scope="module")
+def ex():
+    g = json.load(open(GOLD))
+    v = g["values_used"]
+    p = g["printed"]
+    val = np.array([v[s] for s in p["coo_val"]], np.float32)
+    return g, v, val
+
+
+def _vals(names, v):
+    return [v[s] if isinstance(s, str) else float(s) for s in names]
+
+
+# ------------------------------------------------------------ worked example
+
+def test_worked_example_coo_to_csr(ex):
+    g, v, val = ex
+    p = g["printed"]
+    rp, col, vo = oracle.build_csr(5, 5, p["coo_row"], p["coo_col"], val)
+    assert rp.tolist() == p["csr_row_ptr"]
+    assert col.tolist() == p["csr_col"]
+    assert vo.tolist() == _vals(p["csr_val"], v)
+
+
+def test_worked_example_coo_any_order(ex):
+    """COO may come in any order ([Formats] §2); the CSR is the same."""
+    g, v, val = ex
+    p = g["printed"]
+    for seed in range(6):
+        perm = synth.permutation(seed, 8)
+        rp, col, vo = oracle.build_csr(5, 5, np.array(p["coo_row"])[perm], np.array(p["coo_col"])[perm], val[perm])
+        assert rp.tolist() == p["csr_row_ptr"]
+        assert col.tolist() == p["csr_col"]
+        assert vo.tolist() == _vals(p["csr_val"], v)
+
+
+def test_worked_example_transpose(ex):
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]
+    trp, tc, tv = oracle.transpose(5, 5, p["csr_row_ptr"], p["csr_col"], val)
+    assert trp.tolist() == d["csr_transpose_row_ptr"]
+    assert tc.tolist() == d["csr_transpose_col"]
+    assert tv.tolist() == _vals(d["csr_transpose_val"], v)
+
+
+def test_worked_example_bsr(ex):
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]
+    brp, bcol, bval, fill = oracle.build_bsr(5, 5, p["csr_row_ptr"], p["csr_col"], val, 2, 2)
+    assert brp.tolist() == d["bsr_2x2_row_ptr"]
+    assert bcol.tolist() == d["bsr_2x2_col"]
+    want = [_vals(b, v) for b in d["bsr_2x2_val_rowmajor"]]
+    assert bval.reshape(-1, 4).tolist() == want
+    assert fill == 8 / 24
+
+
+def test_worked_example_stats(ex):
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]
+    st = oracle.row_stats(5, p["csr_row_ptr"])
+    for k, want in d["stats"].items():
+        assert st[k] == pytest.approx(want, rel=0, abs=1e-15), k
+    assert st["mean"] == 1.6 and st["var"] == 16 / 25
+
+
+def test_worked_example_spmv(ex):
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]
+    ref, bound = oracle.spmv(5, p["csr_row_ptr"], p["csr_col"], val, np.ones(5, np.float32))
+    assert ref.tolist() == d["y_for_x_all_ones"]
+    assert bound.tolist() == d["y_for_x_all_ones"]  # all values positive
+    # A e_j is column j of the matrix written out in the page's entry list
+    dense = np.zeros((5, 5))
+    for r, c, s in zip(p["coo_row"], p["coo_col"], p["coo_val"]):
+        dense[r, c] = v[s]
+    for j in range(5):
+        e = np.zeros(5, np.float32)
+        e[j] = 1
+        ref, _ = oracle.spmv(5, p["csr_row_ptr"], p["csr_col"], val, e)
+        assert ref.tolist() == dense[:, j].tolist()
+
+
+# ------------------------------------------------------------ brute force
+
+def _dense(M, K, row, col, val):
+    A = np.zeros((M, K))
+    np.add.at(A, (row, col), val.astype(np.float64))
+    return A
+
+
+CASES = [(1, 1, 0, 1), (7, 5, 0, 5), (33, 64, 0, 9), (64, 17, 3, 17), (50, 50, 0, 0), (0, 4, 0, 2), (9, 1, 0, 1)]
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", CASES)
+@pytest.mark.parametrize("seed", [11, 12])
+def test_bruteforce_spmv_spmm(M, K, lmin, lmax, seed):
+    d = synth.random_coo(seed, M, K, lmin, lmax, values="int")
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = _dense(M, K, d["row"], d["col"], d["val"])
+    x = np.floor(synth.uniform(seed, synth.T_X, K, -3, 4)).astype(np.float32)
+    y = np.floor(synth.uniform(seed, synth.T_Y, M, -3, 4)).astype(np.float32)
+    ref, bound = oracle.spmv(M, rp, col, val, x, alpha=2.0, beta=-3.0, y=y)
+    assert np.array_equal(ref, 2.0 * (A @ x.astype(np.float64)) - 3.0 * y)
+    assert np.array_equal(bound, 2.0 * (np.abs(A) @ np.abs(x.astype(np.float64))) + 3.0 * np.abs(y))
+    # beta == 0: y is not read (NaN must not leak)
+    ref0, _ = oracle.spmv(M, rp, col, val, x, alpha=1.0, beta=0.0, y=np.full(M, np.nan, np.float32))
+    assert np.array_equal(ref0, A @ x.astype(np.float64))
+    for N in (1, 3, 8):
+        B = np.floor(synth.uniform(seed, synth.T_B, K * N, -3, 4)).astype(np.float32).reshape(K, N)
+        C = np.floor(synth.uniform(seed, synth.T_Y, M * N, -3, 4)).astype(np.float32).reshape(M, N)
+        ref, _ = oracle.spmm(M, rp, col, val, B, alpha=-1.0, beta=0.5, C=C)
+        assert np.array_equal(ref, -(A @ B.astype(np.float64)) + 0.5 * C)
+    # the dual direction: CSR(A^T) times u equals the transposed dense product
+    trp, tc, tv = oracle.transpose(M, K, rp, col, val)
+    u = np.floor(synth.uniform(seed, 7, M, -3, 4)).astype(np.float32)
+    reft, _ = oracle.spmv(K, trp, tc, tv, u)
+    assert np.array_equal(reft, A.T @ u.astype(np.float64))
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", CASES)
+@pytest.mark.parametrize("bs", [(1, 1), (2, 2), (3, 2), (4, 8)])
+def test_bruteforce_bsr(M, K, lmin, lmax, bs):
+    br, bc = bs
+    d = synth.random_coo(5, M, K, lmin, lmax, values="int")
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = _dense(M, K, d["row"], d["col"], d["val"])
+    brp, bcol, bval, fill = oracle.build_bsr(M, K, rp, col, val, br, bc)
+    # BSR expanded back to dense equals the CSR's dense form
+    MB, KB = -(-M // br), -(-K // bc)
+    D = np.zeros((MB * br, KB * bc))
+    for I in range(MB):
+        for b in range(brp[I], brp[I + 1]):
+            D[I * br:(I + 1) * br, bcol[b] * bc:(bcol[b] + 1) * bc] = bval[b]
+    assert np.array_equal(D[:M, :K], A)
+    assert not D[M:, :].any() and not D[:, K:].any()
+    # every stored block holds a nonzero; block columns ascend inside a block-row
+    for I in range(MB):
+        cs = bcol[brp[I]:brp[I + 1]]
+        assert np.all(np.diff(cs) > 0)
+    nnzb = brp[-1]
+    assert fill == (rp[-1] / (nnzb * br * bc) if nnzb else 0.0)
+    # BSR SpMM on bf16 bit patterns of small integers (exact in bf16 and fp64)
+    N = 5
+    Bf = np.floor(synth.uniform(3, synth.T_B, K * N, -3, 4)).astype(np.float32).reshape(K, N)
+    ref, bound = oracle.bsr_spmm(M, K, br, bc, brp, bcol, synth.to_bf16_bits(bval).reshape(bval.shape),
+                                 synth.to_bf16_bits(Bf).reshape(K, N))
+    assert np.array_equal(ref, A @ Bf.astype(np.float64))
+    assert np.array_equal(bound, np.abs(A) @ np.abs(Bf.astype(np.float64)))
+
+
+def test_bsr_stored_blocks_nonempty():
+    d = synth.random_coo(8, 40, 40, 0, 6, values="ones")
+    rp, col, val = oracle.build_csr(40, 40, d["row"], d["col"], d["val"])
+    brp, bcol, bval, _ = oracle.build_bsr(40, 40, rp, col, val, 4, 4)
+    assert all(b.any() for b in bval)
+    # count of distinct (i//4, j//4) equals nnzb
+    blocks = {(r // 4, c // 4) for r, c in zip(d["row"], d["col"])}
+    assert len(blocks) == brp[-1]
+
+
+def test_bsr_duplicate_rejected():
+    rp = np.array([0, 2], np.int32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.build_bsr(1, 4, rp, np.array([1, 1], np.int32), np.ones(2, np.float32), 2, 2)
+    assert e.value.code == oracle.ERR_DUP
+
+
+def test_scipy_agrees_on_formats():
+    sp = pytest.importorskip("scipy.sparse")
+    for seed, (M, K) in enumerate([(30, 20), (64, 64), (5, 90)]):
+        d = synth.random_coo(seed, M, K, 0, 12)
+        perm = synth.permutation(seed, d["row"].size)
+        rp, col, val = oracle.build_csr(M, K, d["row"][perm], d["col"][perm], d["val"][perm])
+        S = sp.coo_matrix((d["val"], (d["row"], d["col"])), shape=(M, K)).tocsr()
+        S.sort_indices()
+        assert np.array_equal(rp, S.indptr) and np.array_equal(col, S.indices) and np.array_equal(val, S.data)
+        T = S.T.tocsr()
+        T.sort_indices()
+        trp, tc, tv = oracle.transpose(M, K, rp, col, val)
+        assert np.array_equal(trp, T.indptr) and np.array_equal(tc, T.indices) and np.array_equal(tv, T.data)
+        Mp, Kp = -(-M // 4) * 4, -(-K // 2) * 2
+        Sp = sp.csr_matrix((S.data, S.indices, np.concatenate([S.indptr, np.full(Mp - M, S.indptr[-1])])),
+                           shape=(Mp, Kp))
+        Bs = Sp.tobsr(blocksize=(4, 2))
+        Bs.sort_indices()
+        brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, 4, 2)
+        keep = np.array([np.any(b != 0) for b in Bs.data], bool)  # scipy may keep all-zero blocks
+        assert np.array_equal(bcol, Bs.indices[keep]) and np.array_equal(bval, Bs.data[keep])
+
+
+# ------------------------------------------------------------ invariants
+
+def test_transpose_twice_is_identity():
+    for seed, (M, K) in enumerate([(100, 37), (1, 300), (300, 1), (257, 513)]):
+        d = synth.random_coo(seed, M, K, 0, 20)
+        rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+        t = oracle.transpose(M, K, rp, col, val)
+        back = oracle.transpose(K, M, *t)
+        for a, b in zip((rp, col, val), back):
+            assert np.array_equal(a, b)
+
+
+def test_coo_shuffle_round_trip():
+    d = synth.random_coo(21, 500, 700, 0, 30)
+    rp, col, val = oracle.build_csr(500, 700, d["row"], d["col"], d["val"])
+    perm = synth.permutation(4, rp[-1])
+    row = np.repeat(np.arange(500, dtype=np.int32), np.diff(rp))
+    again = oracle.build_csr(500, 700, row[perm], col[perm], val[perm])
+    for a, b in zip((rp, col, val), again):
+        assert np.array_equal(a, b)
+
+
+def test_duplicates_kept_in_input_order():
+    """Equal (row, col) pairs are kept, not summed, in input order (the pages
+    are silent; this is the reading the library follows)."""
+    row = np.array([1, 0, 1, 1], np.int32)
+    col = np.array([2, 0, 2, 0], np.int32)
+    val = np.array([10, 20, 30, 40], np.float32)
+    rp, c, v = oracle.build_csr(2, 3, row, col, val)
+    assert rp.tolist() == [0, 1, 4] and c.tolist() == [0, 0, 2, 2] and v.tolist() == [20, 40, 10, 30]
+
+
+def test_index_range_rejected():
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.build_csr(2, 2, np.array([0, 2], np.int32), np.array([0, 0], np.int32), np.ones(2, np.float32))
+    assert e.value.code == oracle.ERR_INDEX
+    with pytest.raises(oracle.OracleError):
+        oracle.build_csr(2, 2, np.array([0, 1], np.int32), np.array([0, -1], np.int32), np.ones(2, np.float32))
+
+
+# ------------------------------------------------------------ closed forms
+
+@pytest.mark.parametrize("l", [0, 1, 31, 32, 33, 4097, 200_000])
+def test_row_of_ones(l):
+    K = max(l, 1)
+    rp = np.array([0, l], np.int32)
+    col = np.arange(l, dtype=np.int32)
+    ref, _ = oracle.spmv(1, rp, col, np.ones(l, np.float32), np.ones(K, np.float32))
+    assert ref[0] == l
+
+
+def test_stats_against_numpy():
+    for seed in range(4):
+        L = synth.lengths_uniform(seed, 1000 + seed, 0, 50)
+        rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+        st = oracle.row_stats(L.size, rp)
+        assert st["nnz"] == L.sum() and st["sumsq"] == (L.astype(np.int64) ** 2).sum()
+        assert st["max"] == L.max() and st["min"] == L.min() and st["empty"] == (L == 0).sum()
+        assert st["mean"] == pytest.approx(L.mean(), rel=1e-15)
+        assert st["var"] == pytest.approx(L.var(), rel=1e-12)
+        for q in (50, 95, 99):
+            assert st[f"p{q}"] == np.percentile(L, q, method="inverted_cdf")
+    L = np.full(77, 9, np.int32)
+    st = oracle.row_stats(77, np.arange(0, 78 * 9, 9, dtype=np.int32))
+    assert st["var"] == 0.0 and st["cv"] == 0.0 and st["p99"] == 9 and st["mean"] == 9.0
+
+
+def test_stats_exact_rational():
+    """var is the exact rational (M*S2 - S1^2)/M^2 rounded: compare with
+    Python's exact fractions."""
+    from fractions import Fraction
+
+    L = synth.lengths_uniform(3, 12345, 0, 1000)
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    st = oracle.row_stats(L.size, rp)
+    M, S1, S2 = L.size, int(L.sum()), int((L.astype(np.int64) ** 2).sum())
+    num = M * S2 - S1 * S1
+    assert st["var"] == float(num) / (float(M) * float(M))
+    assert abs(Fraction(st["var"]) - Fraction(num, M * M)) <= Fraction(num, M * M) * Fraction(1, 2 ** 51)
+
+
+# ------------------------------------------------------------ the plan
+
+OPTS_SMALL = dict(block_nnz=16, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=2)
+
+
+def test_plan_hand_example():
+    L = [3, 0, 5, 8, 2, 50, 4, 0, 250, 6, 6, 6]
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    p = oracle.plan_spmv(len(L), rp, **OPTS_SMALL)
+    want = [[1, 5, 0, 0]] + [[2, 8, s, s] for s in range(7)] + [
+        [256, 0, 3, 0], [512, 3, 5, 0], [0, 6, 8, 0], [512, 9, 11, 0], [512, 11, 12, 0]]
+    assert p["tasks"].tolist() == want
+    assert p["longrows"].tolist() == [[8, 0, 7, 0]]
+    assert p["counts"] == dict(tasks=13, long_rows=1, slots=7, packed_rows=10, cta_rows=1, split_rows=1,
+                               thread_groups=1, lane_groups=4)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_invariants(seed):
+    L, _ = synth.lengths_zipf(seed, 3000, 2.1, 3000, 6.0)
+    L[::97] = 0
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    o = dict(block_nnz=64, block_rows=16, pack_max=32, cta_max=200, seg_nnz=50, lanes_div=4)
+    p = oracle.plan_spmv(L.size, rp, **o)
+    covered = np.zeros(L.size, np.int64)
+    seg_cover = {}
+    for kind, a, b, c in p["tasks"].tolist():
+        k = kind & 255
+        if k == 0:
+            rows = np.arange(a, b)
+            assert 1 <= b - a <= o["block_rows"]
+            assert np.all(L[rows] <= o["pack_max"]) and L[rows].sum() <= o["block_nnz"]
+            w = 1 << (kind >> 8)
+            per = -(-int(L[rows].sum()) // ((b - a) * o["lanes_div"]))
+            assert w == min(32, max(1, 1 << int(np.ceil(np.log2(max(per, 1))))))
+            covered[rows] += 1
+        elif k == 1:
+            assert o["pack_max"] < L[a] <= o["cta_max"]
+            covered[a] += 1
+        else:
+            assert L[a] > o["cta_max"]
+            seg_cover.setdefault(a, []).append((b, c))
+    for row, first, ns, _ in p["longrows"].tolist():
+        segs = seg_cover.pop(row)
+        assert [s for s, _ in segs] == list(range(ns)) and [c for _, c in segs] == list(range(first, first + ns))
+        assert (ns - 1) * o["seg_nnz"] < L[row] <= ns * o["seg_nnz"]
+        covered[row] += 1
+    assert not seg_cover
+    assert np.all(covered == 1)
+    c = p["counts"]
+    assert c["packed_rows"] + c["cta_rows"] + c["split_rows"] == L.size
+    # groups are maximal: the next packed row would break a limit
+    groups = [t for t in p["tasks"].tolist() if t[0] & 255 == 0]
+    for (k1, a1, b1, _), (k2, a2, b2, _) in zip(groups, groups[1:]):
+        if b1 == a2:
+            assert b1 - a1 == o["block_rows"] or L[a1:b1].sum() + L[a2] > o["block_nnz"]
