@@ -1,0 +1,516 @@
+"""Benchmark of the sparse x dense hot path on GB300.
+
+Default workload: power-law CSR SpMV, M = K = 4,194,304, Zipf(2.1) row
+lengths clipped to [1, 200000] and rescaled to mean 16 (nnz ~ 67.1M), y =
+A x + 0.5 y -- the configuration the headline metric is quoted on.  One step
+is one SpMV call through the C ABI: the binned main launch plus the long-row
+fix-up launch.  Format conversion and planning are timed once, separately.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload power-law|uniform|dual|spmm32|spmm128|bsr]
+
+Prints one JSON line.  Under torchrun each rank runs an independent replica of
+the workload (the products shard by rows with no exchange; "weak" scaling);
+rank 0 prints.  --impl reference times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SpMV/SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s as % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(*names):
+    h = hashlib.sha1()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "csr_bsr_spmv_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def traffic_from_profile(kernel_key, src_hash):
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_hash") != src_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- workloads
+
+def make_workload(name: str, rows: int = 0):
+    """Host arrays of the workload; `rows` shrinks the power-law case (profiling)."""
+    import synth
+
+    if name == "power-law":
+        c = synth.power_law_rows(M=rows) if rows else synth.power_law_rows()
+    elif name == "uniform":
+        c = synth.uniform_short_rows()
+    elif name == "dual":
+        c = synth.banded_pair()
+    elif name in ("spmm32", "spmm128"):
+        c = synth.clustered_spmm(N=int(name[4:]))
+    elif name == "bsr":
+        c = synth.block_sparse()
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    c["workload"] = name
+    return c
+
+
+def accounting(c):
+    """(flops, algorithmic bytes) of one step, by the compulsory-traffic rules."""
+    M, K, nnz = c["M"], c["K"], c["row"].size
+    w = c["workload"]
+    if w in ("power-law", "uniform"):
+        ybytes = 8 * M if c["beta"] != 0 else 4 * M
+        return 2 * nnz, 8 * nnz + 4 * (M + 1) + 4 * K + ybytes
+    if w == "dual":
+        # u = A v - a u (reads v, reads+writes u); v = A^T u - b v (reads u, reads+writes v)
+        b1 = 8 * nnz + 4 * (M + 1) + 4 * K + 8 * M
+        b2 = 8 * nnz + 4 * (K + 1) + 4 * M + 8 * K
+        return 4 * nnz, b1 + b2
+    if w.startswith("spmm"):
+        N = c["N"]
+        return 2 * nnz * N, 8 * nnz + 4 * (M + 1) + 4 * K * N + 4 * M * N
+    if w == "bsr":
+        nb = c["bcols"].size
+        bs, N = c["bs"], c["N"]
+        return 2 * nb * bs * bs * N, 2 * nb * bs * bs + 4 * nb + 4 * (M // bs + 1) + 2 * K * N + 4 * M * N
+    raise ValueError(w)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+
+    from csr_bsr_spmv_gb300 import spx
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    c = make_workload(args.workload, args.rows)
+    flops, abytes = accounting(c)
+    M, K = c["M"], c["K"]
+    w = c["workload"]
+    stream = torch.cuda.Stream(device=dev)
+    timings = {}
+
+    t0 = time.perf_counter()
+    if w == "bsr":
+        rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val_bf16"])
+    else:
+        rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val"])
+    timings["build_csr_ms"] = 1e3 * (time.perf_counter() - t0)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > L2
+    run = None
+    prep = None
+    h2d = d2h = 0
+    e2e_run = None
+    kernel_key = None
+
+    if w in ("power-law", "uniform"):
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
+        t0 = time.perf_counter()
+        plan = spx.spx_plan_csr(M, K, A.nnz, rp, device=dev, stream=stream)
+        timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
+        x = to_dev(c["x"])
+        y = to_dev(c["y"])
+        alpha, beta = c["alpha"], c["beta"]
+        kernel_key = "spmv_tasks_kernel"
+        src = source_hash("spx_spmv.cu")
+
+        def run():
+            spx.spx_spmv_csr(plan, A, x, y, alpha, beta, stream=stream)
+
+        xh = torch.from_numpy(c["x"]).pin_memory()
+        yh = torch.from_numpy(c["y"]).pin_memory()
+        yo = torch.empty_like(yh).pin_memory()
+        h2d = xh.numel() * 4 + (yh.numel() * 4 if beta != 0 else 0)
+        d2h = yo.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                x.copy_(xh, non_blocking=True)
+                if beta != 0:
+                    y.copy_(yh, non_blocking=True)
+                spx.spx_spmv_csr(plan, A, x, y, alpha, beta, stream=stream)
+                yo.copy_(y, non_blocking=True)
+
+        info = dict(plan.info)
+        extra = {"plan": {k: info[k] for k in ("tasks", "long_rows", "cta_rows", "split_rows", "thread_groups",
+                                                "lane_groups")}, "row_stats": plan.stats}
+    elif w == "dual":
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
+        t0 = time.perf_counter()
+        trp, tc, tv = spx.spx_transpose_csr(M, K, rp, col, val)
+        timings["transpose_ms"] = 1e3 * (time.perf_counter() - t0)
+        At = spx.Csr(K, M, to_dev(trp), to_dev(tc), to_dev(tv))
+        t0 = time.perf_counter()
+        pA = spx.spx_plan_csr(M, K, A.nnz, rp, device=dev, stream=stream)
+        pAt = spx.spx_plan_csr(K, M, A.nnz, trp, device=dev, stream=stream)
+        timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
+        u = to_dev(c["u0"])
+        v = to_dev(c["v0"])
+        a, b = float(c["alphas"][0]), float(c["betas"][0])
+        kernel_key = "spmv_tasks_kernel"
+        src = source_hash("spx_spmv.cu")
+
+        u0, v0 = u.clone(), v.clone()
+
+        def prep():  # every step starts from (u0, v0); untimed
+            u.copy_(u0)
+            v.copy_(v0)
+
+        def run():
+            spx.spx_spmv_csr_dual(pA, pAt, A, At, v, u, 1.0, -a, 1.0, -b, stream=stream)
+
+        uh = torch.from_numpy(c["u0"]).pin_memory()
+        vh = torch.from_numpy(c["v0"]).pin_memory()
+        uo, vo = torch.empty_like(uh).pin_memory(), torch.empty_like(vh).pin_memory()
+        h2d = (uh.numel() + vh.numel()) * 4
+        d2h = h2d
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                u.copy_(uh, non_blocking=True)
+                v.copy_(vh, non_blocking=True)
+                spx.spx_spmv_csr_dual(pA, pAt, A, At, v, u, 1.0, -a, 1.0, -b, stream=stream)
+                uo.copy_(u, non_blocking=True)
+                vo.copy_(v, non_blocking=True)
+
+        extra = {"plan_A": dict(pA.info), "plan_At": dict(pAt.info)}
+    elif w.startswith("spmm"):
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
+        B = to_dev(c["B"])
+        C = torch.empty(M, c["N"], device=dev)
+        kernel_key = "spmm_vec_kernel"
+        src = source_hash("spx_spmm.cu")
+
+        def run():
+            spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream)
+
+        Bh = torch.from_numpy(c["B"]).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 4, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                B.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"variant": spx.spx_spmm_csr_variant(B, C)}
+    else:  # bsr
+        t0 = time.perf_counter()
+        brp, bcol, bval, fill = spx.spx_build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
+        timings["build_bsr_ms"] = 1e3 * (time.perf_counter() - t0)
+        d_brp, d_bcol = to_dev(brp), to_dev(bcol)
+        d_bval = to_dev(bval.view(np.int16))
+        Bm = to_dev(c["B_bf16"].view(np.int16))
+        C = torch.empty(M, c["N"], device=dev)
+        kernel_key = "bsr_spmm_tc_kernel"
+        src = source_hash("spx_bsr.cu")
+
+        def run():
+            spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+
+        Bh = torch.from_numpy(c["B_bf16"].view(np.int16)).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 2, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                Bm.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"fill_ratio": fill, "nnzb": int(bcol.size)}
+
+    # ---------------- timing: warmup, then K steps with an L2 flush between steps
+    def flush_l2():
+        with torch.cuda.stream(stream):
+            if prep is not None:
+                prep()
+            flush.fill_(1.0)
+
+    for _ in range(args.warmup):
+        flush_l2()
+        run()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = spx.launch_count()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        for s, e in ev:
+            flush_l2()
+            s.record(stream)
+            run()
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = spx.launch_count() - launches0
+    times = [s.elapsed_time(e) for s, e in ev]
+    ms = sum(times) / len(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    assert spx.spx_last_device_error(stream) == 0, "device error word set during the timed region"
+
+    # ---------------- end to end through the public call with pinned host buffers
+    e2e = None
+    if e2e_run is not None and not args.no_e2e:
+        for _ in range(2):
+            e2e_run()
+        torch.cuda.synchronize(dev)
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(max(3, args.steps // 2))]
+        for s, e in es:
+            flush_l2()
+            s.record(stream)
+            e2e_run()
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = sum(s.elapsed_time(e) for s, e in es) / len(es)
+        e2e = {"value": round(world * flops / (ems * 1e-3) / 1e9, 3), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4)}
+
+    pk = peaks()
+    gflops = world * flops / (ms * 1e-3) / 1e9
+    if w == "bsr":
+        ach = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16"], 4), "peak_source": pk["src"] + " (bf16 dense, burst)"}
+    else:
+        ach = abytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm"], 4), "peak_source": pk["src"] + " (HBM copy)"}
+    tr = traffic_from_profile(kernel_key, src)
+    roof["traffic"] = tr
+    roof["algorithmic_bytes"] = int(abytes)
+    roof["timed"] = "whole step (all launches of the call), CUDA events on the launching stream"
+
+    line = {
+        "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16->f32" if w == "bsr" else "f32", "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
+                   "N": c.get("N", 1), "l2": "flushed between steps (256 MB write); inputs also exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": round(abytes / (ms * 1e-3) / 1e9, 1), "roofline": roof, "e2e": e2e, "gpu_launches": int(launches),
+        "conversion": {k: round(v, 2) for k, v in timings.items()}, "detail": extra,
+        "step_ms_min": round(min(times), 5), "step_ms_median": round(statistics.median(times), 5),
+    }
+    line["clocks"] = clk.summary()
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def row_major_csr(c, val):
+    """The generator emits COO sorted by (row, col); its CSR row offsets are the
+    first position of each row (no builder involved)."""
+    rp = np.searchsorted(c["row"], np.arange(c["M"] + 1), side="left").astype(np.int32)
+    return rp, c["col"], val
+
+
+def cpu_step_fn(c):
+    """One bounded sample of the workload run by the oracle; returns (fn, flops, sample)."""
+    import oracle
+
+    w = c["workload"]
+    M, K = c["M"], c["K"]
+    if w == "bsr":
+        rp, col, val = row_major_csr(c, c["val_bf16"])
+        brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
+        rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every block-row
+        nb = np.diff(brp)
+        fl = 2 * int(nb.sum()) * c["bs"] * c["N"]
+        return (lambda: oracle.bsr_spmm(M, K, c["bs"], c["bs"], brp, bcol, bval, c["B_bf16"], rows=rows)), fl, \
+            f"{rows.size} output rows (one per block-row) of the {M}x{K} BSR product"
+    rp, col, val = row_major_csr(c, c["val"])
+    if w in ("power-law", "uniform"):
+        return (lambda: oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"])), 2 * int(rp[-1]), \
+            "the full matrix, one SpMV"
+    if w == "dual":
+        trp, tc, tv = oracle.transpose(M, K, rp, col, val)
+
+        def f():
+            u1, _ = oracle.spmv(M, rp, col, val, c["v0"], 1.0, -float(c["alphas"][0]), c["u0"])
+            oracle.spmv(K, trp, tc, tv, u1.astype(np.float32), 1.0, -float(c["betas"][0]), c["v0"])
+        return f, 4 * int(rp[-1]), "the full operator pair, one iteration"
+    N = c["N"]
+    rows = np.arange(0, M, 16, dtype=np.int32)
+    fl = 2 * int(np.diff(rp)[rows].sum()) * N
+    return (lambda: oracle.spmm(M, rp, col, val, c["B"], rows=rows)), fl, f"every 16th row ({rows.size} rows)"
+
+
+def cpu_baseline(c, budget_s=12.0):
+    fn, fl, sample = cpu_step_fn(c)
+    fn()  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 50:
+            break
+    return {"value": round(n * fl / el / 1e9, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample}, repeated {n}x ({el:.1f} s, fp64, single thread)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    c = make_workload(args.workload, args.rows)
+    fn, fl, sample = cpu_step_fn(c)
+    for _ in range(args.warmup):
+        fn()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(ts) / len(ts)
+    val = fl / (ms * 1e-3) / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
+            "config": {"workload": c["name"], "M": c["M"], "K": c["K"], "nnz": int(c["row"].size),
+                       "N": c.get("N", 1)},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{sample} per step (fp64, single thread)"},
+            "e2e": {"value": round(val, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="power-law",
+                    choices=["power-law", "uniform", "dual", "spmm32", "spmm128", "bsr"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rows", type=int, default=0, help="smaller power-law matrix (profiling only)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

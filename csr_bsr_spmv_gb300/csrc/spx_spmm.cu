@@ -1,0 +1,195 @@
+// spx_spmm.cu -- CSR SpMM C = alpha*A*B + beta*C on sm_103a, B and C dense
+// row-major.  [SpMM-ops] §3: for each stored A(i,k), the contiguous run
+// B(k, n:n+N_TILE) updates register accumulators; C is written once.
+// The variant is chosen by N ([SpMM-ops] §3.1-§3.3):
+//   small   N <= 8     : lanes split the row's nonzeros, N accumulators per lane,
+//                        warp-shuffle reduction of each column;
+//   subwarp N%4 == 0, N <= 128: a sub-warp of L = pow2ceil(N/4) lanes per row,
+//                        each lane owns 4 adjacent columns (float4 loads of B);
+//                        32/L rows per warp, so a 4-row cluster shares one warp
+//                        and its B rows hit in L1;
+//   tiled   N%4 == 0, N > 128: a warp owns (row, 128-column tile); the tile
+//                        index is the outer grid dimension so one B column
+//                        slice stays L2-resident while all rows pass over it;
+//   scalar  otherwise  : a warp per row, lanes over columns.
+#include <cuda_runtime.h>
+
+#include "spx_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
+__device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
+
+// ------------------------------------------------------------- small N
+template <int N>
+__global__ void __launch_bounds__(kThreads) spmm_small_kernel(int M, const int* __restrict__ rp,
+                                                              const int* __restrict__ col,
+                                                              const float* __restrict__ val,
+                                                              const float* __restrict__ B, long long ldb,
+                                                              float alpha, float beta, float* C, long long ldc) {
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    float acc[N];
+#pragma unroll
+    for (int c = 0; c < N; ++c) acc[c] = 0.f;
+    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    for (int p = a + lane; p < b; p += 32) {
+        const float v = ld_stream(val + p);
+        const float* brow = B + (long long)ld_stream(col + p) * ldb;
+#pragma unroll
+        for (int c = 0; c < N; ++c) acc[c] += v * __ldg(brow + c);
+    }
+#pragma unroll
+    for (int c = 0; c < N; ++c)
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) acc[c] += __shfl_down_sync(0xffffffffu, acc[c], d);
+    if (lane == 0) {
+        float* crow = C + (long long)row * ldc;
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+            float r = alpha * acc[c];
+            if (beta != 0.f) r += beta * crow[c];
+            crow[c] = r;
+        }
+    }
+}
+
+// ------------------------------------------------------------- float4 sub-warp / tiled
+// L lanes per row, each lane 4 columns; the warp holds 32/L rows.  Column
+// tile origin = blockIdx.y * 4 * L (tiled variant: L = 32, gridDim.y tiles).
+template <int L>
+__global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const int* __restrict__ rp,
+                                                            const int* __restrict__ col,
+                                                            const float* __restrict__ val,
+                                                            const float* __restrict__ B, long long ldb, float alpha,
+                                                            float beta, float* C, long long ldc) {
+    constexpr int RPW = 32 / L;  // rows per warp
+    const int lane = threadIdx.x & 31;
+    const int row = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW + lane / L;
+    const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
+    if (row >= M) return;
+    const bool live = n0 < N;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    const float* Bc = B + n0;
+    int p = a;
+    for (; p + 3 < b; p += 4) {
+        const int c0 = ld_stream(col + p), c1 = ld_stream(col + p + 1), c2 = ld_stream(col + p + 2),
+                  c3 = ld_stream(col + p + 3);
+        const float v0 = ld_stream(val + p), v1 = ld_stream(val + p + 1), v2 = ld_stream(val + p + 2),
+                    v3 = ld_stream(val + p + 3);
+        if (live) {
+            const float4 b0 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c0 * ldb));
+            const float4 b1 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c1 * ldb));
+            const float4 b2 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c2 * ldb));
+            const float4 b3 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c3 * ldb));
+            acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
+            acc.x += v1 * b1.x; acc.y += v1 * b1.y; acc.z += v1 * b1.z; acc.w += v1 * b1.w;
+            acc.x += v2 * b2.x; acc.y += v2 * b2.y; acc.z += v2 * b2.z; acc.w += v2 * b2.w;
+            acc.x += v3 * b3.x; acc.y += v3 * b3.y; acc.z += v3 * b3.z; acc.w += v3 * b3.w;
+        }
+    }
+    for (; p < b; ++p) {
+        const int c0 = ld_stream(col + p);
+        const float v0 = ld_stream(val + p);
+        if (live) {
+            const float4 b0 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c0 * ldb));
+            acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
+        }
+    }
+    if (!live) return;
+    float4* cp = reinterpret_cast<float4*>(C + (long long)row * ldc + n0);
+    float4 r = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
+    if (beta != 0.f) {
+        const float4 o = *cp;
+        r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
+    }
+    *cp = r;
+}
+
+// ------------------------------------------------------------- scalar fallback
+__global__ void __launch_bounds__(kThreads) spmm_scalar_kernel(int M, int N, const int* __restrict__ rp,
+                                                               const int* __restrict__ col,
+                                                               const float* __restrict__ val,
+                                                               const float* __restrict__ B, long long ldb,
+                                                               float alpha, float beta, float* C, long long ldc) {
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    for (int n = blockIdx.y * 32 + lane; n < N; n += 32 * gridDim.y) {
+        float acc = 0.f;
+        for (int p = a; p < b; ++p) acc += __ldg(val + p) * __ldg(B + (long long)__ldg(col + p) * ldb + n);
+        float r = alpha * acc;
+        float* cp = C + (long long)row * ldc + n;
+        if (beta != 0.f) r += beta * *cp;
+        *cp = r;
+    }
+}
+
+int pick_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc) {
+    if (N <= 8) return 0;
+    const bool vec = (N % 4 == 0) && (ldb % 4 == 0) && (ldc % 4 == 0) && spx_aligned(B, 16) && spx_aligned(C, 16);
+    if (!vec) return 3;
+    return N <= 128 ? 1 : 2;
+}
+
+template <int L>
+void launch_vec(int M, int N, const int* rp, const int* col, const float* val, const float* B, long long ldb,
+                float alpha, float beta, float* C, long long ldc, int tiles, cudaStream_t st) {
+    constexpr int rows_per_cta = kWarps * (32 / L);
+    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, tiles);
+    spmm_vec_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc) {
+    return pick_variant(N, B, ldb, C, ldc);
+}
+
+spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
+                        int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                        spx_stream_t stream) {
+    if (M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
+    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 4) || !spx_aligned(B, 4) ||
+        !spx_aligned(C, 4))
+        return SPX_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int v = pick_variant(N, B, ldb, C, ldc);
+    if (v == 0) {
+        const int grid = (M + kWarps - 1) / kWarps;
+        switch (N) {
+#define SPX_SMALL(n) case n: spmm_small_kernel<n><<<grid, kThreads, 0, st>>>(M, rp, col, val, B, ldb, alpha, beta, C, ldc); break;
+            SPX_SMALL(1) SPX_SMALL(2) SPX_SMALL(3) SPX_SMALL(4) SPX_SMALL(5) SPX_SMALL(6) SPX_SMALL(7) SPX_SMALL(8)
+#undef SPX_SMALL
+        }
+    } else if (v == 1) {
+        const int q = N / 4;
+        if (q <= 2) launch_vec<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
+        else if (q <= 4) launch_vec<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
+        else if (q <= 8) launch_vec<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
+        else if (q <= 16) launch_vec<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
+        else launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
+    } else if (v == 2) {
+        launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, (N + 127) / 128, st);
+    } else {
+        dim3 grid((M + kWarps - 1) / kWarps, (N + 31) / 32 < 4 ? (N + 31) / 32 : 4);
+        spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+    }
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,355 @@
+"""Thin ctypes binding over libspx (include/spx.h).
+
+Every function here marshals arguments -- tensor pointers, sizes, the current
+CUDA stream -- into one C-ABI call of the same name; all computation runs in
+the library.  PyTorch supplies device memory and streams only.  There is no
+fallback: if libspx.so is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspx.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "spx.h")
+
+SPX_HOST, SPX_DEVICE = 0, 1
+STATUS = {0: "SPX_OK", -1: "SPX_ERR_ARG", -2: "SPX_ERR_INDEX_RANGE", -3: "SPX_ERR_NOT_SORTED",
+          -4: "SPX_ERR_DUPLICATE", -5: "SPX_ERR_CUDA", -6: "SPX_ERR_TIMEOUT", -7: "SPX_ERR_UNSUPPORTED",
+          -8: "SPX_ERR_ALIGN", -9: "SPX_ERR_NOMEM", -10: "SPX_ERR_NOT_READY"}
+SPMM_VARIANTS = {0: "small-N", 1: "subwarp-float4", 2: "tiled-float4", 3: "scalar"}
+
+
+class SpxError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        msg = _lib().spx_status_string(code).decode() if _LIB is not None else self.name
+        super().__init__(f"{where}: {msg}")
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("block_nnz", ctypes.c_int32), ("block_rows", ctypes.c_int32), ("pack_max", ctypes.c_int32),
+                ("cta_max", ctypes.c_int32), ("seg_nnz", ctypes.c_int32), ("lanes_div", ctypes.c_int32)]
+
+
+class RowStats(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("nnz", ctypes.c_int64), ("sumsq", ctypes.c_int64),
+                ("min", ctypes.c_int32), ("max", ctypes.c_int32), ("p50", ctypes.c_int32),
+                ("p95", ctypes.c_int32), ("p99", ctypes.c_int32), ("empty", ctypes.c_int32),
+                ("mean", ctypes.c_double), ("var", ctypes.c_double), ("cv", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("K", ctypes.c_int64), ("nnz", ctypes.c_int64), ("tasks", ctypes.c_int64),
+                ("long_rows", ctypes.c_int64), ("slots", ctypes.c_int64), ("packed_rows", ctypes.c_int64),
+                ("cta_rows", ctypes.c_int64), ("split_rows", ctypes.c_int64), ("thread_groups", ctypes.c_int64),
+                ("lane_groups", ctypes.c_int64), ("table_bytes", ctypes.c_size_t),
+                ("scratch_bytes", ctypes.c_size_t), ("stats", RowStats)]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        d = ctypes.POINTER(ctypes.c_double)
+        sigs = {
+            "spx_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "spx_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+            "spx_build_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+            "spx_transpose_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+            "spx_build_bsr": ([i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
+                               ctypes.c_int, vp], ctypes.c_int),
+            "spx_check_csr": ([i32, i32, i64, vp, vp, i32, ctypes.c_int, vp], ctypes.c_int),
+            "spx_row_stats": ([i32, vp, ctypes.c_int, ctypes.POINTER(RowStats)], ctypes.c_int),
+            "spx_plan_opts_default": ([ctypes.POINTER(PlanOpts)], ctypes.c_int),
+            "spx_plan_csr": ([i32, i32, i64, vp, ctypes.c_int, ctypes.POINTER(PlanOpts), ctypes.POINTER(vp)],
+                             ctypes.c_int),
+            "spx_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], ctypes.c_int),
+            "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
+            "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
+            "spx_plan_destroy": ([vp], ctypes.c_int),
+            "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
+            "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
+                                   sz, vp], ctypes.c_int),
+            "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
+            "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, vp, i64, vp], ctypes.c_int),
+            "spx_last_device_error": ([vp], ctypes.c_int),
+        }
+        for name, (args, res) in sigs.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def header_symbols() -> list[str]:
+    """Function names declared in include/spx.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(spx_\w+)\s*\(", text, re.M)))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise SpxError(rc, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p) if t.size else None
+    raise TypeError(type(t))
+
+
+def _stream(stream=None):
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream) if stream.cuda_stream else None
+
+
+def _where(*arrays) -> int:
+    dev = [isinstance(a, torch.Tensor) and a.is_cuda for a in arrays if a is not None]
+    if any(dev) and not all(dev):
+        raise ValueError("mix of host and device arrays")
+    return SPX_DEVICE if dev and all(dev) else SPX_HOST
+
+
+def _empty_like_loc(ref, n, dtype_np, dtype_t):
+    if isinstance(ref, torch.Tensor) and ref.is_cuda:
+        return torch.empty(int(n), dtype=dtype_t, device=ref.device)
+    return np.empty(int(n), dtype=dtype_np)
+
+
+_TDT = {np.dtype(np.float32): torch.float32, np.dtype(np.float64): torch.float64,
+        np.dtype(np.uint16): torch.int16, np.dtype(np.int16): torch.int16, np.dtype(np.int32): torch.int32}
+
+
+def _itemsize(a) -> int:
+    return a.element_size() if isinstance(a, torch.Tensor) else a.itemsize
+
+
+def launch_count() -> int:
+    c = ctypes.c_uint64(0)
+    _check(_lib().spx_launch_count(ctypes.byref(c)), "spx_launch_count")
+    return c.value
+
+
+# ------------------------------------------------------------------ builders
+
+def spx_build_csr(M: int, K: int, coo_row, coo_col, coo_val, stream=None):
+    """COO -> CSR; arrays all host (numpy) or all device (torch cuda)."""
+    where = _where(coo_row, coo_col, coo_val)
+    nnz = coo_row.numel() if isinstance(coo_row, torch.Tensor) else coo_row.size
+    vb = _itemsize(coo_val)
+    rp = _empty_like_loc(coo_row, M + 1, np.int32, torch.int32)
+    col = _empty_like_loc(coo_row, nnz, np.int32, torch.int32)
+    if isinstance(coo_val, torch.Tensor):
+        val = torch.empty(nnz, dtype=coo_val.dtype, device=coo_val.device)
+    else:
+        val = np.empty(nnz, dtype=coo_val.dtype)
+    _check(_lib().spx_build_csr(M, K, nnz, _ptr(coo_row), _ptr(coo_col), _ptr(coo_val), vb, _ptr(rp), _ptr(col),
+                                _ptr(val), where, _stream(stream) if where == SPX_DEVICE else None), "spx_build_csr")
+    return rp, col, val
+
+
+def spx_transpose_csr(M: int, K: int, row_ptr, col, val, stream=None):
+    where = _where(row_ptr, col, val)
+    nnz = col.numel() if isinstance(col, torch.Tensor) else col.size
+    trp = _empty_like_loc(row_ptr, K + 1, np.int32, torch.int32)
+    tcol = _empty_like_loc(row_ptr, nnz, np.int32, torch.int32)
+    if isinstance(val, torch.Tensor):
+        tval = torch.empty(nnz, dtype=val.dtype, device=val.device)
+    else:
+        tval = np.empty(nnz, dtype=val.dtype)
+    _check(_lib().spx_transpose_csr(M, K, nnz, _ptr(row_ptr), _ptr(col), _ptr(val), _itemsize(val), _ptr(trp),
+                                    _ptr(tcol), _ptr(tval), where, _stream(stream) if where == SPX_DEVICE else None),
+           "spx_transpose_csr")
+    return trp, tcol, tval
+
+
+def spx_build_bsr(M: int, K: int, row_ptr, col, val, br: int, bc: int, stream=None):
+    """CSR -> BSR (two calls).  Returns (bsr_row_ptr, bsr_col, bsr_val[nnzb, br, bc], fill)."""
+    where = _where(row_ptr, col, val)
+    lib = _lib()
+    MB = (M + br - 1) // br
+    nnzb = ctypes.c_int64(0)
+    fill = ctypes.c_double(0.0)
+    st = _stream(stream) if where == SPX_DEVICE else None
+    brp = _empty_like_loc(row_ptr, MB + 1, np.int32, torch.int32)
+    _check(lib.spx_build_bsr(M, K, _ptr(row_ptr), _ptr(col), _ptr(val), _itemsize(val), br, bc, _ptr(brp), None,
+                             None, ctypes.byref(nnzb), ctypes.byref(fill), where, st), "spx_build_bsr(count)")
+    nb = nnzb.value
+    bcol = _empty_like_loc(row_ptr, nb, np.int32, torch.int32)
+    if isinstance(val, torch.Tensor):
+        bval = torch.empty(nb * br * bc, dtype=val.dtype, device=val.device)
+    else:
+        bval = np.empty(nb * br * bc, dtype=val.dtype)
+    if nb:
+        _check(lib.spx_build_bsr(M, K, _ptr(row_ptr), _ptr(col), _ptr(val), _itemsize(val), br, bc, None,
+                                 _ptr(bcol), _ptr(bval), ctypes.byref(nnzb), ctypes.byref(fill), where, st),
+               "spx_build_bsr")
+    return brp, bcol, bval.reshape(nb, br, bc), fill.value
+
+
+def spx_check_csr(M: int, K: int, row_ptr, col, strict: bool = True, stream=None) -> int:
+    """Returns the spx_status of the structural check (0 == valid)."""
+    where = _where(row_ptr, col)
+    nnz = col.numel() if isinstance(col, torch.Tensor) else col.size
+    return _lib().spx_check_csr(M, K, nnz, _ptr(row_ptr), _ptr(col), int(strict), where,
+                                _stream(stream) if where == SPX_DEVICE else None)
+
+
+def spx_row_stats(M: int, row_ptr) -> dict:
+    st = RowStats()
+    _check(_lib().spx_row_stats(M, _ptr(row_ptr), _where(row_ptr), ctypes.byref(st)), "spx_row_stats")
+    return st.as_dict()
+
+
+def spx_plan_opts_default() -> dict:
+    o = PlanOpts()
+    _check(_lib().spx_plan_opts_default(ctypes.byref(o)), "spx_plan_opts_default")
+    return {f: getattr(o, f) for f, _ in PlanOpts._fields_}
+
+
+# ------------------------------------------------------------------ plan
+
+class Plan:
+    """Owns an spx_plan*, its device table and its scratch (torch tensors)."""
+
+    def __init__(self, M: int, K: int, nnz: int, row_ptr, opts: dict | None = None, device=None, upload=True,
+                 stream=None):
+        lib = _lib()
+        o = None
+        if opts:
+            base = spx_plan_opts_default()
+            base.update(opts)
+            o = PlanOpts(**base)
+        h = ctypes.c_void_p()
+        _check(lib.spx_plan_csr(M, K, nnz, _ptr(row_ptr), _where(row_ptr), ctypes.byref(o) if o else None,
+                                ctypes.byref(h)), "spx_plan_csr")
+        self.handle = h
+        self.M, self.K, self.nnz = M, K, nnz
+        info = PlanInfo()
+        _check(lib.spx_plan_get_info(h, ctypes.byref(info)), "spx_plan_get_info")
+        self.info = {f: getattr(info, f) for f, _ in PlanInfo._fields_ if f != "stats"}
+        self.stats = info.stats.as_dict()
+        self.table = None
+        self.scratch = None
+        if upload:
+            dev = device or (row_ptr.device if isinstance(row_ptr, torch.Tensor) and row_ptr.is_cuda else "cuda")
+            self.table = torch.empty(max(1, (self.info["table_bytes"] + 15) // 16 * 4), dtype=torch.int32,
+                                     device=dev)
+            self.scratch = torch.empty(max(1, self.info["scratch_bytes"] // 4), dtype=torch.float32, device=dev)
+            _check(lib.spx_plan_upload(h, _ptr(self.table), self.table.numel() * 4, _stream(stream)),
+                   "spx_plan_upload")
+
+    def tasks(self):
+        t = np.empty((self.info["tasks"], 4), np.int32)
+        lr = np.empty((self.info["long_rows"], 4), np.int32)
+        _check(_lib().spx_plan_get_tasks(self.handle, _ptr(t), _ptr(lr)), "spx_plan_get_tasks")
+        return t, lr
+
+    def close(self):
+        if self.handle:
+            _lib().spx_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spx_plan_csr(M: int, K: int, nnz: int, row_ptr, opts: dict | None = None, **kw) -> Plan:
+    return Plan(M, K, nnz, row_ptr, opts, **kw)
+
+
+@dataclass
+class Csr:
+    """A CSR matrix held as device tensors (int32 row_ptr/col, fp32 val)."""
+    M: int
+    K: int
+    row_ptr: torch.Tensor
+    col: torch.Tensor
+    val: torch.Tensor
+
+    @property
+    def nnz(self) -> int:
+        return self.col.numel()
+
+
+# ------------------------------------------------------------------ products
+
+def spx_spmv_csr(plan: Plan, A: Csr, x: torch.Tensor, y: torch.Tensor, alpha: float = 1.0, beta: float = 0.0,
+                 stream=None, scratch: torch.Tensor | None = None):
+    """y <- alpha*A*x + beta*y (in place)."""
+    sc = plan.scratch if scratch is None else scratch
+    _check(_lib().spx_spmv_csr(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
+                               float(alpha), _ptr(x), float(beta), _ptr(y), _ptr(sc), sc.numel() * 4,
+                               _stream(stream)), "spx_spmv_csr")
+    return y
+
+
+def spx_spmv_csr_dual(plan_A: Plan, plan_At: Plan, A: Csr, At: Csr, v: torch.Tensor, u: torch.Tensor,
+                      alpha_u: float, beta_u: float, alpha_v: float, beta_v: float, stream=None,
+                      scratch: torch.Tensor | None = None):
+    """u <- alpha_u*A v + beta_u*u, then v <- alpha_v*A^T u + beta_v*v (in place)."""
+    if scratch is None:
+        scratch = plan_A.scratch if plan_A.scratch.numel() >= plan_At.scratch.numel() else plan_At.scratch
+    _check(_lib().spx_spmv_csr_dual(plan_A.handle, plan_At.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col),
+                                    _ptr(A.val), _ptr(At.row_ptr), _ptr(At.col), _ptr(At.val), _ptr(v),
+                                    float(alpha_u), float(beta_u), _ptr(u), float(alpha_v), float(beta_v),
+                                    _ptr(scratch), scratch.numel() * 4, _stream(stream)), "spx_spmv_csr_dual")
+    return u, v
+
+
+def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha*A*B + beta*C; B (K x N) and C (M x N) row-major views (stride(1) == 1)."""
+    N = B.shape[1]
+    assert B.stride(1) == 1 and C.stride(1) == 1
+    _check(_lib().spx_spmm_csr(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
+                               B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
+           "spx_spmm_csr")
+    return C
+
+
+def spx_spmm_csr_variant(B: torch.Tensor, C: torch.Tensor) -> str:
+    v = _lib().spx_spmm_csr_variant(B.shape[1], _ptr(B), B.stride(0), _ptr(C), C.stride(0))
+    return SPMM_VARIANTS[v]
+
+
+def spx_spmm_bsr(M: int, K: int, br: int, bc: int, bsr_row_ptr, bsr_col, bsr_val, B: torch.Tensor,
+                 C: torch.Tensor, stream=None):
+    """C <- A*B, A BSR (bf16 blocks held as int16/uint16 bit patterns or bfloat16), B bf16, C fp32."""
+    nnzb = bsr_col.numel()
+    N = B.shape[1]
+    _check(_lib().spx_spmm_bsr(M, K, br, bc, nnzb, _ptr(bsr_row_ptr), _ptr(bsr_col), _ptr(bsr_val), N, _ptr(B),
+                               B.stride(0), _ptr(C), C.stride(0), _stream(stream)), "spx_spmm_bsr")
+    return C
+
+
+def spx_last_device_error(stream=None) -> int:
+    return _lib().spx_last_device_error(_stream(stream))

@@ -1,0 +1,296 @@
+/*
+ * spx.h -- C ABI of libspx: sparse x dense products on one GB300 (sm_103a).
+ *
+ * Operations (page titles as cited throughout this library):
+ *   [SpMM-ops]    "通用稀疏矩阵乘法CUDA算子实现" (chengzipai.xyz)
+ *   [BCSR-SpMV]   "GPU加速实战用BCSR格式优化稀疏矩阵乘法附CUDA代码" (xxqk.cn)
+ *   [AsyncSparse] AsyncSparse summary, "异步GPU架构下的稀疏矩阵乘法加速" (capital-peak.com)
+ *   [LSMR-dual]   "CUDA LSMR 专栏（二）：用 CSR/CSC 双存储压榨双向 SpMV" (chengzipai.xyz)
+ *   [Formats]     "稀疏矩阵存储格式:COO、CSR、ELL、Hybrid 与块稀疏" (geek-doc.cn)
+ *
+ * Conventions for every call:
+ *   - The caller owns every array.  The library allocates no device memory on
+ *     the compute calls; sizes of the extra device buffers a call needs (the
+ *     plan table, the scratch for long-row partial sums) are reported by the
+ *     plan so the caller can allocate them once.
+ *   - Indices are 0-based int32.  Any size or index that does not fit int32
+ *     (M, K, nnz, nnz of a block pattern) is rejected with
+ *     SPX_ERR_INDEX_RANGE, never truncated ([LSMR-dual] §8).
+ *   - Device work is enqueued on `stream` (NULL = the legacy default stream)
+ *     and the call returns after enqueueing; results are ready when the
+ *     stream reaches that point.  Host-side builders finish before return.
+ *   - beta == 0 means the output is write-only: it is not read, so NaN/Inf
+ *     already in it do not propagate.
+ *   - No call aborts; every failure is a negative spx_status and, for a
+ *     rejected argument, nothing is launched.
+ */
+#ifndef SPX_H_
+#define SPX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* spx_stream_t; /* same type as cudaStream_t */
+
+typedef enum spx_status {
+    SPX_OK = 0,
+    SPX_ERR_ARG = -1,          /* null pointer, negative size, bad option, plan mismatch */
+    SPX_ERR_INDEX_RANGE = -2,  /* size/index beyond int32, or an index outside [0, dim) */
+    SPX_ERR_NOT_SORTED = -3,   /* row_ptr not monotone / columns not ascending where required */
+    SPX_ERR_DUPLICATE = -4,    /* a repeated (row, col) where one value slot exists */
+    SPX_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+    SPX_ERR_TIMEOUT = -6,      /* a bounded device wait gave up (see spx_last_device_error) */
+    SPX_ERR_UNSUPPORTED = -7,  /* shape/type combination this build has no kernel for */
+    SPX_ERR_ALIGN = -8,        /* pointer or leading dimension not aligned as documented */
+    SPX_ERR_NOMEM = -9,        /* host allocation failed */
+    SPX_ERR_NOT_READY = -10    /* plan used before spx_plan_upload */
+} spx_status;
+
+typedef enum spx_loc {
+    SPX_HOST = 0,   /* all array arguments of the call are host pointers   */
+    SPX_DEVICE = 1  /* all array arguments of the call are device pointers */
+} spx_loc;
+
+/* Human-readable name of a status code (static string). */
+const char* spx_status_string(spx_status s);
+
+/* Number of kernel launches this library has issued since load. */
+spx_status spx_launch_count(uint64_t* count);
+
+/* ------------------------------------------------------------ format builders */
+
+/*
+ * COO -> CSR.  [Formats] §3: count entries per row (histogram), exclusive
+ * prefix sum -> row_ptr[M+1], then move col/val into each row's range;
+ * [SpMM-ops] §1.2: entries end sorted by (row, col).  Entries with equal
+ * (row, col) are kept (not summed), in input order.
+ *   coo_row, coo_col, coo_val: nnz entries in any order; coo_val holds
+ *     val_bytes bytes per entry (2, 4 or 8; values are moved, not read).
+ *   row_ptr[M+1], col[nnz], val[nnz*val_bytes]: outputs.
+ * Errors: SPX_ERR_INDEX_RANGE for a row outside [0, M) or col outside [0, K).
+ * where == SPX_DEVICE: arrays are device memory; they are staged through
+ * host memory and the call synchronises `stream`.
+ */
+spx_status spx_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_row, const int32_t* coo_col,
+                         const void* coo_val, int32_t val_bytes, int32_t* row_ptr, int32_t* col, void* val,
+                         spx_loc where, spx_stream_t stream);
+
+/*
+ * CSR(A) (M x K) -> CSR(A^T) (K x M), which is CSC(A): [LSMR-dual] §2 (CSC(A)
+ * has exactly the memory layout of CSR(A^T)) and §4 (build it once, at
+ * construction).  Output row j holds the entries of column j in increasing
+ * source row order (a stable counting sort by column).
+ *   t_row_ptr[K+1], t_col[nnz], t_val[nnz*val_bytes]: outputs.
+ * Errors: SPX_ERR_ARG if row_ptr[0] != 0 or row_ptr[M] != nnz;
+ * SPX_ERR_INDEX_RANGE for a column outside [0, K).
+ * where == SPX_DEVICE: staged through host memory (synchronises `stream`).
+ */
+spx_status spx_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                             const void* val, int32_t val_bytes, int32_t* t_row_ptr, int32_t* t_col, void* t_val,
+                             spx_loc where, spx_stream_t stream);
+
+/*
+ * CSR -> BSR with br x bc blocks.  [AsyncSparse] §2.2.1 (store each block
+ * holding at least one entry, dense and contiguous; block_row_ptr,
+ * block_col_idx; fill_ratio = nnz / (nnz_blocks * br * bc)); [BCSR-SpMV] §1
+ * (one block-column index per block).  Blocks are row-major inside; block
+ * columns ascend within a block-row; a last partial block-row/column is
+ * zero-padded (logical M, K unchanged).
+ * Two calls: with bsr_col == NULL and bsr_val == NULL the call only fills
+ * *nnzb_out, *fill_out and (if non-NULL) bsr_row_ptr[ceil(M/br)+1]; then the
+ * caller allocates bsr_col[nnzb] and bsr_val[nnzb*br*bc*val_bytes].
+ * Errors: SPX_ERR_DUPLICATE for a repeated (row, col); SPX_ERR_INDEX_RANGE.
+ * where == SPX_DEVICE stages the arrays through host memory (synchronous).
+ */
+spx_status spx_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                         int32_t val_bytes, int32_t br, int32_t bc, int32_t* bsr_row_ptr, int32_t* bsr_col,
+                         void* bsr_val, int64_t* nnzb_out, double* fill_out, spx_loc where, spx_stream_t stream);
+
+/*
+ * Structural check of a CSR: row_ptr[0] == 0, non-decreasing, row_ptr[M] ==
+ * nnz, every column in [0, K); with strict != 0 also strictly ascending
+ * columns inside each row.  Returns SPX_OK, SPX_ERR_ARG, SPX_ERR_NOT_SORTED,
+ * SPX_ERR_INDEX_RANGE or SPX_ERR_DUPLICATE.  The compute calls trust their
+ * inputs; run this once on untrusted matrices.
+ */
+spx_status spx_check_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                         int32_t strict, spx_loc where, spx_stream_t stream);
+
+/* ------------------------------------------------------------ row statistics */
+
+typedef struct spx_row_stats_t {
+    int64_t rows;    /* M */
+    int64_t nnz;     /* S1 = sum of row lengths l_i */
+    int64_t sumsq;   /* S2 = sum of l_i^2 */
+    int32_t min, max;
+    int32_t p50, p95, p99; /* nearest rank: the ceil(q*M/100)-th smallest l_i */
+    int32_t empty;         /* rows with l_i == 0 */
+    double mean;     /* (double)S1 / (double)M */
+    double var;      /* (double)(M*S2 - S1^2) / ((double)M*(double)M), population */
+    double cv;       /* sqrt(var) / mean, 0 when mean == 0 */
+} spx_row_stats_t;
+
+/*
+ * Row-length statistics of a CSR.  [LSMR-dual] §5.3 (l_i = row_ptr[i+1] -
+ * row_ptr[i]; mean, variance and long tail) and [SpMM-ops] §4 (avg/p95/max
+ * and coefficient of variation in the dispatch key).
+ */
+spx_status spx_row_stats(int32_t M, const int32_t* row_ptr, spx_loc where, spx_row_stats_t* out);
+
+/* ------------------------------------------------------------ dispatch plan */
+
+typedef struct spx_plan_opts_t {
+    int32_t block_nnz;  /* B: most nonzeros in a packed group (one CTA)             */
+    int32_t block_rows; /* R: most rows in a packed group                           */
+    int32_t pack_max;   /* P: rows with l <= P are packed into groups (P <= B)      */
+    int32_t cta_max;    /* C: rows with P < l <= C get one CTA each                 */
+    int32_t seg_nnz;    /* S: rows with l > C are cut into segments of S nonzeros   */
+    int32_t lanes_div;  /* D: a group reduces each row with w lanes,
+                           w = pow2ceil(ceil(nnz_g / (rows_g * D))) clamped to [1, 32] */
+} spx_plan_opts_t;
+
+/* Fills the defaults the benchmarks were tuned with. */
+spx_status spx_plan_opts_default(spx_plan_opts_t* out);
+
+typedef struct spx_plan_info_t {
+    int64_t M, K, nnz;
+    int64_t tasks;         /* CTAs of the main launch                         */
+    int64_t long_rows;     /* rows split into segments                        */
+    int64_t slots;         /* partial sums (one per segment)                  */
+    int64_t packed_rows, cta_rows, split_rows;
+    int64_t thread_groups; /* groups reduced thread-per-row (w == 1)          */
+    int64_t lane_groups;   /* groups reduced with 2..32 lanes per row         */
+    size_t table_bytes;    /* device bytes for spx_plan_upload (16-B aligned) */
+    size_t scratch_bytes;  /* device scratch bytes each SpMV call needs       */
+    spx_row_stats_t stats;
+} spx_plan_info_t;
+
+typedef struct spx_plan spx_plan; /* opaque, host-side */
+
+/*
+ * Build the dispatch plan of a CSR matrix (rows binned by length onto
+ * thread/lane-group, CTA-per-row and split-row kernels).  [SpMM-ops] §2.1-§2.4
+ * (thread-, warp-, CTA-per-row and segmented long rows with a second-pass
+ * reduction), §4 (profile once, cache it on the descriptor) and [Formats] §6
+ * (pack rows into bundles of similar work).  The rule:
+ *   l <= P: packed; consecutive packed rows form groups of <= R rows and <= B
+ *           nonzeros (a CTA or split row closes a group);
+ *   P < l <= C: one CTA;  l > C: ceil(l/S) segments, then a fix-up pass.
+ * Task table (4 int32 per task): first all CTA rows {1,row,0,0} and segments
+ * {2,row,seg,slot} in row order, then groups {256*log2(w), r0, r1, 0}.
+ * Long-row table (4 int32 per split row): {row, first slot, #segments, 0}.
+ * opts == NULL uses spx_plan_opts_default.  row_ptr is read once (copied to
+ * the host when where == SPX_DEVICE).  *plan_out must be released with
+ * spx_plan_destroy.
+ */
+spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, spx_loc where,
+                        const spx_plan_opts_t* opts, spx_plan** plan_out);
+
+spx_status spx_plan_get_info(const spx_plan* plan, spx_plan_info_t* out);
+
+/* Host copies of the task table (4*tasks int32) and long-row table
+   (4*long_rows int32); either pointer may be NULL. */
+spx_status spx_plan_get_tasks(const spx_plan* plan, int32_t* tasks, int32_t* long_rows);
+
+/*
+ * Copy the plan's tables into caller-owned device memory `table` (at least
+ * info.table_bytes, 16-byte aligned) on `stream`, and remember that address.
+ * Must precede the first compute call with this plan; `table` must stay
+ * valid while the plan is used.
+ */
+spx_status spx_plan_upload(spx_plan* plan, void* table, size_t table_bytes, spx_stream_t stream);
+
+spx_status spx_plan_destroy(spx_plan* plan);
+
+/* ------------------------------------------------------------ SpMV */
+
+/*
+ * y = alpha * A x + beta * y, A in CSR (M x K, fp32 values, int32 indices),
+ * fp32 arithmetic.  [SpMM-ops] §2 (y_i = sum over row i of values[p] *
+ * x[col_indices[p]]; thread/warp/CTA/segment mappings), [LSMR-dual] §2 and
+ * §5.2 (alpha/beta with beta scaling the old output).
+ *   plan: built from this row_ptr with the same M, K, nnz, and uploaded.
+ *   x[K], y[M] device fp32 (4-byte aligned); x and y must not overlap.
+ *   scratch: device memory of at least info.scratch_bytes (may be NULL when
+ *     that is 0); two calls that share a scratch buffer must not overlap in
+ *     time.
+ * Each row is reduced in a fixed order, so the result is bitwise
+ * reproducible run to run (no floating-point atomics).
+ * Launches: 1, plus 1 fix-up launch when the plan has split rows.
+ */
+spx_status spx_spmv_csr(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                        const int32_t* col, const float* val, float alpha, const float* x, float beta, float* y,
+                        void* scratch, size_t scratch_bytes, spx_stream_t stream);
+
+/*
+ * The two-direction operator pair of a least-squares solver, with CSC(A)
+ * stored as CSR(A^T) so both directions are row sweeps ([LSMR-dual] §1, §4,
+ * §5.2):
+ *   u = alpha_u * A v   + beta_u * u     (A: m x n,  CSR(A))
+ *   v = alpha_v * A^T u + beta_v * v     (A^T: n x m, CSR(A^T)), reading the new u
+ * enqueued in that order on one stream.  The solver's step is alpha_u = 1,
+ * beta_u = -alpha_k and alpha_v = 1, beta_v = -beta_k.
+ *   plan_A / plan_At: uploaded plans of CSR(A) and CSR(A^T).
+ *   scratch: at least max(scratch_bytes of both plans).
+ */
+spx_status spx_spmv_csr_dual(const spx_plan* plan_A, const spx_plan* plan_At, int32_t m, int32_t n, int64_t nnz,
+                             const int32_t* A_row_ptr, const int32_t* A_col, const float* A_val,
+                             const int32_t* At_row_ptr, const int32_t* At_col, const float* At_val, float* v,
+                             float alpha_u, float beta_u, float* u, float alpha_v, float beta_v, void* scratch,
+                             size_t scratch_bytes, spx_stream_t stream);
+
+/* ------------------------------------------------------------ SpMM */
+
+/*
+ * C = alpha * A B + beta * C, A in CSR (M x K, fp32), B dense K x N
+ * row-major (leading dimension ldb >= N), C dense M x N row-major (ldc >= N),
+ * fp32 arithmetic.  [SpMM-ops] §3 (C_{i,n} = sum_{k in N(i)} A_{ik} B_{k,n};
+ * B's contiguous columns accumulated in registers) and §3.1-§3.3 (variant
+ * chosen by N):
+ *   N <= 8           lanes split the row's nonzeros, N accumulators each;
+ *   N % 4 == 0, <= 128  a sub-warp of pow2ceil(N/4) lanes per row, float4 B loads;
+ *   N % 4 == 0, > 128   (row, 128-column tile) per warp, tiles outermost;
+ *   otherwise        a warp per row, lanes over columns (scalar).
+ * The float4 variants need B, C 16-byte aligned and ldb, ldc multiples of 4;
+ * otherwise the scalar variant runs.  Launches: 1.
+ */
+spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                        const float* val, int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C,
+                        int64_t ldc, spx_stream_t stream);
+
+/* Which SpMM variant spx_spmm_csr would launch for these arguments:
+   0 = small-N, 1 = sub-warp float4, 2 = column-tiled float4, 3 = scalar. */
+int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);
+
+/*
+ * C = A B with A in BSR (br x bc blocks, row-major inside, bf16), B dense
+ * K x N bf16 row-major (ldb), C dense M x N fp32 row-major (ldc); products
+ * accumulated in fp32 on the tensor cores.  [SpMM-ops] §3.4 (loop over the
+ * nonzero blocks, each a small dense GEMM on the tensor cores) and
+ * [AsyncSparse] §2.2.1, §3 (BCSR SpMM: asynchronous copies of A blocks and
+ * B tiles into shared memory feeding the matrix units).
+ * Supported: br == bc == 64, M and K multiples of 64, N a multiple of 128,
+ * ldb and ldc multiples of 8 and 4, all pointers 16-byte aligned; other
+ * shapes return SPX_ERR_UNSUPPORTED.  Launches: 1.  Its pipeline waits are
+ * bounded: on expiry the kernel records an error that spx_last_device_error
+ * reports as SPX_ERR_TIMEOUT.
+ */
+spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
+                        const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
+                        float* C, int64_t ldc, spx_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error word
+ * that bounded waits set.  SPX_OK if none; SPX_ERR_TIMEOUT otherwise.
+ */
+spx_status spx_last_device_error(spx_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPX_H_ */

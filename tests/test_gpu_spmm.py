@@ -1,0 +1,88 @@
+"""CSR SpMM parity against the fp64 oracle: every variant (chosen by N),
+alpha/beta, leading dimensions, ragged tails, and the clustered 1M x 1M
+workload at N = 32 and N = 128 on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from csr_bsr_spmv_gb300 import spx
+from gpu_util import assert_within, csr_to_device, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run(M, K, d, N, alpha=1.0, beta=0.0, ldb=None, ldc=None, seed=0, want_variant=None):
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    ldb = ldb or N
+    ldc = ldc or N
+    Bfull = synth.uniform(seed, synth.T_B, K * ldb).reshape(K, ldb)
+    Cfull = synth.uniform(seed, synth.T_Y, M * ldc).reshape(M, ldc)
+    Bd = dev(Bfull)[:, :N]
+    Cd = dev(Cfull)
+    Cv = Cd[:, :N]
+    if want_variant:
+        assert spx.spx_spmm_csr_variant(Bd, Cv) == want_variant
+    spx.spx_spmm_csr(A, Bd, Cv, alpha, beta)
+    torch.cuda.synchronize()
+    got = Cd.cpu().numpy()
+    ref, bound = oracle.spmm(M, rp, col, val, Bfull[:, :N], alpha, beta, Cfull[:, :N])
+    assert_within(got[:, :N], ref, bound, what=f"N={N}")
+    assert np.array_equal(got[:, N:], Cfull[:, N:])  # columns beyond N untouched
+
+
+@pytest.mark.parametrize("N,variant", [(1, "small-N"), (2, "small-N"), (3, "small-N"), (8, "small-N"),
+                                       (12, "subwarp-float4"), (16, "subwarp-float4"), (32, "subwarp-float4"),
+                                       (64, "subwarp-float4"), (100, "subwarp-float4"), (128, "subwarp-float4"),
+                                       (132, "tiled-float4"), (256, "tiled-float4"), (520, "tiled-float4"),
+                                       (9, "scalar"), (33, "scalar"), (130, "scalar")])
+def test_variants(N, variant):
+    d = synth.random_coo(N, 1111, 777, 0, 50)
+    run(1111, 777, d, N, alpha=1.0, beta=0.0, want_variant=variant, seed=N)
+
+
+@pytest.mark.parametrize("alpha,beta", [(2.0, 0.0), (1.0, -0.5), (0.0, 1.5)])
+@pytest.mark.parametrize("N", [4, 32, 256])
+def test_alpha_beta(alpha, beta, N):
+    d = synth.random_coo(3, 500, 400, 0, 30)
+    run(500, 400, d, N, alpha, beta, seed=3)
+
+
+@pytest.mark.parametrize("N,ldb,ldc", [(32, 36, 40), (128, 132, 128), (20, 21, 20)])
+def test_leading_dimensions(N, ldb, ldc):
+    d = synth.random_coo(4, 300, 200, 0, 25)
+    run(300, 200, d, N, 1.0, 0.5, ldb=ldb, ldc=ldc, seed=4)
+
+
+def test_long_and_empty_rows():
+    L = np.zeros(70, np.int32)
+    L[3] = 5000
+    L[10:20] = 1
+    L[40] = 900
+    row, col = synth.cols_uniform(8, 6000, L)
+    d = dict(row=row, col=col, val=synth.uniform(8, synth.T_VAL, row.size))
+    for N in (2, 32, 160):
+        run(70, 6000, d, N, 1.0, 0.25, seed=8)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", [32, 128])
+def test_clustered_full_size_sampled(N):
+    """1,048,576^2, Poisson(32) rows in 4x4 clusters, B dense K x N: 4096
+    sampled rows (whole 4-row clusters) against the oracle."""
+    cfg = synth.clustered_spmm(N=N)
+    M, K = cfg["M"], cfg["K"]
+    rp, col, val = spx.spx_build_csr(M, K, cfg["row"], cfg["col"], cfg["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    Bd = dev(cfg["B"])
+    Cd = torch.full((M, N), float("nan"), device="cuda")
+    spx.spx_spmm_csr(A, Bd, Cd)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    g = rng.integers(0, M // 4, 1024)
+    rows = np.unique((g[:, None] * 4 + np.arange(4)).ravel()).astype(np.int32)
+    got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
+    ref, bound = oracle.spmm(M, rp, col, val, cfg["B"], rows=rows)
+    assert_within(got, ref, bound, what=f"clustered N={N}")

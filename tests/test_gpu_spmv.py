@@ -1,0 +1,139 @@
+"""CSR SpMV parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small matrices exercise every task kind (thread/lane groups, CTA rows, split
+rows and the fix-up), empty rows and ragged tails; the full-size workloads are
+checked on sampled rows plus every CTA/split row, in the same launch
+configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from csr_bsr_spmv_gb300 import spx
+from gpu_util import assert_within, csr_to_device, dev
+
+pytestmark = pytest.mark.gpu
+
+SMALL_OPTS = [
+    None,
+    dict(block_nnz=16, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=2),
+    dict(block_nnz=1024, block_rows=128, pack_max=64, cta_max=300, seg_nnz=256, lanes_div=1),
+    dict(block_nnz=4096, block_rows=1024, pack_max=4096, cta_max=4096, seg_nnz=1000, lanes_div=8),
+    dict(block_nnz=2000, block_rows=77, pack_max=33, cta_max=2000, seg_nnz=777, lanes_div=3),
+]
+
+
+def run_spmv(M, K, rp, col, val, x, y0, alpha, beta, opts=None):
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, int(rp[-1]), A.row_ptr, opts=opts)
+    xd, yd = dev(x), dev(y0)
+    spx.spx_spmv_csr(plan, A, xd, yd, alpha, beta)
+    torch.cuda.synchronize()
+    return yd.cpu().numpy(), plan
+
+
+def check(M, K, rp, col, val, x, y0, alpha, beta, opts=None, what=""):
+    got, plan = run_spmv(M, K, rp, col, val, x, y0, alpha, beta, opts)
+    ref, bound = oracle.spmv(M, rp, col, val, x, alpha, beta, y0)
+    assert_within(got, ref, bound, what=what)
+    return got, plan
+
+
+@pytest.mark.parametrize("opts", SMALL_OPTS)
+@pytest.mark.parametrize("seed", [1, 2])
+def test_power_law_small(opts, seed):
+    M = 3000
+    L, _ = synth.lengths_zipf(seed, M, 2.1, 20000, 10.0)
+    L[::13] = 0
+    row, col = synth.cols_uniform(seed, M * 8, L)
+    val = synth.uniform(seed, synth.T_VAL, row.size)
+    rp, col, val = oracle.build_csr(M, M * 8, row, col, val)
+    x = synth.uniform(seed, synth.T_X, M * 8)
+    y0 = synth.uniform(seed, synth.T_Y, M)
+    _, plan = check(M, M * 8, rp, col, val, x, y0, 1.0, 0.5, opts, what=f"opts={opts}")
+    assert plan.info["tasks"] > 0
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-2.5, 0.0), (1.0, 0.5), (0.0, 3.0), (0.75, -1.25)])
+def test_alpha_beta(alpha, beta):
+    d = synth.random_coo(4, 777, 555, 0, 70)
+    rp, col, val = oracle.build_csr(777, 555, d["row"], d["col"], d["val"])
+    x = synth.uniform(4, synth.T_X, 555)
+    y0 = synth.uniform(4, synth.T_Y, 777)
+    check(777, 555, rp, col, val, x, y0, alpha, beta)
+
+
+def test_beta_zero_does_not_read_y():
+    d = synth.random_coo(5, 513, 300, 0, 40)
+    rp, col, val = oracle.build_csr(513, 300, d["row"], d["col"], d["val"])
+    x = synth.uniform(5, synth.T_X, 300)
+    y0 = np.full(513, np.nan, np.float32)
+    got, _ = run_spmv(513, 300, rp, col, val, x, y0, 1.0, 0.0)
+    ref, bound = oracle.spmv(513, rp, col, val, x)
+    assert_within(got, ref, bound)
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 0), (1, 1, 1, 1), (5, 3, 0, 0), (257, 1, 0, 1),
+                                           (1, 100000, 100000, 100000), (33, 70000, 0, 70000)])
+def test_edge_shapes(M, K, lmin, lmax):
+    d = synth.random_coo(6, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    x = synth.uniform(6, synth.T_X, K)
+    y0 = synth.uniform(6, synth.T_Y, M)
+    check(M, K, rp, col, val, x, y0, 1.0, 0.5, what=f"{M}x{K}")
+
+
+@pytest.mark.parametrize("l", [0, 1, 4096, 4097, 8192, 8193, 65536, 200_000])
+def test_row_of_ones_closed_form(l):
+    """A row of l ones times x = 1 gives exactly l in fp32 (integers <= 2^24):
+    pins the segment split and the fix-up sum."""
+    rp = np.array([0, l], np.int32)
+    col = np.arange(l, dtype=np.int32)
+    K = max(l, 1)
+    got, _ = run_spmv(1, K, rp, col, np.ones(l, np.float32), np.ones(K, np.float32), np.zeros(1, np.float32), 1.0,
+                      0.0)
+    assert got[0] == l
+
+
+def test_deterministic_bitwise():
+    cfg = synth.power_law_rows(7, M=200_000, mean=16.0)
+    rp, col, val = oracle.build_csr(cfg["M"], cfg["K"], cfg["row"], cfg["col"], cfg["val"])
+    A = csr_to_device(cfg["M"], cfg["K"], rp, col, val)
+    plan = spx.spx_plan_csr(A.M, A.K, A.nnz, A.row_ptr)
+    assert plan.info["long_rows"] > 0
+    xd = dev(cfg["x"])
+    outs = []
+    for _ in range(3):
+        yd = dev(cfg["y"])
+        spx.spx_spmv_csr(plan, A, xd, yd, 1.0, 0.5)
+        outs.append(yd.cpu().numpy())
+    assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+
+
+def test_uniform_short_rows_full():
+    """4096 x 4096, lengths U{1..16}: every output row against the oracle."""
+    cfg = synth.uniform_short_rows()
+    rp, col, val = oracle.build_csr(cfg["M"], cfg["K"], cfg["row"], cfg["col"], cfg["val"])
+    check(cfg["M"], cfg["K"], rp, col, val, cfg["x"], cfg["y"], cfg["alpha"], cfg["beta"])
+
+
+@pytest.mark.slow
+def test_power_law_full_size_sampled():
+    """4,194,304^2 Zipf(2.1) rows (nnz ~ 67M), y = Ax + 0.5y, default plan as
+    the benchmark runs it; 20k sampled rows plus every CTA and split row."""
+    cfg = synth.power_law_rows()
+    M, K = cfg["M"], cfg["K"]
+    rp, col, val = spx.spx_build_csr(M, K, cfg["row"], cfg["col"], cfg["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr)
+    yd = dev(cfg["y"])
+    spx.spx_spmv_csr(plan, A, dev(cfg["x"]), yd, 1.0, 0.5)
+    got = yd.cpu().numpy()
+    tasks, longrows = plan.tasks()
+    heavy = np.concatenate([tasks[(tasks[:, 0] & 255) == 1, 1], longrows[:, 0]])
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 20000), heavy, [0, M - 1]])).astype(np.int32)
+    ref, bound = oracle.spmv(M, rp, col, val, cfg["x"], 1.0, 0.5, cfg["y"], rows=rows)
+    assert_within(got[rows], ref, bound, what="power-law full size")
+    assert plan.info["split_rows"] > 0 and plan.info["cta_rows"] > 0

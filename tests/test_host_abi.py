@@ -1,0 +1,200 @@
+"""Host-side logic of the C ABI (no GPU): the library loads and exports every
+symbol of include/spx.h; the host format builders, statistics and dispatch
+plan match the oracle bit-exactly; arguments are rejected with the documented
+status codes."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from csr_bsr_spmv_gb300 import spx
+
+
+def test_exports_every_header_symbol():
+    names = spx.header_symbols()
+    assert len(names) >= 19
+    lib = ctypes.CDLL(spx.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    lib = spx._lib()
+    for code, name in spx.STATUS.items():
+        assert lib.spx_status_string(code).decode().startswith(name)
+
+
+MATS = [(1, 1, 0, 1), (40, 30, 0, 12), (300, 7, 0, 7), (7, 300, 50, 120), (1000, 1000, 0, 40), (64, 64, 64, 64),
+        (3, 5, 0, 0)]
+
+
+def _mat(seed, M, K, lmin, lmax):
+    return synth.random_coo(seed, M, K, lmin, lmax)
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", MATS)
+def test_build_csr_matches_oracle(M, K, lmin, lmax):
+    d = _mat(3, M, K, lmin, lmax)
+    perm = synth.permutation(9, d["row"].size)
+    args = (d["row"][perm], d["col"][perm], d["val"][perm])
+    got = spx.spx_build_csr(M, K, *args)
+    want = oracle.build_csr(M, K, *args)
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+
+
+def test_build_csr_keeps_duplicates_in_input_order():
+    row = np.array([1, 0, 1, 1, 0], np.int32)
+    col = np.array([2, 0, 2, 0, 0], np.int32)
+    val = np.arange(5, dtype=np.float32)
+    got = spx.spx_build_csr(2, 3, row, col, val)
+    want = oracle.build_csr(2, 3, row, col, val)
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+
+
+@pytest.mark.parametrize("vdtype", [np.float32, np.uint16, np.float64])
+def test_build_csr_value_widths(vdtype):
+    d = _mat(4, 200, 90, 0, 20)
+    perm = synth.permutation(2, d["row"].size)
+    val = (np.arange(d["row"].size) * 7 % 65000).astype(vdtype)
+    got = spx.spx_build_csr(200, 90, d["row"][perm], d["col"][perm], val[perm])
+    want = oracle.build_csr(200, 90, d["row"][perm], d["col"][perm], val[perm])
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", MATS)
+def test_transpose_matches_oracle(M, K, lmin, lmax):
+    d = _mat(5, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    got = spx.spx_transpose_csr(M, K, rp, col, val)
+    want = oracle.transpose(M, K, rp, col, val)
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", MATS)
+@pytest.mark.parametrize("br,bc", [(1, 1), (2, 2), (4, 3), (64, 64)])
+def test_build_bsr_matches_oracle(M, K, lmin, lmax, br, bc):
+    d = _mat(6, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    g = spx.spx_build_bsr(M, K, rp, col, val, br, bc)
+    w = oracle.build_bsr(M, K, rp, col, val, br, bc)
+    for a, b in zip(g[:3], w[:3]):
+        assert np.array_equal(a, b)
+    assert g[3] == w[3]
+
+
+def test_build_bsr_duplicate_rejected():
+    rp = np.array([0, 2], np.int32)
+    with pytest.raises(spx.SpxError) as e:
+        spx.spx_build_bsr(1, 4, rp, np.array([1, 1], np.int32), np.ones(2, np.float32), 2, 2)
+    assert e.value.name == "SPX_ERR_DUPLICATE"
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_row_stats_bit_exact(seed):
+    L, _ = synth.lengths_zipf(seed, 5000 + 17 * seed, 2.1, 4000, 9.0)
+    L[:: 7 + seed] = 0
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    assert spx.spx_row_stats(L.size, rp) == oracle.row_stats(L.size, rp)
+
+
+PLAN_OPTS = [
+    None,
+    dict(block_nnz=16, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=2),
+    dict(block_nnz=1024, block_rows=256, pack_max=1024, cta_max=1024, seg_nnz=1024, lanes_div=1),
+    dict(block_nnz=4096, block_rows=512, pack_max=64, cta_max=20000, seg_nnz=3000, lanes_div=8),
+]
+
+
+@pytest.mark.parametrize("opts", PLAN_OPTS)
+@pytest.mark.parametrize("seed", range(3))
+def test_plan_matches_oracle(opts, seed):
+    L, _ = synth.lengths_zipf(seed, 20000, 2.1, 60000, 12.0)
+    L[::31] = 0
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    full = spx.spx_plan_opts_default()
+    full.update(opts or {})
+    p = spx.spx_plan_csr(L.size, 70000, int(rp[-1]), rp, opts=opts, upload=False)
+    tasks, longrows = p.tasks()
+    w = oracle.plan_spmv(L.size, rp, **full)
+    assert np.array_equal(tasks, w["tasks"]) and np.array_equal(longrows, w["longrows"])
+    for k, v in w["counts"].items():
+        assert p.info[k] == v, k
+    assert p.stats == oracle.row_stats(L.size, rp)
+    assert p.info["table_bytes"] == 16 * (tasks.shape[0] + longrows.shape[0])
+    assert p.info["scratch_bytes"] == 4 * w["counts"]["slots"]
+
+
+def test_plan_default_options_documented():
+    o = spx.spx_plan_opts_default()
+    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=4)
+
+
+def test_plan_rejects_bad_rows_and_options():
+    lib = spx._lib()
+    h = ctypes.c_void_p()
+    bad = np.array([0, 3, 2, 4], np.int32)  # not monotone
+    assert lib.spx_plan_csr(3, 5, 4, spx._ptr(bad), 0, None, ctypes.byref(h)) == -3
+    rp = np.array([0, 1, 2], np.int32)
+    assert lib.spx_plan_csr(2, 5, 3, spx._ptr(rp), 0, None, ctypes.byref(h)) == -1  # row_ptr[M] != nnz
+    o = spx.PlanOpts(block_nnz=16, block_rows=4, pack_max=32, cta_max=64, seg_nnz=8, lanes_div=1)  # P > B
+    assert lib.spx_plan_csr(2, 5, 2, spx._ptr(rp), 0, ctypes.byref(o), ctypes.byref(h)) == -1
+    assert lib.spx_plan_csr(2, 5, 2 ** 31, spx._ptr(rp), 0, None, ctypes.byref(h)) == -2  # int32 overflow
+
+
+def test_int32_overflow_rejected_not_truncated():
+    lib = spx._lib()
+    one = np.zeros(4, np.int32)
+    assert lib.spx_build_csr(4, 4, 2 ** 31, spx._ptr(one), spx._ptr(one), spx._ptr(one), 4, spx._ptr(one),
+                             spx._ptr(one), spx._ptr(one), 0, None) == -2
+    assert lib.spx_transpose_csr(4, 4, 2 ** 32 + 1, spx._ptr(one), spx._ptr(one), spx._ptr(one), 4,
+                                 spx._ptr(one), spx._ptr(one), spx._ptr(one), 0, None) == -2
+    assert lib.spx_spmm_csr(4, 4, 2 ** 31, spx._ptr(one), spx._ptr(one), spx._ptr(one), 1, spx._ptr(one), 1,
+                            1.0, 0.0, spx._ptr(one), 1, None) == -2
+
+
+def test_index_range_rejected():
+    with pytest.raises(spx.SpxError) as e:
+        spx.spx_build_csr(2, 2, np.array([0, 2], np.int32), np.array([0, 0], np.int32), np.ones(2, np.float32))
+    assert e.value.name == "SPX_ERR_INDEX_RANGE"
+    rp = np.array([0, 1, 2], np.int32)
+    with pytest.raises(spx.SpxError) as e:
+        spx.spx_transpose_csr(2, 2, rp, np.array([0, 5], np.int32), np.ones(2, np.float32))
+    assert e.value.name == "SPX_ERR_INDEX_RANGE"
+
+
+def test_check_csr():
+    rp = np.array([0, 2, 3], np.int32)
+    assert spx.spx_check_csr(2, 4, rp, np.array([0, 3, 1], np.int32)) == 0
+    assert spx.spx_check_csr(2, 4, rp, np.array([3, 0, 1], np.int32)) == -3
+    assert spx.spx_check_csr(2, 4, rp, np.array([3, 0, 1], np.int32), strict=False) == 0
+    assert spx.spx_check_csr(2, 4, rp, np.array([1, 1, 1], np.int32)) == -4
+    assert spx.spx_check_csr(2, 4, rp, np.array([0, 4, 1], np.int32)) == -2
+    assert spx.spx_check_csr(2, 4, np.array([0, 3, 2], np.int32), np.array([0, 1, 2], np.int32)) in (-1, -3)
+
+
+def test_compute_calls_reject_bad_plans_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    assert lib.spx_spmv_csr(None, 1, 1, 0, None, None, None, 1.0, None, 0.0, None, None, 0, None) == -1
+    rp = np.array([0, 1], np.int32)
+    p = spx.spx_plan_csr(1, 1, 1, rp, upload=False)
+    # a plan that was never uploaded
+    assert lib.spx_spmv_csr(p.handle, 1, 1, 1, None, None, None, 1.0, None, 0.0, None, None, 0, None) == -10
+    # sizes that do not match the plan
+    assert lib.spx_spmv_csr(p.handle, 2, 1, 1, None, None, None, 1.0, None, 0.0, None, None, 0, None) == -1
+    assert spx.launch_count() == before
+
+
+def test_spmm_variant_rule():
+    lib = spx._lib()
+    a16 = ctypes.c_void_p(1 << 20)
+    for N, want in [(1, 0), (8, 0), (12, 1), (32, 1), (128, 1), (132, 2), (1024, 2), (9, 3), (130, 3)]:
+        assert lib.spx_spmm_csr_variant(N, a16, N, a16, N) == want, N
+    assert lib.spx_spmm_csr_variant(32, ctypes.c_void_p((1 << 20) + 4), 32, a16, 32) == 3  # misaligned B
+    assert lib.spx_spmm_csr_variant(32, a16, 34, a16, 32) == 3  # ldb not a multiple of 4
