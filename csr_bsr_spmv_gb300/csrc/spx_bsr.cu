@@ -1,18 +1,351 @@
-// spx_bsr.cu -- BSR SpMM on the tensor cores (placeholder until the tcgen05 kernel lands).
+// spx_bsr.cu -- BSR SpMM C = A*B on the sm_103a tensor cores (tcgen05 + TMEM,
+// TMA-fed), bf16 inputs, fp32 accumulation.
+//
+// [SpMM-ops] §3.4: loop over the nonzero blocks of a block-row, each a small
+// dense GEMM on the matrix units, with asynchronous copies into shared memory
+// and a multi-stage pipeline.  [AsyncSparse] §3 gives a Hopper design
+// (warp-specialised TMA producer, WGMMA consumers, full/empty mbarrier ring);
+// this kernel keeps the ring and the producer/consumer split and maps them to
+// Blackwell: one elected thread issues tcgen05.mma into a TMEM accumulator and
+// tcgen05.commit frees each stage, so no warpgroup holds accumulators in
+// registers.  Non-persistent grid (one CTA per (n-tile, block-row)), as
+// [AsyncSparse] §5.2 settles on for sparse work.
+//
+// Tile: a 64-row block-row and 128 output columns.  The MMA computes the
+// transposed tile  D[n, r] += B[J*64 + k, n0 + n] * Ablk[r, k]  with
+// M = 128 (n), N = 64 (r), K = 16: B's tile is the A operand in MN-major form
+// (n contiguous, exactly as B is stored) and the A block is the B operand in
+// K-major form (k contiguous, as BSR stores a row-major block).  Both arrive
+// by 2-D TMA with the 128-byte swizzle.  The accumulator D (128 lanes x 64
+// fp32 columns) is read back with tcgen05.ld: lane n holds C[I*64 + r, n0 + n]
+// for r = 0..63, so each warp stores 128 contiguous bytes per r.
+//
+// Every mbarrier wait is bounded (clock64); on expiry the CTA records an error
+// word (read by spx_last_device_error), stops issuing, waits (bounded) for
+// its copies in flight, frees its TMEM and exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "spx_internal.h"
 
+namespace {
+
+constexpr int kBlk = 64;                  // BSR block edge (rows = cols)
+constexpr int kTileN = 128;               // output columns per CTA = MMA M
+constexpr int kStages = 4;                // smem ring depth
+constexpr int kThreads = 128;             // 4 warps: producer, MMA issuer, all four in the epilogue
+constexpr uint32_t kABytes = kBlk * kBlk * 2;          // one bf16 A block, 8 KB
+constexpr uint32_t kBHalf = kBlk * 64 * 2;             // 64 k-rows x 64 n, 8 KB (one TMA box)
+constexpr uint32_t kStageBytes = kABytes + 2 * kBHalf; // 24 KB
+constexpr uint32_t kTmemCols = 64;
+constexpr size_t kSmemBytes = kStages * kStageBytes + 256 + 1024;
+// kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits 7, 10),
+// A MN-major (bit 15), B K-major (bit 16 = 0), N = 64 (bits 17-22, N>>3),
+// M = 128 (bits 24-28, M>>4).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s): only a broken pipeline reaches it
+
+enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
+
+__device__ int g_bsr_error;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false when the limit expired.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout: start
+// address, leading/stride byte offsets in 16-byte units, version 1 at bit 46,
+// swizzle mode 2 at bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_bsr_error, 0, code); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bsr_spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
+                       long long ldc, long long spin_limit) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ int s_issued, s_consumed;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB alignment for the 128-byte swizzle atoms
+    const uint32_t bars = base + kStages * kStageBytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    const uint32_t acc_bar = bars + 16u * kStages;
+    auto stage_a = [&](int s) { return base + s * kStageBytes; };
+    auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN;
+    const int I = blockIdx.y;
+    const int b0 = __ldg(brp + I);
+    const int nblk = __ldg(brp + I + 1) - b0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        s_abort = 0;
+        s_issued = 0;
+        s_consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = s_tmem;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- producer: one TMA thread feeds the ring
+        int b = 0;
+        for (; b < nblk; ++b) {
+            const int s = b % kStages;
+            const uint32_t ph = (b / kStages) & 1u;
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, spin_limit)) {
+                record_error(kErrEmpty);
+                s_abort = 1;
+                break;
+            }
+            if (s_abort) break;
+            mbar_expect_tx(full_bar(s), kStageBytes);
+            const int J = __ldg(bcol + b0 + b);
+            tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
+            tma_load_2d(stage_b(s), &tmB, n0, J * kBlk, full_bar(s));
+            tma_load_2d(stage_b(s) + kBHalf, &tmB, n0 + 64, J * kBlk, full_bar(s));
+        }
+        s_issued = b;
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        int b = 0;
+        for (; b < nblk; ++b) {
+            const int s = b % kStages;
+            const uint32_t ph = (b / kStages) & 1u;
+            if (!mbar_wait(full_bar(s), ph, spin_limit)) {
+                record_error(kErrFull);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < kBlk / 16; ++ks) {
+                // A operand: B's tile, MN-major; 16 k-rows = two 8-row swizzle atoms (SBO 1 KB);
+                // the two 64-column halves are the two TMA boxes (LBO 8 KB).
+                const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBHalf, 1024u);
+                // B operand: the A block, K-major; 16 k = 32 bytes inside each 128-byte row.
+                const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
+                mma_bf16(tmem_d, adesc, bdesc, (b > 0 || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(empty_bar(s));
+        }
+        s_consumed = b;
+        if (b > 0) mma_commit(acc_bar);  // arrives once every issued MMA has completed
+        else mbar_arrive(acc_bar);
+    }
+    __syncwarp();
+
+    // ---------------- epilogue: TMEM -> registers -> C (each warp its 32 lanes)
+    const bool acc_ok = mbar_wait(acc_bar, 0, spin_limit);
+    if (!acc_ok) record_error(kErrAcc);
+    tc_fence_after();
+    const int n = 32 * warp + lane;
+    float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + n;
+    if (nblk == 0) {
+        for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, 0.f);
+    } else if (acc_ok && !s_abort) {
+#pragma unroll
+        for (int c0 = 0; c0 < kBlk; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) __stcs(cp + static_cast<long long>(c0 + j) * ldc, __uint_as_float(v[j]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        // copies issued but never consumed: wait (bounded) until they have landed
+        for (int b = s_consumed; b < s_issued; ++b)
+            if (!mbar_wait(full_bar(b % kStages), (b / kStages) & 1u, spin_limit)) {
+                record_error(kErrDrain);
+                break;
+            }
+    }
+    __syncthreads();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols) : "memory");
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: inner extent `inner`, `outer` rows, row pitch in bytes,
+// 64 x 64 box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 extern "C" {
 
-spx_status spx_spmm_bsr(int32_t, int32_t, int32_t, int32_t, int64_t, const int32_t*, const int32_t*, const uint16_t*,
-                        int32_t, const uint16_t*, int64_t, float*, int64_t, spx_stream_t) {
-    return SPX_ERR_UNSUPPORTED;
+spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
+                        const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
+                        float* C, int64_t ldc, spx_stream_t stream) {
+    if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
+    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % kTileN) return SPX_ERR_UNSUPPORTED;
+    if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!bsr_row_ptr || !C || (nnzb > 0 && (!bsr_col || !bsr_val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (ldb % 8 || !spx_aligned(bsr_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
+        !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4))
+        return SPX_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (nnzb == 0) {
+        // no stored block: C = 0
+        return spx_cuda_status(cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0, static_cast<size_t>(N) * 4,
+                                                 static_cast<size_t>(M), st));
+    }
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
+        !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
+        return SPX_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(bsr_spmm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemBytes));
+    });
+    if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
+    dim3 grid(N / kTileN, M / kBlk);
+    bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, kSpinLimit);
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
 }
 
 spx_status spx_last_device_error(spx_stream_t stream) {
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SPX_OK : SPX_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int h = 0;
+    const int zero = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&h, g_bsr_error, sizeof(int));
+    if (e == cudaSuccess && h != 0) e = cudaMemcpyToSymbol(g_bsr_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    return h ? SPX_ERR_TIMEOUT : SPX_OK;
 }
 
 }  // extern "C"

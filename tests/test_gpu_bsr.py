@@ -1,0 +1,149 @@
+"""BSR SpMM on the tensor cores (bf16 in, fp32 accumulate) against the fp64
+oracle: exact small-integer cases, identity blocks, empty and long block-rows
+(ring wrap-around), several column tiles, padded leading dimensions, and the
+16384^2 64x64-block workload at N = 1024 on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from csr_bsr_spmv_gb300 import spx
+from gpu_util import BF16_ABS, BF16_REL, assert_within
+
+pytestmark = pytest.mark.gpu
+
+
+def bits_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def run_bsr(M, K, brp, bcol, bval_bits, B_bits, N, ldb=None, ldc=None):
+    ldb = ldb or N
+    ldc = ldc or N
+    Bfull = np.zeros((K, ldb), np.uint16)
+    Bfull[:, :N] = B_bits
+    Bd = bits_dev(Bfull)[:, :N]
+    Cd = torch.full((M, ldc), -7.0, device="cuda")
+    spx.spx_spmm_bsr(M, K, 64, 64, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(bval_bits.reshape(-1)), Bd, Cd[:, :N])
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    out = Cd.cpu().numpy()
+    assert np.all(out[:, N:] == -7.0)
+    return out[:, :N]
+
+
+def pattern(seed, MB, KB, counts):
+    """Block pattern with the given number of blocks per block-row."""
+    cols = []
+    for I, c in enumerate(counts):
+        cols.append(np.sort(synth.permutation(seed * 1000 + I, KB)[:c]).astype(np.int32))
+    brp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return brp, np.concatenate(cols).astype(np.int32) if cols else np.zeros(0, np.int32)
+
+
+def test_small_integers_exact():
+    """Entries and B in {-3..3}: every product and partial sum is an exact
+    integer in fp32, so the result equals the dense product exactly."""
+    MB, KB, N = 4, 8, 128
+    brp, bcol = pattern(1, MB, KB, [3, 0, 8, 1])
+    nb = bcol.size
+    A = np.floor(synth.uniform(1, synth.T_VAL, nb * 4096, -3, 4)).astype(np.float32).reshape(nb, 64, 64)
+    B = np.floor(synth.uniform(1, synth.T_B, KB * 64 * N, -3, 4)).astype(np.float32).reshape(KB * 64, N)
+    got = run_bsr(MB * 64, KB * 64, brp, bcol, synth.to_bf16_bits(A), synth.to_bf16_bits(B).reshape(B.shape), N)
+    dense = np.zeros((MB * 64, KB * 64))
+    for I in range(MB):
+        for b in range(brp[I], brp[I + 1]):
+            dense[I * 64:(I + 1) * 64, bcol[b] * 64:(bcol[b] + 1) * 64] = A[b]
+    assert np.array_equal(got, dense @ B.astype(np.float64))
+
+
+def test_identity_blocks():
+    """Block-diagonal identity: C = B exactly (checks the MN-major / K-major
+    operand layouts and the TMEM lane -> output mapping)."""
+    MB, N = 6, 256
+    brp = np.arange(MB + 1, dtype=np.int32)
+    bcol = np.arange(MB, dtype=np.int32)
+    eye = np.tile(np.eye(64, dtype=np.float32), (MB, 1, 1))
+    B = synth.uniform(2, synth.T_B, MB * 64 * N).reshape(MB * 64, N)
+    Bb = synth.to_bf16_bits(B).reshape(B.shape)
+    got = run_bsr(MB * 64, MB * 64, brp, bcol, synth.to_bf16_bits(eye), Bb, N)
+    assert np.array_equal(got, synth.bf16_bits_to_f32(Bb))
+
+
+def test_permutation_blocks():
+    """One permutation block per block-row (shifted block columns): rows of B
+    land permuted, exactly."""
+    MB, KB, N = 3, 5, 128
+    perm = synth.permutation(3, 64)
+    P = np.eye(64, dtype=np.float32)[perm]
+    brp = np.arange(MB + 1, dtype=np.int32)
+    bcol = np.array([4, 0, 2], np.int32)
+    B = synth.uniform(3, synth.T_B, KB * 64 * N).reshape(KB * 64, N)
+    Bb = synth.to_bf16_bits(B).reshape(B.shape)
+    got = run_bsr(MB * 64, KB * 64, brp, bcol, synth.to_bf16_bits(np.stack([P] * MB)), Bb, N)
+    Bf = synth.bf16_bits_to_f32(Bb).reshape(B.shape)
+    for I in range(MB):
+        assert np.array_equal(got[I * 64:(I + 1) * 64], Bf[bcol[I] * 64:(bcol[I] + 1) * 64][perm])
+
+
+@pytest.mark.parametrize("counts,N,ldb,ldc", [
+    ([1, 2, 3, 4], 128, None, None),
+    ([0, 5, 0, 9, 17], 256, None, None),        # empty block-rows, ring wrap-around
+    ([33, 1], 384, 512, 400),                    # padded leading dimensions
+    ([7] * 12, 640, None, None),
+])
+def test_random_blocks(counts, N, ldb, ldc):
+    MB, KB = len(counts), 40
+    brp, bcol = pattern(4, MB, KB, counts)
+    nb = bcol.size
+    A = synth.normal_bf16(4, synth.T_VAL, nb * 4096, 0.02).reshape(nb, 64, 64)
+    B = synth.normal_bf16(4, synth.T_B, KB * 64 * N, 1.0).reshape(KB * 64, N)
+    got = run_bsr(MB * 64, KB * 64, brp, bcol, A, B, N, ldb, ldc)
+    ref, bound = oracle.bsr_spmm(MB * 64, KB * 64, 64, 64, brp, bcol, A, B)
+    assert_within(got, ref, bound, BF16_REL, BF16_ABS, what=f"counts={counts}")
+    # fp32 accumulation is in fact far tighter than the bf16 bound
+    assert_within(got, ref, bound, 1e-5, 1e-6, what="fp32-level")
+
+
+def test_unsupported_shapes_rejected_without_launch():
+    lib = spx._lib()
+    before = spx.launch_count()
+    z = torch.zeros(64 * 1024, dtype=torch.int32, device="cuda")
+    p = spx._ptr(z)
+    assert lib.spx_spmm_bsr(64, 64, 32, 32, 1, p, p, p, 128, p, 128, p, 128, None) == -7   # block size
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 100, p, 128, p, 128, None) == -7   # N % 128
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, p, 128, None) == -8   # ldb % 8
+    assert spx.launch_count() == before
+
+
+def test_no_blocks_gives_zero():
+    M, K, N = 128, 128, 128
+    brp = np.zeros(3, np.int32)
+    got = run_bsr(M, K, brp, np.zeros(0, np.int32), np.zeros((0, 64, 64), np.uint16),
+                  np.ones((K, N), np.uint16), N)
+    assert not got.any()
+
+
+@pytest.mark.slow
+def test_block_sparse_full_size_sampled():
+    """16384^2 with 64x64 blocks, 26 per block-row (nnzb = 6656), B 16384 x 1024:
+    two sampled rows of every block-row, built through the library's
+    COO -> CSR -> BSR path."""
+    cfg = synth.block_sparse()
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    rp, col, val = spx.spx_build_csr(M, K, cfg["row"], cfg["col"], cfg["val_bf16"])
+    brp, bcol, bval, fill = spx.spx_build_bsr(M, K, rp, col, val, 64, 64)
+    assert bcol.size == 6656 and fill == 1.0
+    Cd = torch.empty(M, N, device="cuda")
+    spx.spx_spmm_bsr(M, K, 64, 64, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(bval.reshape(-1)), bits_dev(cfg["B_bf16"]), Cd)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    rng = np.random.default_rng(5)
+    rows = np.sort(np.concatenate([np.arange(0, M, 64) + rng.integers(0, 64, M // 64),
+                                   np.arange(0, M, 64) + 63])).astype(np.int32)
+    got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
+    ref, bound = oracle.bsr_spmm(M, K, 64, 64, brp, bcol, bval, cfg["B_bf16"], rows=rows)
+    assert_within(got, ref, bound, BF16_REL, BF16_ABS, what="block-sparse full size")
