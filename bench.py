@@ -199,7 +199,7 @@ def run_ours(args, rank, world):
     if w in ("power-law", "uniform"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         t0 = time.perf_counter()
-        plan = spx.spx_plan_csr(M, K, A.nnz, rp, device=dev, stream=stream)
+        plan = spx.spx_plan_csr(M, K, A.nnz, rp, opts=args.plan_opts, device=dev, stream=stream)
         timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         x = to_dev(c["x"])
         y = to_dev(c["y"])
@@ -226,7 +226,8 @@ def run_ours(args, rank, world):
 
         info = dict(plan.info)
         extra = {"plan": {k: info[k] for k in ("tasks", "long_rows", "cta_rows", "split_rows", "thread_groups",
-                                                "lane_groups")}, "row_stats": plan.stats}
+                                                "lane_groups", "segmented_groups")},
+                 "plan_opts": args.plan_opts or "default", "row_stats": plan.stats}
     elif w == "dual":
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         t0 = time.perf_counter()
@@ -234,8 +235,8 @@ def run_ours(args, rank, world):
         timings["transpose_ms"] = 1e3 * (time.perf_counter() - t0)
         At = spx.Csr(K, M, to_dev(trp), to_dev(tc), to_dev(tv))
         t0 = time.perf_counter()
-        pA = spx.spx_plan_csr(M, K, A.nnz, rp, device=dev, stream=stream)
-        pAt = spx.spx_plan_csr(K, M, A.nnz, trp, device=dev, stream=stream)
+        pA = spx.spx_plan_csr(M, K, A.nnz, rp, opts=args.plan_opts, device=dev, stream=stream)
+        pAt = spx.spx_plan_csr(K, M, A.nnz, trp, opts=args.plan_opts, device=dev, stream=stream)
         timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         u = to_dev(c["u0"])
         v = to_dev(c["v0"])
@@ -275,7 +276,7 @@ def run_ours(args, rank, world):
         src = source_hash("spx_spmm.cu")
 
         def run():
-            spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream)
+            spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream, col_tile=args.col_tile)
 
         Bh = torch.from_numpy(c["B"]).pin_memory()
         Co = torch.empty(M, c["N"]).pin_memory()
@@ -284,7 +285,7 @@ def run_ours(args, rank, world):
         def e2e_run():
             with torch.cuda.stream(stream):
                 B.copy_(Bh, non_blocking=True)
-                spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream)
+                spx.spx_spmm_csr(A, B, C, 1.0, 0.0, stream=stream, col_tile=args.col_tile)
                 Co.copy_(C, non_blocking=True)
 
         extra = {"variant": spx.spx_spmm_csr_variant(B, C)}
@@ -491,7 +492,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--rows", type=int, default=0, help="smaller power-law matrix (profiling only)")
+    ap.add_argument("--plan", default="", help="plan options, e.g. block_nnz=4096,lanes_div=4")
+    ap.add_argument("--col-tile", type=int, default=None, help="SpMM column tile (default: automatic)")
     args = ap.parse_args()
+    args.plan_opts = {k: int(v) for k, v in (kv.split("=") for kv in args.plan.split(",") if kv)} or None
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -186,31 +186,41 @@ void row_stats_host(int32_t M, const int32_t* rp, spx_row_stats_t* out) {
 }
 
 // ------------------------------------------------------------ the plan
-int32_t lanes_for(int64_t nnz_g, int64_t rows_g, int32_t div) {
+int32_t reduce_code(int64_t nnz_g, int64_t rows_g, int32_t div) {
+    if (div == 0) return kReduceSegmented;
     int64_t per = (nnz_g + rows_g * div - 1) / (rows_g * div);
     int32_t lg = 0;
     while (lg < 5 && (int64_t{1} << lg) < per) ++lg;
-    return lg;  // log2 of the lane count
+    return lg;  // log2 of the lanes per row
 }
 
 spx_status make_plan(spx_plan* P, const int32_t* rp) {
     const spx_plan_opts_t& o = P->opts;
     const int32_t M = P->M;
-    std::vector<int32_t> groups;
-    int64_t slot = 0, ncta = 0, nsplit = 0, npacked = 0, g1 = 0, gw = 0;
+    std::vector<int32_t> groups, dgroups;
+    int64_t slot = 0, ncta = 0, nsplit = 0, npacked = 0, g1 = 0, gw = 0, gs = 0;
+    int32_t d[4];
+    auto push = [](std::vector<int32_t>& v, const int32_t* q) { v.insert(v.end(), q, q + 4); };
     int32_t i = 0;
     while (i < M) {
         int64_t l = static_cast<int64_t>(rp[i + 1]) - rp[i];
         if (l > o.pack_max) {
             if (l <= o.cta_max) {
                 P->tasks.insert(P->tasks.end(), {kTaskCta, i, 0, 0});
+                spx_dev_task(d, kTaskCta, 0, 0, i, rp[i], rp[i + 1]);
+                push(P->dtasks, d);
                 ++ncta;
             } else {
                 int64_t ns = (l + o.seg_nnz - 1) / o.seg_nnz;
-                if (slot + ns > kI32Max) return SPX_ERR_INDEX_RANGE;
+                if (slot + ns > (int64_t{1} << 23)) return SPX_ERR_INDEX_RANGE;  // slot must fit the task word
                 P->longrows.insert(P->longrows.end(), {i, static_cast<int32_t>(slot), static_cast<int32_t>(ns), 0});
-                for (int64_t s = 0; s < ns; ++s)
-                    P->tasks.insert(P->tasks.end(), {kTaskSeg, i, static_cast<int32_t>(s), static_cast<int32_t>(slot + s)});
+                for (int64_t sg = 0; sg < ns; ++sg) {
+                    P->tasks.insert(P->tasks.end(), {kTaskSeg, i, static_cast<int32_t>(sg), static_cast<int32_t>(slot + sg)});
+                    int64_t lo = rp[i] + sg * o.seg_nnz, hi = std::min<int64_t>(rp[i + 1], lo + o.seg_nnz);
+                    spx_dev_task(d, kTaskSeg, 0, static_cast<int32_t>(slot + sg), i, static_cast<int32_t>(lo),
+                                 static_cast<int32_t>(hi));
+                    push(P->dtasks, d);
+                }
                 slot += ns;
                 ++nsplit;
             }
@@ -226,17 +236,20 @@ spx_status make_plan(spx_plan* P, const int32_t* rp) {
             g += li;
             ++i;
         }
-        int32_t lg = lanes_for(g, i - r0, o.lanes_div);
-        groups.insert(groups.end(), {kTaskGroup + 256 * lg, r0, i, 0});
+        const int32_t c = reduce_code(g, i - r0, o.lanes_div);
+        groups.insert(groups.end(), {kTaskGroup + 256 * c, r0, i, 0});
+        spx_dev_task(d, kTaskGroup, c, i - r0, r0, rp[r0], rp[i]);
+        push(dgroups, d);
         npacked += i - r0;
-        (lg == 0 ? g1 : gw) += 1;
+        (c == 0 ? g1 : c == kReduceSegmented ? gs : gw) += 1;
     }
     P->tasks.insert(P->tasks.end(), groups.begin(), groups.end());
+    P->dtasks.insert(P->dtasks.end(), dgroups.begin(), dgroups.end());
     const int64_t nt = static_cast<int64_t>(P->tasks.size() / 4);
     if (nt > kI32Max) return SPX_ERR_INDEX_RANGE;
-    int64_t c[8] = {nt, static_cast<int64_t>(P->longrows.size() / 4), slot, npacked, ncta, nsplit, g1, gw};
+    int64_t c[9] = {nt, static_cast<int64_t>(P->longrows.size() / 4), slot, npacked, ncta, nsplit, g1, gw, gs};
     std::memcpy(P->counts, c, sizeof(c));
-    P->table_bytes = (P->tasks.size() + P->longrows.size()) * sizeof(int32_t);
+    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t);
     P->scratch_bytes = static_cast<size_t>(slot) * sizeof(float);
     return SPX_OK;
 }
@@ -408,7 +421,7 @@ spx_status spx_plan_opts_default(spx_plan_opts_t* o) {
     o->pack_max = 512;
     o->cta_max = 8192;
     o->seg_nnz = 4096;
-    o->lanes_div = 4;
+    o->lanes_div = 0;
     return SPX_OK;
 }
 
@@ -421,7 +434,7 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     spx_plan_opts_t o;
     if (opts) o = *opts; else spx_plan_opts_default(&o);
     if (o.block_nnz < 1 || o.block_rows < 1 || o.pack_max < 0 || o.pack_max > o.block_nnz || o.cta_max < o.pack_max ||
-        o.seg_nnz < 1 || o.lanes_div < 1 || o.block_nnz > 8192 || o.block_rows > 1024)
+        o.seg_nnz < 1 || o.lanes_div < 0 || o.block_nnz > 8192 || o.block_rows > 1024)
         return SPX_ERR_ARG;
     std::vector<int32_t> rp_h;
     const int32_t* rp = row_ptr;
@@ -468,6 +481,7 @@ spx_status spx_plan_get_info(const spx_plan* P, spx_plan_info_t* out) {
     out->split_rows = P->counts[5];
     out->thread_groups = P->counts[6];
     out->lane_groups = P->counts[7];
+    out->segmented_groups = P->counts[8];
     out->table_bytes = P->table_bytes;
     out->scratch_bytes = P->scratch_bytes;
     out->stats = P->stats;
@@ -491,9 +505,9 @@ spx_status spx_plan_upload(spx_plan* P, void* table, size_t table_bytes, spx_str
     if (!spx_aligned(table, 16)) return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* dst = static_cast<char*>(table);
-    const size_t tb = P->tasks.size() * sizeof(int32_t);
+    const size_t tb = P->dtasks.size() * sizeof(int32_t);
     cudaError_t e = cudaSuccess;
-    if (tb) e = cudaMemcpyAsync(dst, P->tasks.data(), tb, cudaMemcpyHostToDevice, st);
+    if (tb) e = cudaMemcpyAsync(dst, P->dtasks.data(), tb, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && !P->longrows.empty())
         e = cudaMemcpyAsync(dst + tb, P->longrows.data(), P->longrows.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                             st);

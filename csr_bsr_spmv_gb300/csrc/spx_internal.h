@@ -17,9 +17,10 @@ struct spx_plan {
     int32_t M = 0, K = 0;
     int64_t nnz = 0;
     spx_plan_opts_t opts{};
-    std::vector<int32_t> tasks;     // 4 per task
+    std::vector<int32_t> tasks;     // 4 per task, the documented (host) form
+    std::vector<int32_t> dtasks;    // 4 per task, the device form (see spx_spmv.cu)
     std::vector<int32_t> longrows;  // 4 per split row
-    int64_t counts[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int64_t counts[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     spx_row_stats_t stats{};
     const void* d_table = nullptr;  // caller-owned copy of tasks + longrows
     size_t table_bytes = 0;
@@ -30,6 +31,17 @@ struct spx_plan {
 constexpr uint64_t kPlanMagic = 0x5350585f504c414eull;  // "SPX_PLAN"
 
 enum : int32_t { kTaskGroup = 0, kTaskCta = 1, kTaskSeg = 2 };
+constexpr int32_t kReduceSegmented = 6;  // group reduction code of the segmented reduction
+
+// Device task (int4): x = kind | code << 2 | aux << 8 where aux = #rows for a
+// group and the partial-sum slot for a segment; y = first row; z, w = the
+// nonzero range [p0, p1) the task covers.
+inline void spx_dev_task(int32_t* d, int32_t kind, int32_t code, int32_t aux, int32_t row, int32_t p0, int32_t p1) {
+    d[0] = kind | (code << 2) | (aux << 8);
+    d[1] = row;
+    d[2] = p0;
+    d[3] = p1;
+}
 
 inline bool spx_plan_ok(const spx_plan* p) { return p && p->magic == kPlanMagic; }
 

@@ -4,13 +4,14 @@
 // The variant is chosen by N ([SpMM-ops] §3.1-§3.3):
 //   small   N <= 8     : lanes split the row's nonzeros, N accumulators per lane,
 //                        warp-shuffle reduction of each column;
-//   subwarp N%4 == 0, N <= 128: a sub-warp of L = pow2ceil(N/4) lanes per row,
-//                        each lane owns 4 adjacent columns (float4 loads of B);
-//                        32/L rows per warp, so a 4-row cluster shares one warp
-//                        and its B rows hit in L1;
-//   tiled   N%4 == 0, N > 128: a warp owns (row, 128-column tile); the tile
-//                        index is the outer grid dimension so one B column
-//                        slice stays L2-resident while all rows pass over it;
+//   float4  N%4 == 0 : columns are cut into tiles of T = pow2ceil(N) up to 128
+//                        (or the caller's choice, 8..128); a sub-warp of
+//                        L = T/4 lanes owns (row, tile), each lane 4 adjacent
+//                        columns (float4 loads of B); 32/L rows per warp, so a
+//                        4-row cluster shares one warp and its B rows hit in
+//                        L1.  The tile index is the outer grid dimension, B
+//                        loads carry an L2 evict-last hint and A / C stream
+//                        through with evict-first hints;
 //   scalar  otherwise  : a warp per row, lanes over columns.
 #include <cuda_runtime.h>
 
@@ -23,6 +24,20 @@ constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
+
+// B rows are the reused operand: keep them in L2 ahead of the streamed A and C.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ float4 ld_keep(const float* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
 
 // ------------------------------------------------------------- small N
 template <int N>
@@ -74,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
     const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
     if (row >= M) return;
     const bool live = n0 < N;
+    const uint64_t pol = l2_evict_last_policy();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
     const float* Bc = B + n0;
@@ -84,10 +100,10 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
         const float v0 = ld_stream(val + p), v1 = ld_stream(val + p + 1), v2 = ld_stream(val + p + 2),
                     v3 = ld_stream(val + p + 3);
         if (live) {
-            const float4 b0 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c0 * ldb));
-            const float4 b1 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c1 * ldb));
-            const float4 b2 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c2 * ldb));
-            const float4 b3 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c3 * ldb));
+            const float4 b0 = ld_keep(Bc + (long long)c0 * ldb, pol);
+            const float4 b1 = ld_keep(Bc + (long long)c1 * ldb, pol);
+            const float4 b2 = ld_keep(Bc + (long long)c2 * ldb, pol);
+            const float4 b3 = ld_keep(Bc + (long long)c3 * ldb, pol);
             acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
             acc.x += v1 * b1.x; acc.y += v1 * b1.y; acc.z += v1 * b1.z; acc.w += v1 * b1.w;
             acc.x += v2 * b2.x; acc.y += v2 * b2.y; acc.z += v2 * b2.z; acc.w += v2 * b2.w;
@@ -98,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
         const int c0 = ld_stream(col + p);
         const float v0 = ld_stream(val + p);
         if (live) {
-            const float4 b0 = __ldg(reinterpret_cast<const float4*>(Bc + (long long)c0 * ldb));
+            const float4 b0 = ld_keep(Bc + (long long)c0 * ldb, pol);
             acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
         }
     }
@@ -109,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
         const float4 o = *cp;
         r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
     }
-    *cp = r;
+    __stcs(cp, r);  // C is written once: evict-first
 }
 
 // ------------------------------------------------------------- scalar fallback
@@ -139,12 +155,59 @@ int pick_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t
     return N <= 128 ? 1 : 2;
 }
 
+// Column tile of the float4 variants: the whole of N up to 128 columns (a
+// sub-warp of N/4 lanes per row), tiles of 128 beyond.  Narrower tiles that
+// keep a B slice L2-resident were measured slower on GB300 (the matrix is
+// re-streamed once per tile), so they are only taken on request.
+int auto_col_tile(int32_t N) {
+    int t = 8;
+    while (t < N && t < 128) t <<= 1;
+    return t;
+}
+
 template <int L>
 void launch_vec(int M, int N, const int* rp, const int* col, const float* val, const float* B, long long ldb,
-                float alpha, float beta, float* C, long long ldc, int tiles, cudaStream_t st) {
+                float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
     constexpr int rows_per_cta = kWarps * (32 / L);
-    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, tiles);
+    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
     spmm_vec_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+}
+
+spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
+                     int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                     int32_t col_tile, cudaStream_t st) {
+    if (M < 0 || K < 0 || nnz < 0 || N < 0 || col_tile < 0) return SPX_ERR_ARG;
+    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (col_tile && (col_tile < 8 || col_tile > 128 || (col_tile & (col_tile - 1)))) return SPX_ERR_ARG;
+    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 4) || !spx_aligned(B, 4) ||
+        !spx_aligned(C, 4))
+        return SPX_ERR_ALIGN;
+    const int v = pick_variant(N, B, ldb, C, ldc);
+    if (v == 0) {
+        const int grid = (M + kWarps - 1) / kWarps;
+        switch (N) {
+#define SPX_SMALL(n) case n: spmm_small_kernel<n><<<grid, kThreads, 0, st>>>(M, rp, col, val, B, ldb, alpha, beta, C, ldc); break;
+            SPX_SMALL(1) SPX_SMALL(2) SPX_SMALL(3) SPX_SMALL(4) SPX_SMALL(5) SPX_SMALL(6) SPX_SMALL(7) SPX_SMALL(8)
+#undef SPX_SMALL
+        }
+    } else if (v == 3) {
+        dim3 grid((M + kWarps - 1) / kWarps, (N + 31) / 32 < 4 ? (N + 31) / 32 : 4);
+        spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+    } else {
+        const int t = col_tile ? col_tile : auto_col_tile(N);
+        switch (t) {
+            case 8: launch_vec<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+            case 16: launch_vec<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+            case 32: launch_vec<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+            case 64: launch_vec<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+            default: launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        }
+    }
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
 }
 
 }  // namespace
@@ -158,38 +221,14 @@ int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float
 spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
                         int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
                         spx_stream_t stream) {
-    if (M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
-    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (M == 0 || N == 0) return SPX_OK;
-    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
-    if (ldb < N || ldc < N) return SPX_ERR_ARG;
-    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 4) || !spx_aligned(B, 4) ||
-        !spx_aligned(C, 4))
-        return SPX_ERR_ALIGN;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int v = pick_variant(N, B, ldb, C, ldc);
-    if (v == 0) {
-        const int grid = (M + kWarps - 1) / kWarps;
-        switch (N) {
-#define SPX_SMALL(n) case n: spmm_small_kernel<n><<<grid, kThreads, 0, st>>>(M, rp, col, val, B, ldb, alpha, beta, C, ldc); break;
-            SPX_SMALL(1) SPX_SMALL(2) SPX_SMALL(3) SPX_SMALL(4) SPX_SMALL(5) SPX_SMALL(6) SPX_SMALL(7) SPX_SMALL(8)
-#undef SPX_SMALL
-        }
-    } else if (v == 1) {
-        const int q = N / 4;
-        if (q <= 2) launch_vec<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
-        else if (q <= 4) launch_vec<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
-        else if (q <= 8) launch_vec<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
-        else if (q <= 16) launch_vec<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
-        else launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, 1, st);
-    } else if (v == 2) {
-        launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, (N + 127) / 128, st);
-    } else {
-        dim3 grid((M + kWarps - 1) / kWarps, (N + 31) / 32 < 4 ? (N + 31) / 32 : 4);
-        spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
-    }
-    spx_note_launches(1);
-    return spx_cuda_status(cudaGetLastError());
+    return spmm_impl(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
+                              const float* val, int32_t N, const float* B, int64_t ldb, float alpha, float beta,
+                              float* C, int64_t ldc, int32_t col_tile, spx_stream_t stream) {
+    return spmm_impl(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, col_tile,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

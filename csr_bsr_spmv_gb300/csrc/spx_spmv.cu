@@ -4,20 +4,26 @@
 // One launch serves the whole task table of the plan ([SpMM-ops] §2.1-§2.4):
 //   group  : a run of consecutive short rows (<= B nonzeros).  The CTA streams
 //            the group's values/column indices once, coalesced, gathers x
-//            through the read-only path, parks the products in shared memory,
-//            then reduces each row with w lanes (w = 1: thread per row,
-//            w = 32: warp per row) and a shuffle tree.
+//            through the read-only path and parks the products in shared
+//            memory.  Then either
+//              - lanes mode: each row is reduced by w lanes (w = 1: thread per
+//                row, w = 32: warp per row) with a shuffle tree, or
+//              - segmented mode: thread t sums the products [t*P, t*P + P)
+//                whatever rows they belong to, rows that cross threads are
+//                joined by a segmented block scan -- the same work per thread
+//                however the row lengths vary ([Formats] §6, merge-based).
 //   cta    : one row of hundreds..thousands of nonzeros; all threads stride it,
 //            warp shuffles then a fixed-order reduction of the warp sums.
 //   seg    : one segment of a split long row; writes a partial sum.
 // A second small launch (one warp per split row) adds the partial sums in a
 // fixed order and applies the epilogue ([SpMM-ops] §2.4: partial buffer plus
-// second-stage reduction; no floating-point atomics, so results are bitwise
-// reproducible).
+// second-stage reduction).  No floating-point atomics anywhere, so results are
+// bitwise reproducible run to run.
 //
-// Matrix streams (values, column indices) are read with the evict-first
-// (streaming) cache hint so that x -- the gathered operand -- keeps its L2
-// residency ([SpMM-ops] §2.5).
+// Each task carries its nonzero range, so a CTA issues its value/column loads
+// right after reading the task.  Values and column indices are read with the
+// streaming (evict-first) hint so that x -- the gathered operand -- keeps its
+// L2 residency ([SpMM-ops] §2.5).
 #include <cuda_runtime.h>
 
 #include "spx_internal.h"
@@ -26,17 +32,18 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(0xffffffffu, v, d);
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(kFull, v, d);
     return v;
 }
 
-// Sum of v over the NT threads of the CTA in a fixed order; result valid in thread 0.
+// Sum of v over the CTA in a fixed order; result valid in thread 0.
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -50,7 +57,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return s;
 }
 
-// Strided dot product of a nonzero range [a, b) with x; 4 loads in flight per thread.
+// Strided dot product of the nonzero range [a, b) with x; 4 gathers in flight per thread.
 __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__ col, const float* __restrict__ val,
                                            const float* __restrict__ x) {
     float s = 0.f;
@@ -70,22 +77,31 @@ __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__
     return s;
 }
 
-__device__ __forceinline__ float epilogue(float s, float alpha, float beta, const float* y, int row) {
+__device__ __forceinline__ void emit(float* y, int row, float s, float alpha, float beta) {
     float r = alpha * s;
     if (beta != 0.f) r += beta * y[row];
-    return r;
+    y[row] = r;
 }
 
-// ITEMS = block_nnz / kThreads when it is a compile-time case, else 0 (loop).
+// Group epilogue: the old y of the group's rows was prefetched into s_y with the
+// products, so no row waits on a dependent global read here.
+__device__ __forceinline__ void emit_g(float* y, const float* s_y, int r0, int r, float s, float alpha, float beta) {
+    float v = alpha * s;
+    if (beta != 0.f) v += beta * s_y[r];
+    y[r0 + r] = v;
+}
+
+// Shared-memory slot of product k: one padding word after every 32 products,
+// so both the strided writes (thread t: k = t + 256 j) and the blocked reads
+// of the segmented mode (thread t: k = t*P .. t*P + P-1) hit 32 distinct banks.
+__device__ __forceinline__ int sk(int k) { return k + (k >> 5); }
+
+// Products val[p0+k] * x[col[p0+k]], k < n, into s_prod[sk(k)] (coalesced layout);
+// ITEMS = block_nnz / kThreads as a compile-time case, 0 = runtime loop.
 template <int ITEMS>
-__device__ __forceinline__ void group_task(int r0, int r1, int lg, const int* __restrict__ rp,
-                                           const int* __restrict__ col, const float* __restrict__ val,
-                                           const float* __restrict__ x, float alpha, float beta, float* y,
-                                           float* s_prod, int* s_rp) {
-    const int p0 = __ldg(rp + r0);
-    const int nrows = r1 - r0;
-    const int n = __ldg(rp + r1) - p0;
-    for (int i = threadIdx.x; i <= nrows; i += kThreads) s_rp[i] = __ldg(rp + r0 + i) - p0;
+__device__ __forceinline__ void stage_products(int p0, int n, const int* __restrict__ col,
+                                               const float* __restrict__ val, const float* __restrict__ x,
+                                               float* s_prod) {
     if (ITEMS > 0) {
         int c[ITEMS > 0 ? ITEMS : 1];
         float v[ITEMS > 0 ? ITEMS : 1];
@@ -98,13 +114,17 @@ __device__ __forceinline__ void group_task(int r0, int r1, int lg, const int* __
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
             const int k = threadIdx.x + j * kThreads;
-            if (k < n) s_prod[k] = v[j] * __ldg(x + c[j]);
+            if (k < n) s_prod[sk(k)] = v[j] * __ldg(x + c[j]);
         }
     } else {
-        for (int k = threadIdx.x; k < n; k += kThreads) s_prod[k] = ld_stream(val + p0 + k) * __ldg(x + ld_stream(col + p0 + k));
+        for (int k = threadIdx.x; k < n; k += kThreads)
+            s_prod[sk(k)] = ld_stream(val + p0 + k) * __ldg(x + ld_stream(col + p0 + k));
     }
-    __syncthreads();
-    // reduce each row with w = 2^lg lanes; every lane of a warp runs the same trip count
+}
+
+// Lanes mode: each row reduced by w = 2^lg lanes; every lane of a warp runs the same trip count.
+__device__ __forceinline__ void reduce_lanes(int r0, int nrows, int lg, const float* s_prod, const int* s_rp,
+                                             const float* s_y, float alpha, float beta, float* y) {
     const int w = 1 << lg;
     const int sub = threadIdx.x >> lg, lane = threadIdx.x & (w - 1);
     const int nsub = kThreads >> lg;
@@ -113,12 +133,103 @@ __device__ __forceinline__ void group_task(int r0, int r1, int lg, const int* __
         float s = 0.f;
         if (r < nrows) {
             const int a = s_rp[r], b = s_rp[r + 1];
-            for (int k = a + lane; k < b; k += w) s += s_prod[k];
+            for (int k = a + lane; k < b; k += w) s += s_prod[sk(k)];
         }
         for (int d = 16; d > 0; d >>= 1)
-            if (d < w) s += __shfl_down_sync(0xffffffffu, s, d, w);
-        if (r < nrows && lane == 0) y[r0 + r] = epilogue(s, alpha, beta, y, r0 + r);
+            if (d < w) s += __shfl_down_sync(kFull, s, d, w);
+        if (r < nrows && lane == 0) emit_g(y, s_y, r0, r, s, alpha, beta);
     }
+}
+
+// Segmented mode: thread t owns products [t*per, t*per + per).  Rows that end
+// inside a thread's run are written by that thread; a row crossing threads
+// is finished by the thread holding its last product, which adds the carry
+// from an inclusive segmented scan of the threads' trailing partial sums.
+template <int PER>
+__device__ __forceinline__ void reduce_segmented(int r0, int nrows, int n, int per_rt, const float* s_prod,
+                                                 const int* s_rp, const float* s_y, float alpha, float beta, float* y,
+                                                 float* s_sv, int* s_sf) {
+    const int per = PER > 0 ? PER : per_rt;
+    const int a = threadIdx.x * per;
+    const int e = min(a + per, n);
+    float s = 0.f, first_part = 0.f;
+    int flag = 0, first_row = 0;
+    bool first_ends = false;
+    if (threadIdx.x == 0) {  // rows with no products before the first product
+        for (int r = 0; r < nrows && s_rp[r + 1] == 0; ++r) emit_g(y, s_y, r0, r, 0.f, alpha, beta);
+    }
+    if (a < n) {
+        int lo = 0, hi = nrows;  // first index with s_rp[index] > a
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_rp[mid] > a) hi = mid; else lo = mid + 1;
+        }
+        int r = lo - 1;  // the (non-empty) row holding position a
+        bool carry_row = s_rp[r] < a;
+        first_row = r;
+        int next = s_rp[r + 1];
+        if (PER > 0 && a + PER <= n) {
+#pragma unroll
+            for (int j = 0; j < (PER > 0 ? PER : 1); ++j) {
+                const int k = a + j;
+                while (next == k) {
+                    if (carry_row) { first_part = s; first_ends = true; carry_row = false; }
+                    else emit_g(y, s_y, r0, r, s, alpha, beta);
+                    s = 0.f;
+                    ++r;
+                    next = s_rp[r + 1];
+                }
+                s += s_prod[sk(k)];
+            }
+        } else {
+            for (int k = a; k < e; ++k) {
+                while (next == k) {
+                    if (carry_row) { first_part = s; first_ends = true; carry_row = false; }
+                    else emit_g(y, s_y, r0, r, s, alpha, beta);
+                    s = 0.f;
+                    ++r;
+                    next = s_rp[r + 1];
+                }
+                s += s_prod[sk(k)];
+            }
+        }
+        // rows ending exactly at this thread's boundary, and empty rows there
+        while (r < nrows && next == e) {
+            if (carry_row) { first_part = s; first_ends = true; carry_row = false; }
+            else emit_g(y, s_y, r0, r, s, alpha, beta);
+            s = 0.f;
+            ++r;
+            next = r < nrows ? s_rp[r + 1] : -1;
+        }
+        flag = carry_row ? 0 : 1;  // the trailing partial starts inside this thread
+    }
+    // inclusive segmented scan of (flag, s): (f1,v1) + (f2,v2) = (f1|f2, f2 ? v2 : v1 + v2)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float v = s;
+    int f = flag;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float v2 = __shfl_up_sync(kFull, v, d);
+        const int f2 = __shfl_up_sync(kFull, f, d);
+        if (lane >= d) {
+            if (!f) v = v2 + v;
+            f |= f2;
+        }
+    }
+    if (lane == 31) {
+        s_sv[warp] = v;
+        s_sf[warp] = f;
+    }
+    __syncthreads();
+    float wp = 0.f;
+    for (int i = 0; i < warp; ++i) wp = s_sf[i] ? s_sv[i] : wp + s_sv[i];
+    float ex = __shfl_up_sync(kFull, v, 1);
+    int exf = __shfl_up_sync(kFull, f, 1);
+    if (lane == 0) {
+        ex = 0.f;
+        exf = 0;
+    }
+    if (first_ends) emit_g(y, s_y, r0, first_row, (exf ? ex : wp + ex) + first_part, alpha, beta);
 }
 
 template <int ITEMS>
@@ -126,27 +237,38 @@ __global__ void __launch_bounds__(kThreads) spmv_tasks_kernel(const int4* __rest
                                                               const int* __restrict__ rp, const int* __restrict__ col,
                                                               const float* __restrict__ val,
                                                               const float* __restrict__ x, float alpha, float beta,
-                                                              float* y, float* __restrict__ partials, int seg_nnz,
-                                                              int block_nnz) {
+                                                              float* y, float* __restrict__ partials, int block_nnz,
+                                                              int block_rows) {
     extern __shared__ __align__(16) float smem[];
     const int4 t = tasks[blockIdx.x];
-    const int kind = t.x & 255;
+    const int kind = t.x & 3;
     if (kind == kTaskGroup) {
-        group_task<ITEMS>(t.y, t.z, t.x >> 8, rp, col, val, x, alpha, beta, y, smem,
-                          reinterpret_cast<int*>(smem + block_nnz));
-    } else if (kind == kTaskCta) {
-        const int row = t.y;
-        float s = range_dot(__ldg(rp + row), __ldg(rp + row + 1), col, val, x);
-        s = block_sum(s, smem);
-        if (threadIdx.x == 0) y[row] = epilogue(s, alpha, beta, y, row);
+        float* s_prod = smem;
+        int* s_rp = reinterpret_cast<int*>(smem + block_nnz + block_nnz / 32 + 1);
+        float* s_sv = reinterpret_cast<float*>(s_rp + block_rows + 1);
+        int* s_sf = reinterpret_cast<int*>(s_sv + kWarps);
+        float* s_y = reinterpret_cast<float*>(s_sf + kWarps);
+        const int code = (t.x >> 2) & 63, nrows = t.x >> 8, r0 = t.y, p0 = t.z, n = t.w - t.z;
+        for (int i = threadIdx.x; i <= nrows; i += kThreads) {
+            s_rp[i] = __ldg(rp + r0 + i) - p0;
+            if (beta != 0.f && i < nrows) s_y[i] = y[r0 + i];
+        }
+        stage_products<ITEMS>(p0, n, col, val, x, s_prod);
+        __syncthreads();
+        if (code == kReduceSegmented)
+            reduce_segmented<ITEMS>(r0, nrows, n, (block_nnz + kThreads - 1) / kThreads, s_prod, s_rp, s_y, alpha,
+                                    beta, y, s_sv, s_sf);
+        else
+            reduce_lanes(r0, nrows, code, s_prod, s_rp, s_y, alpha, beta, y);
     } else {
-        const int row = t.y;
-        const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
-        const long long lo = (long long)a + (long long)t.z * seg_nnz;
-        const int hi = (int)min((long long)b, lo + seg_nnz);
-        float s = range_dot((int)lo, hi, col, val, x);
+        // the old y of a CTA row is read up front, off the critical path
+        const float y_old = (kind == kTaskCta && beta != 0.f && threadIdx.x == 0) ? y[t.y] : 0.f;
+        float s = range_dot(t.z, t.w, col, val, x);
         s = block_sum(s, smem);
-        if (threadIdx.x == 0) partials[t.w] = s;
+        if (threadIdx.x == 0) {
+            if (kind == kTaskCta) y[t.y] = alpha * s + (beta != 0.f ? beta * y_old : 0.f);
+            else partials[t.x >> 8] = s;
+        }
     }
 }
 
@@ -161,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) spmv_fixup_kernel(const int4* __rest
     float s = 0.f;
     for (int k = lane; k < lr.z; k += 32) s += partials[lr.y + k];
     s = warp_sum(s);
-    if (lane == 0) y[lr.x] = epilogue(s, alpha, beta, y, lr.x);
+    if (lane == 0) emit(y, lr.x, s, alpha, beta);
 }
 
 spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const float* val, float alpha,
@@ -171,21 +293,21 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     if (ntasks == 0) return SPX_OK;
     const int4* tasks = static_cast<const int4*>(P->d_table);
     const int4* longrows = tasks + ntasks;
-    const int B = P->opts.block_nnz;
-    const size_t smem = sizeof(float) * static_cast<size_t>(B) + sizeof(int) * (static_cast<size_t>(P->opts.block_rows) + 1);
-    const int seg = P->opts.seg_nnz;
+    const int B = P->opts.block_nnz, R = P->opts.block_rows;
+    const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) + sizeof(int) * (static_cast<size_t>(R) + 1) +
+                        2 * kWarps * sizeof(float) + sizeof(float) * static_cast<size_t>(R);
     switch (B) {
         case kThreads * 4:
-            spmv_tasks_kernel<4><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, seg, B);
+            spmv_tasks_kernel<4><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         case kThreads * 8:
-            spmv_tasks_kernel<8><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, seg, B);
+            spmv_tasks_kernel<8><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         case kThreads * 16:
-            spmv_tasks_kernel<16><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, seg, B);
+            spmv_tasks_kernel<16><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         default:
-            spmv_tasks_kernel<0><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, seg, B);
+            spmv_tasks_kernel<0><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
     }
     uint64_t launches = 1;

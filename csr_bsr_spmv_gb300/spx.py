@@ -23,7 +23,7 @@ SPX_HOST, SPX_DEVICE = 0, 1
 STATUS = {0: "SPX_OK", -1: "SPX_ERR_ARG", -2: "SPX_ERR_INDEX_RANGE", -3: "SPX_ERR_NOT_SORTED",
           -4: "SPX_ERR_DUPLICATE", -5: "SPX_ERR_CUDA", -6: "SPX_ERR_TIMEOUT", -7: "SPX_ERR_UNSUPPORTED",
           -8: "SPX_ERR_ALIGN", -9: "SPX_ERR_NOMEM", -10: "SPX_ERR_NOT_READY"}
-SPMM_VARIANTS = {0: "small-N", 1: "subwarp-float4", 2: "tiled-float4", 3: "scalar"}
+SPMM_VARIANTS = {0: "small-N", 1: "float4", 2: "float4-wide", 3: "scalar"}
 
 
 class SpxError(RuntimeError):
@@ -53,7 +53,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("K", ctypes.c_int64), ("nnz", ctypes.c_int64), ("tasks", ctypes.c_int64),
                 ("long_rows", ctypes.c_int64), ("slots", ctypes.c_int64), ("packed_rows", ctypes.c_int64),
                 ("cta_rows", ctypes.c_int64), ("split_rows", ctypes.c_int64), ("thread_groups", ctypes.c_int64),
-                ("lane_groups", ctypes.c_int64), ("table_bytes", ctypes.c_size_t),
+                ("lane_groups", ctypes.c_int64), ("segmented_groups", ctypes.c_int64), ("table_bytes", ctypes.c_size_t),
                 ("scratch_bytes", ctypes.c_size_t), ("stats", RowStats)]
 
 
@@ -88,6 +88,7 @@ def _lib():
             "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
                                    sz, vp], ctypes.c_int),
             "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_csr_tiled": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, i32, vp], ctypes.c_int),
             "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
             "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, vp, i64, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
@@ -326,13 +327,19 @@ def spx_spmv_csr_dual(plan_A: Plan, plan_At: Plan, A: Csr, At: Csr, v: torch.Ten
     return u, v
 
 
-def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C <- alpha*A*B + beta*C; B (K x N) and C (M x N) row-major views (stride(1) == 1)."""
+def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None,
+                 col_tile: int | None = None):
+    """C <- alpha*A*B + beta*C; B (K x N) and C (M x N) row-major views (stride(1) == 1).
+    col_tile: None = automatic (spx_spmm_csr), else spx_spmm_csr_tiled's column tile."""
     N = B.shape[1]
     assert B.stride(1) == 1 and C.stride(1) == 1
-    _check(_lib().spx_spmm_csr(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
-                               B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
-           "spx_spmm_csr")
+    lib = _lib()
+    args = (A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B), B.stride(0), float(alpha),
+            float(beta), _ptr(C), C.stride(0))
+    if col_tile is None:
+        _check(lib.spx_spmm_csr(*args, _stream(stream)), "spx_spmm_csr")
+    else:
+        _check(lib.spx_spmm_csr_tiled(*args, int(col_tile), _stream(stream)), "spx_spmm_csr_tiled")
     return C
 
 

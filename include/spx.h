@@ -149,8 +149,11 @@ typedef struct spx_plan_opts_t {
     int32_t pack_max;   /* P: rows with l <= P are packed into groups (P <= B)      */
     int32_t cta_max;    /* C: rows with P < l <= C get one CTA each                 */
     int32_t seg_nnz;    /* S: rows with l > C are cut into segments of S nonzeros   */
-    int32_t lanes_div;  /* D: a group reduces each row with w lanes,
-                           w = pow2ceil(ceil(nnz_g / (rows_g * D))) clamped to [1, 32] */
+    int32_t lanes_div;  /* D >= 1: a group reduces each row with w lanes,
+                           w = pow2ceil(ceil(nnz_g / (rows_g * D))) clamped to [1, 32];
+                           D == 0: segmented reduction -- each thread sums an
+                           equal run of consecutive products, rows crossing
+                           threads are joined by a block scan */
 } spx_plan_opts_t;
 
 /* Fills the defaults the benchmarks were tuned with. */
@@ -164,6 +167,7 @@ typedef struct spx_plan_info_t {
     int64_t packed_rows, cta_rows, split_rows;
     int64_t thread_groups; /* groups reduced thread-per-row (w == 1)          */
     int64_t lane_groups;   /* groups reduced with 2..32 lanes per row         */
+    int64_t segmented_groups; /* groups with the segmented reduction          */
     size_t table_bytes;    /* device bytes for spx_plan_upload (16-B aligned) */
     size_t scratch_bytes;  /* device scratch bytes each SpMV call needs       */
     spx_row_stats_t stats;
@@ -181,7 +185,8 @@ typedef struct spx_plan spx_plan; /* opaque, host-side */
  *           nonzeros (a CTA or split row closes a group);
  *   P < l <= C: one CTA;  l > C: ceil(l/S) segments, then a fix-up pass.
  * Task table (4 int32 per task): first all CTA rows {1,row,0,0} and segments
- * {2,row,seg,slot} in row order, then groups {256*log2(w), r0, r1, 0}.
+ * {2,row,seg,slot} in row order, then groups {256*c, r0, r1, 0} where the
+ * reduction code c is log2(w) (lanes per row) or 6 (segmented, D == 0).
  * Long-row table (4 int32 per split row): {row, first slot, #segments, 0}.
  * opts == NULL uses spx_plan_opts_default.  row_ptr is read once (copied to
  * the host when where == SPX_DEVICE).  *plan_out must be released with
@@ -252,8 +257,9 @@ spx_status spx_spmv_csr_dual(const spx_plan* plan_A, const spx_plan* plan_At, in
  * B's contiguous columns accumulated in registers) and §3.1-§3.3 (variant
  * chosen by N):
  *   N <= 8           lanes split the row's nonzeros, N accumulators each;
- *   N % 4 == 0, <= 128  a sub-warp of pow2ceil(N/4) lanes per row, float4 B loads;
- *   N % 4 == 0, > 128   (row, 128-column tile) per warp, tiles outermost;
+ *   N % 4 == 0       column tiles of T = pow2ceil(N) capped at 128, one
+ *                    sub-warp of T/4 lanes per (row, tile), float4 B loads,
+ *                    tiles outermost;
  *   otherwise        a warp per row, lanes over columns (scalar).
  * The float4 variants need B, C 16-byte aligned and ldb, ldc multiples of 4;
  * otherwise the scalar variant runs.  Launches: 1.
@@ -262,8 +268,14 @@ spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
                         const float* val, int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C,
                         int64_t ldc, spx_stream_t stream);
 
+/* spx_spmm_csr with the column tile T of the float4 variants given by the
+   caller (0 = automatic as above; else a power of two in [8, 128]). */
+spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                              const float* val, int32_t N, const float* B, int64_t ldb, float alpha, float beta,
+                              float* C, int64_t ldc, int32_t col_tile, spx_stream_t stream);
+
 /* Which SpMM variant spx_spmm_csr would launch for these arguments:
-   0 = small-N, 1 = sub-warp float4, 2 = column-tiled float4, 3 = scalar. */
+   0 = small-N, 1 = float4 with N <= 128, 2 = float4 with N > 128, 3 = scalar. */
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);
 
 /*

@@ -148,14 +148,14 @@ def plan_spmv(M, rp, **opts):
     """Returns dict(tasks[ntasks,4], longrows[nlong,4], counts)."""
     rp = _c(rp, np.int32)
     o = PlanOpts(**{f: int(opts[f]) for f in PLAN_FIELDS})
-    counts = np.zeros(8, np.int64)
+    counts = np.zeros(9, np.int64)
     lib = _lib_()
     _check(lib.or_plan_spmv(M, _p(rp), ctypes.byref(o), None, None, _p(counts)))
     tasks = np.empty((int(counts[0]), 4), np.int32)
     longrows = np.empty((int(counts[1]), 4), np.int32)
     _check(lib.or_plan_spmv(M, _p(rp), ctypes.byref(o), _p(tasks), _p(longrows), _p(counts)))
     names = ("tasks", "long_rows", "slots", "packed_rows", "cta_rows", "split_rows", "thread_groups",
-             "lane_groups")
+             "lane_groups", "segmented_groups")
     return dict(tasks=tasks, longrows=longrows, counts=dict(zip(names, (int(c) for c in counts))))
 
 

@@ -229,7 +229,8 @@ typedef struct {
     int32_t pack_max;    /* P: rows with l <= P are packed into groups        */
     int32_t cta_max;     /* C: rows with P < l <= C get one CTA each          */
     int32_t seg_nnz;     /* S: rows with l > C are cut into segments of S     */
-    int32_t lanes_div;   /* D: lanes per row in a group = pow2ceil(ceil(avg/D)) */
+    int32_t lanes_div;   /* D: lanes per row in a group = pow2ceil(ceil(avg/D));
+                            D == 0: every group uses the segmented reduction */
 } or_plan_opts_t;
 
 enum { OR_TASK_GROUP = 0, OR_TASK_CTA = 1, OR_TASK_SEG = 2 };
@@ -252,25 +253,30 @@ static int32_t pow2ceil_clamp32(int64_t v) {
  *                   l > C         -> split into ceil(l/S) segments
  * Groups: scanning rows upward, consecutive packed rows join the current
  * group while it has fewer than R rows and its nonzeros stay <= B; any
- * CTA/split row closes it.  A group reduces each of its rows with w lanes,
- * w = the smallest power of two >= ceil(nnz_g / (rows_g * D)), clamped to
- * [1, 32]: w == 1 is thread-per-row, w == 32 warp-per-row.
+ * CTA/split row closes it.  Reduction code c of a group:
+ *   D >= 1: each row is reduced by w lanes, w = the smallest power of two >=
+ *           ceil(nnz_g / (rows_g * D)), clamped to [1, 32]; c = log2(w)
+ *           (w == 1 is thread-per-row, w == 32 warp-per-row);
+ *   D == 0: c = 6, the segmented reduction -- every thread sums an equal run
+ *           of consecutive products and rows crossing threads are joined by a
+ *           scan, so work per thread no longer follows row length
+ *           ([Formats] §6, the merge-based remedy: equal nonzeros per thread).
  * Task list (4 ints per task): first every CTA row and split segment in row
  * order -- {1, row, 0, 0} or {2, row, segment, slot}, slots numbered
  * 0,1,2,... in that order -- then every group in row order:
- * {0 + 256*log2(w), first row, end row (exclusive), 0}.
+ * {0 + 256*c, first row, end row (exclusive), 0}.
  * Long-row table (4 ints per split row, row order): {row, first slot, #segments, 0}.
  * counts_out = {#tasks, #long rows, #slots, #rows packed, #CTA rows, #split rows,
- *               #groups with w == 1, #groups with w > 1}.
+ *               #groups with c == 0, #groups with 1 <= c <= 5, #groups with c == 6}.
  * Pass tasks/longrows == NULL to only count.
  */
 int or_plan_spmv(int32_t M, const int32_t* rp, const or_plan_opts_t* o, int32_t* tasks, int32_t* longrows,
                  int64_t* counts_out) {
     if (M < 0 || !o || !counts_out) return OR_ERR_ARG;
     if (o->block_nnz < 1 || o->block_rows < 1 || o->pack_max < 0 || o->pack_max > o->block_nnz ||
-        o->cta_max < o->pack_max || o->seg_nnz < 1 || o->lanes_div < 1)
+        o->cta_max < o->pack_max || o->seg_nnz < 1 || o->lanes_div < 0)
         return OR_ERR_ARG;
-    int64_t nt = 0, nl = 0, slot = 0, npacked = 0, ncta = 0, nsplit = 0, g1 = 0, gw = 0;
+    int64_t nt = 0, nl = 0, slot = 0, npacked = 0, ncta = 0, nsplit = 0, g1 = 0, gw = 0, gs = 0;
     /* pass 1: CTA rows and segments */
     for (int32_t i = 0; i < M; ++i) {
         int64_t l = (int64_t)rp[i + 1] - rp[i];
@@ -304,17 +310,20 @@ int or_plan_spmv(int32_t M, const int32_t* rp, const or_plan_opts_t* o, int32_t*
             ++i;
         }
         int64_t rows = i - r0;
-        int64_t per = (gnnz + rows * o->lanes_div - 1) / (rows * o->lanes_div);
-        int32_t w = pow2ceil_clamp32(per);
-        int32_t lg = 0;
-        while ((1 << lg) < w) ++lg;
-        if (tasks) { int32_t* t = tasks + 4 * nt; t[0] = OR_TASK_GROUP + 256 * lg; t[1] = r0; t[2] = i; t[3] = 0; }
+        int32_t c = 6;
+        if (o->lanes_div > 0) {
+            int64_t per = (gnnz + rows * o->lanes_div - 1) / (rows * o->lanes_div);
+            int32_t w = pow2ceil_clamp32(per);
+            c = 0;
+            while ((1 << c) < w) ++c;
+        }
+        if (tasks) { int32_t* t = tasks + 4 * nt; t[0] = OR_TASK_GROUP + 256 * c; t[1] = r0; t[2] = i; t[3] = 0; }
         ++nt;
         npacked += rows;
-        if (w == 1) ++g1; else ++gw;
+        if (c == 0) ++g1; else if (c == 6) ++gs; else ++gw;
     }
     counts_out[0] = nt; counts_out[1] = nl; counts_out[2] = slot; counts_out[3] = npacked;
-    counts_out[4] = ncta; counts_out[5] = nsplit; counts_out[6] = g1; counts_out[7] = gw;
+    counts_out[4] = ncta; counts_out[5] = nsplit; counts_out[6] = g1; counts_out[7] = gw; counts_out[8] = gs;
     return OR_OK;
 }
 

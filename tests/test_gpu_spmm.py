@@ -34,13 +34,27 @@ def run(M, K, d, N, alpha=1.0, beta=0.0, ldb=None, ldc=None, seed=0, want_varian
 
 
 @pytest.mark.parametrize("N,variant", [(1, "small-N"), (2, "small-N"), (3, "small-N"), (8, "small-N"),
-                                       (12, "subwarp-float4"), (16, "subwarp-float4"), (32, "subwarp-float4"),
-                                       (64, "subwarp-float4"), (100, "subwarp-float4"), (128, "subwarp-float4"),
-                                       (132, "tiled-float4"), (256, "tiled-float4"), (520, "tiled-float4"),
+                                       (12, "float4"), (16, "float4"), (32, "float4"),
+                                       (64, "float4"), (100, "float4"), (128, "float4"),
+                                       (132, "float4-wide"), (256, "float4-wide"), (520, "float4-wide"),
                                        (9, "scalar"), (33, "scalar"), (130, "scalar")])
 def test_variants(N, variant):
     d = synth.random_coo(N, 1111, 777, 0, 50)
     run(1111, 777, d, N, alpha=1.0, beta=0.0, want_variant=variant, seed=N)
+
+
+@pytest.mark.parametrize("N,tile", [(32, 8), (32, 16), (64, 32), (128, 16), (100, 64), (256, 128), (48, 8)])
+def test_column_tiles(N, tile):
+    d = synth.random_coo(N + tile, 900, 600, 0, 40)
+    M, K = 900, 600
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    B = synth.uniform(5, synth.T_B, K * N).reshape(K, N)
+    Cd = torch.full((M, N), float("nan"), device="cuda")
+    spx.spx_spmm_csr(A, dev(B), Cd, col_tile=tile)
+    torch.cuda.synchronize()
+    ref, bound = oracle.spmm(M, rp, col, val, B)
+    assert_within(Cd.cpu().numpy(), ref, bound, what=f"N={N} tile={tile}")
 
 
 @pytest.mark.parametrize("alpha,beta", [(2.0, 0.0), (1.0, -0.5), (0.0, 1.5)])

@@ -21,6 +21,11 @@ SMALL_OPTS = [
     dict(block_nnz=1024, block_rows=128, pack_max=64, cta_max=300, seg_nnz=256, lanes_div=1),
     dict(block_nnz=4096, block_rows=1024, pack_max=4096, cta_max=4096, seg_nnz=1000, lanes_div=8),
     dict(block_nnz=2000, block_rows=77, pack_max=33, cta_max=2000, seg_nnz=777, lanes_div=3),
+    dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=4),
+    dict(block_nnz=1024, block_rows=1024, pack_max=1024, cta_max=1024, seg_nnz=512, lanes_div=0),
+    dict(block_nnz=4096, block_rows=300, pack_max=2000, cta_max=9000, seg_nnz=3000, lanes_div=0),
+    dict(block_nnz=1000, block_rows=50, pack_max=999, cta_max=3000, seg_nnz=1000, lanes_div=0),
+    dict(block_nnz=8, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=0),
 ]
 
 

@@ -14,7 +14,7 @@ from csr_bsr_spmv_gb300 import spx
 
 def test_exports_every_header_symbol():
     names = spx.header_symbols()
-    assert len(names) >= 19
+    assert len(names) >= 20
     lib = ctypes.CDLL(spx.LIB_PATH)
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
@@ -108,6 +108,7 @@ PLAN_OPTS = [
     dict(block_nnz=16, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=2),
     dict(block_nnz=1024, block_rows=256, pack_max=1024, cta_max=1024, seg_nnz=1024, lanes_div=1),
     dict(block_nnz=4096, block_rows=512, pack_max=64, cta_max=20000, seg_nnz=3000, lanes_div=8),
+    dict(block_nnz=1000, block_rows=100, pack_max=999, cta_max=5000, seg_nnz=700, lanes_div=0),
 ]
 
 
@@ -132,7 +133,7 @@ def test_plan_matches_oracle(opts, seed):
 
 def test_plan_default_options_documented():
     o = spx.spx_plan_opts_default()
-    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=4)
+    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=0)
 
 
 def test_plan_rejects_bad_rows_and_options():

@@ -302,15 +302,21 @@ def test_plan_hand_example():
     assert p["tasks"].tolist() == want
     assert p["longrows"].tolist() == [[8, 0, 7, 0]]
     assert p["counts"] == dict(tasks=13, long_rows=1, slots=7, packed_rows=10, cta_rows=1, split_rows=1,
-                               thread_groups=1, lane_groups=4)
+                               thread_groups=1, lane_groups=4, segmented_groups=0)
+    # D = 0: the same groups, every one with the segmented reduction (code 6)
+    q = oracle.plan_spmv(len(L), rp, **dict(OPTS_SMALL, lanes_div=0))
+    seg = [t if t[0] & 255 else [6 * 256, t[1], t[2], 0] for t in want]
+    assert q["tasks"].tolist() == seg
+    assert q["counts"]["segmented_groups"] == 5 and q["counts"]["thread_groups"] == 0
 
 
 @pytest.mark.parametrize("seed", range(4))
-def test_plan_invariants(seed):
+@pytest.mark.parametrize("div", [0, 4])
+def test_plan_invariants(seed, div):
     L, _ = synth.lengths_zipf(seed, 3000, 2.1, 3000, 6.0)
     L[::97] = 0
     rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
-    o = dict(block_nnz=64, block_rows=16, pack_max=32, cta_max=200, seg_nnz=50, lanes_div=4)
+    o = dict(block_nnz=64, block_rows=16, pack_max=32, cta_max=200, seg_nnz=50, lanes_div=div)
     p = oracle.plan_spmv(L.size, rp, **o)
     covered = np.zeros(L.size, np.int64)
     seg_cover = {}
@@ -320,9 +326,12 @@ def test_plan_invariants(seed):
             rows = np.arange(a, b)
             assert 1 <= b - a <= o["block_rows"]
             assert np.all(L[rows] <= o["pack_max"]) and L[rows].sum() <= o["block_nnz"]
-            w = 1 << (kind >> 8)
-            per = -(-int(L[rows].sum()) // ((b - a) * o["lanes_div"]))
-            assert w == min(32, max(1, 1 << int(np.ceil(np.log2(max(per, 1))))))
+            if div == 0:
+                assert kind >> 8 == 6
+            else:
+                w = 1 << (kind >> 8)
+                per = -(-int(L[rows].sum()) // ((b - a) * o["lanes_div"]))
+                assert w == min(32, max(1, 1 << int(np.ceil(np.log2(max(per, 1))))))
             covered[rows] += 1
         elif k == 1:
             assert o["pack_max"] < L[a] <= o["cta_max"]
