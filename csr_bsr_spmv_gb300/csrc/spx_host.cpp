@@ -272,6 +272,8 @@ const char* spx_status_string(spx_status s) {
         case SPX_ERR_ALIGN: return "SPX_ERR_ALIGN: misaligned pointer or leading dimension";
         case SPX_ERR_NOMEM: return "SPX_ERR_NOMEM: host allocation failed";
         case SPX_ERR_NOT_READY: return "SPX_ERR_NOT_READY: plan not uploaded";
+        case SPX_ERR_SCRATCH_LIMIT:
+            return "SPX_ERR_SCRATCH_LIMIT: the plan needs more partial-sum slots than the fixed no-alloc buffer holds";
     }
     return "unknown spx_status";
 }

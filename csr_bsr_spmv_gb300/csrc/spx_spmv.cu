@@ -26,6 +26,8 @@
 // L2 residency ([SpMM-ops] §2.5).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "spx_internal.h"
 
 namespace {
@@ -363,3 +365,44 @@ spx_status spx_spmv_csr_dual(const spx_plan* pA, const spx_plan* pAt, int32_t m,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc variant
+// Partial sums of split rows for spx_spmv_csr_noalloc, for callers that cannot
+// allocate device memory.  One copy per device, alive until the process exits;
+// every call on a device shares it (see include/spx.h).
+namespace {
+static __device__ __align__(256) float g_noalloc_partials[SPX_NOALLOC_MAX_SLOTS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device with that device current (host code must not use the symbol itself).
+spx_status noalloc_partials(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPX_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SPX_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return SPX_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPX_OK;
+}
+}  // namespace
+
+extern "C" spx_status spx_spmv_csr_noalloc(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz,
+                                           const int32_t* row_ptr, const int32_t* col, const float* val, float alpha,
+                                           const float* x, float beta, float* y, spx_stream_t stream) {
+    if (!spx_plan_ok(plan)) return SPX_ERR_ARG;
+    if (plan->counts[2] > SPX_NOALLOC_MAX_SLOTS) return SPX_ERR_SCRATCH_LIMIT;
+    float* partials = nullptr;
+    spx_status s = noalloc_partials(&partials);
+    if (s != SPX_OK) return s;
+    s = check_call(plan, M, K, nnz, row_ptr, col, val, x, y, partials, sizeof(float) * SPX_NOALLOC_MAX_SLOTS);
+    if (s != SPX_OK || M == 0) return s;
+    return launch_spmv(plan, row_ptr, col, val, alpha, x, beta, y, partials, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -22,7 +22,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "spx.h")
 SPX_HOST, SPX_DEVICE = 0, 1
 STATUS = {0: "SPX_OK", -1: "SPX_ERR_ARG", -2: "SPX_ERR_INDEX_RANGE", -3: "SPX_ERR_NOT_SORTED",
           -4: "SPX_ERR_DUPLICATE", -5: "SPX_ERR_CUDA", -6: "SPX_ERR_TIMEOUT", -7: "SPX_ERR_UNSUPPORTED",
-          -8: "SPX_ERR_ALIGN", -9: "SPX_ERR_NOMEM", -10: "SPX_ERR_NOT_READY"}
+          -8: "SPX_ERR_ALIGN", -9: "SPX_ERR_NOMEM", -10: "SPX_ERR_NOT_READY", -11: "SPX_ERR_SCRATCH_LIMIT"}
 SPMM_VARIANTS = {0: "small-N", 1: "float4", 2: "float4-wide", 3: "scalar"}
 
 
@@ -85,6 +85,7 @@ def _lib():
             "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
             "spx_plan_destroy": ([vp], ctypes.c_int),
             "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
+            "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
             "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
                                    sz, vp], ctypes.c_int),
             "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
@@ -311,6 +312,17 @@ def spx_spmv_csr(plan: Plan, A: Csr, x: torch.Tensor, y: torch.Tensor, alpha: fl
     _check(_lib().spx_spmv_csr(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
                                float(alpha), _ptr(x), float(beta), _ptr(y), _ptr(sc), sc.numel() * 4,
                                _stream(stream)), "spx_spmv_csr")
+    return y
+
+
+def spx_spmv_csr_noalloc(plan: Plan, A: Csr, x: torch.Tensor, y: torch.Tensor, alpha: float = 1.0,
+                         beta: float = 0.0, stream=None):
+    """y <- alpha*A*x + beta*y without a caller scratch buffer, for callers that
+    cannot allocate device memory: split-row partial sums use the library's
+    fixed device array (see include/spx.h)."""
+    _check(_lib().spx_spmv_csr_noalloc(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
+                                       float(alpha), _ptr(x), float(beta), _ptr(y), _stream(stream)),
+           "spx_spmv_csr_noalloc")
     return y
 
 

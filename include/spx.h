@@ -47,7 +47,8 @@ typedef enum spx_status {
     SPX_ERR_UNSUPPORTED = -7,  /* shape/type combination this build has no kernel for */
     SPX_ERR_ALIGN = -8,        /* pointer or leading dimension not aligned as documented */
     SPX_ERR_NOMEM = -9,        /* host allocation failed */
-    SPX_ERR_NOT_READY = -10    /* plan used before spx_plan_upload */
+    SPX_ERR_NOT_READY = -10,   /* plan used before spx_plan_upload */
+    SPX_ERR_SCRATCH_LIMIT = -11 /* needs more scratch than the library's fixed buffer holds */
 } spx_status;
 
 typedef enum spx_loc {
@@ -247,6 +248,36 @@ spx_status spx_spmv_csr_dual(const spx_plan* plan_A, const spx_plan* plan_At, in
                              const int32_t* At_row_ptr, const int32_t* At_col, const float* At_val, float* v,
                              float alpha_u, float beta_u, float* u, float alpha_v, float beta_v, void* scratch,
                              size_t scratch_bytes, spx_stream_t stream);
+
+/*
+ * spx_spmv_csr for callers that cannot allocate device memory -- code that
+ * runs where cudaMalloc is not available or not allowed (an allocator-free
+ * host runtime, a plugin handed only fixed buffers, a context that forbids
+ * allocation after start-up), and so cannot provide the scratch buffer
+ * spx_spmv_csr takes.  The pages have no counterpart; it is a deployment aid.
+ *
+ * Same operation, kernels and result as spx_spmv_csr (bitwise); the partial
+ * sums of split rows go to one fixed device array inside this library
+ * instead: SPX_NOALLOC_MAX_SLOTS floats (256 KiB), held by every GPU that
+ * loads the library until the process exits.  The caller still provides the
+ * plan (uploaded), the matrix, x and y.  No call allocates: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *   - A plan needing more than SPX_NOALLOC_MAX_SLOTS partial sums (split-row
+ *     segments; spx_plan_info_t.slots) is rejected with
+ *     SPX_ERR_SCRATCH_LIMIT before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each slot is written before it is read within a call,
+ *     so nothing needs clearing.  Calls that overlap in time on the GPU
+ *     (different streams, no ordering between them) race on the array and
+ *     give wrong results; order them on one stream or with events.
+ */
+#define SPX_NOALLOC_MAX_SLOTS 65536
+spx_status spx_spmv_csr_noalloc(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                                const int32_t* col, const float* val, float alpha, const float* x, float beta,
+                                float* y, spx_stream_t stream);
 
 /* ------------------------------------------------------------ SpMM */
 
