@@ -6,48 +6,68 @@
 // and a multi-stage pipeline.  [AsyncSparse] §3 gives a Hopper design
 // (warp-specialised TMA producer, WGMMA consumers, full/empty mbarrier ring);
 // this kernel keeps the ring and the producer/consumer split and maps them to
-// Blackwell: one elected thread issues tcgen05.mma into a TMEM accumulator and
-// tcgen05.commit frees each stage, so no warpgroup holds accumulators in
-// registers.  Non-persistent grid (one CTA per (n-tile, block-row)), as
-// [AsyncSparse] §5.2 settles on for sparse work.
+// Blackwell: one thread issues tcgen05.mma into a TMEM accumulator,
+// tcgen05.commit frees each stage, and the accumulator lives in TMEM, so no
+// warpgroup holds it in registers.
 //
-// Tile: a 64-row block-row and 128 output columns.  The MMA computes the
-// transposed tile  D[n, r] += B[J*64 + k, n0 + n] * Ablk[r, k]  with
+// Tile: a 64-row block-row I and 256 output columns.  Each MMA computes a
+// transposed half tile  D[n, r] += B[J*64 + k, n0 + n] * Ablk[r, k]  with
 // M = 128 (n), N = 64 (r), K = 16: B's tile is the A operand in MN-major form
 // (n contiguous, exactly as B is stored) and the A block is the B operand in
 // K-major form (k contiguous, as BSR stores a row-major block).  Both arrive
-// by 2-D TMA with the 128-byte swizzle.  The accumulator D (128 lanes x 64
-// fp32 columns) is read back with tcgen05.ld: lane n holds C[I*64 + r, n0 + n]
-// for r = 0..63, so each warp stores 128 contiguous bytes per r.
+// by 2-D TMA with the 128-byte swizzle.  A 256-column tile halves the L2->SM
+// re-reads of the A blocks compared with 128 columns; L2->SM bandwidth, not the
+// tensor pipe, bounds this product (every B tile is read once per block-row
+// that uses its block column).
+//
+// Persistent CTAs (one per SM) walk a static tile schedule.  Warps 0..4 are TMA
+// producers, each owning one stage of the ring (one thread cannot issue TMA
+// fast enough to keep one SM fed: a single producer thread measured ~1/3 of
+// the L2->SM rate that several reach); within a stage, five lanes issue the A
+// block and the four B boxes at once.  Warp 5 issues the MMAs, warps 6..9 run
+// the epilogue.  The TMEM
+// accumulator is double-buffered (2 x 128 columns): while the epilogue drains
+// tile i (tcgen05.ld -> coalesced fp32 stores), the MMA warp accumulates tile
+// i+1.  The schedule is static and each tile costs its block-row's block count;
+// for a balanced pattern (equal blocks per block-row) the tail is under one
+// tile per CTA.
 //
 // Every mbarrier wait is bounded (clock64); on expiry the CTA records an error
 // word (read by spx_last_device_error), stops issuing, waits (bounded) for
-// its copies in flight, frees its TMEM and exits.
+// its copies and MMAs in flight, frees its TMEM and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "spx_internal.h"
 
 namespace {
 
-constexpr int kBlk = 64;                  // BSR block edge (rows = cols)
-constexpr int kTileN = 128;               // output columns per CTA = MMA M
-constexpr int kStages = 4;                // smem ring depth
-constexpr int kThreads = 128;             // 4 warps: producer, MMA issuer, all four in the epilogue
-constexpr uint32_t kABytes = kBlk * kBlk * 2;          // one bf16 A block, 8 KB
-constexpr uint32_t kBHalf = kBlk * 64 * 2;             // 64 k-rows x 64 n, 8 KB (one TMA box)
-constexpr uint32_t kStageBytes = kABytes + 2 * kBHalf; // 24 KB
-constexpr uint32_t kTmemCols = 64;
-constexpr size_t kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kBlk = 64;                                // BSR block edge (rows = cols)
+constexpr int kTileN = 256;                             // output columns per tile
+constexpr int kHalves = kTileN / 128;                   // M = 128 MMA halves per tile
+constexpr int kBoxes = kTileN / 64;                     // 64-column TMA boxes of B per stage
+constexpr int kStages = 5;                              // smem ring depth
+constexpr int kProducers = kStages;                     // producer warps; warp p owns ring stage p
+constexpr int kMmaWarp = kProducers;                    // the MMA-issuing warp
+constexpr int kEpiWarp0 = kProducers + 1;               // first of the 4 epilogue warps
+constexpr int kThreads = 32 * (kProducers + 1 + 4);
+constexpr uint32_t kABytes = kBlk * kBlk * 2;           // one bf16 A block, 8 KB
+constexpr uint32_t kBBox = kBlk * 64 * 2;               // 64 k-rows x 64 n, 8 KB
+constexpr uint32_t kStageBytes = kABytes + kBoxes * kBBox;  // 40 KB
+constexpr uint32_t kAccCols = kHalves * 64;             // TMEM columns of one accumulator
+constexpr uint32_t kTmemCols = 2 * kAccCols;            // double-buffered: 256
+constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
 // kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits 7, 10),
 // A MN-major (bit 15), B K-major (bit 16 = 0), N = 64 (bits 17-22, N>>3),
 // M = 128 (bits 24-28, M>>4).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s): only a broken pipeline reaches it
 
-enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
+enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4, kErrTmemEmpty = 5 };
 
 __device__ int g_bsr_error;
 
@@ -140,29 +160,233 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_bsr_error,
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                       long long ldc, long long spin_limit) {
+                       long long ldc, int N, int ntiles, int ntq, long long spin_limit) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ uint32_t s_issued_by[kProducers], s_consumed;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB alignment for the 128-byte swizzle atoms
+    const uint32_t bars = base + kStages * kStageBytes;
+    auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (kStages + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };
+    const uint32_t fin_bar = bars + 8u * (2 * kStages + 4);
+    auto stage_a = [&](uint32_t s) { return base + s * kStageBytes; };
+    auto stage_b = [&](uint32_t s) { return base + s * kStageBytes + kABytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);  // one arrive per epilogue warp
+        }
+        mbar_init(fin_bar, 1);
+        s_abort = 0;
+        for (int p = 0; p < kProducers; ++p) s_issued_by[p] = 0;
+        s_consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp < kProducers) {
+        // ---------------- producers: warp p fills ring stage p for the ring positions g = p (mod kStages)
+        const uint32_t s = static_cast<uint32_t>(warp);
+        uint32_t G0 = 0, mine = 0;  // G0: ring position of the current tile's first block
+        for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+            const int I = t / ntq, n0 = (t % ntq) * kTileN;
+            const int nbox = min(kBoxes, (N - n0) / 64);  // 4, or 2 for a 128-wide last tile
+            const int b0 = __ldg(brp + I), nb = __ldg(brp + I + 1) - b0;
+            bool stop = false;
+            for (int b = static_cast<int>((s + kStages - G0 % kStages) % kStages); b < nb; b += kStages) {
+                const uint32_t g = G0 + static_cast<uint32_t>(b);
+                const uint32_t ph = (g / kStages) & 1u;
+                int ok = 1;
+                if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) record_error(kErrEmpty);
+                    s_abort = 1;
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) mbar_expect_tx(full_bar(s), kABytes + nbox * kBBox);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
+                } else if (lane <= nbox) {
+                    const int J = __ldg(bcol + b0 + b);
+                    tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
+                }
+                __syncwarp();
+                mine = g + 1;
+            }
+            if (stop) break;
+            G0 += static_cast<uint32_t>(nb);
+        }
+        if (lane == 0) s_issued_by[warp] = mine;  // 1 + the last ring position this warp filled (0: none)
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            uint32_t g = 0;
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int buf = i & 1;
+                const uint32_t use = static_cast<uint32_t>(i >> 1);
+                const int I = t / ntq;
+                const int nh = min(kHalves, (N - (t % ntq) * kTileN) / 128);
+                const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+                if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, spin_limit)) {
+                    record_error(kErrTmemEmpty);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * kAccCols;
+                bool ok = true;
+                for (int b = 0; b < nb; ++b, ++g) {
+                    const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, spin_limit)) {
+                        record_error(kErrFull);
+                        s_abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int h = 0; h < nh; ++h)
+#pragma unroll
+                        for (int ks = 0; ks < kBlk / 16; ++ks) {
+                            // A operand: B's tile, MN-major; half h = TMA boxes 2h, 2h+1 (LBO 8 KB);
+                            // 16 k-rows = two 8-row swizzle atoms (SBO 1 KB).
+                            const uint64_t adesc = sw128_desc(stage_b(s) + 2 * h * kBBox + ks * 2048u, kBBox, 1024u);
+                            // B operand: the A block, K-major; 16 k = 32 bytes inside each 128-byte row.
+                            const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
+                            mma_bf16(d + h * 64, adesc, bdesc, (b > 0 || ks > 0) ? 1u : 0u);
+                        }
+                    mma_commit(empty_bar(s));
+                }
+                if (nb > 0) mma_commit(tfull_bar(buf));  // arrives when this tile's MMAs complete
+                else mbar_arrive(tfull_bar(buf));
+                if (!ok) break;
+            }
+            s_consumed = g;
+        }
+    } else {
+        // ---------------- epilogue warps 6..9: TMEM lane quarter (warp % 4) -> 32 output columns per half
+        const int quarter = warp & 3;
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int buf = i & 1;
+            const uint32_t use = static_cast<uint32_t>(i >> 1);
+            const int I = t / ntq, n0 = (t % ntq) * kTileN;
+            const int nh = min(kHalves, (N - n0) / 128);
+            const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(tfull_bar(buf), use & 1u, spin_limit) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) record_error(kErrAcc);
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            for (int h = 0; h < nh; ++h) {
+                float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + h * 128 + 32 * quarter + lane;
+                if (nb == 0) {
+                    for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, 0.f);
+                    continue;
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < kBlk; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kAccCols + h * 64 + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcs(cp + static_cast<long long>(c0 + j) * ldc, __uint_as_float(v[j]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort) {
+        if (warp < kProducers && lane == 0) {
+            // this warp's copies issued but never consumed: wait (bounded) until they have landed
+            const uint32_t last = s_issued_by[warp];
+            if (last > s_consumed && !mbar_wait(full_bar(warp), ((last - 1) / kStages) & 1u, spin_limit))
+                record_error(kErrDrain);
+        } else if (warp == kMmaWarp && lane == 0) {
+            // MMAs in flight: one more commit, then wait (bounded) for it
+            mma_commit(fin_bar);
+            if (!mbar_wait(fin_bar, 0, spin_limit)) record_error(kErrDrain);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ---------------------------------------------------------------- tile variant
+// Non-persistent: one CTA per (128-column tile, block-row), one TMA thread,
+// one MMA thread, four epilogue warps, a STAGES-deep ring of {A block 8 KB,
+// B tile 16 KB}.  Several CTAs share an SM (smem-bound), each an independent
+// load/MMA pipeline, so one pipeline's hand-off latency is covered by the others.
+constexpr int kTThreads = 128;
+constexpr uint32_t kTStageBytes = kABytes + 2 * kBBox;  // 24 KB
+constexpr uint32_t kTTmemCols = 64;
+
+template <int STAGES>
+constexpr size_t tile_smem_bytes() { return STAGES * kTStageBytes + 1024 + 256; }
+
+template <int STAGES>
+__global__ void __launch_bounds__(kTThreads)
+    bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
+                         long long ldc, long long spin_limit) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ int s_issued, s_consumed;
 
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // 1 KB alignment for the 128-byte swizzle atoms
-    const uint32_t bars = base + kStages * kStageBytes;
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bars = base + STAGES * kTStageBytes;
     auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-    const uint32_t acc_bar = bars + 16u * kStages;
-    auto stage_a = [&](int s) { return base + s * kStageBytes; };
-    auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    const uint32_t acc_bar = bars + 16u * STAGES;
+    auto stage_a = [&](int s) { return base + s * kTStageBytes; };
+    auto stage_b = [&](int s) { return base + s * kTStageBytes + kABytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
+    const int n0 = blockIdx.x * 128;
     const int I = blockIdx.y;
     const int b0 = __ldg(brp + I);
     const int nblk = __ldg(brp + I + 1) - b0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -175,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(kTmemCols)
+                     "r"(kTTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -185,30 +409,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_d = s_tmem;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- producer: one TMA thread feeds the ring
         int b = 0;
         for (; b < nblk; ++b) {
-            const int s = b % kStages;
-            const uint32_t ph = (b / kStages) & 1u;
-            if (!mbar_wait(empty_bar(s), ph ^ 1u, spin_limit)) {
+            const int s = b % STAGES;
+            const uint32_t ph = (b / STAGES) & 1u;
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) || s_abort) {
                 record_error(kErrEmpty);
                 s_abort = 1;
                 break;
             }
-            if (s_abort) break;
-            mbar_expect_tx(full_bar(s), kStageBytes);
+            mbar_expect_tx(full_bar(s), kTStageBytes);
             const int J = __ldg(bcol + b0 + b);
             tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
             tma_load_2d(stage_b(s), &tmB, n0, J * kBlk, full_bar(s));
-            tma_load_2d(stage_b(s) + kBHalf, &tmB, n0 + 64, J * kBlk, full_bar(s));
+            tma_load_2d(stage_b(s) + kBBox, &tmB, n0 + 64, J * kBlk, full_bar(s));
         }
         s_issued = b;
     } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
         int b = 0;
         for (; b < nblk; ++b) {
-            const int s = b % kStages;
-            const uint32_t ph = (b / kStages) & 1u;
+            const int s = b % STAGES;
+            const uint32_t ph = (b / STAGES) & 1u;
             if (!mbar_wait(full_bar(s), ph, spin_limit)) {
                 record_error(kErrFull);
                 s_abort = 1;
@@ -217,30 +438,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < kBlk / 16; ++ks) {
-                // A operand: B's tile, MN-major; 16 k-rows = two 8-row swizzle atoms (SBO 1 KB);
-                // the two 64-column halves are the two TMA boxes (LBO 8 KB).
-                const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBHalf, 1024u);
-                // B operand: the A block, K-major; 16 k = 32 bytes inside each 128-byte row.
+                const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
                 const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
                 mma_bf16(tmem_d, adesc, bdesc, (b > 0 || ks > 0) ? 1u : 0u);
             }
             mma_commit(empty_bar(s));
         }
         s_consumed = b;
-        if (b > 0) mma_commit(acc_bar);  // arrives once every issued MMA has completed
+        if (b > 0) mma_commit(acc_bar);
         else mbar_arrive(acc_bar);
     }
     __syncwarp();
 
-    // ---------------- epilogue: TMEM -> registers -> C (each warp its 32 lanes)
-    const bool acc_ok = mbar_wait(acc_bar, 0, spin_limit);
-    if (!acc_ok) record_error(kErrAcc);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(acc_bar, 0, spin_limit) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) record_error(kErrAcc);
     tc_fence_after();
-    const int n = 32 * warp + lane;
-    float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + n;
+    float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 32 * warp + lane;
     if (nblk == 0) {
         for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, 0.f);
-    } else if (acc_ok && !s_abort) {
+    } else if (ok && !s_abort) {
 #pragma unroll
         for (int c0 = 0; c0 < kBlk; c0 += 32) {
             uint32_t v[32];
@@ -253,15 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (s_abort && threadIdx.x == 0) {
-        // copies issued but never consumed: wait (bounded) until they have landed
         for (int b = s_consumed; b < s_issued; ++b)
-            if (!mbar_wait(full_bar(b % kStages), (b / kStages) & 1u, spin_limit)) {
+            if (!mbar_wait(full_bar(b % STAGES), (b / STAGES) & 1u, spin_limit)) {
                 record_error(kErrDrain);
                 break;
             }
     }
     __syncthreads();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols) : "memory");
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTTmemCols) : "memory");
 }
 
 // ------------------------------------------------------------ host side
@@ -292,8 +510,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
     cuuint64_t strides[1] = {pitch_bytes};
     cuuint32_t box[2] = {64, 64};
     cuuint32_t estr[2] = {1, 1};
+#ifndef SPX_BSR_L2_PROMOTION
+#define SPX_BSR_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, SPX_BSR_L2_PROMOTION,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -306,8 +527,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         float* C, int64_t ldc, spx_stream_t stream) {
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
     if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % kTileN) return SPX_ERR_UNSUPPORTED;
-    if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
+    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % 128) return SPX_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return SPX_OK;
     if (!bsr_row_ptr || !C || (nnzb > 0 && (!bsr_col || !bsr_val || !B))) return SPX_ERR_ARG;
     if (ldb < N || ldc < N) return SPX_ERR_ARG;
@@ -324,15 +544,57 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
         !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
         return SPX_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(bsr_spmm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes));
-    });
-    if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
-    dim3 grid(N / kTileN, M / kBlk);
-    bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, kSpinLimit);
+    // Variant: "tileS" = non-persistent 128-column tiles with an S-deep ring
+    // (S = 2..5; smaller rings fit more CTAs per SM), "persistent" = the
+    // persistent 256-column kernel.  SPX_BSR_VARIANT overrides the default.
+    static int variant = -1;
+    if (variant < 0) {
+        variant = 3;
+        if (const char* v = std::getenv("SPX_BSR_VARIANT")) {
+            if (!std::strcmp(v, "persistent")) variant = 0;
+            else if (!std::strncmp(v, "tile", 4) && v[4] >= '2' && v[4] <= '5' && v[5] == 0) variant = v[4] - '0';
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    if (variant == 0) {
+        static std::once_flag attr_once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(attr_once, [] {
+            attr_err = cudaFuncSetAttribute(bsr_spmm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemBytes));
+        });
+        if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
+        static int nsm = 0;
+        if (nsm == 0) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return SPX_ERR_CUDA;
+        }
+        const int ntq = (N + kTileN - 1) / kTileN;
+        const long long tiles = static_cast<long long>(M / kBlk) * ntq;
+        if (tiles > kI32Max) return SPX_ERR_INDEX_RANGE;
+        const int grid = static_cast<int>(tiles < nsm ? tiles : nsm);
+        bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, N,
+                                                               static_cast<int>(tiles), ntq, kSpinLimit);
+    } else {
+        if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
+        dim3 grid(N / 128, M / kBlk);
+        switch (variant) {
+#define SPX_TILE(S)                                                                                             \
+    case S: {                                                                                                   \
+        static cudaError_t ae = cudaFuncSetAttribute(bsr_spmm_tile_kernel<S>,                                   \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,               \
+                                                     static_cast<int>(tile_smem_bytes<S>()));                   \
+        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                             \
+        bsr_spmm_tile_kernel<S><<<grid, kTThreads, tile_smem_bytes<S>(), st>>>(tmA, tmB, bsr_row_ptr, bsr_col, \
+                                                                               C, ldc, kSpinLimit);             \
+        break;                                                                                                  \
+    }
+            SPX_TILE(2) SPX_TILE(3) SPX_TILE(4) SPX_TILE(5)
+#undef SPX_TILE
+        }
+    }
+    (void)e;
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }

@@ -94,20 +94,26 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
     const float* Bc = B + n0;
     int p = a;
-    for (; p + 3 < b; p += 4) {
-        const int c0 = ld_stream(col + p), c1 = ld_stream(col + p + 1), c2 = ld_stream(col + p + 2),
-                  c3 = ld_stream(col + p + 3);
-        const float v0 = ld_stream(val + p), v1 = ld_stream(val + p + 1), v2 = ld_stream(val + p + 2),
-                    v3 = ld_stream(val + p + 3);
+#ifndef SPX_SPMM_UNROLL
+#define SPX_SPMM_UNROLL 8
+#endif
+    constexpr int U = SPX_SPMM_UNROLL;  // B-row loads in flight per lane
+    for (; p + U - 1 < b; p += U) {
+        int c[U];
+        float v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            c[j] = ld_stream(col + p + j);
+            v[j] = ld_stream(val + p + j);
+        }
         if (live) {
-            const float4 b0 = ld_keep(Bc + (long long)c0 * ldb, pol);
-            const float4 b1 = ld_keep(Bc + (long long)c1 * ldb, pol);
-            const float4 b2 = ld_keep(Bc + (long long)c2 * ldb, pol);
-            const float4 b3 = ld_keep(Bc + (long long)c3 * ldb, pol);
-            acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
-            acc.x += v1 * b1.x; acc.y += v1 * b1.y; acc.z += v1 * b1.z; acc.w += v1 * b1.w;
-            acc.x += v2 * b2.x; acc.y += v2 * b2.y; acc.z += v2 * b2.z; acc.w += v2 * b2.w;
-            acc.x += v3 * b3.x; acc.y += v3 * b3.y; acc.z += v3 * b3.z; acc.w += v3 * b3.w;
+            float4 bv[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) bv[j] = ld_keep(Bc + (long long)c[j] * ldb, pol);
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
+            }
         }
     }
     for (; p < b; ++p) {
