@@ -423,7 +423,17 @@ spx_status spx_plan_opts_default(spx_plan_opts_t* o) {
     o->pack_max = 512;
     o->cta_max = 8192;
     o->seg_nnz = 4096;
-    o->lanes_div = 0;
+    o->lanes_div = 4;
+    return SPX_OK;
+}
+
+spx_status spx_plan_opts_auto(const spx_row_stats_t* st, spx_plan_opts_t* o) {
+    if (!st || !o) return SPX_ERR_ARG;
+    spx_plan_opts_default(o);
+    if (st->cv >= 2.0) {
+        o->block_nnz = 1024;
+        o->lanes_div = 0;
+    }
     return SPX_OK;
 }
 
@@ -433,11 +443,6 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     *plan_out = nullptr;
     if (M < 0 || K < 0 || nnz < 0 || !row_ptr) return SPX_ERR_ARG;
     if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
-    spx_plan_opts_t o;
-    if (opts) o = *opts; else spx_plan_opts_default(&o);
-    if (o.block_nnz < 1 || o.block_rows < 1 || o.pack_max < 0 || o.pack_max > o.block_nnz || o.cta_max < o.pack_max ||
-        o.seg_nnz < 1 || o.lanes_div < 0 || o.block_nnz > 8192 || o.block_rows > 1024)
-        return SPX_ERR_ARG;
     std::vector<int32_t> rp_h;
     const int32_t* rp = row_ptr;
     if (where == SPX_DEVICE) {
@@ -447,17 +452,31 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     } else if (where != SPX_HOST) {
         return SPX_ERR_ARG;
     }
-    spx_status s = check_rp(M, nnz, rp);
-    if (s != SPX_OK) return s;
+    {
+        spx_status s = check_rp(M, nnz, rp);
+        if (s != SPX_OK) return s;
+    }
+    spx_row_stats_t stats;
+    try {
+        row_stats_host(M, rp, &stats);
+    } catch (const std::bad_alloc&) {
+        return SPX_ERR_NOMEM;
+    }
+    spx_plan_opts_t o;
+    if (opts) o = *opts; else spx_plan_opts_auto(&stats, &o);
+    if (o.block_nnz < 1 || o.block_rows < 1 || o.pack_max < 0 || o.pack_max > o.block_nnz || o.cta_max < o.pack_max ||
+        o.seg_nnz < 1 || o.lanes_div < 0 || o.block_nnz > 8192 || o.block_rows > 1024)
+        return SPX_ERR_ARG;
+    spx_status s = SPX_OK;
     spx_plan* P = new (std::nothrow) spx_plan();
     if (!P) return SPX_ERR_NOMEM;
     P->M = M;
     P->K = K;
     P->nnz = nnz;
     P->opts = o;
+    P->stats = stats;
     try {
         s = make_plan(P, rp);
-        if (s == SPX_OK) row_stats_host(M, rp, &P->stats);
     } catch (const std::bad_alloc&) {
         s = SPX_ERR_NOMEM;
     }

@@ -32,7 +32,7 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // fix-up kernel
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -45,7 +45,8 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Sum of v over the CTA in a fixed order; result valid in thread 0.
+// Sum of v over the CTA (NT threads) in a fixed order; result valid in thread 0.
+template <int NT>
 __device__ __forceinline__ float block_sum(float v, float* red) {
     v = warp_sum(v);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -53,29 +54,30 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     __syncthreads();
     float s = 0.f;
     if (warp == 0) {
-        s = lane < kWarps ? red[lane] : 0.f;
+        s = lane < NT / 32 ? red[lane] : 0.f;
         s = warp_sum(s);
     }
     return s;
 }
 
 // Strided dot product of the nonzero range [a, b) with x; 4 gathers in flight per thread.
+template <int NT>
 __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__ col, const float* __restrict__ val,
                                            const float* __restrict__ x) {
     float s = 0.f;
     int p = a + threadIdx.x;
-    for (; p + 3 * kThreads < b; p += 4 * kThreads) {
-        int c0 = ld_stream(col + p), c1 = ld_stream(col + p + kThreads);
-        int c2 = ld_stream(col + p + 2 * kThreads), c3 = ld_stream(col + p + 3 * kThreads);
-        float v0 = ld_stream(val + p), v1 = ld_stream(val + p + kThreads);
-        float v2 = ld_stream(val + p + 2 * kThreads), v3 = ld_stream(val + p + 3 * kThreads);
+    for (; p + 3 * NT < b; p += 4 * NT) {
+        int c0 = ld_stream(col + p), c1 = ld_stream(col + p + NT);
+        int c2 = ld_stream(col + p + 2 * NT), c3 = ld_stream(col + p + 3 * NT);
+        float v0 = ld_stream(val + p), v1 = ld_stream(val + p + NT);
+        float v2 = ld_stream(val + p + 2 * NT), v3 = ld_stream(val + p + 3 * NT);
         float x0 = __ldg(x + c0), x1 = __ldg(x + c1), x2 = __ldg(x + c2), x3 = __ldg(x + c3);
         s += v0 * x0;
         s += v1 * x1;
         s += v2 * x2;
         s += v3 * x3;
     }
-    for (; p < b; p += kThreads) s += ld_stream(val + p) * __ldg(x + ld_stream(col + p));
+    for (; p < b; p += NT) s += ld_stream(val + p) * __ldg(x + ld_stream(col + p));
     return s;
 }
 
@@ -99,8 +101,8 @@ __device__ __forceinline__ void emit_g(float* y, const float* s_y, int r0, int r
 __device__ __forceinline__ int sk(int k) { return k + (k >> 5); }
 
 // Products val[p0+k] * x[col[p0+k]], k < n, into s_prod[sk(k)] (coalesced layout);
-// ITEMS = block_nnz / kThreads as a compile-time case, 0 = runtime loop.
-template <int ITEMS>
+// ITEMS = block_nnz / NT as a compile-time case, 0 = runtime loop.
+template <int NT, int ITEMS>
 __device__ __forceinline__ void stage_products(int p0, int n, const int* __restrict__ col,
                                                const float* __restrict__ val, const float* __restrict__ x,
                                                float* s_prod) {
@@ -109,27 +111,28 @@ __device__ __forceinline__ void stage_products(int p0, int n, const int* __restr
         float v[ITEMS > 0 ? ITEMS : 1];
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
-            const int k = threadIdx.x + j * kThreads;
+            const int k = threadIdx.x + j * NT;
             c[j] = k < n ? ld_stream(col + p0 + k) : 0;
             v[j] = k < n ? ld_stream(val + p0 + k) : 0.f;
         }
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
-            const int k = threadIdx.x + j * kThreads;
+            const int k = threadIdx.x + j * NT;
             if (k < n) s_prod[sk(k)] = v[j] * __ldg(x + c[j]);
         }
     } else {
-        for (int k = threadIdx.x; k < n; k += kThreads)
+        for (int k = threadIdx.x; k < n; k += NT)
             s_prod[sk(k)] = ld_stream(val + p0 + k) * __ldg(x + ld_stream(col + p0 + k));
     }
 }
 
 // Lanes mode: each row reduced by w = 2^lg lanes; every lane of a warp runs the same trip count.
+template <int NT>
 __device__ __forceinline__ void reduce_lanes(int r0, int nrows, int lg, const float* s_prod, const int* s_rp,
                                              const float* s_y, float alpha, float beta, float* y) {
     const int w = 1 << lg;
     const int sub = threadIdx.x >> lg, lane = threadIdx.x & (w - 1);
-    const int nsub = kThreads >> lg;
+    const int nsub = NT >> lg;
     for (int base = 0; base < nrows; base += nsub) {
         const int r = base + sub;
         float s = 0.f;
@@ -234,8 +237,8 @@ __device__ __forceinline__ void reduce_segmented(int r0, int nrows, int n, int p
     if (first_ends) emit_g(y, s_y, r0, first_row, (exf ? ex : wp + ex) + first_part, alpha, beta);
 }
 
-template <int ITEMS>
-__global__ void __launch_bounds__(kThreads) spmv_tasks_kernel(const int4* __restrict__ tasks,
+template <int NT, int ITEMS>
+__global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__ tasks,
                                                               const int* __restrict__ rp, const int* __restrict__ col,
                                                               const float* __restrict__ val,
                                                               const float* __restrict__ x, float alpha, float beta,
@@ -248,25 +251,25 @@ __global__ void __launch_bounds__(kThreads) spmv_tasks_kernel(const int4* __rest
         float* s_prod = smem;
         int* s_rp = reinterpret_cast<int*>(smem + block_nnz + block_nnz / 32 + 1);
         float* s_sv = reinterpret_cast<float*>(s_rp + block_rows + 1);
-        int* s_sf = reinterpret_cast<int*>(s_sv + kWarps);
-        float* s_y = reinterpret_cast<float*>(s_sf + kWarps);
+        int* s_sf = reinterpret_cast<int*>(s_sv + (NT / 32));
+        float* s_y = reinterpret_cast<float*>(s_sf + (NT / 32));
         const int code = (t.x >> 2) & 63, nrows = t.x >> 8, r0 = t.y, p0 = t.z, n = t.w - t.z;
-        for (int i = threadIdx.x; i <= nrows; i += kThreads) {
+        for (int i = threadIdx.x; i <= nrows; i += NT) {
             s_rp[i] = __ldg(rp + r0 + i) - p0;
             if (beta != 0.f && i < nrows) s_y[i] = y[r0 + i];
         }
-        stage_products<ITEMS>(p0, n, col, val, x, s_prod);
+        stage_products<NT, ITEMS>(p0, n, col, val, x, s_prod);
         __syncthreads();
         if (code == kReduceSegmented)
-            reduce_segmented<ITEMS>(r0, nrows, n, (block_nnz + kThreads - 1) / kThreads, s_prod, s_rp, s_y, alpha,
+            reduce_segmented<ITEMS>(r0, nrows, n, (block_nnz + NT - 1) / NT, s_prod, s_rp, s_y, alpha,
                                     beta, y, s_sv, s_sf);
         else
-            reduce_lanes(r0, nrows, code, s_prod, s_rp, s_y, alpha, beta, y);
+            reduce_lanes<NT>(r0, nrows, code, s_prod, s_rp, s_y, alpha, beta, y);
     } else {
         // the old y of a CTA row is read up front, off the critical path
         const float y_old = (kind == kTaskCta && beta != 0.f && threadIdx.x == 0) ? y[t.y] : 0.f;
-        float s = range_dot(t.z, t.w, col, val, x);
-        s = block_sum(s, smem);
+        float s = range_dot<NT>(t.z, t.w, col, val, x);
+        s = block_sum<NT>(s, smem);
         if (threadIdx.x == 0) {
             if (kind == kTaskCta) y[t.y] = alpha * s + (beta != 0.f ? beta * y_old : 0.f);
             else partials[t.x >> 8] = s;
@@ -296,20 +299,25 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     const int4* tasks = static_cast<const int4*>(P->d_table);
     const int4* longrows = tasks + ntasks;
     const int B = P->opts.block_nnz, R = P->opts.block_rows;
-    const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) + sizeof(int) * (static_cast<size_t>(R) + 1) +
-                        2 * kWarps * sizeof(float) + sizeof(float) * static_cast<size_t>(R);
+    // Eight products per thread: block_nnz 1024 / 2048 / 4096 runs 128 / 256 /
+    // 512-thread CTAs (smaller CTAs, more of them resident: measured better on
+    // skewed rows); other sizes take the runtime-loop form with 256 threads.
+    const int NT = (B == 1024 || B == 2048 || B == 4096) ? B / 8 : 256;
+    const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) +
+                        sizeof(int) * (static_cast<size_t>(R) + 1) + 2 * (NT / 32) * sizeof(float) +
+                        sizeof(float) * static_cast<size_t>(R);
     switch (B) {
-        case kThreads * 4:
-            spmv_tasks_kernel<4><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+        case 1024:
+            spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
-        case kThreads * 8:
-            spmv_tasks_kernel<8><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+        case 2048:
+            spmv_tasks_kernel<256, 8><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
-        case kThreads * 16:
-            spmv_tasks_kernel<16><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+        case 4096:
+            spmv_tasks_kernel<512, 8><<<ntasks, 512, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         default:
-            spmv_tasks_kernel<0><<<ntasks, kThreads, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<256, 0><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
     }
     uint64_t launches = 1;

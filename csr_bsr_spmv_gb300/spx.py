@@ -78,6 +78,7 @@ def _lib():
             "spx_check_csr": ([i32, i32, i64, vp, vp, i32, ctypes.c_int, vp], ctypes.c_int),
             "spx_row_stats": ([i32, vp, ctypes.c_int, ctypes.POINTER(RowStats)], ctypes.c_int),
             "spx_plan_opts_default": ([ctypes.POINTER(PlanOpts)], ctypes.c_int),
+            "spx_plan_opts_auto": ([ctypes.POINTER(RowStats), ctypes.POINTER(PlanOpts)], ctypes.c_int),
             "spx_plan_csr": ([i32, i32, i64, vp, ctypes.c_int, ctypes.POINTER(PlanOpts), ctypes.POINTER(vp)],
                              ctypes.c_int),
             "spx_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], ctypes.c_int),
@@ -248,6 +249,7 @@ class Plan:
             base = spx_plan_opts_default()
             base.update(opts)
             o = PlanOpts(**base)
+        self.opts_given = dict(opts) if opts else None
         h = ctypes.c_void_p()
         _check(lib.spx_plan_csr(M, K, nnz, _ptr(row_ptr), _where(row_ptr), ctypes.byref(o) if o else None,
                                 ctypes.byref(h)), "spx_plan_csr")

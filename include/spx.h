@@ -157,8 +157,17 @@ typedef struct spx_plan_opts_t {
                            threads are joined by a block scan */
 } spx_plan_opts_t;
 
-/* Fills the defaults the benchmarks were tuned with. */
+/* Fills the fixed defaults: B 2048, R 256, P 512, C 8192, S 4096, D 4. */
 spx_status spx_plan_opts_default(spx_plan_opts_t* out);
+
+/*
+ * Options chosen from a matrix's row statistics (the "dispatch key" of
+ * [SpMM-ops] §4: mean, spread and tail of the row lengths pick the mapping):
+ * cv >= 2 (skewed, power-law-like lengths): B 1024 (128-thread CTAs) and the
+ * segmented reduction (D 0), whose work per thread ignores row length;
+ * otherwise the defaults above (256-thread CTAs, D 4 lanes-per-row rule).
+ */
+spx_status spx_plan_opts_auto(const spx_row_stats_t* stats, spx_plan_opts_t* out);
 
 typedef struct spx_plan_info_t {
     int64_t M, K, nnz;
@@ -189,7 +198,9 @@ typedef struct spx_plan spx_plan; /* opaque, host-side */
  * {2,row,seg,slot} in row order, then groups {256*c, r0, r1, 0} where the
  * reduction code c is log2(w) (lanes per row) or 6 (segmented, D == 0).
  * Long-row table (4 int32 per split row): {row, first slot, #segments, 0}.
- * opts == NULL uses spx_plan_opts_default.  row_ptr is read once (copied to
+ * opts == NULL uses spx_plan_opts_auto of the matrix's statistics.
+ * block_nnz 1024 / 2048 / 4096 runs 128 / 256 / 512-thread CTAs (eight
+ * products per thread); other sizes run 256 threads.  row_ptr is read once (copied to
  * the host when where == SPX_DEVICE).  *plan_out must be released with
  * spx_plan_destroy.
  */

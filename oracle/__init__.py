@@ -65,6 +65,7 @@ def _lib_():
                 "or_build_bsr": [i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp],
                 "or_row_stats": [i32, vp, vp],
                 "or_plan_spmv": [i32, vp, vp, vp, vp, vp],
+                "or_plan_opts_auto": [vp, vp],
                 "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
                 "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
                 "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, vp, i64, vp, vp],
@@ -142,6 +143,16 @@ def row_stats(M, rp):
     st = RowStats()
     _check(_lib_().or_row_stats(M, _p(rp), ctypes.byref(st)))
     return st.as_dict()
+
+
+def plan_opts_auto(M, rp):
+    """Plan options the statistics rule picks for this matrix."""
+    rp = _c(rp, np.int32)
+    st = RowStats()
+    _check(_lib_().or_row_stats(M, _p(rp), ctypes.byref(st)))
+    o = PlanOpts()
+    _check(_lib_().or_plan_opts_auto(ctypes.byref(st), ctypes.byref(o)))
+    return {f: getattr(o, f) for f in PLAN_FIELDS}
 
 
 def plan_spmv(M, rp, **opts):

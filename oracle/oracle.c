@@ -235,6 +235,24 @@ typedef struct {
 
 enum { OR_TASK_GROUP = 0, OR_TASK_CTA = 1, OR_TASK_SEG = 2 };
 
+/*
+ * Plan options from the row statistics ([SpMM-ops] §4: the dispatch key's
+ * row-length spread picks the mapping): with cv >= 2 the groups hold 1024
+ * nonzeros and use the segmented reduction (D = 0); otherwise 2048 nonzeros
+ * and the lanes rule with D = 4.  R 256, P 512, C 8192, S 4096 either way.
+ */
+int or_plan_opts_auto(const or_row_stats_t* st, or_plan_opts_t* o) {
+    if (!st || !o) return OR_ERR_ARG;
+    int skewed = st->cv >= 2.0;
+    o->block_nnz = skewed ? 1024 : 2048;
+    o->block_rows = 256;
+    o->pack_max = 512;
+    o->cta_max = 8192;
+    o->seg_nnz = 4096;
+    o->lanes_div = skewed ? 0 : 4;
+    return OR_OK;
+}
+
 static int32_t pow2ceil_clamp32(int64_t v) {
     int32_t w = 1;
     while (w < v && w < 32) w <<= 1;

@@ -14,7 +14,7 @@ from csr_bsr_spmv_gb300 import spx
 
 def test_exports_every_header_symbol():
     names = spx.header_symbols()
-    assert len(names) >= 20
+    assert len(names) >= 22
     lib = ctypes.CDLL(spx.LIB_PATH)
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
@@ -118,8 +118,11 @@ def test_plan_matches_oracle(opts, seed):
     L, _ = synth.lengths_zipf(seed, 20000, 2.1, 60000, 12.0)
     L[::31] = 0
     rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
-    full = spx.spx_plan_opts_default()
-    full.update(opts or {})
+    if opts is None:
+        full = oracle.plan_opts_auto(L.size, rp)
+    else:
+        full = spx.spx_plan_opts_default()
+        full.update(opts)
     p = spx.spx_plan_csr(L.size, 70000, int(rp[-1]), rp, opts=opts, upload=False)
     tasks, longrows = p.tasks()
     w = oracle.plan_spmv(L.size, rp, **full)
@@ -133,7 +136,28 @@ def test_plan_matches_oracle(opts, seed):
 
 def test_plan_default_options_documented():
     o = spx.spx_plan_opts_default()
-    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=0)
+    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=4)
+
+
+@pytest.mark.parametrize("kind", ["skewed", "uniform", "empty", "constant"])
+def test_plan_auto_options_match_oracle(kind):
+    if kind == "skewed":
+        L, _ = synth.lengths_zipf(3, 50000, 2.1, 100000, 16.0)
+    elif kind == "uniform":
+        L = synth.lengths_uniform(3, 50000, 1, 16)
+    elif kind == "empty":
+        L = np.zeros(100, np.int32)
+    else:
+        L = np.full(1000, 7, np.int32)
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    want = oracle.plan_opts_auto(L.size, rp)
+    lib = spx._lib()
+    st = spx.RowStats()
+    assert lib.spx_row_stats(L.size, spx._ptr(rp), 0, ctypes.byref(st)) == 0
+    o = spx.PlanOpts()
+    assert lib.spx_plan_opts_auto(ctypes.byref(st), ctypes.byref(o)) == 0
+    assert {f: getattr(o, f) for f, _ in spx.PlanOpts._fields_} == want
+    assert want["lanes_div"] == (0 if kind == "skewed" else 4)
 
 
 def test_plan_rejects_bad_rows_and_options():
