@@ -107,13 +107,13 @@ def source_hash(*names):
     return h.hexdigest()[:12]
 
 
-def traffic_from_profile(kernel_key, src_hash):
-    """dram read+write bytes per launch from the committed ncu summary, or None
-    when the kernel source changed since it was captured."""
+def traffic_from_profile(workload, src_hash):
+    """DRAM read+write bytes of the step's dominant kernel from the committed ncu
+    capture for this workload, or None when the kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel_key)
+    d = json.load(open(p)).get(workload)
     if not d or d.get("source_hash") != src_hash:
         return None
     return d.get("dram_bytes_per_launch")
@@ -194,7 +194,6 @@ def run_ours(args, rank, world):
     prep = None
     h2d = d2h = 0
     e2e_run = None
-    kernel_key = None
 
     if w in ("power-law", "uniform"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
@@ -204,7 +203,6 @@ def run_ours(args, rank, world):
         x = to_dev(c["x"])
         y = to_dev(c["y"])
         alpha, beta = c["alpha"], c["beta"]
-        kernel_key = "spmv_tasks_kernel"
         src = source_hash("spx_spmv.cu")
 
         def run():
@@ -227,7 +225,7 @@ def run_ours(args, rank, world):
         info = dict(plan.info)
         extra = {"plan": {k: info[k] for k in ("tasks", "long_rows", "cta_rows", "split_rows", "thread_groups",
                                                 "lane_groups", "segmented_groups")},
-                 "plan_opts": args.plan_opts or "default", "row_stats": plan.stats}
+                 "plan_opts": plan.opts, "row_stats": plan.stats}
     elif w == "dual":
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         t0 = time.perf_counter()
@@ -241,7 +239,6 @@ def run_ours(args, rank, world):
         u = to_dev(c["u0"])
         v = to_dev(c["v0"])
         a, b = float(c["alphas"][0]), float(c["betas"][0])
-        kernel_key = "spmv_tasks_kernel"
         src = source_hash("spx_spmv.cu")
 
         u0, v0 = u.clone(), v.clone()
@@ -267,12 +264,11 @@ def run_ours(args, rank, world):
                 uo.copy_(u, non_blocking=True)
                 vo.copy_(v, non_blocking=True)
 
-        extra = {"plan_A": dict(pA.info), "plan_At": dict(pAt.info)}
+        extra = {"plan_A": dict(pA.info), "plan_At": dict(pAt.info), "plan_opts_A": pA.opts, "plan_opts_At": pAt.opts}
     elif w.startswith("spmm"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         B = to_dev(c["B"])
         C = torch.empty(M, c["N"], device=dev)
-        kernel_key = "spmm_vec_kernel"
         src = source_hash("spx_spmm.cu")
 
         def run():
@@ -297,7 +293,6 @@ def run_ours(args, rank, world):
         d_bval = to_dev(bval.view(np.int16))
         Bm = to_dev(c["B_bf16"].view(np.int16))
         C = torch.empty(M, c["N"], device=dev)
-        kernel_key = "bsr_spmm_tc_kernel"
         src = source_hash("spx_bsr.cu")
 
         def run():
@@ -380,7 +375,7 @@ def run_ours(args, rank, world):
         ach = abytes / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm"], 4), "peak_source": pk["src"] + " (HBM copy)"}
-    tr = traffic_from_profile(kernel_key, src)
+    tr = traffic_from_profile(w, src)
     roof["traffic"] = tr
     roof["algorithmic_bytes"] = int(abytes)
     roof["timed"] = "whole step (all launches of the call), CUDA events on the launching stream"

@@ -506,6 +506,7 @@ spx_status spx_plan_get_info(const spx_plan* P, spx_plan_info_t* out) {
     out->table_bytes = P->table_bytes;
     out->scratch_bytes = P->scratch_bytes;
     out->stats = P->stats;
+    out->opts = P->opts;
     return SPX_OK;
 }
 

@@ -54,7 +54,7 @@ class PlanInfo(ctypes.Structure):
                 ("long_rows", ctypes.c_int64), ("slots", ctypes.c_int64), ("packed_rows", ctypes.c_int64),
                 ("cta_rows", ctypes.c_int64), ("split_rows", ctypes.c_int64), ("thread_groups", ctypes.c_int64),
                 ("lane_groups", ctypes.c_int64), ("segmented_groups", ctypes.c_int64), ("table_bytes", ctypes.c_size_t),
-                ("scratch_bytes", ctypes.c_size_t), ("stats", RowStats)]
+                ("scratch_bytes", ctypes.c_size_t), ("stats", RowStats), ("opts", PlanOpts)]
 
 
 _LIB = None
@@ -257,8 +257,9 @@ class Plan:
         self.M, self.K, self.nnz = M, K, nnz
         info = PlanInfo()
         _check(lib.spx_plan_get_info(h, ctypes.byref(info)), "spx_plan_get_info")
-        self.info = {f: getattr(info, f) for f, _ in PlanInfo._fields_ if f != "stats"}
+        self.info = {f: getattr(info, f) for f, _ in PlanInfo._fields_ if f not in ("stats", "opts")}
         self.stats = info.stats.as_dict()
+        self.opts = {f: getattr(info.opts, f) for f, _ in PlanOpts._fields_}
         self.table = None
         self.scratch = None
         if upload:

@@ -181,6 +181,7 @@ typedef struct spx_plan_info_t {
     size_t table_bytes;    /* device bytes for spx_plan_upload (16-B aligned) */
     size_t scratch_bytes;  /* device scratch bytes each SpMV call needs       */
     spx_row_stats_t stats;
+    spx_plan_opts_t opts;  /* the options the plan was built with             */
 } spx_plan_info_t;
 
 typedef struct spx_plan spx_plan; /* opaque, host-side */
