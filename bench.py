@@ -119,6 +119,24 @@ def traffic_from_profile(workload, src_hash):
     return d.get("dram_bytes_per_launch")
 
 
+def slowest_rank_ms(ms: float, device) -> float:
+    """Max of the per-rank step times over the process group (the job is as
+    slow as its slowest replica); the identity without a group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job GFLOP/s: every replica's work over the slowest replica's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- workloads
 
 def make_workload(name: str, rows: int = 0):
@@ -133,6 +151,11 @@ def make_workload(name: str, rows: int = 0):
         c = synth.banded_pair()
     elif name in ("spmm32", "spmm128"):
         c = synth.clustered_spmm(N=int(name[4:]))
+    elif name in ("spmm32-bf16", "spmm128-bf16"):
+        c = synth.clustered_spmm(N=int(name[4:-5]))
+        c["val_bf16"] = synth.to_bf16_bits(c["val"])
+        c["B_bf16"] = synth.to_bf16_bits(c["B"]).reshape(c["B"].shape)
+        c["name"] += " (bf16 A values and B, fp32 accumulation)"
     elif name == "bsr":
         c = synth.block_sparse()
     else:
@@ -153,6 +176,9 @@ def accounting(c):
         b1 = 8 * nnz + 4 * (M + 1) + 4 * K + 8 * M
         b2 = 8 * nnz + 4 * (K + 1) + 4 * M + 8 * K
         return 4 * nnz, b1 + b2
+    if w.startswith("spmm") and w.endswith("bf16"):
+        N = c["N"]
+        return 2 * nnz * N, 6 * nnz + 4 * (M + 1) + 2 * K * N + 4 * M * N
     if w.startswith("spmm"):
         N = c["N"]
         return 2 * nnz * N, 8 * nnz + 4 * (M + 1) + 4 * K * N + 4 * M * N
@@ -164,6 +190,12 @@ def accounting(c):
 
 
 # ---------------------------------------------------------------- our arm
+
+def synth_bits(val):
+    import synth
+
+    return synth.to_bf16_bits(val).view(np.int16)
+
 
 def run_ours(args, rank, world):
     import torch
@@ -265,6 +297,26 @@ def run_ours(args, rank, world):
                 vo.copy_(v, non_blocking=True)
 
         extra = {"plan_A": dict(pA.info), "plan_At": dict(pAt.info), "plan_opts_A": pA.opts, "plan_opts_At": pAt.opts}
+    elif w.startswith("spmm") and w.endswith("bf16"):
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(synth_bits(val)))
+        B = to_dev(c["B_bf16"].view(np.int16))
+        C = torch.empty(M, c["N"], device=dev)
+        src = source_hash("spx_spmm.cu")
+
+        def run():
+            spx.spx_spmm_csr_bf16(A, B, C, 1.0, 0.0, stream=stream)
+
+        Bh = torch.from_numpy(c["B_bf16"].view(np.int16)).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 2, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                B.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_csr_bf16(A, B, C, 1.0, 0.0, stream=stream)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"variant": "bf16 storage, fp32 accumulation"}
     elif w.startswith("spmm"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         B = to_dev(c["B"])
@@ -340,9 +392,7 @@ def run_ours(args, rank, world):
     ms = sum(times) / len(times)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = slowest_rank_ms(ms, dev)
         dist.barrier()
     torch.cuda.synchronize(dev)
     assert spx.spx_last_device_error(stream) == 0, "device error word set during the timed region"
@@ -366,7 +416,7 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems, 4)}
 
     pk = peaks()
-    gflops = world * flops / (ms * 1e-3) / 1e9
+    gflops = job_throughput(flops, world, ms)
     if w == "bsr":
         ach = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
@@ -383,7 +433,8 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->f32" if w == "bsr" else "f32", "data": "synthetic (seeded SplitMix64)",
+        "vs_baseline": None, "dtype": "bf16->f32" if (w == "bsr" or w.endswith("bf16")) else "f32",
+        "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
                    "N": c.get("N", 1), "l2": "flushed between steps (256 MB write); inputs also exceed L2",
                    "parallelism": f"replicas x{world}"},
@@ -432,6 +483,10 @@ def cpu_step_fn(c):
             oracle.spmv(K, trp, tc, tv, u1.astype(np.float32), 1.0, -float(c["betas"][0]), c["v0"])
         return f, 4 * int(rp[-1]), "the full operator pair, one iteration"
     N = c["N"]
+    if w.endswith("bf16"):
+        import synth
+        val = synth.bf16_bits_to_f32(c["val_bf16"])
+        c = dict(c, B=synth.bf16_bits_to_f32(c["B_bf16"]).reshape(c["B"].shape))
     rows = np.arange(0, M, 16, dtype=np.int32)
     fl = 2 * int(np.diff(rp)[rows].sum()) * N
     return (lambda: oracle.spmm(M, rp, col, val, c["B"], rows=rows)), fl, f"every 16th row ({rows.size} rows)"
@@ -482,7 +537,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
-                    choices=["power-law", "uniform", "dual", "spmm32", "spmm128", "bsr"])
+                    choices=["power-law", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16", "spmm128-bf16", "bsr"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -160,7 +160,7 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_bsr_error,
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                       long long ldc, int N, int ntiles, int ntq, long long spin_limit) {
+                       long long ldc, float alpha, float beta, int N, int ntiles, int ntq, long long spin_limit) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < nh; ++h) {
                 float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + h * 128 + 32 * quarter + lane;
                 if (nb == 0) {
-                    for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, 0.f);
+                    for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
                     continue;
                 }
 #pragma unroll
@@ -319,8 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kAccCols + h * 64 + c0, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        __stcs(cp + static_cast<long long>(c0 + j) * ldc, __uint_as_float(v[j]));
+                    for (int j = 0; j < 32; ++j) {
+                        float* q = cp + static_cast<long long>(c0 + j) * ldc;
+                        const float acc = alpha * __uint_as_float(v[j]);
+                        __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+                    }
                 }
             }
             tc_fence_before();
@@ -364,7 +367,7 @@ template <int STAGES>
 __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                         long long ldc, long long spin_limit) {
+                         long long ldc, float alpha, float beta, long long spin_limit) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(kTThreads)
     tc_fence_after();
     float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 32 * warp + lane;
     if (nblk == 0) {
-        for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, 0.f);
+        for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
     } else if (ok && !s_abort) {
 #pragma unroll
         for (int c0 = 0; c0 < kBlk; c0 += 32) {
@@ -465,7 +468,11 @@ __global__ void __launch_bounds__(kTThreads)
             tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) __stcs(cp + static_cast<long long>(c0 + j) * ldc, __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) {
+                float* q = cp + static_cast<long long>(c0 + j) * ldc;
+                const float acc = alpha * __uint_as_float(v[j]);
+                __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+            }
         }
     }
     tc_fence_before();
@@ -480,6 +487,15 @@ __global__ void __launch_bounds__(kTThreads)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTTmemCols) : "memory");
+}
+
+// C = beta * C (a BSR matrix without stored blocks).
+__global__ void bsr_scale_kernel(float* C, long long ldc, int N, float beta) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c < N) {
+        float* q = C + static_cast<long long>(blockIdx.y) * ldc + c;
+        *q = beta * *q;
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -524,7 +540,7 @@ extern "C" {
 
 spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
-                        float* C, int64_t ldc, spx_stream_t stream) {
+                        float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream) {
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
     if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
     if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % 128) return SPX_ERR_UNSUPPORTED;
@@ -535,10 +551,17 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4))
         return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (nnzb == 0) {
+    if (nnzb == 0 && beta == 0.f) {
         // no stored block: C = 0
         return spx_cuda_status(cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4, 0, static_cast<size_t>(N) * 4,
                                                  static_cast<size_t>(M), st));
+    }
+    if (nnzb == 0) {
+        // no stored block: C = beta * C
+        dim3 grid((N + 255) / 256, M);
+        bsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, N, beta);
+        spx_note_launches(1);
+        return spx_cuda_status(cudaGetLastError());
     }
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
@@ -574,7 +597,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         const long long tiles = static_cast<long long>(M / kBlk) * ntq;
         if (tiles > kI32Max) return SPX_ERR_INDEX_RANGE;
         const int grid = static_cast<int>(tiles < nsm ? tiles : nsm);
-        bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, N,
+        bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, N,
                                                                static_cast<int>(tiles), ntq, kSpinLimit);
     } else {
         if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
@@ -587,7 +610,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                                                      static_cast<int>(tile_smem_bytes<S>()));                   \
         if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                             \
         bsr_spmm_tile_kernel<S><<<grid, kTThreads, tile_smem_bytes<S>(), st>>>(tmA, tmB, bsr_row_ptr, bsr_col, \
-                                                                               C, ldc, kSpinLimit);             \
+                                                                               C, ldc, alpha, beta, kSpinLimit); \
         break;                                                                                                  \
     }
             SPX_TILE(2) SPX_TILE(3) SPX_TILE(4) SPX_TILE(5)

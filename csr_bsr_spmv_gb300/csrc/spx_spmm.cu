@@ -134,6 +134,76 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
     __stcs(cp, r);  // C is written once: evict-first
 }
 
+// ------------------------------------------------------------- bf16 storage, fp32 accumulation
+// Same mapping as spmm_vec_kernel with A's values and B stored as bf16
+// ([SpMM-ops] §5: storage and accumulation precision kept apart; halving B
+// halves the gathered bytes, the term that dominates SpMM).  A lane loads 4
+// bf16 of a B row (8 bytes) and widens them exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint2 ld_keep8(const uint16_t* p, uint64_t pol) {
+    uint2 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
+    return v;
+}
+
+template <int L>
+__global__ void __launch_bounds__(kThreads) spmm_vec_bf16_kernel(int M, int N, const int* __restrict__ rp,
+                                                                 const int* __restrict__ col,
+                                                                 const uint16_t* __restrict__ val,
+                                                                 const uint16_t* __restrict__ B, long long ldb,
+                                                                 float alpha, float beta, float* C, long long ldc) {
+    constexpr int RPW = 32 / L;
+    const int lane = threadIdx.x & 31;
+    const int row = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW + lane / L;
+    const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
+    if (row >= M) return;
+    const bool live = n0 < N;
+    const uint64_t pol = l2_evict_last_policy();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    const uint16_t* Bc = B + n0;
+    constexpr int U = SPX_SPMM_UNROLL;
+    int p = a;
+    for (; p + U - 1 < b; p += U) {
+        int c[U];
+        float v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            c[j] = ld_stream(col + p + j);
+            v[j] = __uint_as_float(static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(val + p + j))) << 16);
+        }
+        if (live) {
+            uint2 bv[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) bv[j] = ld_keep8(Bc + (long long)c[j] * ldb, pol);
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                acc.x += v[j] * bf16_lo(bv[j].x); acc.y += v[j] * bf16_hi(bv[j].x);
+                acc.z += v[j] * bf16_lo(bv[j].y); acc.w += v[j] * bf16_hi(bv[j].y);
+            }
+        }
+    }
+    for (; p < b; ++p) {
+        const int c0 = ld_stream(col + p);
+        const float v0 = __uint_as_float(static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(val + p))) << 16);
+        if (live) {
+            const uint2 b0 = ld_keep8(Bc + (long long)c0 * ldb, pol);
+            acc.x += v0 * bf16_lo(b0.x); acc.y += v0 * bf16_hi(b0.x);
+            acc.z += v0 * bf16_lo(b0.y); acc.w += v0 * bf16_hi(b0.y);
+        }
+    }
+    if (!live) return;
+    float4* cp = reinterpret_cast<float4*>(C + (long long)row * ldc + n0);
+    float4 r = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
+    if (beta != 0.f) {
+        const float4 o = *cp;
+        r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
+    }
+    __stcs(cp, r);
+}
+
 // ------------------------------------------------------------- scalar fallback
 __global__ void __launch_bounds__(kThreads) spmm_scalar_kernel(int M, int N, const int* __restrict__ rp,
                                                                const int* __restrict__ col,
@@ -177,6 +247,14 @@ void launch_vec(int M, int N, const int* rp, const int* col, const float* val, c
     constexpr int rows_per_cta = kWarps * (32 / L);
     dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
     spmm_vec_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+}
+
+template <int L>
+void launch_vec_bf16(int M, int N, const int* rp, const int* col, const uint16_t* val, const uint16_t* B, long long ldb,
+                     float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
+    constexpr int rows_per_cta = kWarps * (32 / L);
+    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
+    spmm_vec_bf16_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
 }
 
 spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
@@ -228,6 +306,30 @@ spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, co
                         int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
                         spx_stream_t stream) {
     return spmm_impl(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
+                             const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                             float* C, int64_t ldc, spx_stream_t stream) {
+    if (M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
+    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (N % 4 || ldb % 4 || ldc % 4) return SPX_ERR_UNSUPPORTED;
+    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 2) || !spx_aligned(B, 8) ||
+        !spx_aligned(C, 16))
+        return SPX_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (auto_col_tile(N)) {
+        case 8: launch_vec_bf16<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 16: launch_vec_bf16<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 32: launch_vec_bf16<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 64: launch_vec_bf16<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        default: launch_vec_bf16<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+    }
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
 }
 
 spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,

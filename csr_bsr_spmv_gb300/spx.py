@@ -92,7 +92,8 @@ def _lib():
             "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_spmm_csr_tiled": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, i32, vp], ctypes.c_int),
             "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
-            "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
@@ -358,18 +359,29 @@ def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, b
     return C
 
 
+def spx_spmm_csr_bf16(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha*A*B + beta*C with A.val and B holding bf16 bit patterns (int16 tensors), C fp32."""
+    N = B.shape[1]
+    assert B.stride(1) == 1 and C.stride(1) == 1 and A.val.element_size() == 2 and B.element_size() == 2
+    _check(_lib().spx_spmm_csr_bf16(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
+                                    B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
+           "spx_spmm_csr_bf16")
+    return C
+
+
 def spx_spmm_csr_variant(B: torch.Tensor, C: torch.Tensor) -> str:
     v = _lib().spx_spmm_csr_variant(B.shape[1], _ptr(B), B.stride(0), _ptr(C), C.stride(0))
     return SPMM_VARIANTS[v]
 
 
 def spx_spmm_bsr(M: int, K: int, br: int, bc: int, bsr_row_ptr, bsr_col, bsr_val, B: torch.Tensor,
-                 C: torch.Tensor, stream=None):
-    """C <- A*B, A BSR (bf16 blocks held as int16/uint16 bit patterns or bfloat16), B bf16, C fp32."""
+                 C: torch.Tensor, stream=None, alpha: float = 1.0, beta: float = 0.0):
+    """C <- alpha*A*B + beta*C, A BSR (bf16 blocks held as int16 bit patterns or bfloat16), B bf16, C fp32."""
     nnzb = bsr_col.numel()
     N = B.shape[1]
     _check(_lib().spx_spmm_bsr(M, K, br, bc, nnzb, _ptr(bsr_row_ptr), _ptr(bsr_col), _ptr(bsr_val), N, _ptr(B),
-                               B.stride(0), _ptr(C), C.stride(0), _stream(stream)), "spx_spmm_bsr")
+                               B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
+           "spx_spmm_bsr")
     return C
 
 

@@ -317,14 +317,28 @@ spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* 
                               const float* val, int32_t N, const float* B, int64_t ldb, float alpha, float beta,
                               float* C, int64_t ldc, int32_t col_tile, spx_stream_t stream);
 
+/*
+ * spx_spmm_csr with A's values and B stored as bf16 (bit patterns), products
+ * and sums in fp32, C fp32.  [SpMM-ops] §5: storage and accumulation
+ * precision are separate; for SpMM the narrower B halves the gathered bytes.
+ * bf16 -> fp32 widening is exact and bf16 x bf16 products are exact in fp32,
+ * so the result carries fp32 summation error only.
+ * Needs N, ldb, ldc multiples of 4; B 8-byte and C 16-byte aligned
+ * (SPX_ERR_UNSUPPORTED / SPX_ERR_ALIGN otherwise).  Launches: 1.
+ */
+spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                             const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                             float* C, int64_t ldc, spx_stream_t stream);
+
 /* Which SpMM variant spx_spmm_csr would launch for these arguments:
    0 = small-N, 1 = float4 with N <= 128, 2 = float4 with N > 128, 3 = scalar. */
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);
 
 /*
- * C = A B with A in BSR (br x bc blocks, row-major inside, bf16), B dense
- * K x N bf16 row-major (ldb), C dense M x N fp32 row-major (ldc); products
- * accumulated in fp32 on the tensor cores.  [SpMM-ops] §3.4 (loop over the
+ * C = alpha * A B + beta * C with A in BSR (br x bc blocks, row-major inside,
+ * bf16), B dense K x N bf16 row-major (ldb), C dense M x N fp32 row-major
+ * (ldc); products accumulated in fp32 on the tensor cores, the epilogue in
+ * fp32 (beta == 0: C is write-only).  [SpMM-ops] §3.4 (loop over the
  * nonzero blocks, each a small dense GEMM on the tensor cores) and
  * [AsyncSparse] §2.2.1, §3 (BCSR SpMM: asynchronous copies of A blocks and
  * B tiles into shared memory feeding the matrix units).
@@ -336,7 +350,7 @@ int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float
  */
 spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
-                        float* C, int64_t ldc, spx_stream_t stream);
+                        float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device-side error word

@@ -68,7 +68,7 @@ def _lib_():
                 "or_plan_opts_auto": [vp, vp],
                 "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
                 "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
-                "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, vp, i64, vp, vp],
+                "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(lib, name)
@@ -197,7 +197,7 @@ def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None):
     return ref, bnd
 
 
-def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None):
+def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None, alpha=1.0, beta=0.0, C=None):
     brp, bcol = _c(brp, np.int32), _c(bcol, np.int32)
     bval = _c(bval_bf16, np.uint16)
     B = _c(B_bf16, np.uint16)
@@ -206,6 +206,8 @@ def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None):
     n = M if rr is None else rr.size
     ref = np.empty((n, N), np.float64)
     bnd = np.empty((n, N), np.float64)
-    _check(_lib_().or_bsr_spmm(M, K, br, bc, _p(brp), _p(bcol), _p(bval), N, _p(B), N, _p(rr),
-                               0 if rr is None else rr.size, _p(ref), _p(bnd)))
+    Cv = _c(C, np.float32) if (C is not None and beta != 0.0) else None
+    _check(_lib_().or_bsr_spmm(M, K, br, bc, _p(brp), _p(bcol), _p(bval), N, _p(B), N, float(alpha), float(beta),
+                               _p(Cv), N if Cv is not None else 0, _p(rr), 0 if rr is None else rr.size, _p(ref),
+                               _p(bnd)))
     return ref, bnd

@@ -439,11 +439,13 @@ static double bf16_to_double(uint16_t h) {
  * block.  [SpMM-ops] §3.4 (outer loop over the nonzero blocks, a small dense
  * product inside) and [AsyncSparse] §3 (BCSR SpMM, each block a dense
  * micro-GEMM against the B rows of its block column).  Padded block columns
- * beyond K contribute nothing.  ref/bound: (#rows x N), leading dimension N.
+ * beyond K contribute nothing.  ref = alpha * sum + beta * C_in (C_in read only
+ * when beta != 0, fp32, leading dimension ldc); bound = |alpha| * sum |a b| +
+ * |beta * C_in|.  ref/bound: (#rows x N), leading dimension N.
  */
 int or_bsr_spmm(int32_t M, int32_t K, int32_t br, int32_t bc, const int32_t* bsr_rp, const int32_t* bcol,
-                const uint16_t* bval, int32_t N, const uint16_t* B, int64_t ldb, const int32_t* rows, int64_t nrows,
-                double* ref, double* bound) {
+                const uint16_t* bval, int32_t N, const uint16_t* B, int64_t ldb, double alpha, double beta,
+                const float* C_in, int64_t ldc, const int32_t* rows, int64_t nrows, double* ref, double* bound) {
     if (M < 0 || K < 0 || N < 0 || br <= 0 || bc <= 0) return OR_ERR_ARG;
     int64_t n = rows ? nrows : M;
     double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * (N ? N : 1)));
@@ -469,8 +471,14 @@ int or_bsr_spmm(int32_t M, int32_t K, int32_t br, int32_t bc, const int32_t* bsr
             }
         }
         for (int32_t c = 0; c < N; ++c) {
-            ref[k * N + c] = acc[c];
-            if (bound) bound[k * N + c] = mag[c];
+            double r = alpha * acc[c], b = fabs(alpha) * mag[c];
+            if (beta != 0.0) {
+                double y = (double)C_in[(int64_t)i * ldc + c];
+                r += beta * y;
+                b += fabs(beta * y);
+            }
+            ref[k * N + c] = r;
+            if (bound) bound[k * N + c] = b;
         }
     }
     free(acc);

@@ -112,10 +112,27 @@ def test_unsupported_shapes_rejected_without_launch():
     before = spx.launch_count()
     z = torch.zeros(64 * 1024, dtype=torch.int32, device="cuda")
     p = spx._ptr(z)
-    assert lib.spx_spmm_bsr(64, 64, 32, 32, 1, p, p, p, 128, p, 128, p, 128, None) == -7   # block size
-    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 100, p, 128, p, 128, None) == -7   # N % 128
-    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, p, 128, None) == -8   # ldb % 8
+    assert lib.spx_spmm_bsr(64, 64, 32, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -7   # block size
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 100, p, 128, 1.0, 0.0, p, 128, None) == -7   # N % 128
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, 1.0, 0.0, p, 128, None) == -8   # ldb % 8
     assert spx.launch_count() == before
+
+
+@pytest.mark.parametrize("alpha,beta", [(2.0, 0.0), (-0.5, 1.5), (1.0, -1.0)])
+def test_alpha_beta(alpha, beta):
+    MB, KB, N = 5, 12, 256
+    brp, bcol = pattern(6, MB, KB, [4, 0, 7, 2, 11])
+    nb = bcol.size
+    A = synth.normal_bf16(6, synth.T_VAL, nb * 4096, 0.02).reshape(nb, 64, 64)
+    B = synth.normal_bf16(6, synth.T_B, KB * 64 * N, 1.0).reshape(KB * 64, N)
+    C0 = synth.uniform(6, synth.T_Y, MB * 64 * N).reshape(MB * 64, N)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_bsr(MB * 64, KB * 64, 64, 64, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(A.reshape(-1)), bits_dev(B), Cd, alpha=alpha, beta=beta)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    ref, bound = oracle.bsr_spmm(MB * 64, KB * 64, 64, 64, brp, bcol, A, B, alpha=alpha, beta=beta, C=C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, BF16_REL, BF16_ABS, what=f"alpha={alpha} beta={beta}")
 
 
 def test_no_blocks_gives_zero():
@@ -124,6 +141,17 @@ def test_no_blocks_gives_zero():
     got = run_bsr(M, K, brp, np.zeros(0, np.int32), np.zeros((0, 64, 64), np.uint16),
                   np.ones((K, N), np.uint16), N)
     assert not got.any()
+
+
+def test_no_blocks_scales_by_beta():
+    M, K, N = 128, 64, 256
+    C0 = synth.uniform(9, synth.T_Y, M * N).reshape(M, N)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    spx.spx_spmm_bsr(M, K, 64, 64, torch.zeros(3, dtype=torch.int32, device="cuda"), z[:0], z[:0].to(torch.int16),
+                     torch.zeros(K, N, dtype=torch.int16, device="cuda"), Cd, beta=-2.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(Cd.cpu().numpy(), np.float32(-2.0) * C0)
 
 
 @pytest.mark.slow

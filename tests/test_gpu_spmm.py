@@ -100,3 +100,42 @@ def test_clustered_full_size_sampled(N):
     got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
     ref, bound = oracle.spmm(M, rp, col, val, cfg["B"], rows=rows)
     assert_within(got, ref, bound, what=f"clustered N={N}")
+
+
+@pytest.mark.parametrize("N,alpha,beta", [(8, 1.0, 0.0), (32, 1.0, 0.0), (64, -2.0, 0.5), (128, 1.0, 0.0),
+                                          (256, 0.5, -1.0), (20, 1.0, 0.0)])
+def test_bf16_values(N, alpha, beta):
+    """bf16 A values and B: exact widening and exact products, so the fp32
+    tolerance against the fp64 oracle (fed the same values widened) holds."""
+    M, K = 700, 500
+    d = synth.random_coo(N + 1, M, K, 0, 45)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    vb = synth.to_bf16_bits(val)
+    Bb = synth.to_bf16_bits(synth.uniform(N, synth.T_B, K * N)).reshape(K, N)
+    C0 = synth.uniform(N, synth.T_Y, M * N).reshape(M, N)
+    A = spx.Csr(M, K, dev(rp), dev(col), dev(vb.view(np.int16)))
+    Cd = dev(C0)
+    spx.spx_spmm_csr_bf16(A, dev(Bb.view(np.int16)), Cd, alpha, beta)
+    torch.cuda.synchronize()
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(K, N),
+                             alpha, beta, C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, what=f"bf16 N={N}")
+
+
+@pytest.mark.slow
+def test_bf16_clustered_full_size_sampled():
+    cfg = synth.clustered_spmm(N=32)
+    M, K = cfg["M"], cfg["K"]
+    rp, col, val = spx.spx_build_csr(M, K, cfg["row"], cfg["col"], cfg["val"])
+    vb = synth.to_bf16_bits(val)
+    Bb = synth.to_bf16_bits(cfg["B"]).reshape(K, 32)
+    A = spx.Csr(M, K, dev(rp), dev(col), dev(vb.view(np.int16)))
+    Cd = torch.empty(M, 32, device="cuda")
+    spx.spx_spmm_csr_bf16(A, dev(Bb.view(np.int16)), Cd)
+    torch.cuda.synchronize()
+    rows = np.unique((np.random.default_rng(3).integers(0, M // 4, 512)[:, None] * 4 + np.arange(4)).ravel())
+    rows = rows.astype(np.int32)
+    got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(K, 32),
+                             rows=rows)
+    assert_within(got, ref, bound, what="bf16 clustered")

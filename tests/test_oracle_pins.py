@@ -165,6 +165,12 @@ def test_bruteforce_bsr(M, K, lmin, lmax, bs):
                                  synth.to_bf16_bits(Bf).reshape(K, N))
     assert np.array_equal(ref, A @ Bf.astype(np.float64))
     assert np.array_equal(bound, np.abs(A) @ np.abs(Bf.astype(np.float64)))
+    # C = alpha*A*B + beta*C with dyadic scalars and integer C: still exact
+    C0 = np.floor(synth.uniform(4, synth.T_Y, M * N, -5, 6)).astype(np.float32).reshape(M, N)
+    ref2, bound2 = oracle.bsr_spmm(M, K, br, bc, brp, bcol, synth.to_bf16_bits(bval).reshape(bval.shape),
+                                   synth.to_bf16_bits(Bf).reshape(K, N), alpha=-1.5, beta=0.25, C=C0)
+    assert np.array_equal(ref2, -1.5 * (A @ Bf.astype(np.float64)) + 0.25 * C0)
+    assert np.array_equal(bound2, 1.5 * (np.abs(A) @ np.abs(Bf.astype(np.float64))) + 0.25 * np.abs(C0))
 
 
 def test_bsr_stored_blocks_nonempty():
