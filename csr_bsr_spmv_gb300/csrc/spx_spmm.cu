@@ -9,9 +9,10 @@
 //                        L = T/4 lanes owns (row, tile), each lane 4 adjacent
 //                        columns (float4 loads of B); 32/L rows per warp, so a
 //                        4-row cluster shares one warp and its B rows hit in
-//                        L1.  The tile index is the outer grid dimension, B
-//                        loads carry an L2 evict-last hint and A / C stream
-//                        through with evict-first hints;
+//                        L1.  The tile index is the outer grid dimension, the
+//                        CTA's run of A is staged in shared memory, B loads
+//                        carry an L2 evict-last hint and A / C stream through
+//                        with evict-first hints;
 //   scalar  otherwise  : a warp per row, lanes over columns.
 #include <cuda_runtime.h>
 
@@ -76,55 +77,130 @@ __global__ void __launch_bounds__(kThreads) spmm_small_kernel(int M, const int* 
 
 // ------------------------------------------------------------- float4 sub-warp / tiled
 // L lanes per row, each lane 4 columns; the warp holds 32/L rows.  Column
-// tile origin = blockIdx.y * 4 * L (tiled variant: L = 32, gridDim.y tiles).
-template <int L>
-__global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const int* __restrict__ rp,
-                                                            const int* __restrict__ col,
-                                                            const float* __restrict__ val,
-                                                            const float* __restrict__ B, long long ldb, float alpha,
-                                                            float beta, float* C, long long ldc) {
-    constexpr int RPW = 32 / L;  // rows per warp
-    const int lane = threadIdx.x & 31;
-    const int row = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW + lane / L;
-    const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
-    if (row >= M) return;
-    const bool live = n0 < N;
-    const uint64_t pol = l2_evict_last_policy();
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
-    const float* Bc = B + n0;
-    int p = a;
+// tile origin = blockIdx.y * 4 * L (gridDim.y tiles).  One template serves
+// fp32 storage and bf16 storage (A's values and B as bf16, widened exactly
+// to fp32: [SpMM-ops] §5 keeps storage and accumulation precision apart;
+// halving B halves the gathered bytes, the term that dominates SpMM).
+//
+// The CTA's rows are consecutive, so their nonzeros are one contiguous run of
+// col/val.  Up to kStageCap of them are first copied into shared memory with
+// coalesced loads by the whole CTA; the row loops then wait only on B rows,
+// not on a dependent col -> B chain through DRAM for every batch of U
+// nonzeros.  A CTA whose run is longer reads col/val from global memory.
+constexpr int kStageCap = 2048;
 #ifndef SPX_SPMM_UNROLL
 #define SPX_SPMM_UNROLL 8
 #endif
-    constexpr int U = SPX_SPMM_UNROLL;  // B-row loads in flight per lane
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint16_t ld_stream(const uint16_t* p) {
+    return static_cast<uint16_t>(__ldcs(reinterpret_cast<const unsigned short*>(p)));
+}
+
+// kMinBlocks: resident CTAs per SM the register budget is sized for.  Measured
+// on the clustered 1M x 1M matrix at N = 32 and 128: fp32 runs fastest at 6
+// (42 registers: 8 B rows of 16 bytes in flight per lane), bf16 at 8 (32).
+struct StoreF32 {
+    using V = float;
+    using Bt = float;
+    static constexpr int kMinBlocks = 6;
+    __device__ static float widen(float v) { return v; }
+    __device__ static float4 brow(const float* p, uint64_t pol) { return ld_keep(p, pol); }
+};
+struct StoreBF16 {
+    using V = uint16_t;
+    using Bt = uint16_t;
+    static constexpr int kMinBlocks = 8;
+    __device__ static float widen(uint16_t v) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
+    __device__ static float4 brow(const uint16_t* p, uint64_t pol) {  // 4 bf16 = 8 bytes
+        uint2 w;
+        asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(w.x), "=r"(w.y) : "l"(p), "l"(pol));
+        return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+};
+
+template <bool SMEM>
+__device__ __forceinline__ int ld_a(const int* p) { return SMEM ? *p : ld_stream(p); }
+template <bool SMEM, class V>
+__device__ __forceinline__ V ld_a(const V* p) { return SMEM ? *p : ld_stream(p); }
+
+// Sum over the nonzeros [a, b) of cols/vals of val * B(col, n0 .. n0+3); U B rows in flight.
+template <class T, bool SMEM>
+__device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* vals, int a, int b,
+                                          const typename T::Bt* Bc, long long ldb, uint64_t pol) {
+    constexpr int U = SPX_SPMM_UNROLL;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = a;
     for (; p + U - 1 < b; p += U) {
         int c[U];
         float v[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-            c[j] = ld_stream(col + p + j);
-            v[j] = ld_stream(val + p + j);
+            c[j] = ld_a<SMEM>(cols + p + j);
+            v[j] = T::widen(ld_a<SMEM>(vals + p + j));
         }
-        if (live) {
-            float4 bv[U];
+        float4 bv[U];
 #pragma unroll
-            for (int j = 0; j < U; ++j) bv[j] = ld_keep(Bc + (long long)c[j] * ldb, pol);
+        for (int j = 0; j < U; ++j) bv[j] = T::brow(Bc + (long long)c[j] * ldb, pol);
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
-            }
+        for (int j = 0; j < U; ++j) {
+            acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
         }
     }
     for (; p < b; ++p) {
-        const int c0 = ld_stream(col + p);
-        const float v0 = ld_stream(val + p);
-        if (live) {
-            const float4 b0 = ld_keep(Bc + (long long)c0 * ldb, pol);
-            acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
-        }
+        const int c0 = ld_a<SMEM>(cols + p);
+        const float v0 = T::widen(ld_a<SMEM>(vals + p));
+        const float4 b0 = T::brow(Bc + (long long)c0 * ldb, pol);
+        acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
     }
-    if (!live) return;
+    return acc;
+}
+
+template <int L, class T>
+__global__ void __launch_bounds__(kThreads, T::kMinBlocks)
+    spmm_vec_kernel(int M, int N, const int* __restrict__ rp, const int* __restrict__ col,
+                    const typename T::V* __restrict__ val, const typename T::Bt* __restrict__ B, long long ldb,
+                    float alpha, float beta, float* C, long long ldc) {
+    constexpr int RPW = 32 / L;         // rows per warp
+    constexpr int R = kWarps * RPW;     // rows per CTA
+    constexpr int IT = kStageCap / kThreads;
+    __shared__ int s_col[kStageCap];
+    __shared__ typename T::V s_val[kStageCap];
+    const int lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * R;
+    const int row = r0 + (threadIdx.x >> 5) * RPW + lane / L;
+    const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
+    const int ca = __ldg(rp + r0);
+    const int cn = __ldg(rp + min(r0 + R, M)) - ca;
+    const bool staged = cn <= kStageCap;  // uniform over the CTA
+    if (staged) {
+        int c[IT];
+        typename T::V v[IT];
+#pragma unroll
+        for (int j = 0; j < IT; ++j) {
+            const int k = threadIdx.x + j * kThreads;
+            if (k < cn) {
+                c[j] = ld_stream(col + ca + k);
+                v[j] = ld_stream(val + ca + k);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < IT; ++j) {
+            const int k = threadIdx.x + j * kThreads;
+            if (k < cn) {
+                s_col[k] = c[j];
+                s_val[k] = v[j];
+            }
+        }
+        __syncthreads();
+    }
+    if (row >= M || n0 >= N) return;
+    const uint64_t pol = l2_evict_last_policy();
+    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    const typename T::Bt* Bc = B + n0;
+    const float4 acc = staged ? row_dot<T, true>(s_col, s_val, a - ca, b - ca, Bc, ldb, pol)
+                              : row_dot<T, false>(col, val, a, b, Bc, ldb, pol);
     float4* cp = reinterpret_cast<float4*>(C + (long long)row * ldc + n0);
     float4 r = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
     if (beta != 0.f) {
@@ -132,76 +208,6 @@ __global__ void __launch_bounds__(kThreads) spmm_vec_kernel(int M, int N, const 
         r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
     }
     __stcs(cp, r);  // C is written once: evict-first
-}
-
-// ------------------------------------------------------------- bf16 storage, fp32 accumulation
-// Same mapping as spmm_vec_kernel with A's values and B stored as bf16
-// ([SpMM-ops] §5: storage and accumulation precision kept apart; halving B
-// halves the gathered bytes, the term that dominates SpMM).  A lane loads 4
-// bf16 of a B row (8 bytes) and widens them exactly to fp32.
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint2 ld_keep8(const uint16_t* p, uint64_t pol) {
-    uint2 v;
-    asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
-    return v;
-}
-
-template <int L>
-__global__ void __launch_bounds__(kThreads) spmm_vec_bf16_kernel(int M, int N, const int* __restrict__ rp,
-                                                                 const int* __restrict__ col,
-                                                                 const uint16_t* __restrict__ val,
-                                                                 const uint16_t* __restrict__ B, long long ldb,
-                                                                 float alpha, float beta, float* C, long long ldc) {
-    constexpr int RPW = 32 / L;
-    const int lane = threadIdx.x & 31;
-    const int row = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW + lane / L;
-    const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
-    if (row >= M) return;
-    const bool live = n0 < N;
-    const uint64_t pol = l2_evict_last_policy();
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
-    const uint16_t* Bc = B + n0;
-    constexpr int U = SPX_SPMM_UNROLL;
-    int p = a;
-    for (; p + U - 1 < b; p += U) {
-        int c[U];
-        float v[U];
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-            c[j] = ld_stream(col + p + j);
-            v[j] = __uint_as_float(static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(val + p + j))) << 16);
-        }
-        if (live) {
-            uint2 bv[U];
-#pragma unroll
-            for (int j = 0; j < U; ++j) bv[j] = ld_keep8(Bc + (long long)c[j] * ldb, pol);
-#pragma unroll
-            for (int j = 0; j < U; ++j) {
-                acc.x += v[j] * bf16_lo(bv[j].x); acc.y += v[j] * bf16_hi(bv[j].x);
-                acc.z += v[j] * bf16_lo(bv[j].y); acc.w += v[j] * bf16_hi(bv[j].y);
-            }
-        }
-    }
-    for (; p < b; ++p) {
-        const int c0 = ld_stream(col + p);
-        const float v0 = __uint_as_float(static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(val + p))) << 16);
-        if (live) {
-            const uint2 b0 = ld_keep8(Bc + (long long)c0 * ldb, pol);
-            acc.x += v0 * bf16_lo(b0.x); acc.y += v0 * bf16_hi(b0.x);
-            acc.z += v0 * bf16_lo(b0.y); acc.w += v0 * bf16_hi(b0.y);
-        }
-    }
-    if (!live) return;
-    float4* cp = reinterpret_cast<float4*>(C + (long long)row * ldc + n0);
-    float4 r = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
-    if (beta != 0.f) {
-        const float4 o = *cp;
-        r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
-    }
-    __stcs(cp, r);
 }
 
 // ------------------------------------------------------------- scalar fallback
@@ -241,20 +247,25 @@ int auto_col_tile(int32_t N) {
     return t;
 }
 
-template <int L>
-void launch_vec(int M, int N, const int* rp, const int* col, const float* val, const float* B, long long ldb,
-                float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
+template <int L, class T>
+void launch_vec(int M, int N, const int* rp, const int* col, const typename T::V* val, const typename T::Bt* B,
+                long long ldb, float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
     constexpr int rows_per_cta = kWarps * (32 / L);
     dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
-    spmm_vec_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+    spmm_vec_kernel<L, T><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
 }
 
-template <int L>
-void launch_vec_bf16(int M, int N, const int* rp, const int* col, const uint16_t* val, const uint16_t* B, long long ldb,
-                     float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
-    constexpr int rows_per_cta = kWarps * (32 / L);
-    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
-    spmm_vec_bf16_kernel<L><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+template <class T>
+void launch_vec_tile(int tile, int M, int N, const int* rp, const int* col, const typename T::V* val,
+                     const typename T::Bt* B, long long ldb, float alpha, float beta, float* C, long long ldc,
+                     cudaStream_t st) {
+    switch (tile) {
+        case 8: launch_vec<2, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 16: launch_vec<4, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 32: launch_vec<8, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 64: launch_vec<16, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        default: launch_vec<32, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+    }
 }
 
 spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
@@ -282,13 +293,7 @@ spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const
         spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
     } else {
         const int t = col_tile ? col_tile : auto_col_tile(N);
-        switch (t) {
-            case 8: launch_vec<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-            case 16: launch_vec<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-            case 32: launch_vec<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-            case 64: launch_vec<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-            default: launch_vec<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        }
+        launch_vec_tile<StoreF32>(t, M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
     }
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
@@ -321,13 +326,7 @@ spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* r
         !spx_aligned(C, 16))
         return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    switch (auto_col_tile(N)) {
-        case 8: launch_vec_bf16<2>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 16: launch_vec_bf16<4>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 32: launch_vec_bf16<8>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 64: launch_vec_bf16<16>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        default: launch_vec_bf16<32>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-    }
+    launch_vec_tile<StoreBF16>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }

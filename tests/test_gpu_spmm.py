@@ -139,3 +139,25 @@ def test_bf16_clustered_full_size_sampled():
     ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(K, 32),
                              rows=rows)
     assert_within(got, ref, bound, what="bf16 clustered")
+
+
+def test_bf16_long_and_empty_rows():
+    """A CTA whose rows hold more nonzeros than its shared-memory stage reads
+    A from global memory; its neighbours are staged.  Both paths, bf16."""
+    L = np.zeros(70, np.int32)
+    L[3] = 5000
+    L[10:20] = 1
+    L[40] = 900
+    row, col = synth.cols_uniform(9, 6000, L)
+    rp, col, val = oracle.build_csr(70, 6000, row, col, synth.uniform(9, synth.T_VAL, row.size))
+    vb = synth.to_bf16_bits(val)
+    for N in (32, 160):
+        Bb = synth.to_bf16_bits(synth.uniform(N, synth.T_B, 6000 * N)).reshape(6000, N)
+        C0 = synth.uniform(N, synth.T_Y, 70 * N).reshape(70, N)
+        Cd = dev(C0)
+        spx.spx_spmm_csr_bf16(spx.Csr(70, 6000, dev(rp), dev(col), dev(vb.view(np.int16))), dev(Bb.view(np.int16)),
+                              Cd, 1.0, 0.25)
+        torch.cuda.synchronize()
+        ref, bound = oracle.spmm(70, rp, col, synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(6000, N),
+                                 1.0, 0.25, C0)
+        assert_within(Cd.cpu().numpy(), ref, bound, what=f"bf16 long rows N={N}")
