@@ -7,7 +7,7 @@ is one SpMV call through the C ABI: the binned main launch plus the long-row
 fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload power-law|uniform|dual|spmm32|spmm128|bsr]
+                    [--workload power-law|power-law-coo|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -143,8 +143,10 @@ def make_workload(name: str, rows: int = 0):
     """Host arrays of the workload; `rows` shrinks the power-law case (profiling)."""
     import synth
 
-    if name == "power-law":
+    if name in ("power-law", "power-law-coo"):
         c = synth.power_law_rows(M=rows) if rows else synth.power_law_rows()
+        if name == "power-law-coo":
+            c["name"] += " as row-sorted COO"
     elif name == "uniform":
         c = synth.uniform_short_rows()
     elif name == "dual":
@@ -171,6 +173,9 @@ def accounting(c):
     if w in ("power-law", "uniform"):
         ybytes = 8 * M if c["beta"] != 0 else 4 * M
         return 2 * nnz, 8 * nnz + 4 * (M + 1) + 4 * K + ybytes
+    if w == "power-law-coo":  # row index per entry instead of row offsets
+        ybytes = 8 * M if c["beta"] != 0 else 4 * M
+        return 2 * nnz, 12 * nnz + 4 * K + ybytes
     if w == "dual":
         # u = A v - a u (reads v, reads+writes u); v = A^T u - b v (reads u, reads+writes v)
         b1 = 8 * nnz + 4 * (M + 1) + 4 * K + 8 * M
@@ -214,6 +219,8 @@ def run_ours(args, rank, world):
     t0 = time.perf_counter()
     if w == "bsr":
         rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val_bf16"])
+    elif w == "power-law-coo":
+        rp = col = val = None  # the generator's triplets are already sorted by row
     else:
         rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val"])
     timings["build_csr_ms"] = 1e3 * (time.perf_counter() - t0)
@@ -258,6 +265,32 @@ def run_ours(args, rank, world):
         extra = {"plan": {k: info[k] for k in ("tasks", "long_rows", "cta_rows", "split_rows", "thread_groups",
                                                 "lane_groups", "segmented_groups")},
                  "plan_opts": plan.opts, "row_stats": plan.stats}
+    elif w == "power-law-coo":
+        crow, ccol, cval = to_dev(c["row"]), to_dev(c["col"]), to_dev(c["val"])
+        x = to_dev(c["x"])
+        y = to_dev(c["y"])
+        alpha, beta = c["alpha"], c["beta"]
+        scratch = torch.empty(max(1, spx.spx_spmv_coo_scratch_bytes(c["row"].size) // 4), device=dev)
+        src = source_hash("spx_coo.cu")
+
+        def run():
+            spx.spx_spmv_coo(M, K, crow, ccol, cval, x, y, alpha, beta, stream=stream, scratch=scratch)
+
+        xh = torch.from_numpy(c["x"]).pin_memory()
+        yh = torch.from_numpy(c["y"]).pin_memory()
+        yo = torch.empty_like(yh).pin_memory()
+        h2d = xh.numel() * 4 + (yh.numel() * 4 if beta != 0 else 0)
+        d2h = yo.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                x.copy_(xh, non_blocking=True)
+                if beta != 0:
+                    y.copy_(yh, non_blocking=True)
+                spx.spx_spmv_coo(M, K, crow, ccol, cval, x, y, alpha, beta, stream=stream, scratch=scratch)
+                yo.copy_(y, non_blocking=True)
+
+        extra = {"chunks": -(-int(c["row"].size) // 2048)}
     elif w == "dual":
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         t0 = time.perf_counter()
@@ -471,6 +504,9 @@ def cpu_step_fn(c):
         fl = 2 * int(nb.sum()) * c["bs"] * c["N"]
         return (lambda: oracle.bsr_spmm(M, K, c["bs"], c["bs"], brp, bcol, bval, c["B_bf16"], rows=rows)), fl, \
             f"{rows.size} output rows (one per block-row) of the {M}x{K} BSR product"
+    if w == "power-law-coo":
+        return (lambda: oracle.spmv_coo(M, K, c["row"], c["col"], c["val"], c["x"], c["alpha"], c["beta"],
+                                        c["y"])), 2 * int(c["row"].size), "the full matrix, one COO SpMV"
     rp, col, val = row_major_csr(c, c["val"])
     if w in ("power-law", "uniform"):
         return (lambda: oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"])), 2 * int(rp[-1]), \
@@ -537,7 +573,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
-                    choices=["power-law", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16", "spmm128-bf16", "bsr"])
+                    choices=["power-law", "power-law-coo", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
+                             "spmm128-bf16", "bsr"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -411,23 +411,33 @@ __global__ void __launch_bounds__(kTThreads)
     tc_fence_after();
     const uint32_t tmem_d = s_tmem;
 
-    if (warp == 0 && lane == 0) {
-        int b = 0;
+    if (warp == 0) {
+        // Producer warp: lane 0 waits for the free slot and arms the barrier,
+        // then lanes 0..2 issue the stage's three boxes side by side (the A
+        // block and the two 64-column halves of the B tile).  The block
+        // columns of this block-row sit in registers, 32 at a time.
+        int b = 0, jreg = 0;
         for (; b < nblk; ++b) {
             const int s = b % STAGES;
             const uint32_t ph = (b / STAGES) & 1u;
-            if (!mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) || s_abort) {
-                record_error(kErrEmpty);
-                s_abort = 1;
+            if ((b & 31) == 0) jreg = b + lane < nblk ? __ldg(bcol + b0 + b + lane) : 0;
+            const int J = __shfl_sync(0xffffffffu, jreg, b & 31);
+            int ok = 1;
+            if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(kErrEmpty);
+                    s_abort = 1;
+                }
                 break;
             }
-            mbar_expect_tx(full_bar(s), kTStageBytes);
-            const int J = __ldg(bcol + b0 + b);
-            tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
-            tma_load_2d(stage_b(s), &tmB, n0, J * kBlk, full_bar(s));
-            tma_load_2d(stage_b(s) + kBBox, &tmB, n0 + 64, J * kBlk, full_bar(s));
+            if (lane == 0) mbar_expect_tx(full_bar(s), kTStageBytes);
+            __syncwarp();
+            if (lane == 0) tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
+            else if (lane < 3) tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
         }
-        s_issued = b;
+        if (lane == 0) s_issued = b;
     } else if (warp == 1 && lane == 0) {
         int b = 0;
         for (; b < nblk; ++b) {
@@ -630,7 +640,9 @@ spx_status spx_last_device_error(spx_stream_t stream) {
     if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&h, g_bsr_error, sizeof(int));
     if (e == cudaSuccess && h != 0) e = cudaMemcpyToSymbol(g_bsr_error, &zero, sizeof(int));
     if (e != cudaSuccess) return SPX_ERR_CUDA;
-    return h ? SPX_ERR_TIMEOUT : SPX_OK;
+    const int coo = spx_coo_error_take();
+    if (h) return SPX_ERR_TIMEOUT;
+    return static_cast<spx_status>(coo);
 }
 
 }  // extern "C"

@@ -423,7 +423,7 @@ spx_status spx_plan_opts_default(spx_plan_opts_t* o) {
     o->pack_max = 512;
     o->cta_max = 8192;
     o->seg_nnz = 4096;
-    o->lanes_div = 4;
+    o->lanes_div = 16;
     return SPX_OK;
 }
 

@@ -13,6 +13,9 @@ void spx_note_launches(uint64_t n);
 // Status of the last CUDA runtime error, or SPX_OK.
 spx_status spx_cuda_status(int cuda_error);
 
+// Reads and clears the error word of the COO kernel: 0 or a negative spx_status.
+int spx_coo_error_take();
+
 struct spx_plan {
     int32_t M = 0, K = 0;
     int64_t nnz = 0;

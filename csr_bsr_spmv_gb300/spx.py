@@ -87,6 +87,8 @@ def _lib():
             "spx_plan_destroy": ([vp], ctypes.c_int),
             "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
+            "spx_spmv_coo_scratch_bytes": ([i64], sz),
+            "spx_spmv_coo": ([i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
                                    sz, vp], ctypes.c_int),
             "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
@@ -327,6 +329,23 @@ def spx_spmv_csr_noalloc(plan: Plan, A: Csr, x: torch.Tensor, y: torch.Tensor, a
     _check(_lib().spx_spmv_csr_noalloc(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
                                        float(alpha), _ptr(x), float(beta), _ptr(y), _stream(stream)),
            "spx_spmv_csr_noalloc")
+    return y
+
+
+def spx_spmv_coo_scratch_bytes(nnz: int) -> int:
+    return int(_lib().spx_spmv_coo_scratch_bytes(int(nnz)))
+
+
+def spx_spmv_coo(M: int, K: int, row: torch.Tensor, col: torch.Tensor, val: torch.Tensor, x: torch.Tensor,
+                 y: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None,
+                 scratch: torch.Tensor | None = None):
+    """y <- alpha*A*x + beta*y for A given as row-sorted COO device tensors (int32 row/col, fp32 val)."""
+    nnz = col.numel()
+    need = spx_spmv_coo_scratch_bytes(nnz)
+    if scratch is None:
+        scratch = torch.empty(max(1, need // 4), dtype=torch.float32, device=y.device)
+    _check(_lib().spx_spmv_coo(M, K, nnz, _ptr(row), _ptr(col), _ptr(val), float(alpha), _ptr(x), float(beta),
+                               _ptr(y), _ptr(scratch), scratch.numel() * 4, _stream(stream)), "spx_spmv_coo")
     return y
 
 

@@ -157,7 +157,7 @@ typedef struct spx_plan_opts_t {
                            threads are joined by a block scan */
 } spx_plan_opts_t;
 
-/* Fills the fixed defaults: B 2048, R 256, P 512, C 8192, S 4096, D 4. */
+/* Fills the fixed defaults: B 2048, R 256, P 512, C 8192, S 4096, D 16. */
 spx_status spx_plan_opts_default(spx_plan_opts_t* out);
 
 /*
@@ -165,7 +165,7 @@ spx_status spx_plan_opts_default(spx_plan_opts_t* out);
  * [SpMM-ops] §4: mean, spread and tail of the row lengths pick the mapping):
  * cv >= 2 (skewed, power-law-like lengths): B 1024 (128-thread CTAs) and the
  * segmented reduction (D 0), whose work per thread ignores row length;
- * otherwise the defaults above (256-thread CTAs, D 4 lanes-per-row rule).
+ * otherwise the defaults above (256-thread CTAs, D 16 lanes-per-row rule).
  */
 spx_status spx_plan_opts_auto(const spx_row_stats_t* stats, spx_plan_opts_t* out);
 
@@ -335,6 +335,30 @@ spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* r
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);
 
 /*
+ * COO SpMV y = alpha * A x + beta * y over triplets sorted by row (columns in
+ * any order within a row; duplicates allowed and summed as separate terms).
+ * [Formats] §1 (the COO format: one row index, column index and value per
+ * stored entry) and the COO row of the dispatch rule table in [SpMM-ops] §4
+ * (work split by nonzeros with a segmented reduction, so row lengths never
+ * unbalance the launch).
+ *   coo_row, coo_col int32[nnz], coo_val fp32[nnz], x fp32[K], y fp32[M]:
+ *   device memory, owned by the caller; x and y must not overlap.
+ *   Each row's sum is taken in a fixed order (bitwise reproducible); rows
+ *   without entries get beta * y (0 when beta == 0: y is then write-only).
+ *   scratch: device memory of at least spx_spmv_coo_scratch_bytes(nnz)
+ *   bytes (two floats per 2048 entries), owned by the caller.
+ * Launches: 1 for nnz <= 2048 or nnz == 0, else 2.  Entries whose row is out
+ * of [0, M) or smaller than the row before it, or whose column is out of
+ * [0, K), are skipped without any out-of-bounds access; the kernel records
+ * SPX_ERR_INDEX_RANGE or SPX_ERR_NOT_SORTED, which spx_last_device_error
+ * returns (y is then unspecified).
+ */
+size_t spx_spmv_coo_scratch_bytes(int64_t nnz);
+spx_status spx_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_row, const int32_t* coo_col,
+                        const float* coo_val, float alpha, const float* x, float beta, float* y, void* scratch,
+                        size_t scratch_bytes, spx_stream_t stream);
+
+/*
  * C = alpha * A B + beta * C with A in BSR (br x bc blocks, row-major inside,
  * bf16), B dense K x N bf16 row-major (ldb), C dense M x N fp32 row-major
  * (ldc); products accumulated in fp32 on the tensor cores, the epilogue in
@@ -353,8 +377,9 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream);
 
 /*
- * Synchronises `stream`, then reads and clears the device-side error word
- * that bounded waits set.  SPX_OK if none; SPX_ERR_TIMEOUT otherwise.
+ * Synchronises `stream`, then reads and clears the device-side error words:
+ * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr gave up, else the index
+ * or ordering error spx_spmv_coo recorded, else SPX_OK.
  */
 spx_status spx_last_device_error(spx_stream_t stream);
 

@@ -67,6 +67,7 @@ def _lib_():
                 "or_plan_spmv": [i32, vp, vp, vp, vp, vp],
                 "or_plan_opts_auto": [vp, vp],
                 "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
+                "or_spmv_coo": [i32, i32, i64, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
                 "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
                 "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
             }
@@ -181,6 +182,17 @@ def spmv(M, rp, col, val, x, alpha=1.0, beta=0.0, y=None, rows=None):
     _check(_lib_().or_spmv(M, _p(rp), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv), _p(rr),
                            0 if rr is None else rr.size, _p(ref), _p(bnd)))
     return ref, bnd
+
+
+def spmv_coo(M, K, row, col, val, x, alpha=1.0, beta=0.0, y=None):
+    """(ref, bound) in fp64 of the COO product over all M rows (triplets in any order)."""
+    row, col, val, x = _c(row, np.int32), _c(col, np.int32), _c(val, np.float32), _c(x, np.float32)
+    yv = _c(y, np.float32) if (y is not None and beta != 0.0) else None
+    ref = np.empty(max(M, 1), np.float64)
+    bnd = np.empty(max(M, 1), np.float64)
+    _check(_lib_().or_spmv_coo(M, K, col.size, _p(row), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv),
+                               _p(ref), _p(bnd)))
+    return ref[:M], bnd[:M]
 
 
 def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None):

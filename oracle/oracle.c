@@ -239,7 +239,7 @@ enum { OR_TASK_GROUP = 0, OR_TASK_CTA = 1, OR_TASK_SEG = 2 };
  * Plan options from the row statistics ([SpMM-ops] §4: the dispatch key's
  * row-length spread picks the mapping): with cv >= 2 the groups hold 1024
  * nonzeros and use the segmented reduction (D = 0); otherwise 2048 nonzeros
- * and the lanes rule with D = 4.  R 256, P 512, C 8192, S 4096 either way.
+ * and the lanes rule with D = 16.  R 256, P 512, C 8192, S 4096 either way.
  */
 int or_plan_opts_auto(const or_row_stats_t* st, or_plan_opts_t* o) {
     if (!st || !o) return OR_ERR_ARG;
@@ -249,7 +249,7 @@ int or_plan_opts_auto(const or_row_stats_t* st, or_plan_opts_t* o) {
     o->pack_max = 512;
     o->cta_max = 8192;
     o->seg_nnz = 4096;
-    o->lanes_div = skewed ? 0 : 4;
+    o->lanes_div = skewed ? 0 : 16;
     return OR_OK;
 }
 
@@ -377,6 +377,42 @@ int or_spmv(int32_t M, const int32_t* rp, const int32_t* col, const float* val, 
         ref[k] = r;
         if (bound) bound[k] = b;
     }
+    return OR_OK;
+}
+
+/*
+ * COO SpMV: y_i = alpha * sum over the triplets p with row_p == i of
+ * val_p * x[col_p] + beta * y_i, fp64, triplets taken in index order.
+ * [Formats] §1 (COO stores one (row, col, val) triplet per entry; the product
+ * visits each triplet once and adds it to its row).  Rows without triplets
+ * give beta * y_i (0 when beta == 0; y_in is then not read).  The triplets
+ * need not be sorted here.  bound as in or_spmv.
+ */
+int or_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* row, const int32_t* col, const float* val,
+                const float* x, double alpha, double beta, const float* y_in, double* ref, double* bound) {
+    if (M < 0 || K < 0 || nnz < 0) return OR_ERR_ARG;
+    double* mag = (double*)calloc((size_t)(M ? M : 1), sizeof(double));
+    if (!mag) return OR_ERR_NOMEM;
+    for (int32_t i = 0; i < M; ++i) ref[i] = 0.0;
+    for (int64_t p = 0; p < nnz; ++p) {
+        if (row[p] < 0 || row[p] >= M || col[p] < 0 || col[p] >= K) {
+            free(mag);
+            return OR_ERR_INDEX;
+        }
+        double t = (double)val[p] * (double)x[col[p]];
+        ref[row[p]] += t;
+        mag[row[p]] += fabs(t);
+    }
+    for (int32_t i = 0; i < M; ++i) {
+        double r = alpha * ref[i], b = fabs(alpha) * mag[i];
+        if (beta != 0.0) {
+            r += beta * (double)y_in[i];
+            b += fabs(beta * (double)y_in[i]);
+        }
+        ref[i] = r;
+        if (bound) bound[i] = b;
+    }
+    free(mag);
     return OR_OK;
 }
 

@@ -136,7 +136,7 @@ def test_plan_matches_oracle(opts, seed):
 
 def test_plan_default_options_documented():
     o = spx.spx_plan_opts_default()
-    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=4)
+    assert o == dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=16)
 
 
 @pytest.mark.parametrize("kind", ["skewed", "uniform", "empty", "constant"])
@@ -157,7 +157,7 @@ def test_plan_auto_options_match_oracle(kind):
     o = spx.PlanOpts()
     assert lib.spx_plan_opts_auto(ctypes.byref(st), ctypes.byref(o)) == 0
     assert {f: getattr(o, f) for f, _ in spx.PlanOpts._fields_} == want
-    assert want["lanes_div"] == (0 if kind == "skewed" else 4)
+    assert want["lanes_div"] == (0 if kind == "skewed" else 16)
 
 
 def test_plan_rejects_bad_rows_and_options():
@@ -223,3 +223,24 @@ def test_spmm_variant_rule():
         assert lib.spx_spmm_csr_variant(N, a16, N, a16, N) == want, N
     assert lib.spx_spmm_csr_variant(32, ctypes.c_void_p((1 << 20) + 4), 32, a16, 32) == 3  # misaligned B
     assert lib.spx_spmm_csr_variant(32, a16, 34, a16, 32) == 3  # ldb not a multiple of 4
+
+
+def test_coo_spmv_rejects_bad_arguments_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    a = ctypes.c_void_p(1 << 20)
+    big = ctypes.c_void_p(1 << 30)
+    # scratch: two floats per 2048 entries
+    assert spx.spx_spmv_coo_scratch_bytes(0) == 0
+    assert spx.spx_spmv_coo_scratch_bytes(1) == 8
+    assert spx.spx_spmv_coo_scratch_bytes(2048) == 8
+    assert spx.spx_spmv_coo_scratch_bytes(2049) == 16
+    assert lib.spx_spmv_coo(-1, 4, 1, a, a, a, 1.0, a, 0.0, big, a, 8, None) == -1
+    assert lib.spx_spmv_coo(4, 4, 1 << 31, a, a, a, 1.0, a, 0.0, big, a, 1 << 22, None) == -2
+    assert lib.spx_spmv_coo(4, 4, 1, None, a, a, 1.0, a, 0.0, big, a, 8, None) == -1
+    assert lib.spx_spmv_coo(4, 4, 3000, a, a, a, 1.0, a, 0.0, big, a, 8, None) == -1      # scratch too small
+    assert lib.spx_spmv_coo(4, 4, 1, a, a, a, 1.0, a, 0.0, a, big, 8, None) == -1          # x and y overlap
+    assert lib.spx_spmv_coo(4, 4, 1, ctypes.c_void_p((1 << 20) + 2), a, a, 1.0, a, 0.0, big, a, 8, None) == -8
+    assert lib.spx_spmv_coo(0, 4, 1, a, a, a, 1.0, a, 0.0, big, a, 8, None) == -2          # entries but no rows
+    assert lib.spx_spmv_coo(0, 4, 0, None, None, None, 1.0, None, 0.0, big, None, 0, None) == 0
+    assert spx.launch_count() == before

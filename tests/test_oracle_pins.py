@@ -99,6 +99,21 @@ def test_worked_example_spmv(ex):
         assert ref.tolist() == dense[:, j].tolist()
 
 
+def test_worked_example_coo_spmv(ex):
+    """The page's triplet list, multiplied as triplets, gives the row sums."""
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]
+    ref, _ = oracle.spmv_coo(5, 5, p["coo_row"], p["coo_col"], val, np.ones(5, np.float32))
+    assert ref.tolist() == d["y_for_x_all_ones"]
+
+
+def test_coo_index_range_rejected():
+    with pytest.raises(Exception):
+        oracle.spmv_coo(2, 2, [0, 2], [0, 1], [1.0, 1.0], np.ones(2, np.float32))
+    with pytest.raises(Exception):
+        oracle.spmv_coo(2, 2, [0, 1], [0, 2], [1.0, 1.0], np.ones(2, np.float32))
+
+
 # ------------------------------------------------------------ brute force
 
 def _dense(M, K, row, col, val):
@@ -129,6 +144,12 @@ def test_bruteforce_spmv_spmm(M, K, lmin, lmax, seed):
         C = np.floor(synth.uniform(seed, synth.T_Y, M * N, -3, 4)).astype(np.float32).reshape(M, N)
         ref, _ = oracle.spmm(M, rp, col, val, B, alpha=-1.0, beta=0.5, C=C)
         assert np.array_equal(ref, -(A @ B.astype(np.float64)) + 0.5 * C)
+    # COO product straight from the triplets, in the generator's order and shuffled
+    for order in (np.arange(d["row"].size), synth.permutation(seed, d["row"].size)):
+        refc, boundc = oracle.spmv_coo(M, K, d["row"][order], d["col"][order], d["val"][order], x, alpha=2.0,
+                                       beta=-3.0, y=y)
+        assert np.array_equal(refc, 2.0 * (A @ x.astype(np.float64)) - 3.0 * y)
+        assert np.array_equal(boundc, 2.0 * (np.abs(A) @ np.abs(x.astype(np.float64))) + 3.0 * np.abs(y))
     # the dual direction: CSR(A^T) times u equals the transposed dense product
     trp, tc, tv = oracle.transpose(M, K, rp, col, val)
     u = np.floor(synth.uniform(seed, 7, M, -3, 4)).astype(np.float32)
