@@ -236,11 +236,16 @@ def run_ours(args, rank, world):
 
     if w in ("power-law", "uniform"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
-        t0 = time.perf_counter()
-        plan = spx.spx_plan_csr(M, K, A.nnz, rp, opts=args.plan_opts, device=dev, stream=stream)
-        timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         x = to_dev(c["x"])
         y = to_dev(c["y"])
+        opts = args.plan_opts
+        if args.tune:
+            t0 = time.perf_counter()
+            opts, tune_ms, _ = spx.spx_plan_autotune(A, rp, x, stream=stream)
+            timings["tune_ms"] = 1e3 * (time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        plan = spx.spx_plan_csr(M, K, A.nnz, rp, opts=opts, device=dev, stream=stream)
+        timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         alpha, beta = c["alpha"], c["beta"]
         src = source_hash("spx_spmv.cu")
 
@@ -297,9 +302,15 @@ def run_ours(args, rank, world):
         trp, tc, tv = spx.spx_transpose_csr(M, K, rp, col, val)
         timings["transpose_ms"] = 1e3 * (time.perf_counter() - t0)
         At = spx.Csr(K, M, to_dev(trp), to_dev(tc), to_dev(tv))
+        oA = oAt = args.plan_opts
+        if args.tune:
+            t1 = time.perf_counter()
+            oA, _, _ = spx.spx_plan_autotune(A, rp, to_dev(c["v0"]), stream=stream)
+            oAt, _, _ = spx.spx_plan_autotune(At, trp, to_dev(c["u0"]), stream=stream)
+            timings["tune_ms"] = 1e3 * (time.perf_counter() - t1)
         t0 = time.perf_counter()
-        pA = spx.spx_plan_csr(M, K, A.nnz, rp, opts=args.plan_opts, device=dev, stream=stream)
-        pAt = spx.spx_plan_csr(K, M, A.nnz, trp, opts=args.plan_opts, device=dev, stream=stream)
+        pA = spx.spx_plan_csr(M, K, A.nnz, rp, opts=oA, device=dev, stream=stream)
+        pAt = spx.spx_plan_csr(K, M, A.nnz, trp, opts=oAt, device=dev, stream=stream)
         timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         u = to_dev(c["u0"])
         v = to_dev(c["v0"])
@@ -575,6 +586,7 @@ def main():
     ap.add_argument("--workload", default="power-law",
                     choices=["power-law", "power-law-coo", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
                              "spmm128-bf16", "bsr"])
+    ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

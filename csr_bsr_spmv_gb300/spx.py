@@ -85,6 +85,10 @@ def _lib():
             "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
             "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
             "spx_plan_destroy": ([vp], ctypes.c_int),
+            "spx_plan_autotune": ([i32, i32, i64, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanOpts), i32, i32, vp,
+                                   ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_float),
+                                   ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "spx_plan_autotune_forget": ([], ctypes.c_int),
             "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
             "spx_spmv_coo_scratch_bytes": ([i64], sz),
@@ -293,6 +297,35 @@ class Plan:
 
 def spx_plan_csr(M: int, K: int, nnz: int, row_ptr, opts: dict | None = None, **kw) -> Plan:
     return Plan(M, K, nnz, row_ptr, opts, **kw)
+
+
+def spx_plan_autotune(A: "Csr", row_ptr_host, x: torch.Tensor, candidates: list[dict] | None = None, reps: int = 5,
+                      stream=None, y_scratch: torch.Tensor | None = None):
+    """Time candidate plan options on the device (cached per matrix profile).
+    Returns (best options dict, per-candidate mean ms or -1 when cached, cached flag)."""
+    rp = np.ascontiguousarray(row_ptr_host, dtype=np.int32)
+    n = len(candidates) if candidates else 4
+    cand = None
+    if candidates:
+        arr = (PlanOpts * n)()
+        for i, c in enumerate(candidates):
+            base = spx_plan_opts_default()
+            base.update(c)
+            arr[i] = PlanOpts(**base)
+        cand = arr
+    ys = torch.empty(max(A.M, 1), dtype=torch.float32, device=x.device) if y_scratch is None else y_scratch
+    best = PlanOpts()
+    times = (ctypes.c_float * n)()
+    cached = ctypes.c_int32(0)
+    _check(_lib().spx_plan_autotune(A.M, A.K, A.nnz, _ptr(rp), _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
+                                    _ptr(x), _ptr(ys), cand, n if cand is not None else 0, int(reps),
+                                    _stream(stream), ctypes.byref(best), times, ctypes.byref(cached)),
+           "spx_plan_autotune")
+    return {f: getattr(best, f) for f, _ in PlanOpts._fields_}, [float(t) for t in times], bool(cached.value)
+
+
+def spx_plan_autotune_forget():
+    _check(_lib().spx_plan_autotune_forget(), "spx_plan_autotune_forget")
 
 
 @dataclass

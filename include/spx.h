@@ -224,6 +224,36 @@ spx_status spx_plan_upload(spx_plan* plan, void* table, size_t table_bytes, spx_
 
 spx_status spx_plan_destroy(spx_plan* plan);
 
+/*
+ * Measured choice of plan options, cached per matrix profile.  [SpMM-ops] §4
+ * (profile the matrix once -- row-length statistics as the dispatch key --
+ * pick the mapping, keep the choice with the matrix).  Times each candidate
+ * option set with spx_spmv_csr on `stream` (one warm-up, then `reps` timed
+ * calls, CUDA events) on the caller's matrix and x, and returns the fastest
+ * in *best.
+ *   row_ptr_host: the row offsets in host memory (for the plans and the key);
+ *   row_ptr, col, val, x: the matrix and a representative x in device memory;
+ *   y_scratch: device fp32[M], overwritten (alpha 1, beta 0).
+ *   candidates: ncand (1..16) option sets, or NULL for the built-in four:
+ *     the defaults (B 2048, D 16); D 4; the segmented reduction (D 0) with
+ *     B 1024; and with B 2048.
+ *   times_ms: optional, ncand (or 4) floats: mean time per call of each
+ *     candidate; -1 when the answer came from the cache.
+ *   cached: optional; 1 when the answer came from the cache, else 0.
+ * The cache is process-wide, keyed by the device, M, K, nnz, the row-length
+ * sum of squares, maximum and 99th percentile, and the candidate list: a
+ * matrix with the same profile reuses the choice without timing.  Unlike
+ * the compute calls, this one allocates and frees device memory for the
+ * candidate plans (cudaMalloc / cudaFree) and synchronises `stream`.
+ */
+spx_status spx_plan_autotune(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr_host, const int32_t* row_ptr,
+                             const int32_t* col, const float* val, const float* x, float* y_scratch,
+                             const spx_plan_opts_t* candidates, int32_t ncand, int32_t reps, spx_stream_t stream,
+                             spx_plan_opts_t* best, float* times_ms, int32_t* cached);
+
+/* Empties the spx_plan_autotune cache. */
+spx_status spx_plan_autotune_forget(void);
+
 /* ------------------------------------------------------------ SpMV */
 
 /*

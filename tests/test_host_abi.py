@@ -244,3 +244,21 @@ def test_coo_spmv_rejects_bad_arguments_without_launching():
     assert lib.spx_spmv_coo(0, 4, 1, a, a, a, 1.0, a, 0.0, big, a, 8, None) == -2          # entries but no rows
     assert lib.spx_spmv_coo(0, 4, 0, None, None, None, 1.0, None, 0.0, big, None, 0, None) == 0
     assert spx.launch_count() == before
+
+
+def test_autotune_rejects_bad_arguments_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    rp = np.array([0, 1, 2], np.int32)
+    a = ctypes.c_void_p(1 << 20)
+    best = spx.PlanOpts()
+    P = spx._ptr(rp)
+    assert lib.spx_plan_autotune(2, 2, 2, None, a, a, a, a, a, None, 0, 3, None, ctypes.byref(best), None, None) == -1
+    assert lib.spx_plan_autotune(2, 2, 2, P, a, a, a, a, a, None, 0, 0, None, ctypes.byref(best), None, None) == -1
+    assert lib.spx_plan_autotune(2, 2, 2, P, a, a, a, a, a, None, 0, 3, None, None, None, None) == -1
+    assert lib.spx_plan_autotune(2, 2, 3, P, a, a, a, a, a, None, 0, 3, None, ctypes.byref(best), None, None) == -1
+    cand = (spx.PlanOpts * 1)()
+    assert lib.spx_plan_autotune(2, 2, 2, P, a, a, a, a, a, cand, 0, 3, None, ctypes.byref(best), None, None) == -1
+    assert lib.spx_plan_autotune(2, 2, 2, P, a, a, a, a, a, cand, 17, 3, None, ctypes.byref(best), None, None) == -1
+    assert lib.spx_plan_autotune_forget() == 0
+    assert spx.launch_count() == before
