@@ -7,7 +7,7 @@ is one SpMV call through the C ABI: the binned main launch plus the long-row
 fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload power-law|power-law-coo|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr]
+                    [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -143,10 +143,12 @@ def make_workload(name: str, rows: int = 0):
     """Host arrays of the workload; `rows` shrinks the power-law case (profiling)."""
     import synth
 
-    if name in ("power-law", "power-law-coo"):
+    if name in ("power-law", "power-law-coo", "power-law-sell"):
         c = synth.power_law_rows(M=rows) if rows else synth.power_law_rows()
         if name == "power-law-coo":
             c["name"] += " as row-sorted COO"
+        if name == "power-law-sell":
+            c["name"] += " as SELL-C-sigma (C 32)"
     elif name == "uniform":
         c = synth.uniform_short_rows()
     elif name == "dual":
@@ -170,7 +172,7 @@ def accounting(c):
     """(flops, algorithmic bytes) of one step, by the compulsory-traffic rules."""
     M, K, nnz = c["M"], c["K"], c["row"].size
     w = c["workload"]
-    if w in ("power-law", "uniform"):
+    if w in ("power-law", "uniform", "power-law-sell"):  # SELL: the CSR definition's bytes (padding is overhead)
         ybytes = 8 * M if c["beta"] != 0 else 4 * M
         return 2 * nnz, 8 * nnz + 4 * (M + 1) + 4 * K + ybytes
     if w == "power-law-coo":  # row index per entry instead of row offsets
@@ -270,6 +272,33 @@ def run_ours(args, rank, world):
         extra = {"plan": {k: info[k] for k in ("tasks", "long_rows", "cta_rows", "split_rows", "thread_groups",
                                                 "lane_groups", "segmented_groups")},
                  "plan_opts": plan.opts, "row_stats": plan.stats}
+    elif w == "power-law-sell":
+        x = to_dev(c["x"])
+        y = to_dev(c["y"])
+        alpha, beta = c["alpha"], c["beta"]
+        t0 = time.perf_counter()
+        S = spx.Sell(M, K, rp, col, val, opts=args.plan_opts, device=dev, stream=stream)
+        timings["build_sell_ms"] = 1e3 * (time.perf_counter() - t0)
+        src = source_hash("spx_sell.cu")
+
+        def run():
+            spx.spx_spmv_sell(S, x, y, alpha, beta, stream=stream)
+
+        xh = torch.from_numpy(c["x"]).pin_memory()
+        yh = torch.from_numpy(c["y"]).pin_memory()
+        yo = torch.empty_like(yh).pin_memory()
+        h2d = xh.numel() * 4 + (yh.numel() * 4 if beta != 0 else 0)
+        d2h = yo.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                x.copy_(xh, non_blocking=True)
+                if beta != 0:
+                    y.copy_(yh, non_blocking=True)
+                spx.spx_spmv_sell(S, x, y, alpha, beta, stream=stream)
+                yo.copy_(y, non_blocking=True)
+
+        extra = {"sell": dict(S.info), "sell_opts": S.opts}
     elif w == "power-law-coo":
         crow, ccol, cval = to_dev(c["row"]), to_dev(c["col"]), to_dev(c["val"])
         x = to_dev(c["x"])
@@ -519,7 +548,7 @@ def cpu_step_fn(c):
         return (lambda: oracle.spmv_coo(M, K, c["row"], c["col"], c["val"], c["x"], c["alpha"], c["beta"],
                                         c["y"])), 2 * int(c["row"].size), "the full matrix, one COO SpMV"
     rp, col, val = row_major_csr(c, c["val"])
-    if w in ("power-law", "uniform"):
+    if w in ("power-law", "uniform", "power-law-sell"):
         return (lambda: oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"])), 2 * int(rp[-1]), \
             "the full matrix, one SpMV"
     if w == "dual":
@@ -584,7 +613,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
-                    choices=["power-law", "power-law-coo", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
+                    choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
                              "spmm128-bf16", "bsr"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-e2e", action="store_true")

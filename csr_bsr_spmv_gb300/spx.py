@@ -57,6 +57,17 @@ class PlanInfo(ctypes.Structure):
                 ("scratch_bytes", ctypes.c_size_t), ("stats", RowStats), ("opts", PlanOpts)]
 
 
+class SellOpts(ctypes.Structure):
+    _fields_ = [("sigma", ctypes.c_int32), ("piece", ctypes.c_int32)]
+
+
+class SellInfo(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("K", ctypes.c_int64), ("nnz", ctypes.c_int64), ("slices", ctypes.c_int64),
+                ("pseudo_rows", ctypes.c_int64), ("padded", ctypes.c_int64), ("long_rows", ctypes.c_int64),
+                ("slots", ctypes.c_int64), ("image_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t),
+                ("opts", SellOpts)]
+
+
 _LIB = None
 
 
@@ -89,6 +100,14 @@ def _lib():
                                    ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_float),
                                    ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "spx_plan_autotune_forget": ([], ctypes.c_int),
+            "spx_sell_opts_default": ([ctypes.POINTER(SellOpts)], ctypes.c_int),
+            "spx_sell_build": ([i32, i32, i64, vp, vp, vp, ctypes.c_int, ctypes.POINTER(SellOpts),
+                                ctypes.POINTER(vp)], ctypes.c_int),
+            "spx_sell_get_info": ([vp, ctypes.POINTER(SellInfo)], ctypes.c_int),
+            "spx_sell_get_arrays": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "spx_sell_upload": ([vp, vp, sz, vp], ctypes.c_int),
+            "spx_sell_destroy": ([vp], ctypes.c_int),
+            "spx_spmv_sell": ([vp, i32, i32, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
             "spx_spmv_coo_scratch_bytes": ([i64], sz),
@@ -297,6 +316,69 @@ class Plan:
 
 def spx_plan_csr(M: int, K: int, nnz: int, row_ptr, opts: dict | None = None, **kw) -> Plan:
     return Plan(M, K, nnz, row_ptr, opts, **kw)
+
+
+class Sell:
+    """Owns an spx_sell* (SELL-C-sigma form of a CSR), its device image and scratch."""
+
+    def __init__(self, M: int, K: int, row_ptr, col, val, opts: dict | None = None, upload=True, device=None,
+                 stream=None):
+        lib = _lib()
+        o = None
+        if opts:
+            base = SellOpts()
+            _check(lib.spx_sell_opts_default(ctypes.byref(base)), "spx_sell_opts_default")
+            d = {f: getattr(base, f) for f, _ in SellOpts._fields_}
+            d.update(opts)
+            o = SellOpts(**d)
+        h = ctypes.c_void_p()
+        nnz = col.numel() if isinstance(col, torch.Tensor) else int(np.asarray(col).size)
+        _check(lib.spx_sell_build(M, K, nnz, _ptr(row_ptr), _ptr(col), _ptr(val), _where(row_ptr),
+                                  ctypes.byref(o) if o else None, ctypes.byref(h)), "spx_sell_build")
+        self.handle = h
+        self.M, self.K, self.nnz = M, K, nnz
+        info = SellInfo()
+        _check(lib.spx_sell_get_info(h, ctypes.byref(info)), "spx_sell_get_info")
+        self.info = {f: getattr(info, f) for f, _ in SellInfo._fields_ if f != "opts"}
+        self.opts = {f: getattr(info.opts, f) for f, _ in SellOpts._fields_}
+        self.image = None
+        self.scratch = None
+        if upload:
+            dev = device or (row_ptr.device if isinstance(row_ptr, torch.Tensor) and row_ptr.is_cuda else "cuda")
+            self.image = torch.empty(max(1, (self.info["image_bytes"] + 15) // 16 * 4), dtype=torch.int32,
+                                     device=dev)
+            self.scratch = torch.empty(max(1, self.info["scratch_bytes"] // 4), dtype=torch.float32, device=dev)
+            _check(lib.spx_sell_upload(h, _ptr(self.image), self.image.numel() * 4, _stream(stream)),
+                   "spx_sell_upload")
+
+    def arrays(self):
+        i = self.info
+        sp = np.empty(i["slices"] + 1, np.int32)
+        pr = np.empty(32 * i["slices"], np.int32)
+        lr = np.empty((i["long_rows"], 4), np.int32)
+        sc = np.empty(i["padded"], np.int32)
+        sv = np.empty(i["padded"], np.float32)
+        _check(_lib().spx_sell_get_arrays(self.handle, _ptr(sp), _ptr(pr), _ptr(lr), _ptr(sc), _ptr(sv)),
+               "spx_sell_get_arrays")
+        return sp, pr, lr, sc, sv
+
+    def close(self):
+        if self.handle:
+            _lib().spx_sell_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spx_spmv_sell(S: Sell, x: torch.Tensor, y: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """y <- alpha*A*x + beta*y with A in uploaded SELL-C-sigma form."""
+    _check(_lib().spx_spmv_sell(S.handle, S.M, S.K, float(alpha), _ptr(x), float(beta), _ptr(y), _ptr(S.scratch),
+                                S.scratch.numel() * 4, _stream(stream)), "spx_spmv_sell")
+    return y
 
 
 def spx_plan_autotune(A: "Csr", row_ptr_host, x: torch.Tensor, candidates: list[dict] | None = None, reps: int = 5,

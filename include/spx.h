@@ -364,6 +364,77 @@ spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* r
    0 = small-N, 1 = float4 with N <= 128, 2 = float4 with N > 128, 3 = scalar. */
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);
 
+/* ------------------------------------------------------------ SELL-C-sigma */
+
+/*
+ * Sliced ELLPACK, C = 32 ([SpMM-ops] §1.4 and [Formats] §6: rows sorted by
+ * length inside windows of sigma rows, slices of C rows padded to their
+ * longest row and stored column-major, so the C threads of a slice read
+ * consecutive words).  Rows longer than `piece` entries are first cut into
+ * pieces of `piece` entries, each sorted and sliced like a row; a second
+ * launch adds each long row's pieces in piece order.
+ *   sigma: window of pseudo-rows sorted together, a multiple of 32 in
+ *          [32, 2^20]; piece: in [1, 2^24].  Defaults: sigma 1024, piece 64
+ *          (fastest of a sweep on a power-law matrix, mean row length 16).
+ */
+typedef struct spx_sell_opts_t {
+    int32_t sigma;
+    int32_t piece;
+} spx_sell_opts_t;
+
+typedef struct spx_sell_info_t {
+    int64_t M, K, nnz;
+    int64_t slices;       /* ceil(pseudo_rows / 32)                          */
+    int64_t pseudo_rows;  /* rows of length <= piece, plus the pieces        */
+    int64_t padded;       /* stored entries including padding (32 per slice
+                             per position up to the slice's longest row)     */
+    int64_t long_rows;    /* rows cut into pieces                            */
+    int64_t slots;        /* partial sums (one per piece)                    */
+    size_t image_bytes;   /* device bytes for spx_sell_upload                */
+    size_t scratch_bytes; /* device scratch bytes of each spx_spmv_sell call */
+    spx_sell_opts_t opts;
+} spx_sell_info_t;
+
+typedef struct spx_sell spx_sell; /* opaque, host-side */
+
+spx_status spx_sell_opts_default(spx_sell_opts_t* out);
+
+/*
+ * Build the SELL-C-sigma form of a CSR matrix (host or device arrays; device
+ * arrays are copied to the host).  Pseudo-rows are listed in row order (a
+ * long row's pieces in piece order), stably sorted by length, longest first,
+ * inside each window of sigma pseudo-rows, then cut into slices of 32.
+ * Within a slice, entry j of lane r sits at slice_ptr[s] + 32 j + r; padding
+ * has column -1 and value 0.  prow holds the row of each pseudo-row, -1-slot
+ * for a piece, INT32_MIN for the unused lanes of the last slice.  opts NULL:
+ * the defaults.  Errors: SPX_ERR_NOT_SORTED (row_ptr decreasing),
+ * SPX_ERR_INDEX_RANGE (a column outside [0, K) or more than 2^31-1 padded
+ * entries).  Release with spx_sell_destroy.
+ */
+spx_status spx_sell_build(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                          const float* val, spx_loc where, const spx_sell_opts_t* opts, spx_sell** out);
+spx_status spx_sell_get_info(const spx_sell* sell, spx_sell_info_t* out);
+/* Host copies of slice_ptr[slices+1], prow[32 slices], longrows[4 long_rows]
+   ({row, first slot, #pieces, 0}), scol[padded], sval[padded]; any may be NULL. */
+spx_status spx_sell_get_arrays(const spx_sell* sell, int32_t* slice_ptr, int32_t* prow, int32_t* longrows,
+                               int32_t* scol, float* sval);
+/* Copy the format into caller-owned device memory (info.image_bytes, 16-byte
+   aligned) and remember the address; required before spx_spmv_sell. */
+spx_status spx_sell_upload(spx_sell* sell, void* image, size_t image_bytes, spx_stream_t stream);
+spx_status spx_sell_destroy(spx_sell* sell);
+
+/*
+ * y = alpha * A x + beta * y with A in uploaded SELL-C-sigma form: one warp
+ * per slice, one thread per pseudo-row, coalesced column-major loads, x
+ * gathered through the read-only path; pieces write partial sums to
+ * `scratch` (info.scratch_bytes) and a second launch (one warp per long
+ * row) adds them in piece order and applies alpha/beta.  Deterministic
+ * (fixed summation order).  x[K], y[M] device fp32, not overlapping.
+ * Launches: 1, plus 1 when the matrix has long rows.
+ */
+spx_status spx_spmv_sell(const spx_sell* sell, int32_t M, int32_t K, float alpha, const float* x, float beta,
+                         float* y, void* scratch, size_t scratch_bytes, spx_stream_t stream);
+
 /*
  * COO SpMV y = alpha * A x + beta * y over triplets sorted by row (columns in
  * any order within a row; duplicates allowed and summed as separate terms).

@@ -68,6 +68,9 @@ def _lib_():
                 "or_plan_opts_auto": [vp, vp],
                 "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
                 "or_spmv_coo": [i32, i32, i64, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
+                "or_build_sell": [i32, vp, vp, vp, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.POINTER(ctypes.c_int64), vp, vp, vp, vp, vp],
                 "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
                 "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
             }
@@ -137,6 +140,25 @@ def build_bsr(M, K, rp, col, val, br, bc):
     _check(lib.or_build_bsr(M, K, _p(rp), _p(col), _p(val), val.itemsize, br, bc, _p(brp), _p(bcol), _p(bval),
                             ctypes.byref(nnzb), ctypes.byref(fill)))
     return brp, bcol, bval.reshape(nb, br, bc), fill.value
+
+
+def build_sell(M, rp, col, val, sigma=1024, piece=64):
+    """SELL-C-sigma (C = 32) with rows longer than `piece` cut into pieces.
+    Returns (slice_ptr, prow, longrows[nlong, 4], scol, sval)."""
+    rp, col, val = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32)
+    n = [ctypes.c_int64(0) for _ in range(4)]
+    lib = _lib_()
+    _check(lib.or_build_sell(M, _p(rp), _p(col), _p(val), sigma, piece, *[ctypes.byref(v) for v in n],
+                             None, None, None, None, None))
+    npseudo, ns, pad, nl = (v.value for v in n)
+    sp = np.empty(ns + 1, np.int32)
+    pr = np.empty(32 * ns, np.int32)
+    lr = np.empty((nl, 4), np.int32)
+    sc = np.empty(pad, np.int32)
+    sv = np.empty(pad, np.float32)
+    _check(lib.or_build_sell(M, _p(rp), _p(col), _p(val), sigma, piece, *[ctypes.byref(v) for v in n], _p(sp),
+                             _p(pr), _p(lr), _p(sc), _p(sv)))
+    return sp, pr, lr, sc, sv
 
 
 def row_stats(M, rp):

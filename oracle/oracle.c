@@ -416,6 +416,105 @@ int or_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* row, const int
     return OR_OK;
 }
 
+/*
+ * SELL-C-sigma with C = 32.  [SpMM-ops] §1.4 and [Formats] §6 (sliced
+ * ELLPACK: sort rows by length inside windows of sigma rows, cut slices of C
+ * rows, pad each slice to its longest row, store the slice column-major).
+ * Rows longer than `piece` are first cut into pieces of `piece` entries (the
+ * last one shorter); every row or piece is a "pseudo-row", listed in row
+ * order (pieces in piece order).  Inside each window of sigma pseudo-rows the
+ * pseudo-rows are emitted longest first, equal lengths in their listed order:
+ * here by sweeping the lengths from the window's maximum down to 0 and
+ * emitting each match in list order (no sort routine).  Layout: entry j of
+ * lane r of slice s at slice_ptr[s] + 32 j + r; padding col -1, val 0.
+ * prow: the row, or -1 - slot for a piece (slots numbered in listing order),
+ * INT32_MIN for unused lanes of the last slice.  longrows: {row, first slot,
+ * #pieces, 0} per cut row.  Two calls: with scol == NULL only the sizes
+ * (npseudo, nslices, padded, nlong) are produced.
+ */
+int or_build_sell(int32_t M, const int32_t* rp, const int32_t* col, const float* val, int32_t sigma, int32_t piece,
+                  int64_t* npseudo, int64_t* nslices, int64_t* padded, int64_t* nlong, int32_t* slice_ptr,
+                  int32_t* prow, int32_t* longrows, int32_t* scol, float* sval) {
+    if (M < 0 || sigma < 32 || sigma % 32 || piece < 1) return OR_ERR_ARG;
+    int64_t np = 0, nl = 0;
+    for (int32_t i = 0; i < M; ++i) {
+        int32_t l = rp[i + 1] - rp[i];
+        if (l > piece) {
+            np += (l + piece - 1) / piece;
+            ++nl;
+        } else {
+            ++np;
+        }
+    }
+    /* the listing: (len, row, start, slot) */
+    int32_t* L = (int32_t*)malloc(sizeof(int32_t) * (size_t)(4 * (np ? np : 1)));
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(np ? np : 1));
+    if (!L || !order) {
+        free(L);
+        free(order);
+        return OR_ERR_NOMEM;
+    }
+    int64_t q = 0, slot = 0, li = 0;
+    for (int32_t i = 0; i < M; ++i) {
+        int32_t l = rp[i + 1] - rp[i];
+        if (l <= piece) {
+            L[4 * q] = l; L[4 * q + 1] = i; L[4 * q + 2] = rp[i]; L[4 * q + 3] = -1;
+            ++q;
+            continue;
+        }
+        int32_t n = (l + piece - 1) / piece;
+        if (longrows) {
+            longrows[4 * li] = i; longrows[4 * li + 1] = (int32_t)slot; longrows[4 * li + 2] = n;
+            longrows[4 * li + 3] = 0;
+        }
+        ++li;
+        for (int32_t k = 0; k < n; ++k) {
+            int32_t len = l - k * piece < piece ? l - k * piece : piece;
+            L[4 * q] = len; L[4 * q + 1] = i; L[4 * q + 2] = rp[i] + k * piece; L[4 * q + 3] = (int32_t)(slot + k);
+            ++q;
+        }
+        slot += n;
+    }
+    /* window order: lengths swept from the maximum down, list order within a length */
+    int64_t o = 0;
+    for (int64_t w0 = 0; w0 < np; w0 += sigma) {
+        int64_t w1 = w0 + sigma < np ? w0 + sigma : np;
+        int32_t mx = 0;
+        for (int64_t p = w0; p < w1; ++p) if (L[4 * p] > mx) mx = L[4 * p];
+        for (int32_t len = mx; len >= 0; --len)
+            for (int64_t p = w0; p < w1; ++p)
+                if (L[4 * p] == len) order[o++] = p;
+    }
+    int64_t ns = (np + 31) / 32, pad = 0;
+    for (int64_t s = 0; s < ns; ++s) {
+        int32_t mx = 0;
+        for (int64_t r = 0; r < 32 && s * 32 + r < np; ++r) {
+            int32_t len = L[4 * order[s * 32 + r]];
+            if (len > mx) mx = len;
+        }
+        if (slice_ptr) slice_ptr[s] = (int32_t)pad;
+        pad += 32 * (int64_t)mx;
+    }
+    if (slice_ptr) slice_ptr[ns] = (int32_t)pad;
+    *npseudo = np; *nslices = ns; *padded = pad; *nlong = nl;
+    if (scol && sval && prow && slice_ptr) {
+        for (int64_t e = 0; e < pad; ++e) { scol[e] = -1; sval[e] = 0.0f; }
+        for (int64_t t = 0; t < 32 * ns; ++t) {
+            if (t >= np) { prow[t] = INT32_MIN; continue; }
+            const int32_t* d = L + 4 * order[t];
+            prow[t] = d[3] < 0 ? d[1] : -1 - d[3];
+            int64_t s = t / 32, r = t % 32;
+            for (int32_t j = 0; j < d[0]; ++j) {
+                scol[slice_ptr[s] + 32 * (int64_t)j + r] = col[d[2] + j];
+                sval[slice_ptr[s] + 32 * (int64_t)j + r] = val[d[2] + j];
+            }
+        }
+    }
+    free(L);
+    free(order);
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------ SpMM */
 
 /*

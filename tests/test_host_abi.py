@@ -262,3 +262,39 @@ def test_autotune_rejects_bad_arguments_without_launching():
     assert lib.spx_plan_autotune(2, 2, 2, P, a, a, a, a, a, cand, 17, 3, None, ctypes.byref(best), None, None) == -1
     assert lib.spx_plan_autotune_forget() == 0
     assert spx.launch_count() == before
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 1), (40, 30, 0, 9), (0, 3, 0, 1), (700, 900, 0, 300)])
+@pytest.mark.parametrize("opts", [None, dict(sigma=32, piece=5), dict(sigma=96, piece=64), dict(sigma=1 << 20)])
+def test_sell_matches_oracle(M, K, lmin, lmax, opts):
+    d = synth.random_coo(33, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    S = spx.Sell(M, K, rp, col, val, opts=opts, upload=False)
+    o = dict(sigma=1024, piece=64)
+    o.update(opts or {})
+    assert S.opts == o
+    want = oracle.build_sell(M, rp, col, val, **o)
+    got = S.arrays()
+    for w, g in zip(want, got):
+        assert np.array_equal(w, g)
+    assert S.info["slices"] == want[0].size - 1 and S.info["padded"] == want[3].size
+    assert S.info["scratch_bytes"] == 4 * int(want[2][:, 2].sum()) if want[2].size else S.info["scratch_bytes"] == 0
+
+
+def test_sell_rejects_bad_input_and_unuploaded_use():
+    lib = spx._lib()
+    rp = np.array([0, 1, 2], np.int32)
+    for o in (dict(sigma=48), dict(sigma=16), dict(piece=0)):
+        with pytest.raises(spx.SpxError):
+            spx.Sell(2, 2, rp, np.array([0, 1], np.int32), np.ones(2, np.float32), opts=o, upload=False)
+    with pytest.raises(spx.SpxError):  # column out of range
+        spx.Sell(2, 2, rp, np.array([0, 2], np.int32), np.ones(2, np.float32), upload=False)
+    with pytest.raises(spx.SpxError):  # row_ptr decreasing
+        spx.Sell(2, 2, np.array([0, 2, 1], np.int32), np.array([0, 1], np.int32), np.ones(2, np.float32),
+                 upload=False)
+    S = spx.Sell(2, 2, rp, np.array([0, 1], np.int32), np.ones(2, np.float32), upload=False)
+    before = spx.launch_count()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.spx_spmv_sell(S.handle, 2, 2, 1.0, a, 0.0, ctypes.c_void_p(1 << 22), None, 0, None) == -10
+    assert lib.spx_spmv_sell(S.handle, 3, 2, 1.0, a, 0.0, ctypes.c_void_p(1 << 22), None, 0, None) == -1
+    assert spx.launch_count() == before

@@ -107,6 +107,84 @@ def test_worked_example_coo_spmv(ex):
     assert ref.tolist() == d["y_for_x_all_ones"]
 
 
+def test_worked_example_sell(ex):
+    """SELL-C-sigma of the printed matrix (sigma 32, pieces of 2), worked out by hand."""
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]["sell_sigma32_piece2"]
+    sp, pr, lr, sc, sv = oracle.build_sell(5, p["csr_row_ptr"], p["csr_col"], val, sigma=32, piece=2)
+    assert sp.tolist() == d["slice_ptr"]
+    assert pr[:6].tolist() == d["prow_used"] and np.all(pr[6:] == np.iinfo(np.int32).min)
+    assert lr.tolist() == d["longrows"]
+    assert sc[:6].tolist() == d["scol_j0_used"] and sc[32:38].tolist() == d["scol_j1_used"]
+    assert sv[:6].tolist() == _vals(d["sval_j0_used"], v) and sv[32:38].tolist() == _vals(d["sval_j1_used"], v)
+    assert np.all(sc[6:32] == -1) and np.all(sc[38:] == -1) and not sv[6:32].any() and not sv[38:].any()
+
+
+def sell_rows(M, sp, pr, lr, sc, sv):
+    """Each row's (col, val) entries read back out of the SELL arrays: whole
+    rows from their lane, long rows by concatenating their pieces in slot order."""
+    piece_of = {}
+    rows = {i: ([], []) for i in range(M)}
+    for t, r in enumerate(pr):
+        if r == np.iinfo(np.int32).min:
+            continue
+        s, lane = divmod(t, 32)
+        L = (sp[s + 1] - sp[s]) // 32
+        idx = sp[s] + 32 * np.arange(L) + lane
+        keep = sc[idx] >= 0
+        ent = (sc[idx][keep].tolist(), sv[idx][keep].tolist())
+        if r >= 0:
+            rows[r] = ent
+        else:
+            piece_of[-1 - r] = ent
+    for row, first, n, _ in lr:
+        cs, vs = [], []
+        for k in range(n):
+            cs += piece_of[first + k][0]
+            vs += piece_of[first + k][1]
+        rows[row] = (cs, vs)
+    return rows
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 1), (7, 5, 0, 5), (33, 64, 0, 9), (50, 50, 0, 0), (0, 4, 0, 2),
+                                          (300, 500, 0, 120)])
+@pytest.mark.parametrize("sigma,piece", [(32, 1), (32, 7), (64, 16), (256, 256)])
+def test_sell_round_trip_and_order(M, K, lmin, lmax, sigma, piece):
+    """Reading the rows back out of SELL gives the CSR exactly; windows are
+    sorted longest first, equal lengths in listing order; slices are as wide
+    as their longest pseudo-row; padding is (-1, 0)."""
+    d = synth.random_coo(31, M, K, lmin, lmax, values="int")
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    sp, pr, lr, sc, sv = oracle.build_sell(M, rp, col, val, sigma=sigma, piece=piece)
+    rows = sell_rows(M, sp, pr, lr, sc, sv)
+    for i in range(M):
+        assert rows[i][0] == col[rp[i]:rp[i + 1]].tolist()
+        assert rows[i][1] == val[rp[i]:rp[i + 1]].tolist()
+    # listing: (row, piece index, length) in row order
+    listing = []
+    for i in range(M):
+        l = int(rp[i + 1] - rp[i])
+        if l <= piece:
+            listing.append((i, 0, l))
+        else:
+            listing += [(i, k, min(piece, l - k * piece)) for k in range(-(-l // piece))]
+    got = []
+    for t, r in enumerate(pr[:len(listing)]):
+        s, lane = divmod(t, 32)
+        L = (sp[s + 1] - sp[s]) // 32
+        n = int((sc[sp[s] + 32 * np.arange(L) + lane] >= 0).sum())
+        got.append(n)
+    for w0 in range(0, len(listing), sigma):
+        win = listing[w0:w0 + sigma]
+        want = sorted(range(len(win)), key=lambda k: (-win[k][2], k))
+        assert got[w0:w0 + len(win)] == [win[k][2] for k in want]
+    for s in range(sp.size - 1):
+        lens = got[32 * s:32 * s + 32]
+        assert sp[s + 1] - sp[s] == 32 * (max(lens) if lens else 0)
+    assert np.all(sv[sc < 0] == 0)
+    assert lr.shape[0] == sum(1 for i in range(M) if rp[i + 1] - rp[i] > piece)
+
+
 def test_coo_index_range_rejected():
     with pytest.raises(Exception):
         oracle.spmv_coo(2, 2, [0, 2], [0, 1], [1.0, 1.0], np.ones(2, np.float32))
