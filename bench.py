@@ -7,7 +7,7 @@ is one SpMV call through the C ABI: the binned main launch plus the long-row
 fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr]
+                    [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr|wcsr]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -162,6 +162,8 @@ def make_workload(name: str, rows: int = 0):
         c["name"] += " (bf16 A values and B, fp32 accumulation)"
     elif name == "bsr":
         c = synth.block_sparse()
+    elif name == "wcsr":
+        c = synth.window_pool()
     else:
         raise SystemExit(f"unknown workload {name}")
     c["workload"] = name
@@ -189,6 +191,9 @@ def accounting(c):
     if w.startswith("spmm"):
         N = c["N"]
         return 2 * nnz * N, 8 * nnz + 4 * (M + 1) + 4 * K * N + 4 * M * N
+    if w == "wcsr":  # flops of the stored chunks (what the tensor cores execute); bytes of the WCSR arrays
+        nch, N = c["nchunks"], c["N"]
+        return 2 * nch * 4096 * N, 2 * nch * 4096 + 4 * 64 * nch + 4 * (M // 64 + 1) + 2 * K * N + 4 * M * N
     if w == "bsr":
         nb = c["bcols"].size
         bs, N = c["bs"], c["N"]
@@ -212,14 +217,14 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     c = make_workload(args.workload, args.rows)
-    flops, abytes = accounting(c)
+    flops, abytes = accounting(c) if args.workload != "wcsr" else (None, None)  # wcsr: after its build
     M, K = c["M"], c["K"]
     w = c["workload"]
     stream = torch.cuda.Stream(device=dev)
     timings = {}
 
     t0 = time.perf_counter()
-    if w == "bsr":
+    if w in ("bsr", "wcsr"):
         rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val_bf16"])
     elif w == "power-law-coo":
         rp = col = val = None  # the generator's triplets are already sorted by row
@@ -410,6 +415,33 @@ def run_ours(args, rank, world):
                 Co.copy_(C, non_blocking=True)
 
         extra = {"variant": spx.spx_spmm_csr_variant(B, C)}
+    elif w == "wcsr":
+        t0 = time.perf_counter()
+        wp, wc, wv, fill = spx.spx_build_wcsr(M, K, rp, col, val)
+        timings["build_wcsr_ms"] = 1e3 * (time.perf_counter() - t0)
+        c["nchunks"] = int(wc.size // 64)
+        flops, abytes = accounting(c)
+        d_wp, d_wc = to_dev(wp), to_dev(wc)
+        d_wv = to_dev(wv.reshape(-1).view(np.int16))
+        Bm = to_dev(c["B_bf16"].view(np.int16))
+        C = torch.empty(M, c["N"], device=dev)
+        src = source_hash("spx_wcsr.cu")
+
+        def run():
+            spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+
+        Bh = torch.from_numpy(c["B_bf16"].view(np.int16)).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 2, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                Bm.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"fill_ratio": fill, "nchunks": c["nchunks"], "useful_flops": 2 * int(c["row"].size) * c["N"],
+                 "useful_gflops": None}
     else:  # bsr
         t0 = time.perf_counter()
         brp, bcol, bval, fill = spx.spx_build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
@@ -490,7 +522,9 @@ def run_ours(args, rank, world):
 
     pk = peaks()
     gflops = job_throughput(flops, world, ms)
-    if w == "bsr":
+    if w == "wcsr":
+        extra["useful_gflops"] = round(extra["useful_flops"] / (ms * 1e-3) / 1e9, 1)
+    if w in ("bsr", "wcsr"):
         ach = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["bf16"], 4), "peak_source": pk["src"] + " (bf16 dense, burst)"}
@@ -506,7 +540,7 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->f32" if (w == "bsr" or w.endswith("bf16")) else "f32",
+        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr") or w.endswith("bf16")) else "f32",
         "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
                    "N": c.get("N", 1), "l2": "flushed between steps (256 MB write); inputs also exceed L2",
@@ -536,6 +570,14 @@ def cpu_step_fn(c):
 
     w = c["workload"]
     M, K = c["M"], c["K"]
+    if w == "wcsr":
+        import synth
+        rp, col, val = row_major_csr(c, synth.bf16_bits_to_f32(c["val_bf16"]))
+        rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every window
+        Bf = synth.bf16_bits_to_f32(c["B_bf16"]).reshape(K, c["N"])
+        fl = 2 * int(np.diff(rp)[rows].sum()) * c["N"]
+        return (lambda: oracle.spmm(M, rp, col, val, Bf, rows=rows)), fl, \
+            f"{rows.size} output rows (one per window) of the {M}x{K} product, nonzero flops"
     if w == "bsr":
         rp, col, val = row_major_csr(c, c["val_bf16"])
         brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
@@ -614,7 +656,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
                     choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
-                             "spmm128-bf16", "bsr"])
+                             "spmm128-bf16", "bsr", "wcsr"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

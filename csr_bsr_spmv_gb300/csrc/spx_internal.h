@@ -16,6 +16,9 @@ spx_status spx_cuda_status(int cuda_error);
 // Reads and clears the error word of the COO kernel: 0 or a negative spx_status.
 int spx_coo_error_take();
 
+// Reads and clears the error word of the WCSR kernel: 0 or SPX_ERR_TIMEOUT.
+int spx_wcsr_error_take();
+
 struct spx_plan {
     int32_t M = 0, K = 0;
     int64_t nnz = 0;

@@ -1,0 +1,423 @@
+// spx_wcsr.cu -- WCSR (window CSR) format and its tensor-core SpMM on sm_103a.
+//
+// [AsyncSparse] §2.2.2: rows are grouped into windows of fixed height (64
+// here); a window stores the union of the columns its rows use
+// (window_col_idx, -1 = padding) and, for those compressed columns, a dense
+// 64-row block of values -- finer than BSR for scattered nonzeros, at the
+// price of an indirect load of B.  Here the compressed columns of a window
+// are cut into chunks of 64, and each chunk's values are one 64 x 64 bf16
+// block stored row-major (8 KB, the BSR block layout), so a chunk is a
+// "BSR block whose B rows are gathered".
+//
+// Kernel ([AsyncSparse] §4.1: TMA for A, cooperative gather of B rows into a
+// 128-byte-swizzled shared tile, tensor-core MMA; mapped to Blackwell): one
+// CTA per (128-column tile of N, window), 192 threads:
+//   warp 0, lane 0: TMA of the chunk's A block into the ring stage;
+//   warp 1, lane 0: tcgen05.mma of the stage into a TMEM accumulator
+//                   (transposed: M = 128 output columns, N = 64 window rows,
+//                   K = 16), tcgen05.commit frees the stage;
+//   warps 2-5     : gather the chunk's 64 B rows (128 columns, 256 bytes each)
+//                   with 16-byte cp.async straight into the swizzled B tile
+//                   (zero-fill for padding columns), several stages in
+//                   flight per thread; then they run the epilogue.
+// Each window is one CTA (no split, no atomics): the product is deterministic.
+// Every mbarrier wait is bounded; on expiry the CTA records an error word
+// (spx_last_device_error), stops, drains its copies, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "spx_internal.h"
+#include "spx_tc.cuh"
+
+using namespace spx_tc;
+
+namespace {
+
+constexpr int kWin = 64;                       // window height = chunk width
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kWin * kWin * 2;  // 8 KB A block
+constexpr uint32_t kBBox = kWin * 64 * 2;      // 64 k-rows x 64 n, 8 KB
+constexpr uint32_t kStageBytes = kABytes + 2 * kBBox;
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kIdesc = idesc_bf16_mn_k(128, 64);
+constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
+constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s)
+
+enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
+
+__device__ int g_wcsr_error;
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_wcsr_error, 0, code); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(kThreads)
+    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const int* __restrict__ win_ptr,
+                     const int* __restrict__ win_col, const uint16_t* __restrict__ B, long long ldb,
+                     float* __restrict__ C, long long ldc, int M, int K, float alpha, float beta,
+                     long long spin_limit) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ int s_issued, s_consumed;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bars = base + kStages * kStageBytes;
+    auto afull = [&](int s) { return bars + 8u * s; };                 // TMA bytes of the A block
+    auto gfull = [&](int s) { return bars + 8u * (kStages + s); };     // 128 gather threads
+    auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); }; // MMA commit
+    const uint32_t acc_bar = bars + 8u * (3 * kStages);
+    auto stage_a = [&](int s) { return base + s * kStageBytes; };
+    auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * 128;
+    const int w = blockIdx.y;
+    const int g0 = __ldg(win_ptr + w);
+    const int nch = __ldg(win_ptr + w + 1) - g0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(afull(s), 1);
+            mbar_init(gfull(s), 128);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        s_abort = 0;
+        s_issued = 0;
+        s_consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = s_tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int b = 0;
+            for (; b < nch; ++b) {
+                const int s = b % kStages;
+                if (!mbar_wait(empty(s), ((b / kStages) & 1u) ^ 1u, spin_limit) || s_abort) {
+                    record_error(kErrEmpty);
+                    s_abort = 1;
+                    break;
+                }
+                mbar_expect_tx(afull(s), kABytes);
+                tma_load_2d(stage_a(s), &tmA, 0, (g0 + b) * kWin, afull(s));
+            }
+            s_issued = b;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int b = 0;
+            for (; b < nch; ++b) {
+                const int s = b % kStages;
+                const uint32_t ph = (b / kStages) & 1u;
+                if (!mbar_wait(afull(s), ph, spin_limit) || !mbar_wait(gfull(s), ph, spin_limit)) {
+                    record_error(kErrFull);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kWin / 16; ++ks) {
+                    const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
+                    const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
+                    mma_bf16(tmem_d, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(empty(s));
+            }
+            s_consumed = b;
+            if (b > 0) mma_commit(acc_bar);
+            else mbar_arrive(acc_bar);
+        }
+    } else {
+        // Gather: thread t copies compressed column k = t/2 (one B row), half h = t%2
+        // (64 of the tile's 128 columns = 128 bytes = 8 chunks of 16 bytes) into the
+        // 128-byte-swizzled box h: row k at k*128, 16-byte chunk j at (j ^ (k & 7)).
+        const int t = threadIdx.x - 64;
+        const int k = t >> 1, h = t & 1;
+        const uint32_t row_off = h * kBBox + k * 128u;
+        int b = 0;
+        for (; b < nch; ++b) {
+            const int s = b % kStages;
+            int ok = 1;
+            if (lane == 0) ok = (mbar_wait(empty(s), ((b / kStages) & 1u) ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(kErrEmpty);
+                    s_abort = 1;
+                }
+                break;
+            }
+            const int cr = __ldg(win_col + static_cast<long long>(g0 + b) * kWin + k);
+            const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
+            const uint16_t* src = c >= 0 ? B + static_cast<long long>(c) * ldb + n0 + 64 * h : B;
+            const uint32_t nbytes = c >= 0 ? 16u : 0u;  // padding column: zero-fill
+            const uint32_t dst = stage_b(s) + row_off;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cp_async16(dst + ((j ^ (k & 7)) << 4), src + (c >= 0 ? 8 * j : 0), nbytes);
+            cp_async_commit();
+            if (b >= kStages - 1) {  // the copies of stage b - (kStages - 1) have landed: publish them
+                cp_async_wait<kStages - 1>();
+                fence_proxy_async();
+                mbar_arrive(gfull((b - (kStages - 1)) % kStages));
+            }
+        }
+        // publish the stages still in flight, oldest first
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (int q = max(0, b - (kStages - 1)); q < b; ++q) mbar_arrive(gfull(q % kStages));
+    }
+    __syncwarp();
+
+    if (warp >= 2) {  // epilogue: TMEM lanes 32*(warp%4) .. +31 = output columns n0 + that range
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(acc_bar, 0, spin_limit) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok && lane == 0) record_error(kErrAcc);
+        tc_fence_after();
+        const int q = warp & 3;
+        float* cp = C + static_cast<long long>(w) * kWin * ldc + n0 + 32 * q + lane;
+        const int rows = min(kWin, M - w * kWin);
+        if (nch == 0) {
+            for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+        } else if (ok && !s_abort) {
+#pragma unroll
+            for (int c0 = 0; c0 < kWin; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (c0 + j < rows) {
+                        float* p = cp + static_cast<long long>(c0 + j) * ldc;
+                        const float acc = alpha * __uint_as_float(v[j]);
+                        __stcs(p, beta != 0.f ? acc + beta * *p : acc);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {  // A blocks issued but never consumed: wait (bounded) until they landed
+        for (int b = s_consumed; b < s_issued; ++b)
+            if (!mbar_wait(afull(b % kStages), (b / kStages) & 1u, spin_limit)) {
+                record_error(kErrDrain);
+                break;
+            }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols) : "memory");
+}
+
+__global__ void wcsr_scale_kernel(float* C, long long ldc, int N, float beta) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c < N) {
+        float* q = C + static_cast<long long>(blockIdx.y) * ldc + c;
+        *q = beta != 0.f ? beta * *q : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------- host builder
+spx_status build_wcsr_host(int32_t M, int32_t K, const int32_t* rp, const int32_t* col, const char* val, int32_t vb,
+                           int32_t* win_ptr, int32_t* win_col, char* win_val, int64_t* nchunks_out, double* fill_out) {
+    if (rp[0] != 0) return SPX_ERR_ARG;
+    for (int32_t i = 0; i < M; ++i)
+        if (rp[i + 1] < rp[i]) return SPX_ERR_NOT_SORTED;
+    const int64_t W = (static_cast<int64_t>(M) + kWin - 1) / kWin;
+    std::vector<int32_t> pos(static_cast<size_t>(K), -1);  // column -> compressed position in this window
+    std::vector<int32_t> cols;
+    std::vector<uint8_t> seen;
+    int64_t g = 0;
+    if (win_ptr) win_ptr[0] = 0;
+    for (int64_t w = 0; w < W; ++w) {
+        const int64_t r0 = w * kWin, r1 = std::min<int64_t>(r0 + kWin, M);
+        cols.clear();
+        for (int64_t p = rp[r0]; p < rp[r1]; ++p) {
+            if (col[p] < 0 || col[p] >= K) return SPX_ERR_INDEX_RANGE;
+            if (pos[col[p]] < 0) {
+                pos[col[p]] = 0;
+                cols.push_back(col[p]);
+            }
+        }
+        std::sort(cols.begin(), cols.end());
+        for (size_t t = 0; t < cols.size(); ++t) pos[cols[t]] = static_cast<int32_t>(t);
+        const int64_t nch = (static_cast<int64_t>(cols.size()) + kWin - 1) / kWin;
+        seen.assign(static_cast<size_t>(nch) * kWin * kWin, 0);
+        for (int64_t i = r0; i < r1; ++i)
+            for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
+                const int64_t k = pos[col[p]];
+                const int64_t slot = (k / kWin) * kWin * kWin + (i - r0) * kWin + k % kWin;
+                if (seen[slot]) {
+                    for (int32_t c : cols) pos[c] = -1;
+                    return SPX_ERR_DUPLICATE;
+                }
+                seen[slot] = 1;
+            }
+        if (win_col && win_val) {
+            for (int64_t k = 0; k < nch * kWin; ++k)
+                win_col[g * kWin + k] = k < static_cast<int64_t>(cols.size()) ? cols[k] : -1;
+            std::memset(win_val + g * kWin * kWin * vb, 0, static_cast<size_t>(nch * kWin * kWin * vb));
+            for (int64_t i = r0; i < r1; ++i)
+                for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
+                    const int64_t k = pos[col[p]];
+                    const int64_t e = (g + k / kWin) * kWin * kWin + (i - r0) * kWin + k % kWin;
+                    std::memcpy(win_val + e * vb, val + p * vb, static_cast<size_t>(vb));
+                }
+        }
+        for (int32_t c : cols) pos[c] = -1;
+        g += nch;
+        if (g * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
+        if (win_ptr) win_ptr[w + 1] = static_cast<int32_t>(g);
+    }
+    if (nchunks_out) *nchunks_out = g;
+    if (fill_out) *fill_out = g ? static_cast<double>(rp[M]) / (static_cast<double>(g) * kWin * kWin) : 0.0;
+    return SPX_OK;
+}
+
+}  // namespace
+
+int spx_wcsr_error_take() {
+    int h = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbol(&h, g_wcsr_error, sizeof(int)) != cudaSuccess) return static_cast<int>(SPX_ERR_CUDA);
+    if (h != 0 && cudaMemcpyToSymbol(g_wcsr_error, &zero, sizeof(int)) != cudaSuccess)
+        return static_cast<int>(SPX_ERR_CUDA);
+    return h ? static_cast<int>(SPX_ERR_TIMEOUT) : 0;
+}
+
+extern "C" {
+
+spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                          int32_t val_bytes, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
+                          double* fill_out, spx_loc where, spx_stream_t stream) {
+    if (M < 0 || K < 0 || !row_ptr) return SPX_ERR_ARG;
+    if (!(val_bytes == 1 || val_bytes == 2 || val_bytes == 4 || val_bytes == 8)) return SPX_ERR_ARG;
+    if ((win_col == nullptr) != (win_val == nullptr)) return SPX_ERR_ARG;
+    const int64_t W = (static_cast<int64_t>(M) + kWin - 1) / kWin;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    std::vector<int32_t> rp_h, col_h, wp_h, wc_h;
+    std::vector<char> val_h, wv_h;
+    try {
+        const int32_t* rp = row_ptr;
+        const int32_t* cl = col;
+        const char* vl = static_cast<const char*>(val);
+        if (where == SPX_DEVICE) {
+            rp_h.resize(static_cast<size_t>(M) + 1);
+            if (cudaMemcpyAsync(rp_h.data(), row_ptr, sizeof(int32_t) * rp_h.size(), cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(st) != cudaSuccess)
+                return SPX_ERR_CUDA;
+            rp = rp_h.data();
+            const int64_t nnz = rp[M];
+            if (nnz < 0 || nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
+            if (nnz > 0 && (!col || !val)) return SPX_ERR_ARG;
+            col_h.resize(static_cast<size_t>(nnz));
+            val_h.resize(static_cast<size_t>(nnz) * val_bytes);
+            if (nnz && (cudaMemcpyAsync(col_h.data(), col, sizeof(int32_t) * col_h.size(), cudaMemcpyDeviceToHost,
+                                        st) != cudaSuccess ||
+                        cudaMemcpyAsync(val_h.data(), val, val_h.size(), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+                        cudaStreamSynchronize(st) != cudaSuccess))
+                return SPX_ERR_CUDA;
+            cl = col_h.data();
+            vl = val_h.data();
+        } else if (where != SPX_HOST) {
+            return SPX_ERR_ARG;
+        } else if (rp[M] > 0 && (!col || !val)) {
+            return SPX_ERR_ARG;
+        }
+        if (where == SPX_HOST) return build_wcsr_host(M, K, rp, cl, vl, val_bytes, win_ptr, win_col,
+                                                      static_cast<char*>(win_val), nchunks_out, fill_out);
+        // device outputs: build on the host, then copy out
+        int64_t nch = 0;
+        double fill = 0.0;
+        const bool full = win_col != nullptr;
+        if (full) {
+            spx_status s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, nullptr, nullptr, nullptr, &nch, nullptr);
+            if (s != SPX_OK) return s;
+            wp_h.resize(static_cast<size_t>(W) + 1);
+            wc_h.resize(static_cast<size_t>(nch) * kWin);
+            wv_h.resize(static_cast<size_t>(nch) * kWin * kWin * val_bytes);
+            s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, wp_h.data(), wc_h.data(), wv_h.data(), &nch, &fill);
+            if (s != SPX_OK) return s;
+        } else {
+            wp_h.resize(static_cast<size_t>(W) + 1);
+            spx_status s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, wp_h.data(), nullptr, nullptr, &nch, &fill);
+            if (s != SPX_OK) return s;
+        }
+        cudaError_t e = cudaSuccess;
+        if (win_ptr) e = cudaMemcpyAsync(win_ptr, wp_h.data(), sizeof(int32_t) * wp_h.size(), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && full && nch) {
+            e = cudaMemcpyAsync(win_col, wc_h.data(), sizeof(int32_t) * wc_h.size(), cudaMemcpyHostToDevice, st);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(win_val, wv_h.data(), wv_h.size(), cudaMemcpyHostToDevice, st);
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return SPX_ERR_CUDA;
+        if (nchunks_out) *nchunks_out = nch;
+        if (fill_out) *fill_out = fill;
+        return SPX_OK;
+    } catch (const std::bad_alloc&) {
+        return SPX_ERR_NOMEM;
+    }
+}
+
+spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* win_ptr, const int32_t* win_col,
+                         const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                         float* C, int64_t ldc, spx_stream_t stream) {
+    if (M < 0 || K < 0 || N < 0 || nchunks < 0) return SPX_ERR_ARG;
+    if (nchunks * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (N % 128) return SPX_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!win_ptr || !C || (nchunks > 0 && (!win_col || !win_val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (ldb % 8 || !spx_aligned(win_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
+        !spx_aligned(win_ptr, 4) || !spx_aligned(win_col, 4))
+        return SPX_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int W = static_cast<int>((static_cast<int64_t>(M) + kWin - 1) / kWin);
+    if (nchunks == 0) {
+        dim3 grid((N + 255) / 256, M);
+        wcsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, N, beta);
+        spx_note_launches(1);
+        return spx_cuda_status(cudaGetLastError());
+    }
+    CUtensorMap tmA;
+    if (!make_map(&tmA, win_val, kWin, static_cast<uint64_t>(nchunks) * kWin, kWin * 2)) return SPX_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(wcsr_spmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemBytes));
+    });
+    if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
+    dim3 grid(N / 128, W);
+    wcsr_spmm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta,
+                                                         kSpinLimit);
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -119,6 +119,9 @@ def _lib():
             "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
             "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
+                                ctypes.c_int, vp], ctypes.c_int),
+            "spx_spmm_wcsr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
@@ -240,6 +243,41 @@ def spx_build_bsr(M: int, K: int, row_ptr, col, val, br: int, bc: int, stream=No
                                  _ptr(bcol), _ptr(bval), ctypes.byref(nnzb), ctypes.byref(fill), where, st),
                "spx_build_bsr")
     return brp, bcol, bval.reshape(nb, br, bc), fill.value
+
+
+def spx_build_wcsr(M: int, K: int, row_ptr, col, val, stream=None):
+    """CSR -> WCSR with 64-row windows (two calls).
+    Returns (win_ptr, win_col[nchunks*64], win_val[nchunks, 64, 64], fill)."""
+    where = _where(row_ptr, col, val)
+    lib = _lib()
+    W = (M + 63) // 64
+    nch = ctypes.c_int64(0)
+    fill = ctypes.c_double(0.0)
+    st = _stream(stream) if where == SPX_DEVICE else None
+    wp = _empty_like_loc(row_ptr, W + 1, np.int32, torch.int32)
+    _check(lib.spx_build_wcsr(M, K, _ptr(row_ptr), _ptr(col), _ptr(val), _itemsize(val), _ptr(wp), None, None,
+                              ctypes.byref(nch), ctypes.byref(fill), where, st), "spx_build_wcsr(count)")
+    nc = nch.value
+    wc = _empty_like_loc(row_ptr, nc * 64, np.int32, torch.int32)
+    if isinstance(val, torch.Tensor):
+        wv = torch.empty(nc * 4096, dtype=val.dtype, device=val.device)
+    else:
+        wv = np.empty(nc * 4096, dtype=val.dtype)
+    if nc:
+        _check(lib.spx_build_wcsr(M, K, _ptr(row_ptr), _ptr(col), _ptr(val), _itemsize(val), None, _ptr(wc),
+                                  _ptr(wv), ctypes.byref(nch), ctypes.byref(fill), where, st), "spx_build_wcsr")
+    return wp, wc, wv.reshape(nc, 64, 64), fill.value
+
+
+def spx_spmm_wcsr(M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor, win_val: torch.Tensor,
+                  B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha*A*B + beta*C, A in WCSR (bf16 bit patterns), B bf16 (K x N), C fp32 (M x N)."""
+    N = B.shape[1]
+    assert B.stride(1) == 1 and C.stride(1) == 1
+    nch = win_col.numel() // 64
+    _check(_lib().spx_spmm_wcsr(M, K, nch, _ptr(win_ptr), _ptr(win_col), _ptr(win_val), N, _ptr(B), B.stride(0),
+                                float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)), "spx_spmm_wcsr")
+    return C
 
 
 def spx_check_csr(M: int, K: int, row_ptr, col, strict: bool = True, stream=None) -> int:

@@ -477,9 +477,47 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream);
 
+/* ------------------------------------------------------------ WCSR */
+
+/*
+ * CSR -> WCSR (window CSR) with windows of 64 rows.  [AsyncSparse] §2.2.2:
+ * each window keeps the union of the columns its rows use (window_col_idx,
+ * -1 = padding) and a dense block of values for those compressed columns.
+ * Here the union of window w (ascending) is padded with -1 to a multiple of
+ * 64 and cut into chunks of 64 compressed columns:
+ *   win_ptr int32[ceil(M/64)+1]: first chunk of each window (chunk count);
+ *   win_col int32[64 * nchunks]: original column of each compressed position;
+ *   win_val [nchunks][64 rows][64 positions] of val_bytes each, row-major,
+ *           zero where the row has no entry in that column (and for rows
+ *           beyond M in the last window).
+ * fill = nnz / (nchunks * 4096).  Two calls: with win_col == win_val == NULL
+ * only *nchunks_out (and win_ptr, when given) is produced.  Arrays are all
+ * host or all device per `where` (device inputs are staged through host
+ * memory).  Errors: SPX_ERR_DUPLICATE (a repeated (row, col)),
+ * SPX_ERR_INDEX_RANGE, SPX_ERR_NOT_SORTED.
+ */
+spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                          int32_t val_bytes, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
+                          double* fill_out, spx_loc where, spx_stream_t stream);
+
+/*
+ * C = alpha * A B + beta * C with A in WCSR (bf16 values), B dense K x N bf16
+ * row-major (ldb), C dense M x N fp32 (ldc); fp32 accumulation on the tensor
+ * cores.  [AsyncSparse] §4.1 (TMA for the window's values, a cooperative
+ * gather of the B rows named by window_col_idx into a swizzled shared tile,
+ * tensor-core MMA).  One CTA per (window, 128 output columns); no atomics,
+ * so the result is deterministic.  Supported: N a multiple of 128, ldb a
+ * multiple of 8, win_val and B 16-byte aligned; any M and K.  Launches: 1.
+ * Bounded pipeline waits report SPX_ERR_TIMEOUT through
+ * spx_last_device_error.
+ */
+spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* win_ptr, const int32_t* win_col,
+                         const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                         float* C, int64_t ldc, spx_stream_t stream);
+
 /*
  * Synchronises `stream`, then reads and clears the device-side error words:
- * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr gave up, else the index
+ * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr or spx_spmm_wcsr gave up, else the index
  * or ordering error spx_spmv_coo recorded, else SPX_OK.
  */
 spx_status spx_last_device_error(spx_stream_t stream);

@@ -68,6 +68,8 @@ def _lib_():
                 "or_plan_opts_auto": [vp, vp],
                 "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
                 "or_spmv_coo": [i32, i32, i64, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
+                "or_build_wcsr": [i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.POINTER(ctypes.c_double)],
                 "or_build_sell": [i32, vp, vp, vp, i32, i32, ctypes.POINTER(ctypes.c_int64),
                                   ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                   ctypes.POINTER(ctypes.c_int64), vp, vp, vp, vp, vp],
@@ -159,6 +161,25 @@ def build_sell(M, rp, col, val, sigma=1024, piece=64):
     _check(lib.or_build_sell(M, _p(rp), _p(col), _p(val), sigma, piece, *[ctypes.byref(v) for v in n], _p(sp),
                              _p(pr), _p(lr), _p(sc), _p(sv)))
     return sp, pr, lr, sc, sv
+
+
+def build_wcsr(M, K, rp, col, val):
+    """Returns (win_ptr, win_col[nchunks*64], win_val[nchunks, 64, 64], fill)."""
+    rp, col = _c(rp, np.int32), _c(col, np.int32)
+    val = np.ascontiguousarray(val)
+    W = (M + 63) // 64
+    nch = ctypes.c_int64(0)
+    fill = ctypes.c_double(0.0)
+    wp = np.empty(W + 1, np.int32)
+    lib = _lib_()
+    _check(lib.or_build_wcsr(M, K, _p(rp), _p(col), _p(val), val.itemsize, _p(wp), None, None, ctypes.byref(nch),
+                             ctypes.byref(fill)))
+    nc = nch.value
+    wc = np.empty(nc * 64, np.int32)
+    wv = np.empty(nc * 4096, val.dtype)
+    _check(lib.or_build_wcsr(M, K, _p(rp), _p(col), _p(val), val.itemsize, _p(wp), _p(wc), _p(wv),
+                             ctypes.byref(nch), ctypes.byref(fill)))
+    return wp, wc, wv.reshape(nc, 64, 64), fill.value
 
 
 def row_stats(M, rp):

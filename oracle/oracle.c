@@ -515,6 +515,75 @@ int or_build_sell(int32_t M, const int32_t* rp, const int32_t* col, const float*
     return OR_OK;
 }
 
+/*
+ * CSR -> WCSR with windows of 64 rows.  [AsyncSparse] §2.2.2 (rows grouped
+ * into fixed-height windows; a window keeps the union of the columns its rows
+ * use, window_col_idx with -1 for padding, and the values of those columns
+ * as a dense block).  Here: the union of window w is found by marking the
+ * columns its entries use and scanning the columns upward (so it comes out
+ * ascending), padded with -1 to a multiple of 64, and cut into chunks of 64
+ * positions; chunk values are a 64 x 64 row-major block (row r of the window,
+ * position k), zero where the row has no entry there.  A repeated (row, col)
+ * would need two values in one slot: OR_ERR_DUP.  Two calls: with
+ * win_col == NULL only the chunk count (and win_ptr) is produced.
+ */
+int or_build_wcsr(int32_t M, int32_t K, const int32_t* rp, const int32_t* col, const void* val, int32_t vbytes,
+                  int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks, double* fill) {
+    if (M < 0 || K < 0 || vbytes <= 0) return OR_ERR_ARG;
+    int64_t W = ((int64_t)M + 63) / 64;
+    unsigned char* mark = (unsigned char*)calloc((size_t)(K ? K : 1), 1);
+    int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K ? K : 1));
+    unsigned char* used = (unsigned char*)malloc(64 * 64);
+    if (!mark || !pos || !used) {
+        free(mark); free(pos); free(used);
+        return OR_ERR_NOMEM;
+    }
+    int64_t g = 0;
+    int rc = OR_OK;
+    if (win_ptr) win_ptr[0] = 0;
+    for (int64_t w = 0; w < W && rc == OR_OK; ++w) {
+        int64_t r0 = w * 64, r1 = r0 + 64 < M ? r0 + 64 : M;
+        for (int64_t p = rp[r0]; p < rp[r1]; ++p) {
+            if (col[p] < 0 || col[p] >= K) { rc = OR_ERR_INDEX; break; }
+            mark[col[p]] = 1;
+        }
+        if (rc != OR_OK) break;
+        int64_t n = 0;
+        for (int32_t c = 0; c < K; ++c)
+            if (mark[c]) pos[c] = (int32_t)(n++);
+        int64_t nch = (n + 63) / 64;
+        if (win_col) {
+            int64_t k = 0;
+            for (int32_t c = 0; c < K; ++c)
+                if (mark[c]) win_col[g * 64 + k++] = c;
+            for (; k < nch * 64; ++k) win_col[g * 64 + k] = -1;
+            memset((char*)win_val + g * 4096 * vbytes, 0, (size_t)(nch * 4096 * vbytes));
+        }
+        for (int64_t ch = 0; ch < nch && rc == OR_OK; ++ch) {
+            memset(used, 0, 64 * 64);
+            for (int64_t i = r0; i < r1 && rc == OR_OK; ++i)
+                for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
+                    int64_t k = pos[col[p]];
+                    if (k / 64 != ch) continue;
+                    int64_t slot = (i - r0) * 64 + k % 64;
+                    if (used[slot]) { rc = OR_ERR_DUP; break; }
+                    used[slot] = 1;
+                    if (win_val)
+                        memcpy((char*)win_val + ((g + ch) * 4096 + slot) * vbytes, (const char*)val + p * vbytes,
+                               (size_t)vbytes);
+                }
+        }
+        for (int64_t p = rp[r0]; p < rp[r1]; ++p) mark[col[p]] = 0;
+        g += nch;
+        if (win_ptr) win_ptr[w + 1] = (int32_t)g;
+    }
+    free(mark); free(pos); free(used);
+    if (rc != OR_OK) return rc;
+    *nchunks = g;
+    if (fill) *fill = g ? (double)rp[M] / ((double)g * 4096.0) : 0.0;
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------ SpMM */
 
 /*

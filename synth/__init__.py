@@ -250,3 +250,24 @@ def block_sparse(seed: int = 5, M: int = 16384, K: int | None = None, bs: int = 
     Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
     return dict(name=f"bsr {M}x{K} {bs}x{bs} {per_row}/row N={N}", M=M, K=K, N=N, bs=bs, row=row, col=col,
                 val_bf16=val, B_bf16=Bm, bcols=bcols)
+
+
+def window_pool(seed: int = 6, M: int = 16384, K: int | None = None, win: int = 64, pool: int = 512,
+                lmin: int = 32, lmax: int = 96, N: int = 1024, sigma_a: float = 0.02, sigma_b: float = 1.0):
+    """Irregular sparsity with window locality: every window of `win` rows
+    draws its own pool of `pool` distinct columns (the first `pool` of a
+    permutation of K); each row takes l ~ U{lmin..lmax} distinct pool entries.
+    Entries bf16 N(0, sigma_a), B is K x N bf16 N(0, sigma_b).  COO comes out
+    sorted by (row, col)."""
+    K = M if K is None else K
+    W = (M + win - 1) // win
+    lengths = lengths_uniform(seed, M, lmin, lmax)
+    row, idx = cols_uniform(seed, pool, lengths)
+    pools = np.stack([permutation(seed, K, tag=1000 + w)[:pool] for w in range(W)]).astype(np.int32)
+    col = pools[row // win, idx]
+    order = np.lexsort((col, row))
+    row, col = row[order], col[order]
+    val = normal_bf16(seed, T_VAL, row.size, sigma_a)
+    Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
+    return dict(name=f"window-pool {M}x{K} windows {win} pool {pool} l~U{{{lmin}..{lmax}}} N={N}", M=M, K=K, N=N,
+                row=row, col=col, val_bf16=val, B_bf16=Bm)

@@ -298,3 +298,38 @@ def test_sell_rejects_bad_input_and_unuploaded_use():
     assert lib.spx_spmv_sell(S.handle, 2, 2, 1.0, a, 0.0, ctypes.c_void_p(1 << 22), None, 0, None) == -10
     assert lib.spx_spmv_sell(S.handle, 3, 2, 1.0, a, 0.0, ctypes.c_void_p(1 << 22), None, 0, None) == -1
     assert spx.launch_count() == before
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 1), (64, 300, 0, 90), (130, 200, 0, 40), (0, 5, 0, 1),
+                                          (257, 4000, 0, 200)])
+@pytest.mark.parametrize("vdtype", [np.float32, np.uint16])
+def test_build_wcsr_matches_oracle(M, K, lmin, lmax, vdtype):
+    d = synth.random_coo(62, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    v = val if vdtype is np.float32 else synth.to_bf16_bits(val)
+    want = oracle.build_wcsr(M, K, rp, col, v)
+    got = spx.spx_build_wcsr(M, K, rp, col, v)
+    for w, g in zip(want[:3], got[:3]):
+        assert np.array_equal(w, g)
+    assert want[3] == got[3]
+
+
+def test_build_wcsr_errors():
+    rp = np.array([0, 2, 3], np.int32)
+    with pytest.raises(spx.SpxError):   # duplicate (row, col)
+        spx.spx_build_wcsr(2, 4, rp, np.array([1, 1, 0], np.int32), np.ones(3, np.float32))
+    with pytest.raises(spx.SpxError):   # column out of range
+        spx.spx_build_wcsr(2, 4, rp, np.array([1, 4, 0], np.int32), np.ones(3, np.float32))
+    with pytest.raises(spx.SpxError):   # row_ptr decreasing
+        spx.spx_build_wcsr(2, 4, np.array([0, 3, 2], np.int32), np.array([1, 2, 0], np.int32), np.ones(3, np.float32))
+
+
+def test_spmm_wcsr_rejects_unsupported_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 100, a, 128, 1.0, 0.0, a, 128, None) == -7   # N % 128
+    assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 128, a, 132, 1.0, 0.0, a, 128, None) == -8   # ldb % 8
+    assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 128, a, 64, 1.0, 0.0, a, 128, None) == -1    # ldb < N
+    assert lib.spx_spmm_wcsr(64, 64, -1, a, a, a, 128, a, 128, 1.0, 0.0, a, 128, None) == -1
+    assert spx.launch_count() == before

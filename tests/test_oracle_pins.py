@@ -185,6 +185,52 @@ def test_sell_round_trip_and_order(M, K, lmin, lmax, sigma, piece):
     assert lr.shape[0] == sum(1 for i in range(M) if rp[i + 1] - rp[i] > piece)
 
 
+def test_worked_example_wcsr(ex):
+    g, v, val = ex
+    p, d = g["printed"], g["derived_by_hand"]["wcsr_window64"]
+    wp, wc, wv, fill = oracle.build_wcsr(5, 5, p["csr_row_ptr"], p["csr_col"], val)
+    assert wp.tolist() == d["win_ptr"]
+    assert wc[:5].tolist() == d["win_col_used"] and np.all(wc[5:] == -1)
+    want = np.zeros((64, 64))
+    want[:5, :5] = [_vals(r, v) for r in d["chunk_top_left_5x5"]]
+    assert np.array_equal(wv[0], want)
+    assert fill == 8 / 4096
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 1), (7, 5, 0, 5), (64, 300, 0, 90), (130, 200, 0, 40),
+                                          (200, 1000, 0, 70), (50, 50, 0, 0)])
+def test_wcsr_against_dense(M, K, lmin, lmax):
+    """Expanding WCSR back to dense gives the matrix; each window's columns are
+    exactly the sorted set of columns its rows use, padded with -1 to whole
+    chunks of 64; the fill ratio is nnz over stored slots."""
+    d = synth.random_coo(61, M, K, lmin, lmax, values="int")
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = _dense(M, K, d["row"], d["col"], d["val"])
+    wp, wc, wv, fill = oracle.build_wcsr(M, K, rp, col, val)
+    W = -(-M // 64)
+    assert wp.size == W + 1
+    D = np.zeros((W * 64, K))
+    for w in range(W):
+        used = sorted(set(col[rp[w * 64]:rp[min(w * 64 + 64, M)]].tolist()))
+        cols = wc[64 * wp[w]:64 * wp[w + 1]]
+        assert wp[w + 1] - wp[w] == -(-len(used) // 64)
+        assert cols[:len(used)].tolist() == used and np.all(cols[len(used):] == -1)
+        for ch in range(wp[w], wp[w + 1]):
+            for k in range(64):
+                c = wc[64 * ch + k]
+                if c < 0:
+                    assert not wv[ch][:, k].any()
+                else:
+                    D[w * 64:(w + 1) * 64, c] += wv[ch][:, k]
+    assert np.array_equal(D[:M], A) and not D[M:].any()
+    assert fill == (rp[-1] / (wp[-1] * 4096) if wp[-1] else 0.0)
+
+
+def test_wcsr_duplicate_rejected():
+    with pytest.raises(Exception):
+        oracle.build_wcsr(2, 4, [0, 2, 3], [1, 1, 0], np.ones(3, np.float32))
+
+
 def test_coo_index_range_rejected():
     with pytest.raises(Exception):
         oracle.spmv_coo(2, 2, [0, 2], [0, 1], [1.0, 1.0], np.ones(2, np.float32))
