@@ -425,7 +425,7 @@ def run_ours(args, rank, world):
         d_wv = to_dev(wv.reshape(-1).view(np.int16))
         Bm = to_dev(c["B_bf16"].view(np.int16))
         C = torch.empty(M, c["N"], device=dev)
-        src = source_hash("spx_wcsr.cu")
+        src = source_hash("spx_wcsr.cu", "spx_tc.cuh")
 
         def run():
             spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
@@ -450,7 +450,7 @@ def run_ours(args, rank, world):
         d_bval = to_dev(bval.view(np.int16))
         Bm = to_dev(c["B_bf16"].view(np.int16))
         C = torch.empty(M, c["N"], device=dev)
-        src = source_hash("spx_bsr.cu")
+        src = source_hash("spx_bsr.cu", "spx_tc.cuh")
 
         def run():
             spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
