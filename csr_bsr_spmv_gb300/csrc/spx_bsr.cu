@@ -269,18 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- tile variant
-// Non-persistent: one CTA per (128-column tile, block-row), one TMA thread,
-// one MMA thread, four epilogue warps, a STAGES-deep ring of {A block 8 KB,
-// B tile 16 KB}.  Several CTAs share an SM (smem-bound), each an independent
-// load/MMA pipeline, so one pipeline's hand-off latency is covered by the others.
+// Non-persistent: one CTA per (128*HALVES-column tile, block-row), one TMA
+// warp, one MMA thread, four epilogue warps, a STAGES-deep ring of {A block
+// 8 KB, B tile 16*HALVES KB}.  Several CTAs share an SM (smem-bound), each an
+// independent load/MMA pipeline, so one pipeline's hand-off latency is covered
+// by the others.  HALVES = 2 shares each A block between two M = 128 MMAs
+// (fewer A bytes per flop, fewer and larger CTAs).
 constexpr int kTThreads = 128;
-constexpr uint32_t kTStageBytes = kABytes + 2 * kBBox;  // 24 KB
-constexpr uint32_t kTTmemCols = 64;
 
-template <int STAGES>
-constexpr size_t tile_smem_bytes() { return STAGES * kTStageBytes + 1024 + 256; }
+template <int HALVES>
+__host__ __device__ constexpr uint32_t tile_stage_bytes() { return kABytes + 2 * HALVES * kBBox; }
 
-template <int STAGES>
+template <int STAGES, int HALVES>
+constexpr size_t tile_smem_bytes() { return STAGES * tile_stage_bytes<HALVES>() + 1024 + 256; }
+
+template <int STAGES, int HALVES>
 __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
@@ -292,15 +295,17 @@ __global__ void __launch_bounds__(kTThreads)
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bars = base + STAGES * kTStageBytes;
+    constexpr uint32_t kSB = tile_stage_bytes<HALVES>();
+    constexpr uint32_t kTmemColsT = 64 * HALVES;
+    const uint32_t bars = base + STAGES * kSB;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     const uint32_t acc_bar = bars + 16u * STAGES;
-    auto stage_a = [&](int s) { return base + s * kTStageBytes; };
-    auto stage_b = [&](int s) { return base + s * kTStageBytes + kABytes; };
+    auto stage_a = [&](int s) { return base + s * kSB; };
+    auto stage_b = [&](int s) { return base + s * kSB + kABytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * 128;
+    const int n0 = blockIdx.x * 128 * HALVES;
     const int I = blockIdx.y;
     const int b0 = __ldg(brp + I);
     const int nblk = __ldg(brp + I + 1) - b0;
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(kTThreads)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(kTTmemCols)
+                     "r"(kTmemColsT)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -330,9 +335,9 @@ __global__ void __launch_bounds__(kTThreads)
 
     if (warp == 0) {
         // Producer warp: lane 0 waits for the free slot and arms the barrier,
-        // then lanes 0..2 issue the stage's three boxes side by side (the A
-        // block and the two 64-column halves of the B tile).  The block
-        // columns of this block-row sit in registers, 32 at a time.
+        // then lanes 0..2*HALVES issue the stage's boxes side by side (the A
+        // block and the 64-column boxes of the B tile).  The block columns
+        // of this block-row sit in registers, 32 at a time.
         int b = 0, jreg = 0;
         for (; b < nblk; ++b) {
             const int s = b % STAGES;
@@ -349,10 +354,11 @@ __global__ void __launch_bounds__(kTThreads)
                 }
                 break;
             }
-            if (lane == 0) mbar_expect_tx(full_bar(s), kTStageBytes);
+            if (lane == 0) mbar_expect_tx(full_bar(s), kSB);
             __syncwarp();
             if (lane == 0) tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
-            else if (lane < 3) tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
+            else if (lane <= 2 * HALVES)
+                tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
         }
         if (lane == 0) s_issued = b;
     } else if (warp == 1 && lane == 0) {
@@ -368,9 +374,12 @@ __global__ void __launch_bounds__(kTThreads)
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < kBlk / 16; ++ks) {
-                const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
                 const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
-                mma_bf16(tmem_d, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < HALVES; ++h) {
+                    const uint64_t adesc = sw128_desc(stage_b(s) + 2 * h * kBBox + ks * 2048u, kBBox, 1024u);
+                    mma_bf16(tmem_d + 64 * h, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+                }
             }
             mma_commit(empty_bar(s));
         }
@@ -385,20 +394,23 @@ __global__ void __launch_bounds__(kTThreads)
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok && lane == 0) record_error(kErrAcc);
     tc_fence_after();
-    float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 32 * warp + lane;
-    if (nblk == 0) {
-        for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
-    } else if (ok && !s_abort) {
 #pragma unroll
-        for (int c0 = 0; c0 < kBlk; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
-            tmem_wait_ld();
+    for (int h = 0; h < HALVES; ++h) {
+        float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 128 * h + 32 * warp + lane;
+        if (nblk == 0) {
+            for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+        } else if (ok && !s_abort) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float* q = cp + static_cast<long long>(c0 + j) * ldc;
-                const float acc = alpha * __uint_as_float(v[j]);
-                __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+            for (int c0 = 0; c0 < kBlk; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + 64 * h + c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float* q = cp + static_cast<long long>(c0 + j) * ldc;
+                    const float acc = alpha * __uint_as_float(v[j]);
+                    __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+                }
             }
         }
     }
@@ -413,14 +425,15 @@ __global__ void __launch_bounds__(kTThreads)
     }
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTTmemCols) : "memory");
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemColsT) : "memory");
 }
 
 // C = beta * C (a BSR matrix without stored blocks).
-__global__ void bsr_scale_kernel(float* C, long long ldc, int N, float beta) {
+__global__ void bsr_scale_kernel(float* C, long long ldc, int M, int N, float beta) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c < N) {
-        float* q = C + static_cast<long long>(blockIdx.y) * ldc + c;
+    if (c >= N) return;
+    for (int r = blockIdx.y; r < M; r += gridDim.y) {
+        float* q = C + static_cast<long long>(r) * ldc + c;
         *q = beta * *q;
     }
 }
@@ -451,8 +464,8 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     }
     if (nnzb == 0) {
         // no stored block: C = beta * C
-        dim3 grid((N + 255) / 256, M);
-        bsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, N, beta);
+        dim3 grid((N + 255) / 256, M < 65535 ? M : 65535);
+        bsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, M, N, beta);
         spx_note_launches(1);
         return spx_cuda_status(cudaGetLastError());
     }
@@ -461,7 +474,8 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
         return SPX_ERR_CUDA;
     // Variant: "tileS" = non-persistent 128-column tiles with an S-deep ring
-    // (S = 2..5; smaller rings fit more CTAs per SM), "persistent" = the
+    // (S = 2..5; smaller rings fit more CTAs per SM), "wideS" = the same with
+    // 256-column tiles (S = 2..4, N a multiple of 256), "persistent" = the
     // persistent 256-column kernel.  SPX_BSR_VARIANT overrides the default.
     static int variant = -1;
     if (variant < 0) {
@@ -469,8 +483,10 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         if (const char* v = std::getenv("SPX_BSR_VARIANT")) {
             if (!std::strcmp(v, "persistent")) variant = 0;
             else if (!std::strncmp(v, "tile", 4) && v[4] >= '2' && v[4] <= '5' && v[5] == 0) variant = v[4] - '0';
+            else if (!std::strncmp(v, "wide", 4) && v[4] >= '2' && v[4] <= '4' && v[5] == 0) variant = 10 + v[4] - '0';
         }
     }
+    if (variant >= 10 && N % 256) variant = 3;
     cudaError_t e = cudaSuccess;
     if (variant == 0) {
         static std::once_flag attr_once;
@@ -494,19 +510,19 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                                                                static_cast<int>(tiles), ntq, kSpinLimit);
     } else {
         if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
-        dim3 grid(N / 128, M / kBlk);
         switch (variant) {
-#define SPX_TILE(S)                                                                                             \
-    case S: {                                                                                                   \
-        static cudaError_t ae = cudaFuncSetAttribute(bsr_spmm_tile_kernel<S>,                                   \
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,               \
-                                                     static_cast<int>(tile_smem_bytes<S>()));                   \
-        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                             \
-        bsr_spmm_tile_kernel<S><<<grid, kTThreads, tile_smem_bytes<S>(), st>>>(tmA, tmB, bsr_row_ptr, bsr_col, \
-                                                                               C, ldc, alpha, beta, kSpinLimit); \
-        break;                                                                                                  \
+#define SPX_TILE(S, H, V)                                                                                      \
+    case V: {                                                                                                     \
+        static cudaError_t ae = cudaFuncSetAttribute(bsr_spmm_tile_kernel<S, H>,                                  \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,                 \
+                                                     static_cast<int>(tile_smem_bytes<S, H>()));                  \
+        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                               \
+        bsr_spmm_tile_kernel<S, H><<<dim3(N / (128 * H), M / kBlk), kTThreads, tile_smem_bytes<S, H>(), st>>>(    \
+            tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit);                                     \
+        break;                                                                                                    \
     }
-            SPX_TILE(2) SPX_TILE(3) SPX_TILE(4) SPX_TILE(5)
+            SPX_TILE(2, 1, 2) SPX_TILE(3, 1, 3) SPX_TILE(4, 1, 4) SPX_TILE(5, 1, 5)
+            SPX_TILE(2, 2, 12) SPX_TILE(3, 2, 13) SPX_TILE(4, 2, 14)
 #undef SPX_TILE
         }
     }

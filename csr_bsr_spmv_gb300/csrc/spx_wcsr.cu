@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -39,15 +40,17 @@ using namespace spx_tc;
 namespace {
 
 constexpr int kWin = 64;                       // window height = chunk width
-constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = kWin * kWin * 2;  // 8 KB A block
 constexpr uint32_t kBBox = kWin * 64 * 2;      // 64 k-rows x 64 n, 8 KB
-constexpr uint32_t kStageBytes = kABytes + 2 * kBBox;
-constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kIdesc = idesc_bf16_mn_k(128, 64);
-constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s)
+
+// A stage holds one A chunk and the gathered B rows for 128*HALVES output columns.
+template <int HALVES>
+__host__ __device__ constexpr uint32_t stage_bytes() { return kABytes + 2 * HALVES * kBBox; }
+template <int STAGES, int HALVES>
+constexpr size_t smem_bytes() { return STAGES * stage_bytes<HALVES>() + 1024 + 256; }
 
 enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
 
@@ -61,6 +64,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+template <int STAGES, int HALVES>
 __global__ void __launch_bounds__(kThreads)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const int* __restrict__ win_ptr,
                      const int* __restrict__ win_col, const uint16_t* __restrict__ B, long long ldb,
@@ -71,6 +75,9 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ volatile int s_abort;
     __shared__ int s_issued, s_consumed;
 
+    constexpr int kStages = STAGES;
+    constexpr uint32_t kStageBytes = stage_bytes<HALVES>();
+    constexpr uint32_t kTmemCols = 64 * HALVES;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t bars = base + kStages * kStageBytes;
     auto afull = [&](int s) { return bars + 8u * s; };                 // TMA bytes of the A block
@@ -81,7 +88,7 @@ __global__ void __launch_bounds__(kThreads)
     auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * 128;
+    const int n0 = blockIdx.x * 128 * HALVES;
     const int w = blockIdx.y;
     const int g0 = __ldg(win_ptr + w);
     const int nch = __ldg(win_ptr + w + 1) - g0;
@@ -139,9 +146,12 @@ __global__ void __launch_bounds__(kThreads)
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kWin / 16; ++ks) {
-                    const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
                     const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
-                    mma_bf16(tmem_d, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh) {
+                        const uint64_t adesc = sw128_desc(stage_b(s) + 2 * hh * kBBox + ks * 2048u, kBBox, 1024u);
+                        mma_bf16(tmem_d + 64 * hh, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(empty(s));
             }
@@ -150,9 +160,9 @@ __global__ void __launch_bounds__(kThreads)
             else mbar_arrive(acc_bar);
         }
     } else {
-        // Gather: thread t copies compressed column k = t/2 (one B row), half h = t%2
-        // (64 of the tile's 128 columns = 128 bytes = 8 chunks of 16 bytes) into the
-        // 128-byte-swizzled box h: row k at k*128, 16-byte chunk j at (j ^ (k & 7)).
+        // Gather: thread t copies compressed column k = t/2 (one B row) into the
+        // boxes h = t%2, t%2 + 2, ... (64 columns = 128 bytes = 8 chunks of 16 bytes
+        // each) of the 128-byte-swizzled tile: row k at k*128, chunk j at (j ^ (k & 7)).
         const int t = threadIdx.x - 64;
         const int k = t >> 1, h = t & 1;
         const uint32_t row_off = h * kBBox + k * 128u;
@@ -175,7 +185,10 @@ __global__ void __launch_bounds__(kThreads)
             const uint32_t nbytes = c >= 0 ? 16u : 0u;  // padding column: zero-fill
             const uint32_t dst = stage_b(s) + row_off;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) cp_async16(dst + ((j ^ (k & 7)) << 4), src + (c >= 0 ? 8 * j : 0), nbytes);
+            for (int hh = 0; hh < HALVES; ++hh)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    cp_async16(dst + 2 * hh * kBBox + ((j ^ (k & 7)) << 4), src + (c >= 0 ? 128 * hh + 8 * j : 0), nbytes);
             cp_async_commit();
             if (b >= kStages - 1) {  // the copies of stage b - (kStages - 1) have landed: publish them
                 cp_async_wait<kStages - 1>();
@@ -197,22 +210,25 @@ __global__ void __launch_bounds__(kThreads)
         if (!ok && lane == 0) record_error(kErrAcc);
         tc_fence_after();
         const int q = warp & 3;
-        float* cp = C + static_cast<long long>(w) * kWin * ldc + n0 + 32 * q + lane;
         const int rows = min(kWin, M - w * kWin);
-        if (nch == 0) {
-            for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
-        } else if (ok && !s_abort) {
 #pragma unroll
-            for (int c0 = 0; c0 < kWin; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
-                tmem_wait_ld();
+        for (int hh = 0; hh < HALVES; ++hh) {
+            float* cp = C + static_cast<long long>(w) * kWin * ldc + n0 + 128 * hh + 32 * q + lane;
+            if (nch == 0) {
+                for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+            } else if (ok && !s_abort) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (c0 + j < rows) {
-                        float* p = cp + static_cast<long long>(c0 + j) * ldc;
-                        const float acc = alpha * __uint_as_float(v[j]);
-                        __stcs(p, beta != 0.f ? acc + beta * *p : acc);
+                for (int c0 = 0; c0 < kWin; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < rows) {
+                            float* p = cp + static_cast<long long>(c0 + j) * ldc;
+                            const float acc = alpha * __uint_as_float(v[j]);
+                            __stcs(p, beta != 0.f ? acc + beta * *p : acc);
+                        }
                     }
                 }
             }
@@ -233,10 +249,11 @@ __global__ void __launch_bounds__(kThreads)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols) : "memory");
 }
 
-__global__ void wcsr_scale_kernel(float* C, long long ldc, int N, float beta) {
+__global__ void wcsr_scale_kernel(float* C, long long ldc, int M, int N, float beta) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c < N) {
-        float* q = C + static_cast<long long>(blockIdx.y) * ldc + c;
+    if (c >= N) return;
+    for (int r = blockIdx.y; r < M; r += gridDim.y) {
+        float* q = C + static_cast<long long>(r) * ldc + c;
         *q = beta != 0.f ? beta * *q : 0.f;
     }
 }
@@ -398,24 +415,42 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
         return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int W = static_cast<int>((static_cast<int64_t>(M) + kWin - 1) / kWin);
+    if (W > 65535) return SPX_ERR_UNSUPPORTED;  // windows map to gridDim.y
     if (nchunks == 0) {
-        dim3 grid((N + 255) / 256, M);
-        wcsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, N, beta);
+        dim3 grid((N + 255) / 256, M < 65535 ? M : 65535);
+        wcsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, M, N, beta);
         spx_note_launches(1);
         return spx_cuda_status(cudaGetLastError());
     }
     CUtensorMap tmA;
     if (!make_map(&tmA, win_val, kWin, static_cast<uint64_t>(nchunks) * kWin, kWin * 2)) return SPX_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(wcsr_spmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes));
-    });
-    if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
-    dim3 grid(N / 128, W);
-    wcsr_spmm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta,
-                                                         kSpinLimit);
+    // Variant: 128-column tiles with a 2-deep ring (default: four CTAs per SM,
+    // measured fastest), "s3" / "s4" deeper rings, "wide" 256-column tiles
+    // with a 2-deep ring (N a multiple of 256); SPX_WCSR_VARIANT overrides.
+    static int variant = -1;
+    if (variant < 0) {
+        variant = 2;
+        if (const char* v = std::getenv("SPX_WCSR_VARIANT")) {
+            if (!std::strcmp(v, "wide")) variant = 1;
+            else if (!std::strcmp(v, "s3")) variant = 3;
+            else if (!std::strcmp(v, "s4")) variant = 4;
+        }
+    }
+    if (variant == 1 && N % 256) variant = 2;
+    switch (variant) {
+#define SPX_WCSR(S, H, V)                                                                                      \
+    case V: {                                                                                                  \
+        static cudaError_t ae = cudaFuncSetAttribute(wcsr_spmm_kernel<S, H>,                                   \
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,              \
+                                                     static_cast<int>(smem_bytes<S, H>()));                    \
+        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                            \
+        wcsr_spmm_kernel<S, H><<<dim3(N / (128 * H), W), kThreads, smem_bytes<S, H>(), st>>>(                  \
+            tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit);                             \
+        break;                                                                                                 \
+    }
+        SPX_WCSR(2, 2, 1) SPX_WCSR(2, 1, 2) SPX_WCSR(3, 1, 3) SPX_WCSR(4, 1, 4)
+#undef SPX_WCSR
+    }
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }

@@ -507,7 +507,8 @@ spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const in
  * gather of the B rows named by window_col_idx into a swizzled shared tile,
  * tensor-core MMA).  One CTA per (window, 128 output columns); no atomics,
  * so the result is deterministic.  Supported: N a multiple of 128, ldb a
- * multiple of 8, win_val and B 16-byte aligned; any M and K.  Launches: 1.
+ * multiple of 8, win_val and B 16-byte aligned, at most 65535 windows
+ * (M <= 4,194,240); any K.  Launches: 1.
  * Bounded pipeline waits report SPX_ERR_TIMEOUT through
  * spx_last_device_error.
  */
