@@ -10,27 +10,22 @@
 // tcgen05.commit frees each stage, and the accumulator lives in TMEM, so no
 // warpgroup holds it in registers.
 //
-// Tile: a 64-row block-row I and 256 output columns.  Each MMA computes a
-// transposed half tile  D[n, r] += B[J*64 + k, n0 + n] * Ablk[r, k]  with
-// M = 128 (n), N = 64 (r), K = 16: B's tile is the A operand in MN-major form
-// (n contiguous, exactly as B is stored) and the A block is the B operand in
-// K-major form (k contiguous, as BSR stores a row-major block).  Both arrive
-// by 2-D TMA with the 128-byte swizzle.  A 256-column tile halves the L2->SM
-// re-reads of the A blocks compared with 128 columns; L2->SM bandwidth, not the
-// tensor pipe, bounds this product (every B tile is read once per block-row
-// that uses its block column).
+// The MMA computes a transposed tile  D[n, r] += B[J*64 + k, n0 + n] * Ablk[r, k]
+// with M = 128 (n), N = 64 (r), K = 16: B's tile is the A operand in MN-major
+// form (n contiguous, exactly as B is stored) and the A block is the B operand
+// in K-major form (k contiguous, as BSR stores a row-major block).  Both
+// arrive by 2-D TMA with the 128-byte swizzle.  L2->SM traffic, not the
+// tensor pipe, bounds this product: every B tile is read once per block-row
+// that uses its block column.
 //
-// Persistent CTAs (one per SM) walk a static tile schedule.  Warps 0..4 are TMA
-// producers, each owning one stage of the ring (one thread cannot issue TMA
-// fast enough to keep one SM fed: a single producer thread measured ~1/3 of
-// the L2->SM rate that several reach); within a stage, five lanes issue the A
-// block and the four B boxes at once.  Warp 5 issues the MMAs, warps 6..9 run
-// the epilogue.  The TMEM
-// accumulator is double-buffered (2 x 128 columns): while the epilogue drains
-// tile i (tcgen05.ld -> coalesced fp32 stores), the MMA warp accumulates tile
-// i+1.  The schedule is static and each tile costs its block-row's block count;
-// for a balanced pattern (equal blocks per block-row) the tail is under one
-// tile per CTA.
+// Default kernel (bsr_spmm_tile_kernel, "tile3"): non-persistent, one CTA per
+// (128-column tile, block-row), three CTAs per SM, each an independent 3-deep
+// TMA -> MMA ring; many small independent pipelines per SM measured fastest.
+// Variants kept for measurement (SPX_BSR_VARIANT): other ring depths, 256-
+// column tiles ("wideS"), and the persistent kernel below (bsr_spmm_tc_kernel:
+// one CTA per SM walking a static tile schedule, five producer warps each
+// owning a ring stage, one MMA warp, four epilogue warps, a double-buffered
+// TMEM accumulator so the epilogue of tile i overlaps tile i+1).
 //
 // Every mbarrier wait is bounded (clock64); on expiry the CTA records an error
 // word (read by spx_last_device_error), stops issuing, waits (bounded) for
@@ -74,6 +69,11 @@ __device__ int g_bsr_error;
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_bsr_error, 0, code); }
 
+// Persistent variant: 256-column tiles (two M = 128 halves share each A block),
+// a static tile schedule over one CTA per SM, warps 0..4 TMA producers each
+// owning one ring stage (lanes issue the A block and the four B boxes at
+// once), warp 5 the MMA issuer, warps 6..9 the epilogue; the TMEM accumulator
+// is double-buffered (2 x 128 columns).
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_spmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
