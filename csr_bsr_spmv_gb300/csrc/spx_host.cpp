@@ -294,18 +294,7 @@ spx_status spx_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_r
         return build_csr_host(M, K, nnz, coo_row, coo_col, static_cast<const char*>(coo_val), val_bytes, row_ptr, col,
                               static_cast<char*>(val));
     if (where != SPX_DEVICE) return SPX_ERR_ARG;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    std::vector<int32_t> r, c, rp_h(static_cast<size_t>(M) + 1), co(static_cast<size_t>(nnz));
-    std::vector<char> v, vo(static_cast<size_t>(nnz * val_bytes));
-    spx_status s = to_host(r, coo_row, nnz, st);
-    if (s == SPX_OK) s = to_host(c, coo_col, nnz, st);
-    if (s == SPX_OK) s = to_host(v, static_cast<const char*>(coo_val), nnz * val_bytes, st);
-    if (s == SPX_OK)
-        s = build_csr_host(M, K, nnz, r.data(), c.data(), v.data(), val_bytes, rp_h.data(), co.data(), vo.data());
-    if (s == SPX_OK) s = to_device(row_ptr, rp_h.data(), rp_h.size() * 4, st);
-    if (s == SPX_OK) s = to_device(col, co.data(), co.size() * 4, st);
-    if (s == SPX_OK) s = to_device(val, vo.data(), vo.size(), st);
-    return s;
+    return spx_dev_build_csr(M, K, nnz, coo_row, coo_col, coo_val, val_bytes, row_ptr, col, val, stream);
 }
 
 spx_status spx_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
@@ -318,18 +307,7 @@ spx_status spx_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* r
         return transpose_host(M, K, nnz, row_ptr, col, static_cast<const char*>(val), val_bytes, t_row_ptr, t_col,
                               static_cast<char*>(t_val));
     if (where != SPX_DEVICE) return SPX_ERR_ARG;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    std::vector<int32_t> rp, c, trp(static_cast<size_t>(K) + 1), tc(static_cast<size_t>(nnz));
-    std::vector<char> v, tv(static_cast<size_t>(nnz * val_bytes));
-    spx_status s = to_host(rp, row_ptr, static_cast<int64_t>(M) + 1, st);
-    if (s == SPX_OK) s = to_host(c, col, nnz, st);
-    if (s == SPX_OK) s = to_host(v, static_cast<const char*>(val), nnz * val_bytes, st);
-    if (s == SPX_OK)
-        s = transpose_host(M, K, nnz, rp.data(), c.data(), v.data(), val_bytes, trp.data(), tc.data(), tv.data());
-    if (s == SPX_OK) s = to_device(t_row_ptr, trp.data(), trp.size() * 4, st);
-    if (s == SPX_OK) s = to_device(t_col, tc.data(), tc.size() * 4, st);
-    if (s == SPX_OK) s = to_device(t_val, tv.data(), tv.size(), st);
-    return s;
+    return spx_dev_transpose_csr(M, K, nnz, row_ptr, col, val, val_bytes, t_row_ptr, t_col, t_val, stream);
 }
 
 spx_status spx_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,

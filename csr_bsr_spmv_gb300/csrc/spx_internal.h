@@ -19,6 +19,16 @@ int spx_coo_error_take();
 // Reads and clears the error word of the WCSR kernel: 0 or SPX_ERR_TIMEOUT.
 int spx_wcsr_error_take();
 
+// Device-side builders (spx_build.cu): stable radix sorts on the GPU, results
+// identical to the host builders.  Stream-ordered; temporary memory from the
+// stream-ordered allocator.
+spx_status spx_dev_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_row, const int32_t* coo_col,
+                             const void* coo_val, int32_t val_bytes, int32_t* row_ptr, int32_t* col, void* val,
+                             spx_stream_t stream);
+spx_status spx_dev_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                                 const void* val, int32_t val_bytes, int32_t* t_row_ptr, int32_t* t_col, void* t_val,
+                                 spx_stream_t stream);
+
 struct spx_plan {
     int32_t M = 0, K = 0;
     int64_t nnz = 0;

@@ -73,8 +73,13 @@ spx_status spx_launch_count(uint64_t* count);
  *     val_bytes bytes per entry (2, 4 or 8; values are moved, not read).
  *   row_ptr[M+1], col[nnz], val[nnz*val_bytes]: outputs.
  * Errors: SPX_ERR_INDEX_RANGE for a row outside [0, M) or col outside [0, K).
- * where == SPX_DEVICE: arrays are device memory; they are staged through
- * host memory and the call synchronises `stream`.
+ * where == SPX_HOST: a counting sort on the host.  where == SPX_DEVICE: the
+ * arrays are device memory and the build runs on the GPU (a stable LSD radix
+ * sort by column, then by row, with 8-bit digits; exact per-row counts and a
+ * scan give row_ptr): same result, bit for bit.  The device build validates
+ * the indices first (one synchronisation of `stream`), then enqueues the rest
+ * on `stream`; its temporary memory (about 16 bytes per entry) comes from the
+ * stream-ordered allocator and is released on `stream`.
  */
 spx_status spx_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_row, const int32_t* coo_col,
                          const void* coo_val, int32_t val_bytes, int32_t* row_ptr, int32_t* col, void* val,
@@ -87,8 +92,10 @@ spx_status spx_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_r
  * source row order (a stable counting sort by column).
  *   t_row_ptr[K+1], t_col[nnz], t_val[nnz*val_bytes]: outputs.
  * Errors: SPX_ERR_ARG if row_ptr[0] != 0 or row_ptr[M] != nnz;
- * SPX_ERR_INDEX_RANGE for a column outside [0, K).
- * where == SPX_DEVICE: staged through host memory (synchronises `stream`).
+ * SPX_ERR_INDEX_RANGE for a column outside [0, K); SPX_ERR_NOT_SORTED when
+ * row_ptr decreases.  where == SPX_DEVICE: built on the GPU by a stable radix
+ * sort of the entries by column (validation synchronises `stream` once; the
+ * rest is stream-ordered, temporary memory from the stream-ordered allocator).
  */
 spx_status spx_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
                              const void* val, int32_t val_bytes, int32_t* t_row_ptr, int32_t* t_col, void* t_val,
