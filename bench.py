@@ -514,6 +514,37 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     assert spx.spx_last_device_error(stream) == 0, "device error word set during the timed region"
 
+    # ---------------- the stream + gather floor of the same matrix (SpMV workloads)
+    gather_floor = None
+    # (workloads with uniformly random columns: there the x gathers have no locality, so no kernel
+    # over these arrays can beat the probe; banded columns give the group kernel a locality the
+    # grid-stride probe does not have)
+    if w in ("power-law", "uniform") and not args.no_floor:
+        probes = [(A, x)]
+        part = torch.empty(spx._lib().spx_gather_probe_blocks(), device=dev)
+
+        def probe():
+            for Am, xv in probes:
+                spx.spx_gather_probe(Am, xv, part, stream=stream)
+
+        for _ in range(args.warmup):
+            flush_l2()
+            probe()
+        torch.cuda.synchronize(dev)
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for s_, e_ in pe:
+            flush_l2()
+            s_.record(stream)
+            probe()
+            e_.record(stream)
+        torch.cuda.synchronize(dev)
+        pms = sum(s_.elapsed_time(e_) for s_, e_ in pe) / len(pe)
+        gather_floor = {"probe_ms": round(pms, 5), "kernel_over_floor": round(ms / pms, 3),
+                        "gathers_per_s": round(c["row"].size / (pms * 1e-3), 1),
+                        "what": "spx_gather_probe on the same col/val/x: stream them and gather x once per nonzero, "
+                                "no row work -- the floor of any SpMV over uniformly random columns; "
+                                "kernel_over_floor = step time / probe time"}
+
     # ---------------- end to end through the public call with pinned host buffers
     e2e = None
     if e2e_run is not None and not args.no_e2e:
@@ -546,6 +577,8 @@ def run_ours(args, rank, world):
                 "frac": round(ach / pk["hbm"], 4), "peak_source": pk["src"] + " (HBM copy)"}
     tr = traffic_from_profile(w, src)
     roof["traffic"] = tr
+    if gather_floor is not None:
+        roof["gather_floor"] = gather_floor
     roof["algorithmic_bytes"] = int(abytes)
     roof["timed"] = "whole step (all launches of the call), CUDA events on the launching stream"
 
@@ -670,6 +703,7 @@ def main():
                     choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
                              "spmm128-bf16", "bsr", "wcsr"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
+    ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

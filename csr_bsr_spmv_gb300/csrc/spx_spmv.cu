@@ -291,6 +291,36 @@ __global__ void __launch_bounds__(kThreads) spmv_fixup_kernel(const int4* __rest
     if (lane == 0) emit(y, lr.x, s, alpha, beta);
 }
 
+// Stream + gather floor of a CSR SpMV: sum of val[p] * x[col[p]] over all
+// nonzeros with no row structure at all (grid-stride, 8 gathers in flight per
+// thread, one partial sum per CTA).  Measurement aid: the time this takes on a
+// matrix is the floor for any SpMV kernel that reads each value and column
+// once and gathers x once per nonzero.
+__global__ void __launch_bounds__(kThreads) gather_probe_kernel(const int* __restrict__ col,
+                                                                const float* __restrict__ val,
+                                                                const float* __restrict__ x, long long n,
+                                                                float* __restrict__ partials) {
+    constexpr int U = 8;
+    const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+    long long p = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x;
+    float s = 0.f;
+    for (; p + (U - 1) * stride < n; p += U * stride) {
+        int c[U];
+        float v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            c[j] = ld_stream(col + p + j * stride);
+            v[j] = ld_stream(val + p + j * stride);
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) s += v[j] * __ldg(x + c[j]);
+    }
+    for (; p < n; p += stride) s += ld_stream(val + p) * __ldg(x + ld_stream(col + p));
+    __shared__ float red[kWarps];
+    s = block_sum<kThreads>(s, red);
+    if (threadIdx.x == 0) partials[blockIdx.x] = s;
+}
+
 spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const float* val, float alpha,
                        const float* x, float beta, float* y, float* scratch, cudaStream_t st) {
     const int ntasks = static_cast<int>(P->counts[0]);
@@ -347,6 +377,25 @@ spx_status check_call(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, cons
 }  // namespace
 
 extern "C" {
+
+int32_t spx_gather_probe_blocks(void) {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return 8 * nsm;
+}
+
+spx_status spx_gather_probe(int64_t nnz, const int32_t* col, const float* val, const float* x, int32_t K,
+                            float* partials, int32_t nblocks, spx_stream_t stream) {
+    if (nnz < 0 || K < 0 || nblocks < 1 || !partials || (nnz > 0 && (!col || !val || !x))) return SPX_ERR_ARG;
+    if (nnz > 0) {
+        gather_probe_kernel<<<nblocks, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(col, val, x, nnz,
+                                                                                            partials);
+        spx_note_launches(1);
+    }
+    return spx_cuda_status(cudaGetLastError());
+}
+
 
 spx_status spx_spmv_csr(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
                         const int32_t* col, const float* val, float alpha, const float* x, float beta, float* y,

@@ -122,6 +122,8 @@ def _lib():
             "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
                                 ctypes.c_int, vp], ctypes.c_int),
             "spx_spmm_wcsr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_gather_probe_blocks": ([], ctypes.c_int32),
+            "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
@@ -555,6 +557,16 @@ def spx_spmm_bsr(M: int, K: int, br: int, bc: int, bsr_row_ptr, bsr_col, bsr_val
                                B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
            "spx_spmm_bsr")
     return C
+
+
+def spx_gather_probe(A: Csr, x: torch.Tensor, partials: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The stream + gather floor kernel over A's col/val and x (see include/spx.h)."""
+    nb = int(_lib().spx_gather_probe_blocks())
+    if partials is None:
+        partials = torch.empty(nb, dtype=torch.float32, device=x.device)
+    _check(_lib().spx_gather_probe(A.nnz, _ptr(A.col), _ptr(A.val), _ptr(x), A.K, _ptr(partials), partials.numel(),
+                                   _stream(stream)), "spx_gather_probe")
+    return partials
 
 
 def spx_last_device_error(stream=None) -> int:

@@ -523,6 +523,24 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
                          const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                          float* C, int64_t ldc, spx_stream_t stream);
 
+/* ------------------------------------------------------------ measurement */
+
+/*
+ * The stream + gather floor of a CSR SpMV over a matrix: partials[b] = the
+ * sum, over a grid-stride share of the nonzeros, of val[p] * x[col[p]] -- each
+ * value and column read once, x gathered once per nonzero, no rows, no
+ * reduction order (a probe, not a product).  Its time is the floor for any
+ * SpMV kernel over the same col/val/x, since the random x gathers, not HBM
+ * bandwidth, bound a product whose columns are spread over a vector larger
+ * than the L1 caches (the request rate of the gathers, [SpMM-ops] §2.5).
+ * Columns must lie in [0, K) (not checked: use matrices built by this
+ * library).  nblocks: CTAs of 256 threads (spx_gather_probe_blocks() = 8 per
+ * SM).  Launches: 1.
+ */
+int32_t spx_gather_probe_blocks(void);
+spx_status spx_gather_probe(int64_t nnz, const int32_t* col, const float* val, const float* x, int32_t K,
+                            float* partials, int32_t nblocks, spx_stream_t stream);
+
 /*
  * Synchronises `stream`, then reads and clears the device-side error words:
  * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr or spx_spmm_wcsr gave up, else the index

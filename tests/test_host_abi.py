@@ -333,3 +333,14 @@ def test_spmm_wcsr_rejects_unsupported_without_launching():
     assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 128, a, 64, 1.0, 0.0, a, 128, None) == -1    # ldb < N
     assert lib.spx_spmm_wcsr(64, 64, -1, a, a, a, 128, a, 128, 1.0, 0.0, a, 128, None) == -1
     assert spx.launch_count() == before
+
+
+def test_gather_probe_rejects_bad_arguments_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.spx_gather_probe(-1, a, a, a, 4, a, 8, None) == -1
+    assert lib.spx_gather_probe(10, None, a, a, 4, a, 8, None) == -1
+    assert lib.spx_gather_probe(10, a, a, a, 4, a, 0, None) == -1
+    assert lib.spx_gather_probe(10, a, a, a, 4, None, 8, None) == -1
+    assert spx.launch_count() == before
