@@ -142,3 +142,15 @@ def test_power_law_full_size_sampled():
     ref, bound = oracle.spmv(M, rp, col, val, cfg["x"], 1.0, 0.5, cfg["y"], rows=rows)
     assert_within(got[rows], ref, bound, what="power-law full size")
     assert plan.info["split_rows"] > 0 and plan.info["cta_rows"] > 0
+
+
+def test_gather_probe_reads_every_nonzero():
+    """The floor probe does the gather work: its partial sums add up to sum_p val_p * x[col_p]."""
+    d = synth.random_coo(55, 30000, 70000, 0, 40)
+    rp, col, val = oracle.build_csr(30000, 70000, d["row"], d["col"], d["val"])
+    A = csr_to_device(30000, 70000, rp, col, val)
+    x = synth.uniform(55, synth.T_X, 70000)
+    parts = spx.spx_gather_probe(A, dev(x))
+    torch.cuda.synchronize()
+    prods = val.astype(np.float64) * x[col].astype(np.float64)
+    assert abs(parts.double().sum().item() - prods.sum()) <= 1e-5 * np.abs(prods).sum() + 1e-6
