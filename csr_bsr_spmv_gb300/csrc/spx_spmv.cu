@@ -406,6 +406,74 @@ spx_status spx_spmv_csr(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t spx_spmv_csr_hostio_work_bytes(int32_t M, int32_t K) {
+    if (M < 0 || K < 0) return 0;
+    const size_t xb = (4 * static_cast<size_t>(K) + 255) & ~static_cast<size_t>(255);
+    const size_t yb = (4 * static_cast<size_t>(M) + 255) & ~static_cast<size_t>(255);
+    return 2 * (xb + yb);
+}
+
+spx_status spx_spmv_csr_hostio(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                               const int32_t* col, const float* val, float alpha, const float* x_host,
+                               int64_t x_stride, float beta, float* y_host, int64_t y_stride, int32_t nbatch,
+                               void* work, size_t work_bytes, void* scratch, size_t scratch_bytes,
+                               spx_stream_t stream) {
+    if (!spx_plan_ok(plan) || nbatch < 0 || (x_stride != 0 && x_stride < K) || y_stride < M) return SPX_ERR_ARG;
+    if (nbatch == 0 || M == 0) return SPX_OK;
+    if (!x_host || !y_host || !work || work_bytes < spx_spmv_csr_hostio_work_bytes(M, K)) return SPX_ERR_ARG;
+    if (!spx_aligned(work, 256)) return SPX_ERR_ALIGN;
+    const size_t xb = (4 * static_cast<size_t>(K) + 255) & ~static_cast<size_t>(255);
+    const size_t yb = (4 * static_cast<size_t>(M) + 255) & ~static_cast<size_t>(255);
+    float* xs[2] = {static_cast<float*>(work), reinterpret_cast<float*>(static_cast<char*>(work) + xb + yb)};
+    float* ys[2] = {reinterpret_cast<float*>(static_cast<char*>(work) + xb),
+                    reinterpret_cast<float*>(static_cast<char*>(work) + 2 * xb + yb)};
+    spx_status s = check_call(plan, M, K, nnz, row_ptr, col, val, xs[0], ys[0], scratch, scratch_bytes);
+    if (s != SPX_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Two copy streams and the caller's stream: batch b's inputs go up while
+    // batch b-1 computes and batch b-2's result comes down (two device slots).
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t ev[8] = {};  // start, up_done[2], k_done[2], down_done[2], end
+    cudaError_t e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking);
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    cudaEvent_t& start = ev[0];
+    cudaEvent_t* up_done = ev + 1;
+    cudaEvent_t* k_done = ev + 3;
+    cudaEvent_t* down_done = ev + 5;
+    cudaEvent_t& end = ev[7];
+    if (e == cudaSuccess) e = cudaEventRecord(start, st);  // the copies follow the caller's earlier work
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
+    for (int32_t b = 0; b < nbatch && e == cudaSuccess && s == SPX_OK; ++b) {
+        const int sl = b & 1;
+        const float* xh = x_host + static_cast<int64_t>(b) * x_stride;
+        float* yh = y_host + static_cast<int64_t>(b) * y_stride;
+        if (b >= 2) e = cudaStreamWaitEvent(up, down_done[sl], 0);  // slot free: batch b-2 is home
+        if (e == cudaSuccess) e = cudaMemcpyAsync(xs[sl], xh, 4 * static_cast<size_t>(K), cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess && beta != 0.f)
+            e = cudaMemcpyAsync(ys[sl], yh, 4 * static_cast<size_t>(M), cudaMemcpyHostToDevice, up);
+        if (e == cudaSuccess) e = cudaEventRecord(up_done[sl], up);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, up_done[sl], 0);
+        if (e == cudaSuccess) s = launch_spmv(plan, row_ptr, col, val, alpha, xs[sl], beta, ys[sl],
+                                              static_cast<float*>(scratch), st);
+        if (e == cudaSuccess && s == SPX_OK) e = cudaEventRecord(k_done[sl], st);
+        if (e == cudaSuccess && s == SPX_OK) e = cudaStreamWaitEvent(down, k_done[sl], 0);
+        if (e == cudaSuccess && s == SPX_OK)
+            e = cudaMemcpyAsync(yh, ys[sl], 4 * static_cast<size_t>(M), cudaMemcpyDeviceToHost, down);
+        if (e == cudaSuccess && s == SPX_OK) e = cudaEventRecord(down_done[sl], down);
+    }
+    // the caller's stream resumes once every result is home
+    if (e == cudaSuccess) e = cudaEventRecord(end, down);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, end, 0);
+    for (int i = 0; i < 8; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    if (up) cudaStreamDestroy(up);
+    if (down) cudaStreamDestroy(down);
+    if (s != SPX_OK) return s;
+    return e == cudaSuccess ? SPX_OK : SPX_ERR_CUDA;
+}
+
 spx_status spx_spmv_csr_dual(const spx_plan* pA, const spx_plan* pAt, int32_t m, int32_t n, int64_t nnz,
                              const int32_t* A_rp, const int32_t* A_col, const float* A_val, const int32_t* At_rp,
                              const int32_t* At_col, const float* At_val, float* v, float alpha_u, float beta_u,

@@ -110,6 +110,9 @@ def _lib():
             "spx_spmv_sell": ([vp, i32, i32, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
+            "spx_spmv_csr_hostio_work_bytes": ([i32, i32], sz),
+            "spx_spmv_csr_hostio": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, i64, f32, vp, i64, i32, vp, sz, vp, sz, vp],
+                                    ctypes.c_int),
             "spx_spmv_coo_scratch_bytes": ([i64], sz),
             "spx_spmv_coo": ([i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
             "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
@@ -485,6 +488,26 @@ def spx_spmv_csr_noalloc(plan: Plan, A: Csr, x: torch.Tensor, y: torch.Tensor, a
                                        float(alpha), _ptr(x), float(beta), _ptr(y), _stream(stream)),
            "spx_spmv_csr_noalloc")
     return y
+
+
+def spx_spmv_csr_hostio(plan: Plan, A: Csr, x_host: torch.Tensor, y_host: torch.Tensor, alpha: float = 1.0,
+                        beta: float = 0.0, work: torch.Tensor | None = None, stream=None):
+    """y_host[b] <- alpha*A*x_host[b] + beta*y_host[b] for every row b of the (batch x K) / (batch x M)
+    host tensors (pinned for full speed); copies pipelined against the products.  Synchronises."""
+    assert not x_host.is_cuda and not y_host.is_cuda and x_host.dim() == 2 and y_host.dim() == 2
+    assert x_host.stride(1) == 1 and y_host.stride(1) == 1
+    assert x_host.shape[0] in (1, y_host.shape[0])  # one x for every batch, or one per batch
+    need = int(_lib().spx_spmv_csr_hostio_work_bytes(A.M, A.K))
+    if work is None:
+        work = torch.empty(max(1, need // 4), dtype=torch.float32, device=plan.table.device)
+    sc = plan.scratch
+    _check(_lib().spx_spmv_csr_hostio(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val),
+                                      float(alpha), _ptr(x_host), x_host.stride(0) if x_host.shape[0] > 1 else 0,
+                                      float(beta), _ptr(y_host), y_host.stride(0), y_host.shape[0], _ptr(work),
+                                      work.numel() * 4, _ptr(sc),
+                                      sc.numel() * 4, _stream(stream)), "spx_spmv_csr_hostio")
+    (stream or torch.cuda.current_stream()).synchronize()
+    return y_host
 
 
 def spx_spmv_coo_scratch_bytes(nnz: int) -> int:

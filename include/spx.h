@@ -282,6 +282,29 @@ spx_status spx_spmv_csr(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz,
                         void* scratch, size_t scratch_bytes, spx_stream_t stream);
 
 /*
+ * spx_spmv_csr over nbatch (x, y) pairs in HOST memory (pinned for full
+ * speed): for batch b, x_host[b*x_stride .. +K) is copied up (x_stride 0:
+ * the same x for every batch; else x_stride >= K), y = alpha*A x +
+ * beta*y is computed (y_host[b*y_stride .. +M) copied up first when beta != 0)
+ * and y is copied back into y_host.  The copies run on two streams of their
+ * own, so batch b's upload and batch b-2's download overlap batch b-1's
+ * product (two device slots for x and y in `work`).  A serving pipeline over
+ * one stored matrix; the pages' SpMV ([SpMM-ops] §2) per batch.
+ *   work: device memory of at least spx_spmv_csr_hostio_work_bytes(M, K)
+ *         bytes, 256-byte aligned, owned by the caller;
+ *   scratch: as for spx_spmv_csr.
+ * All work is ordered after earlier work on `stream`, and `stream` resumes
+ * only when every result is back in y_host: synchronise `stream` before
+ * reading y_host.  Launches: those of spx_spmv_csr, per batch.
+ */
+size_t spx_spmv_csr_hostio_work_bytes(int32_t M, int32_t K);
+spx_status spx_spmv_csr_hostio(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                               const int32_t* col, const float* val, float alpha, const float* x_host,
+                               int64_t x_stride, float beta, float* y_host, int64_t y_stride, int32_t nbatch,
+                               void* work, size_t work_bytes, void* scratch, size_t scratch_bytes,
+                               spx_stream_t stream);
+
+/*
  * The two-direction operator pair of a least-squares solver, with CSC(A)
  * stored as CSR(A^T) so both directions are row sweeps ([LSMR-dual] §1, §4,
  * §5.2):

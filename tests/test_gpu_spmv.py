@@ -154,3 +154,27 @@ def test_gather_probe_reads_every_nonzero():
     torch.cuda.synchronize()
     prods = val.astype(np.float64) * x[col].astype(np.float64)
     assert abs(parts.double().sum().item() - prods.sum()) <= 1e-5 * np.abs(prods).sum() + 1e-6
+
+
+@pytest.mark.parametrize("nbatch,beta,shared_x", [(1, 0.0, False), (2, 0.5, False), (5, -1.25, False),
+                                                  (4, 0.0, True), (3, 2.0, True)])
+def test_hostio_pipeline_equals_device_calls(nbatch, beta, shared_x):
+    """The host-buffer pipeline gives, batch by batch, the device call's result bit for bit."""
+    L, _ = synth.lengths_zipf(56, 40000, 2.1, 20000, 14.0)
+    row, col = synth.cols_uniform(56, 50000, L)
+    rp, col, val = oracle.build_csr(40000, 50000, row, col, synth.uniform(56, synth.T_VAL, row.size))
+    A = csr_to_device(40000, 50000, rp, col, val)
+    plan = spx.spx_plan_csr(40000, 50000, A.nnz, rp)
+    xs = np.stack([synth.uniform(57 + b, synth.T_X, 50000) for b in range(1 if shared_x else nbatch)])
+    ys = np.stack([synth.uniform(57 + b, synth.T_Y, 40000) for b in range(nbatch)])
+    xh = torch.from_numpy(xs).pin_memory()
+    yh = torch.from_numpy(ys.copy()).pin_memory()
+    spx.spx_spmv_csr_hostio(plan, A, xh, yh, 1.5, beta)
+    for b in range(nbatch):
+        x = xs[0 if shared_x else b]
+        yd = dev(ys[b])
+        spx.spx_spmv_csr(plan, A, dev(x), yd, 1.5, beta)
+        torch.cuda.synchronize()
+        assert np.array_equal(yh[b].numpy().view(np.uint32), yd.cpu().numpy().view(np.uint32))
+        ref, bound = oracle.spmv(40000, rp, col, val, x, 1.5, beta, ys[b])
+        assert_within(yh[b].numpy(), ref, bound)

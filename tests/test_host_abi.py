@@ -344,3 +344,24 @@ def test_gather_probe_rejects_bad_arguments_without_launching():
     assert lib.spx_gather_probe(10, a, a, a, 4, a, 0, None) == -1
     assert lib.spx_gather_probe(10, a, a, a, 4, None, 8, None) == -1
     assert spx.launch_count() == before
+
+
+def test_hostio_rejects_bad_arguments_without_launching():
+    lib = spx._lib()
+    rp = np.array([0, 1, 2], np.int32)
+    p = spx.spx_plan_csr(2, 3, 2, rp, upload=False)
+    a = ctypes.c_void_p(1 << 20)
+    w = ctypes.c_void_p(1 << 24)
+    need = lib.spx_spmv_csr_hostio_work_bytes(2, 3)
+    assert need == 2 * (256 + 256)
+    before = spx.launch_count()
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 2, 0.0, a, 2, 1, w, need, None, 0, None) == -1
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 3, 0.0, a, 1, 1, w, need, None, 0, None) == -1
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 3, 0.0, a, 2, 1, w, need - 4, None, 0,
+                                   None) == -1
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 3, 0.0, a, 2, 1,
+                                   ctypes.c_void_p((1 << 24) + 16), need, None, 0, None) == -8
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 0, 0.0, a, 2, 1, w, need, None, 0,
+                                   None) == -10  # x broadcast is fine; the plan was never uploaded
+    assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 3, 0.0, a, 2, 0, w, need, None, 0, None) == 0
+    assert spx.launch_count() == before
