@@ -329,14 +329,18 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     const int4* tasks = static_cast<const int4*>(P->d_table);
     const int4* longrows = tasks + ntasks;
     const int B = P->opts.block_nnz, R = P->opts.block_rows;
-    // Eight products per thread: block_nnz 1024 / 2048 / 4096 runs 128 / 256 /
-    // 512-thread CTAs (smaller CTAs, more of them resident: measured better on
-    // skewed rows); other sizes take the runtime-loop form with 256 threads.
-    const int NT = (B == 1024 || B == 2048 || B == 4096) ? B / 8 : 256;
+    // Eight products per thread: block_nnz 512 / 1024 / 2048 / 4096 runs 64 /
+    // 128 / 256 / 512-thread CTAs (smaller CTAs, more of them resident: measured
+    // better on skewed rows); other sizes take the runtime-loop form with 256
+    // threads.
+    const int NT = (B == 512 || B == 1024 || B == 2048 || B == 4096) ? B / 8 : 256;
     const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) +
                         sizeof(int) * (static_cast<size_t>(R) + 1) + 2 * (NT / 32) * sizeof(float) +
                         sizeof(float) * static_cast<size_t>(R);
     switch (B) {
+        case 512:
+            spmv_tasks_kernel<64, 8><<<ntasks, 64, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            break;
         case 1024:
             spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;

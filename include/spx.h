@@ -207,8 +207,8 @@ typedef struct spx_plan spx_plan; /* opaque, host-side */
  * reduction code c is log2(w) (lanes per row) or 6 (segmented, D == 0).
  * Long-row table (4 int32 per split row): {row, first slot, #segments, 0}.
  * opts == NULL uses spx_plan_opts_auto of the matrix's statistics.
- * block_nnz 1024 / 2048 / 4096 runs 128 / 256 / 512-thread CTAs (eight
- * products per thread); other sizes run 256 threads.  row_ptr is read once (copied to
+ * block_nnz 512 / 1024 / 2048 / 4096 runs 64 / 128 / 256 / 512-thread CTAs
+ * (eight products per thread); other sizes run 256 threads.  row_ptr is read once (copied to
  * the host when where == SPX_DEVICE).  *plan_out must be released with
  * spx_plan_destroy.
  */

@@ -26,6 +26,8 @@ SMALL_OPTS = [
     dict(block_nnz=4096, block_rows=300, pack_max=2000, cta_max=9000, seg_nnz=3000, lanes_div=0),
     dict(block_nnz=1000, block_rows=50, pack_max=999, cta_max=3000, seg_nnz=1000, lanes_div=0),
     dict(block_nnz=8, block_rows=3, pack_max=8, cta_max=100, seg_nnz=40, lanes_div=0),
+    dict(block_nnz=512, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=0),
+    dict(block_nnz=512, block_rows=64, pack_max=200, cta_max=1000, seg_nnz=600, lanes_div=16),
 ]
 
 
