@@ -489,13 +489,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     if (variant >= 10 && N % 256) variant = 3;
     cudaError_t e = cudaSuccess;
     if (variant == 0) {
-        static std::once_flag attr_once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(attr_once, [] {
-            attr_err = cudaFuncSetAttribute(bsr_spmm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kSmemBytes));
-        });
-        if (attr_err != cudaSuccess) return SPX_ERR_CUDA;
+        if (set_smem_limit(bsr_spmm_tc_kernel, kSmemBytes) != cudaSuccess) return SPX_ERR_CUDA;
         static int nsm = 0;
         if (nsm == 0) {
             int dev = 0;
@@ -513,10 +507,8 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         switch (variant) {
 #define SPX_TILE(S, H, V)                                                                                      \
     case V: {                                                                                                     \
-        static cudaError_t ae = cudaFuncSetAttribute(bsr_spmm_tile_kernel<S, H>,                                  \
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,                 \
-                                                     static_cast<int>(tile_smem_bytes<S, H>()));                  \
-        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                               \
+        if (set_smem_limit(bsr_spmm_tile_kernel<S, H>, tile_smem_bytes<S, H>()) != cudaSuccess)                   \
+            return SPX_ERR_CUDA;                                                                                  \
         bsr_spmm_tile_kernel<S, H><<<dim3(N / (128 * H), M / kBlk), kTThreads, tile_smem_bytes<S, H>(), st>>>(    \
             tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit);                                     \
         break;                                                                                                    \

@@ -106,6 +106,22 @@ constexpr uint32_t idesc_bf16_mn_k(uint32_t M, uint32_t N) {
 }
 
 // ------------------------------------------------------------ host side
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device, and a process may drive several).
+template <class K>
+inline cudaError_t set_smem_limit(K* kernel, size_t bytes) {
+    static std::mutex mu;
+    static uint64_t done = 0;  // bit d: device d already set for this kernel
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && (done >> dev & 1u)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+    return e;
+}
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -440,10 +440,7 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
     switch (variant) {
 #define SPX_WCSR(S, H, V)                                                                                      \
     case V: {                                                                                                  \
-        static cudaError_t ae = cudaFuncSetAttribute(wcsr_spmm_kernel<S, H>,                                   \
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,              \
-                                                     static_cast<int>(smem_bytes<S, H>()));                    \
-        if (ae != cudaSuccess) return SPX_ERR_CUDA;                                                            \
+        if (set_smem_limit(wcsr_spmm_kernel<S, H>, smem_bytes<S, H>()) != cudaSuccess) return SPX_ERR_CUDA;    \
         wcsr_spmm_kernel<S, H><<<dim3(N / (128 * H), W), kThreads, smem_bytes<S, H>(), st>>>(                  \
             tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit);                             \
         break;                                                                                                 \
