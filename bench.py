@@ -518,6 +518,30 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     assert spx.spx_last_device_error(stream) == 0, "device error word set during the timed region"
 
+    # ---------------- launch-bound SpMV: the per-call time inside one CUDA graph of many calls
+    if w == "uniform":
+        calls = 200
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            run()  # warm the library's per-device set-up outside the capture
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(calls):
+                    run()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        extra["graph_us_per_call"] = round(g0.elapsed_time(g1) * 1e3 / (5 * calls), 3)
+        extra["graph_note"] = (f"{calls} calls captured in one CUDA graph, replayed 5 times, no L2 flush between calls "
+                               "(the matrix and vectors, 0.33 MB, stay in L2): the launch-bound cost per call")
+
     # ---------------- the stream + gather floor of the same matrix (SpMV workloads)
     gather_floor = None
     # (workloads with uniformly random columns: there the x gathers have no locality, so no kernel

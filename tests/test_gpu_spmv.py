@@ -180,3 +180,28 @@ def test_hostio_pipeline_equals_device_calls(nbatch, beta, shared_x):
         assert np.array_equal(yh[b].numpy().view(np.uint32), yd.cpu().numpy().view(np.uint32))
         ref, bound = oracle.spmv(40000, rp, col, val, x, 1.5, beta, ys[b])
         assert_within(yh[b].numpy(), ref, bound)
+
+
+def test_spmv_calls_capture_in_a_cuda_graph():
+    """The SpMV call enqueues kernels only (no allocation, no host synchronisation): it can be
+    captured in a CUDA graph, and replays give the direct call's result bit for bit."""
+    d = synth.random_coo(58, 5000, 4000, 0, 30)
+    rp, col, val = oracle.build_csr(5000, 4000, d["row"], d["col"], d["val"])
+    A = csr_to_device(5000, 4000, rp, col, val)
+    plan = spx.spx_plan_csr(5000, 4000, A.nnz, rp)
+    x = dev(synth.uniform(58, synth.T_X, 4000))
+    y_direct = dev(np.zeros(5000, np.float32))
+    spx.spx_spmv_csr(plan, A, x, y_direct, 2.0, 0.0)
+    y = dev(np.zeros(5000, np.float32))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        spx.spx_spmv_csr(plan, A, x, y, 2.0, 0.0, stream=s)
+        torch.cuda.synchronize()
+        y.zero_()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(4):
+                spx.spx_spmv_csr(plan, A, x, y, 2.0, 0.0, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_direct.cpu().numpy().view(np.uint32))
