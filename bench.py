@@ -435,6 +435,9 @@ def run_ours(args, rank, world):
         t0 = time.perf_counter()
         wp, wc, wv, fill = spx.spx_build_wcsr(M, K, rp, col, val)
         timings["build_wcsr_ms"] = 1e3 * (time.perf_counter() - t0)
+        dr, dc, dv = to_dev(rp), to_dev(col), to_dev(val.view(np.int16))
+        device_timing("build_wcsr_device_ms", lambda: spx.spx_build_wcsr(M, K, dr, dc, dv, stream=stream))
+        del dr, dc, dv
         c["nchunks"] = int(wc.size // 64)
         flops, abytes = accounting(c)
         d_wp, d_wc = to_dev(wp), to_dev(wc)
@@ -462,6 +465,10 @@ def run_ours(args, rank, world):
         t0 = time.perf_counter()
         brp, bcol, bval, fill = spx.spx_build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
         timings["build_bsr_ms"] = 1e3 * (time.perf_counter() - t0)
+        dr, dc, dv = to_dev(rp), to_dev(col), to_dev(val.view(np.int16))
+        device_timing("build_bsr_device_ms", lambda: spx.spx_build_bsr(M, K, dr, dc, dv, c["bs"], c["bs"],
+                                                                        stream=stream))
+        del dr, dc, dv
         d_brp, d_bcol = to_dev(brp), to_dev(bcol)
         d_bval = to_dev(bval.view(np.int16))
         Bm = to_dev(c["B_bf16"].view(np.int16))

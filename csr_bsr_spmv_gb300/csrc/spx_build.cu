@@ -1,4 +1,5 @@
-// spx_build.cu -- format builders on the GPU: COO -> CSR and CSR -> CSR(A^T).
+// spx_build.cu -- format builders on the GPU: COO -> CSR, CSR -> CSR(A^T),
+// CSR -> BSR and CSR -> WCSR.
 //
 // [Formats] §3 (COO -> CSR: histogram of the row indices, prefix sum, stable
 // scatter, entries of a row in column order) and [LSMR-dual] §2, §4 (CSR(A^T)
@@ -11,7 +12,14 @@
 //   warp counts), so every pass is stable and the result is the unique
 //   stable order.
 // COO -> CSR sorts by column, then by row (LSD over the pair); CSR -> CSR(A^T)
-// sorts by column only (the entries already come in row order).  The sort
+// sorts by column only (the entries already come in row order).  CSR -> BSR
+// ([AsyncSparse] §2.2.1: every block holding an entry, stored dense, block
+// columns ascending in a block-row) sorts by (block row, block column, place
+// in the block); a scan of the block starts numbers the blocks, and each entry
+// is scattered into its zeroed block.  CSR -> WCSR ([AsyncSparse] §2.2.2: per
+// 64-row window the ascending union of its columns, cut into chunks of 64
+// compressed columns) sorts by (window, column, row in the window); a scan of
+// the (window, column) starts gives each column its compressed position.  The sort
 // carries each entry's source index; columns and values (1, 2, 4 or 8 bytes)
 // are gathered through it at the end.  Row offsets come from exact per-row
 // counts and a scan.  Indices are validated first (SPX_ERR_INDEX_RANGE, like
@@ -163,6 +171,18 @@ __global__ void gather_keys(const int* __restrict__ src, const int* __restrict__
         keys[i] = static_cast<uint32_t>(src[idx[i]]);
 }
 
+// BSR sort keys of entry idx[i]: part 0 = its place inside the block
+// ((row mod br) * bc + col mod bc), 1 = its block column, 2 = its block row.
+__global__ void bsr_keys(const int* __restrict__ rowid, const int* __restrict__ col, const int* __restrict__ idx,
+                         int br, int bc, int part, uint32_t* __restrict__ keys, long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = idx[i];
+        const int r = rowid[p], c = col[p];
+        keys[i] = static_cast<uint32_t>(part == 0 ? (r % br) * bc + c % bc : part == 1 ? c / bc : r / br);
+    }
+}
+
 template <class T>
 __global__ void gather_values(const T* __restrict__ src, const int* __restrict__ idx, T* __restrict__ dst,
                               long long n) {
@@ -188,6 +208,111 @@ __global__ void expand_rows(const int* __restrict__ rp, int M, long long n, int*
             else hi = mid;
         }
         rowid[p] = lo;
+    }
+}
+
+// BSR: entries sorted by (block row, block column, place in the block).
+// flag[i] = 1 where a new block starts; bad |= 8 when two neighbours share (row, col).
+__global__ void bsr_mark(const int* __restrict__ ix, const int* __restrict__ rowid, const int* __restrict__ col,
+                         int br, int bc, long long n, uint32_t* __restrict__ flag, int* __restrict__ bad) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = ix[i];
+        const int r = rowid[p], c = col[p];
+        uint32_t f = 1;
+        if (i > 0) {
+            const int q = ix[i - 1];
+            const int r2 = rowid[q], c2 = col[q];
+            f = (r / br != r2 / br || c / bc != c2 / bc) ? 1u : 0u;
+            if (r == r2 && c == c2) atomicOr(bad, 8);
+        }
+        flag[i] = f;
+    }
+}
+
+// blocks per block row (from the block starts), for the block-row offsets
+__global__ void bsr_count(const int* __restrict__ ix, const int* __restrict__ rowid, const uint32_t* __restrict__ flag,
+                          int br, long long n, uint32_t* __restrict__ cnt) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT)
+        if (flag[i]) atomicAdd(&cnt[rowid[ix[i]] / br], 1u);
+}
+
+// Entry i of the sorted order lands in block slot[i] (inclusive scan of the
+// starts, minus one) at (row mod br, col mod bc); the block's column is
+// written by its first entry.
+template <class T>
+__global__ void bsr_scatter(const int* __restrict__ ix, const int* __restrict__ rowid, const int* __restrict__ col,
+                            const T* __restrict__ val, const uint32_t* __restrict__ flag,
+                            const uint32_t* __restrict__ excl, int br, int bc, long long n, int* __restrict__ bcol,
+                            T* __restrict__ bval) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = ix[i];
+        const int r = rowid[p], c = col[p];
+        const long long b = static_cast<long long>(excl[i]) + flag[i] - 1;
+        if (flag[i]) bcol[b] = c / bc;
+        bval[b * br * bc + static_cast<long long>(r % br) * bc + c % bc] = val[p];
+    }
+}
+
+// WCSR (windows of 64 rows): entries sorted by (window, column, row in the
+// window).  flag[i] = 1 where a new (window, column) starts, counted per
+// window in cnt[w]; bad |= 8 when two neighbours share (row, col).
+constexpr int kWin = 64;
+
+__global__ void wcsr_keys(const int* __restrict__ rowid, const int* __restrict__ col, const int* __restrict__ idx,
+                          int part, uint32_t* __restrict__ keys, long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = idx[i];
+        const int r = rowid[p];
+        keys[i] = static_cast<uint32_t>(part == 0 ? r % kWin : part == 1 ? col[p] : r / kWin);
+    }
+}
+
+__global__ void wcsr_mark(const int* __restrict__ ix, const int* __restrict__ rowid, const int* __restrict__ col,
+                          long long n, uint32_t* __restrict__ flag, uint32_t* __restrict__ cnt, int* __restrict__ bad) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = ix[i];
+        const int r = rowid[p], c = col[p];
+        uint32_t f = 1;
+        if (i > 0) {
+            const int q = ix[i - 1];
+            const int r2 = rowid[q], c2 = col[q];
+            f = (r / kWin != r2 / kWin || c != c2) ? 1u : 0u;
+            if (r == r2 && c == c2) atomicOr(bad, 8);
+        }
+        flag[i] = f;
+        if (f) atomicAdd(&cnt[r / kWin], 1u);
+    }
+}
+
+// chunks of window w = ceil(distinct columns / 64)
+__global__ void wcsr_chunks(const uint32_t* __restrict__ cnt, long long W, uint32_t* __restrict__ nch) {
+    for (long long w = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; w < W;
+         w += static_cast<long long>(gridDim.x) * kT)
+        nch[w] = (cnt[w] + kWin - 1) / kWin;
+}
+
+// Entry i has compressed position k = (distinct index) - (window's first
+// distinct index); it lands in chunk wp[w] + k / 64 at (row mod 64, k mod 64).
+// The first entry of each (window, column) writes the column.
+template <class T>
+__global__ void wcsr_scatter(const int* __restrict__ ix, const int* __restrict__ rowid, const int* __restrict__ col,
+                             const T* __restrict__ val, const uint32_t* __restrict__ flag,
+                             const uint32_t* __restrict__ excl, const uint32_t* __restrict__ dstart,
+                             const uint32_t* __restrict__ wp, long long n, int* __restrict__ win_col,
+                             T* __restrict__ win_val) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int p = ix[i];
+        const int r = rowid[p], w = r / kWin;
+        const long long k = static_cast<long long>(excl[i]) + flag[i] - 1 - dstart[w];
+        const long long g0 = wp[w];
+        if (flag[i]) win_col[g0 * kWin + k] = col[p];
+        win_val[((g0 + k / kWin) * kWin + r % kWin) * kWin + k % kWin] = val[p];
     }
 }
 
@@ -375,4 +500,190 @@ spx_status spx_dev_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_
     spx_note_launches(launches);
     if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
     return e == cudaSuccess ? SPX_OK : SPX_ERR_CUDA;
+}
+
+spx_status spx_dev_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                             int32_t vb, int32_t br, int32_t bc, int32_t* bsr_row_ptr, int32_t* bsr_col,
+                             void* bsr_val, int64_t* nnzb_out, double* fill_out, cudaStream_t st) {
+    if (static_cast<long long>(br) * bc > kI32Max) return SPX_ERR_UNSUPPORTED;
+    Pool pool(st);
+    uint64_t launches = 0;
+    int32_t nnz32 = 0;
+    if (cudaMemcpyAsync(&nnz32, row_ptr + M, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SPX_ERR_CUDA;
+    const long long nnz = nnz32;
+    if (nnz < 0) return SPX_ERR_ARG;
+    if (nnz > 0 && (!col || (bsr_val && !val))) return SPX_ERR_ARG;
+    int* bad = pool.get<int>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    if (cudaMemsetAsync(bad, 0, sizeof(int), st) != cudaSuccess) return SPX_ERR_CUDA;
+    check_row_ptr<<<grid_for(M), kT, 0, st>>>(row_ptr, M, nnz, bad);
+    ++launches;
+    if (nnz > 0) {
+        check_indices<<<grid_for(nnz), kT, 0, st>>>(col, nnz, K, bad);
+        ++launches;
+    }
+    int h = 0;
+    spx_status s = read_flag(bad, st, &h);
+    if (s != SPX_OK) return s;
+    if (h & 4) return SPX_ERR_ARG;
+    if (h & 2) return SPX_ERR_NOT_SORTED;
+    if (h & 1) return SPX_ERR_INDEX_RANGE;
+    const long long MB = (static_cast<long long>(M) + br - 1) / br;
+    const long long KB = (static_cast<long long>(K) + bc - 1) / bc;
+    uint32_t *k = pool.get<uint32_t>(nnz), *k2 = pool.get<uint32_t>(nnz), *flag = pool.get<uint32_t>(nnz);
+    uint32_t* excl = pool.get<uint32_t>(nnz);
+    int *ix = pool.get<int>(nnz), *ix2 = pool.get<int>(nnz), *rowid = pool.get<int>(nnz);
+    uint32_t* cnt = pool.get<uint32_t>(MB + 1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    cudaError_t e = cudaSuccess;
+    long long nnzb = 0;
+    if (nnz > 0) {
+        expand_rows<<<grid_for(nnz), kT, 0, st>>>(row_ptr, M, nnz, rowid);
+        iota_keys<<<grid_for(nnz), kT, 0, st>>>(col, k, ix, nnz);  // ix = 0..nnz-1; the keys are set below
+        launches += 2;
+        // LSD over (block row, block column, place in the block): equal
+        // (row, col) pairs end up next to each other whatever the column
+        // order inside the CSR rows
+        const long long lim[3] = {static_cast<long long>(br) * bc, KB, MB};
+        for (int part = 0; part < 3 && e == cudaSuccess; ++part) {
+            if (bits_for(lim[part]) == 0) continue;  // a single key value: nothing to order
+            bsr_keys<<<grid_for(nnz), kT, 0, st>>>(rowid, col, ix, br, bc, part, k, nnz);
+            ++launches;
+            e = radix_sort(k, ix, k2, ix2, nnz, bits_for(lim[part]), pool, launches);
+        }
+        if (e == cudaSuccess) {
+            bsr_mark<<<grid_for(nnz), kT, 0, st>>>(ix, rowid, col, br, bc, nnz, flag, bad);
+            launches += 2;
+            e = scan_exclusive(flag, excl, nnz, pool);
+        }
+        uint32_t last[2] = {0, 0};
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&last[0], excl + nnz - 1, 4, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&last[1], flag + nnz - 1, 4, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&h, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return SPX_ERR_CUDA;
+        if (h & 8) return SPX_ERR_DUPLICATE;
+        nnzb = static_cast<long long>(last[0]) + last[1];
+        if (nnzb > kI32Max) return SPX_ERR_INDEX_RANGE;
+    }
+    if (bsr_row_ptr) {
+        e = cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * static_cast<size_t>(MB + 1), st);
+        if (e == cudaSuccess && nnz > 0) {
+            bsr_count<<<grid_for(nnz), kT, 0, st>>>(ix, rowid, flag, br, nnz, cnt);
+            ++launches;
+        }
+        if (e == cudaSuccess) e = scan_exclusive(cnt, reinterpret_cast<uint32_t*>(bsr_row_ptr), MB + 1, pool);
+    }
+    if (e == cudaSuccess && bsr_col && bsr_val && nnzb > 0) {
+        e = cudaMemsetAsync(bsr_val, 0, static_cast<size_t>(nnzb) * br * bc * vb, st);
+        const int g = grid_for(nnz);
+        if (e == cudaSuccess) {
+            switch (vb) {
+                case 1: bsr_scatter<uint8_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint8_t*>(val), flag, excl, br, bc, nnz, bsr_col, static_cast<uint8_t*>(bsr_val)); break;
+                case 2: bsr_scatter<uint16_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint16_t*>(val), flag, excl, br, bc, nnz, bsr_col, static_cast<uint16_t*>(bsr_val)); break;
+                case 4: bsr_scatter<uint32_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint32_t*>(val), flag, excl, br, bc, nnz, bsr_col, static_cast<uint32_t*>(bsr_val)); break;
+                default: bsr_scatter<uint64_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint64_t*>(val), flag, excl, br, bc, nnz, bsr_col, static_cast<uint64_t*>(bsr_val)); break;
+            }
+            ++launches;
+            e = cudaGetLastError();
+        }
+    }
+    spx_note_launches(launches);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the pool frees, and the caller's host sizes are final
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    if (nnzb_out) *nnzb_out = nnzb;
+    if (fill_out) *fill_out = nnzb ? static_cast<double>(nnz) / (static_cast<double>(nnzb) * br * bc) : 0.0;
+    return SPX_OK;
+}
+
+spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                              int32_t vb, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
+                              double* fill_out, cudaStream_t st) {
+    Pool pool(st);
+    uint64_t launches = 0;
+    int32_t nnz32 = 0;
+    if (cudaMemcpyAsync(&nnz32, row_ptr + M, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SPX_ERR_CUDA;
+    const long long nnz = nnz32;
+    if (nnz < 0) return SPX_ERR_INDEX_RANGE;
+    if (nnz > 0 && (!col || !val)) return SPX_ERR_ARG;
+    int* bad = pool.get<int>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    if (cudaMemsetAsync(bad, 0, sizeof(int), st) != cudaSuccess) return SPX_ERR_CUDA;
+    check_row_ptr<<<grid_for(M), kT, 0, st>>>(row_ptr, M, nnz, bad);
+    ++launches;
+    if (nnz > 0) {
+        check_indices<<<grid_for(nnz), kT, 0, st>>>(col, nnz, K, bad);
+        ++launches;
+    }
+    int h = 0;
+    spx_status s = read_flag(bad, st, &h);
+    if (s != SPX_OK) return s;
+    if (h & 4) return SPX_ERR_ARG;
+    if (h & 2) return SPX_ERR_NOT_SORTED;
+    if (h & 1) return SPX_ERR_INDEX_RANGE;
+    const long long W = (static_cast<long long>(M) + kWin - 1) / kWin;
+    uint32_t *k = pool.get<uint32_t>(nnz), *k2 = pool.get<uint32_t>(nnz), *flag = pool.get<uint32_t>(nnz);
+    uint32_t* excl = pool.get<uint32_t>(nnz);
+    int *ix = pool.get<int>(nnz), *ix2 = pool.get<int>(nnz), *rowid = pool.get<int>(nnz);
+    uint32_t *cnt = pool.get<uint32_t>(W + 1), *wp = pool.get<uint32_t>(W + 1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * static_cast<size_t>(W + 1), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(wp, 0, sizeof(uint32_t) * static_cast<size_t>(W + 1), st);
+    if (e == cudaSuccess && nnz > 0) {
+        expand_rows<<<grid_for(nnz), kT, 0, st>>>(row_ptr, M, nnz, rowid);
+        iota_keys<<<grid_for(nnz), kT, 0, st>>>(col, k, ix, nnz);  // ix = 0..nnz-1; the keys are set below
+        launches += 2;
+        // LSD over (window, column, row in the window)
+        const long long lim[3] = {kWin, K, W};
+        for (int part = 0; part < 3 && e == cudaSuccess; ++part) {
+            if (bits_for(lim[part]) == 0) continue;
+            wcsr_keys<<<grid_for(nnz), kT, 0, st>>>(rowid, col, ix, part, k, nnz);
+            ++launches;
+            e = radix_sort(k, ix, k2, ix2, nnz, bits_for(lim[part]), pool, launches);
+        }
+        if (e == cudaSuccess) {
+            wcsr_mark<<<grid_for(nnz), kT, 0, st>>>(ix, rowid, col, nnz, flag, cnt, bad);
+            wcsr_chunks<<<grid_for(W), kT, 0, st>>>(cnt, W, wp);
+            launches += 2;
+            e = scan_exclusive(flag, excl, nnz, pool);
+        }
+    }
+    // wp[0..W] = first chunk of each window (wp[W] = chunks); cnt -> first distinct index per window
+    if (e == cudaSuccess) e = scan_exclusive(wp, wp, W + 1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(cnt, cnt, W + 1, pool);
+    uint32_t total = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&total, wp + W, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    if (h & 8) return SPX_ERR_DUPLICATE;
+    const long long nch = total;
+    if (nch * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (win_ptr) e = cudaMemcpyAsync(win_ptr, wp, sizeof(uint32_t) * static_cast<size_t>(W + 1),
+                                     cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && win_col && win_val && nch > 0) {
+        e = cudaMemsetAsync(win_col, 0xFF, sizeof(int32_t) * static_cast<size_t>(nch) * kWin, st);  // -1 = padding
+        if (e == cudaSuccess) e = cudaMemsetAsync(win_val, 0, static_cast<size_t>(nch) * kWin * kWin * vb, st);
+        const int g = grid_for(nnz);
+        if (e == cudaSuccess && nnz > 0) {
+            switch (vb) {
+                case 1: wcsr_scatter<uint8_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint8_t*>(val), flag, excl, cnt, wp, nnz, win_col, static_cast<uint8_t*>(win_val)); break;
+                case 2: wcsr_scatter<uint16_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint16_t*>(val), flag, excl, cnt, wp, nnz, win_col, static_cast<uint16_t*>(win_val)); break;
+                case 4: wcsr_scatter<uint32_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint32_t*>(val), flag, excl, cnt, wp, nnz, win_col, static_cast<uint32_t*>(win_val)); break;
+                default: wcsr_scatter<uint64_t><<<g, kT, 0, st>>>(ix, rowid, col, static_cast<const uint64_t*>(val), flag, excl, cnt, wp, nnz, win_col, static_cast<uint64_t*>(win_val)); break;
+            }
+            ++launches;
+            e = cudaGetLastError();
+        }
+    }
+    spx_note_launches(launches);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    if (nchunks_out) *nchunks_out = nch;
+    if (fill_out) *fill_out = nch ? static_cast<double>(nnz) / (static_cast<double>(nch) * kWin * kWin) : 0.0;
+    return SPX_OK;
 }

@@ -321,34 +321,8 @@ spx_status spx_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int
                               bsr_col, static_cast<char*>(bsr_val), nnzb_out, fill_out);
     }
     if (where != SPX_DEVICE) return SPX_ERR_ARG;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    std::vector<int32_t> rp, c;
-    std::vector<char> v;
-    spx_status s = to_host(rp, row_ptr, static_cast<int64_t>(M) + 1, st);
-    if (s != SPX_OK) return s;
-    const int64_t nnz = rp[M];
-    if (nnz > 0 && (!col || !val)) return SPX_ERR_ARG;
-    s = to_host(c, col, nnz, st);
-    if (s == SPX_OK && bsr_val) s = to_host(v, static_cast<const char*>(val), nnz * val_bytes, st);
-    if (s != SPX_OK) return s;
-    const int64_t MB = (static_cast<int64_t>(M) + br - 1) / br;
-    std::vector<int32_t> brp(static_cast<size_t>(MB) + 1);
-    int64_t nb = 0;
-    double fill = 0.0;
-    s = build_bsr_host(M, K, rp.data(), c.data(), nullptr, val_bytes, br, bc, brp.data(), nullptr, nullptr, &nb,
-                       &fill);
-    if (s != SPX_OK) return s;
-    if (nnzb_out) *nnzb_out = nb;
-    if (fill_out) *fill_out = fill;
-    if (bsr_row_ptr) s = to_device(bsr_row_ptr, brp.data(), brp.size() * 4, st);
-    if (s != SPX_OK || !bsr_col) return s;
-    std::vector<int32_t> bcol(static_cast<size_t>(nb));
-    std::vector<char> bval(static_cast<size_t>(nb * br * bc * val_bytes));
-    s = build_bsr_host(M, K, rp.data(), c.data(), v.data(), val_bytes, br, bc, nullptr, bcol.data(), bval.data(),
-                       &nb, &fill);
-    if (s == SPX_OK) s = to_device(bsr_col, bcol.data(), bcol.size() * 4, st);
-    if (s == SPX_OK) s = to_device(bsr_val, bval.data(), bval.size(), st);
-    return s;
+    return spx_dev_build_bsr(M, K, row_ptr, col, val, val_bytes, br, bc, bsr_row_ptr, bsr_col, bsr_val, nnzb_out,
+                             fill_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 spx_status spx_check_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,

@@ -28,6 +28,14 @@ spx_status spx_dev_build_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* c
 spx_status spx_dev_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
                                  const void* val, int32_t val_bytes, int32_t* t_row_ptr, int32_t* t_col, void* t_val,
                                  spx_stream_t stream);
+// CSR -> BSR on the device (same two-call protocol and results as the host builder).
+spx_status spx_dev_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                             int32_t vb, int32_t br, int32_t bc, int32_t* bsr_row_ptr, int32_t* bsr_col,
+                             void* bsr_val, int64_t* nnzb_out, double* fill_out, cudaStream_t st);
+// CSR -> WCSR on the device (same two-call protocol and results as the host builder).
+spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
+                              int32_t vb, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
+                              double* fill_out, cudaStream_t st);
 
 struct spx_plan {
     int32_t M = 0, K = 0;

@@ -334,68 +334,14 @@ spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const in
     if (M < 0 || K < 0 || !row_ptr) return SPX_ERR_ARG;
     if (!(val_bytes == 1 || val_bytes == 2 || val_bytes == 4 || val_bytes == 8)) return SPX_ERR_ARG;
     if ((win_col == nullptr) != (win_val == nullptr)) return SPX_ERR_ARG;
-    const int64_t W = (static_cast<int64_t>(M) + kWin - 1) / kWin;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    std::vector<int32_t> rp_h, col_h, wp_h, wc_h;
-    std::vector<char> val_h, wv_h;
+    if (where == SPX_DEVICE)
+        return spx_dev_build_wcsr(M, K, row_ptr, col, val, val_bytes, win_ptr, win_col, win_val, nchunks_out, fill_out,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    if (where != SPX_HOST) return SPX_ERR_ARG;
+    if (row_ptr[M] > 0 && (!col || !val)) return SPX_ERR_ARG;
     try {
-        const int32_t* rp = row_ptr;
-        const int32_t* cl = col;
-        const char* vl = static_cast<const char*>(val);
-        if (where == SPX_DEVICE) {
-            rp_h.resize(static_cast<size_t>(M) + 1);
-            if (cudaMemcpyAsync(rp_h.data(), row_ptr, sizeof(int32_t) * rp_h.size(), cudaMemcpyDeviceToHost, st) !=
-                    cudaSuccess ||
-                cudaStreamSynchronize(st) != cudaSuccess)
-                return SPX_ERR_CUDA;
-            rp = rp_h.data();
-            const int64_t nnz = rp[M];
-            if (nnz < 0 || nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
-            if (nnz > 0 && (!col || !val)) return SPX_ERR_ARG;
-            col_h.resize(static_cast<size_t>(nnz));
-            val_h.resize(static_cast<size_t>(nnz) * val_bytes);
-            if (nnz && (cudaMemcpyAsync(col_h.data(), col, sizeof(int32_t) * col_h.size(), cudaMemcpyDeviceToHost,
-                                        st) != cudaSuccess ||
-                        cudaMemcpyAsync(val_h.data(), val, val_h.size(), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-                        cudaStreamSynchronize(st) != cudaSuccess))
-                return SPX_ERR_CUDA;
-            cl = col_h.data();
-            vl = val_h.data();
-        } else if (where != SPX_HOST) {
-            return SPX_ERR_ARG;
-        } else if (rp[M] > 0 && (!col || !val)) {
-            return SPX_ERR_ARG;
-        }
-        if (where == SPX_HOST) return build_wcsr_host(M, K, rp, cl, vl, val_bytes, win_ptr, win_col,
-                                                      static_cast<char*>(win_val), nchunks_out, fill_out);
-        // device outputs: build on the host, then copy out
-        int64_t nch = 0;
-        double fill = 0.0;
-        const bool full = win_col != nullptr;
-        if (full) {
-            spx_status s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, nullptr, nullptr, nullptr, &nch, nullptr);
-            if (s != SPX_OK) return s;
-            wp_h.resize(static_cast<size_t>(W) + 1);
-            wc_h.resize(static_cast<size_t>(nch) * kWin);
-            wv_h.resize(static_cast<size_t>(nch) * kWin * kWin * val_bytes);
-            s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, wp_h.data(), wc_h.data(), wv_h.data(), &nch, &fill);
-            if (s != SPX_OK) return s;
-        } else {
-            wp_h.resize(static_cast<size_t>(W) + 1);
-            spx_status s = build_wcsr_host(M, K, rp, cl, vl, val_bytes, wp_h.data(), nullptr, nullptr, &nch, &fill);
-            if (s != SPX_OK) return s;
-        }
-        cudaError_t e = cudaSuccess;
-        if (win_ptr) e = cudaMemcpyAsync(win_ptr, wp_h.data(), sizeof(int32_t) * wp_h.size(), cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess && full && nch) {
-            e = cudaMemcpyAsync(win_col, wc_h.data(), sizeof(int32_t) * wc_h.size(), cudaMemcpyHostToDevice, st);
-            if (e == cudaSuccess) e = cudaMemcpyAsync(win_val, wv_h.data(), wv_h.size(), cudaMemcpyHostToDevice, st);
-        }
-        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-        if (e != cudaSuccess) return SPX_ERR_CUDA;
-        if (nchunks_out) *nchunks_out = nch;
-        if (fill_out) *fill_out = fill;
-        return SPX_OK;
+        return build_wcsr_host(M, K, row_ptr, col, static_cast<const char*>(val), val_bytes, win_ptr, win_col,
+                               static_cast<char*>(win_val), nchunks_out, fill_out);
     } catch (const std::bad_alloc&) {
         return SPX_ERR_NOMEM;
     }

@@ -111,8 +111,15 @@ spx_status spx_transpose_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* r
  * Two calls: with bsr_col == NULL and bsr_val == NULL the call only fills
  * *nnzb_out, *fill_out and (if non-NULL) bsr_row_ptr[ceil(M/br)+1]; then the
  * caller allocates bsr_col[nnzb] and bsr_val[nnzb*br*bc*val_bytes].
- * Errors: SPX_ERR_DUPLICATE for a repeated (row, col); SPX_ERR_INDEX_RANGE.
- * where == SPX_DEVICE stages the arrays through host memory (synchronous).
+ * Errors: SPX_ERR_ARG (row_ptr[0] != 0), SPX_ERR_NOT_SORTED (row_ptr
+ * decreasing), SPX_ERR_INDEX_RANGE (a column outside [0, K), more than
+ * 2^31-1 blocks), SPX_ERR_DUPLICATE for a repeated (row, col).
+ * where == SPX_DEVICE builds on the GPU (device arrays in and out; stable
+ * radix sort of the entries by block row, block column and place in the
+ * block; temporary memory from the stream-ordered allocator) with the same
+ * results as the host build; it synchronises the stream before returning and
+ * returns SPX_ERR_UNSUPPORTED when br * bc exceeds 2^31-1.  With several
+ * errors at once the device path reports the structural ones first.
  */
 spx_status spx_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
                          int32_t val_bytes, int32_t br, int32_t bc, int32_t* bsr_row_ptr, int32_t* bsr_col,
@@ -522,9 +529,12 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
  *           beyond M in the last window).
  * fill = nnz / (nchunks * 4096).  Two calls: with win_col == win_val == NULL
  * only *nchunks_out (and win_ptr, when given) is produced.  Arrays are all
- * host or all device per `where` (device inputs are staged through host
- * memory).  Errors: SPX_ERR_DUPLICATE (a repeated (row, col)),
- * SPX_ERR_INDEX_RANGE, SPX_ERR_NOT_SORTED.
+ * host or all device per `where`.  where == SPX_DEVICE builds on the GPU
+ * (stable radix sort of the entries by window, column and row in the window;
+ * temporary memory from the stream-ordered allocator) with the same results
+ * as the host build, and synchronises the stream before returning.
+ * Errors: SPX_ERR_ARG (row_ptr[0] != 0), SPX_ERR_DUPLICATE (a repeated
+ * (row, col)), SPX_ERR_INDEX_RANGE, SPX_ERR_NOT_SORTED (row_ptr decreasing).
  */
 spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
                           int32_t val_bytes, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,

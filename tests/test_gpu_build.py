@@ -92,3 +92,103 @@ def test_power_law_full_size_device_build():
     gt = spx.spx_transpose_csr(M, K, *got)
     for w, g in zip(wt, gt):
         assert np.array_equal(w, host(g))
+
+
+def _shuffle_within_rows(seed, rp, col, val):
+    """Same matrix, columns no longer ascending inside each row."""
+    key = synth.uniform(seed, 9, col.size, 0.0, 1.0)
+    rows = np.repeat(np.arange(rp.size - 1), np.diff(rp))
+    order = np.lexsort((key, rows))
+    return col[order], val[order]
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax,br,bc", [(1, 1, 0, 1, 1, 1), (7, 5, 0, 5, 2, 3), (1000, 777, 0, 40, 16, 16),
+                                                 (300, 90000, 0, 300, 64, 64), (4097, 5000, 1, 12, 128, 8),
+                                                 (50, 50, 0, 0, 4, 4), (2000, 3000, 0, 30, 1, 64),
+                                                 (2000, 3000, 0, 30, 33, 1)])
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16, np.float64])
+def test_build_bsr_device_equals_oracle(M, K, lmin, lmax, br, bc, dtype):
+    d = synth.random_coo(105 + M + br, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    v = val.astype(dtype) if dtype is not np.uint16 else synth.to_bf16_bits(val)
+    want = oracle.build_bsr(M, K, rp, col, v, br, bc)
+    got = spx.spx_build_bsr(M, K, cuda(rp), cuda(col), cuda(v), br, bc)
+    assert got[3] == want[3]
+    for w, g in zip(want[:3], got[:3]):
+        assert np.array_equal(w, host(g))
+    # columns out of order inside the rows: same blocks
+    c2, v2 = _shuffle_within_rows(106 + M, rp, col, v)
+    got2 = spx.spx_build_bsr(M, K, cuda(rp), cuda(c2), cuda(v2), br, bc)
+    for w, g in zip(want[:3], got2[:3]):
+        assert np.array_equal(w, host(g))
+
+
+def test_build_bsr_device_block_sparse_workload():
+    """The tensor-core workload's shape (16,384^2, 64 x 64 blocks, 26 per block-row), bf16 bits."""
+    c = synth.block_sparse()
+    M, K, bs = c["M"], c["K"], c["bs"]
+    rp, col, val = oracle.build_csr(M, K, c["row"], c["col"], c["val_bf16"])
+    want = oracle.build_bsr(M, K, rp, col, val, bs, bs)
+    got = spx.spx_build_bsr(M, K, cuda(rp), cuda(col), cuda(val), bs, bs)
+    assert got[3] == want[3] == 1.0
+    for w, g in zip(want[:3], got[:3]):
+        assert np.array_equal(w, host(g))
+
+
+def test_build_bsr_device_rejects_bad_input():
+    one = cuda(np.ones(3, np.float32))
+    rp = cuda(np.array([0, 2, 3], np.int32))
+    cases = [(cuda(np.array([0, 0, 1], np.int32)), rp, -4),                       # (0, 0) twice
+             (cuda(np.array([1, 0, 1], np.int32)), cuda(np.array([0, 3, 3], np.int32)), -4),  # not adjacent
+             (cuda(np.array([0, 4, 1], np.int32)), rp, -2),                       # col 4 >= K
+             (cuda(np.array([0, 1, 1], np.int32)), cuda(np.array([0, 3, 2], np.int32)), -3),  # row_ptr decreasing
+             (cuda(np.array([0, 1, 1], np.int32)), cuda(np.array([1, 2, 3], np.int32)), -1)]  # row_ptr[0] != 0
+    for c, r, code in cases:
+        with pytest.raises(spx.SpxError) as e:
+            spx.spx_build_bsr(2, 4, r, c, one, 2, 2)
+        assert e.value.code == code
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 1), (7, 5, 0, 5), (1000, 777, 0, 40), (300, 90000, 0, 300),
+                                          (4097, 200, 1, 120), (50, 50, 0, 0), (64, 64, 64, 64), (130, 70, 0, 70)])
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16, np.float64, np.uint8])
+def test_build_wcsr_device_equals_oracle(M, K, lmin, lmax, dtype):
+    d = synth.random_coo(107 + M + K, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    v = synth.to_bf16_bits(val) if dtype is np.uint16 else (
+        (np.abs(val) * 250).astype(dtype) if dtype is np.uint8 else val.astype(dtype))
+    want = oracle.build_wcsr(M, K, rp, col, v)
+    got = spx.spx_build_wcsr(M, K, cuda(rp), cuda(col), cuda(v))
+    assert got[3] == want[3]
+    for w, g in zip(want[:3], got[:3]):
+        assert np.array_equal(w, host(g))
+    c2, v2 = _shuffle_within_rows(108 + M, rp, col, v)
+    got2 = spx.spx_build_wcsr(M, K, cuda(rp), cuda(c2), cuda(v2))
+    for w, g in zip(want[:3], got2[:3]):
+        assert np.array_equal(w, host(g))
+
+
+def test_build_wcsr_device_window_pool_workload():
+    """The WCSR workload's shape (16,384 rows, 64-row windows over a 512-column pool each)."""
+    c = synth.window_pool()
+    M, K = c["M"], c["K"]
+    rp, col, val = oracle.build_csr(M, K, c["row"], c["col"], c["val_bf16"])
+    want = oracle.build_wcsr(M, K, rp, col, val)
+    got = spx.spx_build_wcsr(M, K, cuda(rp), cuda(col), cuda(val))
+    assert got[3] == want[3]
+    for w, g in zip(want[:3], got[:3]):
+        assert np.array_equal(w, host(g))
+
+
+def test_build_wcsr_device_rejects_bad_input():
+    one = cuda(np.ones(3, np.float32))
+    rp = cuda(np.array([0, 2, 3], np.int32))
+    cases = [(cuda(np.array([1, 1, 0], np.int32)), rp, -4),                       # (0, 1) twice
+             (cuda(np.array([1, 0, 1], np.int32)), cuda(np.array([0, 3, 3], np.int32)), -4),  # not adjacent
+             (cuda(np.array([1, 4, 0], np.int32)), rp, -2),                       # col 4 >= K
+             (cuda(np.array([1, 2, 0], np.int32)), cuda(np.array([0, 3, 2], np.int32)), -3),  # row_ptr decreasing
+             (cuda(np.array([1, 2, 0], np.int32)), cuda(np.array([1, 2, 3], np.int32)), -1)]  # row_ptr[0] != 0
+    for c, r, code in cases:
+        with pytest.raises(spx.SpxError) as e:
+            spx.spx_build_wcsr(2, 4, r, c, one)
+        assert e.value.code == code
