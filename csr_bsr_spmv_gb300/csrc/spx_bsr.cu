@@ -477,25 +477,22 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     // (S = 2..5; smaller rings fit more CTAs per SM), "wideS" = the same with
     // 256-column tiles (S = 2..4, N a multiple of 256), "persistent" = the
     // persistent 256-column kernel.  SPX_BSR_VARIANT overrides the default.
-    static int variant = -1;
-    if (variant < 0) {
-        variant = 3;
-        if (const char* v = std::getenv("SPX_BSR_VARIANT")) {
-            if (!std::strcmp(v, "persistent")) variant = 0;
-            else if (!std::strncmp(v, "tile", 4) && v[4] >= '2' && v[4] <= '5' && v[5] == 0) variant = v[4] - '0';
-            else if (!std::strncmp(v, "wide", 4) && v[4] >= '2' && v[4] <= '4' && v[5] == 0) variant = 10 + v[4] - '0';
+    static const int env_variant = [] {  // read once, thread-safe
+        int v = 3;
+        if (const char* e = std::getenv("SPX_BSR_VARIANT")) {
+            if (!std::strcmp(e, "persistent")) v = 0;
+            else if (!std::strncmp(e, "tile", 4) && e[4] >= '2' && e[4] <= '5' && e[5] == 0) v = e[4] - '0';
+            else if (!std::strncmp(e, "wide", 4) && e[4] >= '2' && e[4] <= '4' && e[5] == 0) v = 10 + e[4] - '0';
         }
-    }
-    if (variant >= 10 && N % 256) variant = 3;
+        return v;
+    }();
+    const int variant = env_variant >= 10 && N % 256 ? 3 : env_variant;  // per call: 256-column tiles need N % 256 == 0
     cudaError_t e = cudaSuccess;
     if (variant == 0) {
         if (set_smem_limit(bsr_spmm_tc_kernel, kSmemBytes) != cudaSuccess) return SPX_ERR_CUDA;
-        static int nsm = 0;
-        if (nsm == 0) {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                return SPX_ERR_CUDA;
-        }
+        int dev = 0, nsm = 0;  // SM count of the current device (cheap attribute query)
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPX_ERR_CUDA;
         const int ntq = (N + kTileN - 1) / kTileN;
         const long long tiles = static_cast<long long>(M / kBlk) * ntq;
         if (tiles > kI32Max) return SPX_ERR_INDEX_RANGE;

@@ -373,16 +373,16 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
     // Variant: 128-column tiles with a 2-deep ring (default: four CTAs per SM,
     // measured fastest), "s3" / "s4" deeper rings, "wide" 256-column tiles
     // with a 2-deep ring (N a multiple of 256); SPX_WCSR_VARIANT overrides.
-    static int variant = -1;
-    if (variant < 0) {
-        variant = 2;
-        if (const char* v = std::getenv("SPX_WCSR_VARIANT")) {
-            if (!std::strcmp(v, "wide")) variant = 1;
-            else if (!std::strcmp(v, "s3")) variant = 3;
-            else if (!std::strcmp(v, "s4")) variant = 4;
+    static const int env_variant = [] {  // read once, thread-safe
+        int v = 2;
+        if (const char* e = std::getenv("SPX_WCSR_VARIANT")) {
+            if (!std::strcmp(e, "wide")) v = 1;
+            else if (!std::strcmp(e, "s3")) v = 3;
+            else if (!std::strcmp(e, "s4")) v = 4;
         }
-    }
-    if (variant == 1 && N % 256) variant = 2;
+        return v;
+    }();
+    const int variant = env_variant == 1 && N % 256 ? 2 : env_variant;  // per call: 256-column tiles need N % 256 == 0
     switch (variant) {
 #define SPX_WCSR(S, H, V)                                                                                      \
     case V: {                                                                                                  \
