@@ -149,13 +149,25 @@ def _check(rc: int, where: str):
 
 
 def _ptr(t):
+    """Address of an array's first element.  The library reads arrays densely,
+    except the rows of 2-D operands, whose leading dimension is passed apart:
+    anything else (a transposed or sliced view) is rejected, not copied."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
+        if t.numel() and not (t.is_contiguous() or (t.dim() == 2 and t.stride(1) == 1)):
+            raise ValueError(f"array with strides {tuple(t.stride())} is not laid out densely")
         return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
     if isinstance(t, np.ndarray):
+        if t.size and not (t.flags.c_contiguous or (t.ndim == 2 and t.strides[1] == t.itemsize)):
+            raise ValueError(f"array with strides {t.strides} is not laid out densely")
         return t.ctypes.data_as(ctypes.c_void_p) if t.size else None
     raise TypeError(type(t))
+
+
+def _require(cond: bool, what: str):
+    if not cond:
+        raise ValueError(what)
 
 
 def _stream(stream=None):
@@ -278,7 +290,8 @@ def spx_spmm_wcsr(M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor, 
                   B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
     """C <- alpha*A*B + beta*C, A in WCSR (bf16 bit patterns), B bf16 (K x N), C fp32 (M x N)."""
     N = B.shape[1]
-    assert B.stride(1) == 1 and C.stride(1) == 1
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
     nch = win_col.numel() // 64
     _check(_lib().spx_spmm_wcsr(M, K, nch, _ptr(win_ptr), _ptr(win_col), _ptr(win_val), N, _ptr(B), B.stride(0),
                                 float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)), "spx_spmm_wcsr")
@@ -494,9 +507,10 @@ def spx_spmv_csr_hostio(plan: Plan, A: Csr, x_host: torch.Tensor, y_host: torch.
                         beta: float = 0.0, work: torch.Tensor | None = None, stream=None):
     """y_host[b] <- alpha*A*x_host[b] + beta*y_host[b] for every row b of the (batch x K) / (batch x M)
     host tensors (pinned for full speed); copies pipelined against the products.  Synchronises."""
-    assert not x_host.is_cuda and not y_host.is_cuda and x_host.dim() == 2 and y_host.dim() == 2
-    assert x_host.stride(1) == 1 and y_host.stride(1) == 1
-    assert x_host.shape[0] in (1, y_host.shape[0])  # one x for every batch, or one per batch
+    _require(not x_host.is_cuda and not y_host.is_cuda and x_host.dim() == 2 and y_host.dim() == 2,
+             "x_host and y_host must be 2-D host tensors")
+    _require(x_host.stride(1) == 1 and y_host.stride(1) == 1, "x_host and y_host need unit column stride")
+    _require(x_host.shape[0] in (1, y_host.shape[0]), "x_host needs one row, or one row per batch")
     need = int(_lib().spx_spmv_csr_hostio_work_bytes(A.M, A.K))
     if work is None:
         work = torch.empty(max(1, need // 4), dtype=torch.float32, device=plan.table.device)
@@ -545,7 +559,8 @@ def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, b
     """C <- alpha*A*B + beta*C; B (K x N) and C (M x N) row-major views (stride(1) == 1).
     col_tile: None = automatic (spx_spmm_csr), else spx_spmm_csr_tiled's column tile."""
     N = B.shape[1]
-    assert B.stride(1) == 1 and C.stride(1) == 1
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
     lib = _lib()
     args = (A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B), B.stride(0), float(alpha),
             float(beta), _ptr(C), C.stride(0))
@@ -559,7 +574,9 @@ def spx_spmm_csr(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, b
 def spx_spmm_csr_bf16(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
     """C <- alpha*A*B + beta*C with A.val and B holding bf16 bit patterns (int16 tensors), C fp32."""
     N = B.shape[1]
-    assert B.stride(1) == 1 and C.stride(1) == 1 and A.val.element_size() == 2 and B.element_size() == 2
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
+    _require(A.val.element_size() == 2 and B.element_size() == 2, "A values and B must be 16-bit (bf16 bit patterns)")
     _check(_lib().spx_spmm_csr_bf16(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
                                     B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
            "spx_spmm_csr_bf16")

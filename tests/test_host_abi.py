@@ -365,3 +365,17 @@ def test_hostio_rejects_bad_arguments_without_launching():
                                    None) == -10  # x broadcast is fine; the plan was never uploaded
     assert lib.spx_spmv_csr_hostio(p.handle, 2, 3, 2, a, a, a, 1.0, a, 3, 0.0, a, 2, 0, w, need, None, 0, None) == 0
     assert spx.launch_count() == before
+
+
+def test_binding_rejects_strided_views():
+    """The binding hands raw addresses to the library, so a view whose elements
+    are not dense (a strided slice, a transpose) is refused instead of misread."""
+    row = np.array([0, 1, 1, 2, 0, 2], np.int32)
+    col = np.array([0, 0, 1, 1, 2, 2], np.int32)
+    val = np.ones(12, np.float32)
+    with pytest.raises(ValueError):
+        spx.spx_build_csr(3, 3, row, col, val[::2])
+    with pytest.raises(ValueError):
+        spx.spx_build_csr(3, 3, row, col, np.ones((2, 3), np.float32).T)
+    rp, c, v = spx.spx_build_csr(3, 3, row, col, np.ascontiguousarray(val[::2]))  # a dense copy is fine
+    assert rp.tolist() == [0, 2, 4, 6]
