@@ -254,6 +254,7 @@ def run_ours(args, rank, world):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         dr, dc, dv = to_dev(c["row"]), to_dev(c["col"]), to_dev(c["val"])
         device_timing("build_csr_device_ms", lambda: spx.spx_build_csr(M, K, dr, dc, dv, stream=stream))
+        device_timing("row_stats_device_ms", lambda: spx.spx_row_stats(M, A.row_ptr))
         del dr, dc, dv
         x = to_dev(c["x"])
         y = to_dev(c["y"])

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <vector>
 
 #include "spx_internal.h"
@@ -313,6 +314,41 @@ __global__ void wcsr_scatter(const int* __restrict__ ix, const int* __restrict__
         const long long g0 = wp[w];
         if (flag[i]) win_col[g0 * kWin + k] = col[p];
         win_val[((g0 + k / kWin) * kWin + r % kWin) * kWin + k % kWin] = val[p];
+    }
+}
+
+// Row statistics: len[i] = row_ptr[i+1] - row_ptr[i] (sort keys for the
+// percentiles) and, per CTA, the sums S1, S2, min, max and empty rows, folded
+// into acc64 = {S1, S2} and acc32 = {min, max, empty} with integer atomics
+// (exact, so the order does not matter).
+__global__ void __launch_bounds__(kT) row_len_stats(const int* __restrict__ rp, int M, uint32_t* __restrict__ len,
+                                                    unsigned long long* __restrict__ acc64, int* __restrict__ acc32) {
+    long long s1 = 0, s2 = 0;
+    int mn = 0x7fffffff, mx = -0x7fffffff - 1, emp = 0;
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int l = rp[i + 1] - rp[i];
+        len[i] = static_cast<uint32_t>(l);
+        s1 += l;
+        s2 += static_cast<long long>(l) * l;
+        mn = min(mn, l);
+        mx = max(mx, l);
+        emp += l == 0;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        s1 += __shfl_down_sync(0xffffffffu, s1, d);
+        s2 += __shfl_down_sync(0xffffffffu, s2, d);
+        mn = min(mn, __shfl_down_sync(0xffffffffu, mn, d));
+        mx = max(mx, __shfl_down_sync(0xffffffffu, mx, d));
+        emp += __shfl_down_sync(0xffffffffu, emp, d);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&acc64[0], static_cast<unsigned long long>(s1));
+        atomicAdd(&acc64[1], static_cast<unsigned long long>(s2));
+        atomicMin(&acc32[0], mn);
+        atomicMax(&acc32[1], mx);
+        atomicAdd(&acc32[2], emp);
     }
 }
 
@@ -685,5 +721,54 @@ spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, cons
     if (e != cudaSuccess) return SPX_ERR_CUDA;
     if (nchunks_out) *nchunks_out = nch;
     if (fill_out) *fill_out = nch ? static_cast<double>(nnz) / (static_cast<double>(nch) * kWin * kWin) : 0.0;
+    return SPX_OK;
+}
+
+spx_status spx_dev_row_stats(int32_t M, const int32_t* row_ptr, spx_row_stats_t* out, cudaStream_t st) {
+    std::memset(out, 0, sizeof(*out));
+    out->rows = M;
+    if (M == 0) return SPX_OK;
+    Pool pool(st);
+    uint64_t launches = 0;
+    unsigned long long* acc64 = pool.get<unsigned long long>(2);
+    int* acc32 = pool.get<int>(3);
+    uint32_t *k = pool.get<uint32_t>(M), *k2 = pool.get<uint32_t>(M);
+    int *ix = pool.get<int>(M), *ix2 = pool.get<int>(M);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    const int init32[3] = {0x7fffffff, -0x7fffffff - 1, 0};
+    unsigned long long h64[2] = {0, 0};
+    int h32[3] = {0, 0, 0};
+    cudaError_t e = cudaMemsetAsync(acc64, 0, 2 * sizeof(unsigned long long), st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(acc32, init32, sizeof(init32), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ix, 0, sizeof(int) * static_cast<size_t>(M), st);  // payload unused
+    if (e == cudaSuccess) {
+        row_len_stats<<<grid_for(M), kT, 0, st>>>(row_ptr, M, k, acc64, acc32);
+        ++launches;
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h64, acc64, sizeof(h64), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h32, acc32, sizeof(h32), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    // nearest-rank percentiles: the ceil(q*M/100)-th smallest length of the sorted lengths
+    const int hi = h32[1] < 0 ? 32 : bits_for(static_cast<long long>(h32[1]) + 1);
+    e = radix_sort(k, ix, k2, ix2, M, hi, pool, launches);
+    const long long rank[3] = {(50LL * M + 99) / 100, (95LL * M + 99) / 100, (99LL * M + 99) / 100};
+    uint32_t q[3] = {0, 0, 0};
+    for (int j = 0; j < 3 && e == cudaSuccess; ++j)
+        e = cudaMemcpyAsync(&q[j], k + rank[j] - 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    spx_note_launches(launches);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    const int64_t s1 = static_cast<int64_t>(h64[0]), s2 = static_cast<int64_t>(h64[1]);
+    out->nnz = s1;
+    out->sumsq = s2;
+    out->min = h32[0];
+    out->max = h32[1];
+    out->empty = h32[2];
+    out->p50 = static_cast<int32_t>(q[0]);
+    out->p95 = static_cast<int32_t>(q[1]);
+    out->p99 = static_cast<int32_t>(q[2]);
+    spx_row_stats_finish(M, out);
     return SPX_OK;
 }

@@ -13,6 +13,16 @@
 
 #include "spx_internal.h"
 
+// mean, population variance and cv from the exact sums (one definition for
+// the host and the device statistics, so both give the same doubles)
+void spx_row_stats_finish(int32_t M, spx_row_stats_t* out) {
+    const int64_t s1 = out->nnz, s2 = out->sumsq;
+    out->mean = static_cast<double>(s1) / static_cast<double>(M);
+    __int128 num = static_cast<__int128>(M) * s2 - static_cast<__int128>(s1) * s1;
+    out->var = static_cast<double>(num) / (static_cast<double>(M) * static_cast<double>(M));
+    out->cv = out->mean > 0.0 ? std::sqrt(out->var) / out->mean : 0.0;
+}
+
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
@@ -179,10 +189,7 @@ void row_stats_host(int32_t M, const int32_t* rp, spx_row_stats_t* out) {
     out->p99 = kth((99LL * M + 99) / 100);
     out->min = *std::min_element(len.begin(), len.end());
     out->max = *std::max_element(len.begin(), len.end());
-    out->mean = static_cast<double>(s1) / static_cast<double>(M);
-    __int128 num = static_cast<__int128>(M) * s2 - static_cast<__int128>(s1) * s1;
-    out->var = static_cast<double>(num) / (static_cast<double>(M) * static_cast<double>(M));
-    out->cv = out->mean > 0.0 ? std::sqrt(out->var) / out->mean : 0.0;
+    spx_row_stats_finish(M, out);
 }
 
 // ------------------------------------------------------------ the plan
@@ -362,10 +369,7 @@ spx_status spx_row_stats(int32_t M, const int32_t* row_ptr, spx_loc where, spx_r
         return SPX_OK;
     }
     if (where != SPX_DEVICE) return SPX_ERR_ARG;
-    std::vector<int32_t> rp;
-    spx_status s = to_host(rp, row_ptr, static_cast<int64_t>(M) + 1, nullptr);
-    if (s == SPX_OK) row_stats_host(M, rp.data(), out);
-    return s;
+    return spx_dev_row_stats(M, row_ptr, out, nullptr);
 }
 
 spx_status spx_plan_opts_default(spx_plan_opts_t* o) {

@@ -36,6 +36,11 @@ spx_status spx_dev_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const
 spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
                               int32_t vb, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
                               double* fill_out, cudaStream_t st);
+// Row statistics of a device row_ptr (lengths, sums and extremes in one
+// kernel, percentiles from a radix sort of the lengths); synchronous.
+spx_status spx_dev_row_stats(int32_t M, const int32_t* row_ptr, spx_row_stats_t* out, cudaStream_t st);
+// mean, variance and cv from out->nnz and out->sumsq (shared by both paths).
+void spx_row_stats_finish(int32_t M, spx_row_stats_t* out);
 
 struct spx_plan {
     int32_t M = 0, K = 0;

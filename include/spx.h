@@ -153,6 +153,11 @@ typedef struct spx_row_stats_t {
  * Row-length statistics of a CSR.  [LSMR-dual] §5.3 (l_i = row_ptr[i+1] -
  * row_ptr[i]; mean, variance and long tail) and [SpMM-ops] §4 (avg/p95/max
  * and coefficient of variation in the dispatch key).
+ * where == SPX_DEVICE computes them on the GPU: one kernel forms the lengths
+ * and folds S1, S2, min, max and the empty rows with integer atomics (exact),
+ * and a radix sort of the lengths gives the percentiles.  It runs on the
+ * default stream, returns when done, and gives the same numbers as the host
+ * path bit for bit (the doubles come from the same integer sums).
  */
 spx_status spx_row_stats(int32_t M, const int32_t* row_ptr, spx_loc where, spx_row_stats_t* out);
 

@@ -192,3 +192,27 @@ def test_build_wcsr_device_rejects_bad_input():
         with pytest.raises(spx.SpxError) as e:
             spx.spx_build_wcsr(2, 4, r, c, one)
         assert e.value.code == code
+
+
+@pytest.mark.parametrize("M,lmin,lmax", [(1, 0, 0), (1, 5, 5), (7, 0, 5), (1000, 0, 40), (4097, 1, 3000),
+                                         (300000, 0, 12), (50, 0, 0)])
+def test_row_stats_device_equals_host(M, lmin, lmax):
+    lengths = synth.lengths_uniform(109 + M, M, lmin, lmax)
+    rp = np.zeros(M + 1, np.int32)
+    rp[1:] = np.cumsum(lengths)
+    want = spx.spx_row_stats(M, rp)
+    got = spx.spx_row_stats(M, cuda(rp))
+    assert got == want
+
+
+def test_row_stats_device_power_law():
+    """4,194,304 rows, lengths from 1 to ~10^5: every field equals the host's, and the percentiles the sorted lengths'."""
+    M = 4_194_304
+    lengths, _ = synth.lengths_zipf(2, M, 2.1, 200_000, 16.0)  # the power-law workload's row lengths
+    rp = np.zeros(M + 1, np.int32)
+    rp[1:] = np.cumsum(lengths)
+    got = spx.spx_row_stats(M, cuda(rp))
+    assert got == spx.spx_row_stats(M, rp)
+    srt = np.sort(lengths)
+    assert [got["p50"], got["p95"], got["p99"]] == [int(srt[(q * M + 99) // 100 - 1]) for q in (50, 95, 99)]
+    assert got["max"] == int(srt[-1]) and got["min"] == int(srt[0])
