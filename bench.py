@@ -266,6 +266,7 @@ def run_ours(args, rank, world):
         t0 = time.perf_counter()
         plan = spx.spx_plan_csr(M, K, A.nnz, rp, opts=opts, device=dev, stream=stream)
         timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
+        device_timing("plan_device_ms", lambda: spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, opts=opts, stream=stream))
         alpha, beta = c["alpha"], c["beta"]
         src = source_hash("spx_spmv.cu")
 

@@ -29,6 +29,8 @@
 
 #include <cstdint>
 #include <cstring>
+#include <new>
+#include <utility>
 #include <vector>
 
 #include "spx_internal.h"
@@ -349,6 +351,150 @@ __global__ void __launch_bounds__(kT) row_len_stats(const int* __restrict__ rp, 
         atomicMin(&acc32[0], mn);
         atomicMax(&acc32[1], mx);
         atomicAdd(&acc32[2], emp);
+    }
+}
+
+// ---------------------------------------------------------------- dispatch plan
+// The plan of [SpMM-ops] §2.1-§2.4 built on the GPU, equal to the host
+// builder's task for task.  Rows longer than pack_max are CTA rows (one task)
+// or split rows (ceil(l / seg_nnz) segment tasks and partial-sum slots); the
+// other rows are packed left to right into groups: a group starting at a short
+// row s takes rows s .. e(s)-1, e(s) being the largest row end with at most
+// block_rows rows, at most block_nnz nonzeros and no long row.  The groups are
+// the chain run start, e(run start), e(e(run start)), ... of each run of short
+// rows.  e is monotone, so the chain is marked by doubling: after round k
+// every e^t(start) with t < 2^(k+1) is marked, and the rounds stop once e^(2^k)
+// is a fixed point everywhere.
+
+// per row: kind (0 short, 1 CTA row, 2 split row), long-row tasks, slots, flags
+__global__ void plan_classify(const int* __restrict__ rp, int M, int pack_max, int cta_max, int seg_nnz,
+                              uint32_t* __restrict__ ntl, uint32_t* __restrict__ nsl, uint32_t* __restrict__ fl,
+                              uint32_t* __restrict__ fs, uint32_t* __restrict__ fshort) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const long long l = static_cast<long long>(rp[i + 1]) - rp[i];
+        const int kind = l > pack_max ? (l <= cta_max ? 1 : 2) : 0;
+        const uint32_t ns = kind == 2 ? static_cast<uint32_t>((l + seg_nnz - 1) / seg_nnz) : 0u;
+        ntl[i] = kind == 1 ? 1u : ns;
+        nsl[i] = ns;
+        fl[i] = kind != 0;
+        fs[i] = kind == 2;
+        fshort[i] = kind == 0;
+    }
+}
+
+// L[lidx[i]] = i for every long row (ascending)
+__global__ void plan_compact(const uint32_t* __restrict__ fl, const uint32_t* __restrict__ lidx, int M,
+                             int* __restrict__ L) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT)
+        if (fl[i]) L[lidx[i]] = static_cast<int>(i);
+}
+
+// E0[s] = e(s) for short rows, s itself for long rows and for s = M; on[s] = 1 at run starts
+__global__ void plan_group_end(const int* __restrict__ rp, int M, const uint32_t* __restrict__ fl,
+                               const int* __restrict__ L, int nL, int block_nnz, int block_rows, int* __restrict__ E0,
+                               uint32_t* __restrict__ on) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i <= M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int s = static_cast<int>(i);
+        if (s == M || fl[s]) {
+            E0[s] = s;
+            on[s] = 0;
+            continue;
+        }
+        int lo = 0, hi = nL;  // first long row after s
+        while (lo < hi) {
+            const int mid = lo + (hi - lo) / 2;
+            if (L[mid] > s) hi = mid; else lo = mid + 1;
+        }
+        const int run_end = lo < nL ? L[lo] : M;
+        const int lim = static_cast<int>(min(static_cast<long long>(run_end), static_cast<long long>(s) + block_rows));
+        const int base = rp[s];
+        int a = s + 1, b = lim;  // largest j in [s+1, lim] with rp[j] - rp[s] <= block_nnz (j = s+1 always fits)
+        while (a < b) {
+            const int mid = a + (b - a + 1) / 2;
+            if (rp[mid] - base <= block_nnz) a = mid; else b = mid - 1;
+        }
+        E0[s] = a;
+        on[s] = (s == 0 || fl[s - 1]) ? 1u : 0u;
+    }
+}
+
+// one doubling round: mark E(s) for every marked s, then E2 = E o E (changed when any entry moved)
+__global__ void plan_mark(const int* __restrict__ E, uint32_t* on, int M) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT)
+        if (on[i]) {
+            const int t = E[i];
+            if (t < M) on[t] = 1u;
+        }
+}
+
+__global__ void plan_compose(const int* __restrict__ E, int* __restrict__ E2, int M, int* __restrict__ changed) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i <= M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int a = E[i];
+        const int b = E[a];
+        E2[i] = b;
+        if (b != a) *changed = 1;
+    }
+}
+
+// group starts = marked short rows
+__global__ void plan_starts(const uint32_t* __restrict__ on, const uint32_t* __restrict__ fshort, int M,
+                            uint32_t* __restrict__ gs) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT)
+        gs[i] = on[i] & fshort[i];
+}
+
+__device__ __forceinline__ int plan_reduce_code(long long nnz_g, long long rows_g, int div) {
+    if (div == 0) return kReduceSegmented;
+    const long long per = (nnz_g + rows_g * div - 1) / (rows_g * div);
+    int lg = 0;
+    while (lg < 5 && (1ll << lg) < per) ++lg;
+    return lg;
+}
+
+__device__ __forceinline__ void put4(int* d, long long pos, int a, int b, int c, int e) {
+    reinterpret_cast<int4*>(d)[pos] = make_int4(a, b, c, e);
+}
+
+// Writes every task in both forms (host form: the documented one; device form:
+// kind | code << 2 | aux << 8, row, p0, p1) and the split-row table; counts the
+// groups by reduction code (cnt[0] thread groups, [1] lane groups, [2] segmented).
+__global__ void plan_write(const int* __restrict__ rp, int M, int seg_nnz, int lanes_div,
+                           const uint32_t* __restrict__ nsl,
+                           const uint32_t* __restrict__ fl, const uint32_t* __restrict__ fs,
+                           const uint32_t* __restrict__ toff, const uint32_t* __restrict__ soff,
+                           const uint32_t* __restrict__ sidx, const uint32_t* __restrict__ gsf,
+                           const uint32_t* __restrict__ gidx, const int* __restrict__ E0, long long nlongtasks,
+                           int* __restrict__ htask, int* __restrict__ dtask, int* __restrict__ longrows,
+                           unsigned long long* __restrict__ cnt) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int r = static_cast<int>(i);
+        if (fl[r] && !fs[r]) {  // CTA row
+            put4(htask, toff[r], kTaskCta, r, 0, 0);
+            put4(dtask, toff[r], kTaskCta, r, rp[r], rp[r + 1]);
+        } else if (fs[r]) {  // split row: its segments and its fix-up entry
+            const int ns = static_cast<int>(nsl[r]), slot = static_cast<int>(soff[r]);
+            put4(longrows, sidx[r], r, slot, ns, 0);
+            for (int sg = 0; sg < ns; ++sg) {
+                const long long lo = rp[r] + static_cast<long long>(sg) * seg_nnz;
+                const long long hi = min(static_cast<long long>(rp[r + 1]), lo + seg_nnz);
+                put4(htask, toff[r] + sg, kTaskSeg, r, sg, slot + sg);
+                put4(dtask, toff[r] + sg, kTaskSeg | ((slot + sg) << 8), r, static_cast<int>(lo), static_cast<int>(hi));
+            }
+        } else if (gsf[r]) {  // a group starts here
+            const int e = E0[r];
+            const int c = plan_reduce_code(static_cast<long long>(rp[e]) - rp[r], e - r, lanes_div);
+            const long long pos = nlongtasks + gidx[r];
+            put4(htask, pos, kTaskGroup + 256 * c, r, e, 0);
+            put4(dtask, pos, kTaskGroup | (c << 2) | ((e - r) << 8), r, rp[r], rp[e]);
+            atomicAdd(&cnt[c == 0 ? 0 : c == kReduceSegmented ? 2 : 1], 1ull);
+        }
     }
 }
 
@@ -770,5 +916,128 @@ spx_status spx_dev_row_stats(int32_t M, const int32_t* row_ptr, spx_row_stats_t*
     out->p95 = static_cast<int32_t>(q[1]);
     out->p99 = static_cast<int32_t>(q[2]);
     spx_row_stats_finish(M, out);
+    return SPX_OK;
+}
+
+spx_status spx_dev_check_rp(int32_t M, int64_t nnz, const int32_t* row_ptr, cudaStream_t st) {
+    Pool pool(st);
+    int* bad = pool.get<int>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    if (cudaMemsetAsync(bad, 0, sizeof(int), st) != cudaSuccess) return SPX_ERR_CUDA;
+    check_row_ptr<<<grid_for(M), kT, 0, st>>>(row_ptr, M, nnz, bad);
+    spx_note_launches(1);
+    int h = 0;
+    spx_status s = read_flag(bad, st, &h);
+    if (s != SPX_OK) return s;
+    if (h & 4) return SPX_ERR_ARG;
+    if (h & 2) return SPX_ERR_NOT_SORTED;
+    return SPX_OK;
+}
+
+spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
+    const spx_plan_opts_t& o = P->opts;
+    const int M = P->M;
+    P->tasks.clear();
+    P->dtasks.clear();
+    P->longrows.clear();
+    std::memset(P->counts, 0, sizeof(P->counts));
+    if (M == 0) {
+        P->table_bytes = 0;
+        P->scratch_bytes = 0;
+        return SPX_OK;
+    }
+    Pool pool(st);
+    uint64_t launches = 0;
+    const long long n1 = static_cast<long long>(M) + 1;
+    uint32_t *toff = pool.get<uint32_t>(n1), *nsl = pool.get<uint32_t>(n1), *soff = pool.get<uint32_t>(n1);
+    uint32_t *fl = pool.get<uint32_t>(n1), *lidx = pool.get<uint32_t>(n1), *fs = pool.get<uint32_t>(n1);
+    uint32_t *sidx = pool.get<uint32_t>(n1), *fsh = pool.get<uint32_t>(n1), *on = pool.get<uint32_t>(n1);
+    uint32_t *gsf = pool.get<uint32_t>(n1), *gidx = pool.get<uint32_t>(n1);
+    int *L = pool.get<int>(n1), *E0 = pool.get<int>(n1), *Ea = pool.get<int>(n1), *Eb = pool.get<int>(n1);
+    int* changed = pool.get<int>(1);
+    unsigned long long* gcnt = pool.get<unsigned long long>(3);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    const int g = grid_for(n1);
+    cudaError_t e = cudaSuccess;
+    for (uint32_t* a : {toff, nsl, fl, fs, fsh, gsf})  // entry M stays 0, so each scan's entry M is the total
+        if (e == cudaSuccess) e = cudaMemsetAsync(a + M, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(gcnt, 0, 3 * sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    plan_classify<<<g, kT, 0, st>>>(rp, M, o.pack_max, o.cta_max, o.seg_nnz, toff, nsl, fl, fs, fsh);
+    ++launches;
+    e = scan_exclusive(toff, toff, n1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(nsl, soff, n1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(fl, lidx, n1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(fs, sidx, n1, pool);
+    uint32_t tot[4] = {0, 0, 0, 0};  // long-row tasks, slots, long rows, split rows
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[0], toff + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[1], soff + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[2], lidx + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[3], sidx + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    if (tot[1] > (1u << 23)) return SPX_ERR_INDEX_RANGE;  // a slot must fit the task word
+    const int nL = static_cast<int>(tot[2]);
+    plan_compact<<<g, kT, 0, st>>>(fl, lidx, M, L);
+    plan_group_end<<<g, kT, 0, st>>>(rp, M, fl, L, nL, o.block_nnz, o.block_rows, E0, on);
+    launches += 2;
+    e = cudaMemcpyAsync(Ea, E0, sizeof(int) * static_cast<size_t>(n1), cudaMemcpyDeviceToDevice, st);
+    // doubling: at most ceil(log2(M + 1)) + 1 rounds
+    for (int round = 0; round < 34 && e == cudaSuccess; ++round) {
+        int h = 0;
+        e = cudaMemsetAsync(changed, 0, sizeof(int), st);
+        if (e != cudaSuccess) break;
+        plan_mark<<<g, kT, 0, st>>>(Ea, on, M);
+        plan_compose<<<g, kT, 0, st>>>(Ea, Eb, M, changed);
+        launches += 2;
+        e = cudaMemcpyAsync(&h, changed, sizeof(int), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess || !h) break;
+        std::swap(Ea, Eb);
+    }
+    if (e == cudaSuccess) {
+        plan_starts<<<g, kT, 0, st>>>(on, fsh, M, gsf);
+        ++launches;
+        e = scan_exclusive(gsf, gidx, n1, pool);
+    }
+    uint32_t ngroups = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&ngroups, gidx + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    const long long nt = static_cast<long long>(tot[0]) + ngroups;
+    if (nt > kI32Max) return SPX_ERR_INDEX_RANGE;
+    int *htask = pool.get<int>(4 * nt), *dtask = pool.get<int>(4 * nt), *lrows = pool.get<int>(4ll * tot[3]);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    plan_write<<<g, kT, 0, st>>>(rp, M, o.seg_nnz, o.lanes_div, nsl, fl, fs, toff, soff, sidx, gsf, gidx, E0,
+                                 static_cast<long long>(tot[0]), htask, dtask, lrows, gcnt);
+    ++launches;
+    unsigned long long gc[3] = {0, 0, 0};
+    try {
+        P->tasks.resize(static_cast<size_t>(4 * nt));
+        P->dtasks.resize(static_cast<size_t>(4 * nt));
+        P->longrows.resize(static_cast<size_t>(4) * tot[3]);
+    } catch (const std::bad_alloc&) {
+        cudaStreamSynchronize(st);
+        return SPX_ERR_NOMEM;
+    }
+    e = cudaGetLastError();
+    if (e == cudaSuccess && nt)
+        e = cudaMemcpyAsync(P->tasks.data(), htask, sizeof(int) * 4 * static_cast<size_t>(nt), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && nt)
+        e = cudaMemcpyAsync(P->dtasks.data(), dtask, sizeof(int) * 4 * static_cast<size_t>(nt), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && tot[3])
+        e = cudaMemcpyAsync(P->longrows.data(), lrows, sizeof(int) * 4 * static_cast<size_t>(tot[3]),
+                            cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(gc, gcnt, sizeof(gc), cudaMemcpyDeviceToHost, st);
+    spx_note_launches(launches);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    const int64_t c[9] = {nt, static_cast<int64_t>(tot[3]), static_cast<int64_t>(tot[1]),
+                          static_cast<int64_t>(M) - tot[2], static_cast<int64_t>(tot[2]) - tot[3],
+                          static_cast<int64_t>(tot[3]), static_cast<int64_t>(gc[0]), static_cast<int64_t>(gc[1]),
+                          static_cast<int64_t>(gc[2])};
+    std::memcpy(P->counts, c, sizeof(c));
+    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t);
+    P->scratch_bytes = static_cast<size_t>(tot[1]) * sizeof(float);
     return SPX_OK;
 }

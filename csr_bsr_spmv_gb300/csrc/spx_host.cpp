@@ -399,22 +399,21 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     *plan_out = nullptr;
     if (M < 0 || K < 0 || nnz < 0 || !row_ptr) return SPX_ERR_ARG;
     if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
-    std::vector<int32_t> rp_h;
+    if (where != SPX_HOST && where != SPX_DEVICE) return SPX_ERR_ARG;
     const int32_t* rp = row_ptr;
-    if (where == SPX_DEVICE) {
-        spx_status s = to_host(rp_h, row_ptr, static_cast<int64_t>(M) + 1, nullptr);
-        if (s != SPX_OK) return s;
-        rp = rp_h.data();
-    } else if (where != SPX_HOST) {
-        return SPX_ERR_ARG;
-    }
+    const bool dev = where == SPX_DEVICE;  // device row_ptr: validation, statistics and plan on the GPU
     {
-        spx_status s = check_rp(M, nnz, rp);
+        spx_status s = dev ? spx_dev_check_rp(M, nnz, rp, nullptr) : check_rp(M, nnz, rp);
         if (s != SPX_OK) return s;
     }
     spx_row_stats_t stats;
     try {
-        row_stats_host(M, rp, &stats);
+        if (dev) {
+            spx_status s = spx_dev_row_stats(M, rp, &stats, nullptr);
+            if (s != SPX_OK) return s;
+        } else {
+            row_stats_host(M, rp, &stats);
+        }
     } catch (const std::bad_alloc&) {
         return SPX_ERR_NOMEM;
     }
@@ -432,7 +431,7 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     P->opts = o;
     P->stats = stats;
     try {
-        s = make_plan(P, rp);
+        s = dev ? spx_dev_make_plan(P, rp, nullptr) : make_plan(P, rp);
     } catch (const std::bad_alloc&) {
         s = SPX_ERR_NOMEM;
     }

@@ -57,6 +57,12 @@ struct spx_plan {
     uint64_t magic = 0;
 };
 
+// Plan on the GPU from a device row_ptr: spx_dev_check_rp validates it (the
+// host checks' codes), spx_dev_make_plan fills P's tasks, device tasks, split
+// rows and counts exactly as the host builder does (P->opts set).  Synchronous.
+spx_status spx_dev_check_rp(int32_t M, int64_t nnz, const int32_t* row_ptr, cudaStream_t st);
+spx_status spx_dev_make_plan(spx_plan* P, const int32_t* row_ptr, cudaStream_t st);
+
 constexpr uint64_t kPlanMagic = 0x5350585f504c414eull;  // "SPX_PLAN"
 
 enum : int32_t { kTaskGroup = 0, kTaskCta = 1, kTaskSeg = 2 };
