@@ -23,6 +23,7 @@
 // (spx_last_device_error); they never cause an out-of-bounds access.
 #include <cuda_runtime.h>
 
+#include "spx_carveout.cuh"
 #include "spx_internal.h"
 
 namespace {
@@ -253,6 +254,7 @@ spx_status spx_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_ro
     const long long nchunks = (nnz + kChunk - 1) / kChunk;
     float* head = static_cast<float*>(scratch);
     float* tail = head + nchunks;
+    spx_carve::fit(coo_chunk_kernel, kThreads, 0);
     coo_chunk_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, st>>>(M, K, nnz, coo_row, coo_col, coo_val, x,
                                                                           alpha, beta, y, head, tail);
     uint64_t launches = 1;

@@ -31,6 +31,7 @@
 #include <numeric>
 #include <vector>
 
+#include "spx_carveout.cuh"
 #include "spx_internal.h"
 
 struct spx_sell {
@@ -325,6 +326,7 @@ spx_status spx_spmv_sell(const spx_sell* S, int32_t M, int32_t K, float alpha, c
     const int nlong = static_cast<int>(S->longrows.size() / 4);
     uint64_t launches = 0;
     if (nslices > 0) {
+        spx_carve::fit(sell_kernel, kC * kWarpsPerCta, 0);
         sell_kernel<<<(nslices + kWarpsPerCta - 1) / kWarpsPerCta, kC * kWarpsPerCta, 0, st>>>(
             nslices, reinterpret_cast<const int*>(img), reinterpret_cast<const int*>(img + S->off_prow),
             reinterpret_cast<const int*>(img + S->off_col), reinterpret_cast<const float*>(img + S->off_val), x, alpha,

@@ -28,6 +28,7 @@
 
 #include <mutex>
 
+#include "spx_carveout.cuh"
 #include "spx_internal.h"
 
 namespace {
@@ -339,18 +340,23 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
                         sizeof(float) * static_cast<size_t>(R);
     switch (B) {
         case 512:
+            spx_carve::fit(spmv_tasks_kernel<64, 8>, 64, smem);
             spmv_tasks_kernel<64, 8><<<ntasks, 64, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         case 1024:
+            spx_carve::fit(spmv_tasks_kernel<128, 8>, 128, smem);
             spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         case 2048:
+            spx_carve::fit(spmv_tasks_kernel<256, 8>, 256, smem);
             spmv_tasks_kernel<256, 8><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         case 4096:
+            spx_carve::fit(spmv_tasks_kernel<512, 8>, 512, smem);
             spmv_tasks_kernel<512, 8><<<ntasks, 512, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
         default:
+            spx_carve::fit(spmv_tasks_kernel<256, 0>, 256, smem);
             spmv_tasks_kernel<256, 0><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
             break;
     }
