@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
     const int p0 = __ldg(slice_ptr + s);
     const int L = (__ldg(slice_ptr + s + 1) - p0) / kC;
     const int pr = __ldg(prow + s * kC + lane);
+    const float y_old = pr >= 0 && beta != 0.f ? y[pr] : 0.f;  // read up front, off the epilogue's path
     const int* cp = scol + p0 + lane;
     const float* vp = sval + p0 + lane;
     float acc = 0.f;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
         const float v0 = __ldcs(vp + j * kC);
         acc += v0 * (c0 >= 0 ? __ldg(x + c0) : 0.f);
     }
-    if (pr >= 0) y[pr] = beta != 0.f ? alpha * acc + beta * y[pr] : alpha * acc;
+    if (pr >= 0) y[pr] = beta != 0.f ? alpha * acc + beta * y_old : alpha * acc;
     else if (pr != INT_MIN) partials[-1 - pr] = acc;
 }
 
