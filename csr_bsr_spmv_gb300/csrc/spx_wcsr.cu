@@ -160,12 +160,14 @@ __global__ void __launch_bounds__(kThreads)
             else mbar_arrive(acc_bar);
         }
     } else {
-        // Gather: thread t copies compressed column k = t/2 (one B row) into the
-        // boxes h = t%2, t%2 + 2, ... (64 columns = 128 bytes = 8 chunks of 16 bytes
-        // each) of the 128-byte-swizzled tile: row k at k*128, chunk j at (j ^ (k & 7)).
+        // Gather: per stage 64 B rows x 64 columns per box (128 bytes = 8 pieces
+        // of 16 bytes).  Eight consecutive threads copy one row's 128 bytes, so
+        // each warp-wide copy covers four whole 128-byte lines.  Thread t copies
+        // piece j = t%8 of box h = (t/8)%2 for rows k = 8i + t/16, i = 0..7, into
+        // the 128-byte-swizzled tile: row k at k*128, piece j at (j ^ (k & 7)).
         const int t = threadIdx.x - 64;
-        const int k = t >> 1, h = t & 1;
-        const uint32_t row_off = h * kBBox + k * 128u;
+        const int j = t & 7, h = (t >> 3) & 1, k0 = t >> 4;
+        const uint32_t piece_off = h * kBBox + (static_cast<uint32_t>(j ^ (k0 & 7)) << 4);
         int b = 0;
         for (; b < nch; ++b) {
             const int s = b % kStages;
@@ -179,16 +181,19 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 break;
             }
-            const int cr = __ldg(win_col + static_cast<long long>(g0 + b) * kWin + k);
-            const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
-            const uint16_t* src = c >= 0 ? B + static_cast<long long>(c) * ldb + n0 + 64 * h : B;
-            const uint32_t nbytes = c >= 0 ? 16u : 0u;  // padding column: zero-fill
-            const uint32_t dst = stage_b(s) + row_off;
+            const int* wc = win_col + static_cast<long long>(g0 + b) * kWin;
 #pragma unroll
-            for (int hh = 0; hh < HALVES; ++hh)
+            for (int i = 0; i < 8; ++i) {
+                const int k = 8 * i + k0;
+                const int cr = __ldg(wc + k);
+                const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
+                const uint16_t* src = c >= 0 ? B + static_cast<long long>(c) * ldb + n0 + 64 * h + 8 * j : B;
+                const uint32_t nbytes = c >= 0 ? 16u : 0u;  // padding column: zero-fill
+                const uint32_t dst = stage_b(s) + k * 128u + piece_off;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    cp_async16(dst + 2 * hh * kBBox + ((j ^ (k & 7)) << 4), src + (c >= 0 ? 128 * hh + 8 * j : 0), nbytes);
+                for (int hh = 0; hh < HALVES; ++hh)
+                    cp_async16(dst + 2 * hh * kBBox, src + (c >= 0 ? 128 * hh : 0), nbytes);
+            }
             cp_async_commit();
             if (b >= kStages - 1) {  // the copies of stage b - (kStages - 1) have landed: publish them
                 cp_async_wait<kStages - 1>();
