@@ -301,6 +301,10 @@ def run_ours(args, rank, world):
         t0 = time.perf_counter()
         S = spx.Sell(M, K, rp, col, val, opts=args.plan_opts, device=dev, stream=stream)
         timings["build_sell_ms"] = 1e3 * (time.perf_counter() - t0)
+        dr, dc, dv = to_dev(rp), to_dev(col), to_dev(val)
+        device_timing("build_sell_device_ms", lambda: spx.Sell(M, K, dr, dc, dv, opts=args.plan_opts,
+                                                                upload=False).close())
+        del dr, dc, dv
         src = source_hash("spx_sell.cu")
 
         def run():

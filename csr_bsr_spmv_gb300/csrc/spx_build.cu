@@ -498,6 +498,109 @@ __global__ void plan_write(const int* __restrict__ rp, int M, int seg_nnz, int l
     }
 }
 
+// ---------------------------------------------------------------- SELL-C-sigma
+// [SpMM-ops] §1.4, [Formats] §6: rows longer than `piece` are cut into pieces
+// (pseudo-rows with a partial-sum slot); pseudo-rows are sorted longest first,
+// stably, inside windows of sigma; slices of 32 take the length of their first
+// (longest) pseudo-row and are stored column-major.  Same image as the host builder.
+constexpr int kSellC = 32;
+
+// per row: pseudo-rows n, long-row flag, slots (entry M stays 0 for the scans)
+__global__ void sell_count(const int* __restrict__ rp, int M, int piece, uint32_t* __restrict__ n,
+                           uint32_t* __restrict__ fl, uint32_t* __restrict__ ns) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const long long l = static_cast<long long>(rp[i + 1]) - rp[i];
+        const bool lng = l > piece;
+        const uint32_t k = lng ? static_cast<uint32_t>((l + piece - 1) / piece) : 1u;
+        n[i] = k;
+        fl[i] = lng;
+        ns[i] = lng ? k : 0u;
+    }
+}
+
+// pseudo-row arrays in row order (pieces in order) and the long-row table
+__global__ void sell_pseudo(const int* __restrict__ rp, int M, int piece, const uint32_t* __restrict__ pst,
+                            const uint32_t* __restrict__ fl, const uint32_t* __restrict__ lidx,
+                            const uint32_t* __restrict__ lslot, int* __restrict__ plen, int* __restrict__ prow,
+                            int* __restrict__ pstart, int* __restrict__ pslot, int* __restrict__ longrows) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < M;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int r = static_cast<int>(i);
+        const int a = rp[r], l = rp[r + 1] - a;
+        const uint32_t q0 = pst[r];
+        if (!fl[r]) {
+            plen[q0] = l;
+            prow[q0] = r;
+            pstart[q0] = a;
+            pslot[q0] = -1;
+            continue;
+        }
+        const int n = (l + piece - 1) / piece, slot = static_cast<int>(lslot[r]);
+        reinterpret_cast<int4*>(longrows)[lidx[r]] = make_int4(r, slot, n, 0);
+        for (int k = 0; k < n; ++k) {
+            plen[q0 + k] = min(piece, l - k * piece);
+            prow[q0 + k] = r;
+            pstart[q0 + k] = a + k * piece;
+            pslot[q0 + k] = slot + k;
+        }
+    }
+}
+
+// sort keys: descending length (piece - len), payload the pseudo-row index
+__global__ void sell_len_keys(const int* __restrict__ plen, int piece, uint32_t* __restrict__ keys,
+                              int* __restrict__ idx, long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        keys[i] = static_cast<uint32_t>(piece - plen[i]);
+        idx[i] = static_cast<int>(i);
+    }
+}
+
+// window of the pseudo-row now at position i
+__global__ void sell_win_keys(const int* __restrict__ idx, int sigma, uint32_t* __restrict__ keys, long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT)
+        keys[i] = static_cast<uint32_t>(idx[i] / sigma);
+}
+
+// padded entries of slice s = 32 x the length of its first pseudo-row; total in acc
+__global__ void sell_slices(const int* __restrict__ idx, const int* __restrict__ plen, long long ns,
+                            uint32_t* __restrict__ width, unsigned long long* __restrict__ acc) {
+    for (long long s = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; s < ns;
+         s += static_cast<long long>(gridDim.x) * kT) {
+        const uint32_t w = static_cast<uint32_t>(plen[idx[s * kSellC]]) * kSellC;
+        width[s] = w;
+        atomicAdd(acc, static_cast<unsigned long long>(w));
+    }
+}
+
+__global__ void fill_i32(int* __restrict__ a, long long n, int v) {
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kT)
+        a[i] = v;
+}
+
+// the pseudo-row at sorted position q: its row code and its entries, column-major in slice q / 32
+__global__ void sell_scatter(const int* __restrict__ idx, const int* __restrict__ plen, const int* __restrict__ prow,
+                             const int* __restrict__ pstart, const int* __restrict__ pslot,
+                             const uint32_t* __restrict__ sp, const int* __restrict__ col,
+                             const float* __restrict__ val, long long np, int* __restrict__ prow_out,
+                             int* __restrict__ scol, float* __restrict__ sval) {
+    for (long long q = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; q < np;
+         q += static_cast<long long>(gridDim.x) * kT) {
+        const int p = idx[q];
+        const int slot = pslot[p];
+        prow_out[q] = slot < 0 ? prow[p] : -1 - slot;
+        const long long base = static_cast<long long>(sp[q / kSellC]) + q % kSellC;
+        const int a = pstart[p], l = plen[p];
+        for (int j = 0; j < l; ++j) {
+            scol[base + static_cast<long long>(j) * kSellC] = col[a + j];
+            sval[base + static_cast<long long>(j) * kSellC] = val[a + j];
+        }
+    }
+}
+
 int grid_for(long long n) {
     long long g = (n + kT - 1) / kT;
     if (g > 152 * 32) g = 152 * 32;
@@ -1039,5 +1142,129 @@ spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
     std::memcpy(P->counts, c, sizeof(c));
     P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t);
     P->scratch_bytes = static_cast<size_t>(tot[1]) * sizeof(float);
+    return SPX_OK;
+}
+
+spx_status spx_dev_build_sell(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
+                              const float* val, int32_t sigma, int32_t piece, spx_sell_dev_image* out,
+                              cudaStream_t st) {
+    *out = spx_sell_dev_image{};
+    Pool pool(st);
+    uint64_t launches = 0;
+    int* bad = pool.get<int>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    if (cudaMemsetAsync(bad, 0, sizeof(int), st) != cudaSuccess) return SPX_ERR_CUDA;
+    check_row_ptr<<<grid_for(M), kT, 0, st>>>(rp, M, nnz, bad);
+    ++launches;
+    if (nnz > 0) {
+        check_indices<<<grid_for(nnz), kT, 0, st>>>(col, nnz, K, bad);
+        ++launches;
+    }
+    int h = 0;
+    spx_status s = read_flag(bad, st, &h);
+    if (s != SPX_OK) return s;
+    if (h & 4) return SPX_ERR_ARG;
+    if (h & 2) return SPX_ERR_NOT_SORTED;
+    if (h & 1) return SPX_ERR_INDEX_RANGE;
+    // pseudo-rows per row, long rows, slots
+    const long long n1 = static_cast<long long>(M) + 1;
+    uint32_t *cnt = pool.get<uint32_t>(n1), *fl = pool.get<uint32_t>(n1), *nsl = pool.get<uint32_t>(n1);
+    uint32_t *pst = pool.get<uint32_t>(n1), *lidx = pool.get<uint32_t>(n1), *lslot = pool.get<uint32_t>(n1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    cudaError_t e = cudaSuccess;
+    for (uint32_t* a : {cnt, fl, nsl})
+        if (e == cudaSuccess) e = cudaMemsetAsync(a + M, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess && M > 0) {
+        sell_count<<<grid_for(M), kT, 0, st>>>(rp, M, piece, cnt, fl, nsl);
+        ++launches;
+    }
+    if (e == cudaSuccess) e = scan_exclusive(cnt, pst, n1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(fl, lidx, n1, pool);
+    if (e == cudaSuccess) e = scan_exclusive(nsl, lslot, n1, pool);
+    uint32_t tot[3] = {0, 0, 0};  // pseudo-rows, long rows, slots
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[0], pst + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[1], lidx + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&tot[2], lslot + M, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    const long long np = tot[0], nlong = tot[1], slots = tot[2];
+    if (slots > kI32Max || np > kI32Max - kSellC) return SPX_ERR_INDEX_RANGE;
+    const long long ns = (np + kSellC - 1) / kSellC;
+    int *plen = pool.get<int>(np), *prow = pool.get<int>(np), *pstart = pool.get<int>(np), *pslot = pool.get<int>(np);
+    int* lrows = pool.get<int>(4 * nlong);
+    uint32_t *k = pool.get<uint32_t>(np), *k2 = pool.get<uint32_t>(np), *width = pool.get<uint32_t>(ns + 1);
+    uint32_t* sp = pool.get<uint32_t>(ns + 1);
+    int *ix = pool.get<int>(np), *ix2 = pool.get<int>(np);
+    unsigned long long* acc = pool.get<unsigned long long>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    if (M > 0) {
+        sell_pseudo<<<grid_for(M), kT, 0, st>>>(rp, M, piece, pst, fl, lidx, lslot, plen, prow, pstart, pslot, lrows);
+        ++launches;
+    }
+    // longest first, stably, inside windows of sigma pseudo-rows (LSD: length, then window)
+    if (np > 0) {
+        sell_len_keys<<<grid_for(np), kT, 0, st>>>(plen, piece, k, ix, np);
+        ++launches;
+        e = radix_sort(k, ix, k2, ix2, np, bits_for(static_cast<long long>(piece) + 1), pool, launches);
+        const long long nwin = (np + sigma - 1) / sigma;
+        if (e == cudaSuccess && bits_for(nwin) > 0) {
+            sell_win_keys<<<grid_for(np), kT, 0, st>>>(ix, sigma, k, np);
+            ++launches;
+            e = radix_sort(k, ix, k2, ix2, np, bits_for(nwin), pool, launches);
+        }
+    }
+    if (e == cudaSuccess) e = cudaMemsetAsync(width + ns, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long), st);
+    if (e == cudaSuccess && ns > 0) {
+        sell_slices<<<grid_for(ns), kT, 0, st>>>(ix, plen, ns, width, acc);
+        ++launches;
+    }
+    if (e == cudaSuccess) e = scan_exclusive(width, sp, ns + 1, pool);
+    unsigned long long padded = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&padded, acc, sizeof(padded), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    if (padded > static_cast<unsigned long long>(kI32Max)) return SPX_ERR_INDEX_RANGE;
+    // the image (same layout as the host builder's), allocated for the caller
+    auto a16 = [](size_t n) { return (n + 15) & ~static_cast<size_t>(15); };
+    spx_sell_dev_image img;
+    img.off_prow = a16(sizeof(int32_t) * static_cast<size_t>(ns + 1));
+    img.off_long = img.off_prow + a16(sizeof(int32_t) * static_cast<size_t>(ns * kSellC));
+    img.off_col = img.off_long + a16(sizeof(int32_t) * static_cast<size_t>(4 * nlong));
+    img.off_val = img.off_col + a16(sizeof(int32_t) * static_cast<size_t>(padded));
+    img.bytes = img.off_val + a16(sizeof(float) * static_cast<size_t>(padded));
+    if (cudaMalloc(&img.image, img.bytes) != cudaSuccess) {
+        cudaGetLastError();  // clear the allocation error
+        return SPX_ERR_NOMEM;
+    }
+    char* d = static_cast<char*>(img.image);
+    int* prow_out = reinterpret_cast<int*>(d + img.off_prow);
+    int* scol = reinterpret_cast<int*>(d + img.off_col);
+    float* sval = reinterpret_cast<float*>(d + img.off_val);
+    e = cudaMemcpyAsync(d, sp, sizeof(uint32_t) * static_cast<size_t>(ns + 1), cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && nlong)
+        e = cudaMemcpyAsync(d + img.off_long, lrows, sizeof(int) * static_cast<size_t>(4 * nlong),
+                            cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && padded) e = cudaMemsetAsync(scol, 0xFF, sizeof(int) * padded, st);  // -1: padding
+    if (e == cudaSuccess && padded) e = cudaMemsetAsync(sval, 0, sizeof(float) * padded, st);
+    if (e == cudaSuccess && ns > 0) {
+        fill_i32<<<grid_for(ns * kSellC), kT, 0, st>>>(prow_out, ns * kSellC, INT32_MIN);  // unused tail lanes
+        sell_scatter<<<grid_for(np), kT, 0, st>>>(ix, plen, prow, pstart, pslot, sp, col, val, np, prow_out, scol,
+                                                  sval);
+        launches += 2;
+        e = cudaGetLastError();
+    }
+    spx_note_launches(launches);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        cudaFree(img.image);
+        return SPX_ERR_CUDA;
+    }
+    img.nslices = ns;
+    img.pseudo_rows = np;
+    img.padded = static_cast<int64_t>(padded);
+    img.nlong = nlong;
+    img.slots = slots;
+    *out = img;
     return SPX_OK;
 }

@@ -36,6 +36,16 @@ spx_status spx_dev_build_bsr(int32_t M, int32_t K, const int32_t* row_ptr, const
 spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const int32_t* col, const void* val,
                               int32_t vb, int32_t* win_ptr, int32_t* win_col, void* win_val, int64_t* nchunks_out,
                               double* fill_out, cudaStream_t st);
+// SELL-C-sigma image built on the GPU (layout of spx_sell.cu): `image` is
+// device memory from cudaMalloc that the caller of spx_dev_build_sell owns.
+struct spx_sell_dev_image {
+    void* image = nullptr;
+    size_t bytes = 0, off_prow = 0, off_long = 0, off_col = 0, off_val = 0;
+    int64_t nslices = 0, pseudo_rows = 0, padded = 0, nlong = 0, slots = 0;
+};
+spx_status spx_dev_build_sell(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                              const float* val, int32_t sigma, int32_t piece, spx_sell_dev_image* out,
+                              cudaStream_t st);
 // Row statistics of a device row_ptr (lengths, sums and extremes in one
 // kernel, percentiles from a radix sort of the lengths); synchronous.
 spx_status spx_dev_row_stats(int32_t M, const int32_t* row_ptr, spx_row_stats_t* out, cudaStream_t st);

@@ -38,11 +38,13 @@ struct spx_sell {
     int32_t M = 0, K = 0;
     int64_t nnz = 0;
     spx_sell_opts_t opts{};
-    std::vector<int32_t> slice_ptr, prow, longrows, scol;
+    std::vector<int32_t> slice_ptr, prow, longrows, scol;  // host-built image (empty when built on the GPU)
     std::vector<float> sval;
-    int64_t pseudo_rows = 0, slots = 0;
+    int64_t nslices = 0, padded = 0, nlong = 0, pseudo_rows = 0, slots = 0;
     size_t off_prow = 0, off_long = 0, off_col = 0, off_val = 0, bytes = 0;
-    const void* d_image = nullptr;
+    bool gpu_built = false;         // built on the GPU: the host vectors stay empty
+    void* d_own = nullptr;          // GPU-built image held by the library until the first upload
+    const void* d_image = nullptr;  // the caller's uploaded copy
     uint64_t magic = 0;
 };
 
@@ -110,6 +112,9 @@ spx_status build(spx_sell* S, const int32_t* rp, const int32_t* col, const float
     }
     S->pseudo_rows = np;
     S->slots = slots;
+    S->nslices = ns;
+    S->padded = padded;
+    S->nlong = static_cast<int64_t>(S->longrows.size() / 4);
     S->off_prow = align16(sizeof(int32_t) * S->slice_ptr.size());
     S->off_long = S->off_prow + align16(sizeof(int32_t) * S->prow.size());
     S->off_col = S->off_long + align16(sizeof(int32_t) * S->longrows.size());
@@ -194,29 +199,39 @@ spx_status spx_sell_build(int32_t M, int32_t K, int64_t nnz, const int32_t* row_
     spx_sell_opts_t o;
     if (opts) o = *opts; else spx_sell_opts_default(&o);
     if (o.sigma < kC || o.sigma % kC || o.sigma > (1 << 20) || o.piece < 1 || o.piece > (1 << 24)) return SPX_ERR_ARG;
-    std::vector<int32_t> rph, colh;
-    std::vector<float> valh;
+    if (where == SPX_DEVICE) {  // built on the GPU (spx_build.cu); the image stays in device memory
+        spx_sell_dev_image img;
+        spx_status s = spx_dev_build_sell(M, K, nnz, row_ptr, col, val, o.sigma, o.piece, &img, nullptr);
+        if (s != SPX_OK) return s;
+        spx_sell* S = new (std::nothrow) spx_sell();
+        if (!S) {
+            cudaFree(img.image);
+            return SPX_ERR_NOMEM;
+        }
+        S->M = M;
+        S->K = K;
+        S->nnz = nnz;
+        S->opts = o;
+        S->gpu_built = true;
+        S->d_own = img.image;
+        S->bytes = img.bytes;
+        S->off_prow = img.off_prow;
+        S->off_long = img.off_long;
+        S->off_col = img.off_col;
+        S->off_val = img.off_val;
+        S->nslices = img.nslices;
+        S->padded = img.padded;
+        S->nlong = img.nlong;
+        S->pseudo_rows = img.pseudo_rows;
+        S->slots = img.slots;
+        S->magic = kSellMagic;
+        *out = S;
+        return SPX_OK;
+    }
+    if (where != SPX_HOST) return SPX_ERR_ARG;
     const int32_t* rp = row_ptr;
     const int32_t* cl = col;
     const float* vl = val;
-    if (where == SPX_DEVICE) {
-        try {
-            rph.resize(static_cast<size_t>(M) + 1);
-            colh.resize(static_cast<size_t>(nnz));
-            valh.resize(static_cast<size_t>(nnz));
-        } catch (const std::bad_alloc&) {
-            return SPX_ERR_NOMEM;
-        }
-        cudaError_t e = cudaMemcpy(rph.data(), row_ptr, sizeof(int32_t) * rph.size(), cudaMemcpyDeviceToHost);
-        if (e == cudaSuccess && nnz) e = cudaMemcpy(colh.data(), col, sizeof(int32_t) * colh.size(), cudaMemcpyDeviceToHost);
-        if (e == cudaSuccess && nnz) e = cudaMemcpy(valh.data(), val, sizeof(float) * valh.size(), cudaMemcpyDeviceToHost);
-        if (e != cudaSuccess) return SPX_ERR_CUDA;
-        rp = rph.data();
-        cl = colh.data();
-        vl = valh.data();
-    } else if (where != SPX_HOST) {
-        return SPX_ERR_ARG;
-    }
     if (rp[0] != 0 || rp[M] != nnz) return SPX_ERR_ARG;
     for (int32_t i = 0; i < M; ++i)
         if (rp[i + 1] < rp[i]) return SPX_ERR_NOT_SORTED;
@@ -249,10 +264,10 @@ spx_status spx_sell_get_info(const spx_sell* S, spx_sell_info_t* out) {
     out->M = S->M;
     out->K = S->K;
     out->nnz = S->nnz;
-    out->slices = static_cast<int64_t>(S->slice_ptr.size()) - 1;
+    out->slices = S->nslices;
     out->pseudo_rows = S->pseudo_rows;
-    out->padded = S->slice_ptr.back();
-    out->long_rows = static_cast<int64_t>(S->longrows.size() / 4);
+    out->padded = S->padded;
+    out->long_rows = S->nlong;
     out->slots = S->slots;
     out->image_bytes = S->bytes;
     out->scratch_bytes = sizeof(float) * static_cast<size_t>(S->slots);
@@ -263,6 +278,20 @@ spx_status spx_sell_get_info(const spx_sell* S, spx_sell_info_t* out) {
 spx_status spx_sell_get_arrays(const spx_sell* S, int32_t* slice_ptr, int32_t* prow, int32_t* longrows, int32_t* scol,
                                float* sval) {
     if (!sell_ok(S)) return SPX_ERR_ARG;
+    const char* dimg = static_cast<const char*>(S->d_own ? S->d_own : S->d_image);
+    if (S->gpu_built) {  // copy the sections down
+        if (!dimg) return SPX_ERR_NOT_READY;
+        const size_t n[5] = {sizeof(int32_t) * static_cast<size_t>(S->nslices + 1),
+                             sizeof(int32_t) * static_cast<size_t>(S->nslices * kC),
+                             sizeof(int32_t) * static_cast<size_t>(4 * S->nlong),
+                             sizeof(int32_t) * static_cast<size_t>(S->padded), sizeof(float) * static_cast<size_t>(S->padded)};
+        const size_t off[5] = {0, S->off_prow, S->off_long, S->off_col, S->off_val};
+        void* dst[5] = {slice_ptr, prow, longrows, scol, sval};
+        for (int i = 0; i < 5; ++i)
+            if (dst[i] && n[i] && cudaMemcpy(dst[i], dimg + off[i], n[i], cudaMemcpyDeviceToHost) != cudaSuccess)
+                return SPX_ERR_CUDA;
+        return SPX_OK;
+    }
     auto cp = [](void* dst, const void* src, size_t n) {
         if (dst && n) std::memcpy(dst, src, n);
     };
@@ -280,6 +309,17 @@ spx_status spx_sell_upload(spx_sell* S, void* image, size_t image_bytes, spx_str
     if (!spx_aligned(image, 16)) return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* d = static_cast<char*>(image);
+    if (S->gpu_built) {  // one device-to-device copy, then the library's copy is freed
+        const void* src = S->d_own ? S->d_own : S->d_image;
+        if (!src) return SPX_ERR_NOT_READY;
+        cudaError_t e = src == image ? cudaSuccess : cudaMemcpyAsync(d, src, S->bytes, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return SPX_ERR_CUDA;
+        if (S->d_own) cudaFree(S->d_own);
+        S->d_own = nullptr;
+        S->d_image = image;
+        return SPX_OK;
+    }
     struct Part {
         size_t off;
         const void* src;
@@ -302,6 +342,7 @@ spx_status spx_sell_destroy(spx_sell* S) {
     if (!S) return SPX_OK;
     if (!sell_ok(S)) return SPX_ERR_ARG;
     S->magic = 0;
+    if (S->d_own) cudaFree(S->d_own);
     delete S;
     return SPX_OK;
 }
@@ -323,8 +364,8 @@ spx_status spx_spmv_sell(const spx_sell* S, int32_t M, int32_t K, float alpha, c
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const char* img = static_cast<const char*>(S->d_image);
-    const int nslices = static_cast<int>(S->slice_ptr.size()) - 1;
-    const int nlong = static_cast<int>(S->longrows.size() / 4);
+    const int nslices = static_cast<int>(S->nslices);
+    const int nlong = static_cast<int>(S->nlong);
     uint64_t launches = 0;
     if (nslices > 0) {
         spx_carve::fit(sell_kernel, kC * kWarpsPerCta, 0);

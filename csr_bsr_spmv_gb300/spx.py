@@ -389,7 +389,7 @@ class Sell:
             o = SellOpts(**d)
         h = ctypes.c_void_p()
         nnz = col.numel() if isinstance(col, torch.Tensor) else int(np.asarray(col).size)
-        _check(lib.spx_sell_build(M, K, nnz, _ptr(row_ptr), _ptr(col), _ptr(val), _where(row_ptr),
+        _check(lib.spx_sell_build(M, K, nnz, _ptr(row_ptr), _ptr(col), _ptr(val), _where(row_ptr, col, val),
                                   ctypes.byref(o) if o else None, ctypes.byref(h)), "spx_sell_build")
         self.handle = h
         self.M, self.K, self.nnz = M, K, nnz

@@ -442,14 +442,21 @@ typedef struct spx_sell spx_sell; /* opaque, host-side */
 spx_status spx_sell_opts_default(spx_sell_opts_t* out);
 
 /*
- * Build the SELL-C-sigma form of a CSR matrix (host or device arrays; device
- * arrays are copied to the host).  Pseudo-rows are listed in row order (a
+ * Build the SELL-C-sigma form of a CSR matrix from host or device arrays.
+ * Device arrays are converted on the GPU (the default stream, synchronous):
+ * pieces and slots from per-row counts and scans, the window-local order by two
+ * stable radix passes (length descending, then window), slice widths from
+ * each slice's first pseudo-row, and a scatter into the column-major image.
+ * The image then lives in library-owned device memory until the first
+ * spx_sell_upload, which copies it device to device and frees it.  Both paths
+ * give the same image.  Pseudo-rows are listed in row order (a
  * long row's pieces in piece order), stably sorted by length, longest first,
  * inside each window of sigma pseudo-rows, then cut into slices of 32.
  * Within a slice, entry j of lane r sits at slice_ptr[s] + 32 j + r; padding
  * has column -1 and value 0.  prow holds the row of each pseudo-row, -1-slot
  * for a piece, INT32_MIN for the unused lanes of the last slice.  opts NULL:
- * the defaults.  Errors: SPX_ERR_NOT_SORTED (row_ptr decreasing),
+ * the defaults.  Errors: SPX_ERR_ARG (row_ptr[0] != 0 or row_ptr[M] != nnz),
+ * SPX_ERR_NOT_SORTED (row_ptr decreasing),
  * SPX_ERR_INDEX_RANGE (a column outside [0, K) or more than 2^31-1 padded
  * entries).  Release with spx_sell_destroy.
  */
@@ -457,7 +464,9 @@ spx_status spx_sell_build(int32_t M, int32_t K, int64_t nnz, const int32_t* row_
                           const float* val, spx_loc where, const spx_sell_opts_t* opts, spx_sell** out);
 spx_status spx_sell_get_info(const spx_sell* sell, spx_sell_info_t* out);
 /* Host copies of slice_ptr[slices+1], prow[32 slices], longrows[4 long_rows]
-   ({row, first slot, #pieces, 0}), scol[padded], sval[padded]; any may be NULL. */
+   ({row, first slot, #pieces, 0}), scol[padded], sval[padded]; any may be NULL.
+   A GPU-built form is read back from device memory (its own copy before the
+   first upload, the uploaded image after it). */
 spx_status spx_sell_get_arrays(const spx_sell* sell, int32_t* slice_ptr, int32_t* prow, int32_t* longrows,
                                int32_t* scol, float* sval);
 /* Copy the format into caller-owned device memory (info.image_bytes, 16-byte

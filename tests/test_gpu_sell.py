@@ -80,3 +80,53 @@ def test_power_law_full_size_sampled():
     ref, bound = oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"], rows=rows)
     got = y[torch.from_numpy(rows).long().cuda()].cpu().numpy()
     assert_within(got, ref, bound, what="power-law SELL")
+
+
+def _sell_arrays_equal(Sh, Sd):
+    assert Sd.info == Sh.info
+    for a, b in zip(Sh.arrays(), Sd.arrays()):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("M,K,lmin,lmax", [(1, 1, 0, 0), (1, 5, 5, 5), (37, 50, 0, 9), (1000, 700, 0, 40),
+                                          (5000, 6000, 0, 700), (3000, 100, 0, 0)])
+@pytest.mark.parametrize("opts", [None, dict(sigma=32, piece=8), dict(sigma=64, piece=1), dict(sigma=4096, piece=1000)])
+def test_device_build_equals_host_build(M, K, lmin, lmax, opts):
+    """SELL-C-sigma built on the GPU from device arrays: the same image as the host build,
+    read back before and after the upload, and the same product bit for bit."""
+    d = synth.random_coo(M + 5, M, K, lmin, lmax)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    Sh = spx.Sell(M, K, rp, col, val, opts=opts)
+    Sd = spx.Sell(M, K, dev(rp), dev(col), dev(val), opts=opts, upload=False)
+    _sell_arrays_equal(Sh, Sd)  # from the library's device copy
+    Sd.image = torch.empty_like(Sh.image)
+    Sd.scratch = torch.empty_like(Sh.scratch)
+    spx._check(spx._lib().spx_sell_upload(Sd.handle, spx._ptr(Sd.image), Sd.image.numel() * 4, None), "upload")
+    torch.cuda.synchronize()
+    _sell_arrays_equal(Sh, Sd)  # from the uploaded image (the bytes between sections are unspecified)
+    x = synth.uniform(M + 1, synth.T_X, K)
+    y0 = synth.uniform(M + 1, synth.T_Y, M)
+    yh, yd = dev(y0), dev(y0)
+    spx.spx_spmv_sell(Sh, dev(x), yh, 1.5, -0.5)
+    spx.spx_spmv_sell(Sd, dev(x), yd, 1.5, -0.5)
+    assert torch.equal(yh, yd)
+
+
+def test_device_build_power_law():
+    """The 4,194,304^2 power-law workload built on the GPU equals the host build."""
+    c = synth.power_law_rows()
+    M, K = c["M"], c["K"]
+    rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val"])
+    Sh = spx.Sell(M, K, rp, col, val)
+    Sd = spx.Sell(M, K, dev(rp), dev(col), dev(val))
+    _sell_arrays_equal(Sh, Sd)
+
+
+def test_device_build_rejects_bad_input():
+    for rp, col, code in [([1, 2, 3], [0, 1, 1], -1),   # row_ptr[0] != 0
+                          ([0, 3, 2], [0, 1], -3),      # decreasing
+                          ([0, 2, 3], [0, 9, 1], -2)]:  # column outside [0, K)
+        with pytest.raises(spx.SpxError) as e:
+            spx.Sell(2, 4, dev(np.array(rp, np.int32)), dev(np.array(col, np.int32)),
+                     dev(np.ones(len(col), np.float32)))
+        assert e.value.code == code
