@@ -7,7 +7,8 @@ is one SpMV call through the C ABI: the binned main launch plus the long-row
 fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|bsr|wcsr]
+                    [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|
+                                spmm32-f16|spmm128-f16|bsr|wcsr]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -160,6 +161,10 @@ def make_workload(name: str, rows: int = 0):
         c["val_bf16"] = synth.to_bf16_bits(c["val"])
         c["B_bf16"] = synth.to_bf16_bits(c["B"]).reshape(c["B"].shape)
         c["name"] += " (bf16 A values and B, fp32 accumulation)"
+    elif name in ("spmm32-f16", "spmm128-f16"):
+        c = synth.clustered_spmm(N=int(name[4:-4]))
+        c["B_f16"] = c["B"].astype(np.float16)
+        c["name"] += " (fp16 A values and B, fp32 accumulation)"
     elif name == "bsr":
         c = synth.block_sparse()
     elif name == "wcsr":
@@ -185,7 +190,7 @@ def accounting(c):
         b1 = 8 * nnz + 4 * (M + 1) + 4 * K + 8 * M
         b2 = 8 * nnz + 4 * (K + 1) + 4 * M + 8 * K
         return 4 * nnz, b1 + b2
-    if w.startswith("spmm") and w.endswith("bf16"):
+    if w.startswith("spmm") and w.endswith("f16"):  # bf16 or fp16 values and B
         N = c["N"]
         return 2 * nnz * N, 6 * nnz + 4 * (M + 1) + 2 * K * N + 4 * M * N
     if w.startswith("spmm"):
@@ -417,6 +422,26 @@ def run_ours(args, rank, world):
                 Co.copy_(C, non_blocking=True)
 
         extra = {"variant": "bf16 storage, fp32 accumulation"}
+    elif w.startswith("spmm") and w.endswith("-f16"):
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val.astype(np.float16).view(np.int16)))
+        B = to_dev(c["B_f16"].view(np.int16))
+        C = torch.empty(M, c["N"], device=dev)
+        src = source_hash("spx_spmm.cu")
+
+        def run():
+            spx.spx_spmm_csr_f16(A, B, C, 1.0, 0.0, stream=stream)
+
+        Bh = torch.from_numpy(c["B_f16"].view(np.int16)).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 2, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                B.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_csr_f16(A, B, C, 1.0, 0.0, stream=stream)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"variant": "fp16 storage, fp32 accumulation"}
     elif w.startswith("spmm"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         B = to_dev(c["B"])
@@ -647,7 +672,8 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr") or w.endswith("bf16")) else "f32",
+        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr") or w.endswith("bf16"))
+        else "f16->f32" if w.endswith("-f16") else "f32",
         "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
                    "N": c.get("N", 1), "l2": "flushed between steps (256 MB write); inputs also exceed L2",
@@ -712,6 +738,9 @@ def cpu_step_fn(c):
         import synth
         val = synth.bf16_bits_to_f32(c["val_bf16"])
         c = dict(c, B=synth.bf16_bits_to_f32(c["B_bf16"]).reshape(c["B"].shape))
+    elif w.endswith("-f16"):
+        val = val.astype(np.float16).astype(np.float64)
+        c = dict(c, B=c["B_f16"].astype(np.float64))
     rows = np.arange(0, M, 16, dtype=np.int32)
     fl = 2 * int(np.diff(rp)[rows].sum()) * N
     return (lambda: oracle.spmm(M, rp, col, val, c["B"], rows=rows)), fl, f"every 16th row ({rows.size} rows)"
@@ -762,7 +791,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
-                    choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-bf16",
+                    choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-f16",
+                             "spmm128-f16", "spmm32-bf16",
                              "spmm128-bf16", "bsr", "wcsr"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")

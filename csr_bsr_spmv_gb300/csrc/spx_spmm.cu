@@ -14,6 +14,7 @@
 //                        carry an L2 evict-last hint and A / C stream through
 //                        with evict-first hints;
 //   scalar  otherwise  : a warp per row, lanes over columns.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "spx_internal.h"
@@ -78,9 +79,9 @@ __global__ void __launch_bounds__(kThreads) spmm_small_kernel(int M, const int* 
 // ------------------------------------------------------------- float4 sub-warp / tiled
 // L lanes per row, each lane 4 columns; the warp holds 32/L rows.  Column
 // tile origin = blockIdx.y * 4 * L (gridDim.y tiles).  One template serves
-// fp32 storage and bf16 storage (A's values and B as bf16, widened exactly
-// to fp32: [SpMM-ops] §5 keeps storage and accumulation precision apart;
-// halving B halves the gathered bytes, the term that dominates SpMM).
+// fp32 storage and 16-bit storage (A's values and B as bf16 or fp16, widened
+// exactly to fp32: [SpMM-ops] §5 keeps storage and accumulation precision
+// apart; halving B halves the gathered bytes, the term that dominates SpMM).
 //
 // The CTA's rows are consecutive, so their nonzeros are one contiguous run of
 // col/val.  Up to kStageCap of them are first copied into shared memory with
@@ -117,6 +118,19 @@ struct StoreBF16 {
         uint2 w;
         asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(w.x), "=r"(w.y) : "l"(p), "l"(pol));
         return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+};
+
+struct StoreF16 {  // IEEE binary16 values; widened with the hardware conversion (exact)
+    using V = uint16_t;
+    using Bt = uint16_t;
+    static constexpr int kMinBlocks = 8;
+    __device__ static float widen(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+    __device__ static float4 brow(const uint16_t* p, uint64_t pol) {  // 4 fp16 = 8 bytes
+        uint2 w;
+        asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(w.x), "=r"(w.y) : "l"(p), "l"(pol));
+        return make_float4(widen(static_cast<uint16_t>(w.x & 0xffffu)), widen(static_cast<uint16_t>(w.x >> 16)),
+                           widen(static_cast<uint16_t>(w.y & 0xffffu)), widen(static_cast<uint16_t>(w.y >> 16)));
     }
 };
 
@@ -268,6 +282,25 @@ void launch_vec_tile(int tile, int M, int N, const int* rp, const int* col, cons
     }
 }
 
+// 16-bit A values and B (bf16 or fp16 bit patterns), fp32 products and sums, fp32 C.
+template <class T>
+spx_status spmm_16bit(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const uint16_t* val,
+                      int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                      cudaStream_t st) {
+    if (M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
+    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (N % 4 || ldb % 4 || ldc % 4) return SPX_ERR_UNSUPPORTED;
+    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 2) || !spx_aligned(B, 8) ||
+        !spx_aligned(C, 16))
+        return SPX_ERR_ALIGN;
+    launch_vec_tile<T>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
+    spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
+}
+
 spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col, const float* val,
                      int32_t N, const float* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
                      int32_t col_tile, cudaStream_t st) {
@@ -316,19 +349,15 @@ spx_status spx_spmm_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, co
 spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
                              const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                              float* C, int64_t ldc, spx_stream_t stream) {
-    if (M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
-    if (nnz > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (M == 0 || N == 0) return SPX_OK;
-    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
-    if (ldb < N || ldc < N) return SPX_ERR_ARG;
-    if (N % 4 || ldb % 4 || ldc % 4) return SPX_ERR_UNSUPPORTED;
-    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 2) || !spx_aligned(B, 8) ||
-        !spx_aligned(C, 16))
-        return SPX_ERR_ALIGN;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    launch_vec_tile<StoreBF16>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
-    spx_note_launches(1);
-    return spx_cuda_status(cudaGetLastError());
+    return spmm_16bit<StoreBF16>(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_spmm_csr_f16(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
+                            const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                            float* C, int64_t ldc, spx_stream_t stream) {
+    return spmm_16bit<StoreF16>(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,

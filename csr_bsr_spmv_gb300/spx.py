@@ -121,6 +121,7 @@ def _lib():
             "spx_spmm_csr_tiled": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, i32, vp], ctypes.c_int),
             "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
             "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_csr_f16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
                                 ctypes.c_int, vp], ctypes.c_int),
@@ -580,6 +581,18 @@ def spx_spmm_csr_bf16(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1
     _check(_lib().spx_spmm_csr_bf16(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
                                     B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
            "spx_spmm_csr_bf16")
+    return C
+
+
+def spx_spmm_csr_f16(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha*A*B + beta*C with A.val and B holding fp16 values (float16 or int16 bit patterns), C fp32."""
+    N = B.shape[1]
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
+    _require(A.val.element_size() == 2 and B.element_size() == 2, "A values and B must be 16-bit (fp16)")
+    _check(_lib().spx_spmm_csr_f16(A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
+                                   B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
+           "spx_spmm_csr_f16")
     return C
 
 

@@ -402,6 +402,17 @@ spx_status spx_spmm_csr_bf16(int32_t M, int32_t K, int64_t nnz, const int32_t* r
                              const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                              float* C, int64_t ldc, spx_stream_t stream);
 
+/*
+ * spx_spmm_csr_bf16 with IEEE binary16 (fp16) bit patterns instead of bf16
+ * ([SpMM-ops] §5 names both 16-bit formats).  fp16 -> fp32 widening is exact
+ * (subnormals included) and an fp16 x fp16 product (11-bit significands) is
+ * exact in fp32, so the result again carries fp32 summation error only.  Same
+ * shape and alignment rules as spx_spmm_csr_bf16.  Launches: 1.
+ */
+spx_status spx_spmm_csr_f16(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, const int32_t* col,
+                            const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
+                            float* C, int64_t ldc, spx_stream_t stream);
+
 /* Which SpMM variant spx_spmm_csr would launch for these arguments:
    0 = small-N, 1 = float4 with N <= 128, 2 = float4 with N > 128, 3 = scalar. */
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);

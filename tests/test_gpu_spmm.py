@@ -161,3 +161,31 @@ def test_bf16_long_and_empty_rows():
         ref, bound = oracle.spmm(70, rp, col, synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(6000, N),
                                  1.0, 0.25, C0)
         assert_within(Cd.cpu().numpy(), ref, bound, what=f"bf16 long rows N={N}")
+
+
+@pytest.mark.parametrize("N", [4, 32, 128, 256])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, -1.5)])
+def test_f16_values(N, alpha, beta):
+    """fp16 A values and B (subnormals and the largest finite values included):
+    exact widening and exact products, so the fp32 sums meet the fp32 bound."""
+    M, K = 700, 900
+    d = synth.random_coo(N + 11, M, K, 0, 60)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    vh = val.astype(np.float16)
+    Bh = synth.uniform(N + 12, synth.T_B, K * N).astype(np.float16).reshape(K, N)
+    Bh[0, :2] = [np.float16(6.0e-8), np.float16(-6.5e4)]  # a subnormal and a near-maximal value
+    vh[:3] = [np.float16(3.0e-5), np.float16(1.0e3), np.float16(-2.0e-7)]
+    A = spx.Csr(M, K, dev(rp), dev(col), dev(vh.view(np.int16)))
+    C0 = synth.uniform(N + 13, synth.T_Y, M * N).reshape(M, N)
+    Cd = dev(C0)
+    spx.spx_spmm_csr_f16(A, dev(Bh.view(np.int16)), Cd, alpha, beta)
+    ref, bound = oracle.spmm(M, rp, col, vh.astype(np.float64), Bh.astype(np.float64), alpha, beta, C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, what=f"f16 N={N}")
+
+
+def test_f16_rejects_unsupported_shapes():
+    rp = dev(np.array([0, 1], np.int32))
+    A = spx.Csr(1, 1, rp, dev(np.array([0], np.int32)), dev(np.zeros(1, np.int16)))
+    with pytest.raises(spx.SpxError) as e:
+        spx.spx_spmm_csr_f16(A, dev(np.zeros((1, 6), np.int16)), dev(np.zeros((1, 6), np.float32)))
+    assert e.value.code == -7  # N not a multiple of 4
