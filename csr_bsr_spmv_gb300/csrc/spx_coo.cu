@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "spx_carveout.cuh"
+#include "spx_gather.cuh"
 #include "spx_internal.h"
 
 namespace {
@@ -90,14 +91,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) coo_chunk_kernel(int M, 
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int k = threadIdx.x + j * kThreads;
-        rr[j] = k < n ? __ldcs(row + base + k) : 0;
-        cc[j] = k < n ? __ldcs(col + base + k) : 0;
-        vv[j] = k < n ? __ldcs(val + base + k) : 0.f;
+        rr[j] = k < n ? spx_gather::ld_once(row + base + k) : 0;
+        cc[j] = k < n ? spx_gather::ld_once(col + base + k) : 0;
+        vv[j] = k < n ? spx_gather::ld_once(val + base + k) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const bool in = cc[j] >= 0 && cc[j] < K;
-        vv[j] = in ? vv[j] * __ldg(x + cc[j]) : 0.f;
+        vv[j] = in ? vv[j] * spx_gather::ld_x(x + cc[j]) : 0.f;
         if (!in && threadIdx.x + j * kThreads < n) coo_error(static_cast<int>(SPX_ERR_INDEX_RANGE));
     }
 #pragma unroll

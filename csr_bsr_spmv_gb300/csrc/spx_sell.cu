@@ -32,6 +32,7 @@
 #include <vector>
 
 #include "spx_carveout.cuh"
+#include "spx_gather.cuh"
 #include "spx_internal.h"
 
 struct spx_sell {
@@ -147,16 +148,16 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
         float v[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            c[u] = __ldcs(cp + (j + u) * kC);
-            v[u] = __ldcs(vp + (j + u) * kC);
+            c[u] = spx_gather::ld_once(cp + (j + u) * kC);
+            v[u] = spx_gather::ld_once(vp + (j + u) * kC);
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) acc += v[u] * (c[u] >= 0 ? __ldg(x + c[u]) : 0.f);
+        for (int u = 0; u < kU; ++u) acc += v[u] * (c[u] >= 0 ? spx_gather::ld_x(x + c[u]) : 0.f);
     }
     for (; j < L; ++j) {
-        const int c0 = __ldcs(cp + j * kC);
-        const float v0 = __ldcs(vp + j * kC);
-        acc += v0 * (c0 >= 0 ? __ldg(x + c0) : 0.f);
+        const int c0 = spx_gather::ld_once(cp + j * kC);
+        const float v0 = spx_gather::ld_once(vp + j * kC);
+        acc += v0 * (c0 >= 0 ? spx_gather::ld_x(x + c0) : 0.f);
     }
     if (pr >= 0) y[pr] = beta != 0.f ? alpha * acc + beta * y_old : alpha * acc;
     else if (pr != INT_MIN) partials[-1 - pr] = acc;

@@ -22,13 +22,14 @@
 //
 // Each task carries its nonzero range, so a CTA issues its value/column loads
 // right after reading the task.  Values and column indices are read with the
-// streaming (evict-first) hint so that x -- the gathered operand -- keeps its
-// L2 residency ([SpMM-ops] §2.5).
+// streaming hint (no L1 allocation) so that x -- the gathered operand -- keeps
+// its L1 and L2 residency ([SpMM-ops] §2.5).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "spx_carveout.cuh"
+#include "spx_gather.cuh"
 #include "spx_internal.h"
 
 namespace {
@@ -37,8 +38,9 @@ constexpr int kThreads = 256;  // fix-up kernel
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
-__device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
+__device__ __forceinline__ float ld_stream(const float* p) { return spx_gather::ld_once(p); }
+__device__ __forceinline__ int ld_stream(const int* p) { return spx_gather::ld_once(p); }
+using spx_gather::ld_x;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -72,13 +74,13 @@ __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__
         int c2 = ld_stream(col + p + 2 * NT), c3 = ld_stream(col + p + 3 * NT);
         float v0 = ld_stream(val + p), v1 = ld_stream(val + p + NT);
         float v2 = ld_stream(val + p + 2 * NT), v3 = ld_stream(val + p + 3 * NT);
-        float x0 = __ldg(x + c0), x1 = __ldg(x + c1), x2 = __ldg(x + c2), x3 = __ldg(x + c3);
+        float x0 = ld_x(x + c0), x1 = ld_x(x + c1), x2 = ld_x(x + c2), x3 = ld_x(x + c3);
         s += v0 * x0;
         s += v1 * x1;
         s += v2 * x2;
         s += v3 * x3;
     }
-    for (; p < b; p += NT) s += ld_stream(val + p) * __ldg(x + ld_stream(col + p));
+    for (; p < b; p += NT) s += ld_stream(val + p) * ld_x(x + ld_stream(col + p));
     return s;
 }
 
@@ -119,11 +121,11 @@ __device__ __forceinline__ void stage_products(int p0, int n, const int* __restr
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
             const int k = threadIdx.x + j * NT;
-            if (k < n) s_prod[sk(k)] = v[j] * __ldg(x + c[j]);
+            if (k < n) s_prod[sk(k)] = v[j] * ld_x(x + c[j]);
         }
     } else {
         for (int k = threadIdx.x; k < n; k += NT)
-            s_prod[sk(k)] = ld_stream(val + p0 + k) * __ldg(x + ld_stream(col + p0 + k));
+            s_prod[sk(k)] = ld_stream(val + p0 + k) * ld_x(x + ld_stream(col + p0 + k));
     }
 }
 
@@ -314,9 +316,9 @@ __global__ void __launch_bounds__(kThreads) gather_probe_kernel(const int* __res
             v[j] = ld_stream(val + p + j * stride);
         }
 #pragma unroll
-        for (int j = 0; j < U; ++j) s += v[j] * __ldg(x + c[j]);
+        for (int j = 0; j < U; ++j) s += v[j] * ld_x(x + c[j]);
     }
-    for (; p < n; p += stride) s += ld_stream(val + p) * __ldg(x + ld_stream(col + p));
+    for (; p < n; p += stride) s += ld_stream(val + p) * ld_x(x + ld_stream(col + p));
     __shared__ float red[kWarps];
     s = block_sum<kThreads>(s, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = s;
