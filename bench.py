@@ -273,7 +273,7 @@ def run_ours(args, rank, world):
         timings["plan_ms"] = 1e3 * (time.perf_counter() - t0)
         device_timing("plan_device_ms", lambda: spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, opts=opts, stream=stream))
         alpha, beta = c["alpha"], c["beta"]
-        src = source_hash("spx_spmv.cu")
+        src = source_hash("spx_spmv.cu", "spx_gather.cuh", "spx_carveout.cuh")
 
         def run():
             spx.spx_spmv_csr(plan, A, x, y, alpha, beta, stream=stream)
@@ -310,7 +310,7 @@ def run_ours(args, rank, world):
         device_timing("build_sell_device_ms", lambda: spx.Sell(M, K, dr, dc, dv, opts=args.plan_opts,
                                                                 upload=False).close())
         del dr, dc, dv
-        src = source_hash("spx_sell.cu")
+        src = source_hash("spx_sell.cu", "spx_gather.cuh", "spx_carveout.cuh")
 
         def run():
             spx.spx_spmv_sell(S, x, y, alpha, beta, stream=stream)
@@ -336,7 +336,7 @@ def run_ours(args, rank, world):
         y = to_dev(c["y"])
         alpha, beta = c["alpha"], c["beta"]
         scratch = torch.empty(max(1, spx.spx_spmv_coo_scratch_bytes(c["row"].size) // 4), device=dev)
-        src = source_hash("spx_coo.cu")
+        src = source_hash("spx_coo.cu", "spx_gather.cuh", "spx_carveout.cuh")
 
         def run():
             spx.spx_spmv_coo(M, K, crow, ccol, cval, x, y, alpha, beta, stream=stream, scratch=scratch)
@@ -376,7 +376,7 @@ def run_ours(args, rank, world):
         u = to_dev(c["u0"])
         v = to_dev(c["v0"])
         a, b = float(c["alphas"][0]), float(c["betas"][0])
-        src = source_hash("spx_spmv.cu")
+        src = source_hash("spx_spmv.cu", "spx_gather.cuh", "spx_carveout.cuh")
 
         u0, v0 = u.clone(), v.clone()
 
