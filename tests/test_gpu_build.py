@@ -216,3 +216,25 @@ def test_row_stats_device_power_law():
     srt = np.sort(lengths)
     assert [got["p50"], got["p95"], got["p99"]] == [int(srt[(q * M + 99) // 100 - 1]) for q in (50, 95, 99)]
     assert got["max"] == int(srt[-1]) and got["min"] == int(srt[0])
+
+
+@pytest.mark.parametrize("M,K", [(0, 0), (0, 7), (5, 0), (130, 0)])
+def test_device_builders_empty_matrices(M, K):
+    """No rows or no columns (so no entries): every GPU builder returns the host builders' empty forms."""
+    rp = np.zeros(M + 1, np.int32)
+    col = np.zeros(0, np.int32)
+    val = np.zeros(0, np.float32)
+    for want, got in ((oracle.build_bsr(M, K, rp, col, val, 4, 4),
+                       spx.spx_build_bsr(M, K, cuda(rp), cuda(col), cuda(val), 4, 4)),
+                      (oracle.build_wcsr(M, K, rp, col, val), spx.spx_build_wcsr(M, K, cuda(rp), cuda(col), cuda(val))),
+                      (oracle.transpose(M, K, rp, col, val), spx.spx_transpose_csr(M, K, cuda(rp), cuda(col), cuda(val))),
+                      (oracle.build_csr(M, K, col, col, val), spx.spx_build_csr(M, K, cuda(col), cuda(col), cuda(val)))):
+        for w, g in zip(want[:3], got[:3]):
+            assert np.array_equal(w, host(g))
+    assert spx.spx_row_stats(M, cuda(rp)) == spx.spx_row_stats(M, rp)
+    ph, pd = spx.spx_plan_csr(M, K, 0, rp), spx.spx_plan_csr(M, K, 0, cuda(rp))
+    assert ph.info == pd.info
+    Sh, Sd = spx.Sell(M, K, rp, col, val), spx.Sell(M, K, cuda(rp), cuda(col), cuda(val))
+    assert Sh.info == Sd.info
+    for a, b in zip(Sh.arrays(), Sd.arrays()):
+        assert np.array_equal(a, b)
