@@ -8,7 +8,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <utility>
 
 namespace spx_tc {
 
@@ -107,19 +109,22 @@ constexpr uint32_t idesc_bf16_mn_k(uint32_t M, uint32_t N) {
 
 // ------------------------------------------------------------ host side
 
-// Raise a kernel's dynamic shared-memory limit once per device (the attribute
-// is per device, and a process may drive several).
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
+// attribute is per device, a process may drive several, and kernels of one
+// signature (the template variants) are told apart by their address.
 template <class K>
 inline cudaError_t set_smem_limit(K* kernel, size_t bytes) {
     static std::mutex mu;
-    static uint64_t done = 0;  // bit d: device d already set for this kernel
+    static std::map<std::pair<const void*, int>, size_t> done;  // (kernel, device) -> bytes set
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && (done >> dev & 1u)) return cudaSuccess;
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-    if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+    if (e == cudaSuccess) done[key] = bytes;
     return e;
 }
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
