@@ -8,7 +8,7 @@ fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|
-                                spmm32-f16|spmm128-f16|bsr|wcsr]
+                                spmm32-f16|spmm128-f16|spmm32-power-law|bsr|wcsr]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -161,6 +161,11 @@ def make_workload(name: str, rows: int = 0):
         c["val_bf16"] = synth.to_bf16_bits(c["val"])
         c["B_bf16"] = synth.to_bf16_bits(c["B"]).reshape(c["B"].shape)
         c["name"] += " (bf16 A values and B, fp32 accumulation)"
+    elif name == "spmm32-power-law":  # skewed rows: the planned SpMM (long rows split)
+        c = synth.power_law_rows()
+        c["N"] = 32
+        c["B"] = synth.uniform(8, synth.T_B, c["K"] * 32).reshape(c["K"], 32)
+        c["name"] += " SpMM N=32 (planned: long rows split)"
     elif name in ("spmm32-f16", "spmm128-f16"):
         c = synth.clustered_spmm(N=int(name[4:-4]))
         c["B_f16"] = c["B"].astype(np.float16)
@@ -442,6 +447,32 @@ def run_ours(args, rank, world):
                 Co.copy_(C, non_blocking=True)
 
         extra = {"variant": "fp16 storage, fp32 accumulation"}
+    elif w == "spmm32-power-law":
+        A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
+        B = to_dev(c["B"])
+        C = torch.empty(M, c["N"], device=dev)
+        # plan options that suit SpMM: rows past 64 nonzeros get whole CTAs, past 2048 segments
+        popts = args.plan_opts or {"block_nnz": 1024, "lanes_div": 0, "pack_max": 64, "cta_max": 2048, "seg_nnz": 2048}
+        t0 = time.perf_counter()
+        plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, opts=popts, stream=stream)
+        timings["plan_device_ms"] = 1e3 * (time.perf_counter() - t0)
+        sc = torch.empty(max(1, plan.info["slots"] * c["N"]), device=dev)
+        src = source_hash("spx_spmm.cu")
+
+        def run():
+            spx.spx_spmm_csr_planned(plan, A, B, C, 1.0, 0.0, stream=stream, scratch=sc)
+
+        Bh = torch.from_numpy(c["B"]).pin_memory()
+        Co = torch.empty(M, c["N"]).pin_memory()
+        h2d, d2h = Bh.numel() * 4, Co.numel() * 4
+
+        def e2e_run():
+            with torch.cuda.stream(stream):
+                B.copy_(Bh, non_blocking=True)
+                spx.spx_spmm_csr_planned(plan, A, B, C, 1.0, 0.0, stream=stream, scratch=sc)
+                Co.copy_(C, non_blocking=True)
+
+        extra = {"plan": dict(plan.info), "plan_opts": plan.opts}
     elif w.startswith("spmm"):
         A = spx.Csr(M, K, to_dev(rp), to_dev(col), to_dev(val))
         B = to_dev(c["B"])
@@ -792,7 +823,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="power-law",
                     choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-f16",
-                             "spmm128-f16", "spmm32-bf16",
+                             "spmm128-f16", "spmm32-power-law", "spmm32-bf16",
                              "spmm128-bf16", "bsr", "wcsr"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")

@@ -106,6 +106,7 @@ struct StoreF32 {
     using V = float;
     using Bt = float;
     static constexpr int kMinBlocks = 6;
+    static constexpr bool kBatchTail = true;  // the last partial batch of a row loads in parallel
     __device__ static float widen(float v) { return v; }
     __device__ static float4 brow(const float* p, uint64_t pol) { return ld_keep(p, pol); }
 };
@@ -113,6 +114,7 @@ struct StoreBF16 {
     using V = uint16_t;
     using Bt = uint16_t;
     static constexpr int kMinBlocks = 8;
+    static constexpr bool kBatchTail = false;  // at 32 registers the batched tail spills
     __device__ static float widen(uint16_t v) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
     __device__ static float4 brow(const uint16_t* p, uint64_t pol) {  // 4 bf16 = 8 bytes
         uint2 w;
@@ -125,6 +127,7 @@ struct StoreF16 {  // IEEE binary16 values; widened with the hardware conversion
     using V = uint16_t;
     using Bt = uint16_t;
     static constexpr int kMinBlocks = 8;
+    static constexpr bool kBatchTail = false;
     __device__ static float widen(uint16_t v) { return __half2float(__ushort_as_half(v)); }
     __device__ static float4 brow(const uint16_t* p, uint64_t pol) {  // 4 fp16 = 8 bytes
         uint2 w;
@@ -162,6 +165,24 @@ __device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* 
             acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
         }
     }
+    if (T::kBatchTail && p < b) {  // the last partial batch, its loads issued together (no serial tail)
+        int c[U];
+        float v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            c[j] = p + j < b ? ld_a<SMEM>(cols + p + j) : 0;
+            v[j] = p + j < b ? T::widen(ld_a<SMEM>(vals + p + j)) : 0.f;
+        }
+        float4 bv[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+            bv[j] = p + j < b ? T::brow(Bc + (long long)c[j] * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
+        }
+        p = b;
+    }
     for (; p < b; ++p) {
         const int c0 = ld_a<SMEM>(cols + p);
         const float v0 = T::widen(ld_a<SMEM>(vals + p));
@@ -175,7 +196,7 @@ template <int L, class T>
 __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
     spmm_vec_kernel(int M, int N, const int* __restrict__ rp, const int* __restrict__ col,
                     const typename T::V* __restrict__ val, const typename T::Bt* __restrict__ B, long long ldb,
-                    float alpha, float beta, float* C, long long ldc) {
+                    float alpha, float beta, float* C, long long ldc, int long_min) {
     constexpr int RPW = 32 / L;         // rows per warp
     constexpr int R = kWarps * RPW;     // rows per CTA
     constexpr int IT = kStageCap / kThreads;
@@ -212,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
     if (row >= M || n0 >= N) return;
     const uint64_t pol = l2_evict_last_policy();
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    if (b - a > long_min) return;  // a long row: its CTA task or segments (planned call) produce it
     const typename T::Bt* Bc = B + n0;
     const float4 acc = staged ? row_dot<T, true>(s_col, s_val, a - ca, b - ca, Bc, ldb, pol)
                               : row_dot<T, false>(col, val, a, b, Bc, ldb, pol);
@@ -222,6 +244,85 @@ __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
         r.x += beta * o.x; r.y += beta * o.y; r.z += beta * o.z; r.w += beta * o.w;
     }
     __stcs(cp, r);  // C is written once: evict-first
+}
+
+// ------------------------------------------------------------- long rows (planned call)
+// One CTA per long task of an SpMV plan and per column tile ([SpMM-ops] §2.4:
+// split a long row, combine the partial sums in a second pass).  The kT/L
+// sub-warps stride the task's nonzeros; their float4 sums are combined in a
+// fixed order through shared memory.  A CTA row writes C; a segment of a split
+// row writes its partial row to partials[slot][0..N).
+template <int L, class T>
+__global__ void __launch_bounds__(kThreads) spmm_long_kernel(const int4* __restrict__ tasks, int N,
+                                                            const int* __restrict__ col,
+                                                            const typename T::V* __restrict__ val,
+                                                            const typename T::Bt* __restrict__ B, long long ldb,
+                                                            float alpha, float beta, float* C, long long ldc,
+                                                            float* __restrict__ partials) {
+    constexpr int NSUB = kThreads / L;
+    constexpr int U = 4;
+    __shared__ float4 red[NSUB][L];
+    const int4 t = tasks[blockIdx.x];
+    const int kind = t.x & 3, row = t.y, p0 = t.z, p1 = t.w;
+    const int q = threadIdx.x / L, l = threadIdx.x % L;
+    const int n0 = blockIdx.y * 4 * L + 4 * l;
+    const uint64_t pol = l2_evict_last_policy();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n0 < N) {
+        const typename T::Bt* Bc = B + n0;
+        int p = p0 + q;
+        for (; p + (U - 1) * NSUB < p1; p += U * NSUB) {
+            int c[U];
+            float v[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                c[j] = ld_stream(col + p + j * NSUB);
+                v[j] = T::widen(ld_stream(val + p + j * NSUB));
+            }
+            float4 bv[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) bv[j] = T::brow(Bc + (long long)c[j] * ldb, pol);
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
+            }
+        }
+        for (; p < p1; p += NSUB) {
+            const float v0 = T::widen(ld_stream(val + p));
+            const float4 b0 = T::brow(Bc + (long long)ld_stream(col + p) * ldb, pol);
+            acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
+        }
+    }
+    red[q][l] = acc;
+    __syncthreads();
+    if (threadIdx.x >= 4 * L) return;
+    // thread c sums column c of the tile over the sub-warps, in sub-warp order
+    const int c = threadIdx.x, n = blockIdx.y * 4 * L + c;
+    if (n >= N) return;
+    const float* rf = reinterpret_cast<const float*>(&red[0][0]);
+    float s = 0.f;
+    for (int k = 0; k < NSUB; ++k) s += rf[k * 4 * L + c];
+    if (kind == 1) {  // a CTA row: the whole row is here
+        float* cp = C + (long long)row * ldc + n;
+        *cp = beta != 0.f ? alpha * s + beta * *cp : alpha * s;
+    } else {  // a segment: its partial row
+        partials[(long long)(t.x >> 8) * N + n] = s;
+    }
+}
+
+// One thread per (split row, column): the row's segment partials in segment order, then alpha/beta.
+__global__ void __launch_bounds__(kThreads) spmm_long_fixup_kernel(const int4* __restrict__ longrows, int nlong,
+                                                                  int N, const float* __restrict__ partials,
+                                                                  float alpha, float beta, float* C, long long ldc) {
+    for (int r = blockIdx.y; r < nlong; r += gridDim.y) {
+        const int4 lr = longrows[r];
+        for (int n = blockIdx.x * kThreads + threadIdx.x; n < N; n += gridDim.x * kThreads) {
+            float s = 0.f;
+            for (int k = 0; k < lr.z; ++k) s += partials[(long long)(lr.y + k) * N + n];
+            float* cp = C + (long long)lr.x * ldc + n;
+            *cp = beta != 0.f ? alpha * s + beta * *cp : alpha * s;
+        }
+    }
 }
 
 // ------------------------------------------------------------- scalar fallback
@@ -261,24 +362,43 @@ int auto_col_tile(int32_t N) {
     return t;
 }
 
+// Long-row work of a planned call: the plan's CTA-row and segment tasks (the
+// first nlong_tasks entries of its device table), then the split-row fix-up.
+struct LongWork {
+    const int4* tasks = nullptr;
+    int ntasks = 0;
+    const int4* longrows = nullptr;
+    int nlongrows = 0;
+    float* partials = nullptr;
+    int long_min = 0x7fffffff;  // rows longer than this are long (skipped by the row kernel)
+};
+
 template <int L, class T>
 void launch_vec(int M, int N, const int* rp, const int* col, const typename T::V* val, const typename T::Bt* B,
-                long long ldb, float alpha, float beta, float* C, long long ldc, cudaStream_t st) {
+                long long ldb, float alpha, float beta, float* C, long long ldc, cudaStream_t st,
+                const LongWork& lw) {
     constexpr int rows_per_cta = kWarps * (32 / L);
-    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, (N + 4 * L - 1) / (4 * L));
-    spmm_vec_kernel<L, T><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+    const int tiles = (N + 4 * L - 1) / (4 * L);
+    dim3 grid((M + rows_per_cta - 1) / rows_per_cta, tiles);
+    spmm_vec_kernel<L, T><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, lw.long_min);
+    if (lw.ntasks > 0)
+        spmm_long_kernel<L, T><<<dim3(lw.ntasks, tiles), kThreads, 0, st>>>(lw.tasks, N, col, val, B, ldb, alpha,
+                                                                             beta, C, ldc, lw.partials);
+    if (lw.nlongrows > 0)
+        spmm_long_fixup_kernel<<<dim3((N + kThreads - 1) / kThreads, lw.nlongrows < 65535 ? lw.nlongrows : 65535),
+                                 kThreads, 0, st>>>(lw.longrows, lw.nlongrows, N, lw.partials, alpha, beta, C, ldc);
 }
 
 template <class T>
 void launch_vec_tile(int tile, int M, int N, const int* rp, const int* col, const typename T::V* val,
                      const typename T::Bt* B, long long ldb, float alpha, float beta, float* C, long long ldc,
-                     cudaStream_t st) {
+                     cudaStream_t st, const LongWork& lw = LongWork()) {
     switch (tile) {
-        case 8: launch_vec<2, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 16: launch_vec<4, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 32: launch_vec<8, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        case 64: launch_vec<16, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
-        default: launch_vec<32, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st); break;
+        case 8: launch_vec<2, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
+        case 16: launch_vec<4, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
+        case 32: launch_vec<8, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
+        case 64: launch_vec<16, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
+        default: launch_vec<32, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
     }
 }
 
@@ -298,6 +418,38 @@ spx_status spmm_16bit(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, cons
         return SPX_ERR_ALIGN;
     launch_vec_tile<T>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
     spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
+}
+
+// A planned call: the plan's long rows (CTA rows and split rows, as for the
+// SpMV) get whole CTAs and segment partials; the other rows run as usual.
+template <class T>
+spx_status spmm_planned(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
+                        const typename T::V* val, int32_t N, const typename T::Bt* B, int64_t ldb, float alpha,
+                        float beta, float* C, int64_t ldc, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+    if (!spx_plan_ok(P) || M < 0 || K < 0 || nnz < 0 || N < 0) return SPX_ERR_ARG;
+    if (P->M != M || P->K != K || P->nnz != nnz) return SPX_ERR_ARG;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (P->table_bytes > 0 && !P->d_table) return SPX_ERR_NOT_READY;
+    if (!rp || !C || (nnz > 0 && (!col || !val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (N % 4 || ldb % 4 || ldc % 4) return SPX_ERR_UNSUPPORTED;
+    if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, sizeof(typename T::V)) ||
+        !spx_aligned(B, 4 * sizeof(typename T::Bt)) || !spx_aligned(C, 16) || !spx_aligned(scratch, 4))
+        return SPX_ERR_ALIGN;
+    const int64_t slots = P->counts[2];
+    const size_t need = sizeof(float) * static_cast<size_t>(slots) * static_cast<size_t>(N);
+    if (need && (!scratch || scratch_bytes < need)) return SPX_ERR_ARG;
+    LongWork lw;
+    const int64_t ngroups = P->counts[6] + P->counts[7] + P->counts[8];
+    lw.tasks = static_cast<const int4*>(P->d_table);
+    lw.ntasks = static_cast<int>(P->counts[0] - ngroups);  // long-row tasks come first in the table
+    lw.longrows = lw.tasks + P->counts[0];
+    lw.nlongrows = static_cast<int>(P->counts[1]);
+    lw.partials = static_cast<float*>(scratch);
+    lw.long_min = P->opts.pack_max;
+    launch_vec_tile<T>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw);
+    spx_note_launches(1 + (lw.ntasks > 0) + (lw.nlongrows > 0));
     return spx_cuda_status(cudaGetLastError());
 }
 
@@ -358,6 +510,35 @@ spx_status spx_spmm_csr_f16(int32_t M, int32_t K, int64_t nnz, const int32_t* rp
                             float* C, int64_t ldc, spx_stream_t stream) {
     return spmm_16bit<StoreF16>(M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc,
                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t spx_spmm_csr_planned_scratch_bytes(const spx_plan* plan, int32_t N) {
+    if (!spx_plan_ok(plan) || N < 0) return 0;
+    return sizeof(float) * static_cast<size_t>(plan->counts[2]) * static_cast<size_t>(N);
+}
+
+spx_status spx_spmm_csr_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* rp,
+                                const int32_t* col, const float* val, int32_t N, const float* B, int64_t ldb,
+                                float alpha, float beta, float* C, int64_t ldc, void* scratch, size_t scratch_bytes,
+                                spx_stream_t stream) {
+    return spmm_planned<StoreF32>(plan, M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, scratch,
+                                  scratch_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_spmm_csr_bf16_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* rp,
+                                     const int32_t* col, const uint16_t* val, int32_t N, const uint16_t* B,
+                                     int64_t ldb, float alpha, float beta, float* C, int64_t ldc, void* scratch,
+                                     size_t scratch_bytes, spx_stream_t stream) {
+    return spmm_planned<StoreBF16>(plan, M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, scratch,
+                                   scratch_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_spmm_csr_f16_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* rp,
+                                    const int32_t* col, const uint16_t* val, int32_t N, const uint16_t* B,
+                                    int64_t ldb, float alpha, float beta, float* C, int64_t ldc, void* scratch,
+                                    size_t scratch_bytes, spx_stream_t stream) {
+    return spmm_planned<StoreF16>(plan, M, K, nnz, rp, col, val, N, B, ldb, alpha, beta, C, ldc, scratch,
+                                  scratch_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 spx_status spx_spmm_csr_tiled(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,

@@ -122,6 +122,13 @@ def _lib():
             "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
             "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_spmm_csr_f16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_spmm_csr_planned_scratch_bytes": ([vp, i32], sz),
+            "spx_spmm_csr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                     ctypes.c_int),
+            "spx_spmm_csr_bf16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                          ctypes.c_int),
+            "spx_spmm_csr_f16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                         ctypes.c_int),
             "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
             "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
                                 ctypes.c_int, vp], ctypes.c_int),
@@ -594,6 +601,41 @@ def spx_spmm_csr_f16(A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.
                                    B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)),
            "spx_spmm_csr_f16")
     return C
+
+
+def _spmm_planned(name: str, plan: Plan, A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float, beta: float,
+                  stream, scratch):
+    N = B.shape[1]
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
+    lib = _lib()
+    need = int(lib.spx_spmm_csr_planned_scratch_bytes(plan.handle, N))
+    if scratch is None:
+        scratch = torch.empty(max(1, (need + 3) // 4), dtype=torch.float32, device=C.device)
+    _check(getattr(lib, name)(plan.handle, A.M, A.K, A.nnz, _ptr(A.row_ptr), _ptr(A.col), _ptr(A.val), N, _ptr(B),
+                              B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _ptr(scratch),
+                              scratch.numel() * scratch.element_size(), _stream(stream)), name)
+    return C
+
+
+def spx_spmm_csr_planned(plan: Plan, A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+                         beta: float = 0.0, stream=None, scratch: torch.Tensor | None = None):
+    """C <- alpha*A*B + beta*C with the plan's long rows split (CTA rows, segments + fix-up)."""
+    return _spmm_planned("spx_spmm_csr_planned", plan, A, B, C, alpha, beta, stream, scratch)
+
+
+def spx_spmm_csr_bf16_planned(plan: Plan, A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+                              beta: float = 0.0, stream=None, scratch: torch.Tensor | None = None):
+    """spx_spmm_csr_planned with bf16 bit patterns for A.val and B."""
+    _require(A.val.element_size() == 2 and B.element_size() == 2, "A values and B must be 16-bit (bf16)")
+    return _spmm_planned("spx_spmm_csr_bf16_planned", plan, A, B, C, alpha, beta, stream, scratch)
+
+
+def spx_spmm_csr_f16_planned(plan: Plan, A: Csr, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+                             beta: float = 0.0, stream=None, scratch: torch.Tensor | None = None):
+    """spx_spmm_csr_planned with fp16 values for A.val and B."""
+    _require(A.val.element_size() == 2 and B.element_size() == 2, "A values and B must be 16-bit (fp16)")
+    return _spmm_planned("spx_spmm_csr_f16_planned", plan, A, B, C, alpha, beta, stream, scratch)
 
 
 def spx_spmm_csr_variant(B: torch.Tensor, C: torch.Tensor) -> str:

@@ -413,6 +413,39 @@ spx_status spx_spmm_csr_f16(int32_t M, int32_t K, int64_t nnz, const int32_t* ro
                             const uint16_t* val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                             float* C, int64_t ldc, spx_stream_t stream);
 
+/*
+ * Planned SpMM for skewed rows.  [SpMM-ops] §2.4 (a long row is split, its
+ * partial sums combined in a second pass) applied to C = alpha*A*B + beta*C:
+ * the rows the SpMV plan `plan` (spx_plan_csr of the same matrix, uploaded)
+ * classes as long -- longer than its pack_max -- are not walked by one
+ * sub-warp.  A CTA row (length <= cta_max) is reduced by a whole CTA; a split
+ * row's segments of seg_nnz nonzeros each write a partial row to scratch, and
+ * a fix-up launch adds them in segment order and applies alpha/beta.  All
+ * other rows run as in spx_spmm_csr.  Every sum is in a fixed order, so the
+ * result is reproducible run to run (it may differ in rounding from
+ * spx_spmm_csr, which sums a long row in one sequence).
+ * scratch: spx_spmm_csr_planned_scratch_bytes(plan, N) bytes (slots x N
+ * floats, 4-byte aligned; none without split rows).  Needs N, ldb, ldc
+ * multiples of 4, B 16-byte (fp32) or 8-byte (16-bit) and C 16-byte aligned
+ * (SPX_ERR_UNSUPPORTED / SPX_ERR_ALIGN otherwise); SPX_ERR_ARG for a plan of
+ * another matrix or too little scratch, SPX_ERR_NOT_READY before the upload.
+ * Launches: 1 to 3.  The _bf16 and _f16 forms take 16-bit A values and B as
+ * spx_spmm_csr_bf16 / spx_spmm_csr_f16 do.
+ */
+size_t spx_spmm_csr_planned_scratch_bytes(const spx_plan* plan, int32_t N);
+spx_status spx_spmm_csr_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                                const int32_t* col, const float* val, int32_t N, const float* B, int64_t ldb,
+                                float alpha, float beta, float* C, int64_t ldc, void* scratch, size_t scratch_bytes,
+                                spx_stream_t stream);
+spx_status spx_spmm_csr_bf16_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz,
+                                     const int32_t* row_ptr, const int32_t* col, const uint16_t* val, int32_t N,
+                                     const uint16_t* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                                     void* scratch, size_t scratch_bytes, spx_stream_t stream);
+spx_status spx_spmm_csr_f16_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz,
+                                    const int32_t* row_ptr, const int32_t* col, const uint16_t* val, int32_t N,
+                                    const uint16_t* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                                    void* scratch, size_t scratch_bytes, spx_stream_t stream);
+
 /* Which SpMM variant spx_spmm_csr would launch for these arguments:
    0 = small-N, 1 = float4 with N <= 128, 2 = float4 with N > 128, 3 = scalar. */
 int32_t spx_spmm_csr_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t ldc);

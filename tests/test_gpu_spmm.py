@@ -189,3 +189,90 @@ def test_f16_rejects_unsupported_shapes():
     with pytest.raises(spx.SpxError) as e:
         spx.spx_spmm_csr_f16(A, dev(np.zeros((1, 6), np.int16)), dev(np.zeros((1, 6), np.float32)))
     assert e.value.code == -7  # N not a multiple of 4
+
+
+def _skewed(seed, M, K, lmax):
+    """Power-law rows up to lmax (< K) entries (a few long ones), distinct uniform columns."""
+    assert lmax < K
+    L, _ = synth.lengths_zipf(seed, M, 2.1, lmax, 12.0)
+    row, col = synth.cols_uniform(seed, K, L)
+    val = synth.uniform(seed, synth.T_VAL, row.size)
+    return oracle.build_csr(M, K, row, col, val)
+
+
+PLAN_OPTS = [None, {"pack_max": 64, "cta_max": 1000, "seg_nnz": 500},
+             {"block_nnz": 1024, "pack_max": 8, "cta_max": 8, "seg_nnz": 3, "lanes_div": 0}]
+
+
+@pytest.mark.parametrize("opts", PLAN_OPTS)
+@pytest.mark.parametrize("N,alpha,beta", [(4, 1.0, 0.0), (32, 1.0, 0.0), (32, -0.5, 2.0), (128, 1.0, 0.0),
+                                          (256, 0.75, -1.0), (20, 1.0, 0.5)])
+def test_planned_skewed_rows(opts, N, alpha, beta):
+    """Planned SpMM on power-law rows (CTA rows and split rows under several plans) against the fp64 oracle."""
+    M, K = 3000, 20000
+    rp, col, val = _skewed(31, M, K, 9000)
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, opts)
+    assert plan.info["cta_rows"] + plan.info["split_rows"] > 0
+    Bm = synth.uniform(N + 2, synth.T_B, K * N).reshape(K, N)
+    C0 = synth.uniform(N + 3, synth.T_Y, M * N).reshape(M, N)
+    Cd = dev(C0)
+    spx.spx_spmm_csr_planned(plan, A, dev(Bm), Cd, alpha, beta)
+    ref, bound = oracle.spmm(M, rp, col, val, Bm, alpha, beta, C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, what=f"planned N={N} opts={opts}")
+    C2 = dev(C0)
+    spx.spx_spmm_csr_planned(plan, A, dev(Bm), C2, alpha, beta)
+    assert torch.equal(Cd, C2)  # fixed-order sums: reproducible
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_planned_16bit(fmt):
+    M, K, N = 2000, 12000, 64
+    rp, col, val = _skewed(32, M, K, 6000)
+    if fmt == "bf16":
+        vb, Bb = synth.to_bf16_bits(val), synth.to_bf16_bits(synth.uniform(5, synth.T_B, K * N)).reshape(K, N)
+        vf, Bf, fn = synth.bf16_bits_to_f32(vb), synth.bf16_bits_to_f32(Bb).reshape(K, N), spx.spx_spmm_csr_bf16_planned
+    else:
+        vb, Bb = val.astype(np.float16), synth.uniform(5, synth.T_B, K * N).astype(np.float16).reshape(K, N)
+        vf, Bf, fn = vb.astype(np.float32), Bb.astype(np.float32), spx.spx_spmm_csr_f16_planned
+    A = spx.Csr(M, K, dev(rp), dev(col), dev(vb.view(np.int16)))
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, {"pack_max": 32, "cta_max": 500, "seg_nnz": 400})
+    Cd = torch.empty(M, N, device="cuda")
+    fn(plan, A, dev(Bb.view(np.int16)), Cd)
+    ref, bound = oracle.spmm(M, rp, col, vf, Bf)
+    assert_within(Cd.cpu().numpy(), ref, bound, what=f"planned {fmt}")
+
+
+def test_planned_errors():
+    M, K = 300, 300
+    rp, col, val = _skewed(33, M, K, 250)
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, {"pack_max": 16, "cta_max": 32, "seg_nnz": 8})
+    B, C = torch.zeros(K, 32, device="cuda"), torch.zeros(M, 32, device="cuda")
+    other = spx.spx_plan_csr(M + 1, K, A.nnz, torch.cat([A.row_ptr, A.row_ptr[-1:]]))
+    cases = [(lambda: spx.spx_spmm_csr_planned(other, A, B, C), -1),                               # another matrix
+             (lambda: spx.spx_spmm_csr_planned(plan, A, B, C, scratch=torch.zeros(1, device="cuda")), -1),
+             (lambda: spx.spx_spmm_csr_planned(plan, A, B[:, :6], C[:, :6]), -7),                  # N % 4
+             (lambda: spx.spx_spmm_csr_planned(spx.Plan(M, K, A.nnz, A.row_ptr, upload=False), A, B, C), -10)]
+    for f, code in cases:
+        with pytest.raises(spx.SpxError) as e:
+            f()
+        assert e.value.code == code
+
+
+@pytest.mark.slow
+def test_planned_power_law_full_size_sampled():
+    """The 4,194,304-row power-law matrix (rows up to 200,000) at N = 32, sampled rows incl. every long row."""
+    c = synth.power_law_rows()
+    M, K = c["M"], c["K"]
+    rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr)
+    N = 32
+    Bm = synth.uniform(7, synth.T_B, K * N).reshape(K, N)
+    Cd = torch.empty(M, N, device="cuda")
+    spx.spx_spmm_csr_planned(plan, A, dev(Bm), Cd)
+    L = np.diff(rp)
+    rows = np.unique(np.concatenate([np.nonzero(L > plan.opts["pack_max"])[0], np.arange(0, M, 4099)])).astype(np.int32)
+    ref, bound = oracle.spmm(M, rp, col, val, Bm, rows=rows)
+    assert_within(Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy(), ref, bound, what="planned power-law")
