@@ -8,7 +8,7 @@ fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|
-                                spmm32-f16|spmm128-f16|spmm32-power-law|bsr|wcsr]
+                                spmm32-f16|spmm128-f16|spmm32-power-law|bsr|wcsr|wcsr-skewed]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -174,6 +174,8 @@ def make_workload(name: str, rows: int = 0):
         c = synth.block_sparse()
     elif name == "wcsr":
         c = synth.window_pool()
+    elif name == "wcsr-skewed":  # every 16th window ~6.5x wider: the planned call splits it
+        c = synth.window_pool_skewed()
     else:
         raise SystemExit(f"unknown workload {name}")
     c["workload"] = name
@@ -201,7 +203,7 @@ def accounting(c):
     if w.startswith("spmm"):
         N = c["N"]
         return 2 * nnz * N, 8 * nnz + 4 * (M + 1) + 4 * K * N + 4 * M * N
-    if w == "wcsr":  # flops of the stored chunks (what the tensor cores execute); bytes of the WCSR arrays
+    if w.startswith("wcsr"):  # flops of the stored chunks (what the tensor cores execute); bytes of the WCSR arrays
         nch, N = c["nchunks"], c["N"]
         return 2 * nch * 4096 * N, 2 * nch * 4096 + 4 * 64 * nch + 4 * (M // 64 + 1) + 2 * K * N + 4 * M * N
     if w == "bsr":
@@ -227,14 +229,14 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     c = make_workload(args.workload, args.rows)
-    flops, abytes = accounting(c) if args.workload != "wcsr" else (None, None)  # wcsr: after its build
+    flops, abytes = accounting(c) if not args.workload.startswith("wcsr") else (None, None)  # wcsr: after its build
     M, K = c["M"], c["K"]
     w = c["workload"]
     stream = torch.cuda.Stream(device=dev)
     timings = {}
 
     t0 = time.perf_counter()
-    if w in ("bsr", "wcsr"):
+    if w in ("bsr", "wcsr", "wcsr-skewed"):
         rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val_bf16"])
     elif w == "power-law-coo":
         rp = col = val = None  # the generator's triplets are already sorted by row
@@ -493,7 +495,7 @@ def run_ours(args, rank, world):
                 Co.copy_(C, non_blocking=True)
 
         extra = {"variant": spx.spx_spmm_csr_variant(B, C)}
-    elif w == "wcsr":
+    elif w.startswith("wcsr"):
         t0 = time.perf_counter()
         wp, wc, wv, fill = spx.spx_build_wcsr(M, K, rp, col, val)
         timings["build_wcsr_ms"] = 1e3 * (time.perf_counter() - t0)
@@ -508,8 +510,18 @@ def run_ours(args, rank, world):
         C = torch.empty(M, c["N"], device=dev)
         src = source_hash("spx_wcsr.cu", "spx_tc.cuh")
 
+        wplan = spx.WcsrPlan(M, c["nchunks"], d_wp, stream=stream) if w == "wcsr-skewed" else None
+        wscratch = (torch.empty(max(4, spx._lib().spx_spmm_wcsr_planned_scratch_bytes(wplan.handle, c["N"]) // 4),
+                                device=dev) if wplan else None)
+
+        def wcsr_call():
+            if wplan is None:
+                spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+            else:
+                spx.spx_spmm_wcsr_planned(wplan, M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream, scratch=wscratch)
+
         def run():
-            spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+            wcsr_call()
 
         Bh = torch.from_numpy(c["B_bf16"].view(np.int16)).pin_memory()
         Co = torch.empty(M, c["N"]).pin_memory()
@@ -518,11 +530,23 @@ def run_ours(args, rank, world):
         def e2e_run():
             with torch.cuda.stream(stream):
                 Bm.copy_(Bh, non_blocking=True)
-                spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+                wcsr_call()
                 Co.copy_(C, non_blocking=True)
 
         extra = {"fill_ratio": fill, "nchunks": c["nchunks"], "useful_flops": 2 * int(c["row"].size) * c["N"],
                  "useful_gflops": None}
+        if wplan is not None:  # the same product without the task split, for comparison (untimed by the step)
+            extra["task_split"] = dict(wplan.info)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(5):
+                with torch.cuda.stream(stream):
+                    ev0.record(stream)
+                    spx.spx_spmm_wcsr(M, K, d_wp, d_wc, d_wv, Bm, C, stream=stream)
+                    ev1.record(stream)
+                ev1.synchronize()
+                ts.append(ev0.elapsed_time(ev1))
+            extra["unsplit_ms"] = round(sorted(ts)[2], 5)
     else:  # bsr
         t0 = time.perf_counter()
         brp, bcol, bval, fill = spx.spx_build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
@@ -683,9 +707,9 @@ def run_ours(args, rank, world):
 
     pk = peaks()
     gflops = job_throughput(flops, world, ms)
-    if w == "wcsr":
+    if w.startswith("wcsr"):
         extra["useful_gflops"] = round(extra["useful_flops"] / (ms * 1e-3) / 1e9, 1)
-    if w in ("bsr", "wcsr"):
+    if w in ("bsr", "wcsr", "wcsr-skewed"):
         ach = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["bf16"], 4), "peak_source": pk["src"] + " (bf16 dense, burst)"}
@@ -703,7 +727,7 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr") or w.endswith("bf16"))
+        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr", "wcsr-skewed") or w.endswith("bf16"))
         else "f16->f32" if w.endswith("-f16") else "f32",
         "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
@@ -734,7 +758,7 @@ def cpu_step_fn(c):
 
     w = c["workload"]
     M, K = c["M"], c["K"]
-    if w == "wcsr":
+    if w.startswith("wcsr"):
         import synth
         rp, col, val = row_major_csr(c, synth.bf16_bits_to_f32(c["val_bf16"]))
         rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every window
@@ -824,7 +848,7 @@ def main():
     ap.add_argument("--workload", default="power-law",
                     choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-f16",
                              "spmm128-f16", "spmm32-power-law", "spmm32-bf16",
-                             "spmm128-bf16", "bsr", "wcsr"])
+                             "spmm128-bf16", "bsr", "wcsr", "wcsr-skewed"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")
     ap.add_argument("--no-e2e", action="store_true")

@@ -64,12 +64,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int STAGES, int HALVES>
+template <int STAGES, int HALVES, bool TASKS>
 __global__ void __launch_bounds__(kThreads)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const int* __restrict__ win_ptr,
                      const int* __restrict__ win_col, const uint16_t* __restrict__ B, long long ldb,
                      float* __restrict__ C, long long ldc, int M, int K, float alpha, float beta,
-                     long long spin_limit) {
+                     long long spin_limit, const int4* __restrict__ tasks, float* __restrict__ partials, int N) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -89,9 +89,20 @@ __global__ void __launch_bounds__(kThreads)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * 128 * HALVES;
-    const int w = blockIdx.y;
-    const int g0 = __ldg(win_ptr + w);
-    const int nch = __ldg(win_ptr + w + 1) - g0;
+    // one window per CTA row of the grid, or (planned call) one task: a piece
+    // of a window's chunks {window, first chunk, chunks, partial slot or -1}
+    int w, g0, nch, slot = -1;
+    if (TASKS) {
+        const int4 t = tasks[blockIdx.y];
+        w = t.x;
+        g0 = t.y;
+        nch = t.z;
+        slot = t.w;
+    } else {
+        w = blockIdx.y;
+        g0 = __ldg(win_ptr + w);
+        nch = __ldg(win_ptr + w + 1) - g0;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -219,6 +230,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int hh = 0; hh < HALVES; ++hh) {
             float* cp = C + static_cast<long long>(w) * kWin * ldc + n0 + 128 * hh + 32 * q + lane;
+            // a piece of a split window writes its raw partial tile (1 * sum, exact; the fix-up applies alpha/beta)
+            const bool raw = TASKS && slot >= 0;
+            float* dst = raw ? partials + static_cast<long long>(slot) * kWin * N + n0 + 128 * hh + 32 * q + lane : cp;
+            const long long dstride = raw ? N : ldc;
+            const float ealpha = raw ? 1.f : alpha, ebeta = raw ? 0.f : beta;
             if (nch == 0) {
                 for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
             } else if (ok && !s_abort) {
@@ -230,9 +246,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (c0 + j < rows) {
-                            float* p = cp + static_cast<long long>(c0 + j) * ldc;
-                            const float acc = alpha * __uint_as_float(v[j]);
-                            __stcs(p, beta != 0.f ? acc + beta * *p : acc);
+                            float* p = dst + static_cast<long long>(c0 + j) * dstride;
+                            const float acc = ealpha * __uint_as_float(v[j]);
+                            __stcs(p, ebeta != 0.f ? acc + ebeta * *p : acc);
                         }
                     }
                 }
@@ -252,6 +268,24 @@ __global__ void __launch_bounds__(kThreads)
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols) : "memory");
+}
+
+// Split windows of a planned call: C rows of window w = alpha * (sum of its
+// pieces' partial tiles, in piece order) + beta * C.  One thread per (row of
+// the window, column): grid (column blocks, 64 rows, split windows).
+__global__ void __launch_bounds__(256) wcsr_fixup_kernel(const int4* __restrict__ splits, int nsplit,
+                                                        const float* __restrict__ partials, int M, int N, float alpha,
+                                                        float beta, float* C, long long ldc) {
+    const int n = blockIdx.x * 256 + threadIdx.x, r = blockIdx.y;
+    if (n >= N) return;
+    for (int i = blockIdx.z; i < nsplit; i += gridDim.z) {
+        const int4 sp = splits[i];  // {window, first slot, pieces, 0}
+        if (r >= M - sp.x * kWin) continue;
+        float s = 0.f;
+        for (int k = 0; k < sp.z; ++k) s += __ldcs(partials + (static_cast<long long>(sp.y + k) * kWin + r) * N + n);
+        float* q = C + (static_cast<long long>(sp.x) * kWin + r) * ldc + n;
+        *q = beta != 0.f ? alpha * s + beta * *q : alpha * s;
+    }
 }
 
 __global__ void wcsr_scale_kernel(float* C, long long ldc, int M, int N, float beta) {
@@ -320,6 +354,102 @@ spx_status build_wcsr_host(int32_t M, int32_t K, const int32_t* rp, const int32_
     return SPX_OK;
 }
 
+constexpr int32_t kDefaultTaskChunks = 16;  // chunks per task before a window is split
+constexpr uint64_t kWcsrPlanMagic = 0x5350585f57504c4eull;  // "SPX_WPLN"
+
+}  // namespace
+
+struct spx_wcsr_plan {
+    int32_t M = 0;
+    int64_t nchunks = 0;
+    int32_t max_chunks = 0;
+    std::vector<int32_t> tasks;   // 4 per task: window, first chunk, chunks, partial slot (-1: the whole window)
+    std::vector<int32_t> splits;  // 4 per split window: window, first slot, pieces, 0
+    int64_t slots = 0;
+    size_t table_bytes = 0;
+    const void* d_table = nullptr;  // caller-owned copy: tasks, then splits
+    uint64_t magic = 0;
+};
+
+namespace {
+
+inline bool wplan_ok(const spx_wcsr_plan* P) { return P && P->magic == kWcsrPlanMagic; }
+
+// One WCSR product: all windows (P == nullptr), or the plan's tasks followed
+// by the fix-up of its split windows.
+spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunks, const int32_t* win_ptr,
+                    const int32_t* win_col, const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb,
+                    float alpha, float beta, float* C, int64_t ldc, void* scratch, size_t scratch_bytes,
+                    cudaStream_t st) {
+    if (M < 0 || K < 0 || N < 0 || nchunks < 0) return SPX_ERR_ARG;
+    if (nchunks * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (N % 128) return SPX_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (!win_ptr || !C || (nchunks > 0 && (!win_col || !win_val || !B))) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (ldb % 8 || !spx_aligned(win_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
+        !spx_aligned(win_ptr, 4) || !spx_aligned(win_col, 4))
+        return SPX_ERR_ALIGN;
+    const int W = static_cast<int>((static_cast<int64_t>(M) + kWin - 1) / kWin);
+    const int64_t ntasks = P ? static_cast<int64_t>(P->tasks.size() / 4) : W;
+    const int nsplit = P ? static_cast<int>(P->splits.size() / 4) : 0;
+    if (ntasks > 65535) return SPX_ERR_UNSUPPORTED;  // windows (tasks) map to gridDim.y
+    const int4* tasks = P ? static_cast<const int4*>(P->d_table) : nullptr;
+    const int4* splits = tasks ? tasks + ntasks : nullptr;
+    float* partials = static_cast<float*>(scratch);
+    if (nsplit > 0) {
+        const size_t need = sizeof(float) * static_cast<size_t>(P->slots) * kWin * static_cast<size_t>(N);
+        if (!scratch || scratch_bytes < need) return SPX_ERR_ARG;
+        if (!spx_aligned(scratch, 16)) return SPX_ERR_ALIGN;
+    }
+    if (nchunks == 0) {
+        dim3 grid((N + 255) / 256, M < 65535 ? M : 65535);
+        wcsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, M, N, beta);
+        spx_note_launches(1);
+        return spx_cuda_status(cudaGetLastError());
+    }
+    CUtensorMap tmA;
+    if (!make_map(&tmA, win_val, kWin, static_cast<uint64_t>(nchunks) * kWin, kWin * 2)) return SPX_ERR_CUDA;
+    // Variant: 128-column tiles with a 2-deep ring (default: four CTAs per SM,
+    // measured fastest), "s3" / "s4" deeper rings, "wide" 256-column tiles
+    // with a 2-deep ring (N a multiple of 256); SPX_WCSR_VARIANT overrides.
+    static const int env_variant = [] {  // read once, thread-safe
+        int v = 2;
+        if (const char* e = std::getenv("SPX_WCSR_VARIANT")) {
+            if (!std::strcmp(e, "wide")) v = 1;
+            else if (!std::strcmp(e, "s3")) v = 3;
+            else if (!std::strcmp(e, "s4")) v = 4;
+        }
+        return v;
+    }();
+    const int variant = env_variant == 1 && N % 256 ? 2 : env_variant;  // per call: 256-column tiles need N % 256 == 0
+    switch (variant) {
+#define SPX_WCSR_LAUNCH(S, H, T)                                                                               \
+    do {                                                                                                       \
+        if (set_smem_limit(wcsr_spmm_kernel<S, H, T>, smem_bytes<S, H>()) != cudaSuccess) return SPX_ERR_CUDA; \
+        wcsr_spmm_kernel<S, H, T><<<dim3(N / (128 * H), static_cast<unsigned>(ntasks)), kThreads,              \
+                                    smem_bytes<S, H>(), st>>>(tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, \
+                                                              beta, kSpinLimit, tasks, partials, N);           \
+    } while (0)
+#define SPX_WCSR(S, H, V)                                                                                      \
+    case V:                                                                                                    \
+        if (tasks) SPX_WCSR_LAUNCH(S, H, true);                                                                \
+        else SPX_WCSR_LAUNCH(S, H, false);                                                                     \
+        break;
+        SPX_WCSR(2, 2, 1) SPX_WCSR(2, 1, 2) SPX_WCSR(3, 1, 3) SPX_WCSR(4, 1, 4)
+#undef SPX_WCSR
+#undef SPX_WCSR_LAUNCH
+    }
+    uint64_t launches = 1;
+    if (nsplit > 0) {
+        wcsr_fixup_kernel<<<dim3((N + 255) / 256, kWin, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(
+            splits, nsplit, partials, M, N, alpha, beta, C, ldc);
+        ++launches;
+    }
+    spx_note_launches(launches);
+    return spx_cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 
 int spx_wcsr_error_take() {
@@ -355,52 +485,127 @@ spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const in
 spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* win_ptr, const int32_t* win_col,
                          const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                          float* C, int64_t ldc, spx_stream_t stream) {
-    if (M < 0 || K < 0 || N < 0 || nchunks < 0) return SPX_ERR_ARG;
+    return wcsr_run(nullptr, M, K, nchunks, win_ptr, win_col, win_val, N, B, ldb, alpha, beta, C, ldc, nullptr, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+spx_status spx_wcsr_plan_build(int32_t M, int64_t nchunks, const int32_t* win_ptr, spx_loc where, int32_t max_chunks,
+                               spx_wcsr_plan** out) {
+    if (!out) return SPX_ERR_ARG;
+    *out = nullptr;
+    if (M < 0 || nchunks < 0 || !win_ptr || max_chunks < 0) return SPX_ERR_ARG;
     if (nchunks * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (N % 128) return SPX_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0) return SPX_OK;
-    if (!win_ptr || !C || (nchunks > 0 && (!win_col || !win_val || !B))) return SPX_ERR_ARG;
-    if (ldb < N || ldc < N) return SPX_ERR_ARG;
-    if (ldb % 8 || !spx_aligned(win_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
-        !spx_aligned(win_ptr, 4) || !spx_aligned(win_col, 4))
-        return SPX_ERR_ALIGN;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int W = static_cast<int>((static_cast<int64_t>(M) + kWin - 1) / kWin);
-    if (W > 65535) return SPX_ERR_UNSUPPORTED;  // windows map to gridDim.y
-    if (nchunks == 0) {
-        dim3 grid((N + 255) / 256, M < 65535 ? M : 65535);
-        wcsr_scale_kernel<<<grid, 256, 0, st>>>(C, ldc, M, N, beta);
-        spx_note_launches(1);
-        return spx_cuda_status(cudaGetLastError());
+    const int64_t W = (static_cast<int64_t>(M) + kWin - 1) / kWin;
+    std::vector<int32_t> wp;
+    try {
+        wp.resize(static_cast<size_t>(W) + 1);
+    } catch (const std::bad_alloc&) {
+        return SPX_ERR_NOMEM;
     }
-    CUtensorMap tmA;
-    if (!make_map(&tmA, win_val, kWin, static_cast<uint64_t>(nchunks) * kWin, kWin * 2)) return SPX_ERR_CUDA;
-    // Variant: 128-column tiles with a 2-deep ring (default: four CTAs per SM,
-    // measured fastest), "s3" / "s4" deeper rings, "wide" 256-column tiles
-    // with a 2-deep ring (N a multiple of 256); SPX_WCSR_VARIANT overrides.
-    static const int env_variant = [] {  // read once, thread-safe
-        int v = 2;
-        if (const char* e = std::getenv("SPX_WCSR_VARIANT")) {
-            if (!std::strcmp(e, "wide")) v = 1;
-            else if (!std::strcmp(e, "s3")) v = 3;
-            else if (!std::strcmp(e, "s4")) v = 4;
+    if (where == SPX_DEVICE) {
+        if (cudaMemcpy(wp.data(), win_ptr, sizeof(int32_t) * wp.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return SPX_ERR_CUDA;
+    } else if (where == SPX_HOST) {
+        std::memcpy(wp.data(), win_ptr, sizeof(int32_t) * wp.size());
+    } else {
+        return SPX_ERR_ARG;
+    }
+    if (wp[0] != 0 || wp[W] != nchunks) return SPX_ERR_ARG;
+    for (int64_t w = 0; w < W; ++w)
+        if (wp[w + 1] < wp[w]) return SPX_ERR_NOT_SORTED;
+    spx_wcsr_plan* P = new (std::nothrow) spx_wcsr_plan();
+    if (!P) return SPX_ERR_NOMEM;
+    P->M = M;
+    P->nchunks = nchunks;
+    P->max_chunks = max_chunks > 0 ? max_chunks : kDefaultTaskChunks;
+    try {
+        for (int64_t w = 0; w < W; ++w) {
+            const int32_t g0 = wp[w], nch = wp[w + 1] - wp[w];
+            if (nch <= P->max_chunks) {
+                P->tasks.insert(P->tasks.end(), {static_cast<int32_t>(w), g0, nch, -1});
+                continue;
+            }
+            const int32_t np = (nch + P->max_chunks - 1) / P->max_chunks, q = nch / np, r = nch % np;
+            if (P->slots + np > kI32Max) {
+                delete P;
+                return SPX_ERR_INDEX_RANGE;
+            }
+            P->splits.insert(P->splits.end(), {static_cast<int32_t>(w), static_cast<int32_t>(P->slots), np, 0});
+            int32_t start = g0;
+            for (int32_t k = 0; k < np; ++k) {  // balanced pieces in chunk order
+                const int32_t len = q + (k < r ? 1 : 0);
+                P->tasks.insert(P->tasks.end(), {static_cast<int32_t>(w), start, len, static_cast<int32_t>(P->slots + k)});
+                start += len;
+            }
+            P->slots += np;
         }
-        return v;
-    }();
-    const int variant = env_variant == 1 && N % 256 ? 2 : env_variant;  // per call: 256-column tiles need N % 256 == 0
-    switch (variant) {
-#define SPX_WCSR(S, H, V)                                                                                      \
-    case V: {                                                                                                  \
-        if (set_smem_limit(wcsr_spmm_kernel<S, H>, smem_bytes<S, H>()) != cudaSuccess) return SPX_ERR_CUDA;    \
-        wcsr_spmm_kernel<S, H><<<dim3(N / (128 * H), W), kThreads, smem_bytes<S, H>(), st>>>(                  \
-            tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit);                             \
-        break;                                                                                                 \
+    } catch (const std::bad_alloc&) {
+        delete P;
+        return SPX_ERR_NOMEM;
     }
-        SPX_WCSR(2, 2, 1) SPX_WCSR(2, 1, 2) SPX_WCSR(3, 1, 3) SPX_WCSR(4, 1, 4)
-#undef SPX_WCSR
-    }
-    spx_note_launches(1);
-    return spx_cuda_status(cudaGetLastError());
+    P->table_bytes = sizeof(int32_t) * (P->tasks.size() + P->splits.size());
+    P->magic = kWcsrPlanMagic;
+    *out = P;
+    return SPX_OK;
+}
+
+spx_status spx_wcsr_plan_info(const spx_wcsr_plan* P, spx_wcsr_plan_info_t* out) {
+    if (!wplan_ok(P) || !out) return SPX_ERR_ARG;
+    out->windows = (static_cast<int64_t>(P->M) + kWin - 1) / kWin;
+    out->tasks = static_cast<int64_t>(P->tasks.size() / 4);
+    out->split_windows = static_cast<int64_t>(P->splits.size() / 4);
+    out->slots = P->slots;
+    out->table_bytes = P->table_bytes;
+    out->max_chunks = P->max_chunks;
+    return SPX_OK;
+}
+
+spx_status spx_wcsr_plan_get_tasks(const spx_wcsr_plan* P, int32_t* tasks, int32_t* splits) {
+    if (!wplan_ok(P)) return SPX_ERR_ARG;
+    if (tasks && !P->tasks.empty()) std::memcpy(tasks, P->tasks.data(), sizeof(int32_t) * P->tasks.size());
+    if (splits && !P->splits.empty()) std::memcpy(splits, P->splits.data(), sizeof(int32_t) * P->splits.size());
+    return SPX_OK;
+}
+
+spx_status spx_wcsr_plan_upload(spx_wcsr_plan* P, void* table, size_t table_bytes, spx_stream_t stream) {
+    if (!wplan_ok(P)) return SPX_ERR_ARG;
+    if (P->table_bytes == 0) return SPX_OK;
+    if (!table || table_bytes < P->table_bytes) return SPX_ERR_ARG;
+    if (!spx_aligned(table, 16)) return SPX_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* d = static_cast<char*>(table);
+    cudaError_t e = cudaMemcpyAsync(d, P->tasks.data(), sizeof(int32_t) * P->tasks.size(), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !P->splits.empty())
+        e = cudaMemcpyAsync(d + sizeof(int32_t) * P->tasks.size(), P->splits.data(), sizeof(int32_t) * P->splits.size(),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    P->d_table = table;
+    return SPX_OK;
+}
+
+spx_status spx_wcsr_plan_destroy(spx_wcsr_plan* P) {
+    if (!P) return SPX_OK;
+    if (!wplan_ok(P)) return SPX_ERR_ARG;
+    P->magic = 0;
+    delete P;
+    return SPX_OK;
+}
+
+size_t spx_spmm_wcsr_planned_scratch_bytes(const spx_wcsr_plan* P, int32_t N) {
+    if (!wplan_ok(P) || N < 0) return 0;
+    return sizeof(float) * static_cast<size_t>(P->slots) * kWin * static_cast<size_t>(N);
+}
+
+spx_status spx_spmm_wcsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunks,
+                                 const int32_t* win_ptr, const int32_t* win_col, const uint16_t* win_val, int32_t N,
+                                 const uint16_t* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                                 void* scratch, size_t scratch_bytes, spx_stream_t stream) {
+    if (!wplan_ok(P)) return SPX_ERR_ARG;
+    if (P->M != M || P->nchunks != nchunks) return SPX_ERR_ARG;
+    if (P->table_bytes > 0 && !P->d_table) return SPX_ERR_NOT_READY;
+    return wcsr_run(P, M, K, nchunks, win_ptr, win_col, win_val, N, B, ldb, alpha, beta, C, ldc, scratch,
+                    scratch_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -68,6 +68,11 @@ class SellInfo(ctypes.Structure):
                 ("opts", SellOpts)]
 
 
+class WcsrPlanInfo(ctypes.Structure):
+    _fields_ = [("windows", ctypes.c_int64), ("tasks", ctypes.c_int64), ("split_windows", ctypes.c_int64),
+                ("slots", ctypes.c_int64), ("table_bytes", ctypes.c_size_t), ("max_chunks", ctypes.c_int32)]
+
+
 _LIB = None
 
 
@@ -133,6 +138,14 @@ def _lib():
             "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
                                 ctypes.c_int, vp], ctypes.c_int),
             "spx_spmm_wcsr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+            "spx_wcsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
+            "spx_wcsr_plan_info": ([vp, ctypes.POINTER(WcsrPlanInfo)], ctypes.c_int),
+            "spx_wcsr_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
+            "spx_wcsr_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
+            "spx_wcsr_plan_destroy": ([vp], ctypes.c_int),
+            "spx_spmm_wcsr_planned_scratch_bytes": ([vp, i32], sz),
+            "spx_spmm_wcsr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                      ctypes.c_int),
             "spx_gather_probe_blocks": ([], ctypes.c_int32),
             "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
@@ -303,6 +316,62 @@ def spx_spmm_wcsr(M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor, 
     nch = win_col.numel() // 64
     _check(_lib().spx_spmm_wcsr(M, K, nch, _ptr(win_ptr), _ptr(win_col), _ptr(win_val), N, _ptr(B), B.stride(0),
                                 float(alpha), float(beta), _ptr(C), C.stride(0), _stream(stream)), "spx_spmm_wcsr")
+    return C
+
+
+class WcsrPlan:
+    """Owns an spx_wcsr_plan* (the WCSR task split) and its uploaded device table."""
+
+    def __init__(self, M: int, nchunks: int, win_ptr, max_chunks: int = 0, device=None, upload=True, stream=None):
+        lib = _lib()
+        h = ctypes.c_void_p()
+        _check(lib.spx_wcsr_plan_build(M, nchunks, _ptr(win_ptr), _where(win_ptr), int(max_chunks), ctypes.byref(h)),
+               "spx_wcsr_plan_build")
+        self.handle, self.M, self.nchunks = h, M, nchunks
+        info = WcsrPlanInfo()
+        _check(lib.spx_wcsr_plan_info(h, ctypes.byref(info)), "spx_wcsr_plan_info")
+        self.info = {f: getattr(info, f) for f, _ in WcsrPlanInfo._fields_}
+        self.table = None
+        if upload:
+            dev = device or (win_ptr.device if isinstance(win_ptr, torch.Tensor) and win_ptr.is_cuda else "cuda")
+            self.table = torch.empty(max(4, (self.info["table_bytes"] + 15) // 16 * 4), dtype=torch.int32, device=dev)
+            _check(lib.spx_wcsr_plan_upload(h, _ptr(self.table), self.table.numel() * 4, _stream(stream)),
+                   "spx_wcsr_plan_upload")
+
+    def tasks(self):
+        t = np.empty((self.info["tasks"], 4), np.int32)
+        sp = np.empty((self.info["split_windows"], 4), np.int32)
+        _check(_lib().spx_wcsr_plan_get_tasks(self.handle, _ptr(t), _ptr(sp)), "spx_wcsr_plan_get_tasks")
+        return t, sp
+
+    def close(self):
+        if self.handle:
+            _lib().spx_wcsr_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spx_spmm_wcsr_planned(plan: WcsrPlan, M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor,
+                          win_val: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+                          beta: float = 0.0, stream=None, scratch: torch.Tensor | None = None):
+    """spx_spmm_wcsr with the plan's wide windows split into pieces (partial tiles + fixed-order fix-up)."""
+    N = B.shape[1]
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
+    lib = _lib()
+    need = int(lib.spx_spmm_wcsr_planned_scratch_bytes(plan.handle, N))
+    if scratch is None:
+        scratch = torch.empty(max(4, (need + 15) // 16 * 4), dtype=torch.float32, device=C.device)
+    nch = win_col.numel() // 64
+    _check(lib.spx_spmm_wcsr_planned(plan.handle, M, K, nch, _ptr(win_ptr), _ptr(win_col), _ptr(win_val), N, _ptr(B),
+                                     B.stride(0), float(alpha), float(beta), _ptr(C), C.stride(0), _ptr(scratch),
+                                     scratch.numel() * scratch.element_size(), _stream(stream)),
+           "spx_spmm_wcsr_planned")
     return C
 
 

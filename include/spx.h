@@ -614,6 +614,45 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
                          const uint16_t* win_val, int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta,
                          float* C, int64_t ldc, spx_stream_t stream);
 
+/*
+ * WCSR task split.  [AsyncSparse] §4.1 (the WCSR kernel splits windows with
+ * many chunks over several thread blocks so that no block carries a whole
+ * wide window).  spx_wcsr_plan_build reads win_ptr (host or device, once) and
+ * cuts every window with more than max_chunks chunks (max_chunks <= 0: 16)
+ * into balanced pieces of consecutive chunks; the other windows stay whole.
+ * tasks: {window, first chunk, chunks, partial slot or -1 for a whole
+ * window}; splits: {window, first slot, pieces, 0}.  The table (tasks then
+ * splits, table_bytes, 16-byte aligned caller memory) goes to the device with
+ * spx_wcsr_plan_upload.  spx_spmm_wcsr_planned runs one CTA per task and
+ * column tile; a whole window writes C as spx_spmm_wcsr does, a piece writes
+ * its raw 64 x N partial tile to scratch (spx_spmm_wcsr_planned_scratch_bytes:
+ * slots x 64 x N floats, 16-byte aligned), and a fix-up launch adds a split
+ * window's pieces in piece order and applies alpha/beta -- no atomics, so the
+ * result is reproducible.  Errors: SPX_ERR_ARG (win_ptr[0] != 0 or
+ * win_ptr[W] != nchunks, a plan of another matrix, too little scratch),
+ * SPX_ERR_NOT_SORTED (win_ptr decreasing), SPX_ERR_NOT_READY (not uploaded),
+ * SPX_ERR_UNSUPPORTED (more than 65535 tasks), and those of spx_spmm_wcsr.
+ * Launches: 1, or 2 with split windows.
+ */
+typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side */
+typedef struct spx_wcsr_plan_info_t {
+    int64_t windows, tasks, split_windows, slots;
+    size_t table_bytes;
+    int32_t max_chunks;
+} spx_wcsr_plan_info_t;
+spx_status spx_wcsr_plan_build(int32_t M, int64_t nchunks, const int32_t* win_ptr, spx_loc where, int32_t max_chunks,
+                               spx_wcsr_plan** out);
+spx_status spx_wcsr_plan_info(const spx_wcsr_plan* plan, spx_wcsr_plan_info_t* out);
+/* Host copies of tasks[4 tasks] and splits[4 split_windows]; either may be NULL. */
+spx_status spx_wcsr_plan_get_tasks(const spx_wcsr_plan* plan, int32_t* tasks, int32_t* splits);
+spx_status spx_wcsr_plan_upload(spx_wcsr_plan* plan, void* table, size_t table_bytes, spx_stream_t stream);
+spx_status spx_wcsr_plan_destroy(spx_wcsr_plan* plan);
+size_t spx_spmm_wcsr_planned_scratch_bytes(const spx_wcsr_plan* plan, int32_t N);
+spx_status spx_spmm_wcsr_planned(const spx_wcsr_plan* plan, int32_t M, int32_t K, int64_t nchunks,
+                                 const int32_t* win_ptr, const int32_t* win_col, const uint16_t* win_val, int32_t N,
+                                 const uint16_t* B, int64_t ldb, float alpha, float beta, float* C, int64_t ldc,
+                                 void* scratch, size_t scratch_bytes, spx_stream_t stream);
+
 /* ------------------------------------------------------------ measurement */
 
 /*

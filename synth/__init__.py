@@ -271,3 +271,31 @@ def window_pool(seed: int = 6, M: int = 16384, K: int | None = None, win: int = 
     Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
     return dict(name=f"window-pool {M}x{K} windows {win} pool {pool} l~U{{{lmin}..{lmax}}} N={N}", M=M, K=K, N=N,
                 row=row, col=col, val_bf16=val, B_bf16=Bm)
+
+
+def window_pool_skewed(seed: int = 7, M: int = 16384, K: int | None = None, win: int = 64, pool: int = 512,
+                       big_pool: int = 8192, big_every: int = 16, lmin: int = 32, lmax: int = 96, N: int = 1024,
+                       sigma_a: float = 0.02, sigma_b: float = 1.0):
+    """window_pool with skewed windows: every `big_every`-th window draws its rows'
+    columns from a pool of `big_pool` columns instead of `pool`, so its union of
+    columns (and its WCSR chunk count) is many times larger."""
+    K = M if K is None else K
+    pool, big_pool = min(pool, K), min(big_pool, K)
+    W = (M + win - 1) // win
+    lengths = lengths_uniform(seed, M, lmin, min(lmax, pool))
+    big = (np.arange(M) // win) % big_every == 0
+    rs, ids = cols_uniform(seed, pool, np.where(big, 0, lengths).astype(np.int32))
+    rb, idb = cols_uniform(seed + 1, big_pool, np.where(big, lengths, 0).astype(np.int32))
+    pools = np.stack([permutation(seed, K, tag=1000 + w)[:pool] for w in range(W)]).astype(np.int32)
+    bigw = np.arange(0, W, big_every)
+    bpools = np.zeros((W, big_pool), np.int32)
+    for w in bigw:
+        bpools[w] = permutation(seed, K, tag=5000 + int(w))[:big_pool]
+    row = np.concatenate([rs, rb])
+    col = np.concatenate([pools[rs // win, ids], bpools[rb // win, idb]])
+    order = np.lexsort((col, row))
+    row, col = row[order].astype(np.int32), col[order].astype(np.int32)
+    val = normal_bf16(seed, T_VAL, row.size, sigma_a)
+    Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
+    return dict(name=f"window-pool skewed {M}x{K} windows {win} pools {pool}/{big_pool} (every {big_every}th) "
+                     f"l~U{{{lmin}..{lmax}}} N={N}", M=M, K=K, N=N, row=row, col=col, val_bf16=val, B_bf16=Bm)

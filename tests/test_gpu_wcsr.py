@@ -115,3 +115,72 @@ def test_window_pool_full_size_sampled():
                              rows=rows)
     assert_within(got, ref, bound, BF16_REL, BF16_ABS, what="window-pool")
     assert_within(got, ref, bound, 1e-5, 1e-6, what="window-pool fp32-level")
+
+
+def _skewed_wcsr(M, N, seed=7):
+    c = synth.window_pool_skewed(seed, M=M, N=N)
+    rp, col, val = oracle.build_csr(M, c["K"], c["row"], c["col"], c["val_bf16"])
+    wp, wc, wv, _ = oracle.build_wcsr(M, c["K"], rp, col, val)
+    return c, rp, col, val, wp, wc, wv
+
+
+@pytest.mark.parametrize("max_chunks", [0, 1, 4, 7])
+@pytest.mark.parametrize("N,alpha,beta", [(128, 1.0, 0.0), (256, -0.5, 1.5)])
+def test_planned_task_split(max_chunks, N, alpha, beta):
+    """Wide windows split into pieces (partial tiles + fixed-order fix-up) against the fp64
+    oracle; reproducible; equal within the bf16 bound to the unsplit call."""
+    M = 2048
+    c, rp, col, val, wp, wc, wv = _skewed_wcsr(M, N)
+    K = c["K"]
+    P = spx.WcsrPlan(M, wc.size // 64, torch.from_numpy(wp).cuda(), max_chunks=max_chunks)
+    assert P.info["split_windows"] > 0
+    C0 = synth.uniform(N, synth.T_Y, M * N).reshape(M, N)
+    dwp, dwc, dwv, dB = torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)), bits(c["B_bf16"])
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_wcsr_planned(P, M, K, dwp, dwc, dwv, dB, Cd, alpha, beta)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), alpha, beta,
+                             C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, rel=BF16_REL, ab=BF16_ABS, what=f"planned wcsr max={max_chunks}")
+    C2 = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_wcsr_planned(P, M, K, dwp, dwc, dwv, dB, C2, alpha, beta)
+    assert torch.equal(Cd, C2)
+    C3 = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_wcsr(M, K, dwp, dwc, dwv, dB, C3, alpha, beta)
+    assert_within(C3.cpu().numpy(), ref, bound, rel=BF16_REL, ab=BF16_ABS, what="unsplit wcsr")
+
+
+def test_planned_errors():
+    M, N = 256, 128
+    c, rp, col, val, wp, wc, wv = _skewed_wcsr(M, N)
+    K, nch = c["K"], wc.size // 64
+    dwp, dwc, dwv, dB = torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)), bits(c["B_bf16"])
+    C = torch.empty(M, N, device="cuda")
+    P = spx.WcsrPlan(M, nch, wp, max_chunks=2)
+    cases = [(lambda: spx.spx_spmm_wcsr_planned(spx.WcsrPlan(M, nch, wp, max_chunks=2, upload=False), M, K, dwp, dwc,
+                                                dwv, dB, C), -10),
+             (lambda: spx.spx_spmm_wcsr_planned(P, M, K, dwp, dwc, dwv, dB, C, scratch=torch.zeros(4, device="cuda")), -1),
+             (lambda: spx.spx_spmm_wcsr_planned(P, M - 64, K, dwp, dwc, dwv, dB, C[:M - 64]), -1)]
+    for f, code in cases:
+        with pytest.raises(spx.SpxError) as e:
+            f()
+        assert e.value.code == code
+
+
+@pytest.mark.slow
+def test_planned_skewed_full_size_sampled():
+    """The 16,384^2 skewed window-pool matrix at N = 1024 with the default split, two rows of every window."""
+    M, N = 16384, 1024
+    c, rp, col, val, wp, wc, wv = _skewed_wcsr(M, N)
+    K = c["K"]
+    P = spx.WcsrPlan(M, wc.size // 64, wp)
+    Cd = torch.empty(M, N, device="cuda")
+    spx.spx_spmm_wcsr_planned(P, M, K, torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)),
+                              bits(c["B_bf16"]), Cd)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    rows = np.sort(np.concatenate([np.arange(0, M, 64), np.arange(37, M, 64)])).astype(np.int32)
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), rows=rows)
+    got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
+    assert_within(got, ref, bound, rel=BF16_REL, ab=BF16_ABS, what="planned skewed full size")
