@@ -276,3 +276,28 @@ def test_planned_power_law_full_size_sampled():
     rows = np.unique(np.concatenate([np.nonzero(L > plan.opts["pack_max"])[0], np.arange(0, M, 4099)])).astype(np.int32)
     ref, bound = oracle.spmm(M, rp, col, val, Bm, rows=rows)
     assert_within(Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy(), ref, bound, what="planned power-law")
+
+
+def test_planned_without_long_rows_equals_plain():
+    """A plan whose rows are all short changes nothing: the planned call equals spx_spmm_csr bit for bit."""
+    M, K, N = 5000, 3000, 64
+    d = synth.random_coo(34, M, K, 0, 40)
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], d["val"])
+    A = csr_to_device(M, K, rp, col, val)
+    plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr)
+    assert plan.info["cta_rows"] == 0 and plan.info["split_rows"] == 0
+    Bm = dev(synth.uniform(35, synth.T_B, K * N).reshape(K, N))
+    C1, C2 = torch.empty(M, N, device="cuda"), torch.empty(M, N, device="cuda")
+    spx.spx_spmm_csr(A, Bm, C1, 2.0, 0.0)
+    spx.spx_spmm_csr_planned(plan, A, Bm, C2, 2.0, 0.0)
+    assert torch.equal(C1, C2)
+
+
+def test_planned_empty_matrix():
+    for M, K in ((0, 5), (7, 0), (7, 5)):
+        rp = np.zeros(M + 1, np.int32)
+        A = csr_to_device(M, K, rp, np.zeros(0, np.int32), np.zeros(0, np.float32))
+        plan = spx.spx_plan_csr(M, K, 0, A.row_ptr)
+        C = torch.full((M, 8), 3.0, device="cuda")
+        spx.spx_spmm_csr_planned(plan, A, torch.zeros(K, 8, device="cuda"), C, 1.0, 0.5)
+        assert torch.equal(C, torch.full((M, 8), 1.5, device="cuda"))

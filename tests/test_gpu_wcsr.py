@@ -184,3 +184,18 @@ def test_planned_skewed_full_size_sampled():
     ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), rows=rows)
     got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
     assert_within(got, ref, bound, rel=BF16_REL, ab=BF16_ABS, what="planned skewed full size")
+
+
+def test_planned_without_splits_equals_plain():
+    """A plan that splits no window runs the same tiles: equal to spx_spmm_wcsr bit for bit."""
+    M, N = 1024, 128
+    c = synth.window_pool(6, M=M, N=N)
+    rp, col, val = oracle.build_csr(M, c["K"], c["row"], c["col"], c["val_bf16"])
+    wp, wc, wv, _ = oracle.build_wcsr(M, c["K"], rp, col, val)
+    P = spx.WcsrPlan(M, wc.size // 64, wp, max_chunks=64)
+    assert P.info["split_windows"] == 0
+    args = (torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)), bits(c["B_bf16"]))
+    C1, C2 = torch.empty(M, N, device="cuda"), torch.empty(M, N, device="cuda")
+    spx.spx_spmm_wcsr(M, c["K"], *args, C1, 1.5, 0.0)
+    spx.spx_spmm_wcsr_planned(P, M, c["K"], *args, C2, 1.5, 0.0)
+    assert torch.equal(C1, C2)
