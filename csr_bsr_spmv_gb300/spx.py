@@ -176,13 +176,17 @@ def _ptr(t):
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
-        if t.numel() and not (t.is_contiguous() or (t.dim() == 2 and t.stride(1) == 1)):
+        if not t.numel():
+            return None
+        if not (t.is_contiguous() or (t.dim() == 2 and t.stride(1) == 1)):
             raise ValueError(f"array with strides {tuple(t.stride())} is not laid out densely")
-        return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+        return t.data_ptr()  # a plain address: the c_void_p argtypes take ints without building objects
     if isinstance(t, np.ndarray):
-        if t.size and not (t.flags.c_contiguous or (t.ndim == 2 and t.strides[1] == t.itemsize)):
+        if not t.size:
+            return None
+        if not (t.flags.c_contiguous or (t.ndim == 2 and t.strides[1] == t.itemsize)):
             raise ValueError(f"array with strides {t.strides} is not laid out densely")
-        return t.ctypes.data_as(ctypes.c_void_p) if t.size else None
+        return t.ctypes.data  # the caller keeps the array alive for the call
     raise TypeError(type(t))
 
 
@@ -191,12 +195,18 @@ def _require(cond: bool, what: str):
         raise ValueError(what)
 
 
+_CUDA_OK = None
+
+
 def _stream(stream=None):
+    global _CUDA_OK
     if stream is None:
-        if not torch.cuda.is_available():
+        if _CUDA_OK is None:
+            _CUDA_OK = torch.cuda.is_available()
+        if not _CUDA_OK:
             return None
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream) if stream.cuda_stream else None
+    return stream.cuda_stream or None  # the raw handle (0: the legacy default stream)
 
 
 def _where(*arrays) -> int:
