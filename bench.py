@@ -8,7 +8,8 @@ fix-up launch.  Format conversion and planning are timed once, separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload power-law|power-law-coo|power-law-sell|uniform|dual|spmm32|spmm128|spmm32-bf16|spmm128-bf16|
-                                spmm32-f16|spmm128-f16|spmm32-power-law|bsr|wcsr|wcsr-skewed]
+                                spmm32-f16|spmm128-f16|spmm32-power-law|bsr|bsr-skewed|wcsr|
+                                wcsr-skewed]
 
 Prints one JSON line.  Under torchrun each rank runs an independent replica of
 the workload (the products shard by rows with no exchange; "weak" scaling);
@@ -172,6 +173,8 @@ def make_workload(name: str, rows: int = 0):
         c["name"] += " (fp16 A values and B, fp32 accumulation)"
     elif name == "bsr":
         c = synth.block_sparse()
+    elif name == "bsr-skewed":  # every 16th block-row 8x longer: the planned call splits it
+        c = synth.block_sparse_skewed()
     elif name == "wcsr":
         c = synth.window_pool()
     elif name == "wcsr-skewed":  # every 16th window ~6.5x wider: the planned call splits it
@@ -206,9 +209,9 @@ def accounting(c):
     if w.startswith("wcsr"):  # flops of the stored chunks (what the tensor cores execute); bytes of the WCSR arrays
         nch, N = c["nchunks"], c["N"]
         return 2 * nch * 4096 * N, 2 * nch * 4096 + 4 * 64 * nch + 4 * (M // 64 + 1) + 2 * K * N + 4 * M * N
-    if w == "bsr":
-        nb = c["bcols"].size
+    if w.startswith("bsr"):
         bs, N = c["bs"], c["N"]
+        nb = c["bcols"].size if "bcols" in c else c["row"].size // (bs * bs)  # dense blocks
         return 2 * nb * bs * bs * N, 2 * nb * bs * bs + 4 * nb + 4 * (M // bs + 1) + 2 * K * N + 4 * M * N
     raise ValueError(w)
 
@@ -236,7 +239,7 @@ def run_ours(args, rank, world):
     timings = {}
 
     t0 = time.perf_counter()
-    if w in ("bsr", "wcsr", "wcsr-skewed"):
+    if w in ("bsr", "bsr-skewed", "wcsr", "wcsr-skewed"):
         rp, col, val = spx.spx_build_csr(M, K, c["row"], c["col"], c["val_bf16"])
     elif w == "power-law-coo":
         rp = col = val = None  # the generator's triplets are already sorted by row
@@ -561,8 +564,19 @@ def run_ours(args, rank, world):
         C = torch.empty(M, c["N"], device=dev)
         src = source_hash("spx_bsr.cu", "spx_tc.cuh")
 
+        bplan = spx.BsrPlan(M, int(bcol.size), d_brp, stream=stream) if w == "bsr-skewed" else None
+        bscratch = (torch.empty(max(4, spx._lib().spx_spmm_bsr_planned_scratch_bytes(bplan.handle, c["N"]) // 4),
+                                device=dev) if bplan else None)
+
+        def bsr_call():
+            if bplan is None:
+                spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+            else:
+                spx.spx_spmm_bsr_planned(bplan, M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream,
+                                         scratch=bscratch)
+
         def run():
-            spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+            bsr_call()
 
         Bh = torch.from_numpy(c["B_bf16"].view(np.int16)).pin_memory()
         Co = torch.empty(M, c["N"]).pin_memory()
@@ -571,10 +585,22 @@ def run_ours(args, rank, world):
         def e2e_run():
             with torch.cuda.stream(stream):
                 Bm.copy_(Bh, non_blocking=True)
-                spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+                bsr_call()
                 Co.copy_(C, non_blocking=True)
 
         extra = {"fill_ratio": fill, "nnzb": int(bcol.size)}
+        if bplan is not None:  # the same product without the task split, for comparison (untimed by the step)
+            extra["task_split"] = dict(bplan.info)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(5):
+                with torch.cuda.stream(stream):
+                    ev0.record(stream)
+                    spx.spx_spmm_bsr(M, K, c["bs"], c["bs"], d_brp, d_bcol, d_bval, Bm, C, stream=stream)
+                    ev1.record(stream)
+                ev1.synchronize()
+                ts.append(ev0.elapsed_time(ev1))
+            extra["unsplit_ms"] = round(sorted(ts)[2], 5)
 
     # ---------------- timing: warmup, then K steps with an L2 flush between steps
     def flush_l2():
@@ -709,7 +735,7 @@ def run_ours(args, rank, world):
     gflops = job_throughput(flops, world, ms)
     if w.startswith("wcsr"):
         extra["useful_gflops"] = round(extra["useful_flops"] / (ms * 1e-3) / 1e9, 1)
-    if w in ("bsr", "wcsr", "wcsr-skewed"):
+    if w in ("bsr", "bsr-skewed", "wcsr", "wcsr-skewed"):
         ach = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["bf16"], 4), "peak_source": pk["src"] + " (bf16 dense, burst)"}
@@ -727,7 +753,7 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "wcsr", "wcsr-skewed") or w.endswith("bf16"))
+        "vs_baseline": None, "dtype": "bf16->f32" if (w in ("bsr", "bsr-skewed", "wcsr", "wcsr-skewed") or w.endswith("bf16"))
         else "f16->f32" if w.endswith("-f16") else "f32",
         "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c["name"], "M": M, "K": K, "nnz": int(c["row"].size),
@@ -766,7 +792,7 @@ def cpu_step_fn(c):
         fl = 2 * int(np.diff(rp)[rows].sum()) * c["N"]
         return (lambda: oracle.spmm(M, rp, col, val, Bf, rows=rows)), fl, \
             f"{rows.size} output rows (one per window) of the {M}x{K} product, nonzero flops"
-    if w == "bsr":
+    if w.startswith("bsr"):
         rp, col, val = row_major_csr(c, c["val_bf16"])
         brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
         rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every block-row
@@ -848,7 +874,7 @@ def main():
     ap.add_argument("--workload", default="power-law",
                     choices=["power-law", "power-law-coo", "power-law-sell", "uniform", "dual", "spmm32", "spmm128", "spmm32-f16",
                              "spmm128-f16", "spmm32-power-law", "spmm32-bf16",
-                             "spmm128-bf16", "bsr", "wcsr", "wcsr-skewed"])
+                             "spmm128-bf16", "bsr", "bsr-skewed", "wcsr", "wcsr-skewed"])
     ap.add_argument("--tune", action="store_true", help="choose the SpMV plan options by spx_plan_autotune")
     ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")
     ap.add_argument("--no-e2e", action="store_true")

@@ -268,6 +268,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
+constexpr int32_t kDefaultTaskBlocks = 64;  // blocks per task before a block-row is split
+
+// Split block-rows of a planned call: C rows of block-row I = alpha * (sum of
+// its pieces' partial tiles, in piece order) + beta * C; one thread per
+// (row, column), grid (column blocks, 64 rows, split block-rows).
+__global__ void __launch_bounds__(256) bsr_fixup_kernel(const int4* __restrict__ splits, int nsplit,
+                                                       const float* __restrict__ partials, int N, float alpha,
+                                                       float beta, float* C, long long ldc) {
+    const int n = blockIdx.x * 256 + threadIdx.x, r = blockIdx.y;
+    if (n >= N) return;
+    for (int i = blockIdx.z; i < nsplit; i += gridDim.z) {
+        const int4 sp = splits[i];  // {block-row, first slot, pieces, 0}
+        float s = 0.f;
+        for (int k = 0; k < sp.z; ++k) s += __ldcs(partials + (static_cast<long long>(sp.y + k) * kBlk + r) * N + n);
+        float* q = C + (static_cast<long long>(sp.x) * kBlk + r) * ldc + n;
+        *q = beta != 0.f ? alpha * s + beta * *q : alpha * s;
+    }
+}
+
 // ---------------------------------------------------------------- tile variant
 // Non-persistent: one CTA per (128*HALVES-column tile, block-row), one TMA
 // warp, one MMA thread, four epilogue warps, a STAGES-deep ring of {A block
@@ -283,11 +302,13 @@ __host__ __device__ constexpr uint32_t tile_stage_bytes() { return kABytes + 2 *
 template <int STAGES, int HALVES>
 constexpr size_t tile_smem_bytes() { return STAGES * tile_stage_bytes<HALVES>() + 1024 + 256; }
 
-template <int STAGES, int HALVES>
+template <int STAGES, int HALVES, bool TASKS = false>
 __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                         long long ldc, float alpha, float beta, long long spin_limit) {
+                         long long ldc, float alpha, float beta, long long spin_limit,
+                         const int4* __restrict__ tasks = nullptr, float* __restrict__ partials = nullptr,
+                         int N = 0) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -306,9 +327,20 @@ __global__ void __launch_bounds__(kTThreads)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * 128 * HALVES;
-    const int I = blockIdx.y;
-    const int b0 = __ldg(brp + I);
-    const int nblk = __ldg(brp + I + 1) - b0;
+    // one block-row per grid row, or (planned call) one task: a piece of a
+    // block-row's blocks {block-row, first block, blocks, partial slot or -1}
+    int I, b0, nblk, slot = -1;
+    if (TASKS) {
+        const int4 t = tasks[blockIdx.y];
+        I = t.x;
+        b0 = t.y;
+        nblk = t.z;
+        slot = t.w;
+    } else {
+        I = blockIdx.y;
+        b0 = __ldg(brp + I);
+        nblk = __ldg(brp + I + 1) - b0;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -397,6 +429,11 @@ __global__ void __launch_bounds__(kTThreads)
 #pragma unroll
     for (int h = 0; h < HALVES; ++h) {
         float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 128 * h + 32 * warp + lane;
+        // a piece of a split block-row writes its raw partial tile (1 * sum, exact; the fix-up applies alpha/beta)
+        const bool raw = TASKS && slot >= 0;
+        float* dst = raw ? partials + static_cast<long long>(slot) * kBlk * N + n0 + 128 * h + 32 * warp + lane : cp;
+        const long long dstride = raw ? N : ldc;
+        const float ealpha = raw ? 1.f : alpha, ebeta = raw ? 0.f : beta;
         if (nblk == 0) {
             for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
         } else if (ok && !s_abort) {
@@ -407,9 +444,9 @@ __global__ void __launch_bounds__(kTThreads)
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float* q = cp + static_cast<long long>(c0 + j) * ldc;
-                    const float acc = alpha * __uint_as_float(v[j]);
-                    __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+                    float* q = dst + static_cast<long long>(c0 + j) * dstride;
+                    const float acc = ealpha * __uint_as_float(v[j]);
+                    __stcs(q, ebeta != 0.f ? acc + ebeta * *q : acc);
                 }
             }
         }
@@ -517,6 +554,62 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     }
     (void)e;
     spx_note_launches(1);
+    return spx_cuda_status(cudaGetLastError());
+}
+
+spx_status spx_bsr_plan_build(int32_t M, int64_t nnzb, const int32_t* bsr_row_ptr, spx_loc where, int32_t max_blocks,
+                              spx_wcsr_plan** out) {
+    return spx_wcsr_plan_build(M, nnzb, bsr_row_ptr, where, max_blocks > 0 ? max_blocks : kDefaultTaskBlocks, out);
+}
+
+size_t spx_spmm_bsr_planned_scratch_bytes(const spx_wcsr_plan* plan, int32_t N) {
+    return spx_spmm_wcsr_planned_scratch_bytes(plan, N);
+}
+
+spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb,
+                                const int32_t* bsr_row_ptr, const int32_t* bsr_col, const uint16_t* bsr_val,
+                                int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta, float* C,
+                                int64_t ldc, void* scratch, size_t scratch_bytes, spx_stream_t stream) {
+    if (!P || P->magic != kWcsrPlanMagic) return SPX_ERR_ARG;
+    if (P->M != M || P->nchunks != nnzb) return SPX_ERR_ARG;
+    if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
+    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
+    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % 128) return SPX_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return SPX_OK;
+    if (nnzb == 0)  // nothing to split
+        return spx_spmm_bsr(M, K, br, bc, nnzb, bsr_row_ptr, bsr_col, bsr_val, N, B, ldb, alpha, beta, C, ldc, stream);
+    if (P->table_bytes > 0 && !P->d_table) return SPX_ERR_NOT_READY;
+    if (!bsr_row_ptr || !C || !bsr_col || !bsr_val || !B) return SPX_ERR_ARG;
+    if (ldb < N || ldc < N) return SPX_ERR_ARG;
+    if (ldb % 8 || !spx_aligned(bsr_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
+        !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4))
+        return SPX_ERR_ALIGN;
+    const int64_t ntasks = static_cast<int64_t>(P->tasks.size() / 4);
+    const int nsplit = static_cast<int>(P->splits.size() / 4);
+    if (ntasks > 65535) return SPX_ERR_UNSUPPORTED;  // tasks map to gridDim.y
+    if (nsplit > 0) {
+        const size_t need = sizeof(float) * static_cast<size_t>(P->slots) * kBlk * static_cast<size_t>(N);
+        if (!scratch || scratch_bytes < need) return SPX_ERR_ARG;
+        if (!spx_aligned(scratch, 16)) return SPX_ERR_ALIGN;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
+        !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
+        return SPX_ERR_CUDA;
+    const int4* tasks = static_cast<const int4*>(P->d_table);
+    float* partials = static_cast<float*>(scratch);
+    if (set_smem_limit(bsr_spmm_tile_kernel<3, 1, true>, tile_smem_bytes<3, 1>()) != cudaSuccess) return SPX_ERR_CUDA;
+    bsr_spmm_tile_kernel<3, 1, true><<<dim3(N / 128, static_cast<unsigned>(ntasks)), kTThreads, tile_smem_bytes<3, 1>(),
+                                       st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit, tasks,
+                                             partials, N);
+    uint64_t launches = 1;
+    if (nsplit > 0) {
+        bsr_fixup_kernel<<<dim3((N + 255) / 256, kBlk, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(
+            tasks + ntasks, nsplit, partials, N, alpha, beta, C, ldc);
+        ++launches;
+    }
+    spx_note_launches(launches);
     return spx_cuda_status(cudaGetLastError());
 }
 

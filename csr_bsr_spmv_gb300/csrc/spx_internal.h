@@ -73,6 +73,21 @@ struct spx_plan {
 spx_status spx_dev_check_rp(int32_t M, int64_t nnz, const int32_t* row_ptr, cudaStream_t st);
 spx_status spx_dev_make_plan(spx_plan* P, const int32_t* row_ptr, cudaStream_t st);
 
+// Task split of 64-row units (WCSR windows, BSR block-rows): units with more
+// than max_chunks chunks (blocks) are cut into pieces with partial-tile slots.
+struct spx_wcsr_plan {
+    int32_t M = 0;
+    int64_t nchunks = 0;  // chunks (WCSR) or blocks (BSR) in all
+    int32_t max_chunks = 0;
+    std::vector<int32_t> tasks;   // 4 per task: unit, first chunk, chunks, partial slot (-1: the whole unit)
+    std::vector<int32_t> splits;  // 4 per split unit: unit, first slot, pieces, 0
+    int64_t slots = 0;
+    size_t table_bytes = 0;
+    const void* d_table = nullptr;  // caller-owned copy: tasks, then splits
+    uint64_t magic = 0;
+};
+constexpr uint64_t kWcsrPlanMagic = 0x5350585f57504c4eull;  // "SPX_WPLN"
+
 constexpr uint64_t kPlanMagic = 0x5350585f504c414eull;  // "SPX_PLAN"
 
 enum : int32_t { kTaskGroup = 0, kTaskCta = 1, kTaskSeg = 2 };

@@ -355,21 +355,8 @@ spx_status build_wcsr_host(int32_t M, int32_t K, const int32_t* rp, const int32_
 }
 
 constexpr int32_t kDefaultTaskChunks = 16;  // chunks per task before a window is split
-constexpr uint64_t kWcsrPlanMagic = 0x5350585f57504c4eull;  // "SPX_WPLN"
 
 }  // namespace
-
-struct spx_wcsr_plan {
-    int32_t M = 0;
-    int64_t nchunks = 0;
-    int32_t max_chunks = 0;
-    std::vector<int32_t> tasks;   // 4 per task: window, first chunk, chunks, partial slot (-1: the whole window)
-    std::vector<int32_t> splits;  // 4 per split window: window, first slot, pieces, 0
-    int64_t slots = 0;
-    size_t table_bytes = 0;
-    const void* d_table = nullptr;  // caller-owned copy: tasks, then splits
-    uint64_t magic = 0;
-};
 
 namespace {
 

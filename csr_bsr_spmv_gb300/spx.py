@@ -146,6 +146,10 @@ def _lib():
             "spx_spmm_wcsr_planned_scratch_bytes": ([vp, i32], sz),
             "spx_spmm_wcsr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
                                       ctypes.c_int),
+            "spx_bsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
+            "spx_spmm_bsr_planned_scratch_bytes": ([vp, i32], sz),
+            "spx_spmm_bsr_planned": ([vp, i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz,
+                                      vp], ctypes.c_int),
             "spx_gather_probe_blocks": ([], ctypes.c_int32),
             "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
@@ -332,11 +336,13 @@ def spx_spmm_wcsr(M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor, 
 class WcsrPlan:
     """Owns an spx_wcsr_plan* (the WCSR task split) and its uploaded device table."""
 
+    _build = "spx_wcsr_plan_build"
+
     def __init__(self, M: int, nchunks: int, win_ptr, max_chunks: int = 0, device=None, upload=True, stream=None):
         lib = _lib()
         h = ctypes.c_void_p()
-        _check(lib.spx_wcsr_plan_build(M, nchunks, _ptr(win_ptr), _where(win_ptr), int(max_chunks), ctypes.byref(h)),
-               "spx_wcsr_plan_build")
+        _check(getattr(lib, self._build)(M, nchunks, _ptr(win_ptr), _where(win_ptr), int(max_chunks), ctypes.byref(h)),
+               self._build)
         self.handle, self.M, self.nchunks = h, M, nchunks
         info = WcsrPlanInfo()
         _check(lib.spx_wcsr_plan_info(h, ctypes.byref(info)), "spx_wcsr_plan_info")
@@ -364,6 +370,30 @@ class WcsrPlan:
             self.close()
         except Exception:
             pass
+
+
+class BsrPlan(WcsrPlan):
+    """The task split of BSR block-rows (spx_bsr_plan_build): same object as WcsrPlan,
+    built from bsr_row_ptr with nnzb blocks and max_blocks (0: 64)."""
+    _build = "spx_bsr_plan_build"
+
+
+def spx_spmm_bsr_planned(plan: BsrPlan, M: int, K: int, br: int, bc: int, bsr_row_ptr: torch.Tensor,
+                         bsr_col: torch.Tensor, bsr_val: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                         alpha: float = 1.0, beta: float = 0.0, stream=None, scratch: torch.Tensor | None = None):
+    """spx_spmm_bsr with the plan's long block-rows split (partial tiles + fixed-order fix-up)."""
+    N = B.shape[1]
+    _require(B.dim() == 2 and C.dim() == 2 and B.stride(1) == 1 and C.stride(1) == 1,
+             "B and C must be 2-D with unit column stride")
+    lib = _lib()
+    need = int(lib.spx_spmm_bsr_planned_scratch_bytes(plan.handle, N))
+    if scratch is None:
+        scratch = torch.empty(max(4, (need + 15) // 16 * 4), dtype=torch.float32, device=C.device)
+    _check(lib.spx_spmm_bsr_planned(plan.handle, M, K, br, bc, bsr_col.numel(), _ptr(bsr_row_ptr), _ptr(bsr_col),
+                                    _ptr(bsr_val), N, _ptr(B), B.stride(0), float(alpha), float(beta), _ptr(C),
+                                    C.stride(0), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                    _stream(stream)), "spx_spmm_bsr_planned")
+    return C
 
 
 def spx_spmm_wcsr_planned(plan: WcsrPlan, M: int, K: int, win_ptr: torch.Tensor, win_col: torch.Tensor,

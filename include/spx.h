@@ -554,6 +554,8 @@ spx_status spx_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_ro
                         const float* coo_val, float alpha, const float* x, float beta, float* y, void* scratch,
                         size_t scratch_bytes, spx_stream_t stream);
 
+typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side: the task split of WCSR windows / BSR block-rows */
+
 /*
  * C = alpha * A B + beta * C with A in BSR (br x bc blocks, row-major inside,
  * bf16), B dense K x N bf16 row-major (ldb), C dense M x N fp32 row-major
@@ -571,6 +573,27 @@ spx_status spx_spmv_coo(int32_t M, int32_t K, int64_t nnz, const int32_t* coo_ro
 spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream);
+
+/*
+ * BSR task split, the counterpart of the WCSR one for block-rows (the same
+ * plan type): spx_bsr_plan_build(M, nnzb, bsr_row_ptr, where, max_blocks,
+ * &plan) cuts every block-row of more than max_blocks blocks (max_blocks <= 0:
+ * 64) into balanced pieces of consecutive blocks; upload, inspect and
+ * destroy it with the spx_wcsr_plan_* calls.  spx_spmm_bsr_planned runs one
+ * CTA per task and column tile; whole block-rows write C as spx_spmm_bsr
+ * does, pieces write raw 64 x N partial tiles to scratch
+ * (spx_spmm_bsr_planned_scratch_bytes) and a fix-up adds them in piece order
+ * and applies alpha/beta.  Same shape, alignment and error rules as
+ * spx_spmm_bsr, plus those of spx_spmm_wcsr_planned for the plan and scratch.
+ * Launches: 1, or 2 with split block-rows.
+ */
+spx_status spx_bsr_plan_build(int32_t M, int64_t nnzb, const int32_t* bsr_row_ptr, spx_loc where, int32_t max_blocks,
+                              spx_wcsr_plan** out);
+size_t spx_spmm_bsr_planned_scratch_bytes(const spx_wcsr_plan* plan, int32_t N);
+spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* plan, int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb,
+                                const int32_t* bsr_row_ptr, const int32_t* bsr_col, const uint16_t* bsr_val,
+                                int32_t N, const uint16_t* B, int64_t ldb, float alpha, float beta, float* C,
+                                int64_t ldc, void* scratch, size_t scratch_bytes, spx_stream_t stream);
 
 /* ------------------------------------------------------------ WCSR */
 
@@ -634,7 +657,6 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
  * SPX_ERR_UNSUPPORTED (more than 65535 tasks), and those of spx_spmm_wcsr.
  * Launches: 1, or 2 with split windows.
  */
-typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side */
 typedef struct spx_wcsr_plan_info_t {
     int64_t windows, tasks, split_windows, slots;
     size_t table_bytes;

@@ -299,3 +299,27 @@ def window_pool_skewed(seed: int = 7, M: int = 16384, K: int | None = None, win:
     Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
     return dict(name=f"window-pool skewed {M}x{K} windows {win} pools {pool}/{big_pool} (every {big_every}th) "
                      f"l~U{{{lmin}..{lmax}}} N={N}", M=M, K=K, N=N, row=row, col=col, val_bf16=val, B_bf16=Bm)
+
+
+def block_sparse_skewed(seed: int = 9, M: int = 16384, K: int | None = None, bs: int = 64, per_row: int = 26,
+                        big_per_row: int = 208, big_every: int = 16, N: int = 1024, sigma_a: float = 0.02,
+                        sigma_b: float = 1.0):
+    """block_sparse with skewed block-rows: every `big_every`-th block-row holds
+    `big_per_row` blocks instead of `per_row` (distinct block columns, uniform)."""
+    K = M if K is None else K
+    MB, KB = M // bs, K // bs
+    per_row, big_per_row = min(per_row, KB), min(big_per_row, KB)
+    small = block_cols(seed, MB, KB, per_row)
+    big = block_cols(seed + 1, MB, KB, big_per_row)
+    ar = np.arange(bs, dtype=np.int32)
+    rows, cols = [], []
+    for I in range(MB):
+        bc = big[I] if I % big_every == 0 else small[I]
+        per_blockrow = (bc[:, None] * bs + ar[None, :]).reshape(-1)
+        cols.append(np.tile(per_blockrow, bs))
+        rows.append(np.repeat(np.arange(I * bs, (I + 1) * bs, dtype=np.int32), per_blockrow.size))
+    row, col = np.concatenate(rows), np.concatenate(cols).astype(np.int32)
+    val = normal_bf16(seed, T_VAL, row.size, sigma_a)
+    Bm = normal_bf16(seed, T_B, K * N, sigma_b).reshape(K, N)
+    return dict(name=f"bsr skewed {M}x{K} {bs}x{bs} {per_row}/row, {big_per_row} every {big_every}th N={N}", M=M,
+                K=K, N=N, bs=bs, row=row, col=col, val_bf16=val, B_bf16=Bm)

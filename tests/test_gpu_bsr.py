@@ -223,3 +223,78 @@ def test_two_kernel_variants_in_one_process():
     r = subprocess.run([sys.executable, "-c", _TWO_VARIANTS.format(root=root)], env=env, capture_output=True,
                        text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+def _skewed_bsr(M, N, seed=9):
+    c = synth.block_sparse_skewed(seed, M=M, N=N)
+    rp, col, val = oracle.build_csr(M, c["K"], c["row"], c["col"], c["val_bf16"])
+    brp, bcol, bval, _ = oracle.build_bsr(M, c["K"], rp, col, val, 64, 64)
+    dev_args = (torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                torch.from_numpy(np.ascontiguousarray(bval).reshape(-1).view(np.int16)).cuda())
+    return c, rp, col, val, brp, dev_args
+
+
+@pytest.mark.parametrize("max_blocks", [0, 1, 8, 27])
+@pytest.mark.parametrize("N,alpha,beta", [(128, 1.0, 0.0), (256, -0.5, 1.5)])
+def test_planned_task_split(max_blocks, N, alpha, beta):
+    """Long block-rows split into pieces (partial tiles + fixed-order fix-up) against the
+    fp64 oracle; reproducible; the plain call meets the same bound."""
+    M = 2048
+    c, rp, col, val, brp, (dbrp, dbcol, dbval) = _skewed_bsr(M, N)
+    K = c["K"]
+    P = spx.BsrPlan(M, dbcol.numel(), dbrp, max_chunks=max_blocks)
+    assert max_blocks == 0 or P.info["split_windows"] > 0
+    dB = torch.from_numpy(c["B_bf16"].view(np.int16)).cuda()
+    C0 = synth.uniform(N, synth.T_Y, M * N).reshape(M, N)
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), alpha, beta,
+                             C0)
+    outs = []
+    for _ in range(2):
+        Cd = torch.from_numpy(C0.copy()).cuda()
+        spx.spx_spmm_bsr_planned(P, M, K, 64, 64, dbrp, dbcol, dbval, dB, Cd, alpha, beta)
+        torch.cuda.synchronize()
+        assert spx.spx_last_device_error() == 0
+        outs.append(Cd)
+    assert_within(outs[0].cpu().numpy(), ref, bound, rel=BF16_REL, ab=BF16_ABS, what=f"planned bsr max={max_blocks}")
+    assert torch.equal(outs[0], outs[1])
+    C3 = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_bsr(M, K, 64, 64, dbrp, dbcol, dbval, dB, C3, alpha=alpha, beta=beta)
+    if P.info["split_windows"] == 0:
+        assert torch.equal(outs[0], C3)  # no split: the same tiles
+    assert_within(C3.cpu().numpy(), ref, bound, rel=BF16_REL, ab=BF16_ABS, what="plain bsr")
+
+
+def test_planned_errors():
+    M, N = 1024, 128
+    c, rp, col, val, brp, (dbrp, dbcol, dbval) = _skewed_bsr(M, N)
+    K = c["K"]
+    dB, C = torch.from_numpy(c["B_bf16"].view(np.int16)).cuda(), torch.empty(M, N, device="cuda")
+    P = spx.BsrPlan(M, dbcol.numel(), brp, max_chunks=4)
+    cases = [(lambda: spx.spx_spmm_bsr_planned(spx.BsrPlan(M, dbcol.numel(), brp, max_chunks=4, upload=False), M, K,
+                                               64, 64, dbrp, dbcol, dbval, dB, C), -10),
+             (lambda: spx.spx_spmm_bsr_planned(P, M, K, 64, 64, dbrp, dbcol, dbval, dB, C,
+                                               scratch=torch.zeros(4, device="cuda")), -1),
+             (lambda: spx.spx_spmm_bsr_planned(P, M - 64, K, 64, 64, dbrp, dbcol, dbval, dB, C[:M - 64]), -1)]
+    for f, code in cases:
+        with pytest.raises(spx.SpxError) as e:
+            f()
+        assert e.value.code == code
+
+
+@pytest.mark.slow
+def test_planned_skewed_full_size_sampled():
+    """16,384^2 with every 16th block-row 8x longer (208 blocks), N = 1024, default split; two rows per block-row."""
+    M, N = 16384, 1024
+    c, rp, col, val, brp, (dbrp, dbcol, dbval) = _skewed_bsr(M, N)
+    K = c["K"]
+    P = spx.BsrPlan(M, dbcol.numel(), brp)
+    assert P.info["split_windows"] == M // 64 // 16
+    Cd = torch.empty(M, N, device="cuda")
+    spx.spx_spmm_bsr_planned(P, M, K, 64, 64, dbrp, dbcol, dbval, torch.from_numpy(c["B_bf16"].view(np.int16)).cuda(),
+                             Cd)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    rows = np.sort(np.concatenate([np.arange(0, M, 64), np.arange(41, M, 64)])).astype(np.int32)
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), rows=rows)
+    got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
+    assert_within(got, ref, bound, rel=BF16_REL, ab=BF16_ABS, what="planned bsr skewed full size")
