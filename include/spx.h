@@ -430,7 +430,11 @@ spx_status spx_spmm_csr_f16(int32_t M, int32_t K, int64_t nnz, const int32_t* ro
  * (SPX_ERR_UNSUPPORTED / SPX_ERR_ALIGN otherwise); SPX_ERR_ARG for a plan of
  * another matrix or too little scratch, SPX_ERR_NOT_READY before the upload.
  * Launches: 1 to 3.  The _bf16 and _f16 forms take 16-bit A values and B as
- * spx_spmm_csr_bf16 / spx_spmm_csr_f16 do.
+ * spx_spmm_csr_bf16 / spx_spmm_csr_f16 do.  A row costs an SpMM sub-warp far
+ * more than an SpMV group, so plans for SpMM want a lower pack_max than the
+ * SpMV defaults: on a 4.2M-row power-law matrix at N = 32, block_nnz 1024,
+ * pack_max 64, cta_max 2048, seg_nnz 2048 measured 1.9 ms against 2.9 ms
+ * with spx_plan_opts_auto's choice (and 32.7 ms for spx_spmm_csr).
  */
 size_t spx_spmm_csr_planned_scratch_bytes(const spx_plan* plan, int32_t N);
 spx_status spx_spmm_csr_planned(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
