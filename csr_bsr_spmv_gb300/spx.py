@@ -547,10 +547,12 @@ class Sell:
             pass
 
 
-def spx_spmv_sell(S: Sell, x: torch.Tensor, y: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """y <- alpha*A*x + beta*y with A in uploaded SELL-C-sigma form."""
-    _check(_lib().spx_spmv_sell(S.handle, S.M, S.K, float(alpha), _ptr(x), float(beta), _ptr(y), _ptr(S.scratch),
-                                S.scratch.numel() * 4, _stream(stream)), "spx_spmv_sell")
+def spx_spmv_sell(S: Sell, x: torch.Tensor, y: torch.Tensor, alpha: float = 1.0, beta: float = 0.0, stream=None,
+                  scratch: torch.Tensor | None = None):
+    """y <- alpha*A*x + beta*y with A in uploaded SELL-C-sigma form (scratch: the form's own by default)."""
+    sc = S.scratch if scratch is None else scratch
+    _check(_lib().spx_spmv_sell(S.handle, S.M, S.K, float(alpha), _ptr(x), float(beta), _ptr(y), _ptr(sc),
+                                sc.numel() * 4, _stream(stream)), "spx_spmv_sell")
     return y
 
 

@@ -23,6 +23,12 @@
  *     already in it do not propagate.
  *   - No call aborts; every failure is a negative spx_status and, for a
  *     rejected argument, nothing is launched.
+ *   - Calls may come from several host threads at once.  Plans, SELL forms
+ *     and task splits are read-only once built and uploaded, so calls on any
+ *     stream may share them.  A scratch buffer is written by the call that
+ *     gets it: calls that can overlap on the GPU (different streams with no
+ *     ordering between them) each need their own, while calls ordered on one
+ *     stream may share one.
  */
 #ifndef SPX_H_
 #define SPX_H_
@@ -700,7 +706,9 @@ spx_status spx_gather_probe(int64_t nnz, const int32_t* col, const float* val, c
 /*
  * Synchronises `stream`, then reads and clears the device-side error words:
  * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr or spx_spmm_wcsr gave up, else the index
- * or ordering error spx_spmv_coo recorded, else SPX_OK.
+ * or ordering error spx_spmv_coo recorded, else SPX_OK.  The words are one
+ * per device, shared by every stream: with calls still running on other
+ * streams, the status read may come from any of them.
  */
 spx_status spx_last_device_error(spx_stream_t stream);
 
