@@ -973,6 +973,39 @@ spx_status spx_dev_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, cons
     return SPX_OK;
 }
 
+// Structure fingerprint of row_ptr[0..M]: the sum of spx_fp_term(i, row_ptr[i])
+// mod 2^64, summed per warp and added into one 64-bit word (integer sums: the
+// value does not depend on the order).
+__global__ void __launch_bounds__(kT) rp_fingerprint(const int* __restrict__ rp, int M,
+                                                     unsigned long long* __restrict__ acc) {
+    unsigned long long f = 0;
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i <= M;
+         i += static_cast<long long>(gridDim.x) * kT)
+        f += spx_fp_term(static_cast<uint64_t>(i), rp[i]);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) f += __shfl_down_sync(0xffffffffu, f, d);
+    if ((threadIdx.x & 31) == 0) atomicAdd(acc, f);
+}
+
+spx_status spx_dev_rp_fingerprint(int32_t M, const int32_t* row_ptr, uint64_t* out, cudaStream_t st) {
+    if (M < 0 || !row_ptr || !out) return SPX_ERR_ARG;
+    Pool pool(st);
+    unsigned long long* acc = pool.get<unsigned long long>(1);
+    if (pool.err != cudaSuccess) return SPX_ERR_NOMEM;
+    unsigned long long h = 0;
+    cudaError_t e = cudaMemsetAsync(acc, 0, sizeof(unsigned long long), st);
+    if (e == cudaSuccess) {
+        rp_fingerprint<<<grid_for(static_cast<long long>(M) + 1), kT, 0, st>>>(row_ptr, M, acc);
+        spx_note_launches(1);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, acc, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SPX_ERR_CUDA;
+    *out = h;
+    return SPX_OK;
+}
+
 spx_status spx_dev_row_stats(int32_t M, const int32_t* row_ptr, spx_row_stats_t* out, cudaStream_t st) {
     std::memset(out, 0, sizeof(*out));
     out->rows = M;

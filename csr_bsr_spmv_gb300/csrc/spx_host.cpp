@@ -393,6 +393,12 @@ spx_status spx_plan_opts_auto(const spx_row_stats_t* st, spx_plan_opts_t* o) {
     return SPX_OK;
 }
 
+static uint64_t rp_fingerprint_host(int32_t M, const int32_t* rp) {
+    uint64_t f = 0;
+    for (int64_t i = 0; i <= M; ++i) f += spx_fp_term(static_cast<uint64_t>(i), rp[i]);
+    return f;
+}
+
 spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, spx_loc where,
                         const spx_plan_opts_t* opts, spx_plan** plan_out) {
     if (!plan_out) return SPX_ERR_ARG;
@@ -435,6 +441,10 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     } catch (const std::bad_alloc&) {
         s = SPX_ERR_NOMEM;
     }
+    if (s == SPX_OK) {
+        if (dev) s = spx_dev_rp_fingerprint(M, rp, &P->fingerprint, nullptr);
+        else P->fingerprint = rp_fingerprint_host(M, rp);
+    }
     if (s != SPX_OK) {
         delete P;
         return s;
@@ -442,6 +452,26 @@ spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_pt
     P->magic = kPlanMagic;
     *plan_out = P;
     return SPX_OK;
+}
+
+spx_status spx_plan_fingerprint(const spx_plan* P, uint64_t* out) {
+    if (!spx_plan_ok(P) || !out) return SPX_ERR_ARG;
+    *out = P->fingerprint;
+    return SPX_OK;
+}
+
+spx_status spx_plan_validate(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                             spx_loc where, spx_stream_t stream) {
+    if (!spx_plan_ok(P) || !row_ptr || (where != SPX_HOST && where != SPX_DEVICE)) return SPX_ERR_ARG;
+    if (P->M != M || P->K != K || P->nnz != nnz) return SPX_ERR_ARG;
+    uint64_t f = 0;
+    if (where == SPX_DEVICE) {
+        spx_status s = spx_dev_rp_fingerprint(M, row_ptr, &f, reinterpret_cast<cudaStream_t>(stream));
+        if (s != SPX_OK) return s;
+    } else {
+        f = rp_fingerprint_host(M, row_ptr);
+    }
+    return f == P->fingerprint ? SPX_OK : SPX_ERR_ARG;
 }
 
 spx_status spx_plan_get_info(const spx_plan* P, spx_plan_info_t* out) {

@@ -7,6 +7,26 @@
 
 #include "spx.h"
 
+#ifdef __CUDACC__
+#define SPX_HD __host__ __device__
+#else
+#define SPX_HD
+#endif
+
+// One term of a row_ptr's structure fingerprint: SplitMix64's output function
+// (Steele, Lea, Flood, "Fast splittable pseudorandom number generators",
+// OOPSLA 2014) of the state 2^32 * i + (uint32) row_ptr[i].  The fingerprint
+// is the sum of the terms mod 2^64, so any summation order gives the same value.
+inline SPX_HD uint64_t spx_fp_term(uint64_t i, int32_t v) {
+    uint64_t z = ((i << 32) | static_cast<uint32_t>(v)) + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// Fingerprint of a device row_ptr[0..M] (one launch; synchronises st).
+spx_status spx_dev_rp_fingerprint(int32_t M, const int32_t* row_ptr, uint64_t* out, cudaStream_t st);
+
 // Counts kernel launches (reported by spx_launch_count).
 void spx_note_launches(uint64_t n);
 
@@ -64,6 +84,7 @@ struct spx_plan {
     const void* d_table = nullptr;  // caller-owned copy of tasks + longrows
     size_t table_bytes = 0;
     size_t scratch_bytes = 0;
+    uint64_t fingerprint = 0;       // of the row_ptr the plan was built from
     uint64_t magic = 0;
 };
 

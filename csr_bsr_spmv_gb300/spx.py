@@ -101,6 +101,8 @@ def _lib():
             "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
             "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
             "spx_plan_destroy": ([vp], ctypes.c_int),
+            "spx_plan_fingerprint": ([vp, ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+            "spx_plan_validate": ([vp, i32, i32, i64, vp, ctypes.c_int, vp], ctypes.c_int),
             "spx_plan_autotune": ([i32, i32, i64, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanOpts), i32, i32, vp,
                                    ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_float),
                                    ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
@@ -468,6 +470,19 @@ class Plan:
             self.scratch = torch.empty(max(1, self.info["scratch_bytes"] // 4), dtype=torch.float32, device=dev)
             _check(lib.spx_plan_upload(h, _ptr(self.table), self.table.numel() * 4, _stream(stream)),
                    "spx_plan_upload")
+
+    @property
+    def fingerprint(self) -> int:
+        """Structure fingerprint of the row_ptr the plan was built from (spx_plan_fingerprint)."""
+        f = ctypes.c_uint64()
+        _check(_lib().spx_plan_fingerprint(self.handle, ctypes.byref(f)), "spx_plan_fingerprint")
+        return f.value
+
+    def validate(self, row_ptr, stream=None) -> int:
+        """spx_status of spx_plan_validate for this row_ptr (0: the plan still fits; -1: stale)."""
+        where = _where(row_ptr)
+        return _lib().spx_plan_validate(self.handle, self.M, self.K, self.nnz, _ptr(row_ptr), where,
+                                        _stream(stream) if where == SPX_DEVICE else None)
 
     def tasks(self):
         t = np.empty((self.info["tasks"], 4), np.int32)

@@ -250,6 +250,28 @@ spx_status spx_plan_upload(spx_plan* plan, void* table, size_t table_bytes, spx_
 spx_status spx_plan_destroy(spx_plan* plan);
 
 /*
+ * Structure fingerprint of a plan, for callers that rewrite a matrix's row
+ * offsets in place and keep its plan.  [SpMM-ops] §4 (the profile cached on
+ * the matrix descriptor is invalidated when the matrix changes).  A plan is
+ * built from one row_ptr, and the compute calls check only M, K and nnz, so a
+ * changed row_ptr with the same sizes would use a stale plan.  The fingerprint
+ * of row_ptr[0..M] is
+ *   F = sum over i = 0..M of mix(2^32 * i + (uint32) row_ptr[i])   (mod 2^64),
+ * where mix is SplitMix64's output function (add 0x9E3779B97F4A7C15, then
+ * xor-shift-multiply by 0xBF58476D1CE4E5B9 and 0x94D049BB133111EB with shifts
+ * 30, 27, 31).  Being a sum, it is the same on the host and on the GPU.
+ *   spx_plan_fingerprint: F of the row_ptr the plan was built from.
+ *   spx_plan_validate: recomputes F from `row_ptr` (host, or device memory:
+ *     one launch and temporary memory from the stream-ordered allocator, then
+ *     `stream` is synchronised) and returns SPX_OK when M, K, nnz and F all
+ *     match the plan, SPX_ERR_ARG otherwise (a stale plan: build a new one).
+ *     One O(M) read of row_ptr; not needed on the compute path.
+ */
+spx_status spx_plan_fingerprint(const spx_plan* plan, uint64_t* fingerprint_out);
+spx_status spx_plan_validate(const spx_plan* plan, int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr,
+                             spx_loc where, spx_stream_t stream);
+
+/*
  * Measured choice of plan options, cached per matrix profile.  [SpMM-ops] §4
  * (profile the matrix once -- row-length statistics as the dispatch key --
  * pick the mapping, keep the choice with the matrix).  Times each candidate

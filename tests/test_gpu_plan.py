@@ -32,6 +32,9 @@ def _same_plan(M, rp, opts=None):
     assert np.array_equal(th, td) and np.array_equal(lh, ld)
     n = ph.info["table_bytes"] // 4
     assert torch.equal(ph.table[:n].cpu(), pd.table[:n].cpu())
+    # the structure fingerprint: the same on both sides, and each side validates the other's row_ptr
+    assert pd.fingerprint == ph.fingerprint
+    assert pd.validate(rp) == 0 and ph.validate(torch.from_numpy(rp).cuda()) == 0
     return ph.info
 
 
@@ -71,3 +74,17 @@ def test_device_plan_rejects_bad_row_ptr():
         with pytest.raises(spx.SpxError) as e:
             spx.spx_plan_csr(2, 2, nnz, torch.from_numpy(rp).cuda())
         assert e.value.code == code
+
+
+def test_validate_detects_a_moved_entry_on_the_device():
+    """Same M, K, nnz, one entry moved to the next row: the device check reports the stale plan."""
+    L, _ = synth.lengths_zipf(82, 300000, 2.1, 20000, 12.0)
+    rp = _rp(L)
+    plan = spx.spx_plan_csr(300000, 300000, int(rp[-1]), torch.from_numpy(rp).cuda())
+    moved = rp.copy()
+    nz = np.flatnonzero(L > 0)
+    r = int(nz[nz.size // 2])
+    moved[r + 1] -= 1
+    assert r + 1 < rp.size - 1 and moved[r + 1] >= moved[r]
+    assert plan.validate(torch.from_numpy(moved).cuda()) == -1
+    assert plan.validate(torch.from_numpy(rp).cuda()) == 0

@@ -403,3 +403,39 @@ def test_wcsr_plan_errors():
         with pytest.raises(spx.SpxError) as e:
             spx.WcsrPlan(64 * (len(wp) - 1), nch, np.array(wp, np.int32), upload=False)
         assert e.value.code == code
+
+
+def _fingerprint(rp):
+    """The documented plan fingerprint, restated: sum of SplitMix64 outputs of 2^32*i + row_ptr[i]."""
+    mask = (1 << 64) - 1
+    f = 0
+    for i, v in enumerate(np.asarray(rp, np.int64).tolist()):
+        z = (((i << 32) | (v & 0xFFFFFFFF)) + 0x9E3779B97F4A7C15) & mask
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & mask
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & mask
+        f = (f + (z ^ (z >> 31))) & mask
+    return f
+
+
+def test_plan_fingerprint_and_validate():
+    """The fingerprint of row_ptr = [0] is SplitMix64's first output from seed 0
+    (0xE220A8397B1DCDAF, its published first value); larger row_ptrs follow the
+    documented sum.  validate accepts the plan's own row_ptr and rejects a row_ptr
+    with the same M, K, nnz but one nonzero moved to the next row, and other sizes."""
+    p0 = spx.spx_plan_csr(0, 7, 0, np.zeros(1, np.int32), upload=False)
+    assert p0.fingerprint == 0xE220A8397B1DCDAF
+    L, _ = synth.lengths_zipf(81, 5000, 2.1, 3000, 12.0)
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    nnz = int(rp[-1])
+    p = spx.spx_plan_csr(5000, 70000, nnz, rp, upload=False)
+    assert p.fingerprint == _fingerprint(rp)
+    assert p.validate(rp) == 0
+    moved = rp.copy()
+    r = int(np.flatnonzero(L > 0)[7])
+    moved[r + 1] -= 1  # the last entry of row r now belongs to row r + 1
+    assert moved[r + 1] >= moved[r]
+    assert p.validate(moved) == -1
+    lib = spx._lib()
+    assert lib.spx_plan_validate(p.handle, 5000, 70001, nnz, spx._ptr(rp), 0, None) == -1  # K differs
+    assert lib.spx_plan_validate(p.handle, 5000, 70000, nnz, None, 0, None) == -1
+    assert lib.spx_plan_validate(p.handle, 5000, 70000, nnz, spx._ptr(rp), 7, None) == -1  # bad location
