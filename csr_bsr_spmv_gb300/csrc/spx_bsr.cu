@@ -35,6 +35,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 #include <mutex>
 
 #include "spx_internal.h"
@@ -274,12 +275,13 @@ constexpr int32_t kDefaultTaskBlocks = 64;  // blocks per task before a block-ro
 // its pieces' partial tiles, in piece order) + beta * C; one thread per
 // (row, column), grid (column blocks, 64 rows, split block-rows).
 __global__ void __launch_bounds__(256) bsr_fixup_kernel(const int4* __restrict__ splits, int nsplit,
-                                                       const float* __restrict__ partials, int N, float alpha,
+                                                       const float* __restrict__ partials, int M, int N, float alpha,
                                                        float beta, float* C, long long ldc) {
     const int n = blockIdx.x * 256 + threadIdx.x, r = blockIdx.y;
     if (n >= N) return;
     for (int i = blockIdx.z; i < nsplit; i += gridDim.z) {
         const int4 sp = splits[i];  // {block-row, first slot, pieces, 0}
+        if (sp.x * kBlk + r >= M) continue;  // a ragged last block-row: rows beyond M are not stored
         float s = 0.f;
         for (int k = 0; k < sp.z; ++k) s += __ldcs(partials + (static_cast<long long>(sp.y + k) * kBlk + r) * N + n);
         float* q = C + (static_cast<long long>(sp.x) * kBlk + r) * ldc + n;
@@ -306,9 +308,8 @@ template <int STAGES, int HALVES, bool TASKS = false>
 __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                         long long ldc, float alpha, float beta, long long spin_limit,
-                         const int4* __restrict__ tasks = nullptr, float* __restrict__ partials = nullptr,
-                         int N = 0) {
+                         long long ldc, float alpha, float beta, long long spin_limit, int M, int N,
+                         const int4* __restrict__ tasks = nullptr, float* __restrict__ partials = nullptr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -426,29 +427,44 @@ __global__ void __launch_bounds__(kTThreads)
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok && lane == 0) record_error(kErrAcc);
     tc_fence_after();
+    // C rows of this block-row inside [0, M) (a ragged last block-row is zero-padded in A)
+    const int mrows = min(kBlk, M - I * kBlk);
 #pragma unroll
     for (int h = 0; h < HALVES; ++h) {
-        float* cp = C + static_cast<long long>(I) * kBlk * ldc + n0 + 128 * h + 32 * warp + lane;
+        const int cn = n0 + 128 * h + 32 * warp + lane;  // this thread's column; columns >= N are not stored
+        const bool cok = cn < N;
+        float* cp = C + static_cast<long long>(I) * kBlk * ldc + cn;
         // a piece of a split block-row writes its raw partial tile (1 * sum, exact; the fix-up applies alpha/beta)
         const bool raw = TASKS && slot >= 0;
-        float* dst = raw ? partials + static_cast<long long>(slot) * kBlk * N + n0 + 128 * h + 32 * warp + lane : cp;
+        float* dst = raw ? partials + static_cast<long long>(slot) * kBlk * N + cn : cp;
         const long long dstride = raw ? N : ldc;
+        const int rows = raw ? kBlk : mrows;
         const float ealpha = raw ? 1.f : alpha, ebeta = raw ? 0.f : beta;
         if (nblk == 0) {
-            for (int r = 0; r < kBlk; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+            if (cok)
+                for (int r = 0; r < mrows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
         } else if (ok && !s_abort) {
+            // GUARD: the tile reaches past row M or column N (a ragged edge), so each store is checked;
+            // whole tiles (CTA-uniform test) take the unchecked copy of the loop
+            auto drain = [&](auto guard) {
+                constexpr bool GUARD = decltype(guard)::value;
 #pragma unroll
-            for (int c0 = 0; c0 < kBlk; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + 64 * h + c0, v);
-                tmem_wait_ld();
+                for (int c0 = 0; c0 < kBlk; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * warp) << 16) + 64 * h + c0, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float* q = dst + static_cast<long long>(c0 + j) * dstride;
-                    const float acc = ealpha * __uint_as_float(v[j]);
-                    __stcs(q, ebeta != 0.f ? acc + ebeta * *q : acc);
+                    for (int j = 0; j < 32; ++j) {
+                        if (!GUARD || (cok && c0 + j < rows)) {
+                            float* q = dst + static_cast<long long>(c0 + j) * dstride;
+                            const float acc = ealpha * __uint_as_float(v[j]);
+                            __stcs(q, ebeta != 0.f ? acc + ebeta * *q : acc);
+                        }
+                    }
                 }
-            }
+            };
+            if (n0 + 128 * (h + 1) <= N && rows == kBlk) drain(std::false_type{});
+            else drain(std::true_type{});
         }
     }
     tc_fence_before();
@@ -486,7 +502,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream) {
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
     if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % 128) return SPX_ERR_UNSUPPORTED;
+    if (br != kBlk || bc != kBlk) return SPX_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return SPX_OK;
     if (!bsr_row_ptr || !C || (nnzb > 0 && (!bsr_col || !bsr_val || !B))) return SPX_ERR_ARG;
     if (ldb < N || ldc < N) return SPX_ERR_ARG;
@@ -523,7 +539,11 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         }
         return v;
     }();
-    const int variant = env_variant >= 10 && N % 256 ? 3 : env_variant;  // per call: 256-column tiles need N % 256 == 0
+    // per call: 256-column tiles need N % 256 == 0, and the persistent and 256-column kernels whole
+    // 64-row block-rows, 64-row block columns and 128-column tiles; other shapes take the tile kernel
+    const bool ragged = M % kBlk || K % kBlk || N % 128;
+    int variant = env_variant;
+    if ((variant >= 10 && (N % 256 || ragged)) || (variant == 0 && ragged)) variant = 3;
     cudaError_t e = cudaSuccess;
     if (variant == 0) {
         if (set_smem_limit(bsr_spmm_tc_kernel, kSmemBytes) != cudaSuccess) return SPX_ERR_CUDA;
@@ -537,14 +557,15 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         bsr_spmm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, N,
                                                                static_cast<int>(tiles), ntq, kSpinLimit);
     } else {
-        if (M / kBlk > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
+        const int MB = (M + kBlk - 1) / kBlk;
+        if (MB > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
         switch (variant) {
 #define SPX_TILE(S, H, V)                                                                                      \
     case V: {                                                                                                     \
         if (set_smem_limit(bsr_spmm_tile_kernel<S, H>, tile_smem_bytes<S, H>()) != cudaSuccess)                   \
             return SPX_ERR_CUDA;                                                                                  \
-        bsr_spmm_tile_kernel<S, H><<<dim3(N / (128 * H), M / kBlk), kTThreads, tile_smem_bytes<S, H>(), st>>>(    \
-            tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit);                                     \
+        bsr_spmm_tile_kernel<S, H><<<dim3((N + 128 * H - 1) / (128 * H), MB), kTThreads, tile_smem_bytes<S, H>(), \
+                                     st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N); \
         break;                                                                                                    \
     }
             SPX_TILE(2, 1, 2) SPX_TILE(3, 1, 3) SPX_TILE(4, 1, 4) SPX_TILE(5, 1, 5)
@@ -574,7 +595,7 @@ spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, in
     if (P->M != M || P->nchunks != nnzb) return SPX_ERR_ARG;
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
     if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (br != kBlk || bc != kBlk || M % kBlk || K % kBlk || N % 128) return SPX_ERR_UNSUPPORTED;
+    if (br != kBlk || bc != kBlk) return SPX_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return SPX_OK;
     if (nnzb == 0)  // nothing to split
         return spx_spmm_bsr(M, K, br, bc, nnzb, bsr_row_ptr, bsr_col, bsr_val, N, B, ldb, alpha, beta, C, ldc, stream);
@@ -600,13 +621,13 @@ spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, in
     const int4* tasks = static_cast<const int4*>(P->d_table);
     float* partials = static_cast<float*>(scratch);
     if (set_smem_limit(bsr_spmm_tile_kernel<3, 1, true>, tile_smem_bytes<3, 1>()) != cudaSuccess) return SPX_ERR_CUDA;
-    bsr_spmm_tile_kernel<3, 1, true><<<dim3(N / 128, static_cast<unsigned>(ntasks)), kTThreads, tile_smem_bytes<3, 1>(),
-                                       st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit, tasks,
-                                             partials, N);
+    bsr_spmm_tile_kernel<3, 1, true><<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kTThreads,
+                                       tile_smem_bytes<3, 1>(), st>>>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha,
+                                                                      beta, kSpinLimit, M, N, tasks, partials);
     uint64_t launches = 1;
     if (nsplit > 0) {
         bsr_fixup_kernel<<<dim3((N + 255) / 256, kBlk, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(
-            tasks + ntasks, nsplit, partials, N, alpha, beta, C, ldc);
+            tasks + ntasks, nsplit, partials, M, N, alpha, beta, C, ldc);
         ++launches;
     }
     spx_note_launches(launches);

@@ -29,6 +29,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 #include <new>
 #include <vector>
 
@@ -198,12 +199,15 @@ __global__ void __launch_bounds__(kThreads)
                 const int k = 8 * i + k0;
                 const int cr = __ldg(wc + k);
                 const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
-                const uint16_t* src = c >= 0 ? B + static_cast<long long>(c) * ldb + n0 + 64 * h + 8 * j : B;
-                const uint32_t nbytes = c >= 0 ? 16u : 0u;  // padding column: zero-fill
+                const uint16_t* row = c >= 0 ? B + static_cast<long long>(c) * ldb : B;
                 const uint32_t dst = stage_b(s) + k * 128u + piece_off;
 #pragma unroll
-                for (int hh = 0; hh < HALVES; ++hh)
-                    cp_async16(dst + 2 * hh * kBBox, src + (c >= 0 ? 128 * hh : 0), nbytes);
+                for (int hh = 0; hh < HALVES; ++hh) {
+                    // padding, or a piece past column N (a ragged last tile): zero-fill, no read
+                    const int cc = n0 + 128 * hh + 64 * h + 8 * j;
+                    const bool in = c >= 0 && cc < N;
+                    cp_async16(dst + 2 * hh * kBBox, in ? row + cc : B, in ? 16u : 0u);
+                }
             }
             cp_async_commit();
             if (b >= kStages - 1) {  // the copies of stage b - (kStages - 1) have landed: publish them
@@ -229,29 +233,39 @@ __global__ void __launch_bounds__(kThreads)
         const int rows = min(kWin, M - w * kWin);
 #pragma unroll
         for (int hh = 0; hh < HALVES; ++hh) {
-            float* cp = C + static_cast<long long>(w) * kWin * ldc + n0 + 128 * hh + 32 * q + lane;
+            const int cn = n0 + 128 * hh + 32 * q + lane;  // this thread's column; columns >= N are not stored
+            const bool cok = cn < N;
+            float* cp = C + static_cast<long long>(w) * kWin * ldc + cn;
             // a piece of a split window writes its raw partial tile (1 * sum, exact; the fix-up applies alpha/beta)
             const bool raw = TASKS && slot >= 0;
-            float* dst = raw ? partials + static_cast<long long>(slot) * kWin * N + n0 + 128 * hh + 32 * q + lane : cp;
+            float* dst = raw ? partials + static_cast<long long>(slot) * kWin * N + cn : cp;
             const long long dstride = raw ? N : ldc;
             const float ealpha = raw ? 1.f : alpha, ebeta = raw ? 0.f : beta;
             if (nch == 0) {
-                for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+                if (cok)
+                    for (int r = 0; r < rows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
             } else if (ok && !s_abort) {
+                // GUARD: the tile reaches past row M or column N (a ragged edge), so each store is
+                // checked; whole tiles (CTA-uniform test) take the unchecked copy of the loop
+                auto drain = [&](auto guard) {
+                    constexpr bool GUARD = decltype(guard)::value;
 #pragma unroll
-                for (int c0 = 0; c0 < kWin; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + c0, v);
-                    tmem_wait_ld();
+                    for (int c0 = 0; c0 < kWin; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + c0, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (c0 + j < rows) {
-                            float* p = dst + static_cast<long long>(c0 + j) * dstride;
-                            const float acc = ealpha * __uint_as_float(v[j]);
-                            __stcs(p, ebeta != 0.f ? acc + ebeta * *p : acc);
+                        for (int j = 0; j < 32; ++j) {
+                            if (!GUARD || (cok && c0 + j < rows)) {
+                                float* p = dst + static_cast<long long>(c0 + j) * dstride;
+                                const float acc = ealpha * __uint_as_float(v[j]);
+                                __stcs(p, ebeta != 0.f ? acc + ebeta * *p : acc);
+                            }
                         }
                     }
-                }
+                };
+                if (rows == kWin && n0 + 128 * (hh + 1) <= N) drain(std::false_type{});
+                else drain(std::true_type{});
             }
         }
     }
@@ -370,7 +384,7 @@ spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunk
                     cudaStream_t st) {
     if (M < 0 || K < 0 || N < 0 || nchunks < 0) return SPX_ERR_ARG;
     if (nchunks * kWin > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (N % 128) return SPX_ERR_UNSUPPORTED;
+    if (N % 8) return SPX_ERR_UNSUPPORTED;  // B rows are gathered in 16-byte pieces
     if (M == 0 || N == 0) return SPX_OK;
     if (!win_ptr || !C || (nchunks > 0 && (!win_col || !win_val || !B))) return SPX_ERR_ARG;
     if (ldb < N || ldc < N) return SPX_ERR_ARG;
@@ -414,7 +428,7 @@ spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunk
 #define SPX_WCSR_LAUNCH(S, H, T)                                                                               \
     do {                                                                                                       \
         if (set_smem_limit(wcsr_spmm_kernel<S, H, T>, smem_bytes<S, H>()) != cudaSuccess) return SPX_ERR_CUDA; \
-        wcsr_spmm_kernel<S, H, T><<<dim3(N / (128 * H), static_cast<unsigned>(ntasks)), kThreads,              \
+        wcsr_spmm_kernel<S, H, T><<<dim3((N + 128 * H - 1) / (128 * H), static_cast<unsigned>(ntasks)), kThreads, \
                                     smem_bytes<S, H>(), st>>>(tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, \
                                                               beta, kSpinLimit, tasks, partials, N);           \
     } while (0)

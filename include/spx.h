@@ -596,11 +596,15 @@ typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side: the task split
  * nonzero blocks, each a small dense GEMM on the tensor cores) and
  * [AsyncSparse] §2.2.1, §3 (BCSR SpMM: asynchronous copies of A blocks and
  * B tiles into shared memory feeding the matrix units).
- * Supported: br == bc == 64, M and K multiples of 64, N a multiple of 128,
- * ldb and ldc multiples of 8 and 4, all pointers 16-byte aligned; other
- * shapes return SPX_ERR_UNSUPPORTED.  Launches: 1.  Its pipeline waits are
- * bounded: on expiry the kernel records an error that spx_last_device_error
- * reports as SPX_ERR_TIMEOUT.
+ * Shapes: br == bc == 64 (else SPX_ERR_UNSUPPORTED), any M, K and N.  A
+ * ragged last block-row or block column is zero-padded in the BSR arrays (as
+ * spx_build_bsr writes them).  B rows at or beyond K are read as zeros, and C
+ * is stored only inside its M x N part, so a ragged last 128-column tile does
+ * a whole tile's work but writes nothing past column N.  ldb >= N and a
+ * multiple of 8, ldc >= N; bsr_val and B 16-byte aligned, C 4-byte aligned
+ * (SPX_ERR_ALIGN otherwise).  Launches: 1.  Its pipeline waits are bounded:
+ * on expiry the kernel records an error that spx_last_device_error reports as
+ * SPX_ERR_TIMEOUT.
  */
 spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
@@ -659,9 +663,11 @@ spx_status spx_build_wcsr(int32_t M, int32_t K, const int32_t* row_ptr, const in
  * cores.  [AsyncSparse] §4.1 (TMA for the window's values, a cooperative
  * gather of the B rows named by window_col_idx into a swizzled shared tile,
  * tensor-core MMA).  One CTA per (window, 128 output columns); no atomics,
- * so the result is deterministic.  Supported: N a multiple of 128, ldb a
- * multiple of 8, win_val and B 16-byte aligned, at most 65535 windows
- * (M <= 4,194,240); any K.  Launches: 1.
+ * so the result is deterministic.  Supported: N a multiple of 8 (B rows are
+ * gathered in 16-byte pieces; a ragged last 128-column tile gathers zeros
+ * past column N and stores nothing there), ldb a multiple of 8, win_val and
+ * B 16-byte aligned, at most 65535 windows (M <= 4,194,240); any K.
+ * Launches: 1.
  * Bounded pipeline waits report SPX_ERR_TIMEOUT through
  * spx_last_device_error.
  */

@@ -113,7 +113,8 @@ def test_unsupported_shapes_rejected_without_launch():
     z = torch.zeros(64 * 1024, dtype=torch.int32, device="cuda")
     p = spx._ptr(z)
     assert lib.spx_spmm_bsr(64, 64, 32, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -7   # block size
-    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 100, p, 128, 1.0, 0.0, p, 128, None) == -7   # N % 128
+    assert lib.spx_spmm_bsr(64, 64, 64, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -7   # bc != 64
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 100, 1.0, 0.0, p, 128, None) == -1   # ldb < N
     assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, 1.0, 0.0, p, 128, None) == -8   # ldb % 8
     assert spx.launch_count() == before
 
@@ -298,3 +299,42 @@ def test_planned_skewed_full_size_sampled():
     ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(c["B_bf16"]), rows=rows)
     got = Cd[torch.from_numpy(rows).long().cuda()].cpu().numpy()
     assert_within(got, ref, bound, rel=BF16_REL, ab=BF16_ABS, what="planned bsr skewed full size")
+
+
+def _ragged_bsr(M, K, seed, lmax=40):
+    """A random CSR (bf16 values) and its BSR with 64 x 64 blocks; M and K need not be multiples of 64."""
+    d = synth.random_coo(seed, M, K, 1, lmax)
+    vb = synth.to_bf16_bits(d["val"])
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], vb)
+    brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, 64, 64)
+    return brp, bcol, np.ascontiguousarray(bval)
+
+
+@pytest.mark.parametrize("M,K,N", [(100, 130, 200), (64 * 3 + 1, 128, 8), (64, 63, 40), (1, 1, 1000),
+                                   (300, 500, 129), (257, 700, 384)])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, -1.5)])
+@pytest.mark.parametrize("split", [False, True])
+def test_ragged_shapes(M, K, N, alpha, beta, split):
+    """Any M, K, N: a ragged last block-row / block column (zero-padded in the BSR arrays, B rows past K
+    read as zeros) and a ragged last 128-column tile; nothing is written outside the M x N part of C.
+    split: the planned call with block-rows cut into pieces of two blocks."""
+    brp, bcol, bval = _ragged_bsr(M, K, 90 + M + N)
+    ldb, ldc = (N + 7) // 8 * 8 + 8, N + 3
+    Bb = synth.to_bf16_bits(synth.uniform(91, synth.T_B, K * N)).reshape(K, N)
+    Bfull = np.zeros((K, ldb), np.uint16)
+    Bfull[:, :N] = Bb
+    C0 = synth.uniform(92, synth.T_Y, M * ldc).reshape(M, ldc)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    dbrp, dbcol, dbval = torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(), bits_dev(bval.reshape(-1))
+    dB = bits_dev(Bfull)[:, :N]
+    if split:
+        P = spx.BsrPlan(M, bcol.size, dbrp, max_chunks=2)
+        spx.spx_spmm_bsr_planned(P, M, K, 64, 64, dbrp, dbcol, dbval, dB, Cd[:, :N], alpha, beta)
+    else:
+        spx.spx_spmm_bsr(M, K, 64, 64, dbrp, dbcol, dbval, dB, Cd[:, :N], alpha=alpha, beta=beta)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    got = Cd.cpu().numpy()
+    assert np.array_equal(got[:, N:], C0[:, N:])  # columns past N untouched
+    ref, bound = oracle.bsr_spmm(M, K, 64, 64, brp, bcol, bval, Bb, alpha=alpha, beta=beta, C=C0[:, :N])
+    assert_within(got[:, :N], ref, bound, BF16_REL, BF16_ABS, what=f"M={M} K={K} N={N} split={split}")

@@ -199,3 +199,35 @@ def test_planned_without_splits_equals_plain():
     spx.spx_spmm_wcsr(M, c["K"], *args, C1, 1.5, 0.0)
     spx.spx_spmm_wcsr_planned(P, M, c["K"], *args, C2, 1.5, 0.0)
     assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("M,K,N", [(150, 700, 8), (1, 50, 40), (64 * 3 + 5, 300, 136), (200, 2000, 200),
+                                   (129, 4000, 392)])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-0.5, 1.5)])
+@pytest.mark.parametrize("split", [False, True])
+def test_ragged_columns(M, K, N, alpha, beta, split):
+    """N any multiple of 8: the last 128-column tile gathers zeros past column N and stores nothing there;
+    a partial last window; split: the planned call with windows cut into single chunks."""
+    d = synth.random_coo(120 + N, M, K, 1, 150)
+    vb = synth.to_bf16_bits(d["val"])
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], vb)
+    wp, wc, wv, _ = oracle.build_wcsr(M, K, rp, col, val)
+    Bb = synth.to_bf16_bits(synth.uniform(121, synth.T_B, K * N)).reshape(K, N)
+    ldb, ldc = N + 8, N + 5
+    Bfull = np.zeros((K, ldb), np.uint16)
+    Bfull[:, :N] = Bb
+    C0 = synth.uniform(122, synth.T_Y, M * ldc).reshape(M, ldc)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    dwp, dwc, dwv, dB = torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)), bits(Bfull)[:, :N]
+    if split:
+        P = spx.WcsrPlan(M, wc.size // 64, dwp, max_chunks=1)
+        spx.spx_spmm_wcsr_planned(P, M, K, dwp, dwc, dwv, dB, Cd[:, :N], alpha, beta)
+    else:
+        spx.spx_spmm_wcsr(M, K, dwp, dwc, dwv, dB, Cd[:, :N], alpha, beta)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    got = Cd.cpu().numpy()
+    assert np.array_equal(got[:, N:], C0[:, N:])  # columns past N untouched
+    ref, bound = oracle.spmm(M, rp, col, synth.bf16_bits_to_f32(val), synth.bf16_bits_to_f32(Bb), alpha, beta,
+                             C0[:, :N])
+    assert_within(got[:, :N], ref, bound, rel=BF16_REL, ab=BF16_ABS, what=f"M={M} K={K} N={N} split={split}")

@@ -328,7 +328,7 @@ def test_spmm_wcsr_rejects_unsupported_without_launching():
     lib = spx._lib()
     before = spx.launch_count()
     a = ctypes.c_void_p(1 << 20)
-    assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 100, a, 128, 1.0, 0.0, a, 128, None) == -7   # N % 128
+    assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 100, a, 128, 1.0, 0.0, a, 128, None) == -7   # N % 8
     assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 128, a, 132, 1.0, 0.0, a, 128, None) == -8   # ldb % 8
     assert lib.spx_spmm_wcsr(64, 64, 1, a, a, a, 128, a, 64, 1.0, 0.0, a, 128, None) == -1    # ldb < N
     assert lib.spx_spmm_wcsr(64, 64, -1, a, a, a, 128, a, 128, 1.0, 0.0, a, 128, None) == -1
