@@ -639,6 +639,19 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     assert spx.spx_last_device_error(stream) == 0, "device error word set during the timed region"
 
+    # ---------------- warm steps: the same calls back to back with no L2 flush (reported beside the flushed number)
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    run()
+    for s, e in wev:
+        s.record(stream)
+        run()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    wtimes = [s.elapsed_time(e) for s, e in wev]
+    extra["warm"] = {"ms_per_step_median": round(statistics.median(wtimes), 5),
+                     "ms_per_step_min": round(min(wtimes), 5),
+                     "how": "the same steps back to back without the L2 flush (rank-local, CUDA events)"}
+
     # ---------------- launch-bound SpMV: the per-call time inside one CUDA graph of many calls
     if w == "uniform":
         calls = 200
