@@ -111,6 +111,21 @@ def source_hash(*names):
     return h.hexdigest()[:12]
 
 
+def env_info(dev) -> dict:
+    """The run's environment: GPU, SM count, compute capability, CUDA runtime, driver, torch, host cores."""
+    import torch
+    prop = torch.cuda.get_device_properties(dev)
+    drv = None
+    try:
+        drv = subprocess.run(["nvidia-smi", f"--id={dev.index}", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"gpu": prop.name, "sms": prop.multi_processor_count, "cc": f"{prop.major}.{prop.minor}",
+            "cuda_runtime": torch.version.cuda, "driver": drv, "torch": torch.__version__,
+            "host_cores": os.cpu_count()}
+
+
 def traffic_from_profile(workload, src_hash):
     """DRAM read+write bytes of the step's dominant kernel from the committed ncu
     capture for this workload, or None when the kernel source changed since."""
@@ -790,7 +805,7 @@ def run_ours(args, rank, world):
                    "N": c.get("N", 1), "l2": "flushed between steps (256 MB write); inputs also exceed L2",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs": round(abytes / (ms * 1e-3) / 1e9, 1), "roofline": roof, "e2e": e2e, "gpu_launches": int(launches),
-        "conversion": {k: round(v, 2) for k, v in timings.items()}, "detail": extra,
+        "conversion": {k: round(v, 2) for k, v in timings.items()}, "detail": extra, "env": env_info(dev),
         "step_ms_min": round(min(times), 5), "step_ms_median": round(statistics.median(times), 5),
     }
     line["clocks"] = clk.summary()
