@@ -52,7 +52,6 @@ constexpr int kBoxes = kTileN / 64;                     // 64-column TMA boxes o
 constexpr int kStages = 5;                              // smem ring depth
 constexpr int kProducers = kStages;                     // producer warps; warp p owns ring stage p
 constexpr int kMmaWarp = kProducers;                    // the MMA-issuing warp
-constexpr int kEpiWarp0 = kProducers + 1;               // first of the 4 epilogue warps
 constexpr int kThreads = 32 * (kProducers + 1 + 4);
 constexpr uint32_t kABytes = kBlk * kBlk * 2;           // one bf16 A block, 8 KB
 constexpr uint32_t kBBox = kBlk * 64 * 2;               // 64 k-rows x 64 n, 8 KB
@@ -63,7 +62,7 @@ constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr uint32_t kIdesc = idesc_bf16_mn_k(128, 64);  // M = 128 output columns, N = 64 block rows
 constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s): only a broken pipeline reaches it
 
-enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4, kErrTmemEmpty = 5 };
+enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4, kErrTmemEmpty = 5, kErrProbe = 6 };
 
 __device__ int g_bsr_error;
 
@@ -481,6 +480,19 @@ __global__ void __launch_bounds__(kTThreads)
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemColsT) : "memory");
 }
 
+// Test aid for the bounded waits: one thread arms an mbarrier that nothing
+// completes and waits on it with the pipelines' own bounded wait; when the
+// limit runs out it records the timeout in the error word, as a stalled
+// pipeline would, and the kernel returns.
+__global__ void wait_probe_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(smem_u32(&bar), 0u, limit)) record_error(kErrProbe);
+    }
+}
+
 // C = beta * C (a BSR matrix without stored blocks).
 __global__ void bsr_scale_kernel(float* C, long long ldc, int M, int N, float beta) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
@@ -544,7 +556,6 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     const bool ragged = M % kBlk || K % kBlk || N % 128;
     int variant = env_variant;
     if ((variant >= 10 && (N % 256 || ragged)) || (variant == 0 && ragged)) variant = 3;
-    cudaError_t e = cudaSuccess;
     if (variant == 0) {
         if (set_smem_limit(bsr_spmm_tc_kernel, kSmemBytes) != cudaSuccess) return SPX_ERR_CUDA;
         int dev = 0, nsm = 0;  // SM count of the current device (cheap attribute query)
@@ -573,7 +584,6 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
 #undef SPX_TILE
         }
     }
-    (void)e;
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }
@@ -631,6 +641,13 @@ spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, in
         ++launches;
     }
     spx_note_launches(launches);
+    return spx_cuda_status(cudaGetLastError());
+}
+
+spx_status spx_wait_probe(int64_t limit_cycles, spx_stream_t stream) {
+    if (limit_cycles < 0 || limit_cycles > kSpinLimit) return SPX_ERR_ARG;
+    wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_cycles);
+    spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }
 

@@ -155,6 +155,7 @@ def _lib():
             "spx_gather_probe_blocks": ([], ctypes.c_int32),
             "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
             "spx_last_device_error": ([vp], ctypes.c_int),
+            "spx_wait_probe": ([i64, vp], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -788,6 +789,11 @@ def spx_gather_probe(A: Csr, x: torch.Tensor, partials: torch.Tensor | None = No
     _check(_lib().spx_gather_probe(A.nnz, _ptr(A.col), _ptr(A.val), _ptr(x), A.K, _ptr(partials), partials.numel(),
                                    _stream(stream)), "spx_gather_probe")
     return partials
+
+
+def spx_wait_probe(limit_cycles: int, stream=None):
+    """Arm a wait that nothing completes and let it run out after limit_cycles (see include/spx.h)."""
+    _check(_lib().spx_wait_probe(int(limit_cycles), _stream(stream)), "spx_wait_probe")
 
 
 def spx_last_device_error(stream=None) -> int:

@@ -732,6 +732,18 @@ spx_status spx_gather_probe(int64_t nnz, const int32_t* col, const float* val, c
                             float* partials, int32_t nblocks, spx_stream_t stream);
 
 /*
+ * Test aid for the bounded device waits: failure detection without a GPU fault
+ * or hang.  One CTA arms an mbarrier that nothing completes and waits on it
+ * with the same bounded wait the BSR and WCSR pipelines use.  After
+ * limit_cycles SM clock cycles (0 .. 2e9; about 1 ms per 2e6 at 2 GHz) the
+ * wait gives up, the timeout is recorded in the device error word and the
+ * kernel returns: spx_last_device_error then reports SPX_ERR_TIMEOUT once,
+ * and the context stays usable.  SPX_ERR_ARG (nothing launched) for a limit
+ * outside that range.  Launches: 1.
+ */
+spx_status spx_wait_probe(int64_t limit_cycles, spx_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device-side error words:
  * SPX_ERR_TIMEOUT if a bounded wait of spx_spmm_bsr or spx_spmm_wcsr gave up, else the index
  * or ordering error spx_spmv_coo recorded, else SPX_OK.  The words are one

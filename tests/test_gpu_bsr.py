@@ -338,3 +338,15 @@ def test_ragged_shapes(M, K, N, alpha, beta, split):
     assert np.array_equal(got[:, N:], C0[:, N:])  # columns past N untouched
     ref, bound = oracle.bsr_spmm(M, K, 64, 64, brp, bcol, bval, Bb, alpha=alpha, beta=beta, C=C0[:, :N])
     assert_within(got[:, :N], ref, bound, BF16_REL, BF16_ABS, what=f"M={M} K={K} N={N} split={split}")
+
+
+def test_bounded_wait_runs_out_and_reports_timeout():
+    """A wait that nothing completes gives up after its limit (about 1 ms here), the device error word
+    then reads SPX_ERR_TIMEOUT exactly once, and the context stays usable: a BSR product right after is
+    exact."""
+    assert spx.spx_last_device_error() == 0
+    spx.spx_wait_probe(2_000_000)
+    assert spx.spx_last_device_error() == -6
+    assert spx.spx_last_device_error() == 0
+    test_small_integers_exact()
+    assert spx.spx_last_device_error() == 0

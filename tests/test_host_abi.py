@@ -439,3 +439,11 @@ def test_plan_fingerprint_and_validate():
     assert lib.spx_plan_validate(p.handle, 5000, 70001, nnz, spx._ptr(rp), 0, None) == -1  # K differs
     assert lib.spx_plan_validate(p.handle, 5000, 70000, nnz, None, 0, None) == -1
     assert lib.spx_plan_validate(p.handle, 5000, 70000, nnz, spx._ptr(rp), 7, None) == -1  # bad location
+
+
+def test_wait_probe_rejects_limits_out_of_range_without_launching():
+    lib = spx._lib()
+    before = spx.launch_count()
+    assert lib.spx_wait_probe(-1, None) == -1
+    assert lib.spx_wait_probe(3_000_000_000, None) == -1
+    assert spx.launch_count() == before
