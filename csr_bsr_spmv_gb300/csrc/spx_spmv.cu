@@ -514,18 +514,26 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the array on the current device, looked up once per
-// device with that device current (host code must not use the symbol itself).
-spx_status noalloc_partials(float** out) {
+// Device address of the array on the current device, with that device
+// current (host code must not use the symbol itself).  Looked up again on
+// every call made outside stream capture -- a cheap host call -- so a device
+// reset by the caller between calls cannot leave a stale address behind; a
+// call on a capturing stream reuses the address of the last call outside
+// capture, and the first call on a device must come before any capture.
+spx_status noalloc_partials(cudaStream_t st, float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPX_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SPX_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool capturing = cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
+    if (capturing) cudaGetLastError();  // a refused query leaves no sticky error behind
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!capturing) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return SPX_ERR_CUDA;
         g_noalloc_ptr[dev] = static_cast<float*>(p);
     }
+    if (!g_noalloc_ptr[dev]) return SPX_ERR_NOT_READY;
     *out = g_noalloc_ptr[dev];
     return SPX_OK;
 }
@@ -537,7 +545,7 @@ extern "C" spx_status spx_spmv_csr_noalloc(const spx_plan* plan, int32_t M, int3
     if (!spx_plan_ok(plan)) return SPX_ERR_ARG;
     if (plan->counts[2] > SPX_NOALLOC_MAX_SLOTS) return SPX_ERR_SCRATCH_LIMIT;
     float* partials = nullptr;
-    spx_status s = noalloc_partials(&partials);
+    spx_status s = noalloc_partials(reinterpret_cast<cudaStream_t>(stream), &partials);
     if (s != SPX_OK) return s;
     s = check_call(plan, M, K, nnz, row_ptr, col, val, x, y, partials, sizeof(float) * SPX_NOALLOC_MAX_SLOTS);
     if (s != SPX_OK || M == 0) return s;

@@ -53,7 +53,7 @@ typedef enum spx_status {
     SPX_ERR_UNSUPPORTED = -7,  /* shape/type combination this build has no kernel for */
     SPX_ERR_ALIGN = -8,        /* pointer or leading dimension not aligned as documented */
     SPX_ERR_NOMEM = -9,        /* host allocation failed */
-    SPX_ERR_NOT_READY = -10,   /* plan used before spx_plan_upload */
+    SPX_ERR_NOT_READY = -10,   /* plan used before spx_plan_upload (or see spx_spmv_csr_noalloc) */
     SPX_ERR_SCRATCH_LIMIT = -11 /* needs more scratch than the library's fixed buffer holds */
 } spx_status;
 
@@ -377,9 +377,13 @@ spx_status spx_spmv_csr_dual(const spx_plan* plan_A, const spx_plan* plan_At, in
  *   - A plan needing more than SPX_NOALLOC_MAX_SLOTS partial sums (split-row
  *     segments; spx_plan_info_t.slots) is rejected with
  *     SPX_ERR_SCRATCH_LIMIT before anything is launched.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on the device.
+ *   - Each call made outside stream capture looks up the array's device
+ *     address (cudaGetSymbolAddress, with the calling device current), so a
+ *     cudaDeviceReset between calls is picked up by the next such call.  A
+ *     call on a capturing stream reuses the address the last call outside
+ *     capture found on that device: make the first call on each device before
+ *     any stream capture there (SPX_ERR_NOT_READY otherwise), and do not
+ *     reset the device between that call and the end of the capture.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents; each slot is written before it is read within a call,
  *     so nothing needs clearing.  Calls that overlap in time on the GPU

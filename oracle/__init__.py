@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
 with ``csr_bsr_spmv_gb300`` and never imports it; the arithmetic lives in
 ``oracle.c`` (plain C, fp64 accumulation, single-threaded), built with the
-host C compiler.  Each function's docstring in ``oracle.c`` cites the page
+host C compiler; a second build of the same source with OpenMP runs the
+products' independent row loops on all host cores for the CPU baseline.  Each function's docstring in ``oracle.c`` cites the page
 section it follows.
 """
 from __future__ import annotations
@@ -19,8 +20,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 OK, ERR_ARG, ERR_INDEX, ERR_DUP = 0, -1, -2, -4
 
@@ -43,45 +46,68 @@ class RowStats(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
-def build(force: bool = False) -> str:
-    """Compile liboracle.so: -O2, no fast-math, no FMA contraction."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile liboracle.so: -O2, no fast-math, no FMA contraction.  With
+    openmp=True the same source goes to liboracle_omp.so with -fopenmp: the
+    all-core build that the CPU baseline times (row loops on all cores)."""
+    out = _LIB_OMP if openmp else _LIB
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fno-fast-math",
-                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _LIB)
-    return _LIB
+                               "-ffp-contract=off"] + (["-fopenmp"] if openmp else []) + [_SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, out)
+    return out
 
 
-def _lib_():
-    global _lib
+def _lib_(threads: int = 1):
+    """The single-thread library, or with threads > 1 the all-core build set to that many threads."""
+    global _lib, _lib_omp
+    if threads > 1:
+        with _lock:
+            if _lib_omp is None:
+                lib = ctypes.CDLL(build(openmp=True))
+                _declare(lib)
+                _lib_omp = lib
+        _lib_omp.or_threads(int(threads))
+        return _lib_omp
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(build())
-            vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-            sig = {
-                "or_build_csr": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
-                "or_transpose": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
-                "or_build_bsr": [i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp],
-                "or_row_stats": [i32, vp, vp],
-                "or_plan_spmv": [i32, vp, vp, vp, vp, vp],
-                "or_plan_opts_auto": [vp, vp],
-                "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
-                "or_spmv_coo": [i32, i32, i64, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
-                "or_build_wcsr": [i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
-                                  ctypes.POINTER(ctypes.c_double)],
-                "or_build_sell": [i32, vp, vp, vp, i32, i32, ctypes.POINTER(ctypes.c_int64),
-                                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
-                                  ctypes.POINTER(ctypes.c_int64), vp, vp, vp, vp, vp],
-                "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
-                "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
-            }
-            for name, args in sig.items():
-                f = getattr(lib, name)
-                f.argtypes = args
-                f.restype = ctypes.c_int
+            _declare(lib)
             _lib = lib
     return _lib
+
+
+def omp_threads(threads: int) -> int:
+    """Threads the all-core build actually runs with when asked for `threads`."""
+    return int(_lib_(max(2, threads)).or_threads(int(threads)))
+
+
+def _declare(lib):
+    vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    sig = {
+        "or_build_csr": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
+        "or_transpose": [i32, i32, i64, vp, vp, vp, i32, vp, vp, vp],
+        "or_build_bsr": [i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp],
+        "or_row_stats": [i32, vp, vp],
+        "or_plan_spmv": [i32, vp, vp, vp, vp, vp],
+        "or_plan_opts_auto": [vp, vp],
+        "or_spmv": [i32, vp, vp, vp, vp, dbl, dbl, vp, vp, i64, vp, vp],
+        "or_spmv_f32": [i32, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp, i64, vp],
+        "or_threads": [i32],
+        "or_spmv_coo": [i32, i32, i64, vp, vp, vp, vp, dbl, dbl, vp, vp, vp],
+        "or_build_wcsr": [i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
+                          ctypes.POINTER(ctypes.c_double)],
+        "or_build_sell": [i32, vp, vp, vp, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                          ctypes.POINTER(ctypes.c_int64), vp, vp, vp, vp, vp],
+        "or_spmm": [i32, i32, vp, vp, vp, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
+        "or_bsr_spmm": [i32, i32, i32, i32, vp, vp, vp, i32, vp, i64, dbl, dbl, vp, i64, vp, i64, vp, vp],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
 
 
 def _p(a):
@@ -199,6 +225,14 @@ def plan_opts_auto(M, rp):
     return {f: getattr(o, f) for f in PLAN_FIELDS}
 
 
+def plan_opts_from_stats(stats):
+    """Plan options the statistics rule picks for a row-statistics record (dict with the RowStats fields)."""
+    st = RowStats(**{f: stats[f] for f, _ in RowStats._fields_})
+    o = PlanOpts()
+    _check(_lib_().or_plan_opts_auto(ctypes.byref(st), ctypes.byref(o)))
+    return {f: getattr(o, f) for f in PLAN_FIELDS}
+
+
 def plan_spmv(M, rp, **opts):
     """Returns dict(tasks[ntasks,4], longrows[nlong,4], counts)."""
     rp = _c(rp, np.int32)
@@ -214,17 +248,30 @@ def plan_spmv(M, rp, **opts):
     return dict(tasks=tasks, longrows=longrows, counts=dict(zip(names, (int(c) for c in counts))))
 
 
-def spmv(M, rp, col, val, x, alpha=1.0, beta=0.0, y=None, rows=None):
-    """(ref, bound) in fp64, for all rows or the given sample of rows."""
+def spmv(M, rp, col, val, x, alpha=1.0, beta=0.0, y=None, rows=None, threads=1):
+    """(ref, bound) in fp64, for all rows or the given sample of rows
+    (threads > 1: the all-core build, same result)."""
     rp, col, val, x = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32), _c(x, np.float32)
     yv = _c(y, np.float32) if (y is not None and beta != 0.0) else None
     rr = None if rows is None else _c(rows, np.int32)
     n = M if rr is None else rr.size
     ref = np.empty(n, np.float64)
     bnd = np.empty(n, np.float64)
-    _check(_lib_().or_spmv(M, _p(rp), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv), _p(rr),
-                           0 if rr is None else rr.size, _p(ref), _p(bnd)))
+    _check(_lib_(threads).or_spmv(M, _p(rp), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv), _p(rr),
+                                  0 if rr is None else rr.size, _p(ref), _p(bnd)))
     return ref, bnd
+
+
+def spmv_f32(M, rp, col, val, x, alpha=1.0, beta=0.0, y=None, rows=None):
+    """The fp32 index-order SpMV (products and running sums rounded to fp32), for all rows or a sample."""
+    rp, col, val, x = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32), _c(x, np.float32)
+    yv = _c(y, np.float32) if (y is not None and beta != 0.0) else None
+    rr = None if rows is None else _c(rows, np.int32)
+    n = M if rr is None else rr.size
+    out = np.empty(max(n, 1), np.float32)
+    _check(_lib_().or_spmv_f32(M, _p(rp), _p(col), _p(val), _p(x), float(alpha), float(beta), _p(yv), _p(rr),
+                               0 if rr is None else rr.size, _p(out)))
+    return out[:n]
 
 
 def spmv_coo(M, K, row, col, val, x, alpha=1.0, beta=0.0, y=None):
@@ -238,7 +285,7 @@ def spmv_coo(M, K, row, col, val, x, alpha=1.0, beta=0.0, y=None):
     return ref[:M], bnd[:M]
 
 
-def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None):
+def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None, threads=1):
     rp, col, val = _c(rp, np.int32), _c(col, np.int32), _c(val, np.float32)
     B = _c(B, np.float32)
     N = B.shape[1]
@@ -247,12 +294,12 @@ def spmm(M, rp, col, val, B, alpha=1.0, beta=0.0, C=None, rows=None):
     n = M if rr is None else rr.size
     ref = np.empty((n, N), np.float64)
     bnd = np.empty((n, N), np.float64)
-    _check(_lib_().or_spmm(M, N, _p(rp), _p(col), _p(val), _p(B), N, float(alpha), float(beta), _p(Cv),
+    _check(_lib_(threads).or_spmm(M, N, _p(rp), _p(col), _p(val), _p(B), N, float(alpha), float(beta), _p(Cv),
                            N if Cv is not None else 0, _p(rr), 0 if rr is None else rr.size, _p(ref), _p(bnd)))
     return ref, bnd
 
 
-def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None, alpha=1.0, beta=0.0, C=None):
+def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None, alpha=1.0, beta=0.0, C=None, threads=1):
     brp, bcol = _c(brp, np.int32), _c(bcol, np.int32)
     bval = _c(bval_bf16, np.uint16)
     B = _c(B_bf16, np.uint16)
@@ -262,7 +309,7 @@ def bsr_spmm(M, K, br, bc, brp, bcol, bval_bf16, B_bf16, rows=None, alpha=1.0, b
     ref = np.empty((n, N), np.float64)
     bnd = np.empty((n, N), np.float64)
     Cv = _c(C, np.float32) if (C is not None and beta != 0.0) else None
-    _check(_lib_().or_bsr_spmm(M, K, br, bc, _p(brp), _p(bcol), _p(bval), N, _p(B), N, float(alpha), float(beta),
+    _check(_lib_(threads).or_bsr_spmm(M, K, br, bc, _p(brp), _p(bcol), _p(bval), N, _p(B), N, float(alpha), float(beta),
                                _p(Cv), N if Cv is not None else 0, _p(rr), 0 if rr is None else rr.size, _p(ref),
                                _p(bnd)))
     return ref, bnd

@@ -7,7 +7,11 @@
  *
  * Every function is the plain definition written out: single-threaded,
  * index order, fp64 accumulation for floating point, comparison sorts where
- * the library uses counting sorts.  No blocking, fusion or reordering.
+ * the library uses counting sorts.  No blocking, fusion or reordering.  The
+ * same source built a second time with -fopenmp (liboracle_omp.so) runs the
+ * independent row loops of the products on all host cores, for the CPU
+ * baseline only; each row is still summed alone in index order, so no
+ * result changes.
  *
  * Pages cited (by title and section):
  *   [SpMM-ops]  "通用稀疏矩阵乘法CUDA算子实现" (chengzipai.xyz)
@@ -20,6 +24,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_ERR_ARG (-1)
@@ -360,9 +367,13 @@ int or_spmv(int32_t M, const int32_t* rp, const int32_t* col, const float* val, 
             double beta, const float* y_in, const int32_t* rows, int64_t nrows, double* ref, double* bound) {
     if (M < 0) return OR_ERR_ARG;
     int64_t n = rows ? nrows : M;
+    for (int64_t k = 0; rows && k < n; ++k)
+        if (rows[k] < 0 || rows[k] >= M) return OR_ERR_INDEX;
+    /* rows are independent: the all-core build (-fopenmp) hands them out to
+       threads; every row is still summed alone, in p order */
+#pragma omp parallel for schedule(dynamic, 256)
     for (int64_t k = 0; k < n; ++k) {
         int32_t i = rows ? rows[k] : (int32_t)k;
-        if (i < 0 || i >= M) return OR_ERR_INDEX;
         double acc = 0.0, mag = 0.0;
         for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
             double t = (double)val[p] * (double)x[col[p]];
@@ -376,6 +387,36 @@ int or_spmv(int32_t M, const int32_t* rp, const int32_t* col, const float* val, 
         }
         ref[k] = r;
         if (bound) bound[k] = b;
+    }
+    return OR_OK;
+}
+
+/*
+ * The same product summed the way a plain fp32 loop would: each product
+ * val_p * x[col_p] rounded to fp32, added in p order to an fp32 running sum
+ * (no fused multiply-add), then y_i = alpha * sum + beta * y_i in fp32.
+ * [SpMM-ops] §5 (check a lower-precision result against a higher-precision
+ * reference and report the error): this is the low-precision side.  Its
+ * distance to or_spmv obeys the textbook bound for a recursively summed dot
+ * product of length l, |fl(s) - s| <= gamma_l * sum |val_p x_col_p| with
+ * gamma_l = l u / (1 - l u), u = 2^-24, which the tests check.
+ */
+int or_spmv_f32(int32_t M, const int32_t* rp, const int32_t* col, const float* val, const float* x, float alpha,
+                float beta, const float* y_in, const int32_t* rows, int64_t nrows, float* out) {
+    if (M < 0) return OR_ERR_ARG;
+    int64_t n = rows ? nrows : M;
+    for (int64_t k = 0; rows && k < n; ++k)
+        if (rows[k] < 0 || rows[k] >= M) return OR_ERR_INDEX;
+    for (int64_t k = 0; k < n; ++k) {
+        int32_t i = rows ? rows[k] : (int32_t)k;
+        float acc = 0.0f;
+        for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
+            float t = val[p] * x[col[p]];
+            acc = acc + t;
+        }
+        float r = alpha * acc;
+        if (beta != 0.0f) r = r + beta * y_in[i];
+        out[k] = r;
     }
     return OR_OK;
 }
@@ -597,35 +638,43 @@ int or_spmm(int32_t M, int32_t N, const int32_t* rp, const int32_t* col, const f
             int64_t nrows, double* ref, double* bound) {
     if (M < 0 || N < 0) return OR_ERR_ARG;
     int64_t n = rows ? nrows : M;
-    double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * (N ? N : 1)));
-    if (!acc) return OR_ERR_NOMEM;
-    double* mag = acc + N;
-    for (int64_t k = 0; k < n; ++k) {
-        int32_t i = rows ? rows[k] : (int32_t)k;
-        if (i < 0 || i >= M) { free(acc); return OR_ERR_INDEX; }
-        for (int32_t c = 0; c < N; ++c) { acc[c] = 0.0; mag[c] = 0.0; }
-        for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
-            double a = (double)val[p];
-            const float* brow = B + (int64_t)col[p] * ldb;
+    for (int64_t k = 0; rows && k < n; ++k)
+        if (rows[k] < 0 || rows[k] >= M) return OR_ERR_INDEX;
+    int err = OR_OK;
+    /* rows are independent: the all-core build (-fopenmp) hands them out to
+       threads, each with its own accumulators */
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * (N ? N : 1)));
+        double* mag = acc ? acc + N : NULL;
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t k = 0; k < n; ++k) {
+            if (!acc) { err = OR_ERR_NOMEM; continue; }
+            int32_t i = rows ? rows[k] : (int32_t)k;
+            for (int32_t c = 0; c < N; ++c) { acc[c] = 0.0; mag[c] = 0.0; }
+            for (int64_t p = rp[i]; p < rp[i + 1]; ++p) {
+                double a = (double)val[p];
+                const float* brow = B + (int64_t)col[p] * ldb;
+                for (int32_t c = 0; c < N; ++c) {
+                    double t = a * (double)brow[c];
+                    acc[c] += t;
+                    mag[c] += fabs(t);
+                }
+            }
             for (int32_t c = 0; c < N; ++c) {
-                double t = a * (double)brow[c];
-                acc[c] += t;
-                mag[c] += fabs(t);
+                double r = alpha * acc[c], b = fabs(alpha) * mag[c];
+                if (beta != 0.0) {
+                    double y = (double)C_in[(int64_t)i * ldc + c];
+                    r += beta * y;
+                    b += fabs(beta * y);
+                }
+                ref[k * N + c] = r;
+                if (bound) bound[k * N + c] = b;
             }
         }
-        for (int32_t c = 0; c < N; ++c) {
-            double r = alpha * acc[c], b = fabs(alpha) * mag[c];
-            if (beta != 0.0) {
-                double y = (double)C_in[(int64_t)i * ldc + c];
-                r += beta * y;
-                b += fabs(beta * y);
-            }
-            ref[k * N + c] = r;
-            if (bound) bound[k * N + c] = b;
-        }
+        free(acc);
     }
-    free(acc);
-    return OR_OK;
+    return err;
 }
 
 /* -------------------------------------------------------------- BSR SpMM */
@@ -652,39 +701,62 @@ int or_bsr_spmm(int32_t M, int32_t K, int32_t br, int32_t bc, const int32_t* bsr
                 const float* C_in, int64_t ldc, const int32_t* rows, int64_t nrows, double* ref, double* bound) {
     if (M < 0 || K < 0 || N < 0 || br <= 0 || bc <= 0) return OR_ERR_ARG;
     int64_t n = rows ? nrows : M;
-    double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * (N ? N : 1)));
-    if (!acc) return OR_ERR_NOMEM;
-    double* mag = acc + N;
-    for (int64_t k = 0; k < n; ++k) {
-        int32_t i = rows ? rows[k] : (int32_t)k;
-        if (i < 0 || i >= M) { free(acc); return OR_ERR_INDEX; }
-        int32_t I = i / br, r = i % br;
-        for (int32_t c = 0; c < N; ++c) { acc[c] = 0.0; mag[c] = 0.0; }
-        for (int64_t blk = bsr_rp[I]; blk < bsr_rp[I + 1]; ++blk) {
-            const uint16_t* arow = bval + blk * (int64_t)br * bc + (int64_t)r * bc;
-            for (int32_t cc = 0; cc < bc; ++cc) {
-                int64_t kk = (int64_t)bcol[blk] * bc + cc;
-                if (kk >= K) break;
-                double a = bf16_to_double(arow[cc]);
-                const uint16_t* brow = B + kk * ldb;
-                for (int32_t c = 0; c < N; ++c) {
-                    double t = a * bf16_to_double(brow[c]);
-                    acc[c] += t;
-                    mag[c] += fabs(t);
+    for (int64_t k = 0; rows && k < n; ++k)
+        if (rows[k] < 0 || rows[k] >= M) return OR_ERR_INDEX;
+    int err = OR_OK;
+    /* rows are independent: the all-core build (-fopenmp) hands them out to
+       threads, each with its own accumulators */
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)(2 * (N ? N : 1)));
+        double* mag = acc ? acc + N : NULL;
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t k = 0; k < n; ++k) {
+            if (!acc) { err = OR_ERR_NOMEM; continue; }
+            int32_t i = rows ? rows[k] : (int32_t)k;
+            int32_t I = i / br, r = i % br;
+            for (int32_t c = 0; c < N; ++c) { acc[c] = 0.0; mag[c] = 0.0; }
+            for (int64_t blk = bsr_rp[I]; blk < bsr_rp[I + 1]; ++blk) {
+                const uint16_t* arow = bval + blk * (int64_t)br * bc + (int64_t)r * bc;
+                for (int32_t cc = 0; cc < bc; ++cc) {
+                    int64_t kk = (int64_t)bcol[blk] * bc + cc;
+                    if (kk >= K) break;
+                    double a = bf16_to_double(arow[cc]);
+                    const uint16_t* brow = B + kk * ldb;
+                    for (int32_t c = 0; c < N; ++c) {
+                        double t = a * bf16_to_double(brow[c]);
+                        acc[c] += t;
+                        mag[c] += fabs(t);
+                    }
                 }
             }
-        }
-        for (int32_t c = 0; c < N; ++c) {
-            double r = alpha * acc[c], b = fabs(alpha) * mag[c];
-            if (beta != 0.0) {
-                double y = (double)C_in[(int64_t)i * ldc + c];
-                r += beta * y;
-                b += fabs(beta * y);
+            for (int32_t c = 0; c < N; ++c) {
+                double rr = alpha * acc[c], b = fabs(alpha) * mag[c];
+                if (beta != 0.0) {
+                    double y = (double)C_in[(int64_t)i * ldc + c];
+                    rr += beta * y;
+                    b += fabs(beta * y);
+                }
+                ref[k * N + c] = rr;
+                if (bound) bound[k * N + c] = b;
             }
-            ref[k * N + c] = r;
-            if (bound) bound[k * N + c] = b;
         }
+        free(acc);
     }
-    free(acc);
-    return OR_OK;
+    return err;
+}
+
+/*
+ * Threads of the all-core build: the same source compiled with -fopenmp runs
+ * the row loops above on `threads` host threads (rows are independent, so no
+ * result changes).  The single-thread build ignores the request and reports 1.
+ */
+int or_threads(int32_t threads) {
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+    return omp_get_max_threads();
+#else
+    (void)threads;
+    return 1;
+#endif
 }

@@ -203,6 +203,7 @@ def test_row_stats_device_equals_host(M, lmin, lmax):
     want = spx.spx_row_stats(M, rp)
     got = spx.spx_row_stats(M, cuda(rp))
     assert got == want
+    assert got == oracle.row_stats(M, rp)
 
 
 def test_row_stats_device_power_law():
@@ -213,6 +214,7 @@ def test_row_stats_device_power_law():
     rp[1:] = np.cumsum(lengths)
     got = spx.spx_row_stats(M, cuda(rp))
     assert got == spx.spx_row_stats(M, rp)
+    assert got == oracle.row_stats(M, rp)
     srt = np.sort(lengths)
     assert [got["p50"], got["p95"], got["p99"]] == [int(srt[(q * M + 99) // 100 - 1]) for q in (50, 95, 99)]
     assert got["max"] == int(srt[-1]) and got["min"] == int(srt[0])

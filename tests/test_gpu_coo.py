@@ -132,3 +132,31 @@ def test_bad_indices_reported(bad):
     g = guard.cpu().numpy()
     assert np.all(g[:32] == 123.0) and np.all(g[32 + M:] == 123.0)
     assert spx.spx_last_device_error() == 0  # the word is cleared by the read
+
+
+@pytest.mark.slow
+def test_power_law_full_size_every_row():
+    """The benchmarked COO workload at full size: the 4,194,304-row power-law matrix (67.1M row-sorted
+    triplets, 32,769 chunks, rows of up to ~10^5 entries spanning many chunks), y = Ax + 0.5y, in the
+    launch configuration the benchmark times -- every output row against the oracle, and bitwise
+    equal on a second run."""
+    cfg = synth.power_law_rows()
+    M, K = cfg["M"], cfg["K"]
+    row, col, val = cfg["row"], cfg["col"], cfg["val"]
+    assert np.all(np.diff(row) >= 0)
+    drow, dcol, dval, dx = dev(row), dev(col), dev(val), dev(cfg["x"])
+    scratch = torch.empty(max(1, spx.spx_spmv_coo_scratch_bytes(row.size) // 4), device="cuda")
+    outs = []
+    for _ in range(2):
+        y = dev(cfg["y"])
+        spx.spx_spmv_coo(M, K, drow, dcol, dval, dx, y, cfg["alpha"], cfg["beta"], scratch=scratch)
+        torch.cuda.synchronize()
+        assert spx.spx_last_device_error() == 0
+        outs.append(y.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    ref, bound = oracle.spmv_coo(M, K, row, col, val, cfg["x"], cfg["alpha"], cfg["beta"], cfg["y"])
+    assert_within(outs[0], ref, bound, what="power-law COO full size")
+    # the rows that cross chunk boundaries are among them; make sure there are many
+    starts = np.arange(0, row.size, CHUNK)
+    crossing = np.unique(row[starts[1:]][row[starts[1:]] == row[starts[1:] - 1]])
+    assert crossing.size > 1000

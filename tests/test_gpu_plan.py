@@ -1,7 +1,8 @@
 """The dispatch plan built on the GPU from a device row_ptr ([SpMM-ops] §2.1-§2.4:
 packed groups, CTA rows, split rows with their segments and partial-sum slots)
 must equal the host builder's plan task for task: the documented task list,
-the split-row table, the uploaded device table, the counts and the statistics.
+the split-row table, the uploaded device table, the counts and the statistics;
+and both must equal the oracle's plan and statistics.
 Cases cover long chains of groups (no long rows at all), every row long, empty
 rows, tiny and extreme options, and the full 4,194,304-row power-law matrix;
 bad row offsets get the host checks' error codes."""
@@ -9,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from csr_bsr_spmv_gb300 import spx
 
@@ -35,6 +37,14 @@ def _same_plan(M, rp, opts=None):
     # the structure fingerprint: the same on both sides, and each side validates the other's row_ptr
     assert pd.fingerprint == ph.fingerprint
     assert pd.validate(rp) == 0 and ph.validate(torch.from_numpy(rp).cuda()) == 0
+    # and the oracle's plan, built from the same row offsets with the same (resolved) options
+    full = oracle.plan_opts_auto(M, rp) if opts is None else dict(spx.spx_plan_opts_default(), **opts)
+    assert pd.opts == full
+    w = oracle.plan_spmv(M, rp, **full)
+    assert np.array_equal(td, w["tasks"]) and np.array_equal(ld, w["longrows"])
+    for k, v in w["counts"].items():
+        assert pd.info[k] == v, k
+    assert pd.stats == oracle.row_stats(M, rp)
     return ph.info
 
 

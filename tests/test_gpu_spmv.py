@@ -11,7 +11,7 @@ import torch
 import oracle
 import synth
 from csr_bsr_spmv_gb300 import spx
-from gpu_util import assert_within, csr_to_device, dev
+from gpu_util import FP32_ABS, FP32_REL, assert_within, csr_to_device, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -144,6 +144,58 @@ def test_power_law_full_size_sampled():
     ref, bound = oracle.spmv(M, rp, col, val, cfg["x"], 1.0, 0.5, cfg["y"], rows=rows)
     assert_within(got[rows], ref, bound, what="power-law full size")
     assert plan.info["split_rows"] > 0 and plan.info["cta_rows"] > 0
+    tolerance_self_check(got[rows], M, rp, col, val, cfg["x"], 1.0, 0.5, cfg["y"], rows=rows)
+
+
+# ------------------------------------------------------------ the tolerance self-check
+
+def _gamma(n):
+    """gamma_n = n u / (1 - n u), u = 2^-24: the rounding-error factor of a sum of fp32 products
+    with at most n roundings along any path from an input to the result."""
+    u = 2.0 ** -24
+    return n * u / (1.0 - n * u)
+
+
+def tolerance_self_check(got, M, rp, col, val, x, alpha, beta, y0, rows=None):
+    """[SpMM-ops] §5: check the low-precision result against a reference and report the error.
+    (1) Against the fp32 index-order oracle, the stated tolerance widened by that oracle's own
+    rounding bound gamma_(l+4) * bound.  (2) Against the fp64 oracle, the rounding bound itself:
+    any fp32 summation order of l products (a tree, segments and a fix-up, fused multiply-adds)
+    plus the alpha/beta epilogue has at most l + 4 roundings on every path, so a correct kernel
+    can never leave it -- a test tolerance or bound formula that is too loose or too tight shows."""
+    ref, bound = oracle.spmv(M, rp, col, val, x, alpha, beta, y0, rows=rows)
+    r32 = oracle.spmv_f32(M, rp, col, val, x, alpha, beta, y0, rows=rows).astype(np.float64)
+    L = np.diff(rp).astype(np.float64)
+    if rows is not None:
+        L = L[rows]
+    g = _gamma(L + 4)
+    got = np.asarray(got, np.float64)
+    e32 = np.abs(got - r32)
+    assert np.all(e32 <= (FP32_REL + g) * bound + FP32_ABS), "GPU vs fp32 index-order oracle"
+    e64 = np.abs(got - ref)
+    assert np.all(e64 <= g * bound), "GPU vs fp64 oracle outside the fp32 rounding bound"
+    return float(np.max(e64 / np.maximum(g * bound, 1e-300), initial=0.0))
+
+
+@pytest.mark.parametrize("opts", [None, SMALL_OPTS[1], SMALL_OPTS[6], SMALL_OPTS[11]])
+def test_tolerance_self_check_power_law_small(opts):
+    M = 3000
+    L, _ = synth.lengths_zipf(3, M, 2.1, 100000, 12.0)
+    L[:2] = (100000, 0)
+    row, col = synth.cols_uniform(3, 200000, L)
+    val = synth.uniform(3, synth.T_VAL, row.size)
+    rp, col, val = oracle.build_csr(M, 200000, row, col, val)
+    x = synth.uniform(3, synth.T_X, 200000)
+    y0 = synth.uniform(3, synth.T_Y, M)
+    got, _ = run_spmv(M, 200000, rp, col, val, x, y0, -1.5, 0.5, opts)
+    tolerance_self_check(got, M, rp, col, val, x, -1.5, 0.5, y0)
+
+
+def test_tolerance_self_check_uniform_short_rows():
+    cfg = synth.uniform_short_rows()
+    rp, col, val = oracle.build_csr(cfg["M"], cfg["K"], cfg["row"], cfg["col"], cfg["val"])
+    got, _ = run_spmv(cfg["M"], cfg["K"], rp, col, val, cfg["x"], cfg["y"], cfg["alpha"], cfg["beta"])
+    tolerance_self_check(got, cfg["M"], rp, col, val, cfg["x"], cfg["alpha"], cfg["beta"], cfg["y"])
 
 
 def test_gather_probe_reads_every_nonzero():

@@ -504,3 +504,123 @@ def test_plan_invariants(seed, div):
     for (k1, a1, b1, _), (k2, a2, b2, _) in zip(groups, groups[1:]):
         if b1 == a2:
             assert b1 - a1 == o["block_rows"] or L[a1:b1].sum() + L[a2] > o["block_nnz"]
+
+
+# ------------------------------------------------------------ the automatic plan options
+
+# The rule as this library defines it (the pages give the dispatch key -- mean,
+# spread and tail of the row lengths -- but no thresholds, [SpMM-ops] §4): a
+# coefficient of variation of 2 or more picks 1024-nonzero groups with the
+# segmented reduction, anything below keeps the defaults.  Written out here
+# field by field, not taken from either implementation.
+RULE_SKEWED = dict(block_nnz=1024, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=0)
+RULE_DEFAULT = dict(block_nnz=2048, block_rows=256, pack_max=512, cta_max=8192, seg_nnz=4096, lanes_div=16)
+
+
+def _stats(cv, **kw):
+    base = dict(rows=1000, nnz=16000, sumsq=400000, min=1, max=300, p50=10, p95=60, p99=200, empty=0,
+                mean=16.0, var=(cv * 16.0) ** 2, cv=cv)
+    base.update(kw)
+    return base
+
+
+@pytest.mark.parametrize("cv,skewed", [(0.0, False), (0.5, False), (1.0, False), (np.nextafter(2.0, 0.0), False),
+                                       (2.0, True), (np.nextafter(2.0, 3.0), True), (2.5, True), (40.0, True)])
+def test_plan_opts_auto_threshold(cv, skewed):
+    """The cv >= 2 edge, one ulp either side of it, and every field of both outcomes."""
+    assert oracle.plan_opts_from_stats(_stats(cv)) == (RULE_SKEWED if skewed else RULE_DEFAULT)
+
+
+def test_plan_opts_auto_reads_only_cv():
+    """Extreme values in every other field (an enormous tail, all-empty rows, a huge mean) do not move the choice."""
+    for kw in (dict(max=200000, p99=100000, p95=50000), dict(empty=1000, min=0, nnz=0, mean=0.0),
+               dict(mean=1e6, nnz=10 ** 12, sumsq=10 ** 15), dict(rows=1, p50=0)):
+        assert oracle.plan_opts_from_stats(_stats(1.99, **kw)) == RULE_DEFAULT
+        assert oracle.plan_opts_from_stats(_stats(2.01, **kw)) == RULE_SKEWED
+
+
+def test_plan_opts_auto_on_the_worked_example(ex):
+    """The worked example's lengths [2, 1, 3, 1, 1]: mean 1.6, variance 0.64, cv 0.5 -> the defaults."""
+    g, _, _ = ex
+    rp = np.array(g["printed"]["csr_row_ptr"], np.int32)
+    st = oracle.row_stats(5, rp)
+    assert st["cv"] == pytest.approx(0.5, rel=1e-15)
+    assert oracle.plan_opts_from_stats(st) == RULE_DEFAULT
+    assert oracle.plan_opts_auto(5, rp) == RULE_DEFAULT
+
+
+def test_plan_opts_auto_on_closed_form_lengths():
+    """Lengths with a cv known in closed form: constant rows (cv 0) and one row of n with M-1 empty rows
+    (cv = sqrt(M - 1)): M = 4 gives sqrt(3) < 2, M = 5 gives exactly 2, M = 6 gives sqrt(5) > 2."""
+    for M, want in ((4, RULE_DEFAULT), (5, RULE_SKEWED), (6, RULE_SKEWED)):
+        rp = np.array([0] + [7] * M, np.int32)
+        st = oracle.row_stats(M, rp)
+        assert st["cv"] == pytest.approx(np.sqrt(M - 1), rel=1e-15)
+        assert oracle.plan_opts_auto(M, rp) == want
+    rp = np.arange(0, 9 * 100 + 1, 9, dtype=np.int32)
+    assert oracle.row_stats(100, rp)["cv"] == 0.0 and oracle.plan_opts_auto(100, rp) == RULE_DEFAULT
+
+
+# ------------------------------------------------------------ the fp32 sequential variant
+
+U32 = 2.0 ** -24
+
+
+def gamma(n):
+    """gamma_n = n u / (1 - n u): the textbook bound on the relative error of n
+    fp32 roundings in a recursively summed dot product (u = 2^-24)."""
+    return n * U32 / (1.0 - n * U32)
+
+
+def _f32_bound_check(M, rp, col, val, x, alpha, beta, y0):
+    ref, bound = oracle.spmv(M, rp, col, val, x, alpha, beta, y0)
+    r32 = oracle.spmv_f32(M, rp, col, val, x, alpha, beta, y0).astype(np.float64)
+    L = np.diff(rp).astype(np.float64)
+    # l products and l - 1 additions in the row, then alpha * s, beta * y and their sum: at most l + 2
+    # roundings along any path; the fp64 reference's own error (2^-52 per step) is added for rigour
+    tol = gamma(L + 2) * bound + (L + 2) * 2.0 ** -52 * bound
+    err = np.abs(r32 - ref)
+    assert np.all(err <= tol), np.max(err - tol)
+    return err, ref, bound
+
+
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-1.5, 0.5)])
+def test_fp32_sequential_within_textbook_bound(seed, alpha, beta):
+    """Random rows of lengths 0 .. 200,000 with values and x in [-1, 1): the fp32 index-order sum stays within
+    gamma_(l+2) times the oracle's bound of the fp64 result, row by row."""
+    L, _ = synth.lengths_zipf(seed, 2000, 2.1, 200_000, 30.0)
+    L[:2] = (200_000, 0)
+    row, col = synth.cols_uniform(seed, 300_000, L)
+    val = synth.uniform(seed, synth.T_VAL, row.size)
+    rp, col, val = oracle.build_csr(L.size, 300_000, row, col, val)
+    x = synth.uniform(seed, synth.T_X, 300_000)
+    y0 = synth.uniform(seed, synth.T_Y, L.size)
+    _f32_bound_check(L.size, rp, col, val, x, alpha, beta, y0)
+
+
+def test_fp32_sequential_exact_on_small_integers():
+    """Small-integer values and x: every fp32 partial sum is an integer below 2^24, so both variants agree exactly."""
+    d = synth.random_coo(12, 300, 200, 0, 60)
+    rp, col, _ = oracle.build_csr(300, 200, d["row"], d["col"], d["val"])
+    rng = np.random.default_rng(12)
+    val = rng.integers(-8, 9, col.size).astype(np.float32)
+    x = rng.integers(-8, 9, 200).astype(np.float32)
+    y0 = rng.integers(-8, 9, 300).astype(np.float32)
+    ref, _ = oracle.spmv(300, rp, col, val, x, 2.0, -3.0, y0)
+    assert np.array_equal(oracle.spmv_f32(300, rp, col, val, x, 2.0, -3.0, y0).astype(np.float64), ref)
+
+
+def test_fp32_bound_needs_absolute_values():
+    """Heavy cancellation: l - 1 products of 0.1 then one product of -(l - 1) * 0.1.  The fp32 running sum drifts
+    by far more than gamma_l times |exact sum|, yet stays within gamma_l times sum |products| -- so a bound
+    written with the signed sum (a dropped absolute value) would fail the check above."""
+    for l in (1000, 50_000, 200_000):
+        val = np.full(l, np.float32(0.1), np.float32)
+        val[-1] = np.float32(-(l - 1) * 0.1)
+        col = np.zeros(l, np.int32)
+        rp = np.array([0, l], np.int32)
+        x = np.ones(1, np.float32)
+        err, ref, bound = _f32_bound_check(1, rp, col, val, x, 1.0, 0.0, None)
+        assert err[0] > gamma(l + 2) * abs(ref[0])
+        assert bound[0] > 10 * abs(ref[0])
