@@ -27,7 +27,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdlib>
 #include <cstring>
 #include <type_traits>
 #include <new>
@@ -47,11 +46,13 @@ constexpr uint32_t kBBox = kWin * 64 * 2;      // 64 k-rows x 64 n, 8 KB
 constexpr uint32_t kIdesc = idesc_bf16_mn_k(128, 64);
 constexpr long long kSpinLimit = 2000000000LL;  // cycles (~1 s)
 
-// A stage holds one A chunk and the gathered B rows for 128*HALVES output columns.
-template <int HALVES>
-__host__ __device__ constexpr uint32_t stage_bytes() { return kABytes + 2 * HALVES * kBBox; }
-template <int STAGES, int HALVES>
-constexpr size_t smem_bytes() { return STAGES * stage_bytes<HALVES>() + 1024 + 256; }
+// A 2-deep ring (four CTAs per SM) measured fastest; deeper rings and
+// 256-column tiles were slower.  A stage holds one A chunk and the gathered B
+// rows for 128 output columns (HALVES M = 128 halves).
+constexpr int STAGES = 2;
+constexpr int HALVES = 1;
+constexpr uint32_t kStageBytesW = kABytes + 2 * HALVES * kBBox;  // 24 KB
+constexpr size_t kSmemW = STAGES * kStageBytesW + 1024 + 256;
 
 enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
 
@@ -65,7 +66,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int STAGES, int HALVES, bool TASKS>
+template <bool TASKS>
 __global__ void __launch_bounds__(kThreads)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const int* __restrict__ win_ptr,
                      const int* __restrict__ win_col, const uint16_t* __restrict__ B, long long ldb,
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ int s_issued, s_consumed;
 
     constexpr int kStages = STAGES;
-    constexpr uint32_t kStageBytes = stage_bytes<HALVES>();
+    constexpr uint32_t kStageBytes = kStageBytesW;
     constexpr uint32_t kTmemCols = 64 * HALVES;
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t bars = base + kStages * kStageBytes;
@@ -411,36 +412,15 @@ spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunk
     }
     CUtensorMap tmA;
     if (!make_map(&tmA, win_val, kWin, static_cast<uint64_t>(nchunks) * kWin, kWin * 2)) return SPX_ERR_CUDA;
-    // Variant: 128-column tiles with a 2-deep ring (default: four CTAs per SM,
-    // measured fastest), "s3" / "s4" deeper rings, "wide" 256-column tiles
-    // with a 2-deep ring (N a multiple of 256); SPX_WCSR_VARIANT overrides.
-    static const int env_variant = [] {  // read once, thread-safe
-        int v = 2;
-        if (const char* e = std::getenv("SPX_WCSR_VARIANT")) {
-            if (!std::strcmp(e, "wide")) v = 1;
-            else if (!std::strcmp(e, "s3")) v = 3;
-            else if (!std::strcmp(e, "s4")) v = 4;
-        }
-        return v;
-    }();
-    const int variant = env_variant == 1 && N % 256 ? 2 : env_variant;  // per call: 256-column tiles need N % 256 == 0
-    switch (variant) {
-#define SPX_WCSR_LAUNCH(S, H, T)                                                                               \
+#define SPX_WCSR_LAUNCH(T)                                                                                     \
     do {                                                                                                       \
-        if (set_smem_limit(wcsr_spmm_kernel<S, H, T>, smem_bytes<S, H>()) != cudaSuccess) return SPX_ERR_CUDA; \
-        wcsr_spmm_kernel<S, H, T><<<dim3((N + 128 * H - 1) / (128 * H), static_cast<unsigned>(ntasks)), kThreads, \
-                                    smem_bytes<S, H>(), st>>>(tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, \
-                                                              beta, kSpinLimit, tasks, partials, N);           \
+        if (set_smem_limit(wcsr_spmm_kernel<T>, kSmemW) != cudaSuccess) return SPX_ERR_CUDA;                   \
+        wcsr_spmm_kernel<T><<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kThreads, kSmemW, st>>>(   \
+            tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit, tasks, partials, N);         \
     } while (0)
-#define SPX_WCSR(S, H, V)                                                                                      \
-    case V:                                                                                                    \
-        if (tasks) SPX_WCSR_LAUNCH(S, H, true);                                                                \
-        else SPX_WCSR_LAUNCH(S, H, false);                                                                     \
-        break;
-        SPX_WCSR(2, 2, 1) SPX_WCSR(2, 1, 2) SPX_WCSR(3, 1, 3) SPX_WCSR(4, 1, 4)
-#undef SPX_WCSR
+    if (tasks) SPX_WCSR_LAUNCH(true);
+    else SPX_WCSR_LAUNCH(false);
 #undef SPX_WCSR_LAUNCH
-    }
     uint64_t launches = 1;
     if (nsplit > 0) {
         wcsr_fixup_kernel<<<dim3((N + 255) / 256, kWin, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(

@@ -178,54 +178,6 @@ def test_block_sparse_full_size_sampled():
     assert_within(got, ref, bound, BF16_REL, BF16_ABS, what="block-sparse full size")
 
 
-_TWO_VARIANTS = r"""
-import sys
-import numpy as np
-import torch
-sys.path.insert(0, {root!r})
-import oracle, synth
-from csr_bsr_spmv_gb300 import spx
-
-def bits(a):
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
-
-for N in (128, 256, 128):  # 128 falls back to the default kernel, 256 takes the wide one
-    cfg = synth.block_sparse(3, M=256, K=512, per_row=3, N=N)
-    rp, col, val = oracle.build_csr(256, 512, cfg["row"], cfg["col"], cfg["val_bf16"])
-    brp, bcol, bval, _ = oracle.build_bsr(256, 512, rp, col, val, 64, 64)
-    ref, bound = oracle.bsr_spmm(256, 512, 64, 64, brp, bcol, bval, cfg["B_bf16"])
-    C = torch.empty(256, N, device="cuda")
-    spx.spx_spmm_bsr(256, 512, 64, 64, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(), bits(bval),
-                     bits(cfg["B_bf16"]), C)
-    torch.cuda.synchronize()
-    assert spx.spx_last_device_error() == 0
-    assert (np.abs(C.cpu().numpy() - ref) <= 2e-2 * bound + 1e-3).all(), N
-    wp, wc, wv, _ = oracle.build_wcsr(256, 512, rp, col, val)
-    Cw = torch.empty(256, N, device="cuda")
-    spx.spx_spmm_wcsr(256, 512, torch.from_numpy(wp).cuda(), torch.from_numpy(wc).cuda(), bits(wv.reshape(-1)),
-                      bits(cfg["B_bf16"]), Cw)
-    torch.cuda.synchronize()
-    assert spx.spx_last_device_error() == 0
-    assert (np.abs(Cw.cpu().numpy() - ref) <= 2e-2 * bound + 1e-3).all(), N
-print("ok")
-"""
-
-
-def test_two_kernel_variants_in_one_process():
-    """Two tile-kernel variants of one signature in one process (the default
-    one for N = 128, the 256-column one for N = 256): each raises its own
-    shared-memory limit, so both launch and both are right."""
-    import os
-    import subprocess
-    import sys
-
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, SPX_BSR_VARIANT="wide3", SPX_WCSR_VARIANT="wide")
-    r = subprocess.run([sys.executable, "-c", _TWO_VARIANTS.format(root=root)], env=env, capture_output=True,
-                       text=True, timeout=300)
-    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
-
-
 def _skewed_bsr(M, N, seed=9):
     c = synth.block_sparse_skewed(seed, M=M, N=N)
     rp, col, val = oracle.build_csr(M, c["K"], c["row"], c["col"], c["val_bf16"])
