@@ -241,15 +241,15 @@ def synth_bits(val):
     return synth.to_bf16_bits(val).view(np.int16)
 
 
-def run_ours(args, rank, world):
+def run_ours(args, rank, world, workload=None, cpu_seconds=None):
     import torch
 
     from csr_bsr_spmv_gb300 import spx
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    c = make_workload(args.workload, args.rows)
-    flops, abytes = accounting(c) if not args.workload.startswith("wcsr") else (None, None)  # wcsr: after its build
+    c = make_workload(workload or args.workload, args.rows if workload in (None, args.workload) else 0)
+    flops, abytes = accounting(c) if not c["workload"].startswith("wcsr") else (None, None)  # wcsr: after its build
     M, K = c["M"], c["K"]
     w = c["workload"]
     stream = torch.cuda.Stream(device=dev)
@@ -809,8 +809,8 @@ def run_ours(args, rank, world):
         "step_ms_min": round(min(times), 5), "step_ms_median": round(statistics.median(times), 5),
     }
     line["clocks"] = clk.summary()
-    if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
+    if rank == 0 and world == 1 and not args.no_cpu and cpu_seconds != 0:
+        line["cpu_baseline"] = cpu_baseline(c, budget_s=cpu_seconds or args.cpu_seconds)
     return line
 
 
@@ -823,41 +823,47 @@ def row_major_csr(c, val):
     return rp, c["col"], val
 
 
-def cpu_step_fn(c):
-    """One bounded sample of the workload run by the oracle; returns (fn, flops, sample)."""
+def cpu_step_fn(c, threads=1):
+    """One bounded sample of the workload run by the oracle; returns (fn, flops, sample).
+    threads > 1 runs the oracle's all-core build (OpenMP over rows; the same sums)."""
     import oracle
 
     w = c["workload"]
     M, K = c["M"], c["K"]
+    t = dict(threads=threads)
     if w.startswith("wcsr"):
         import synth
         rp, col, val = row_major_csr(c, synth.bf16_bits_to_f32(c["val_bf16"]))
-        rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every window
+        rows = np.arange(0, M, 64 if threads == 1 else 4, dtype=np.int32)  # rows spread over every window
         Bf = synth.bf16_bits_to_f32(c["B_bf16"]).reshape(K, c["N"])
         fl = 2 * int(np.diff(rp)[rows].sum()) * c["N"]
-        return (lambda: oracle.spmm(M, rp, col, val, Bf, rows=rows)), fl, \
-            f"{rows.size} output rows (one per window) of the {M}x{K} product, nonzero flops"
+        return (lambda: oracle.spmm(M, rp, col, val, Bf, rows=rows, **t)), fl, \
+            f"{rows.size} output rows (every {M // rows.size}th) of the {M}x{K} product, nonzero flops"
     if w.startswith("bsr"):
         rp, col, val = row_major_csr(c, c["val_bf16"])
-        brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
-        rows = np.arange(0, M, 64, dtype=np.int32)  # one row of every block-row
-        nb = np.diff(brp)
+        if "_oracle_bsr" not in c:  # built once per workload (set-up, not timed)
+            c["_oracle_bsr"] = oracle.build_bsr(M, K, rp, col, val, c["bs"], c["bs"])
+        brp, bcol, bval, _ = c["_oracle_bsr"]
+        rows = np.arange(0, M, 64 if threads == 1 else 4, dtype=np.int32)  # rows spread over every block-row
+        nb = np.diff(brp)[rows // c["bs"]]
         fl = 2 * int(nb.sum()) * c["bs"] * c["N"]
-        return (lambda: oracle.bsr_spmm(M, K, c["bs"], c["bs"], brp, bcol, bval, c["B_bf16"], rows=rows)), fl, \
-            f"{rows.size} output rows (one per block-row) of the {M}x{K} BSR product"
+        return (lambda: oracle.bsr_spmm(M, K, c["bs"], c["bs"], brp, bcol, bval, c["B_bf16"], rows=rows, **t)), fl, \
+            f"{rows.size} output rows (every {M // rows.size}th) of the {M}x{K} BSR product, stored-block flops"
     if w == "power-law-coo":
         return (lambda: oracle.spmv_coo(M, K, c["row"], c["col"], c["val"], c["x"], c["alpha"], c["beta"],
-                                        c["y"])), 2 * int(c["row"].size), "the full matrix, one COO SpMV"
+                                        c["y"])), 2 * int(c["row"].size), "the full matrix, one COO SpMV (one core)"
     rp, col, val = row_major_csr(c, c["val"])
     if w in ("power-law", "uniform", "power-law-sell"):
-        return (lambda: oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"])), 2 * int(rp[-1]), \
-            "the full matrix, one SpMV"
+        return (lambda: oracle.spmv(M, rp, col, val, c["x"], c["alpha"], c["beta"], c["y"], **t)), \
+            2 * int(rp[-1]), "the full matrix, one SpMV"
     if w == "dual":
-        trp, tc, tv = oracle.transpose(M, K, rp, col, val)
+        if "_oracle_t" not in c:  # built once per workload (set-up, not timed)
+            c["_oracle_t"] = oracle.transpose(M, K, rp, col, val)
+        trp, tc, tv = c["_oracle_t"]
 
         def f():
-            u1, _ = oracle.spmv(M, rp, col, val, c["v0"], 1.0, -float(c["alphas"][0]), c["u0"])
-            oracle.spmv(K, trp, tc, tv, u1.astype(np.float32), 1.0, -float(c["betas"][0]), c["v0"])
+            u1, _ = oracle.spmv(M, rp, col, val, c["v0"], 1.0, -float(c["alphas"][0]), c["u0"], **t)
+            oracle.spmv(K, trp, tc, tv, u1.astype(np.float32), 1.0, -float(c["betas"][0]), c["v0"], **t)
         return f, 4 * int(rp[-1]), "the full operator pair, one iteration"
     N = c["N"]
     if w.endswith("bf16"):
@@ -867,23 +873,49 @@ def cpu_step_fn(c):
     elif w.endswith("-f16"):
         val = val.astype(np.float16).astype(np.float64)
         c = dict(c, B=c["B_f16"].astype(np.float64))
-    rows = np.arange(0, M, 16, dtype=np.int32)
+    rows = np.arange(0, M, 16 if threads == 1 else 2, dtype=np.int32)
     fl = 2 * int(np.diff(rp)[rows].sum()) * N
-    return (lambda: oracle.spmm(M, rp, col, val, c["B"], rows=rows)), fl, f"every 16th row ({rows.size} rows)"
+    return (lambda: oracle.spmm(M, rp, col, val, c["B"], rows=rows, **t)), fl, f"every {M // rows.size}th row ({rows.size} rows)"
 
 
-def cpu_baseline(c, budget_s=12.0):
-    fn, fl, sample = cpu_step_fn(c)
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _time_sample(fn, budget_s, max_reps=100000):
     fn()  # warm
     n, t0 = 0, time.perf_counter()
     while True:
         fn()
         n += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or n >= 50:
-            break
-    return {"value": round(n * fl / el / 1e9, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{sample}, repeated {n}x ({el:.1f} s, fp64, single thread)"}
+        if el >= budget_s or n >= max_reps:
+            return n, el
+
+
+def cpu_baseline(c, budget_s=12.0):
+    """The oracle on the host cores: one core (the oracle as it stands), and its all-core build
+    (OpenMP over rows on every core this process may use)."""
+    fn, fl, sample = cpu_step_fn(c)
+    n, el = _time_sample(fn, budget_s)
+    out = {"value": round(n * fl / el / 1e9, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": f"{sample}, repeated {n}x ({el:.1f} s, fp64, single thread)"}
+    cores = host_cores()
+    if c["workload"] != "power-law-coo" and cores > 1:
+        try:
+            import oracle
+            used = oracle.omp_threads(cores)
+            fn, fl, sample = cpu_step_fn(c, threads=cores)
+            n, el = _time_sample(fn, budget_s)
+            out["all_cores"] = {"value": round(n * fl / el / 1e9, 4), "unit": "GFLOP/s", "cores": used,
+                                "kind": "oracle (OpenMP build, rows over threads)",
+                                "sample": f"{sample}, repeated {n}x ({el:.1f} s, fp64, {used} threads)"}
+        except Exception as e:  # no OpenMP runtime on this host
+            out["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -910,6 +942,26 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(val, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# The five configured workloads besides the headline (uniform 4096^2 SpMV, the dual pair, the clustered SpMM
+# at N = 32 and 128, the block-sparse BSR SpMM) and the NEXT rows (SELL-C-sigma and COO SpMV on the power-law
+# matrix, the bf16 CSR SpMM, the WCSR SpMM).  The oracle is timed beside the five configured workloads.
+DEFAULT_CONFIGS = ("uniform", "dual", "spmm32", "spmm128", "bsr", "power-law-sell", "power-law-coo", "spmm32-bf16",
+                   "wcsr")
+CPU_CONFIGS = ("uniform", "dual", "spmm32", "spmm128", "bsr")
+
+
+def config_summary(sub: dict) -> dict:
+    """The figures of one configuration's run that the headline line carries for it."""
+    keep = ("value", "unit", "ms_per_step", "step_ms_min", "step_ms_median", "dtype", "config", "hbm_gbs", "roofline",
+            "e2e", "gpu_launches", "clocks", "cpu_baseline", "conversion")
+    out = {k: sub[k] for k in keep if k in sub}
+    det = sub.get("detail", {})
+    for k in ("graph_us_per_call", "graph_note", "warm", "fill_ratio", "nnzb", "nchunks", "useful_gflops", "variant"):
+        if k in det:
+            out[k] = det[k]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -924,7 +976,11 @@ def main():
     ap.add_argument("--no-floor", action="store_true", help="skip timing the stream + gather floor probe")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--configs", default=",".join(DEFAULT_CONFIGS),
+                    help="other workloads measured in the same run, reported under detail.configs ('' for none)")
+    ap.add_argument("--config-cpu-seconds", type=float, default=4.0,
+                    help="CPU oracle time per variant for each of those configurations")
     ap.add_argument("--rows", type=int, default=0, help="smaller power-law matrix (profiling only)")
     ap.add_argument("--plan", default="", help="plan options, e.g. block_nnz=4096,lanes_div=4")
     ap.add_argument("--col-tile", type=int, default=None, help="SpMM column tile (default: automatic)")
@@ -943,6 +999,20 @@ def main():
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world)
+        configs = [w for w in args.configs.split(",") if w and w != args.workload]
+        if configs:
+            import torch
+            line["detail"]["configs"] = {}
+            for w in configs:  # the other workloads, measured the same way in the same run
+                torch.cuda.empty_cache()
+                t0 = time.perf_counter()
+                try:
+                    sub = run_ours(args, rank, world, workload=w,
+                                   cpu_seconds=args.config_cpu_seconds if w in CPU_CONFIGS else 0)
+                    line["detail"]["configs"][w] = config_summary(sub)
+                except Exception as e:  # one configuration failing must not lose the others
+                    line["detail"]["configs"][w] = {"error": f"{type(e).__name__}: {e}"}
+                print(f"bench: {w} done in {time.perf_counter() - t0:.1f} s", file=sys.stderr, flush=True)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if world > 1 and args.impl == "ours":
