@@ -18,11 +18,18 @@
 // tensor pipe, bounds this product: every B tile is read once per block-row
 // that uses its block column.
 //
-// The kernel (bsr_spmm_tile_kernel): non-persistent, one CTA per (128-column
-// tile, block-row), three CTAs per SM, each an independent 3-deep TMA -> MMA
-// ring; many small independent pipelines per SM measured fastest (deeper or
-// shallower rings, 256-column tiles sharing each A block, and a persistent
-// one-CTA-per-SM kernel with a double-buffered accumulator were all slower).
+// Two kernels share the tile (128 output columns x one 64-row block-row), the
+// 3-deep ring of {A block 8 KB, B tile 16 KB} stages and three CTAs per SM:
+//   bsr_spmm_persist_kernel (spx_spmm_bsr): persistent, a static schedule of
+//     tiles per CTA, the ring running on across tiles, a double-buffered TMEM
+//     accumulator so each tile's epilogue overlaps the next tile's MMAs
+//     (86.7 -> 78.5 us on 256 block-rows of 26 blocks, N = 1024);
+//   bsr_spmm_tile_kernel (spx_spmm_bsr_planned): one CTA per (task, column
+//     tile), where tasks are block-rows or pieces of unequal length and the
+//     hardware's dynamic CTA scheduling balances them better.
+// Three CTAs of three stages per SM measured fastest: two CTAs of four
+// stages, four of two and one of five were slower, as were 256-column tiles
+// sharing each A block; many independent pipelines per SM beat deep ones.
 //
 // Every mbarrier wait is bounded (clock64); on expiry the CTA records an error
 // word (read by spx_last_device_error), stops issuing, waits (bounded) for
@@ -30,6 +37,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "spx_internal.h"
@@ -83,12 +91,11 @@ constexpr uint32_t kSB = kABytes + 2 * kBBox;                 // one ring stage:
 constexpr size_t kTileSmem = STAGES * kSB + 1024 + 256;      // the ring, 1 KB alignment slack, barriers
 constexpr uint32_t kTmemColsT = 64;                           // the 128 x 64 fp32 accumulator
 
-template <bool TASKS = false>
 __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
-                         long long ldc, float alpha, float beta, long long spin_limit, int M, int N,
-                         const int4* __restrict__ tasks = nullptr, float* __restrict__ partials = nullptr) {
+                         const int* __restrict__ bcol, float* __restrict__ C, long long ldc, float alpha, float beta,
+                         long long spin_limit, int M, int N, const int4* __restrict__ tasks,
+                         float* __restrict__ partials) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -105,20 +112,9 @@ __global__ void __launch_bounds__(kTThreads)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * 128;
-    // one block-row per grid row, or (planned call) one task: a piece of a
-    // block-row's blocks {block-row, first block, blocks, partial slot or -1}
-    int I, b0, nblk, slot = -1;
-    if (TASKS) {
-        const int4 t = tasks[blockIdx.y];
-        I = t.x;
-        b0 = t.y;
-        nblk = t.z;
-        slot = t.w;
-    } else {
-        I = blockIdx.y;
-        b0 = __ldg(brp + I);
-        nblk = __ldg(brp + I + 1) - b0;
-    }
+    // one task per grid row: a block-row or a piece of one {block-row, first block, blocks, partial slot or -1}
+    const int4 task = tasks[blockIdx.y];
+    const int I = task.x, b0 = task.y, nblk = task.z, slot = task.w;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -208,7 +204,7 @@ __global__ void __launch_bounds__(kTThreads)
         const bool cok = cn < N;
         float* cp = C + static_cast<long long>(I) * kBlk * ldc + cn;
         // a piece of a split block-row writes its raw partial tile (1 * sum, exact; the fix-up applies alpha/beta)
-        const bool raw = TASKS && slot >= 0;
+        const bool raw = slot >= 0;
         float* dst = raw ? partials + static_cast<long long>(slot) * kBlk * N + cn : cp;
         const long long dstride = raw ? N : ldc;
         const int rows = raw ? kBlk : mrows;
@@ -254,6 +250,224 @@ __global__ void __launch_bounds__(kTThreads)
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemColsT) : "memory");
 }
 
+// ---------------------------------------------------------------- the persistent kernel
+// The same tiles (128 output columns x one 64-row block-row) and the same
+// ring stages as the tile kernel, but a CTA stays resident and walks a static
+// schedule of tiles (tile = block-row * column tiles + column tile; CTA b runs
+// tiles b, b + G, b + 2G, ...), so the ring never drains between tiles:
+//   warps 0-3 : epilogue (TMEM lane quarter = warp), one tile behind the MMAs;
+//   warp 4    : TMA producer, one ring position per block, across tiles;
+//   warp 5    : lane 0 issues the MMAs into one of two TMEM accumulators
+//               (64 columns each), so tile i+1 accumulates while tile i is
+//               stored.
+// On dense block-rows (256 blocks each) the tile kernel reaches its steady
+// rate; on short ones (26 blocks) each CTA's start-up, pipeline fill and
+// epilogue are paid per tile, and this kernel hides them.
+constexpr int kPThreads = 192;
+constexpr uint32_t kPTmemCols = 2 * kTmemColsT;
+enum : int { kErrTmemFree = 7 };
+
+__global__ void __launch_bounds__(kPThreads)
+    bsr_spmm_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
+                            long long ldc, float alpha, float beta, long long spin_limit, int M, int N, int ntiles,
+                            int ntq) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ uint32_t s_issued, s_consumed;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bars = base + STAGES * kSB;
+    auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t fin_bar = bars + 8u * (2 * STAGES + 4);
+    auto stage_a = [&](uint32_t s) { return base + s * kSB; };
+    auto stage_b = [&](uint32_t s) { return base + s * kSB + kABytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = static_cast<int>(gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);  // one arrive per epilogue warp
+        }
+        mbar_init(fin_bar, 1);
+        s_abort = 0;
+        s_issued = 0;
+        s_consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kPTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 4) {
+        // ---------------- producer: lane 0 waits for a free stage and arms it, lanes 0..2 issue its boxes
+        uint32_t g = 0;
+        for (int t = blockIdx.x; t < ntiles && !s_abort; t += G) {
+            const int I = t / ntq, n0 = (t % ntq) * 128;
+            const int b0 = __ldg(brp + I), nb = __ldg(brp + I + 1) - b0;
+            int jreg = 0;
+            bool stop = false;
+            for (int b = 0; b < nb; ++b, ++g) {
+                const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+                if ((b & 31) == 0) jreg = b + lane < nb ? __ldg(bcol + b0 + b + lane) : 0;
+                const int J = __shfl_sync(0xffffffffu, jreg, b & 31);
+                int ok = 1;
+                if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        record_error(kErrEmpty);
+                        s_abort = 1;
+                    }
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) mbar_expect_tx(full_bar(s), kSB);
+                __syncwarp();
+                if (lane == 0) tma_load_2d(stage_a(s), &tmA, 0, (b0 + b) * kBlk, full_bar(s));
+                else if (lane <= 2)
+                    tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
+                __syncwarp();
+            }
+            if (stop) break;
+        }
+        if (lane == 0) s_issued = g;
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            uint32_t g = 0;
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += G, ++i) {
+                const int buf = i & 1;
+                const uint32_t use = static_cast<uint32_t>(i >> 1);
+                const int I = t / ntq;
+                const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+                if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, spin_limit) || s_abort) {
+                    record_error(kErrTmemFree);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * kTmemColsT;
+                bool ok = true;
+                for (int b = 0; b < nb; ++b, ++g) {
+                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, spin_limit)) {
+                        record_error(kErrFull);
+                        s_abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < kBlk / 16; ++ks) {
+                        const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
+                        const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
+                        mma_bf16(d, adesc, bdesc, kIdesc, (b > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                if (nb > 0) mma_commit(tfull_bar(buf));  // arrives when this tile's MMAs have completed
+                else mbar_arrive(tfull_bar(buf));
+            }
+            s_consumed = g;
+        }
+    } else {
+        // ---------------- epilogue warps 0..3: TMEM lane quarter = warp -> 32 output columns
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += G, ++i) {
+            const int buf = i & 1;
+            const uint32_t use = static_cast<uint32_t>(i >> 1);
+            const int I = t / ntq, n0 = (t % ntq) * 128;
+            const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+            int ok = 1;
+            if (lane == 0) ok = (mbar_wait(tfull_bar(buf), use & 1u, spin_limit) && !s_abort) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    record_error(kErrAcc);
+                    s_abort = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int cn = n0 + 32 * warp + lane;  // this thread's column; columns >= N are not stored
+            const bool cok = cn < N;
+            const int mrows = min(kBlk, M - I * kBlk);  // rows of this block-row inside [0, M)
+            float* cp = C + static_cast<long long>(I) * kBlk * ldc + cn;
+            if (nb == 0) {
+                if (cok)
+                    for (int r = 0; r < mrows; ++r) __stcs(cp + r * ldc, beta != 0.f ? beta * cp[r * ldc] : 0.f);
+            } else {
+                // GUARD: a tile on a ragged edge (row M or column N inside it) checks each store
+                auto drain = [&](auto guard) {
+                    constexpr bool GUARD = decltype(guard)::value;
+#pragma unroll
+                    for (int c0 = 0; c0 < kBlk; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + buf * kTmemColsT + c0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (!GUARD || (cok && c0 + j < mrows)) {
+                                float* q = cp + static_cast<long long>(c0 + j) * ldc;
+                                const float acc = alpha * __uint_as_float(v[j]);
+                                __stcs(q, beta != 0.f ? acc + beta * *q : acc);
+                            }
+                        }
+                    }
+                };
+                if (n0 + 128 <= N && mrows == kBlk) drain(std::false_type{});
+                else drain(std::true_type{});
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort) {
+        if (warp == 4 && lane == 0) {
+            // copies issued but never consumed: wait (bounded) until each has landed
+            for (uint32_t g = s_consumed; g < s_issued; ++g)
+                if (!mbar_wait(full_bar(g % STAGES), (g / STAGES) & 1u, spin_limit)) {
+                    record_error(kErrDrain);
+                    break;
+                }
+        } else if (warp == 5 && lane == 0) {
+            // MMAs in flight: one more commit, then wait (bounded) for it
+            mma_commit(fin_bar);
+            if (!mbar_wait(fin_bar, 0, spin_limit)) record_error(kErrDrain);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols) : "memory");
+}
+
 // Test aid for the bounded waits: one thread arms an mbarrier that nothing
 // completes and waits on it with the pipelines' own bounded wait; when the
 // limit runs out it records the timeout in the error word, as a stalled
@@ -278,6 +492,35 @@ __global__ void bsr_scale_kernel(float* C, long long ldc, int M, int N, float be
 }
 
 // ------------------------------------------------------------ host side
+
+// Grid of the persistent kernel: the CTAs the SMs hold at once, from the
+// shared-memory, thread and register limits with the whole L1/shared array as
+// shared memory (three rings per SM), at most one per tile.
+spx_status launch_persist(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* brp, const int* bcol, float* C,
+                          long long ldc, float alpha, float beta, int M, int N, int ntiles, int ntq, cudaStream_t st) {
+    auto* kernel = bsr_spmm_persist_kernel;
+    int dev = 0, nsm = 0, smem_sm = 0, reserved = 0, max_thr = 0, regs_sm = 0;
+    cudaFuncAttributes fa{};
+    if (set_smem_limit(kernel, kTileSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_thr, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
+        return SPX_ERR_CUDA;
+    const long long per_block = static_cast<long long>(kTileSmem) + fa.sharedSizeBytes + reserved;
+    long long per_sm = smem_sm / per_block;
+    per_sm = std::min<long long>(per_sm, max_thr / kPThreads);
+    per_sm = std::min<long long>(per_sm, regs_sm / (static_cast<long long>(fa.numRegs > 0 ? fa.numRegs : 1) * kPThreads));
+    const long long resident = std::max<long long>(per_sm, 1) * nsm;
+    const int grid = static_cast<int>(ntiles < resident ? ntiles : resident);
+    kernel<<<grid, kPThreads, kTileSmem, st>>>(tmA, tmB, brp, bcol, C, ldc, alpha, beta, kSpinLimit, M, N, ntiles, ntq);
+    return spx_cuda_status(cudaGetLastError());
+}
+
 
 }  // namespace
 
@@ -312,13 +555,12 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
     if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
         !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
         return SPX_ERR_CUDA;
-    const int MB = (M + kBlk - 1) / kBlk;
-    if (MB > 65535) return SPX_ERR_UNSUPPORTED;  // block-rows map to gridDim.y
-    if (set_smem_limit(bsr_spmm_tile_kernel<>, kTileSmem) != cudaSuccess) return SPX_ERR_CUDA;
-    bsr_spmm_tile_kernel<><<<dim3((N + 127) / 128, MB), kTThreads, kTileSmem, st>>>(
-        tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N);
-    spx_note_launches(1);
-    return spx_cuda_status(cudaGetLastError());
+    const long long ntiles = static_cast<long long>((M + kBlk - 1) / kBlk) * ((N + 127) / 128);
+    if (ntiles > kI32Max) return SPX_ERR_INDEX_RANGE;
+    const spx_status s = launch_persist(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N,
+                                        static_cast<int>(ntiles), (N + 127) / 128, st);
+    if (s == SPX_OK) spx_note_launches(1);
+    return s;
 }
 
 spx_status spx_bsr_plan_build(int32_t M, int64_t nnzb, const int32_t* bsr_row_ptr, spx_loc where, int32_t max_blocks,
@@ -363,9 +605,12 @@ spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, in
         return SPX_ERR_CUDA;
     const int4* tasks = static_cast<const int4*>(P->d_table);
     float* partials = static_cast<float*>(scratch);
-    if (set_smem_limit(bsr_spmm_tile_kernel<true>, kTileSmem) != cudaSuccess) return SPX_ERR_CUDA;
-    bsr_spmm_tile_kernel<true><<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kTThreads, kTileSmem, st>>>(
-        tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N, tasks, partials);
+    // Pieces of unequal length: one CTA per (task, column tile), so the hardware hands the next task to
+    // whichever CTA slot frees first (the persistent kernel's static schedule balanced them worse:
+    // 160 against 123 us on block-rows of 26 and of 208 blocks)
+    if (set_smem_limit(bsr_spmm_tile_kernel, kTileSmem) != cudaSuccess) return SPX_ERR_CUDA;
+    bsr_spmm_tile_kernel<<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kTThreads, kTileSmem, st>>>(
+        tmA, tmB, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N, tasks, partials);
     uint64_t launches = 1;
     if (nsplit > 0) {
         bsr_fixup_kernel<<<dim3((N + 255) / 256, kBlk, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(
