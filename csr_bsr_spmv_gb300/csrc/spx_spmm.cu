@@ -353,9 +353,13 @@ int pick_variant(int32_t N, const float* B, int64_t ldb, const float* C, int64_t
 }
 
 // Column tile of the float4 variants: the whole of N up to 128 columns (a
-// sub-warp of N/4 lanes per row), tiles of 128 beyond.  Narrower tiles that
-// keep a B slice L2-resident were measured slower on GB300 (the matrix is
-// re-streamed once per tile), so they are only taken on request.
+// sub-warp of N/4 lanes per row), tiles of 128 beyond.  Narrower tiles keep
+// less of B per pass but were slower on GB300 (1M x 1M clustered matrix,
+// N = 128: 1.11 ms at 128 columns, 1.18 / 1.29 / 1.93 ms at 64 / 32 / 16):
+// every tile re-streams the matrix, and below 32 fp32 columns a B-row
+// fragment is smaller than the 128-byte lines L2 fills from DRAM, so DRAM
+// traffic grows (5.1 GB at 128 columns, 10.6 GB at 16).  They are only taken
+// on request.
 int auto_col_tile(int32_t N) {
     int t = 8;
     while (t < N && t < 128) t <<= 1;
