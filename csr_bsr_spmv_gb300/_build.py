@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_obj")
 LIB = os.path.join(PKG, "libspx.so")
+# the bounds-checked build: the same sources with -DSPX_CHECK (every index a kernel
+# reads from the caller's arrays is tested before use; see csrc/spx_check.cuh)
+OBJ_CHECK = os.path.join(PKG, "_obj_check")
+LIB_CHECK = os.path.join(PKG, "libspx_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -56,14 +60,17 @@ def _stamp(src: str, extra) -> str:
     return h.hexdigest()[:16]
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile every translation unit (in parallel) and link libspx.so."""
-    os.makedirs(OBJ, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Compile every translation unit (in parallel) and link libspx.so (checked=True: libspx_check.so)."""
+    obj_dir, lib = (OBJ_CHECK, LIB_CHECK) if checked else (OBJ, LIB)
+    if checked:
+        extra = (*extra, "-DSPX_CHECK")
+    os.makedirs(obj_dir, exist_ok=True)
     jobs = []
     objs = []
     for src in _sources():
         base = os.path.splitext(os.path.basename(src))[0]
-        obj = os.path.join(OBJ, f"{base}.{_stamp(src, extra)}.o")
+        obj = os.path.join(obj_dir, f"{base}.{_stamp(src, extra)}.o")
         objs.append(obj)
         if force or not os.path.exists(obj):
             jobs.append((src, obj))
@@ -83,21 +90,21 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
                 if out:
                     print(out)
     newest = max(os.path.getmtime(o) for o in objs)
-    if force or jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
         keep = set(objs)
-        for o in glob.glob(os.path.join(OBJ, "*.o")):
+        for o in glob.glob(os.path.join(obj_dir, "*.o")):
             if o not in keep:
                 os.remove(o)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     import sys
 
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "spx_check.cuh"
 #include "spx_internal.h"
 #include "spx_tc.cuh"
 
@@ -59,6 +60,28 @@ __device__ int g_bsr_error;
 
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_bsr_error, 0, code); }
+
+SPX_CHECK_WORD(g_bsr_check)
+
+// The checked build's tests (the TMA engine already turns an out-of-range box
+// into zeros, so these guard the index reads and report the error): a block
+// column in [0, KB) -- else it becomes KB, a box past the end, read as zeros --
+// and a block-row's blocks inside [0, nnzb) -- else the block-row counts as
+// empty, identically in every role of the kernel.
+__device__ __forceinline__ int checked_bcol(int J, int KB) {
+    if (SPX_CHECKED && (J < 0 || J >= KB)) {
+        check_fail();
+        return KB;
+    }
+    return J;
+}
+__device__ __forceinline__ int checked_nb(int b0, int nb, long long nnzb, bool report) {
+    if (SPX_CHECKED && !(b0 >= 0 && nb >= 0 && b0 + static_cast<long long>(nb) <= nnzb)) {
+        if (report) check_fail();
+        return 0;
+    }
+    return nb;
+}
 
 constexpr int32_t kDefaultTaskBlocks = 64;  // blocks per task before a block-row is split
 
@@ -95,7 +118,7 @@ __global__ void __launch_bounds__(kTThreads)
     bsr_spmm_tile_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int* __restrict__ bcol, float* __restrict__ C, long long ldc, float alpha, float beta,
                          long long spin_limit, int M, int N, const int4* __restrict__ tasks,
-                         float* __restrict__ partials) {
+                         float* __restrict__ partials, int KB) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(kTThreads)
             const int s = b % STAGES;
             const uint32_t ph = (b / STAGES) & 1u;
             if ((b & 31) == 0) jreg = b + lane < nblk ? __ldg(bcol + b0 + b + lane) : 0;
-            const int J = __shfl_sync(0xffffffffu, jreg, b & 31);
+            const int J = checked_bcol(__shfl_sync(0xffffffffu, jreg, b & 31), KB);
             int ok = 1;
             if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -271,7 +294,7 @@ __global__ void __launch_bounds__(kPThreads)
     bsr_spmm_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
                             long long ldc, float alpha, float beta, long long spin_limit, int M, int N, int ntiles,
-                            int ntq) {
+                            int ntq, int KB, long long nnzb) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -323,13 +346,13 @@ __global__ void __launch_bounds__(kPThreads)
         uint32_t g = 0;
         for (int t = blockIdx.x; t < ntiles && !s_abort; t += G) {
             const int I = t / ntq, n0 = (t % ntq) * 128;
-            const int b0 = __ldg(brp + I), nb = __ldg(brp + I + 1) - b0;
+            const int b0 = __ldg(brp + I), nb = checked_nb(b0, __ldg(brp + I + 1) - b0, nnzb, lane == 0);
             int jreg = 0;
             bool stop = false;
             for (int b = 0; b < nb; ++b, ++g) {
                 const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
                 if ((b & 31) == 0) jreg = b + lane < nb ? __ldg(bcol + b0 + b + lane) : 0;
-                const int J = __shfl_sync(0xffffffffu, jreg, b & 31);
+                const int J = checked_bcol(__shfl_sync(0xffffffffu, jreg, b & 31), KB);
                 int ok = 1;
                 if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -360,7 +383,7 @@ __global__ void __launch_bounds__(kPThreads)
                 const int buf = i & 1;
                 const uint32_t use = static_cast<uint32_t>(i >> 1);
                 const int I = t / ntq;
-                const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+                const int nb = checked_nb(__ldg(brp + I), __ldg(brp + I + 1) - __ldg(brp + I), nnzb, false);
                 if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, spin_limit) || s_abort) {
                     record_error(kErrTmemFree);
                     s_abort = 1;
@@ -399,7 +422,7 @@ __global__ void __launch_bounds__(kPThreads)
             const int buf = i & 1;
             const uint32_t use = static_cast<uint32_t>(i >> 1);
             const int I = t / ntq, n0 = (t % ntq) * 128;
-            const int nb = __ldg(brp + I + 1) - __ldg(brp + I);
+            const int nb = checked_nb(__ldg(brp + I), __ldg(brp + I + 1) - __ldg(brp + I), nnzb, false);
             int ok = 1;
             if (lane == 0) ok = (mbar_wait(tfull_bar(buf), use & 1u, spin_limit) && !s_abort) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -497,7 +520,8 @@ __global__ void bsr_scale_kernel(float* C, long long ldc, int M, int N, float be
 // shared-memory, thread and register limits with the whole L1/shared array as
 // shared memory (three rings per SM), at most one per tile.
 spx_status launch_persist(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* brp, const int* bcol, float* C,
-                          long long ldc, float alpha, float beta, int M, int N, int ntiles, int ntq, cudaStream_t st) {
+                          long long ldc, float alpha, float beta, int M, int N, int K, long long nnzb, int ntiles,
+                          int ntq, cudaStream_t st) {
     auto* kernel = bsr_spmm_persist_kernel;
     int dev = 0, nsm = 0, smem_sm = 0, reserved = 0, max_thr = 0, regs_sm = 0;
     cudaFuncAttributes fa{};
@@ -517,7 +541,8 @@ spx_status launch_persist(const CUtensorMap& tmA, const CUtensorMap& tmB, const 
     per_sm = std::min<long long>(per_sm, regs_sm / (static_cast<long long>(fa.numRegs > 0 ? fa.numRegs : 1) * kPThreads));
     const long long resident = std::max<long long>(per_sm, 1) * nsm;
     const int grid = static_cast<int>(ntiles < resident ? ntiles : resident);
-    kernel<<<grid, kPThreads, kTileSmem, st>>>(tmA, tmB, brp, bcol, C, ldc, alpha, beta, kSpinLimit, M, N, ntiles, ntq);
+    kernel<<<grid, kPThreads, kTileSmem, st>>>(tmA, tmB, brp, bcol, C, ldc, alpha, beta, kSpinLimit, M, N, ntiles, ntq,
+                                               (K + kBlk - 1) / kBlk, nnzb);
     return spx_cuda_status(cudaGetLastError());
 }
 
@@ -557,7 +582,7 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         return SPX_ERR_CUDA;
     const long long ntiles = static_cast<long long>((M + kBlk - 1) / kBlk) * ((N + 127) / 128);
     if (ntiles > kI32Max) return SPX_ERR_INDEX_RANGE;
-    const spx_status s = launch_persist(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N,
+    const spx_status s = launch_persist(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N, K, nnzb,
                                         static_cast<int>(ntiles), (N + 127) / 128, st);
     if (s == SPX_OK) spx_note_launches(1);
     return s;
@@ -610,7 +635,7 @@ spx_status spx_spmm_bsr_planned(const spx_wcsr_plan* P, int32_t M, int32_t K, in
     // 160 against 123 us on block-rows of 26 and of 208 blocks)
     if (set_smem_limit(bsr_spmm_tile_kernel, kTileSmem) != cudaSuccess) return SPX_ERR_CUDA;
     bsr_spmm_tile_kernel<<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kTThreads, kTileSmem, st>>>(
-        tmA, tmB, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N, tasks, partials);
+        tmA, tmB, bsr_col, C, ldc, alpha, beta, kSpinLimit, M, N, tasks, partials, (K + kBlk - 1) / kBlk);
     uint64_t launches = 1;
     if (nsplit > 0) {
         bsr_fixup_kernel<<<dim3((N + 255) / 256, kBlk, nsplit < 65535 ? nsplit : 65535), 256, 0, st>>>(
@@ -638,9 +663,17 @@ spx_status spx_last_device_error(spx_stream_t stream) {
     if (e != cudaSuccess) return SPX_ERR_CUDA;
     const int coo = spx_coo_error_take();
     const int wcsr = spx_wcsr_error_take();
+    // the checked build's index errors (always 0 in the product build, which reads no word for them)
+    const int checked[] = {spx_check_take(g_bsr_check), spx_spmv_check_take(), spx_spmm_check_take(),
+                           spx_sell_check_take(), spx_wcsr_check_take()};
     if (h || wcsr == SPX_ERR_TIMEOUT) return SPX_ERR_TIMEOUT;
     if (wcsr == SPX_ERR_CUDA) return SPX_ERR_CUDA;
-    return static_cast<spx_status>(coo);
+    for (int c : checked)
+        if (c == SPX_ERR_CUDA) return SPX_ERR_CUDA;
+    if (coo) return static_cast<spx_status>(coo);
+    for (int c : checked)
+        if (c) return static_cast<spx_status>(c);
+    return SPX_OK;
 }
 
 }  // extern "C"

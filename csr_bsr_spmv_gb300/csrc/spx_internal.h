@@ -39,6 +39,14 @@ int spx_coo_error_take();
 // Reads and clears the error word of the WCSR kernel: 0 or SPX_ERR_TIMEOUT.
 int spx_wcsr_error_take();
 
+// The checked build (-DSPX_CHECK): read and clear the index-error word of each
+// translation unit's kernels, 0 or SPX_ERR_INDEX_RANGE (0 without reading
+// anything in the product build).
+int spx_spmv_check_take();
+int spx_spmm_check_take();
+int spx_sell_check_take();
+int spx_wcsr_check_take();
+
 // Device-side builders (spx_build.cu): stable radix sorts on the GPU, results
 // identical to the host builders.  Stream-ordered; temporary memory from the
 // stream-ordered allocator.

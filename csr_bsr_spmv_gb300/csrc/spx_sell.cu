@@ -33,6 +33,7 @@
 
 #include "spx_carveout.cuh"
 #include "spx_gather.cuh"
+#include "spx_check.cuh"
 #include "spx_internal.h"
 
 struct spx_sell {
@@ -58,6 +59,20 @@ constexpr int kU = 8;          // entries in flight per thread
 constexpr int kMinBlocks = 6;  // register budget: 42 per thread (measured best of 4, 6, 8)
 
 inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
+
+SPX_CHECK_WORD(g_sell_check)
+
+// The checked build's tests of the uploaded image (caller memory): a column in
+// [-1, K) (-1 is padding), a slice inside the padded entries, a row in [0, M),
+// a piece slot in [0, slots).  A failed test skips the access.
+struct SellBounds {
+    int M, K;
+    long long padded, slots;
+};
+__device__ __forceinline__ bool sell_fail() {
+    check_fail();
+    return false;
+}
 
 struct Pseudo {
     int32_t len, row, start, slot;
@@ -131,13 +146,23 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
                                                                  const int* __restrict__ scol,
                                                                  const float* __restrict__ sval,
                                                                  const float* __restrict__ x, float alpha, float beta,
-                                                                 float* y, float* __restrict__ partials) {
+                                                                 float* y, float* __restrict__ partials,
+                                                                 SellBounds bd) {
     const int s = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= nslices) return;
     const int p0 = __ldg(slice_ptr + s);
     const int L = (__ldg(slice_ptr + s + 1) - p0) / kC;
     const int pr = __ldg(prow + s * kC + lane);
+    if (SPX_CHECKED) {
+        const long long p1 = p0 + static_cast<long long>(L) * kC;
+        const bool slice_ok = p0 >= 0 && L >= 0 && p1 <= bd.padded;
+        const bool row_ok = (pr >= 0 && pr < bd.M) || pr == INT_MIN || (pr < 0 && -1LL - pr < bd.slots);
+        if (!slice_ok || !row_ok) {
+            sell_fail();
+            return;
+        }
+    }
     const float y_old = pr >= 0 && beta != 0.f ? y[pr] : 0.f;  // read up front, off the epilogue's path
     const int* cp = scol + p0 + lane;
     const float* vp = sval + p0 + lane;
@@ -152,11 +177,21 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
             v[u] = spx_gather::ld_once(vp + (j + u) * kC);
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) acc += v[u] * (c[u] >= 0 ? spx_gather::ld_x(x + c[u]) : 0.f);
+        for (int u = 0; u < kU; ++u) {
+            if (SPX_CHECKED && (c[u] < -1 || c[u] >= bd.K)) {
+                sell_fail();
+                c[u] = -1;
+            }
+            acc += v[u] * (c[u] >= 0 ? spx_gather::ld_x(x + c[u]) : 0.f);
+        }
     }
     for (; j < L; ++j) {
-        const int c0 = spx_gather::ld_once(cp + j * kC);
+        int c0 = spx_gather::ld_once(cp + j * kC);
         const float v0 = spx_gather::ld_once(vp + j * kC);
+        if (SPX_CHECKED && (c0 < -1 || c0 >= bd.K)) {
+            sell_fail();
+            c0 = -1;
+        }
         acc += v0 * (c0 >= 0 ? spx_gather::ld_x(x + c0) : 0.f);
     }
     if (pr >= 0) y[pr] = beta != 0.f ? alpha * acc + beta * y_old : alpha * acc;
@@ -166,11 +201,15 @@ __global__ void __launch_bounds__(kC * kWarpsPerCta, kMinBlocks) sell_kernel(int
 // One warp per long row: its pieces' sums in piece order (lane-strided, then a fixed tree).
 __global__ void __launch_bounds__(256) sell_fixup_kernel(const int4* __restrict__ longrows, int nlong,
                                                          const float* __restrict__ partials, float alpha, float beta,
-                                                         float* y) {
+                                                         float* y, SellBounds bd) {
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= nlong) return;
     const int4 lr = longrows[w];
+    if (SPX_CHECKED && !(lr.x >= 0 && lr.x < bd.M && lr.y >= 0 && lr.z >= 0 && lr.y + static_cast<long long>(lr.z) <= bd.slots)) {
+        if (lane == 0) sell_fail();
+        return;
+    }
     float s = 0.f;
     for (int k = lane; k < lr.z; k += 32) s += partials[lr.y + k];
 #pragma unroll
@@ -181,6 +220,8 @@ __global__ void __launch_bounds__(256) sell_fixup_kernel(const int4* __restrict_
 inline bool sell_ok(const spx_sell* S) { return S && S->magic == kSellMagic; }
 
 }  // namespace
+
+int spx_sell_check_take() { return spx_check_take(g_sell_check); }
 
 extern "C" {
 
@@ -373,12 +414,13 @@ spx_status spx_spmv_sell(const spx_sell* S, int32_t M, int32_t K, float alpha, c
         sell_kernel<<<(nslices + kWarpsPerCta - 1) / kWarpsPerCta, kC * kWarpsPerCta, 0, st>>>(
             nslices, reinterpret_cast<const int*>(img), reinterpret_cast<const int*>(img + S->off_prow),
             reinterpret_cast<const int*>(img + S->off_col), reinterpret_cast<const float*>(img + S->off_val), x, alpha,
-            beta, y, static_cast<float*>(scratch));
+            beta, y, static_cast<float*>(scratch), SellBounds{M, K, S->padded, S->slots});
         ++launches;
     }
     if (nlong > 0) {
         sell_fixup_kernel<<<(nlong + 7) / 8, 256, 0, st>>>(reinterpret_cast<const int4*>(img + S->off_long), nlong,
-                                                           static_cast<const float*>(scratch), alpha, beta, y);
+                                                           static_cast<const float*>(scratch), alpha, beta, y,
+                                                           SellBounds{M, K, S->padded, S->slots});
         ++launches;
     }
     spx_note_launches(launches);

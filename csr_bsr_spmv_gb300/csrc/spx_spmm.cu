@@ -17,12 +17,28 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "spx_check.cuh"
 #include "spx_internal.h"
 
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+
+SPX_CHECK_WORD(g_spmm_check)
+
+// The checked build's tests: a column inside [0, K) (else the term is skipped)
+// and a row range inside [lo, hi] (else the row is skipped).
+__device__ __forceinline__ bool col_ok(int c, int K) {
+    if (!SPX_CHECKED || (c >= 0 && c < K)) return true;
+    check_fail();
+    return false;
+}
+__device__ __forceinline__ bool range_ok(long long a, long long b, long long lo, long long hi) {
+    if (!SPX_CHECKED || (lo <= a && a <= b && b <= hi)) return true;
+    check_fail();
+    return false;
+}
 
 __device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
@@ -47,7 +63,8 @@ __global__ void __launch_bounds__(kThreads) spmm_small_kernel(int M, const int* 
                                                               const int* __restrict__ col,
                                                               const float* __restrict__ val,
                                                               const float* __restrict__ B, long long ldb,
-                                                              float alpha, float beta, float* C, long long ldc) {
+                                                              float alpha, float beta, float* C, long long ldc, int K,
+                                                              long long nnz) {
     const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
@@ -55,9 +72,12 @@ __global__ void __launch_bounds__(kThreads) spmm_small_kernel(int M, const int* 
 #pragma unroll
     for (int c = 0; c < N; ++c) acc[c] = 0.f;
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    if (!range_ok(a, b, 0, nnz)) return;
     for (int p = a + lane; p < b; p += 32) {
         const float v = ld_stream(val + p);
-        const float* brow = B + (long long)ld_stream(col + p) * ldb;
+        const int cp = ld_stream(col + p);
+        if (!col_ok(cp, K)) continue;
+        const float* brow = B + (long long)cp * ldb;
 #pragma unroll
         for (int c = 0; c < N; ++c) acc[c] += v * __ldg(brow + c);
     }
@@ -145,7 +165,7 @@ __device__ __forceinline__ V ld_a(const V* p) { return SMEM ? *p : ld_stream(p);
 // Sum over the nonzeros [a, b) of cols/vals of val * B(col, n0 .. n0+3); U B rows in flight.
 template <class T, bool SMEM>
 __device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* vals, int a, int b,
-                                          const typename T::Bt* Bc, long long ldb, uint64_t pol) {
+                                          const typename T::Bt* Bc, long long ldb, uint64_t pol, int K) {
     constexpr int U = SPX_SPMM_UNROLL;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int p = a;
@@ -159,7 +179,8 @@ __device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* 
         }
         float4 bv[U];
 #pragma unroll
-        for (int j = 0; j < U; ++j) bv[j] = T::brow(Bc + (long long)c[j] * ldb, pol);
+        for (int j = 0; j < U; ++j)
+            bv[j] = col_ok(c[j], K) ? T::brow(Bc + (long long)c[j] * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
@@ -176,7 +197,8 @@ __device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* 
         float4 bv[U];
 #pragma unroll
         for (int j = 0; j < U; ++j)
-            bv[j] = p + j < b ? T::brow(Bc + (long long)c[j] * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+            bv[j] = p + j < b && col_ok(c[j], K) ? T::brow(Bc + (long long)c[j] * ldb, pol)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
@@ -186,7 +208,7 @@ __device__ __forceinline__ float4 row_dot(const int* cols, const typename T::V* 
     for (; p < b; ++p) {
         const int c0 = ld_a<SMEM>(cols + p);
         const float v0 = T::widen(ld_a<SMEM>(vals + p));
-        const float4 b0 = T::brow(Bc + (long long)c0 * ldb, pol);
+        const float4 b0 = col_ok(c0, K) ? T::brow(Bc + (long long)c0 * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
         acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
     }
     return acc;
@@ -196,7 +218,7 @@ template <int L, class T>
 __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
     spmm_vec_kernel(int M, int N, const int* __restrict__ rp, const int* __restrict__ col,
                     const typename T::V* __restrict__ val, const typename T::Bt* __restrict__ B, long long ldb,
-                    float alpha, float beta, float* C, long long ldc, int long_min) {
+                    float alpha, float beta, float* C, long long ldc, int long_min, int K, long long nnz) {
     constexpr int RPW = 32 / L;         // rows per warp
     constexpr int R = kWarps * RPW;     // rows per CTA
     constexpr int IT = kStageCap / kThreads;
@@ -208,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
     const int n0 = blockIdx.y * 4 * L + 4 * (lane % L);
     const int ca = __ldg(rp + r0);
     const int cn = __ldg(rp + min(r0 + R, M)) - ca;
-    const bool staged = cn <= kStageCap;  // uniform over the CTA
+    // (checked build: a run outside [0, nnz] is not staged; its rows fail the range test below)
+    const bool staged = cn <= kStageCap && (!SPX_CHECKED || (ca >= 0 && cn >= 0 && ca + (long long)cn <= nnz));
     if (staged) {
         int c[IT];
         typename T::V v[IT];
@@ -234,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, T::kMinBlocks)
     const uint64_t pol = l2_evict_last_policy();
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
     if (b - a > long_min) return;  // a long row: its CTA task or segments (planned call) produce it
+    if (!range_ok(a, b, staged ? ca : 0, staged ? (long long)ca + cn : nnz)) return;
     const typename T::Bt* Bc = B + n0;
-    const float4 acc = staged ? row_dot<T, true>(s_col, s_val, a - ca, b - ca, Bc, ldb, pol)
-                              : row_dot<T, false>(col, val, a, b, Bc, ldb, pol);
+    const float4 acc = staged ? row_dot<T, true>(s_col, s_val, a - ca, b - ca, Bc, ldb, pol, K)
+                              : row_dot<T, false>(col, val, a, b, Bc, ldb, pol, K);
     float4* cp = reinterpret_cast<float4*>(C + (long long)row * ldc + n0);
     float4 r = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
     if (beta != 0.f) {
@@ -258,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) spmm_long_kernel(const int4* __restr
                                                             const typename T::V* __restrict__ val,
                                                             const typename T::Bt* __restrict__ B, long long ldb,
                                                             float alpha, float beta, float* C, long long ldc,
-                                                            float* __restrict__ partials) {
+                                                            float* __restrict__ partials, int K) {
     constexpr int NSUB = kThreads / L;
     constexpr int U = 4;
     __shared__ float4 red[NSUB][L];
@@ -281,7 +305,8 @@ __global__ void __launch_bounds__(kThreads) spmm_long_kernel(const int4* __restr
             }
             float4 bv[U];
 #pragma unroll
-            for (int j = 0; j < U; ++j) bv[j] = T::brow(Bc + (long long)c[j] * ldb, pol);
+            for (int j = 0; j < U; ++j)
+                bv[j] = col_ok(c[j], K) ? T::brow(Bc + (long long)c[j] * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 acc.x += v[j] * bv[j].x; acc.y += v[j] * bv[j].y; acc.z += v[j] * bv[j].z; acc.w += v[j] * bv[j].w;
@@ -289,7 +314,8 @@ __global__ void __launch_bounds__(kThreads) spmm_long_kernel(const int4* __restr
         }
         for (; p < p1; p += NSUB) {
             const float v0 = T::widen(ld_stream(val + p));
-            const float4 b0 = T::brow(Bc + (long long)ld_stream(col + p) * ldb, pol);
+            const int c0 = ld_stream(col + p);
+            const float4 b0 = col_ok(c0, K) ? T::brow(Bc + (long long)c0 * ldb, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
             acc.x += v0 * b0.x; acc.y += v0 * b0.y; acc.z += v0 * b0.z; acc.w += v0 * b0.w;
         }
     }
@@ -330,14 +356,19 @@ __global__ void __launch_bounds__(kThreads) spmm_scalar_kernel(int M, int N, con
                                                                const int* __restrict__ col,
                                                                const float* __restrict__ val,
                                                                const float* __restrict__ B, long long ldb,
-                                                               float alpha, float beta, float* C, long long ldc) {
+                                                               float alpha, float beta, float* C, long long ldc, int K,
+                                                               long long nnz) {
     const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
     const int a = __ldg(rp + row), b = __ldg(rp + row + 1);
+    if (!range_ok(a, b, 0, nnz)) return;
     for (int n = blockIdx.y * 32 + lane; n < N; n += 32 * gridDim.y) {
         float acc = 0.f;
-        for (int p = a; p < b; ++p) acc += __ldg(val + p) * __ldg(B + (long long)__ldg(col + p) * ldb + n);
+        for (int p = a; p < b; ++p) {
+            const int c = __ldg(col + p);
+            if (col_ok(c, K)) acc += __ldg(val + p) * __ldg(B + (long long)c * ldb + n);
+        }
         float r = alpha * acc;
         float* cp = C + (long long)row * ldc + n;
         if (beta != 0.f) r += beta * *cp;
@@ -369,6 +400,8 @@ int auto_col_tile(int32_t N) {
 // Long-row work of a planned call: the plan's CTA-row and segment tasks (the
 // first nlong_tasks entries of its device table), then the split-row fix-up.
 struct LongWork {
+    int K = 0;          // columns of A (the checked build tests every column against it)
+    long long nnz = 0;  // entries of A (and every row range against it)
     const int4* tasks = nullptr;
     int ntasks = 0;
     const int4* longrows = nullptr;
@@ -384,10 +417,11 @@ void launch_vec(int M, int N, const int* rp, const int* col, const typename T::V
     constexpr int rows_per_cta = kWarps * (32 / L);
     const int tiles = (N + 4 * L - 1) / (4 * L);
     dim3 grid((M + rows_per_cta - 1) / rows_per_cta, tiles);
-    spmm_vec_kernel<L, T><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, lw.long_min);
+    spmm_vec_kernel<L, T><<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, lw.long_min, lw.K,
+                                                    lw.nnz);
     if (lw.ntasks > 0)
         spmm_long_kernel<L, T><<<dim3(lw.ntasks, tiles), kThreads, 0, st>>>(lw.tasks, N, col, val, B, ldb, alpha,
-                                                                             beta, C, ldc, lw.partials);
+                                                                             beta, C, ldc, lw.partials, lw.K);
     if (lw.nlongrows > 0)
         spmm_long_fixup_kernel<<<dim3((N + kThreads - 1) / kThreads, lw.nlongrows < 65535 ? lw.nlongrows : 65535),
                                  kThreads, 0, st>>>(lw.longrows, lw.nlongrows, N, lw.partials, alpha, beta, C, ldc);
@@ -396,7 +430,7 @@ void launch_vec(int M, int N, const int* rp, const int* col, const typename T::V
 template <class T>
 void launch_vec_tile(int tile, int M, int N, const int* rp, const int* col, const typename T::V* val,
                      const typename T::Bt* B, long long ldb, float alpha, float beta, float* C, long long ldc,
-                     cudaStream_t st, const LongWork& lw = LongWork()) {
+                     cudaStream_t st, const LongWork& lw) {
     switch (tile) {
         case 8: launch_vec<2, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
         case 16: launch_vec<4, T>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw); break;
@@ -420,7 +454,10 @@ spx_status spmm_16bit(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, cons
     if (!spx_aligned(rp, 4) || !spx_aligned(col, 4) || !spx_aligned(val, 2) || !spx_aligned(B, 8) ||
         !spx_aligned(C, 16))
         return SPX_ERR_ALIGN;
-    launch_vec_tile<T>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
+    LongWork lw;
+    lw.K = K;
+    lw.nnz = nnz;
+    launch_vec_tile<T>(auto_col_tile(N), M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw);
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }
@@ -445,6 +482,8 @@ spx_status spmm_planned(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, co
     const size_t need = sizeof(float) * static_cast<size_t>(slots) * static_cast<size_t>(N);
     if (need && (!scratch || scratch_bytes < need)) return SPX_ERR_ARG;
     LongWork lw;
+    lw.K = K;
+    lw.nnz = nnz;
     const int64_t ngroups = P->counts[6] + P->counts[7] + P->counts[8];
     lw.tasks = static_cast<const int4*>(P->d_table);
     lw.ntasks = static_cast<int>(P->counts[0] - ngroups);  // long-row tasks come first in the table
@@ -473,22 +512,27 @@ spx_status spmm_impl(int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const
     if (v == 0) {
         const int grid = (M + kWarps - 1) / kWarps;
         switch (N) {
-#define SPX_SMALL(n) case n: spmm_small_kernel<n><<<grid, kThreads, 0, st>>>(M, rp, col, val, B, ldb, alpha, beta, C, ldc); break;
+#define SPX_SMALL(n) case n: spmm_small_kernel<n><<<grid, kThreads, 0, st>>>(M, rp, col, val, B, ldb, alpha, beta, C, ldc, K, nnz); break;
             SPX_SMALL(1) SPX_SMALL(2) SPX_SMALL(3) SPX_SMALL(4) SPX_SMALL(5) SPX_SMALL(6) SPX_SMALL(7) SPX_SMALL(8)
 #undef SPX_SMALL
         }
     } else if (v == 3) {
         dim3 grid((M + kWarps - 1) / kWarps, (N + 31) / 32 < 4 ? (N + 31) / 32 : 4);
-        spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc);
+        spmm_scalar_kernel<<<grid, kThreads, 0, st>>>(M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, K, nnz);
     } else {
         const int t = col_tile ? col_tile : auto_col_tile(N);
-        launch_vec_tile<StoreF32>(t, M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st);
+        LongWork lw;
+        lw.K = K;
+        lw.nnz = nnz;
+        launch_vec_tile<StoreF32>(t, M, N, rp, col, val, B, ldb, alpha, beta, C, ldc, st, lw);
     }
     spx_note_launches(1);
     return spx_cuda_status(cudaGetLastError());
 }
 
 }  // namespace
+
+int spx_spmm_check_take() { return spx_check_take(g_spmm_check); }
 
 extern "C" {
 

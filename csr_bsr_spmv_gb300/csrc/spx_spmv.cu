@@ -29,12 +29,15 @@
 #include <mutex>
 
 #include "spx_carveout.cuh"
+#include "spx_check.cuh"
 #include "spx_gather.cuh"
 #include "spx_internal.h"
 
 namespace {
 
 constexpr int kThreads = 256;  // fix-up kernel
+
+SPX_CHECK_WORD(g_spmv_check)
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -63,10 +66,19 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return s;
 }
 
+// x[c]; the checked build loads it only for a column inside [0, K) (else 0).
+__device__ __forceinline__ float gather_x(const float* __restrict__ x, int c, int K) {
+    if (SPX_CHECKED && (c < 0 || c >= K)) {
+        check_fail();
+        return 0.f;
+    }
+    return ld_x(x + c);
+}
+
 // Strided dot product of the nonzero range [a, b) with x; 4 gathers in flight per thread.
 template <int NT>
 __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__ col, const float* __restrict__ val,
-                                           const float* __restrict__ x) {
+                                           const float* __restrict__ x, int K) {
     float s = 0.f;
     int p = a + threadIdx.x;
     for (; p + 3 * NT < b; p += 4 * NT) {
@@ -74,13 +86,13 @@ __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__
         int c2 = ld_stream(col + p + 2 * NT), c3 = ld_stream(col + p + 3 * NT);
         float v0 = ld_stream(val + p), v1 = ld_stream(val + p + NT);
         float v2 = ld_stream(val + p + 2 * NT), v3 = ld_stream(val + p + 3 * NT);
-        float x0 = ld_x(x + c0), x1 = ld_x(x + c1), x2 = ld_x(x + c2), x3 = ld_x(x + c3);
+        float x0 = gather_x(x, c0, K), x1 = gather_x(x, c1, K), x2 = gather_x(x, c2, K), x3 = gather_x(x, c3, K);
         s += v0 * x0;
         s += v1 * x1;
         s += v2 * x2;
         s += v3 * x3;
     }
-    for (; p < b; p += NT) s += ld_stream(val + p) * ld_x(x + ld_stream(col + p));
+    for (; p < b; p += NT) s += ld_stream(val + p) * gather_x(x, ld_stream(col + p), K);
     return s;
 }
 
@@ -107,7 +119,7 @@ __device__ __forceinline__ int sk(int k) { return k + (k >> 5); }
 // ITEMS = block_nnz / NT as a compile-time case, 0 = runtime loop.
 template <int NT, int ITEMS>
 __device__ __forceinline__ void stage_products(int p0, int n, const int* __restrict__ col,
-                                               const float* __restrict__ val, const float* __restrict__ x,
+                                               const float* __restrict__ val, const float* __restrict__ x, int K,
                                                float* s_prod) {
     if (ITEMS > 0) {
         int c[ITEMS > 0 ? ITEMS : 1];
@@ -121,11 +133,11 @@ __device__ __forceinline__ void stage_products(int p0, int n, const int* __restr
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
             const int k = threadIdx.x + j * NT;
-            if (k < n) s_prod[sk(k)] = v[j] * ld_x(x + c[j]);
+            if (k < n) s_prod[sk(k)] = v[j] * gather_x(x, c[j], K);
         }
     } else {
         for (int k = threadIdx.x; k < n; k += NT)
-            s_prod[sk(k)] = ld_stream(val + p0 + k) * ld_x(x + ld_stream(col + p0 + k));
+            s_prod[sk(k)] = ld_stream(val + p0 + k) * gather_x(x, ld_stream(col + p0 + k), K);
     }
 }
 
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
                                                               const float* __restrict__ val,
                                                               const float* __restrict__ x, float alpha, float beta,
                                                               float* y, float* __restrict__ partials, int block_nnz,
-                                                              int block_rows) {
+                                                              int block_rows, int K) {
     extern __shared__ __align__(16) float smem[];
     const int4 t = tasks[blockIdx.x];
     const int kind = t.x & 3;
@@ -261,8 +273,20 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
             s_rp[i] = __ldg(rp + r0 + i) - p0;
             if (beta != 0.f && i < nrows) s_y[i] = y[r0 + i];
         }
-        stage_products<NT, ITEMS>(p0, n, col, val, x, s_prod);
+        stage_products<NT, ITEMS>(p0, n, col, val, x, K, s_prod);
         __syncthreads();
+        if (SPX_CHECKED) {
+            // the row offsets of this group, read from the caller's row_ptr, must fit the plan's range
+            // [p0, p1) and rise; otherwise the rows are not reduced (no shared read outside the products)
+            bool bad = false;
+            for (int i = threadIdx.x; i <= nrows; i += NT)
+                bad |= s_rp[i] < 0 || s_rp[i] > n || (i < nrows && s_rp[i + 1] < s_rp[i]) ||
+                       (i == 0 && s_rp[0] != 0) || (i == nrows && s_rp[nrows] != n);
+            if (__syncthreads_or(bad)) {
+                if (threadIdx.x == 0) check_fail();
+                return;
+            }
+        }
         if (code == kReduceSegmented)
             reduce_segmented<ITEMS>(r0, nrows, n, (block_nnz + NT - 1) / NT, s_prod, s_rp, s_y, alpha,
                                     beta, y, s_sv, s_sf);
@@ -271,7 +295,7 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
     } else {
         // the old y of a CTA row is read up front, off the critical path
         const float y_old = (kind == kTaskCta && beta != 0.f && threadIdx.x == 0) ? y[t.y] : 0.f;
-        float s = range_dot<NT>(t.z, t.w, col, val, x);
+        float s = range_dot<NT>(t.z, t.w, col, val, x, K);
         s = block_sum<NT>(s, smem);
         if (threadIdx.x == 0) {
             if (kind == kTaskCta) y[t.y] = alpha * s + (beta != 0.f ? beta * y_old : 0.f);
@@ -343,23 +367,28 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     switch (B) {
         case 512:
             spx_carve::fit(spmv_tasks_kernel<64, 8>, 64, smem);
-            spmv_tasks_kernel<64, 8><<<ntasks, 64, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<64, 8><<<ntasks, 64, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
+                                                                     static_cast<int>(P->K));
             break;
         case 1024:
             spx_carve::fit(spmv_tasks_kernel<128, 8>, 128, smem);
-            spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
+                                                                     static_cast<int>(P->K));
             break;
         case 2048:
             spx_carve::fit(spmv_tasks_kernel<256, 8>, 256, smem);
-            spmv_tasks_kernel<256, 8><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<256, 8><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
+                                                                     static_cast<int>(P->K));
             break;
         case 4096:
             spx_carve::fit(spmv_tasks_kernel<512, 8>, 512, smem);
-            spmv_tasks_kernel<512, 8><<<ntasks, 512, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<512, 8><<<ntasks, 512, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
+                                                                     static_cast<int>(P->K));
             break;
         default:
             spx_carve::fit(spmv_tasks_kernel<256, 0>, 256, smem);
-            spmv_tasks_kernel<256, 0><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R);
+            spmv_tasks_kernel<256, 0><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
+                                                                     static_cast<int>(P->K));
             break;
     }
     uint64_t launches = 1;
@@ -387,6 +416,8 @@ spx_status check_call(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, cons
 }
 
 }  // namespace
+
+int spx_spmv_check_take() { return spx_check_take(g_spmv_check); }
 
 extern "C" {
 

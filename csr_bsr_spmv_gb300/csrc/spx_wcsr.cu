@@ -32,6 +32,7 @@
 #include <new>
 #include <vector>
 
+#include "spx_check.cuh"
 #include "spx_internal.h"
 #include "spx_tc.cuh"
 
@@ -59,6 +60,11 @@ enum : int { kErrFull = 1, kErrEmpty = 2, kErrAcc = 3, kErrDrain = 4 };
 __device__ int g_wcsr_error;
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_wcsr_error, 0, code); }
 
+// The checked build's word: a column outside [-1, K) (read as padding in
+// either build, reported here) or a window whose chunks leave [0, nchunks)
+// (treated as empty here).
+SPX_CHECK_WORD(g_wcsr_check)
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -71,7 +77,8 @@ __global__ void __launch_bounds__(kThreads)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const int* __restrict__ win_ptr,
                      const int* __restrict__ win_col, const uint16_t* __restrict__ B, long long ldb,
                      float* __restrict__ C, long long ldc, int M, int K, float alpha, float beta,
-                     long long spin_limit, const int4* __restrict__ tasks, float* __restrict__ partials, int N) {
+                     long long spin_limit, const int4* __restrict__ tasks, float* __restrict__ partials, int N,
+                     long long nchunks) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -104,6 +111,10 @@ __global__ void __launch_bounds__(kThreads)
         w = blockIdx.y;
         g0 = __ldg(win_ptr + w);
         nch = __ldg(win_ptr + w + 1) - g0;
+    }
+    if (SPX_CHECKED && !(g0 >= 0 && nch >= 0 && g0 + static_cast<long long>(nch) <= nchunks)) {
+        if (threadIdx.x == 0) check_fail();
+        nch = 0;
     }
 
     if (threadIdx.x == 0) {
@@ -199,6 +210,7 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < 8; ++i) {
                 const int k = 8 * i + k0;
                 const int cr = __ldg(wc + k);
+                if (SPX_CHECKED && (cr < -1 || cr >= K)) check_fail();
                 const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
                 const uint16_t* row = c >= 0 ? B + static_cast<long long>(c) * ldb : B;
                 const uint32_t dst = stage_b(s) + k * 128u + piece_off;
@@ -416,7 +428,7 @@ spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunk
     do {                                                                                                       \
         if (set_smem_limit(wcsr_spmm_kernel<T>, kSmemW) != cudaSuccess) return SPX_ERR_CUDA;                   \
         wcsr_spmm_kernel<T><<<dim3((N + 127) / 128, static_cast<unsigned>(ntasks)), kThreads, kSmemW, st>>>(   \
-            tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit, tasks, partials, N);         \
+            tmA, win_ptr, win_col, B, ldb, C, ldc, M, K, alpha, beta, kSpinLimit, tasks, partials, N, nchunks); \
     } while (0)
     if (tasks) SPX_WCSR_LAUNCH(true);
     else SPX_WCSR_LAUNCH(false);
@@ -432,6 +444,8 @@ spx_status wcsr_run(const spx_wcsr_plan* P, int32_t M, int32_t K, int64_t nchunk
 }
 
 }  // namespace
+
+int spx_wcsr_check_take() { return spx_check_take(g_wcsr_check); }
 
 int spx_wcsr_error_take() {
     int h = 0;

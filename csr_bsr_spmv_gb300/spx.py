@@ -73,96 +73,129 @@ class WcsrPlanInfo(ctypes.Structure):
                 ("slots", ctypes.c_int64), ("table_bytes", ctypes.c_size_t), ("max_chunks", ctypes.c_int32)]
 
 
+LIB_CHECK_PATH = os.path.join(_HERE, "libspx_check.so")  # the bounds-checked build of the same sources
+
 _LIB = None
+_CHECKED = None
+_use_checked = False
 
 
 def _lib():
-    global _LIB
+    """The library every call below goes through: libspx.so, or inside `checked_build()` libspx_check.so."""
+    global _LIB, _CHECKED
+    if _use_checked:
+        if _CHECKED is None:
+            if not os.path.exists(LIB_CHECK_PATH):
+                raise ImportError(f"{LIB_CHECK_PATH} is not built; run __graft_entry__.build()")
+            _CHECKED = _load(LIB_CHECK_PATH)
+        return _CHECKED
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
             raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
-        lib = ctypes.CDLL(LIB_PATH)
-        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-        d = ctypes.POINTER(ctypes.c_double)
-        sigs = {
-            "spx_status_string": ([ctypes.c_int], ctypes.c_char_p),
-            "spx_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
-            "spx_build_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
-            "spx_transpose_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
-            "spx_build_bsr": ([i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
-                               ctypes.c_int, vp], ctypes.c_int),
-            "spx_check_csr": ([i32, i32, i64, vp, vp, i32, ctypes.c_int, vp], ctypes.c_int),
-            "spx_row_stats": ([i32, vp, ctypes.c_int, ctypes.POINTER(RowStats)], ctypes.c_int),
-            "spx_plan_opts_default": ([ctypes.POINTER(PlanOpts)], ctypes.c_int),
-            "spx_plan_opts_auto": ([ctypes.POINTER(RowStats), ctypes.POINTER(PlanOpts)], ctypes.c_int),
-            "spx_plan_csr": ([i32, i32, i64, vp, ctypes.c_int, ctypes.POINTER(PlanOpts), ctypes.POINTER(vp)],
-                             ctypes.c_int),
-            "spx_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], ctypes.c_int),
-            "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
-            "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
-            "spx_plan_destroy": ([vp], ctypes.c_int),
-            "spx_plan_fingerprint": ([vp, ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
-            "spx_plan_validate": ([vp, i32, i32, i64, vp, ctypes.c_int, vp], ctypes.c_int),
-            "spx_plan_autotune": ([i32, i32, i64, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanOpts), i32, i32, vp,
-                                   ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_float),
-                                   ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
-            "spx_plan_autotune_forget": ([], ctypes.c_int),
-            "spx_sell_opts_default": ([ctypes.POINTER(SellOpts)], ctypes.c_int),
-            "spx_sell_build": ([i32, i32, i64, vp, vp, vp, ctypes.c_int, ctypes.POINTER(SellOpts),
-                                ctypes.POINTER(vp)], ctypes.c_int),
-            "spx_sell_get_info": ([vp, ctypes.POINTER(SellInfo)], ctypes.c_int),
-            "spx_sell_get_arrays": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
-            "spx_sell_upload": ([vp, vp, sz, vp], ctypes.c_int),
-            "spx_sell_destroy": ([vp], ctypes.c_int),
-            "spx_spmv_sell": ([vp, i32, i32, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
-            "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
-            "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
-            "spx_spmv_csr_hostio_work_bytes": ([i32, i32], sz),
-            "spx_spmv_csr_hostio": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, i64, f32, vp, i64, i32, vp, sz, vp, sz, vp],
-                                    ctypes.c_int),
-            "spx_spmv_coo_scratch_bytes": ([i64], sz),
-            "spx_spmv_coo": ([i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
-            "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
-                                   sz, vp], ctypes.c_int),
-            "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
-            "spx_spmm_csr_tiled": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, i32, vp], ctypes.c_int),
-            "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
-            "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
-            "spx_spmm_csr_f16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
-            "spx_spmm_csr_planned_scratch_bytes": ([vp, i32], sz),
-            "spx_spmm_csr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
-                                     ctypes.c_int),
-            "spx_spmm_csr_bf16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
-                                          ctypes.c_int),
-            "spx_spmm_csr_f16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
-                                         ctypes.c_int),
-            "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
-            "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
-                                ctypes.c_int, vp], ctypes.c_int),
-            "spx_spmm_wcsr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
-            "spx_wcsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
-            "spx_wcsr_plan_info": ([vp, ctypes.POINTER(WcsrPlanInfo)], ctypes.c_int),
-            "spx_wcsr_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
-            "spx_wcsr_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
-            "spx_wcsr_plan_destroy": ([vp], ctypes.c_int),
-            "spx_spmm_wcsr_planned_scratch_bytes": ([vp, i32], sz),
-            "spx_spmm_wcsr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
-                                      ctypes.c_int),
-            "spx_bsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
-            "spx_spmm_bsr_planned_scratch_bytes": ([vp, i32], sz),
-            "spx_spmm_bsr_planned": ([vp, i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz,
-                                      vp], ctypes.c_int),
-            "spx_gather_probe_blocks": ([], ctypes.c_int32),
-            "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
-            "spx_last_device_error": ([vp], ctypes.c_int),
-            "spx_wait_probe": ([i64, vp], ctypes.c_int),
-        }
-        for name, (args, res) in sigs.items():
-            f = getattr(lib, name)
-            f.argtypes = args
-            f.restype = res
-        _LIB = lib
+        _LIB = _load(LIB_PATH)
     return _LIB
+
+
+class checked_build:
+    """Context in which the calls of this module go to libspx_check.so, the build that tests every
+    index it reads from the caller's arrays before using it and reports a bad one through
+    spx_last_device_error (SPX_ERR_INDEX_RANGE) instead of reading out of bounds.  For finding bad
+    inputs; objects (plans, SELL forms, task splits) made inside the context belong to it."""
+
+    def __enter__(self):
+        global _use_checked
+        self._prev = _use_checked
+        _use_checked = True
+        return _lib()
+
+    def __exit__(self, *exc):
+        global _use_checked
+        _use_checked = self._prev
+        return False
+
+
+def _load(path):
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    d = ctypes.POINTER(ctypes.c_double)
+    sigs = {
+        "spx_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "spx_launch_count": ([ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+        "spx_build_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "spx_transpose_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, vp, vp, ctypes.c_int, vp], ctypes.c_int),
+        "spx_build_bsr": ([i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
+                           ctypes.c_int, vp], ctypes.c_int),
+        "spx_check_csr": ([i32, i32, i64, vp, vp, i32, ctypes.c_int, vp], ctypes.c_int),
+        "spx_row_stats": ([i32, vp, ctypes.c_int, ctypes.POINTER(RowStats)], ctypes.c_int),
+        "spx_plan_opts_default": ([ctypes.POINTER(PlanOpts)], ctypes.c_int),
+        "spx_plan_opts_auto": ([ctypes.POINTER(RowStats), ctypes.POINTER(PlanOpts)], ctypes.c_int),
+        "spx_plan_csr": ([i32, i32, i64, vp, ctypes.c_int, ctypes.POINTER(PlanOpts), ctypes.POINTER(vp)],
+                         ctypes.c_int),
+        "spx_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], ctypes.c_int),
+        "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
+        "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
+        "spx_plan_destroy": ([vp], ctypes.c_int),
+        "spx_plan_fingerprint": ([vp, ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+        "spx_plan_validate": ([vp, i32, i32, i64, vp, ctypes.c_int, vp], ctypes.c_int),
+        "spx_plan_autotune": ([i32, i32, i64, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanOpts), i32, i32, vp,
+                               ctypes.POINTER(PlanOpts), ctypes.POINTER(ctypes.c_float),
+                               ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+        "spx_plan_autotune_forget": ([], ctypes.c_int),
+        "spx_sell_opts_default": ([ctypes.POINTER(SellOpts)], ctypes.c_int),
+        "spx_sell_build": ([i32, i32, i64, vp, vp, vp, ctypes.c_int, ctypes.POINTER(SellOpts),
+                            ctypes.POINTER(vp)], ctypes.c_int),
+        "spx_sell_get_info": ([vp, ctypes.POINTER(SellInfo)], ctypes.c_int),
+        "spx_sell_get_arrays": ([vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "spx_sell_upload": ([vp, vp, sz, vp], ctypes.c_int),
+        "spx_sell_destroy": ([vp], ctypes.c_int),
+        "spx_spmv_sell": ([vp, i32, i32, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
+        "spx_spmv_csr": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
+        "spx_spmv_csr_noalloc": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp], ctypes.c_int),
+        "spx_spmv_csr_hostio_work_bytes": ([i32, i32], sz),
+        "spx_spmv_csr_hostio": ([vp, i32, i32, i64, vp, vp, vp, f32, vp, i64, f32, vp, i64, i32, vp, sz, vp, sz, vp],
+                                ctypes.c_int),
+        "spx_spmv_coo_scratch_bytes": ([i64], sz),
+        "spx_spmv_coo": ([i32, i32, i64, vp, vp, vp, f32, vp, f32, vp, vp, sz, vp], ctypes.c_int),
+        "spx_spmv_csr_dual": ([vp, vp, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, f32, f32, vp, f32, f32, vp,
+                               sz, vp], ctypes.c_int),
+        "spx_spmm_csr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+        "spx_spmm_csr_tiled": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, i32, vp], ctypes.c_int),
+        "spx_spmm_csr_variant": ([i32, vp, i64, vp, i64], ctypes.c_int32),
+        "spx_spmm_csr_bf16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+        "spx_spmm_csr_f16": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+        "spx_spmm_csr_planned_scratch_bytes": ([vp, i32], sz),
+        "spx_spmm_csr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                 ctypes.c_int),
+        "spx_spmm_csr_bf16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                      ctypes.c_int),
+        "spx_spmm_csr_f16_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                     ctypes.c_int),
+        "spx_spmm_bsr": ([i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+        "spx_build_wcsr": ([i32, i32, vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(ctypes.c_int64), d,
+                            ctypes.c_int, vp], ctypes.c_int),
+        "spx_spmm_wcsr": ([i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp], ctypes.c_int),
+        "spx_wcsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
+        "spx_wcsr_plan_info": ([vp, ctypes.POINTER(WcsrPlanInfo)], ctypes.c_int),
+        "spx_wcsr_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
+        "spx_wcsr_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
+        "spx_wcsr_plan_destroy": ([vp], ctypes.c_int),
+        "spx_spmm_wcsr_planned_scratch_bytes": ([vp, i32], sz),
+        "spx_spmm_wcsr_planned": ([vp, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz, vp],
+                                  ctypes.c_int),
+        "spx_bsr_plan_build": ([i32, i64, vp, ctypes.c_int, i32, ctypes.POINTER(vp)], ctypes.c_int),
+        "spx_spmm_bsr_planned_scratch_bytes": ([vp, i32], sz),
+        "spx_spmm_bsr_planned": ([vp, i32, i32, i32, i32, i64, vp, vp, vp, i32, vp, i64, f32, f32, vp, i64, vp, sz,
+                                  vp], ctypes.c_int),
+        "spx_gather_probe_blocks": ([], ctypes.c_int32),
+        "spx_gather_probe": ([i64, vp, vp, vp, i32, vp, i32, vp], ctypes.c_int),
+        "spx_last_device_error": ([vp], ctypes.c_int),
+        "spx_wait_probe": ([i64, vp], ctypes.c_int),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
 
 
 def header_symbols() -> list[str]:
@@ -343,6 +376,7 @@ class WcsrPlan:
 
     def __init__(self, M: int, nchunks: int, win_ptr, max_chunks: int = 0, device=None, upload=True, stream=None):
         lib = _lib()
+        self._owner = lib  # the library that made this object also releases it
         h = ctypes.c_void_p()
         _check(getattr(lib, self._build)(M, nchunks, _ptr(win_ptr), _where(win_ptr), int(max_chunks), ctypes.byref(h)),
                self._build)
@@ -365,7 +399,7 @@ class WcsrPlan:
 
     def close(self):
         if self.handle:
-            _lib().spx_wcsr_plan_destroy(self.handle)
+            self._owner.spx_wcsr_plan_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -446,6 +480,7 @@ class Plan:
     def __init__(self, M: int, K: int, nnz: int, row_ptr, opts: dict | None = None, device=None, upload=True,
                  stream=None):
         lib = _lib()
+        self._owner = lib  # the library that made this object also releases it
         o = None
         if opts:
             base = spx_plan_opts_default()
@@ -493,7 +528,7 @@ class Plan:
 
     def close(self):
         if self.handle:
-            _lib().spx_plan_destroy(self.handle)
+            self._owner.spx_plan_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -513,6 +548,7 @@ class Sell:
     def __init__(self, M: int, K: int, row_ptr, col, val, opts: dict | None = None, upload=True, device=None,
                  stream=None):
         lib = _lib()
+        self._owner = lib  # the library that made this object also releases it
         o = None
         if opts:
             base = SellOpts()
@@ -553,7 +589,7 @@ class Sell:
 
     def close(self):
         if self.handle:
-            _lib().spx_sell_destroy(self.handle)
+            self._owner.spx_sell_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

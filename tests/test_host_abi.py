@@ -12,10 +12,12 @@ import synth
 from csr_bsr_spmv_gb300 import spx
 
 
-def test_exports_every_header_symbol():
+@pytest.mark.parametrize("path", [spx.LIB_PATH, spx.LIB_CHECK_PATH])
+def test_exports_every_header_symbol(path):
+    """The product library and its bounds-checked twin both export every call the header declares."""
     names = spx.header_symbols()
     assert len(names) >= 22
-    lib = ctypes.CDLL(spx.LIB_PATH)
+    lib = ctypes.CDLL(path)
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
 
