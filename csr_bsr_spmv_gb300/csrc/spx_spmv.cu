@@ -45,6 +45,15 @@ __device__ __forceinline__ float ld_stream(const float* p) { return spx_gather::
 __device__ __forceinline__ int ld_stream(const int* p) { return spx_gather::ld_once(p); }
 using spx_gather::ld_x;
 
+// Programmatic dependent launch (a kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running): let_dependents_start() lets the next kernel's CTAs be scheduled
+// as this grid's SMs free up; predecessor_done() waits until the previous
+// kernel has finished and its writes are visible.  Both are no-ops for a
+// kernel launched the ordinary way.
+__device__ __forceinline__ void let_dependents_start() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void predecessor_done() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(kFull, v, d);
@@ -130,12 +139,14 @@ __device__ __forceinline__ void stage_products(int p0, int n, const int* __restr
             c[j] = k < n ? ld_stream(col + p0 + k) : 0;
             v[j] = k < n ? ld_stream(val + p0 + k) : 0.f;
         }
+        predecessor_done();  // x may be the previous kernel's output: the matrix loads above are already in flight
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
             const int k = threadIdx.x + j * NT;
             if (k < n) s_prod[sk(k)] = v[j] * gather_x(x, c[j], K);
         }
     } else {
+        predecessor_done();
         for (int k = threadIdx.x; k < n; k += NT)
             s_prod[sk(k)] = ld_stream(val + p0 + k) * gather_x(x, ld_stream(col + p0 + k), K);
     }
@@ -260,6 +271,7 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
                                                               float* y, float* __restrict__ partials, int block_nnz,
                                                               int block_rows, int K) {
     extern __shared__ __align__(16) float smem[];
+    let_dependents_start();
     const int4 t = tasks[blockIdx.x];
     const int kind = t.x & 3;
     if (kind == kTaskGroup) {
@@ -295,6 +307,7 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
     } else {
         // the old y of a CTA row is read up front, off the critical path
         const float y_old = (kind == kTaskCta && beta != 0.f && threadIdx.x == 0) ? y[t.y] : 0.f;
+        predecessor_done();
         float s = range_dot<NT>(t.z, t.w, col, val, x, K);
         s = block_sum<NT>(s, smem);
         if (threadIdx.x == 0) {
@@ -310,6 +323,7 @@ __global__ void __launch_bounds__(kThreads) spmv_fixup_kernel(const int4* __rest
                                                               float beta, float* y) {
     const int w = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    predecessor_done();  // the partial sums are the main kernel's output
     if (w >= nlong) return;
     const int4 lr = longrows[w];
     float s = 0.f;
@@ -348,14 +362,47 @@ __global__ void __launch_bounds__(kThreads) gather_probe_kernel(const int* __res
     if (threadIdx.x == 0) partials[blockIdx.x] = s;
 }
 
+// A launch of `kernel` on st; with pdl, one that may start while the kernel
+// before it on st is still running (programmatic stream serialization): the
+// kernel waits for it with predecessor_done() before reading its output.
+template <typename... P, typename... A>
+cudaError_t launch(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t st, bool pdl,
+                   A... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<P>(args)...);
+}
+
+template <int NT, int ITEMS>
+cudaError_t launch_tasks(int ntasks, size_t smem, cudaStream_t st, bool pdl, const int4* tasks, const int* rp,
+                         const int* col, const float* val, const float* x, float alpha, float beta, float* y,
+                         float* scratch, int B, int R, int K) {
+    spx_carve::fit(spmv_tasks_kernel<NT, ITEMS>, NT, smem);
+    return launch(spmv_tasks_kernel<NT, ITEMS>, ntasks, NT, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y,
+                  scratch, B, R, K);
+}
+
+// The SpMV of one plan: the task kernel, then (split rows) the fix-up.  pdl:
+// the task kernel may start while the previous kernel on st runs (its matrix
+// loads overlap that kernel's last CTAs; it reads x only once that kernel is
+// done) -- the second product of the operator pair, whose x is the first's y.
+// The fix-up always starts that way behind the task kernel.
 spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const float* val, float alpha,
-                       const float* x, float beta, float* y, float* scratch, cudaStream_t st) {
+                       const float* x, float beta, float* y, float* scratch, cudaStream_t st, bool pdl = false) {
     const int ntasks = static_cast<int>(P->counts[0]);
     const int nlong = static_cast<int>(P->counts[1]);
     if (ntasks == 0) return SPX_OK;
     const int4* tasks = static_cast<const int4*>(P->d_table);
     const int4* longrows = tasks + ntasks;
-    const int B = P->opts.block_nnz, R = P->opts.block_rows;
+    const int B = P->opts.block_nnz, R = P->opts.block_rows, K = static_cast<int>(P->K);
     // Eight products per thread: block_nnz 512 / 1024 / 2048 / 4096 runs 64 /
     // 128 / 256 / 512-thread CTAs (smaller CTAs, more of them resident: measured
     // better on skewed rows); other sizes take the runtime-loop form with 256
@@ -364,40 +411,22 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) +
                         sizeof(int) * (static_cast<size_t>(R) + 1) + 2 * (NT / 32) * sizeof(float) +
                         sizeof(float) * static_cast<size_t>(R);
+    cudaError_t e = cudaSuccess;
     switch (B) {
-        case 512:
-            spx_carve::fit(spmv_tasks_kernel<64, 8>, 64, smem);
-            spmv_tasks_kernel<64, 8><<<ntasks, 64, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
-                                                                     static_cast<int>(P->K));
-            break;
-        case 1024:
-            spx_carve::fit(spmv_tasks_kernel<128, 8>, 128, smem);
-            spmv_tasks_kernel<128, 8><<<ntasks, 128, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
-                                                                     static_cast<int>(P->K));
-            break;
-        case 2048:
-            spx_carve::fit(spmv_tasks_kernel<256, 8>, 256, smem);
-            spmv_tasks_kernel<256, 8><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
-                                                                     static_cast<int>(P->K));
-            break;
-        case 4096:
-            spx_carve::fit(spmv_tasks_kernel<512, 8>, 512, smem);
-            spmv_tasks_kernel<512, 8><<<ntasks, 512, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
-                                                                     static_cast<int>(P->K));
-            break;
-        default:
-            spx_carve::fit(spmv_tasks_kernel<256, 0>, 256, smem);
-            spmv_tasks_kernel<256, 0><<<ntasks, 256, smem, st>>>(tasks, rp, col, val, x, alpha, beta, y, scratch, B, R,
-                                                                     static_cast<int>(P->K));
-            break;
+        case 512: e = launch_tasks<64, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
+        case 1024: e = launch_tasks<128, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
+        case 2048: e = launch_tasks<256, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
+        case 4096: e = launch_tasks<512, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
+        default: e = launch_tasks<256, 0>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
     }
     uint64_t launches = 1;
-    if (nlong > 0) {
-        spmv_fixup_kernel<<<(nlong + kWarps - 1) / kWarps, kThreads, 0, st>>>(longrows, nlong, scratch, alpha, beta, y);
+    if (e == cudaSuccess && nlong > 0) {
+        e = launch(spmv_fixup_kernel, (nlong + kWarps - 1) / kWarps, kThreads, 0, st, true, longrows, nlong, scratch,
+                   alpha, beta, y);
         ++launches;
     }
     spx_note_launches(launches);
-    return spx_cuda_status(cudaGetLastError());
+    return spx_cuda_status(e != cudaSuccess ? e : cudaGetLastError());
 }
 
 spx_status check_call(const spx_plan* P, int32_t M, int32_t K, int64_t nnz, const int32_t* rp, const int32_t* col,
@@ -527,8 +556,8 @@ spx_status spx_spmv_csr_dual(const spx_plan* pA, const spx_plan* pAt, int32_t m,
     if (s != SPX_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (m > 0) s = launch_spmv(pA, A_rp, A_col, A_val, alpha_u, v, beta_u, u, static_cast<float*>(scratch), st);
-    if (s == SPX_OK && n > 0)
-        s = launch_spmv(pAt, At_rp, At_col, At_val, alpha_v, u, beta_v, v, static_cast<float*>(scratch), st);
+    if (s == SPX_OK && n > 0)  // starts while the first product finishes; gathers u once it is done
+        s = launch_spmv(pAt, At_rp, At_col, At_val, alpha_v, u, beta_v, v, static_cast<float*>(scratch), st, m > 0);
     return s;
 }
 

@@ -354,6 +354,9 @@ spx_status spx_spmv_csr_hostio(const spx_plan* plan, int32_t M, int32_t K, int64
  * beta_u = -alpha_k and alpha_v = 1, beta_v = -beta_k.
  *   plan_A / plan_At: uploaded plans of CSR(A) and CSR(A^T).
  *   scratch: at least max(scratch_bytes of both plans).
+ * The second product is launched with programmatic dependent launch: its
+ * CTAs start loading CSR(A^T) while the first product's last CTAs run, and
+ * read u only after the first product has finished.
  */
 spx_status spx_spmv_csr_dual(const spx_plan* plan_A, const spx_plan* plan_At, int32_t m, int32_t n, int64_t nnz,
                              const int32_t* A_row_ptr, const int32_t* A_col, const float* A_val,
