@@ -266,13 +266,19 @@ __global__ void __launch_bounds__(kThreads)
                     for (int c0 = 0; c0 < kWin; c0 += 32) {
                         uint32_t v[32];
                         tmem_ld32(tmem_d + (static_cast<uint32_t>(32 * q) << 16) + 64 * hh + c0, v);
+                        float old[32];  // beta != 0: all 32 old values are loaded before any store
+                        if (ebeta != 0.f) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                old[j] = (!GUARD || (cok && c0 + j < rows)) ? dst[static_cast<long long>(c0 + j) * dstride] : 0.f;
+                        }
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             if (!GUARD || (cok && c0 + j < rows)) {
                                 float* p = dst + static_cast<long long>(c0 + j) * dstride;
                                 const float acc = ealpha * __uint_as_float(v[j]);
-                                __stcs(p, ebeta != 0.f ? acc + ebeta * *p : acc);
+                                __stcs(p, ebeta != 0.f ? acc + ebeta * old[j] : acc);
                             }
                         }
                     }

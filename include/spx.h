@@ -611,9 +611,15 @@ typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side: the task split
  * multiple of 8, ldc >= N; bsr_val and B 16-byte aligned, C 4-byte aligned
  * (SPX_ERR_ALIGN otherwise).  Launches: 1 persistent kernel (as many CTAs
  * as the SMs hold at once, each walking a static list of 128-column x 64-row
- * output tiles; a tile's epilogue overlaps the next tile's MMAs).  Its
- * pipeline waits are bounded: on expiry the kernel records an error that
- * spx_last_device_error reports as SPX_ERR_TIMEOUT.
+ * output tiles; a tile's epilogue overlaps the next tile's MMAs), or 2 when
+ * the last round of tiles would leave at least half the CTAs idle and the
+ * block-rows average 48 blocks or more: that round's tiles are then cut in
+ * two, the first launch storing their head pieces and a second one (allowed
+ * to start early, programmatic dependent launch) adding the tail pieces into
+ * C after the first has finished.  Results are then rounded in a different
+ * order than with one launch (fp32 rounding level), but are the same from
+ * run to run.  Pipeline waits are bounded: on expiry the kernel records an
+ * error that spx_last_device_error reports as SPX_ERR_TIMEOUT.
  */
 spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,

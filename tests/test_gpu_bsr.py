@@ -213,7 +213,9 @@ def test_planned_task_split(max_blocks, N, alpha, beta):
     C3 = torch.from_numpy(C0.copy()).cuda()
     spx.spx_spmm_bsr(M, K, 64, 64, dbrp, dbcol, dbval, dB, C3, alpha=alpha, beta=beta)
     if P.info["split_windows"] == 0:
-        assert torch.equal(outs[0], C3)  # no split: the same tiles
+        # no task split: the same products; the plain call may still cut its last round of tiles in two
+        # (head and tail pieces added in another order), so the two agree to fp32 rounding
+        assert_within(C3.cpu().numpy(), outs[0].cpu().numpy().astype(np.float64), bound, what="plain vs planned")
     assert_within(C3.cpu().numpy(), ref, bound, rel=BF16_REL, ab=BF16_ABS, what="plain bsr")
 
 
@@ -302,3 +304,36 @@ def test_bounded_wait_runs_out_and_reports_timeout():
     assert spx.spx_last_device_error() == 0
     test_small_integers_exact()
     assert spx.spx_last_device_error() == 0
+
+
+@pytest.mark.parametrize("MB,KB,per_row,N,beta", [(20, 80, 60, 256, 0.0), (20, 80, 60, 200, 0.5),
+                                                  (64, 70, 64, 1024, -1.0), (9, 40, 31, 384, 0.0)])
+def test_last_round_cut_in_two(MB, KB, per_row, N, beta):
+    """When the last round of tiles leaves at least half the resident CTAs idle and block-rows hold 48 blocks or
+    more on average, its tiles are cut in two: a head piece stored by the first launch, a tail piece added by a
+    second launch (two launches).  Against the oracle (bf16 bound and fp32 rounding), with beta, reproducibly,
+    with nothing written past column N; a pattern below the 48-block average stays whole (one launch)."""
+    counts = [per_row] * MB
+    brp, bcol = pattern(7, MB, KB, counts)
+    nb = bcol.size
+    A = synth.normal_bf16(7, synth.T_VAL, nb * 4096, 0.02).reshape(nb, 64, 64)
+    B = synth.normal_bf16(7, synth.T_B, KB * 64 * N, 1.0).reshape(KB * 64, N)
+    C0 = synth.uniform(7, synth.T_Y, MB * 64 * N).reshape(MB * 64, N)
+    ntiles = MB * ((N + 127) // 128)
+    G = 3 * torch.cuda.get_device_properties(0).multi_processor_count  # the persistent kernel's resident CTAs
+    R = ntiles % G
+    cut = R > 0 and 2 * R <= G and per_row >= 48
+    outs = []
+    for _ in range(2):
+        Cd = torch.from_numpy(C0.copy()).cuda()
+        before = spx.launch_count()
+        spx.spx_spmm_bsr(MB * 64, KB * 64, 64, 64, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                         bits_dev(A.reshape(-1)), bits_dev(B), Cd, alpha=1.0, beta=beta)
+        torch.cuda.synchronize()
+        assert spx.launch_count() - before == (2 if cut else 1)
+        assert spx.spx_last_device_error() == 0
+        outs.append(Cd.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    ref, bound = oracle.bsr_spmm(MB * 64, KB * 64, 64, 64, brp, bcol, A, B, alpha=1.0, beta=beta, C=C0)
+    assert_within(outs[0], ref, bound, BF16_REL, BF16_ABS, what=f"cut={cut}")
+    assert_within(outs[0], ref, bound, 1e-5, 1e-6, what="fp32-level")
