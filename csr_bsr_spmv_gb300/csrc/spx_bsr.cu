@@ -661,13 +661,16 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream) {
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
-    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * kBlk > kI32Max) return SPX_ERR_INDEX_RANGE;
-    if (br != kBlk || bc != kBlk) return SPX_ERR_UNSUPPORTED;
+    const bool tc = br == kBlk && bc == kBlk;  // the tensor-core shape; others run bsr_spmm_simt_kernel
+    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * (tc ? kBlk : bc) > kI32Max) return SPX_ERR_INDEX_RANGE;
     if (M == 0 || N == 0) return SPX_OK;
     if (!bsr_row_ptr || !C || (nnzb > 0 && (!bsr_col || !bsr_val || !B))) return SPX_ERR_ARG;
     if (ldb < N || ldc < N) return SPX_ERR_ARG;
-    if (ldb % 8 || !spx_aligned(bsr_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
-        !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4))
+    if (tc && (ldb % 8 || !spx_aligned(bsr_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
+               !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
+        return SPX_ERR_ALIGN;
+    if (!tc && (ldb % 2 || !spx_aligned(bsr_val, 2) || !spx_aligned(B, 4) || !spx_aligned(C, 4) ||
+                !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
         return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (nnzb == 0 && beta == 0.f) {
@@ -682,6 +685,9 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         spx_note_launches(1);
         return spx_cuda_status(cudaGetLastError());
     }
+    if (!tc)
+        return spx_bsr_simt_spmm(M, K, br, bc, nnzb, bsr_row_ptr, bsr_col, bsr_val, N, B, ldb, alpha, beta, C, ldc,
+                                 st);
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
         !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
@@ -772,7 +778,7 @@ spx_status spx_last_device_error(spx_stream_t stream) {
     const int wcsr = spx_wcsr_error_take();
     // the checked build's index errors (always 0 in the product build, which reads no word for them)
     const int checked[] = {spx_check_take(g_bsr_check), spx_spmv_check_take(), spx_spmm_check_take(),
-                           spx_sell_check_take(), spx_wcsr_check_take()};
+                           spx_sell_check_take(), spx_wcsr_check_take(), spx_bsrg_check_take()};
     if (h || wcsr == SPX_ERR_TIMEOUT) return SPX_ERR_TIMEOUT;
     if (wcsr == SPX_ERR_CUDA) return SPX_ERR_CUDA;
     for (int c : checked)

@@ -46,6 +46,14 @@ int spx_spmv_check_take();
 int spx_spmm_check_take();
 int spx_sell_check_take();
 int spx_wcsr_check_take();
+int spx_bsrg_check_take();
+
+// BSR SpMM for block shapes other than 64 x 64 (spx_bsr_simt.cu): the
+// arguments of spx_spmm_bsr, validated by it (ldb even; bsr_val 2-, B and C
+// 4-byte aligned); nnzb > 0, M > 0, N > 0.
+spx_status spx_bsr_simt_spmm(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nnzb, const int32_t* bsr_row_ptr,
+                             const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B,
+                             int64_t ldb, float alpha, float beta, float* C, int64_t ldc, cudaStream_t st);
 
 // Device-side builders (spx_build.cu): stable radix sorts on the GPU, results
 // identical to the host builders.  Stream-ordered; temporary memory from the

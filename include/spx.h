@@ -598,19 +598,24 @@ typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side: the task split
 /*
  * C = alpha * A B + beta * C with A in BSR (br x bc blocks, row-major inside,
  * bf16), B dense K x N bf16 row-major (ldb), C dense M x N fp32 row-major
- * (ldc); products accumulated in fp32 on the tensor cores, the epilogue in
- * fp32 (beta == 0: C is write-only).  [SpMM-ops] §3.4 (loop over the
+ * (ldc); products accumulated in fp32 (on the tensor cores for 64 x 64
+ * blocks), the epilogue in fp32 (beta == 0: C is write-only).  [SpMM-ops] §3.4 (loop over the
  * nonzero blocks, each a small dense GEMM on the tensor cores) and
  * [AsyncSparse] §2.2.1, §3 (BCSR SpMM: asynchronous copies of A blocks and
  * B tiles into shared memory feeding the matrix units).
- * Shapes: br == bc == 64 (else SPX_ERR_UNSUPPORTED), any M, K and N.  A
- * ragged last block-row or block column is zero-padded in the BSR arrays (as
- * spx_build_bsr writes them).  B rows at or beyond K are read as zeros, and C
- * is stored only inside its M x N part, so a ragged last 128-column tile does
- * a whole tile's work but writes nothing past column N.  ldb >= N and a
- * multiple of 8, ldc >= N; bsr_val and B 16-byte aligned, C 4-byte aligned
- * (SPX_ERR_ALIGN otherwise).  Launches: 1 persistent kernel (as many CTAs
- * as the SMs hold at once, each walking a static list of 128-column x 64-row
+ * Shapes: any br x bc block, any M, K and N.  A ragged last block-row or
+ * block column is zero-padded in the BSR arrays (as spx_build_bsr writes
+ * them).  B rows at or beyond K are read as zeros, and C is stored only
+ * inside its M x N part, so a ragged last column tile does a whole tile's
+ * work but writes nothing past column N.  ldb >= N, ldc >= N; nnzb * bc
+ * must fit int32 (SPX_ERR_INDEX_RANGE otherwise).
+ * Blocks other than 64 x 64 run on the CUDA cores (one launch; each CTA
+ * owns up to 64 rows of a block-row and a strip of columns and sums every
+ * element's terms in their stored order with fp32 fused multiply-adds): ldb
+ * even, bsr_val 2-byte, B and C 4-byte aligned.  64 x 64 blocks run on the
+ * tensor cores: ldb a multiple of 8, bsr_val and B 16-byte aligned, C 4-byte
+ * aligned (SPX_ERR_ALIGN otherwise), and the launches are 1 persistent
+ * kernel (as many CTAs as the SMs hold at once, each walking a static list of 128-column x 64-row
  * output tiles; a tile's epilogue overlaps the next tile's MMAs), or 2 when
  * the last round of tiles would leave at least half the CTAs idle and the
  * block-rows average 48 blocks or more: that round's tiles are then cut in
@@ -635,7 +640,8 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
  * does, pieces write raw 64 x N partial tiles to scratch
  * (spx_spmm_bsr_planned_scratch_bytes) and a fix-up adds them in piece order
  * and applies alpha/beta.  Same shape, alignment and error rules as
- * spx_spmm_bsr, plus those of spx_spmm_wcsr_planned for the plan and scratch.
+ * spx_spmm_bsr, plus those of spx_spmm_wcsr_planned for the plan and scratch;
+ * the planned call takes 64 x 64 blocks only (SPX_ERR_UNSUPPORTED otherwise).
  * Launches: 1, or 2 with split block-rows.
  */
 spx_status spx_bsr_plan_build(int32_t M, int64_t nnzb, const int32_t* bsr_row_ptr, spx_loc where, int32_t max_blocks,

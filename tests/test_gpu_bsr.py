@@ -107,16 +107,126 @@ def test_random_blocks(counts, N, ldb, ldc):
     assert_within(got, ref, bound, 1e-5, 1e-6, what="fp32-level")
 
 
-def test_unsupported_shapes_rejected_without_launch():
+def test_bad_arguments_rejected_without_launch():
     lib = spx._lib()
     before = spx.launch_count()
     z = torch.zeros(64 * 1024, dtype=torch.int32, device="cuda")
     p = spx._ptr(z)
-    assert lib.spx_spmm_bsr(64, 64, 32, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -7   # block size
-    assert lib.spx_spmm_bsr(64, 64, 64, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -7   # bc != 64
+    assert lib.spx_spmm_bsr(64, 64, 0, 32, 1, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -1    # br <= 0
     assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 100, 1.0, 0.0, p, 128, None) == -1   # ldb < N
-    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, 1.0, 0.0, p, 128, None) == -8   # ldb % 8
+    assert lib.spx_spmm_bsr(64, 64, 64, 64, 1, p, p, p, 128, p, 132, 1.0, 0.0, p, 128, None) == -8   # ldb % 8 (64 x 64)
+    assert lib.spx_spmm_bsr(64, 64, 16, 8, 1, p, p, p, 128, p, 131, 1.0, 0.0, p, 128, None) == -8    # odd ldb (others)
+    assert lib.spx_spmm_bsr(64, 64, 16, 8, 1, p, p, p + 2, 128, p + 2, 130, 1.0, 0.0, p, 128, None) == -8  # B 2-byte
+    assert lib.spx_spmm_bsr(64, 64, 16, 16, 1 << 27, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None) == -2  # nnzb*bc
+    # the block-row split is built for 64-row block-rows only
+    plan = spx.BsrPlan(64, 0, torch.zeros(2, dtype=torch.int32))
+    assert lib.spx_spmm_bsr_planned(plan.handle, 64, 64, 16, 16, 0, p, p, p, 128, p, 128, 1.0, 0.0, p, 128, None, 0,
+                                    None) == -7
     assert spx.launch_count() == before
+
+
+def _bsr_case(seed, M, K, br, bc, lmin, lmax, values="uniform"):
+    d = synth.random_coo(seed, M, K, lmin, lmax, values)
+    vb = synth.to_bf16_bits(d["val"])
+    rp, col, val = oracle.build_csr(M, K, d["row"], d["col"], vb)
+    brp, bcol, bval, _ = oracle.build_bsr(M, K, rp, col, val, br, bc)
+    return brp, bcol, bval
+
+
+def _gamma(n):
+    u = 2.0 ** -24
+    return n * u / (1 - n * u)
+
+
+@pytest.mark.parametrize("M,K,br,bc,N", [
+    (37, 29, 1, 1, 64),
+    (100, 90, 2, 2, 130),
+    (97, 203, 3, 5, 77),
+    (256, 256, 4, 4, 512),
+    (300, 260, 8, 8, 129),
+    (512, 384, 16, 16, 256),
+    (200, 330, 32, 32, 96),
+    (190, 400, 16, 64, 200),
+    (400, 190, 64, 16, 200),
+    (333, 333, 64, 32, 65),
+    (300, 500, 128, 128, 130),
+    (250, 250, 100, 70, 33),
+    (64, 70, 1, 64, 8),
+    (70, 64, 64, 1, 1),
+])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_general_block_shapes(M, K, br, bc, N, beta):
+    """Block shapes other than 64 x 64 (the CUDA-core kernel): ragged M, K, N,
+    padded leading dimensions, alpha/beta; against the oracle within the fp32
+    accumulation bound of each element's term count, nothing written outside
+    the M x N part of C, and beta = 0 never reading C (NaN there stays out)."""
+    brp, bcol, bval = _bsr_case(11 + br * 7 + bc, M, K, br, bc, 0, 40)
+    B = synth.normal_bf16(12, synth.T_B, K * N, 1.0).reshape(K, N)
+    C0 = synth.uniform(13, synth.T_Y, M * N).reshape(M, N).astype(np.float32)
+    ldb, ldc = N + (N % 2) + 6, N + 3
+    Bfull = np.zeros((K, ldb), np.uint16)
+    Bfull[:, :N] = B
+    Bd = bits_dev(Bfull)[:, :N]
+    Cfull = torch.full((M + 1, ldc), -7.0, device="cuda")
+    Cd = Cfull[:M, :N]
+    Cd.copy_(torch.from_numpy(C0) if beta != 0.0 else torch.full((M, N), float("nan")))
+    spx.spx_spmm_bsr(M, K, br, bc, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(bval.reshape(-1)), Bd, Cd, alpha=1.5, beta=beta)
+    torch.cuda.synchronize()
+    assert spx.spx_last_device_error() == 0
+    out = Cfull.cpu().numpy()
+    assert np.all(out[:M, N:] == -7.0) and np.all(out[M] == -7.0)
+    got = out[:M, :N]
+    ref, bound = oracle.bsr_spmm(M, K, br, bc, brp, bcol, bval, B, alpha=1.5, beta=beta,
+                                 C=C0 if beta != 0.0 else None)
+    nterm = int(np.diff(brp).max(initial=0)) * bc
+    assert_within(got, ref, bound, _gamma(nterm + 3), 0.0, what=f"{br}x{bc}")
+    # bitwise the same on a second call
+    Cd2 = torch.from_numpy(C0).cuda() if beta != 0.0 else torch.zeros(M, N, device="cuda")
+    spx.spx_spmm_bsr(M, K, br, bc, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(bval.reshape(-1)), Bd, Cd2, alpha=1.5, beta=beta)
+    assert np.array_equal(Cd2.cpu().numpy().view(np.uint32), got.view(np.uint32))
+
+
+@pytest.mark.parametrize("br,bc", [(4, 4), (16, 8), (3, 7), (96, 48)])
+def test_general_shapes_small_integers_exact(br, bc):
+    """Entries and B small integers: every product and partial sum is exact in
+    fp32, so the result equals the dense product exactly."""
+    M, K, N = 180, 150, 70
+    brp, bcol, bval = _bsr_case(21 + br, M, K, br, bc, 0, 30, "int")
+    B = np.floor(synth.uniform(22, synth.T_B, K * N, -3, 4)).astype(np.float32).reshape(K, N)
+    Bb = synth.to_bf16_bits(B).reshape(K, N)
+    Cd = torch.full((M, N), -7.0, device="cuda")
+    spx.spx_spmm_bsr(M, K, br, bc, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(bval.reshape(-1)), bits_dev(Bb), Cd)
+    torch.cuda.synchronize()
+    dense = np.zeros(((M + br - 1) // br * br, (K + bc - 1) // bc * bc))
+    Af = synth.bf16_bits_to_f32(bval.reshape(-1)).reshape(bval.shape)
+    for I in range(brp.size - 1):
+        for b in range(brp[I], brp[I + 1]):
+            dense[I * br:(I + 1) * br, bcol[b] * bc:(bcol[b] + 1) * bc] = Af[b]
+    assert np.array_equal(Cd.cpu().numpy(), dense[:M, :K] @ B.astype(np.float64))
+
+
+def test_general_shape_empty_and_long_block_rows():
+    """Empty block-rows (C = beta C) next to a block-row of every block column
+    (chunk boundaries inside a block, many chunks)."""
+    M, K, br, bc, N = 5 * 12, 40 * 12, 12, 12, 96
+    counts = [0, 40, 3, 0, 17]
+    brp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    bcol = np.concatenate([np.sort(synth.permutation(31 + I, 40)[:c]) for I, c in enumerate(counts)]).astype(np.int32)
+    nb = bcol.size
+    A = synth.normal_bf16(31, synth.T_VAL, nb * br * bc, 0.5).reshape(nb, br, bc)
+    B = synth.normal_bf16(32, synth.T_B, K * N, 1.0).reshape(K, N)
+    C0 = synth.uniform(33, synth.T_Y, M * N).reshape(M, N).astype(np.float32)
+    Cd = torch.from_numpy(C0.copy()).cuda()
+    spx.spx_spmm_bsr(M, K, br, bc, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
+                     bits_dev(A.reshape(-1)), bits_dev(B), Cd, alpha=-1.0, beta=2.0)
+    torch.cuda.synchronize()
+    ref, bound = oracle.bsr_spmm(M, K, br, bc, brp, bcol, A, B, alpha=-1.0, beta=2.0, C=C0)
+    assert_within(Cd.cpu().numpy(), ref, bound, _gamma(40 * bc + 3), 0.0, what="empty/long")
+    got = Cd.cpu().numpy()
+    assert np.array_equal(got[:br], (2.0 * C0[:br]).astype(np.float32))
 
 
 @pytest.mark.parametrize("alpha,beta", [(2.0, 0.0), (-0.5, 1.5), (1.0, -1.0)])

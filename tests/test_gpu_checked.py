@@ -204,6 +204,40 @@ def test_bsr_bad_block_column_and_offsets_reported():
         assert spx.spx_last_device_error() == 0
 
 
+def test_bsr_other_shape_bad_block_column_and_offsets_reported():
+    """The CUDA-core kernel of block shapes other than 64 x 64 (here 16 x 8)."""
+    br, bc, MB, KB, N = 16, 8, 7, 12, 100
+    counts = [2, 0, 5, 12, 1, 3, 4]
+    brp = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    bcol = np.concatenate([np.sort(synth.permutation(70 + I, KB)[:c]) for I, c in enumerate(counts)]).astype(np.int32)
+    nb = bcol.size
+    A = synth.normal_bf16(8, synth.T_VAL, nb * br * bc, 0.5).reshape(nb, br, bc)
+    B = synth.normal_bf16(8, synth.T_B, KB * bc * N, 1.0).reshape(KB * bc, N)
+
+    def call(brp_, bcol_):
+        C = torch.zeros(MB * br, N, device="cuda")
+        spx.spx_spmm_bsr(MB * br, KB * bc, br, bc, dev(brp_), dev(bcol_), dev(A.reshape(-1).view(np.int16)),
+                         dev(B.view(np.int16)), C)
+        return C
+
+    C_prod = call(brp, bcol)
+    with spx.checked_build():
+        C_chk = call(brp, bcol)
+        assert spx.spx_last_device_error() == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(C_chk), bits(C_prod))
+        b2 = bcol.copy()
+        b2[6] = -1
+        call(brp, b2)
+        assert spx.spx_last_device_error() == INDEX_RANGE
+        r2 = brp.copy()
+        r2[2] = nb + 9
+        call(r2, bcol)
+        assert spx.spx_last_device_error() == INDEX_RANGE
+        call(brp, bcol)
+        assert spx.spx_last_device_error() == 0
+
+
 def test_wcsr_bad_window_column_reported():
     M, K, N = 256, 4096, 128
     d = synth.random_coo(7, M, K, 5, 60)
