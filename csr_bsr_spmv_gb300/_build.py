@@ -89,10 +89,12 @@ def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = 
             for out in ex.map(run, jobs):
                 if out:
                     print(out)
-    newest = max(os.path.getmtime(o) for o in objs)
+    exports = os.path.join(CSRC, "libspx.map")  # the exported symbols: the C ABI only
+    newest = max([os.path.getmtime(o) for o in objs] + [os.path.getmtime(exports)])
     if force or jobs or not os.path.exists(lib) or os.path.getmtime(lib) < newest:
         tmp = lib + f".tmp{os.getpid()}"
-        cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
+        cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC", "-Xlinker",
+               f"--version-script={exports}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

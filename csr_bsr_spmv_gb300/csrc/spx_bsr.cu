@@ -301,6 +301,45 @@ constexpr int kPThreads = 192;
 constexpr uint32_t kPTmemCols = 2 * kTmemColsT;
 enum : int { kErrTmemFree = 7 };
 
+// Block shapes other than 64 x 64 on the same kernel (GEN = true): br rows
+// (the MMA's N, a multiple of 16 up to 128) and bc columns, taken in chunks
+// of up to 64 (one ring stage each; bc <= 64 or a multiple of 64).  The
+// A box is always 64 wide: a block narrower than 64 columns is read with the
+// columns past bc zero-filled by the copy engine, and only bc / 16 K-steps
+// are issued on its chunk.  The B box has min(bc, 64) rows, so no stage
+// reads B rows of another block column.
+struct TcShape {
+    int br, bc, kc, ksl, brows;  // rows, columns, chunks per block, K-steps of the last chunk, B box rows
+    uint32_t abytes, sb, tx;     // A region and stage bytes (the B region is 16 KB), bytes a stage's copies bring
+    uint32_t pitch, cols;        // TMEM columns per accumulator (a power of two) and allocated (two of them)
+};
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+inline TcShape tc_shape(int br, int bc) {
+    TcShape sh{};
+    sh.br = br;
+    sh.bc = bc;
+    sh.kc = (bc + kBlk - 1) / kBlk;
+    sh.ksl = (bc - (sh.kc - 1) * kBlk) / 16;
+    sh.brows = bc < kBlk ? bc : kBlk;
+    sh.abytes = static_cast<uint32_t>(kBlk * 2 * br);
+    sh.sb = sh.abytes + 2 * kBBox;
+    sh.tx = sh.abytes + 2u * static_cast<uint32_t>(64 * 2 * sh.brows);
+    sh.pitch = pow2_at_least(static_cast<uint32_t>(br));
+    sh.cols = 2 * sh.pitch;
+    return sh;
+}
+
+// Shapes the tensor-core kernel takes besides 64 x 64.
+inline bool tc_general_shape(int br, int bc) {
+    return br % 16 == 0 && br >= 16 && br <= 128 && bc % 16 == 0 && bc >= 16 && (bc <= kBlk || bc % kBlk == 0);
+}
+
 // The work of one CTA of the persistent kernel, item by item.  First launch:
 // the whole tiles c, c + G, c + 2G, ... below `full`, then -- when c < tail --
 // the head piece of tile full + c (its first nb/2 blocks), stored as a whole
@@ -340,29 +379,36 @@ __device__ __forceinline__ bool work_item(int i, int G, int full, int tail, int 
     return true;
 }
 
-template <bool TAIL = false>
+template <bool TAIL = false, bool GEN = false>
 __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the shared-memory limit)
     bsr_spmm_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const int* __restrict__ brp, const int* __restrict__ bcol, float* __restrict__ C,
                             long long ldc, float alpha, float beta, long long spin_limit, int M, int N, int full,
-                            int tail, int ntq, int KB, long long nnzb) {
+                            int tail, int ntq, int KB, long long nnzb, TcShape sh) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ uint32_t s_issued, s_consumed;
 
+    // the block shape: constants for 64 x 64, the launch's TcShape otherwise
+    const int BR = GEN ? sh.br : kBlk, BC = GEN ? sh.bc : kBlk, KC = GEN ? sh.kc : 1, KSL = GEN ? sh.ksl : 4;
+    const int BROWS = GEN ? sh.brows : kBlk;
+    const uint32_t SB = GEN ? sh.sb : kSB, AB = GEN ? sh.abytes : kABytes, TX = GEN ? sh.tx : kSB;
+    const uint32_t PITCH = GEN ? sh.pitch : kTmemColsT, TCOLS = GEN ? sh.cols : kPTmemCols;
+    const uint32_t IDESC = GEN ? idesc_bf16_mn_k(128, static_cast<uint32_t>(BR)) : kIdesc;
+
     // the second launch may start while the first runs: let it be scheduled as this grid's SMs free up
     if (!TAIL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bars = base + STAGES * kSB;
+    const uint32_t bars = base + STAGES * SB;
     auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
     auto empty_bar = [&](uint32_t s) { return bars + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
     const uint32_t fin_bar = bars + 8u * (2 * STAGES + 4);
-    auto stage_a = [&](uint32_t s) { return base + s * kSB; };
-    auto stage_b = [&](uint32_t s) { return base + s * kSB + kABytes; };
+    auto stage_a = [&](uint32_t s) { return base + s * SB; };
+    auto stage_b = [&](uint32_t s) { return base + s * SB + AB; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
@@ -385,7 +431,7 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
     }
     if (warp == 5) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(kPTmemCols)
+                     "r"(TCOLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -402,28 +448,31 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
         for (int i = 0; !stop && !s_abort && work_item<TAIL>(i, G, full, tail, ntq, brp, nnzb, lane == 0, it); ++i) {
             const int n0 = (it.t % ntq) * 128;
             int jreg = 0;
-            for (int b = it.blo; b < it.bhi; ++b, ++g) {
-                const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+            for (int b = it.blo; !stop && b < it.bhi; ++b) {
                 const int k = b - it.blo;
                 if ((k & 31) == 0) jreg = b + lane < it.bhi ? __ldg(bcol + it.b0 + b + lane) : 0;
                 const int J = checked_bcol(__shfl_sync(0xffffffffu, jreg, k & 31), KB);
-                int ok = 1;
-                if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        record_error(kErrEmpty);
-                        s_abort = 1;
+                for (int kc = 0; kc < KC; ++kc, ++g) {  // the block's column chunks, one stage each
+                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+                    int ok = 1;
+                    if (lane == 0) ok = (mbar_wait(empty_bar(s), ph ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            record_error(kErrEmpty);
+                            s_abort = 1;
+                        }
+                        stop = true;
+                        break;
                     }
-                    stop = true;
-                    break;
+                    if (lane == 0) mbar_expect_tx(full_bar(s), TX);
+                    __syncwarp();
+                    if (lane == 0) tma_load_2d(stage_a(s), &tmA, kBlk * kc, (it.b0 + b) * BR, full_bar(s));
+                    else if (lane <= 2)
+                        tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * BC + kBlk * kc,
+                                    full_bar(s));
+                    __syncwarp();
                 }
-                if (lane == 0) mbar_expect_tx(full_bar(s), kSB);
-                __syncwarp();
-                if (lane == 0) tma_load_2d(stage_a(s), &tmA, 0, (it.b0 + b) * kBlk, full_bar(s));
-                else if (lane <= 2)
-                    tma_load_2d(stage_b(s) + (lane - 1) * kBBox, &tmB, n0 + 64 * (lane - 1), J * kBlk, full_bar(s));
-                __syncwarp();
             }
         }
         if (lane == 0) s_issued = g;
@@ -441,23 +490,27 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + buf * kTmemColsT;
-                for (int b = it.blo; b < it.bhi; ++b, ++g) {
-                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
-                    if (!mbar_wait(full_bar(s), ph, spin_limit)) {
-                        record_error(kErrFull);
-                        s_abort = 1;
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                const uint32_t d = tmem + buf * PITCH;
+                for (int b = it.blo; ok && b < it.bhi; ++b) {
+                    for (int kc = 0; kc < KC; ++kc, ++g) {
+                        const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+                        if (!mbar_wait(full_bar(s), ph, spin_limit)) {
+                            record_error(kErrFull);
+                            s_abort = 1;
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int nks = kc == KC - 1 ? KSL : 4;  // K-steps of 16 columns in this chunk
 #pragma unroll
-                    for (int ks = 0; ks < kBlk / 16; ++ks) {
-                        const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
-                        const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
-                        mma_bf16(d, adesc, bdesc, kIdesc, (b > it.blo || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            if (ks >= nks) break;
+                            const uint64_t bdesc = sw128_desc(stage_a(s) + ks * 32u, 16u, 1024u);
+                            const uint64_t adesc = sw128_desc(stage_b(s) + ks * 2048u, kBBox, 1024u);
+                            mma_bf16(d, adesc, bdesc, IDESC, (b > it.blo || kc > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar(s));
                     }
-                    mma_commit(empty_bar(s));
                 }
                 if (!ok) break;
                 if (it.bhi > it.blo) mma_commit(tfull_bar(buf));  // arrives when this item's MMAs have completed
@@ -487,8 +540,8 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
             if (TAIL) asm volatile("griddepcontrol.wait;" ::: "memory");
             const int cn = n0 + 32 * warp + lane;  // this thread's column; columns >= N are not stored
             const bool cok = cn < N;
-            const int mrows = min(kBlk, M - I * kBlk);  // rows of this block-row inside [0, M)
-            float* cp = C + static_cast<long long>(I) * kBlk * ldc + cn;
+            const int mrows = min(BR, M - I * BR);  // rows of this block-row inside [0, M)
+            float* cp = C + static_cast<long long>(I) * BR * ldc + cn;
             if (empty) {
                 // nothing to add (a tail piece), or C = 0 * A B + beta C (a whole tile or a head piece)
                 if (!TAIL && cok)
@@ -498,9 +551,9 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
                 auto drain = [&](auto guard) {
                     constexpr bool GUARD = decltype(guard)::value;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kBlk; c0 += 16) {  // 16 rows at a time: few live registers
+                    for (int c0 = 0; c0 < BR; c0 += 16) {  // 16 rows at a time: few live registers
                         uint32_t v[16];
-                        tmem_ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + buf * kTmemColsT + c0, v);
+                        tmem_ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + buf * PITCH + c0, v);
                         // old values (a tail piece, or beta != 0): all 16 loaded before any store, so no load
                         // waits on the store before it
                         float old[16];
@@ -521,7 +574,7 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
                         }
                     }
                 };
-                if (n0 + 128 <= N && mrows == kBlk) drain(std::false_type{});
+                if (n0 + 128 <= N && mrows == BR) drain(std::false_type{});
                 else drain(std::true_type{});
             }
             tc_fence_before();
@@ -549,7 +602,7 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
     __syncthreads();
     tc_fence_after();
     if (warp == 5)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS) : "memory");
 }
 
 // Test aid for the bounded waits: one thread arms an mbarrier that nothing
@@ -577,81 +630,112 @@ __global__ void bsr_scale_kernel(float* C, long long ldc, int M, int N, float be
 
 // ------------------------------------------------------------ host side
 
+// Dynamic shared memory of the persistent kernel for a stage of `sb` bytes:
+// the ring, 1 KB alignment slack, the barriers.
+constexpr size_t persist_smem(uint32_t sb) { return STAGES * static_cast<size_t>(sb) + 1024 + 256; }
+constexpr size_t kPersistSmemMax = persist_smem(kBlk * 2 * 128 + 2 * kBBox);  // 128-row blocks
+
 // CTAs of the persistent kernel that the SMs of the current device hold at
-// once, from the shared-memory, thread and register limits with the whole
-// L1/shared array as shared memory (three rings per SM).  The kernels'
-// attributes are set and the count worked out once per device.
-long long persist_resident() {
+// once, from the shared-memory, thread, register and tensor-memory limits
+// with the whole L1/shared array as shared memory, for a stage of `sb` bytes
+// and `cols` TMEM columns per CTA (64 x 64 blocks: three per SM).  The
+// kernels' attributes are set and each count worked out once per device.
+long long persist_resident(uint32_t sb, uint32_t cols) {
     static std::mutex mu;
-    static std::map<int, long long> by_device;
+    static std::map<std::pair<int, uint64_t>, long long> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    const auto key = std::make_pair(dev, (static_cast<uint64_t>(sb) << 32) | cols);
     std::lock_guard<std::mutex> lock(mu);
-    auto it = by_device.find(dev);
-    if (it != by_device.end()) return it->second;
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
     int nsm = 0, smem_sm = 0, reserved = 0, max_thr = 0, regs_sm = 0;
-    cudaFuncAttributes fa{};
-    for (auto* k : {bsr_spmm_persist_kernel<false>, bsr_spmm_persist_kernel<true>})
-        if (set_smem_limit(k, kTileSmem) != cudaSuccess ||
+    int regs = 1;
+    size_t static_smem = 0;
+    for (auto* k : {bsr_spmm_persist_kernel<false, false>, bsr_spmm_persist_kernel<true, false>,
+                    bsr_spmm_persist_kernel<false, true>, bsr_spmm_persist_kernel<true, true>}) {
+        cudaFuncAttributes fa{};
+        if (set_smem_limit(k, kPersistSmemMax) != cudaSuccess ||
             cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
-                cudaSuccess)
+                cudaSuccess ||
+            cudaFuncGetAttributes(&fa, k) != cudaSuccess)
             return -1;
-    if (cudaFuncGetAttributes(&fa, bsr_spmm_persist_kernel<false>) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        regs = std::max(regs, fa.numRegs);
+        static_smem = std::max(static_smem, fa.sharedSizeBytes);
+    }
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&max_thr, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
         return -1;
-    const long long per_block = static_cast<long long>(kTileSmem) + fa.sharedSizeBytes + reserved;
+    const long long per_block = static_cast<long long>(persist_smem(sb) + static_smem) + reserved;
     long long per_sm = smem_sm / per_block;
     per_sm = std::min<long long>(per_sm, max_thr / kPThreads);
-    per_sm = std::min<long long>(per_sm, regs_sm / (static_cast<long long>(fa.numRegs > 0 ? fa.numRegs : 1) * kPThreads));
+    per_sm = std::min<long long>(per_sm, regs_sm / (static_cast<long long>(regs) * kPThreads));
+    per_sm = std::min<long long>(per_sm, 512 / cols);  // the SM's 512 TMEM columns
     const long long G = std::max<long long>(per_sm, 1) * nsm;
-    by_device[dev] = G;
+    cache[key] = G;
     return G;
 }
 
+template <bool GEN>
 spx_status launch_persist(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* brp, const int* bcol, float* C,
                           long long ldc, float alpha, float beta, int M, int N, int K, long long nnzb, int ntiles,
-                          int ntq, cudaStream_t st, uint64_t* launches) {
-    const long long G = persist_resident();  // CTAs the SMs hold at once
+                          int ntq, const TcShape& sh, cudaStream_t st, uint64_t* launches) {
+    const long long G = persist_resident(GEN ? sh.sb : kSB, GEN ? sh.cols : kPTmemCols);  // CTAs held at once
     if (G <= 0) return SPX_ERR_CUDA;
+    const size_t smem = persist_smem(GEN ? sh.sb : kSB);
     // The last round of tiles: with at most half the CTAs busy in it, its tiles are cut in two.  The first
     // launch stores each such tile's head piece (its first half of the blocks) beside the whole tiles; a
     // second launch of as many CTAs computes the tail pieces on the SMs the first launch frees and adds them
     // into C once the first has finished.  Every tile is then done after about ntiles / G rounds, not
     // ceil(ntiles / G).  A piece pays a CTA start-up and a pipeline fill of its own, so block-rows of fewer
-    // than kSplitBlocks blocks on average are not cut (256 block-rows, N = 1024, the whole tiles against
-    // the cut last round: 26 blocks 76.4 / 78.5 us, 52 blocks 133.8 / 130.7, 104 blocks 250.5 / 237.2,
-    // 256 blocks 582.3 / 537.2).
+    // than kSplitBlocks ring stages on average are not cut (64 x 64 blocks, 256 block-rows, N = 1024, the
+    // whole tiles against the cut last round: 26 blocks 76.4 / 78.5 us, 52 blocks 133.8 / 130.7, 104 blocks
+    // 250.5 / 237.2, 256 blocks 582.3 / 537.2).
     constexpr long long kSplitBlocks = 48;
     const int R = static_cast<int>(ntiles % G);
-    const long long MB = (M + kBlk - 1) / kBlk;
-    const bool split = R > 0 && 2LL * R <= G && nnzb >= kSplitBlocks * MB;
+    const int br = GEN ? sh.br : kBlk, kc = GEN ? sh.kc : 1;
+    const long long MB = (M + br - 1) / br;
+    const bool split = R > 0 && 2LL * R <= G && nnzb * kc >= kSplitBlocks * MB;
     const int full = split ? ntiles - R : ntiles, tail = split ? R : 0;
     const int grid = static_cast<int>(split ? (full > 0 ? G : R) : std::min<long long>(ntiles, G));
-    const int KB = (K + kBlk - 1) / kBlk;
-    bsr_spmm_persist_kernel<false><<<grid, kPThreads, kTileSmem, st>>>(tmA, tmB, brp, bcol, C, ldc, alpha, beta,
-                                                                       kSpinLimit, M, N, full, tail, ntq, KB, nnzb);
+    const int KB = (K + (GEN ? sh.bc : kBlk) - 1) / (GEN ? sh.bc : kBlk);
+    bsr_spmm_persist_kernel<false, GEN><<<grid, kPThreads, smem, st>>>(tmA, tmB, brp, bcol, C, ldc, alpha, beta,
+                                                                       kSpinLimit, M, N, full, tail, ntq, KB, nnzb,
+                                                                       sh);
     *launches = 1;
     if (!split) return spx_cuda_status(cudaGetLastError());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(R));
     cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kTileSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the first launch ends
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, bsr_spmm_persist_kernel<true>, tmA, tmB, brp, bcol, C, ldc, alpha,
-                                             beta, kSpinLimit, M, N, full, tail, ntq, KB, nnzb);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bsr_spmm_persist_kernel<true, GEN>, tmA, tmB, brp, bcol, C, ldc,
+                                             alpha, beta, kSpinLimit, M, N, full, tail, ntq, KB, nnzb, sh);
     *launches = 2;
     return spx_cuda_status(e != cudaSuccess ? e : cudaGetLastError());
 }
 
+// 2-D bf16 tensor map with a box of box_inner x box_outer elements, 128-byte swizzle.
+bool make_map_box(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                  uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -661,16 +745,20 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
                         const int32_t* bsr_col, const uint16_t* bsr_val, int32_t N, const uint16_t* B, int64_t ldb,
                         float alpha, float beta, float* C, int64_t ldc, spx_stream_t stream) {
     if (M < 0 || K < 0 || N < 0 || nnzb < 0 || br <= 0 || bc <= 0) return SPX_ERR_ARG;
-    const bool tc = br == kBlk && bc == kBlk;  // the tensor-core shape; others run bsr_spmm_simt_kernel
-    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * (tc ? kBlk : bc) > kI32Max) return SPX_ERR_INDEX_RANGE;
+    // 64 x 64 blocks: the tensor-core kernel, which needs its alignment; other shapes whose sides are
+    // multiples of 16 (tc_general_shape): the same kernel when the arrays are aligned for it, else, and for
+    // every other shape, bsr_spmm_simt_kernel
+    const bool tc64 = br == kBlk && bc == kBlk;
+    const bool tc_aligned = ldb % 8 == 0 && spx_aligned(bsr_val, 16) && spx_aligned(B, 16);
+    const bool tcg = !tc64 && tc_general_shape(br, bc) && tc_aligned;
+    if (nnzb > kI32Max || static_cast<int64_t>(nnzb) * std::max(br, bc) > kI32Max) return SPX_ERR_INDEX_RANGE;
     if (M == 0 || N == 0) return SPX_OK;
     if (!bsr_row_ptr || !C || (nnzb > 0 && (!bsr_col || !bsr_val || !B))) return SPX_ERR_ARG;
     if (ldb < N || ldc < N) return SPX_ERR_ARG;
-    if (tc && (ldb % 8 || !spx_aligned(bsr_val, 16) || !spx_aligned(B, 16) || !spx_aligned(C, 4) ||
-               !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
+    if (tc64 && (!tc_aligned || !spx_aligned(C, 4) || !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
         return SPX_ERR_ALIGN;
-    if (!tc && (ldb % 2 || !spx_aligned(bsr_val, 2) || !spx_aligned(B, 4) || !spx_aligned(C, 4) ||
-                !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
+    if (!tc64 && (ldb % 2 || !spx_aligned(bsr_val, 2) || !spx_aligned(B, 4) || !spx_aligned(C, 4) ||
+                  !spx_aligned(bsr_row_ptr, 4) || !spx_aligned(bsr_col, 4)))
         return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (nnzb == 0 && beta == 0.f) {
@@ -685,18 +773,28 @@ spx_status spx_spmm_bsr(int32_t M, int32_t K, int32_t br, int32_t bc, int64_t nn
         spx_note_launches(1);
         return spx_cuda_status(cudaGetLastError());
     }
-    if (!tc)
+    CUtensorMap tmA, tmB;
+    // A as nnzb * br rows of bc columns, read in 64-column boxes (past bc: zero-filled); B in boxes of
+    // min(bc, 64) rows
+    const bool mapped =
+        (tc64 || tcg) &&
+        make_map_box(&tmA, bsr_val, static_cast<uint64_t>(bc), static_cast<uint64_t>(nnzb) * br,
+                     static_cast<uint64_t>(bc) * 2, kBlk, static_cast<uint32_t>(br)) &&
+        make_map_box(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2,
+                     64, static_cast<uint32_t>(std::min(bc, kBlk)));
+    if (tc64 && !mapped) return SPX_ERR_CUDA;
+    if (!mapped)
         return spx_bsr_simt_spmm(M, K, br, bc, nnzb, bsr_row_ptr, bsr_col, bsr_val, N, B, ldb, alpha, beta, C, ldc,
                                  st);
-    CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, bsr_val, kBlk, static_cast<uint64_t>(nnzb) * kBlk, kBlk * 2) ||
-        !make_map(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(ldb) * 2))
-        return SPX_ERR_CUDA;
-    const long long ntiles = static_cast<long long>((M + kBlk - 1) / kBlk) * ((N + 127) / 128);
+    const long long ntiles = static_cast<long long>((M + br - 1) / br) * ((N + 127) / 128);
     if (ntiles > kI32Max) return SPX_ERR_INDEX_RANGE;
     uint64_t launches = 0;
-    const spx_status s = launch_persist(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N, K, nnzb,
-                                        static_cast<int>(ntiles), (N + 127) / 128, st, &launches);
+    const TcShape sh = tc_shape(br, bc);
+    const spx_status s =
+        tc64 ? launch_persist<false>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N, K, nnzb,
+                                     static_cast<int>(ntiles), (N + 127) / 128, sh, st, &launches)
+             : launch_persist<true>(tmA, tmB, bsr_row_ptr, bsr_col, C, ldc, alpha, beta, M, N, K, nnzb,
+                                    static_cast<int>(ntiles), (N + 127) / 128, sh, st, &launches);
     spx_note_launches(launches);
     return s;
 }

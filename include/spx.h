@@ -598,27 +598,33 @@ typedef struct spx_wcsr_plan spx_wcsr_plan; /* opaque, host-side: the task split
 /*
  * C = alpha * A B + beta * C with A in BSR (br x bc blocks, row-major inside,
  * bf16), B dense K x N bf16 row-major (ldb), C dense M x N fp32 row-major
- * (ldc); products accumulated in fp32 (on the tensor cores for 64 x 64
- * blocks), the epilogue in fp32 (beta == 0: C is write-only).  [SpMM-ops] §3.4 (loop over the
- * nonzero blocks, each a small dense GEMM on the tensor cores) and
+ * (ldc); products accumulated in fp32 (on the tensor cores for the shapes
+ * below), the epilogue in fp32 (beta == 0: C is write-only).  [SpMM-ops]
+ * §3.4 (loop over the nonzero blocks, each a small dense GEMM on the tensor
+ * cores) and
  * [AsyncSparse] §2.2.1, §3 (BCSR SpMM: asynchronous copies of A blocks and
  * B tiles into shared memory feeding the matrix units).
  * Shapes: any br x bc block, any M, K and N.  A ragged last block-row or
  * block column is zero-padded in the BSR arrays (as spx_build_bsr writes
  * them).  B rows at or beyond K are read as zeros, and C is stored only
  * inside its M x N part, so a ragged last column tile does a whole tile's
- * work but writes nothing past column N.  ldb >= N, ldc >= N; nnzb * bc
- * must fit int32 (SPX_ERR_INDEX_RANGE otherwise).
- * Blocks other than 64 x 64 run on the CUDA cores (one launch; each CTA
+ * work but writes nothing past column N.  ldb >= N, ldc >= N; nnzb * br
+ * and nnzb * bc must fit int32 (SPX_ERR_INDEX_RANGE otherwise).
+ * 64 x 64 blocks run on the tensor cores: ldb a multiple of 8, bsr_val and
+ * B 16-byte aligned, C 4-byte aligned (SPX_ERR_ALIGN otherwise).  Blocks
+ * whose br is a multiple of 16 up to 128 and whose bc is 16, 32, 48, 64 or a
+ * multiple of 64 run on the same tensor-core kernel when ldb is a multiple
+ * of 8 and bsr_val and B are 16-byte aligned.  Every other shape, or those
+ * shapes with other alignments, runs on the CUDA cores (one launch; each CTA
  * owns up to 64 rows of a block-row and a strip of columns and sums every
  * element's terms in their stored order with fp32 fused multiply-adds): ldb
- * even, bsr_val 2-byte, B and C 4-byte aligned.  64 x 64 blocks run on the
- * tensor cores: ldb a multiple of 8, bsr_val and B 16-byte aligned, C 4-byte
- * aligned (SPX_ERR_ALIGN otherwise), and the launches are 1 persistent
- * kernel (as many CTAs as the SMs hold at once, each walking a static list of 128-column x 64-row
- * output tiles; a tile's epilogue overlaps the next tile's MMAs), or 2 when
+ * even, bsr_val 2-byte, B and C 4-byte aligned (SPX_ERR_ALIGN otherwise).
+ * The tensor-core launches are 1 persistent kernel (as many CTAs as the SMs
+ * hold at once, each walking a static list of output tiles of 128 columns x
+ * one block-row; a tile's epilogue overlaps the next tile's MMAs), or 2 when
  * the last round of tiles would leave at least half the CTAs idle and the
- * block-rows average 48 blocks or more: that round's tiles are then cut in
+ * block-rows average 48 ring stages (64-column chunks of blocks) or more:
+ * that round's tiles are then cut in
  * two, the first launch storing their head pieces and a second one (allowed
  * to start early, programmatic dependent launch) adding the tail pieces into
  * C after the first has finished.  Results are then rounded in a different

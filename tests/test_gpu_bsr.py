@@ -133,12 +133,16 @@ def _bsr_case(seed, M, K, br, bc, lmin, lmax, values="uniform"):
     return brp, bcol, bval
 
 
-def _gamma(n):
-    u = 2.0 ** -24
+def _gamma(n, u=2.0 ** -24):
     return n * u / (1 - n * u)
 
 
-@pytest.mark.parametrize("M,K,br,bc,N", [
+def _tc_shape(br, bc):
+    """Shapes the tensor-core kernel takes (with ldb a multiple of 8 and 16-byte aligned arrays)."""
+    return (br, bc) == (64, 64) or (br % 16 == 0 and 16 <= br <= 128 and bc % 16 == 0 and (bc <= 64 or bc % 64 == 0))
+
+
+SHAPES = [
     (37, 29, 1, 1, 64),
     (100, 90, 2, 2, 130),
     (97, 203, 3, 5, 77),
@@ -153,17 +157,36 @@ def _gamma(n):
     (250, 250, 100, 70, 33),
     (64, 70, 1, 64, 8),
     (70, 64, 64, 1, 1),
-])
+    (230, 700, 48, 48, 300),
+    (260, 520, 32, 128, 136),
+    (330, 400, 112, 64, 129),
+    (290, 600, 96, 192, 64),
+    (100, 300, 128, 16, 257),
+]
+
+
+@pytest.mark.parametrize("M,K,br,bc,N", SHAPES)
 @pytest.mark.parametrize("beta", [0.0, 0.5])
-def test_general_block_shapes(M, K, br, bc, N, beta):
-    """Block shapes other than 64 x 64 (the CUDA-core kernel): ragged M, K, N,
-    padded leading dimensions, alpha/beta; against the oracle within the fp32
-    accumulation bound of each element's term count, nothing written outside
-    the M x N part of C, and beta = 0 never reading C (NaN there stays out)."""
+@pytest.mark.parametrize("layout", ["cuda-core", "tensor-core"])
+def test_general_block_shapes(M, K, br, bc, N, beta, layout):
+    """Block shapes other than 64 x 64: ragged M, K, N, padded leading
+    dimensions, alpha/beta; against the oracle within the fp32 accumulation
+    bound of each element's term count, nothing written outside the M x N part
+    of C, and beta = 0 never reading C (NaN there stays out).  With ldb a
+    multiple of 8, shapes whose sides are multiples of 16 (bc <= 64 or a
+    multiple of 64, br <= 128) run on the tensor cores; with an ldb that is
+    not, and for every other shape, on the CUDA cores."""
+    if layout == "tensor-core" and not _tc_shape(br, bc):
+        pytest.skip("not a tensor-core shape")
     brp, bcol, bval = _bsr_case(11 + br * 7 + bc, M, K, br, bc, 0, 40)
     B = synth.normal_bf16(12, synth.T_B, K * N, 1.0).reshape(K, N)
     C0 = synth.uniform(13, synth.T_Y, M * N).reshape(M, N).astype(np.float32)
-    ldb, ldc = N + (N % 2) + 6, N + 3
+    if layout == "tensor-core":
+        ldb, ldc = (N + 7) // 8 * 8 + 8, N + 3
+    else:
+        ldb, ldc = N + (N % 2) + 6, N + 3
+        if ldb % 8 == 0:
+            ldb += 2
     Bfull = np.zeros((K, ldb), np.uint16)
     Bfull[:, :N] = B
     Bd = bits_dev(Bfull)[:, :N]
@@ -180,7 +203,10 @@ def test_general_block_shapes(M, K, br, bc, N, beta):
     ref, bound = oracle.bsr_spmm(M, K, br, bc, brp, bcol, bval, B, alpha=1.5, beta=beta,
                                  C=C0 if beta != 0.0 else None)
     nterm = int(np.diff(brp).max(initial=0)) * bc
-    assert_within(got, ref, bound, _gamma(nterm + 3), 0.0, what=f"{br}x{bc}")
+    # the tensor cores' fp32 accumulation is not specified to round to nearest: bound it with a unit
+    # roundoff of 2^-23 (any faithful rounding) there, 2^-24 for the CUDA cores' fused multiply-adds
+    rel = _gamma(nterm + 3, 2.0 ** -23 if layout == "tensor-core" else 2.0 ** -24)
+    assert_within(got, ref, bound, rel, 0.0, what=f"{br}x{bc} {layout}")
     # bitwise the same on a second call
     Cd2 = torch.from_numpy(C0).cuda() if beta != 0.0 else torch.zeros(M, N, device="cuda")
     spx.spx_spmm_bsr(M, K, br, bc, torch.from_numpy(brp).cuda(), torch.from_numpy(bcol).cuda(),
@@ -188,11 +214,13 @@ def test_general_block_shapes(M, K, br, bc, N, beta):
     assert np.array_equal(Cd2.cpu().numpy().view(np.uint32), got.view(np.uint32))
 
 
-@pytest.mark.parametrize("br,bc", [(4, 4), (16, 8), (3, 7), (96, 48)])
-def test_general_shapes_small_integers_exact(br, bc):
+@pytest.mark.parametrize("br,bc,N", [(4, 4, 70), (16, 8, 70), (3, 7, 70), (96, 48, 70), (16, 16, 72), (32, 64, 72),
+                                     (128, 128, 136), (48, 192, 64)])
+def test_general_shapes_small_integers_exact(br, bc, N):
     """Entries and B small integers: every product and partial sum is exact in
-    fp32, so the result equals the dense product exactly."""
-    M, K, N = 180, 150, 70
+    fp32, so the result equals the dense product exactly (N = 70: the CUDA
+    cores; N a multiple of 8 with 16-multiple sides: the tensor cores)."""
+    M, K = 180, 150
     brp, bcol, bval = _bsr_case(21 + br, M, K, br, bc, 0, 30, "int")
     B = np.floor(synth.uniform(22, synth.T_B, K * N, -3, 4)).astype(np.float32).reshape(K, N)
     Bb = synth.to_bf16_bits(B).reshape(K, N)
