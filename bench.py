@@ -626,6 +626,15 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
                 prep()
             flush.fill_(1.0)
 
+    def hold_stream(steps):
+        # A spin kernel keeps the stream busy while the host enqueues the steps that follow, so that
+        # a start event never waits on the host's next launch: the events then time device work only
+        # (for a call of a few microseconds the host's enqueue would otherwise show up in the step)
+        spin = getattr(torch.cuda, "_sleep", None)
+        if spin is not None:
+            with torch.cuda.stream(stream):
+                spin(int(4e6 + 6e5 * steps))  # SM cycles: about 2 ms + 0.3 ms per step at 2 GHz
+
     for _ in range(args.warmup):
         flush_l2()
         run()
@@ -638,6 +647,7 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
     launches0 = spx.launch_count()
     with ClockSampler(dev.index) as clk:
         time.sleep(0.3)
+        hold_stream(len(ev))
         for s, e in ev:
             flush_l2()
             s.record(stream)
@@ -657,6 +667,7 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
     # ---------------- warm steps: the same calls back to back with no L2 flush (reported beside the flushed number)
     wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     run()
+    hold_stream(len(wev))
     for s, e in wev:
         s.record(stream)
         run()
@@ -690,6 +701,37 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
         extra["graph_us_per_call"] = round(g0.elapsed_time(g1) * 1e3 / (5 * calls), 3)
         extra["graph_note"] = (f"{calls} calls captured in one CUDA graph, replayed 5 times, no L2 flush between calls "
                                "(the matrix and vectors, 0.33 MB, stay in L2): the launch-bound cost per call")
+        # the same two timings of the smallest kernel there is (one 4-byte store): the floor that launching
+        # and event-timing one kernel put under any call
+        tiny = torch.zeros(1, device=dev)
+        with torch.cuda.stream(stream):
+            tiny.fill_(1.0)
+        torch.cuda.synchronize(dev)
+        te = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        hold_stream(len(te))
+        for s_, e_ in te:
+            s_.record(stream)
+            with torch.cuda.stream(stream):
+                tiny.fill_(1.0)
+            e_.record(stream)
+        torch.cuda.synchronize(dev)
+        tgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(tgraph, stream=stream):
+                for _ in range(calls):
+                    tiny.fill_(1.0)
+        tgraph.replay()
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                tgraph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        extra["launch_floor"] = {
+            "us_per_call_median": round(statistics.median(s_.elapsed_time(e_) for s_, e_ in te) * 1e3, 3),
+            "graph_us_per_call": round(g0.elapsed_time(g1) * 1e3 / (5 * calls), 3),
+            "what": "a one-element fill timed the same two ways: the launch + event floor under any single call"}
 
     # ---------------- the stream + gather floor of the same matrix (SpMV workloads)
     gather_floor = None
@@ -709,6 +751,7 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
             probe()
         torch.cuda.synchronize(dev)
         pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        hold_stream(len(pe))
         for s_, e_ in pe:
             flush_l2()
             s_.record(stream)
@@ -793,7 +836,8 @@ def run_ours(args, rank, world, workload=None, cpu_seconds=None):
     if gather_floor is not None:
         roof["gather_floor"] = gather_floor
     roof["algorithmic_bytes"] = int(abytes)
-    roof["timed"] = "whole step (all launches of the call), CUDA events on the launching stream"
+    roof["timed"] = ("whole step (all launches of the call), CUDA events on the launching stream; a spin kernel "
+                  "holds the stream while the host enqueues the steps")
 
     line = {
         "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -956,7 +1000,8 @@ def config_summary(sub: dict) -> dict:
             "e2e", "gpu_launches", "clocks", "cpu_baseline", "conversion")
     out = {k: sub[k] for k in keep if k in sub}
     det = sub.get("detail", {})
-    for k in ("graph_us_per_call", "graph_note", "warm", "fill_ratio", "nnzb", "nchunks", "useful_gflops", "variant"):
+    for k in ("graph_us_per_call", "graph_note", "launch_floor", "warm", "fill_ratio", "nnzb", "nchunks", "useful_gflops",
+              "variant"):
         if k in det:
             out[k] = det[k]
     return out
