@@ -392,7 +392,6 @@ __global__ void __launch_bounds__(kPThreads, 3)  // three resident per SM (the s
 
     // the block shape: constants for 64 x 64, the launch's TcShape otherwise
     const int BR = GEN ? sh.br : kBlk, BC = GEN ? sh.bc : kBlk, KC = GEN ? sh.kc : 1, KSL = GEN ? sh.ksl : 4;
-    const int BROWS = GEN ? sh.brows : kBlk;
     const uint32_t SB = GEN ? sh.sb : kSB, AB = GEN ? sh.abytes : kABytes, TX = GEN ? sh.tx : kSB;
     const uint32_t PITCH = GEN ? sh.pitch : kTmemColsT, TCOLS = GEN ? sh.cols : kPTmemCols;
     const uint32_t IDESC = GEN ? idesc_bf16_mn_k(128, static_cast<uint32_t>(BR)) : kIdesc;
