@@ -192,9 +192,24 @@ __global__ void __launch_bounds__(kThreads)
         const int t = threadIdx.x - 64;
         const int j = t & 7, h = (t >> 3) & 1, k0 = t >> 4;
         const uint32_t piece_off = h * kBBox + (static_cast<uint32_t>(j ^ (k0 & 7)) << 4);
+        // this thread's eight column indices of the next chunk, loaded one chunk ahead so that their
+        // latency overlaps the current chunk's wait and copies
+        int cnext[8];
+        if (nch > 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cnext[i] = __ldg(win_col + static_cast<long long>(g0) * kWin + 8 * i + k0);
+        }
         int b = 0;
         for (; b < nch; ++b) {
             const int s = b % kStages;
+            int cur[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cur[i] = cnext[i];
+            if (b + 1 < nch) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    cnext[i] = __ldg(win_col + static_cast<long long>(g0 + b + 1) * kWin + 8 * i + k0);
+            }
             int ok = 1;
             if (lane == 0) ok = (mbar_wait(empty(s), ((b / kStages) & 1u) ^ 1u, spin_limit) && !s_abort) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -205,11 +220,10 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 break;
             }
-            const int* wc = win_col + static_cast<long long>(g0 + b) * kWin;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = 8 * i + k0;
-                const int cr = __ldg(wc + k);
+                const int cr = cur[i];
                 if (SPX_CHECKED && (cr < -1 || cr >= K)) check_fail();
                 const int c = cr < K ? cr : -1;  // a column outside B is read as padding, never dereferenced
                 const uint16_t* row = c >= 0 ? B + static_cast<long long>(c) * ldb : B;
