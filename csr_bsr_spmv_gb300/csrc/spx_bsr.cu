@@ -30,6 +30,10 @@
 //   bsr_spmm_tile_kernel (spx_spmm_bsr_planned): one CTA per (task, column
 //     tile), where tasks are block-rows or pieces of unequal length and the
 //     hardware's dynamic CTA scheduling balances them better.
+// The persistent kernel also takes other block shapes (GEN = true, the
+// shape in a TcShape argument): br rows as the MMA's N (a multiple of 16 up
+// to 128), bc columns in 64-column chunks of one ring stage each, a narrower
+// block read with its columns past bc zero-filled and only bc / 16 K-steps.
 // Three CTAs of three stages per SM measured fastest: two CTAs of four
 // stages, four of two and one of five were slower, as were 256-column tiles
 // sharing each A block; many independent pipelines per SM beat deep ones.
