@@ -22,6 +22,23 @@ def test_exports_every_header_symbol(path):
     assert not missing, missing
 
 
+@pytest.mark.parametrize("path", [spx.LIB_PATH, spx.LIB_CHECK_PATH])
+def test_exports_only_the_c_abi(path):
+    """Each library's dynamic symbol table defines the spx_* C calls and nothing else: C++ statics
+    (and their initialisation guards) of one library must never bind to the other's when both are
+    loaded in one process."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    names = [line.split()[-1] for line in out.splitlines() if line.strip()]
+    others = [n for n in names if not n.startswith("spx_")]
+    assert not others, others[:10]
+    assert set(spx.header_symbols()) <= set(names)
+
+
 def test_status_strings():
     lib = spx._lib()
     for code, name in spx.STATUS.items():
