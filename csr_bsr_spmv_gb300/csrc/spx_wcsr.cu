@@ -554,6 +554,17 @@ spx_status spx_wcsr_plan_build(int32_t M, int64_t nchunks, const int32_t* win_pt
             }
             P->slots += np;
         }
+        // longest tasks first (stable): CTAs start in task order, so the long pieces run early and the
+        // last wave holds short ones
+        const size_t nt = P->tasks.size() / 4;
+        std::vector<int32_t> order(nt);
+        for (size_t i = 0; i < nt; ++i) order[i] = static_cast<int32_t>(i);
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t x, int32_t y) { return P->tasks[4 * x + 2] > P->tasks[4 * y + 2]; });
+        std::vector<int32_t> sorted(P->tasks.size());
+        for (size_t i = 0; i < nt; ++i)
+            for (int f = 0; f < 4; ++f) sorted[4 * i + f] = P->tasks[4 * static_cast<size_t>(order[i]) + f];
+        P->tasks.swap(sorted);
     } catch (const std::bad_alloc&) {
         delete P;
         return SPX_ERR_NOMEM;

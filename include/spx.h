@@ -709,7 +709,9 @@ spx_status spx_spmm_wcsr(int32_t M, int32_t K, int64_t nchunks, const int32_t* w
  * cuts every window with more than max_chunks chunks (max_chunks <= 0: 16)
  * into balanced pieces of consecutive chunks; the other windows stay whole.
  * tasks: {window, first chunk, chunks, partial slot or -1 for a whole
- * window}; splits: {window, first slot, pieces, 0}.  The table (tasks then
+ * window}, longest first (ties in window and piece order: CTAs start in task
+ * order, so the long tasks run early and the last wave holds short ones);
+ * splits: {window, first slot, pieces, 0}.  The table (tasks then
  * splits, table_bytes, 16-byte aligned caller memory) goes to the device with
  * spx_wcsr_plan_upload.  spx_spmm_wcsr_planned runs one CTA per task and
  * column tile; a whole window writes C as spx_spmm_wcsr does, a piece writes

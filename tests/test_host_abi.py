@@ -402,15 +402,16 @@ def test_binding_rejects_strided_views():
 
 def test_wcsr_plan_task_split():
     """Windows with more than max_chunks chunks are cut into balanced pieces of consecutive
-    chunks with consecutive partial slots; the others stay whole (slot -1)."""
+    chunks with consecutive partial slots; the others stay whole (slot -1).  Tasks are listed
+    longest first, ties in window and piece order."""
     wp = np.array([0, 3, 3, 20, 21, 33], np.int32)  # chunks per window: 3, 0, 17, 1, 12
     P = spx.WcsrPlan(5 * 64 - 10, 33, wp, max_chunks=5, upload=False)
     tasks, splits = P.tasks()
     assert P.info["split_windows"] == 2 and P.info["slots"] == 4 + 3
     # window 2: 17 chunks -> 4 pieces of 5, 4, 4, 4; window 4: 12 chunks -> 3 pieces of 4
-    assert tasks.tolist() == [[0, 0, 3, -1], [1, 3, 0, -1],
-                              [2, 3, 5, 0], [2, 8, 4, 1], [2, 12, 4, 2], [2, 16, 4, 3],
-                              [3, 20, 1, -1], [4, 21, 4, 4], [4, 25, 4, 5], [4, 29, 4, 6]]
+    assert tasks.tolist() == [[2, 3, 5, 0], [2, 8, 4, 1], [2, 12, 4, 2], [2, 16, 4, 3],
+                              [4, 21, 4, 4], [4, 25, 4, 5], [4, 29, 4, 6],
+                              [0, 0, 3, -1], [3, 20, 1, -1], [1, 3, 0, -1]]
     assert splits.tolist() == [[2, 0, 4, 0], [4, 4, 3, 0]]
     assert P.info["table_bytes"] == 4 * 4 * (10 + 2)
     whole = spx.WcsrPlan(5 * 64, 33, wp, max_chunks=0, upload=False)  # default 16: only window 2 splits
