@@ -84,12 +84,26 @@ __device__ __forceinline__ float gather_x(const float* __restrict__ x, int c, in
     return ld_x(x + c);
 }
 
-// Strided dot product of the nonzero range [a, b) with x; 4 gathers in flight per thread.
+// Strided dot product of the nonzero range [a, b) with x; 8 gathers in flight per thread
+// (then 4, then 1 for the rest), summed in a fixed order.
 template <int NT>
 __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__ col, const float* __restrict__ val,
                                            const float* __restrict__ x, int K) {
     float s = 0.f;
     int p = a + threadIdx.x;
+    for (; p + 7 * NT < b; p += 8 * NT) {
+        int c[8];
+        float v[8], xv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = ld_stream(col + p + j * NT);
+            v[j] = ld_stream(val + p + j * NT);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xv[j] = gather_x(x, c[j], K);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += v[j] * xv[j];
+    }
     for (; p + 3 * NT < b; p += 4 * NT) {
         int c0 = ld_stream(col + p), c1 = ld_stream(col + p + NT);
         int c2 = ld_stream(col + p + 2 * NT), c3 = ld_stream(col + p + 3 * NT);
