@@ -289,15 +289,17 @@ __global__ void __launch_bounds__(kTThreads)
 }
 
 // ---------------------------------------------------------------- the persistent kernel
-// The same tiles (128 output columns x one 64-row block-row) and the same
-// ring stages as the tile kernel, but a CTA stays resident and walks a static
-// schedule of tiles (tile = block-row * column tiles + column tile; CTA b runs
-// tiles b, b + G, b + 2G, ...), so the ring never drains between tiles:
+// The same tiles (128 output columns x one block-row: 64 rows, or br for
+// the other shapes) and the same ring stages as the tile kernel, but a CTA
+// stays resident and walks a static schedule of tiles (tile = block-row *
+// column tiles + column tile; CTA b runs tiles b, b + G, b + 2G, ...), so the
+// ring never drains between tiles:
 //   warps 0-3 : epilogue (TMEM lane quarter = warp), one tile behind the MMAs;
-//   warp 4    : TMA producer, one ring position per block, across tiles;
+//   warp 4    : TMA producer, one ring position per block (per 64-column chunk
+//               of a block), across tiles;
 //   warp 5    : lane 0 issues the MMAs into one of two TMEM accumulators
-//               (64 columns each), so tile i+1 accumulates while tile i is
-//               stored.
+//               (64 columns each for 64-row blocks), so tile i+1 accumulates
+//               while tile i is stored.
 // On dense block-rows (256 blocks each) the tile kernel reaches its steady
 // rate; on short ones (26 blocks) each CTA's start-up, pipeline fill and
 // epilogue are paid per tile, and this kernel hides them.
