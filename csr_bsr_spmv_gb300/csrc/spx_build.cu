@@ -498,6 +498,29 @@ __global__ void plan_write(const int* __restrict__ rp, int M, int seg_nnz, int l
     }
 }
 
+// Segmented groups: the first row of each thread (spx_first_entry), by a
+// binary search of the group's row offsets; one entry per (group, thread).
+__global__ void plan_first(const int* __restrict__ rp, const int4* __restrict__ groups, long long ngroups,
+                           int nth, int per, uint16_t* __restrict__ first) {
+    const long long total = ngroups * nth;
+    for (long long i = blockIdx.x * static_cast<long long>(kT) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * kT) {
+        const int4 g = groups[i / nth];
+        const long long a = (i % nth) * static_cast<long long>(per);
+        const int nrows = g.x >> 8, r0 = g.y, p0 = g.z, n = g.w - g.z;
+        uint16_t v = 0;
+        if (a < n) {
+            int lo = 0, hi = nrows;  // first index with rp[r0 + index] - p0 > a
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (rp[r0 + mid] - p0 > a) hi = mid; else lo = mid + 1;
+            }
+            v = spx_first_entry(lo - 1, rp[r0 + lo - 1] - p0 < a);
+        }
+        first[i] = v;
+    }
+}
+
 // ---------------------------------------------------------------- SELL-C-sigma
 // [SpMM-ops] §1.4, [Formats] §6: rows longer than `piece` are cut into pieces
 // (pseudo-rows with a partial-sum slot); pseudo-rows are sorted longest first,
@@ -1076,6 +1099,7 @@ spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
     P->tasks.clear();
     P->dtasks.clear();
     P->longrows.clear();
+    P->first.clear();
     std::memset(P->counts, 0, sizeof(P->counts));
     if (M == 0) {
         P->table_bytes = 0;
@@ -1147,11 +1171,24 @@ spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
     plan_write<<<g, kT, 0, st>>>(rp, M, o.seg_nnz, o.lanes_div, nsl, fl, fs, toff, soff, sidx, gsf, gidx, E0,
                                  static_cast<long long>(tot[0]), htask, dtask, lrows, gcnt);
     ++launches;
+    const int nth = spx_group_threads(o.block_nnz);
+    const long long nfirst = o.lanes_div == 0 ? static_cast<long long>(ngroups) * nth : 0;
+    uint16_t* first = nfirst ? pool.get<uint16_t>(nfirst) : nullptr;
+    if (pool.err != cudaSuccess) {
+        cudaStreamSynchronize(st);
+        return SPX_ERR_NOMEM;
+    }
+    if (nfirst) {
+        plan_first<<<grid_for(nfirst), kT, 0, st>>>(rp, reinterpret_cast<const int4*>(dtask) + tot[0], ngroups, nth,
+                                                    spx_group_per(o.block_nnz), first);
+        ++launches;
+    }
     unsigned long long gc[3] = {0, 0, 0};
     try {
         P->tasks.resize(static_cast<size_t>(4 * nt));
         P->dtasks.resize(static_cast<size_t>(4 * nt));
         P->longrows.resize(static_cast<size_t>(4) * tot[3]);
+        P->first.resize(static_cast<size_t>(nfirst));
     } catch (const std::bad_alloc&) {
         cudaStreamSynchronize(st);
         return SPX_ERR_NOMEM;
@@ -1164,6 +1201,9 @@ spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
     if (e == cudaSuccess && tot[3])
         e = cudaMemcpyAsync(P->longrows.data(), lrows, sizeof(int) * 4 * static_cast<size_t>(tot[3]),
                             cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && nfirst)
+        e = cudaMemcpyAsync(P->first.data(), first, sizeof(uint16_t) * static_cast<size_t>(nfirst),
+                            cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(gc, gcnt, sizeof(gc), cudaMemcpyDeviceToHost, st);
     spx_note_launches(launches);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -1173,7 +1213,7 @@ spx_status spx_dev_make_plan(spx_plan* P, const int32_t* rp, cudaStream_t st) {
                           static_cast<int64_t>(tot[3]), static_cast<int64_t>(gc[0]), static_cast<int64_t>(gc[1]),
                           static_cast<int64_t>(gc[2])};
     std::memcpy(P->counts, c, sizeof(c));
-    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t);
+    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t) + P->first.size() * sizeof(uint16_t);
     P->scratch_bytes = static_cast<size_t>(tot[1]) * sizeof(float);
     return SPX_OK;
 }

@@ -250,13 +250,28 @@ spx_status make_plan(spx_plan* P, const int32_t* rp) {
         npacked += i - r0;
         (c == 0 ? g1 : c == kReduceSegmented ? gs : gw) += 1;
     }
+    if (o.lanes_div == 0) {
+        // segmented groups: each thread's first row, one walk over the group's rows
+        const int32_t nth = spx_group_threads(o.block_nnz), per = spx_group_per(o.block_nnz);
+        P->first.assign(groups.size() / 4 * static_cast<size_t>(nth), 0);
+        uint16_t* f = P->first.data();
+        for (size_t k = 0; k < groups.size(); k += 4, f += nth) {
+            const int32_t r0 = groups[k + 1], r1 = groups[k + 2], p0 = rp[r0], n = rp[r1] - p0;
+            int32_t r = 0;
+            for (int32_t t = 0; t < nth && static_cast<int64_t>(t) * per < n; ++t) {  // past the products: 0
+                const int32_t a = t * per;
+                while (rp[r0 + r + 1] - p0 <= a) ++r;
+                f[t] = spx_first_entry(r, rp[r0 + r] - p0 < a);
+            }
+        }
+    }
     P->tasks.insert(P->tasks.end(), groups.begin(), groups.end());
     P->dtasks.insert(P->dtasks.end(), dgroups.begin(), dgroups.end());
     const int64_t nt = static_cast<int64_t>(P->tasks.size() / 4);
     if (nt > kI32Max) return SPX_ERR_INDEX_RANGE;
     int64_t c[9] = {nt, static_cast<int64_t>(P->longrows.size() / 4), slot, npacked, ncta, nsplit, g1, gw, gs};
     std::memcpy(P->counts, c, sizeof(c));
-    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t);
+    P->table_bytes = (P->dtasks.size() + P->longrows.size()) * sizeof(int32_t) + P->first.size() * sizeof(uint16_t);
     P->scratch_bytes = static_cast<size_t>(slot) * sizeof(float);
     return SPX_OK;
 }
@@ -502,6 +517,18 @@ spx_status spx_plan_get_tasks(const spx_plan* P, int32_t* tasks, int32_t* long_r
     return SPX_OK;
 }
 
+spx_status spx_plan_get_table(const spx_plan* P, void* table) {
+    if (!spx_plan_ok(P)) return SPX_ERR_ARG;
+    if (P->table_bytes == 0) return SPX_OK;
+    if (!table) return SPX_ERR_ARG;
+    char* dst = static_cast<char*>(table);
+    const size_t tb = P->dtasks.size() * sizeof(int32_t), lb = P->longrows.size() * sizeof(int32_t);
+    if (tb) std::memcpy(dst, P->dtasks.data(), tb);
+    if (lb) std::memcpy(dst + tb, P->longrows.data(), lb);
+    if (!P->first.empty()) std::memcpy(dst + tb + lb, P->first.data(), P->first.size() * sizeof(uint16_t));
+    return SPX_OK;
+}
+
 spx_status spx_plan_upload(spx_plan* P, void* table, size_t table_bytes, spx_stream_t stream) {
     if (!spx_plan_ok(P)) return SPX_ERR_ARG;
     if (P->table_bytes == 0) {
@@ -512,11 +539,12 @@ spx_status spx_plan_upload(spx_plan* P, void* table, size_t table_bytes, spx_str
     if (!spx_aligned(table, 16)) return SPX_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* dst = static_cast<char*>(table);
-    const size_t tb = P->dtasks.size() * sizeof(int32_t);
+    const size_t tb = P->dtasks.size() * sizeof(int32_t), lb = P->longrows.size() * sizeof(int32_t);
     cudaError_t e = cudaSuccess;
     if (tb) e = cudaMemcpyAsync(dst, P->dtasks.data(), tb, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && !P->longrows.empty())
-        e = cudaMemcpyAsync(dst + tb, P->longrows.data(), P->longrows.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+    if (e == cudaSuccess && lb) e = cudaMemcpyAsync(dst + tb, P->longrows.data(), lb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !P->first.empty())
+        e = cudaMemcpyAsync(dst + tb + lb, P->first.data(), P->first.size() * sizeof(uint16_t), cudaMemcpyHostToDevice,
                             st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return SPX_ERR_CUDA;

@@ -95,9 +95,10 @@ struct spx_plan {
     std::vector<int32_t> tasks;     // 4 per task, the documented (host) form
     std::vector<int32_t> dtasks;    // 4 per task, the device form (see spx_spmv.cu)
     std::vector<int32_t> longrows;  // 4 per split row
+    std::vector<uint16_t> first;    // segmented groups: spx_group_threads entries per group (see below)
     int64_t counts[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     spx_row_stats_t stats{};
-    const void* d_table = nullptr;  // caller-owned copy of tasks + longrows
+    const void* d_table = nullptr;  // caller-owned copy of dtasks, longrows, first
     size_t table_bytes = 0;
     size_t scratch_bytes = 0;
     uint64_t fingerprint = 0;       // of the row_ptr the plan was built from
@@ -129,6 +130,27 @@ constexpr uint64_t kPlanMagic = 0x5350585f504c414eull;  // "SPX_PLAN"
 
 enum : int32_t { kTaskGroup = 0, kTaskCta = 1, kTaskSeg = 2 };
 constexpr int32_t kReduceSegmented = 6;  // group reduction code of the segmented reduction
+
+// A packed group runs on spx_group_threads(B) threads, thread t owning the
+// products [t * P, t * P + P) of the group (P = spx_group_per(B)) in the
+// segmented reduction.  B = 512 / 1024 / 2048 / 4096 run B / 8 threads with
+// eight products each; other sizes run 256 threads.
+inline SPX_HD int32_t spx_group_threads(int32_t B) {
+    return (B == 512 || B == 1024 || B == 2048 || B == 4096) ? B / 8 : 256;
+}
+inline SPX_HD int32_t spx_group_per(int32_t B) {
+    const int32_t nt = spx_group_threads(B);
+    return (B + nt - 1) / nt;
+}
+// Entry `first` of a segmented group's thread t (relative rows r of the
+// group, products counted from the group's first): the row holding product
+// a = t * P -- the last r with start(r) <= a -- shifted left once, plus 1 when
+// that row starts before a (its first products belong to earlier threads);
+// 0 for a thread past the group's products.  The plan stores the entries of
+// all groups (in task order) after the split-row table when lanes_div == 0.
+inline SPX_HD uint16_t spx_first_entry(int32_t r, bool starts_before) {
+    return static_cast<uint16_t>((r << 1) | (starts_before ? 1 : 0));
+}
 
 // Device task (int4): x = kind | code << 2 | aux << 8 where aux = #rows for a
 // group and the partial-sum slot for a segment; y = first row; z, w = the

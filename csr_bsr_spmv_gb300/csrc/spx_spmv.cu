@@ -84,38 +84,29 @@ __device__ __forceinline__ float gather_x(const float* __restrict__ x, int c, in
     return ld_x(x + c);
 }
 
-// Strided dot product of the nonzero range [a, b) with x; 8 gathers in flight per thread
-// (then 4, then 1 for the rest), summed in a fixed order.
+// Strided dot product of the nonzero range [a, b) with x: each thread takes its
+// entries eight at a time (all eight loads, then all eight gathers in flight),
+// the last batch predicated, and sums them in index order.
 template <int NT>
 __device__ __forceinline__ float range_dot(int a, int b, const int* __restrict__ col, const float* __restrict__ val,
                                            const float* __restrict__ x, int K) {
     float s = 0.f;
-    int p = a + threadIdx.x;
-    for (; p + 7 * NT < b; p += 8 * NT) {
+    for (int p = a + threadIdx.x; p < b; p += 8 * NT) {
+        const int m = (b - p + NT - 1) / NT;  // entries of this batch (8 but in the last)
         int c[8];
-        float v[8], xv[8];
+        float v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            c[j] = ld_stream(col + p + j * NT);
-            v[j] = ld_stream(val + p + j * NT);
+            c[j] = j < m ? ld_stream(col + p + j * NT) : 0;
+            v[j] = j < m ? ld_stream(val + p + j * NT) : 0.f;
         }
+        float xv[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) xv[j] = gather_x(x, c[j], K);
+        for (int j = 0; j < 8; ++j) xv[j] = j < m ? gather_x(x, c[j], K) : 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s += v[j] * xv[j];
+        for (int j = 0; j < 8; ++j)
+            if (j < m) s += v[j] * xv[j];
     }
-    for (; p + 3 * NT < b; p += 4 * NT) {
-        int c0 = ld_stream(col + p), c1 = ld_stream(col + p + NT);
-        int c2 = ld_stream(col + p + 2 * NT), c3 = ld_stream(col + p + 3 * NT);
-        float v0 = ld_stream(val + p), v1 = ld_stream(val + p + NT);
-        float v2 = ld_stream(val + p + 2 * NT), v3 = ld_stream(val + p + 3 * NT);
-        float x0 = gather_x(x, c0, K), x1 = gather_x(x, c1, K), x2 = gather_x(x, c2, K), x3 = gather_x(x, c3, K);
-        s += v0 * x0;
-        s += v1 * x1;
-        s += v2 * x2;
-        s += v3 * x3;
-    }
-    for (; p < b; p += NT) s += ld_stream(val + p) * gather_x(x, ld_stream(col + p), K);
     return s;
 }
 
@@ -190,10 +181,13 @@ __device__ __forceinline__ void reduce_lanes(int r0, int nrows, int lg, const fl
 // inside a thread's run are written by that thread; a row crossing threads
 // is finished by the thread holding its last product, which adds the carry
 // from an inclusive segmented scan of the threads' trailing partial sums.
+// The row holding the thread's first product, and whether that row started
+// before it, come from the plan (fr = spx_first_entry), so no thread searches
+// the row offsets between the product barrier and its sums.
 template <int PER>
 __device__ __forceinline__ void reduce_segmented(int r0, int nrows, int n, int per_rt, const float* s_prod,
                                                  const int* s_rp, const float* s_y, float alpha, float beta, float* y,
-                                                 float* s_sv, int* s_sf) {
+                                                 float* s_sv, int* s_sf, unsigned fr) {
     const int per = PER > 0 ? PER : per_rt;
     const int a = threadIdx.x * per;
     const int e = min(a + per, n);
@@ -204,13 +198,8 @@ __device__ __forceinline__ void reduce_segmented(int r0, int nrows, int n, int p
         for (int r = 0; r < nrows && s_rp[r + 1] == 0; ++r) emit_g(y, s_y, r0, r, 0.f, alpha, beta);
     }
     if (a < n) {
-        int lo = 0, hi = nrows;  // first index with s_rp[index] > a
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (s_rp[mid] > a) hi = mid; else lo = mid + 1;
-        }
-        int r = lo - 1;  // the (non-empty) row holding position a
-        bool carry_row = s_rp[r] < a;
+        int r = static_cast<int>(fr >> 1);  // the (non-empty) row holding position a
+        bool carry_row = fr & 1u;
         first_row = r;
         int next = s_rp[r + 1];
         if (PER > 0 && a + PER <= n) {
@@ -283,9 +272,14 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
                                                               const float* __restrict__ val,
                                                               const float* __restrict__ x, float alpha, float beta,
                                                               float* y, float* __restrict__ partials, int block_nnz,
-                                                              int block_rows, int K) {
+                                                              int block_rows, int K,
+                                                              const uint16_t* __restrict__ first, int first_group) {
     extern __shared__ __align__(16) float smem[];
     let_dependents_start();
+    // segmented groups (the last tasks): this thread's first row, read with the task
+    const unsigned fr = (first && static_cast<int>(blockIdx.x) >= first_group)
+                            ? __ldcs(first + static_cast<long long>(blockIdx.x - first_group) * NT + threadIdx.x)
+                            : 0u;
     const int4 t = tasks[blockIdx.x];
     const int kind = t.x & 3;
     if (kind == kTaskGroup) {
@@ -308,6 +302,13 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
             for (int i = threadIdx.x; i <= nrows; i += NT)
                 bad |= s_rp[i] < 0 || s_rp[i] > n || (i < nrows && s_rp[i + 1] < s_rp[i]) ||
                        (i == 0 && s_rp[0] != 0) || (i == nrows && s_rp[nrows] != n);
+            if (code == kReduceSegmented) {
+                // the plan's first row of this thread must hold its first product
+                const int a = threadIdx.x * ((block_nnz + NT - 1) / NT), r = static_cast<int>(fr >> 1);
+                if (!first) bad = true;
+                else if (a < n && !bad)
+                    bad = r >= nrows || s_rp[r] > a || s_rp[r + 1] <= a || ((fr & 1u) != 0) != (s_rp[r] < a);
+            }
             if (__syncthreads_or(bad)) {
                 if (threadIdx.x == 0) check_fail();
                 return;
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(NT) spmv_tasks_kernel(const int4* __restrict__
         }
         if (code == kReduceSegmented)
             reduce_segmented<ITEMS>(r0, nrows, n, (block_nnz + NT - 1) / NT, s_prod, s_rp, s_y, alpha,
-                                    beta, y, s_sv, s_sf);
+                                    beta, y, s_sv, s_sf, fr);
         else
             reduce_lanes<NT>(r0, nrows, code, s_prod, s_rp, s_y, alpha, beta, y);
     } else {
@@ -398,10 +399,10 @@ cudaError_t launch(void (*kernel)(P...), unsigned grid, unsigned block, size_t s
 template <int NT, int ITEMS>
 cudaError_t launch_tasks(int ntasks, size_t smem, cudaStream_t st, bool pdl, const int4* tasks, const int* rp,
                          const int* col, const float* val, const float* x, float alpha, float beta, float* y,
-                         float* scratch, int B, int R, int K) {
+                         float* scratch, int B, int R, int K, const uint16_t* first, int first_group) {
     spx_carve::fit(spmv_tasks_kernel<NT, ITEMS>, NT, smem);
     return launch(spmv_tasks_kernel<NT, ITEMS>, ntasks, NT, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y,
-                  scratch, B, R, K);
+                  scratch, B, R, K, first, first_group);
 }
 
 // The SpMV of one plan: the task kernel, then (split rows) the fix-up.  pdl:
@@ -421,17 +422,22 @@ spx_status launch_spmv(const spx_plan* P, const int* rp, const int* col, const f
     // 128 / 256 / 512-thread CTAs (smaller CTAs, more of them resident: measured
     // better on skewed rows); other sizes take the runtime-loop form with 256
     // threads.
-    const int NT = (B == 512 || B == 1024 || B == 2048 || B == 4096) ? B / 8 : 256;
+    const int NT = spx_group_threads(B);
+    // the groups are the last tasks; their threads' first rows follow the split-row table
+    const int ngroups = static_cast<int>(P->counts[6] + P->counts[7] + P->counts[8]);
+    const int first_group = ntasks - ngroups;
+    const uint16_t* first =
+        P->first.empty() ? nullptr : reinterpret_cast<const uint16_t*>(longrows + nlong);
     const size_t smem = sizeof(float) * static_cast<size_t>(B + B / 32 + 1) +
                         sizeof(int) * (static_cast<size_t>(R) + 1) + 2 * (NT / 32) * sizeof(float) +
                         sizeof(float) * static_cast<size_t>(R);
     cudaError_t e = cudaSuccess;
     switch (B) {
-        case 512: e = launch_tasks<64, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
-        case 1024: e = launch_tasks<128, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
-        case 2048: e = launch_tasks<256, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
-        case 4096: e = launch_tasks<512, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
-        default: e = launch_tasks<256, 0>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K); break;
+        case 512: e = launch_tasks<64, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K, first, first_group); break;
+        case 1024: e = launch_tasks<128, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K, first, first_group); break;
+        case 2048: e = launch_tasks<256, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K, first, first_group); break;
+        case 4096: e = launch_tasks<512, 8>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K, first, first_group); break;
+        default: e = launch_tasks<256, 0>(ntasks, smem, st, pdl, tasks, rp, col, val, x, alpha, beta, y, scratch, B, R, K, first, first_group); break;
     }
     uint64_t launches = 1;
     if (e == cudaSuccess && nlong > 0) {

@@ -133,6 +133,7 @@ def _load(path):
                          ctypes.c_int),
         "spx_plan_get_info": ([vp, ctypes.POINTER(PlanInfo)], ctypes.c_int),
         "spx_plan_get_tasks": ([vp, vp, vp], ctypes.c_int),
+        "spx_plan_get_table": ([vp, vp], ctypes.c_int),
         "spx_plan_upload": ([vp, vp, sz, vp], ctypes.c_int),
         "spx_plan_destroy": ([vp], ctypes.c_int),
         "spx_plan_fingerprint": ([vp, ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
@@ -525,6 +526,22 @@ class Plan:
         lr = np.empty((self.info["long_rows"], 4), np.int32)
         _check(_lib().spx_plan_get_tasks(self.handle, _ptr(t), _ptr(lr)), "spx_plan_get_tasks")
         return t, lr
+
+    def device_table(self) -> np.ndarray:
+        """Host copy of the bytes spx_plan_upload writes (spx_plan_get_table), as uint8."""
+        b = np.zeros(self.info["table_bytes"], np.uint8)
+        _check(_lib().spx_plan_get_table(self.handle, _ptr(b) if b.size else None), "spx_plan_get_table")
+        return b
+
+    def first_rows(self) -> np.ndarray:
+        """The per-thread first-row entries of the segmented groups (uint16, one row per group;
+        empty when the plan's groups are not segmented)."""
+        if self.opts["lanes_div"] != 0:
+            return np.zeros((0, 0), np.uint16)
+        B = self.opts["block_nnz"]
+        T = B // 8 if B in (512, 1024, 2048, 4096) else 256
+        off = 16 * (self.info["tasks"] + self.info["long_rows"])
+        return self.device_table()[off:].view(np.uint16).reshape(-1, T)
 
     def close(self):
         if self.handle:

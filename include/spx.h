@@ -226,9 +226,9 @@ typedef struct spx_plan spx_plan; /* opaque, host-side */
  * Long-row table (4 int32 per split row): {row, first slot, #segments, 0}.
  * opts == NULL uses spx_plan_opts_auto of the matrix's statistics.
  * block_nnz 512 / 1024 / 2048 / 4096 runs 64 / 128 / 256 / 512-thread CTAs
- * (eight products per thread); other sizes run 256 threads.  row_ptr is read once (copied to
- * the host when where == SPX_DEVICE).  *plan_out must be released with
- * spx_plan_destroy.
+ * (eight products per thread); other sizes run 256 threads.  row_ptr is read once (on the
+ * GPU when where == SPX_DEVICE: validation, statistics and the plan are built
+ * there).  *plan_out must be released with spx_plan_destroy.
  */
 spx_status spx_plan_csr(int32_t M, int32_t K, int64_t nnz, const int32_t* row_ptr, spx_loc where,
                         const spx_plan_opts_t* opts, spx_plan** plan_out);
@@ -240,10 +240,29 @@ spx_status spx_plan_get_info(const spx_plan* plan, spx_plan_info_t* out);
 spx_status spx_plan_get_tasks(const spx_plan* plan, int32_t* tasks, int32_t* long_rows);
 
 /*
- * Copy the plan's tables into caller-owned device memory `table` (at least
- * info.table_bytes, 16-byte aligned) on `stream`, and remember that address.
- * Must precede the first compute call with this plan; `table` must stay
- * valid while the plan is used.
+ * The device table (info.table_bytes bytes), in this order:
+ *   - the tasks in the device form, 4 int32 each: {kind | code << 2 |
+ *     aux << 8, first row, p0, p1} with aux = #rows of a group or the slot of
+ *     a segment, [p0, p1) the nonzeros the task covers;
+ *   - the long-row table as spx_plan_get_tasks gives it;
+ *   - when lanes_div == 0 (every group segmented): T uint16 per group, in task
+ *     order, T = the group's threads (block_nnz / 8 for block_nnz 512, 1024,
+ *     2048 or 4096, else 256).  Thread t sums the group's products [t*Q,
+ *     t*Q + Q), Q = ceil(block_nnz / T); its entry is 2*r + s, r the group's
+ *     row (counted from its first) holding product t*Q (the last row starting
+ *     at or before it), s = 1 when that row starts before t*Q; 0 for a thread
+ *     past the group's products.  The SpMV kernel takes each thread's first
+ *     row from here instead of searching the row offsets.
+ * The table depends only on row_ptr (the structure), like the plan.
+ */
+/* Host copy of the device table: writes info.table_bytes bytes to `table`. */
+spx_status spx_plan_get_table(const spx_plan* plan, void* table);
+
+/*
+ * Copy the plan's device table into caller-owned device memory `table` (at
+ * least info.table_bytes, 16-byte aligned) on `stream`, and remember that
+ * address.  Must precede the first compute call with this plan; `table` must
+ * stay valid while the plan is used.
  */
 spx_status spx_plan_upload(spx_plan* plan, void* table, size_t table_bytes, spx_stream_t stream);
 

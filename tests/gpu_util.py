@@ -32,3 +32,25 @@ def assert_within(got, ref, bound, rel=FP32_REL, ab=FP32_ABS, what=""):
                              f"got {got.ravel()[i].tolist()} ref {ref.ravel()[i].tolist()} "
                              f"tol {tol.ravel()[i].tolist()}")
     return float((err / np.maximum(tol, 1e-300)).max()) if err.size else 0.0
+
+
+def first_rows_expected(rp, tasks, block_nnz):
+    """The plan's per-thread first-row entries of its groups, derived here with a
+    sorted search of each group's row offsets: thread t of a group sums the
+    products [t*Q, t*Q + Q) (T threads: block_nnz / 8 for 512..4096, else 256;
+    Q = ceil(block_nnz / T)); its entry is 2*r + s with r the group's row holding
+    product t*Q (the last row starting at or before it) and s = 1 when that row
+    starts before t*Q; 0 past the group's products."""
+    T = block_nnz // 8 if block_nnz in (512, 1024, 2048, 4096) else 256
+    Q = -(-block_nnz // T)
+    rp = np.asarray(rp, np.int64)
+    groups = tasks[(tasks[:, 0] & 255) == 0]
+    out = np.zeros((groups.shape[0], T), np.uint16)
+    a = np.arange(T, dtype=np.int64) * Q
+    for g, (_, r0, r1, _) in enumerate(groups):
+        s = rp[r0:r1 + 1] - rp[r0]
+        ok = a < s[-1]
+        r = np.searchsorted(s, a, side="right") - 1
+        r = np.clip(r, 0, max(len(s) - 2, 0))
+        out[g] = np.where(ok, 2 * r + (s[r] < a), 0)
+    return out

@@ -13,6 +13,7 @@ import torch
 import oracle
 import synth
 from csr_bsr_spmv_gb300 import spx
+from gpu_util import first_rows_expected
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +35,11 @@ def _same_plan(M, rp, opts=None):
     assert np.array_equal(th, td) and np.array_equal(lh, ld)
     n = ph.info["table_bytes"] // 4
     assert torch.equal(ph.table[:n].cpu(), pd.table[:n].cpu())
+    assert np.array_equal(pd.device_table(), ph.device_table())
+    assert np.array_equal(ph.table[:n].cpu().numpy().view(np.uint8), ph.device_table())
+    # each segmented group's per-thread first rows, against a sorted search of its row offsets
+    if pd.opts["lanes_div"] == 0:
+        assert np.array_equal(pd.first_rows(), first_rows_expected(rp, td, pd.opts["block_nnz"]))
     # the structure fingerprint: the same on both sides, and each side validates the other's row_ptr
     assert pd.fingerprint == ph.fingerprint
     assert pd.validate(rp) == 0 and ph.validate(torch.from_numpy(rp).cuda()) == 0

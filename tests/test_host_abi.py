@@ -10,6 +10,7 @@ import pytest
 import oracle
 import synth
 from csr_bsr_spmv_gb300 import spx
+from gpu_util import first_rows_expected
 
 
 @pytest.mark.parametrize("path", [spx.LIB_PATH, spx.LIB_CHECK_PATH])
@@ -128,6 +129,9 @@ PLAN_OPTS = [
     dict(block_nnz=1024, block_rows=256, pack_max=1024, cta_max=1024, seg_nnz=1024, lanes_div=1),
     dict(block_nnz=4096, block_rows=512, pack_max=64, cta_max=20000, seg_nnz=3000, lanes_div=8),
     dict(block_nnz=1000, block_rows=100, pack_max=999, cta_max=5000, seg_nnz=700, lanes_div=0),
+    dict(block_nnz=512, block_rows=1024, pack_max=512, cta_max=4096, seg_nnz=2048, lanes_div=0),
+    dict(block_nnz=4096, block_rows=300, pack_max=200, cta_max=8192, seg_nnz=4096, lanes_div=0),
+    dict(block_nnz=16, block_rows=1024, pack_max=16, cta_max=64, seg_nnz=64, lanes_div=0),
 ]
 
 
@@ -149,8 +153,31 @@ def test_plan_matches_oracle(opts, seed):
     for k, v in w["counts"].items():
         assert p.info[k] == v, k
     assert p.stats == oracle.row_stats(L.size, rp)
-    assert p.info["table_bytes"] == 16 * (tasks.shape[0] + longrows.shape[0])
+    groups = int((tasks[:, 0] & 255).tolist().count(0))
+    first = 2 * groups * (full["block_nnz"] // 8 if full["block_nnz"] in (512, 1024, 2048, 4096) else 256)
+    assert p.info["table_bytes"] == 16 * (tasks.shape[0] + longrows.shape[0]) + (first if full["lanes_div"] == 0 else 0)
     assert p.info["scratch_bytes"] == 4 * w["counts"]["slots"]
+    if full["lanes_div"] == 0:
+        assert np.array_equal(p.first_rows(), first_rows_expected(rp, tasks, full["block_nnz"]))
+    else:
+        assert p.first_rows().size == 0
+
+
+@pytest.mark.parametrize("B", [512, 1000, 4096])
+def test_plan_first_rows_with_runs_of_empty_rows(B):
+    """Groups of up to 1024 rows, most of them empty: each thread's first row is the
+    last row starting at or before its first product, never an empty row before it."""
+    rng = np.random.default_rng(B)
+    L = np.where(rng.random(50_000) < 0.05, rng.integers(1, 40, 50_000), 0).astype(np.int32)
+    L[:700] = 0
+    rp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    opts = dict(block_nnz=B, block_rows=1024, pack_max=64, cta_max=4096, seg_nnz=1024, lanes_div=0)
+    p = spx.spx_plan_csr(L.size, 100, int(rp[-1]), rp, opts=opts, upload=False)
+    tasks, _ = p.tasks()
+    got = p.first_rows()
+    assert got.shape[0] == p.info["segmented_groups"] > 0
+    assert np.array_equal(got, first_rows_expected(rp, tasks, B))
+    assert got.max() > 1000  # rows deep inside a group of mostly empty rows
 
 
 def test_plan_default_options_documented():
