@@ -62,6 +62,32 @@ def test_power_law_small(opts, seed):
     assert plan.info["tasks"] > 0
 
 
+@pytest.mark.parametrize("B", [512, 1000, 4096])
+def test_segmented_groups_with_runs_of_empty_rows(B):
+    """Groups of up to 1024 rows, most of them empty (so a thread's first row, taken from the
+    plan, lies hundreds of rows into its group), some rows starting exactly at a thread's first
+    product: the oracle's result, and the same bits from a plan built on the host and one built
+    on the GPU."""
+    rng = np.random.default_rng(B)
+    M, K = 40_000, 30_000
+    L = np.where(rng.random(M) < 0.05, rng.integers(1, 40, M), 0).astype(np.int32)
+    L[:900] = 0
+    L[1000:1064] = 8  # runs of rows that each start on an eight-product boundary
+    row, col = synth.cols_uniform(B, K, L)
+    val = synth.uniform(B, synth.T_VAL, row.size)
+    rp, col, val = oracle.build_csr(M, K, row, col, val)
+    x = synth.uniform(B, synth.T_X, K)
+    y0 = synth.uniform(B, synth.T_Y, M)
+    opts = dict(block_nnz=B, block_rows=1024, pack_max=64, cta_max=4096, seg_nnz=1024, lanes_div=0)
+    got, plan = check(M, K, rp, col, val, x, y0, 1.0, 0.5, opts, what=f"B={B}")
+    assert plan.info["segmented_groups"] > 0 and plan.first_rows().max() > 1000
+    A = csr_to_device(M, K, rp, col, val)
+    ph = spx.spx_plan_csr(M, K, A.nnz, rp, opts=opts)  # host row_ptr: planned on the host
+    yd = dev(y0)
+    spx.spx_spmv_csr(ph, A, dev(x), yd, 1.0, 0.5)
+    assert np.array_equal(yd.cpu().numpy().view(np.uint32), got.view(np.uint32))
+
+
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-2.5, 0.0), (1.0, 0.5), (0.0, 3.0), (0.75, -1.25)])
 def test_alpha_beta(alpha, beta):
     d = synth.random_coo(4, 777, 555, 0, 70)
