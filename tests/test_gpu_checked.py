@@ -118,6 +118,38 @@ def test_spmv_inconsistent_row_offsets_reported():
     assert_within(y.cpu().numpy()[keep], ref[keep], bound[keep], what="rows outside the bad group")
 
 
+@pytest.mark.parametrize("how", ["row past the group", "carry bit flipped"])
+def test_spmv_corrupt_first_rows_reported(how):
+    """The plan's per-thread first rows (uploaded into caller memory with the task table) corrupted for
+    one segmented group: the group is not reduced, the error is reported, the other rows are right and
+    nothing around y changes."""
+    M, K = 3000, 20000
+    rp, col, val = _csr(6, M, K)
+    x = synth.uniform(6, synth.T_X, K)
+    with spx.checked_build():
+        A = csr_to_device(M, K, rp, col, val)
+        plan = spx.spx_plan_csr(M, K, A.nnz, A.row_ptr, opts=dict(block_nnz=1024, lanes_div=0))
+        tasks, longrows = plan.tasks()
+        gidx = np.flatnonzero((tasks[:, 0] & 255) == 0)
+        g = len(gidx) // 2
+        r0, r1 = int(tasks[gidx[g], 1]), int(tasks[gidx[g], 2])
+        assert r1 - r0 >= 3 and rp[r1] - rp[r0] > 16
+        first = plan.first_rows()
+        e = int(first[g, 1]) if how == "carry bit flipped" else 2 * (r1 - r0 + 3)
+        e ^= 1 if how == "carry bit flipped" else 0
+        table = plan.table.view(torch.int16)  # the uploaded device table, as 2-byte words
+        table[8 * (len(tasks) + len(longrows)) + g * first.shape[1] + 1] = e
+        gy, y = _guarded(M, np.zeros(M, np.float32))
+        spx.spx_spmv_csr(plan, A, dev(x), y, 1.0, 0.0)
+        assert spx.spx_last_device_error() == INDEX_RANGE
+    assert _guards_intact(gy, M)
+    ref, bound = oracle.spmv(M, rp, col, val, x)
+    keep = np.ones(M, bool)
+    keep[r0:r1] = False
+    assert_within(y.cpu().numpy()[keep], ref[keep], bound[keep], what="rows outside the corrupted group")
+    assert not y.cpu().numpy()[r0:r1].any()  # the group was not reduced
+
+
 def test_spmm_bad_columns_and_rows_reported():
     M, K, N = 3000, 5000, 32
     d = synth.random_coo(4, M, K, 1, 40)
